@@ -1,0 +1,384 @@
+"""Pins for the fp64 oracle: each test checks the oracle against something other than itself --
+an identity or closed form proved in "OSDN: Improving Delta Rule with Provable Online
+Preconditioning in Linear Attention" (arXiv:2605.13473), a special case that reduces to a
+textbook routine, a value printed on the pages (tests/golden/), or an independent formulation
+(the chunkwise WY form of Appendix A.2).  A plausible slip in the oracle -- a dropped beta, a
+swapped read/write key, a wrong sign, emission after the update, a transposed state -- fails at
+least one of them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+INF = float("inf")
+
+
+def rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def unit(x):
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+def rand_problem(seed, B=1, T=32, H=2, K=8, V=6, unit_keys=True, apf=False):
+    g = rng(seed)
+    q = unit(g.standard_normal((B, T, H, K)))
+    k = g.standard_normal((B, T, H, K))
+    k = unit(k) if unit_keys else k
+    v = g.standard_normal((B, T, H, V))
+    beta = 1.0 / (1.0 + np.exp(-g.standard_normal((B, T, H))))
+    r = 1.0 / (1.0 + np.exp(-(2.0 + g.standard_normal((B, T, H))))) if apf else None
+    return q, k, v, beta, r
+
+
+def step_forward(q, k, v, beta, r, d, S, **kw):
+    """Run the oracle forward on a single token (T=1) carrying (d, S); returns (o, S, d, kt)."""
+    out = oracle.osdn_forward(q[:, None], k[:, None], v[:, None], beta[:, None],
+                              None if r is None else r[:, None], d, S, **kw)
+    return out["o"][:, 0], out["S"], out["d"], out["k_tilde"][:, 0]
+
+
+# ---------------------------------------------------------------------------------------------
+# Special case that reduces to a textbook routine: eta = 0, d = 1 is DeltaNet (Section 3 /
+# Algorithm 2 part (1)).
+# ---------------------------------------------------------------------------------------------
+def textbook_deltanet(q, k, v, beta):
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.zeros((B, T, H, V))
+    S_all = np.zeros((B, H, V, K))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((V, K))
+            for t in range(T):
+                u = v[b, t, h] - S @ k[b, t, h]
+                S = S + beta[b, t, h] * np.outer(u, k[b, t, h])
+                o[b, t, h] = S @ q[b, t, h]
+            S_all[b, h] = S
+    return o, S_all
+
+
+def test_textbook_deltanet_at_eta0():
+    q, k, v, beta, _ = rand_problem(1, B=2, T=40, H=3, K=8, V=5)
+    out = oracle.osdn_forward(q, k, v, beta, eta=0.0)
+    o_ref, S_ref = textbook_deltanet(q, k, v, beta)
+    np.testing.assert_allclose(out["o"], o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out["S"], S_ref, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(out["k_tilde"], k)
+    np.testing.assert_array_equal(out["d"], np.ones_like(out["d"]))
+
+
+# ---------------------------------------------------------------------------------------------
+# Lemma 4.1 and its proof (Appendix A.3): S_t k_t - v_t = -u_t (1 - a_t), a_t = beta <d_t, k_t^2>,
+# and the closed-form surrogate h_t = ((1 - a_t)^2 - 1) / (2 n_t).
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("beta_aware", [True, False])
+def test_residual_identity_and_closed_form_surrogate(beta_aware):
+    q, k, v, beta, _ = rand_problem(2, B=1, T=24, H=2, K=7, V=5, unit_keys=False)
+    g = rng(22)
+    d = g.uniform(0.5, 2.0, size=(1, 2, 7))
+    S = g.standard_normal((1, 2, 5, 7)) * 0.3
+    for t in range(24):
+        S_prev, d_prev = S.copy(), d.copy()
+        o, S, d, kt = step_forward(q[:, t], k[:, t], v[:, t], beta[:, t], None, d, S, eta=0.3,
+                                   beta_aware=beta_aware)
+        for h in range(2):
+            kk, vv, bb = k[0, t, h], v[0, t, h], beta[0, t, h]
+            u = vv - S_prev[0, h] @ kk
+            a = bb * np.dot(d_prev[0, h], kk * kk)
+            lhs = S[0, h] @ kk - vv
+            np.testing.assert_allclose(lhs, -u * (1.0 - a), rtol=1e-11, atol=1e-12)
+            n = np.dot(kk, kk)
+            f_new, f_old = 0.5 * np.sum(lhs ** 2), 0.5 * np.sum(u ** 2)
+            h_direct = (f_new - f_old) / (np.sum(u ** 2) * n)
+            np.testing.assert_allclose(h_direct, ((1 - a) ** 2 - 1) / (2 * n), rtol=1e-10, atol=1e-13)
+            # readout after the write: o_t = S_t q_t
+            np.testing.assert_allclose(o[0, h], S[0, h] @ q[0, t, h], rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------------
+# The phase-1 step is projected online gradient descent on the surrogate (Section 4.2, Eq. (4)),
+# with retention on the old d for APF (Eq. (7)).  The gradient is taken here by central finite
+# differences of h(d) = [f(S_t(d)) - f(S_{t-1})] / |grad f(S_{t-1})|^2, where S_t(d) comes from the
+# oracle's own phase-2 step with write key d . k -- so the d update is tied to the memory write
+# through the pages' definition, not through a retyped formula.
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("beta_aware,apf", [(True, False), (False, False), (True, True)])
+def test_d_step_is_ogd_on_surrogate(beta_aware, apf):
+    g = rng(3)
+    K, V = 6, 4
+    for trial in range(6):
+        k = g.standard_normal(K) * (0.6 if trial % 2 else 1.0)
+        v = g.standard_normal(V)
+        S0 = g.standard_normal((V, K)) * 0.5
+        beta = float(1 / (1 + np.exp(-g.standard_normal())))
+        r = float(1 / (1 + np.exp(-(2 + g.standard_normal())))) if apf else 1.0
+        d0 = g.uniform(0.6, 1.8, size=K)
+        eta = 0.05
+        b_fb = beta if beta_aware else 1.0  # the beta seen by the phase-1 feedback
+
+        def h_of(dvec):
+            kt = (dvec * k)[None, None, None, :]
+            _, S1 = oracle.delta_phase2(k[None, None, None], k[None, None, None], kt,
+                                        v[None, None, None], np.array([[[b_fb]]]), S0[None, None])
+            res_new = S1[0, 0] @ k - v
+            res_old = S0 @ k - v
+            return (0.5 * res_new @ res_new - 0.5 * res_old @ res_old) / ((res_old @ res_old) * (k @ k))
+
+        grad = np.zeros(K)
+        step = 1e-4
+        for i in range(K):
+            e = np.zeros(K)
+            e[i] = step
+            grad[i] = (h_of(d0 + e) - h_of(d0 - e)) / (2 * step)
+        _, d1 = oracle.precond_scan(k[None, None, None], np.array([[[beta]]]),
+                                    np.array([[[r]]]) if apf else None, d0[None, None],
+                                    eta=eta, d_min=-INF, d_max=INF, beta_aware=beta_aware)
+        np.testing.assert_allclose(d1[0, 0], r * d0 - eta * grad, rtol=1e-8, atol=1e-10)
+        # with the box switched on, the step is the projection of the same point
+        _, d1c = oracle.precond_scan(k[None, None, None], np.array([[[beta]]]),
+                                     np.array([[[r]]]) if apf else None, d0[None, None],
+                                     eta=eta, d_min=0.9, d_max=1.2, beta_aware=beta_aware)
+        np.testing.assert_allclose(d1c[0, 0], np.clip(r * d0 - eta * grad, 0.9, 1.2), rtol=1e-8,
+                                   atol=1e-10)
+
+
+def test_eps_floor_on_tiny_key():
+    """|k|^2 = 1e-8 < eps = 1e-6: the normaliser is eps (Listing 1 clamps the squared norm).
+    Hand-computed: step = 0.003*0.5*(1 - 0.5e-8)/1e-6 = 1499.9999925, d_0 += step * 1e-8."""
+    k = np.array([1e-4, 0.0])[None, None, None]
+    kt, d1 = oracle.precond_scan(k, np.array([[[0.5]]]), None, np.ones((1, 1, 2)), eta=0.003,
+                                 eps=1e-6)
+    assert d1[0, 0, 0] == pytest.approx(1.000014999999925, rel=0, abs=1e-15)
+    assert d1[0, 0, 1] == 1.0
+    np.testing.assert_array_equal(kt, k)  # emitted with d_1 = 1, before the update
+
+
+# ---------------------------------------------------------------------------------------------
+# Emission order (Algorithm 1: emit k~_t = d_t . k_t BEFORE the update) and projection onto D.
+# ---------------------------------------------------------------------------------------------
+def test_emission_uses_d_before_update():
+    _, k, _, beta, r = rand_problem(4, B=1, T=6, H=1, K=5, V=2, apf=True)
+    d0 = rng(44).uniform(0.5, 2.0, size=(1, 1, 5))
+    kw = dict(eta=0.2, d_min=0.5, d_max=2.0)
+    kt, _ = oracle.precond_scan(k, beta, r, d0, **kw)
+    np.testing.assert_array_equal(kt[0, 0, 0], d0[0, 0] * k[0, 0, 0])
+    for t in range(1, 6):
+        _, d_t = oracle.precond_scan(k[:, :t], beta[:, :t], r[:, :t], d0, **kw)
+        np.testing.assert_allclose(kt[0, t, 0], d_t[0, 0] * k[0, t, 0], rtol=1e-15, atol=0)
+
+
+def test_box_invariant_and_binding():
+    _, k, _, beta, _ = rand_problem(5, B=2, T=300, H=3, K=16, V=2, unit_keys=False)
+    # long keys (beta <d, k^2> > 1) push d down, short keys push it up
+    k = k * np.where(np.arange(2)[:, None, None, None] == 0, 1.0, 0.15)
+    hit_lo = hit_hi = False
+    for eta in (0.3, 3.0):
+        kt, d = oracle.precond_scan(k, beta, None, None, eta=eta, d_min=0.5, d_max=2.0)
+        dt = kt / k  # every intermediate d_t, read back through the emitted keys
+        assert np.all(dt >= 0.5 - 1e-15) and np.all(dt <= 2.0 + 1e-15)
+        assert np.all(d >= 0.5) and np.all(d <= 2.0)
+        hit_lo |= bool(np.any(dt == 0.5))
+        hit_hi |= bool(np.any(dt == 2.0))
+    assert hit_lo and hit_hi  # the projection binds on both faces of the box
+
+
+def test_fixed_point_leaves_d_unchanged():
+    """If beta <d, k^2> = 1 the hypergradient vanishes (Appendix D.4: exact matching)."""
+    k = unit(rng(6).standard_normal(8))
+    beta = 0.8
+    d0 = np.full(8, 1.0 / beta)  # <d, k^2> = 1/beta for a unit key
+    _, d1 = oracle.precond_scan(k[None, None, None], np.array([[[beta]]]), None, d0[None, None],
+                                eta=0.5, d_min=0.5, d_max=2.0)
+    np.testing.assert_allclose(d1[0, 0], d0, rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------------------------
+# Corollary A.2: unit keys, d in [0.5, 2], beta in (0, 1)  =>  0 < a_t < 2 and q_t < 1, with the
+# residual ratio f_t(S_t) / f_t(S_{t-1}) = (1 - a_t)^2 measured on the states.
+# ---------------------------------------------------------------------------------------------
+def test_stability_band_unit_keys():
+    q, k, v, beta, r = rand_problem(7, B=1, T=64, H=2, K=8, V=5, apf=True)
+    out = oracle.osdn_forward(q, k, v, beta, r, eta=0.3)
+    a = beta * np.sum(out["k_tilde"] * k, axis=-1)  # beta <d_t . k_t, k_t> = beta <d_t, k_t^2>
+    assert np.all(a > 0) and np.all(a < 2)
+    d = None
+    S = None
+    for t in range(64):
+        S_prev = np.zeros((1, 2, 5, 8)) if S is None else S
+        _, S, d, _ = step_forward(q[:, t], k[:, t], v[:, t], beta[:, t], r[:, t], d, S, eta=0.3)
+        for h in range(2):
+            f_new = 0.5 * np.sum((S[0, h] @ k[0, t, h] - v[0, t, h]) ** 2)
+            f_old = 0.5 * np.sum((S_prev[0, h] @ k[0, t, h] - v[0, t, h]) ** 2)
+            np.testing.assert_allclose(f_new / f_old, (1 - a[0, t, h]) ** 2, rtol=1e-9)
+            assert f_new < f_old
+
+
+def test_worked_example():
+    with open(os.path.join(GOLDEN, "worked_example.json")) as f:
+        ex = json.load(f)
+    k = np.array(ex["k"])[None, None, None]
+    for case in ex["cases"]:
+        d0 = np.array(case["d"])[None, None]
+        v = np.ones((1, 1, 1, 1))
+        out = oracle.osdn_forward(k, k, v, np.array([[[ex["beta"]]]]), d0=d0, eta=0.0)
+        S1 = out["S"][0, 0]
+        ratio = (0.5 * np.sum((S1 @ k[0, 0, 0] - 1.0) ** 2)) / 0.5
+        assert ratio == pytest.approx(case["q"], abs=1e-15)
+        assert out["a"][0, 0, 0] == pytest.approx(case["a"], abs=1e-15)
+
+
+def test_counterexample_alternating():
+    with open(os.path.join(GOLDEN, "counterexample.json")) as f:
+        ex = json.load(f)
+    T = ex["T"]
+    v = np.array(ex["v"], dtype=float).reshape(1, T, 1, 1)
+    one = np.ones((1, T, 1, 1))
+    for eta in (0.003, 0.7):
+        out = oracle.osdn_forward(one, one, v, np.full((1, T, 1), ex["beta"]),
+                                  d0=np.full((1, 1, 1), ex["d0"]), eta=eta, d_min=0.5, d_max=2.0)
+        np.testing.assert_array_equal(out["o"].reshape(T), np.array(ex["S_after_each_token"], float))
+        assert out["d"][0, 0, 0] == ex["d_final"]
+
+
+# ---------------------------------------------------------------------------------------------
+# Corollary D.8: block-disjoint orthogonal class keys with fixed targets:
+# prod_c F_c(S_T) / F_c(S_0) = prod_t q_t,  q_t = (1 - a_t)^2.
+# ---------------------------------------------------------------------------------------------
+def test_repeated_key_contraction_identity():
+    g = rng(8)
+    n_cls, blk = 4, 3
+    K, V, T = n_cls * blk, 5, 40
+    keys = np.zeros((n_cls, K))
+    for c in range(n_cls):
+        keys[c, c * blk:(c + 1) * blk] = unit(g.standard_normal(blk))
+    targets = g.standard_normal((n_cls, V))
+    cls = np.concatenate([np.arange(n_cls), g.integers(0, n_cls, T - n_cls)])
+    k = keys[cls].reshape(1, T, 1, K)
+    v = targets[cls].reshape(1, T, 1, V)
+    beta = (1 / (1 + np.exp(-g.standard_normal(T)))).reshape(1, T, 1)
+    S0 = g.standard_normal((1, 1, V, K))
+    out = oracle.osdn_forward(k, k, v, beta, S0=S0, eta=0.4)
+    a = beta[0, :, 0] * np.sum(out["k_tilde"][0, :, 0] * k[0, :, 0], axis=-1)
+    log_q = np.sum(np.log((1 - a) ** 2))
+    F = lambda S, c: 0.5 * np.sum((S @ keys[c] - targets[c]) ** 2)
+    log_F = sum(np.log(F(out["S"][0, 0], c) / F(S0[0, 0], c)) for c in range(n_cls))
+    assert log_F == pytest.approx(log_q, rel=1e-9, abs=1e-9)
+
+
+# ---------------------------------------------------------------------------------------------
+# Independent formulation: the chunkwise WY/UT form (Appendix A.2, Eqs. (8)-(11); Section 4.3
+# Eq. (6)) written here in numpy from the equations, against the token recurrence.
+# ---------------------------------------------------------------------------------------------
+def chunk_form(q, k, kt, v, beta, S0, C):
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.zeros((B, T, H, V))
+    S_out = np.zeros((B, H, V, K))
+    for b in range(B):
+        for h in range(H):
+            S = S0[b, h].copy()
+            for c0 in range(0, T, C):
+                sl = slice(c0, c0 + C)
+                Kc, Ktc, Vc, Qc, bc = k[b, sl, h], kt[b, sl, h], v[b, sl, h], q[b, sl, h], beta[b, sl, h]
+                n = Kc.shape[0]
+                A = np.tril(bc[:, None] * (Kc @ Ktc.T), -1)
+                Tm = np.linalg.inv(np.eye(n) + A)                     # Eq. (8)
+                W = Tm @ (bc[:, None] * Kc)                            # Eq. (9)
+                U = Tm @ (bc[:, None] * Vc)
+                X = U - W @ S.T
+                o[b, sl, h] = Qc @ S.T + np.tril(Qc @ Ktc.T, 0) @ X     # score keeps the diagonal
+                S = S + X.T @ Ktc                                      # Eq. (11)
+            S_out[b, h] = S
+    return o, S_out
+
+
+@pytest.mark.parametrize("C", [16, 64])
+def test_chunk_form_equals_sequential(C):
+    q, k, v, beta, r = rand_problem(9, B=1, T=256, H=2, K=16, V=12, apf=True)
+    S0 = rng(99).standard_normal((1, 2, 12, 16)) * 0.1
+    kt, _ = oracle.precond_scan(k, beta, r, None, eta=0.3)
+    o_seq, S_seq = oracle.delta_phase2(q, k, kt, v, beta, S0)
+    o_chk, S_chk = chunk_form(q, k, kt, v, beta, S0, C)
+    np.testing.assert_allclose(o_seq, o_chk, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(S_seq, S_chk, rtol=0, atol=1e-11)
+
+
+def test_wy_product_identity():
+    """Eq. (10): prod_i (I - beta_i k_i k~_i^T) = I - W^T K~ (product ordered left to right)."""
+    g = rng(10)
+    C, K = 12, 7
+    Kc = g.standard_normal((C, K)) * 0.4
+    Ktc = Kc * g.uniform(0.5, 2.0, size=K)
+    bc = 1 / (1 + np.exp(-g.standard_normal(C)))
+    P = np.eye(K)
+    for i in range(C):
+        P = P @ (np.eye(K) - bc[i] * np.outer(Kc[i], Ktc[i]))
+    W = np.linalg.inv(np.eye(C) + np.tril(bc[:, None] * (Kc @ Ktc.T), -1)) @ (bc[:, None] * Kc)
+    np.testing.assert_allclose(P, np.eye(K) - W.T @ Ktc, rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------------
+# Structural consequences of the recurrence.
+# ---------------------------------------------------------------------------------------------
+def test_decoupling_two_phases_equal_interleaved():
+    """Lemma 4.1 (i): the d trajectory needs only keys and gates, so phase 1 then phase 2 equals
+    the per-token interleaving."""
+    q, k, v, beta, r = rand_problem(11, B=2, T=50, H=2, K=8, V=6, apf=True)
+    full = oracle.osdn_forward(q, k, v, beta, r, eta=0.2, scale=0.7)
+    kt, d = oracle.precond_scan(k, beta, r, None, eta=0.2)
+    o, S = oracle.delta_phase2(q, k, kt, v, beta, None, scale=0.7)
+    np.testing.assert_array_equal(kt, full["k_tilde"])
+    np.testing.assert_array_equal(d, full["d"])
+    np.testing.assert_allclose(o, full["o"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(S, full["S"], rtol=0, atol=1e-13)
+
+
+def test_continuation_split_equals_whole():
+    q, k, v, beta, r = rand_problem(12, B=1, T=70, H=2, K=8, V=6, apf=True)
+    kw = dict(eta=0.2)
+    whole = oracle.osdn_forward(q, k, v, beta, r, **kw)
+    first = oracle.osdn_forward(q[:, :33], k[:, :33], v[:, :33], beta[:, :33], r[:, :33], **kw)
+    second = oracle.osdn_forward(q[:, 33:], k[:, 33:], v[:, 33:], beta[:, 33:], r[:, 33:],
+                                 d0=first["d"], S0=first["S"], **kw)
+    np.testing.assert_allclose(np.concatenate([first["o"], second["o"]], 1), whole["o"], atol=1e-13)
+    np.testing.assert_allclose(second["S"], whole["S"], atol=1e-13)
+    np.testing.assert_allclose(second["d"], whole["d"], atol=1e-15)
+
+
+def test_decode_steps_equal_forward():
+    q, k, v, beta, r = rand_problem(13, B=2, T=20, H=3, K=8, V=6, apf=True)
+    g = rng(130)
+    S0 = g.standard_normal((2, 3, 6, 8)) * 0.1
+    d0 = g.uniform(0.5, 2.0, size=(2, 3, 8))
+    kw = dict(eta=0.2, scale=0.5)
+    whole = oracle.osdn_forward(q, k, v, beta, r, d0, S0, **kw)
+    S, d = S0, d0
+    for t in range(20):
+        o, S, d = oracle.decode_step(q[:, t], k[:, t], v[:, t], beta[:, t], S, d, r[:, t], **kw)
+        np.testing.assert_allclose(o, whole["o"][:, t], atol=1e-13)
+    np.testing.assert_allclose(S, whole["S"], atol=1e-13)
+    np.testing.assert_allclose(d, whole["d"], atol=1e-15)
+
+
+def test_retention_one_is_eq4():
+    """Eq. (7) with r = 1 recovers Eq. (4)."""
+    q, k, v, beta, _ = rand_problem(14, B=1, T=40, H=2, K=8, V=6)
+    a = oracle.osdn_forward(q, k, v, beta, None, eta=0.2)
+    b = oracle.osdn_forward(q, k, v, beta, np.ones_like(beta), eta=0.2)
+    for key in ("o", "S", "d", "k_tilde"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_scale_multiplies_readout():
+    q, k, v, beta, _ = rand_problem(15, B=1, T=16, H=1, K=8, V=4)
+    a = oracle.osdn_forward(q, k, v, beta, scale=1.0)
+    b = oracle.osdn_forward(q, k, v, beta, scale=0.125)
+    np.testing.assert_allclose(b["o"], 0.125 * a["o"], rtol=1e-15, atol=0)
+    np.testing.assert_array_equal(a["S"], b["S"])
