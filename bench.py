@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Benchmark of the OSDN forward hot path on GB300.
+
+One step = one pass of the layer forward over one batch: osdn_precond_scan (phase 1) then
+osdn_chunk_fwd (phase 2), on the 340M-shaped layer (B=8, H=8, T=2048, K=V=128, bf16 q/k/v,
+fp32 gates and state), inputs resident in HBM.  The decode step (B=256, H=16, 1024 sequential
+tokens, fp32 state) is measured in the same run and reported under "decode".
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead (the
+reference arm: the pages publish no code, so the plain recurrence is the only reference).
+Multi-GPU (torchrun): every rank runs an independent replica of the same workload (the path
+shards over (batch, head) with no collective); value = all ranks' tokens / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+METRIC = "OSDN fwd tokens/sec per layer (B,H,T,K=V=128) and % roofline; decode steps/sec"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def layer_bytes(w):
+    """Algorithmic HBM bytes per launch (inputs read once, outputs written once)."""
+    th = w.B * w.T * w.H
+    e = 2 if w.dtype != "f32" else 4
+    scan = th * (w.K * e + 4 + w.K * e + (4 if w.apf else 0)) + w.B * w.H * w.K * 4
+    chunk = th * (3 * w.K * e + w.V * e + 4 + w.V * e) + w.B * w.H * w.V * w.K * 4
+    return scan, chunk
+
+
+def decode_bytes(w):
+    bh = w.B * w.H
+    return bh * (2 * w.V * w.K * 4 + 2 * w.K * 4 + 2 * w.K * 2 + w.V * 2 + 4 + w.V * 2)
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if self.proc is None or not getattr(self, "lines", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle (the reference arm and the cpu_baseline leg)
+# ------------------------------------------------------------------------------------------------
+def oracle_layer_rate(w, inp, budget_s=12.0):
+    """Time the fp64 oracle forward on a bounded sample of (b, h) sequences of the workload.
+    Returns (layer tokens/s, seconds, sample description, threads)."""
+    import oracle
+
+    threads = len(os.sched_getaffinity(0))
+    q, k, v, beta, r = inp["q"], inp["k"], inp["v"], inp["beta"], inp["r"]
+
+    def run(nb, nh):
+        sl = lambda x: None if x is None else x[:nb, :, :nh]
+        t0 = time.perf_counter()
+        oracle.osdn_forward(sl(q), sl(k), sl(v), sl(beta), sl(r), eta=w.eta, d_min=w.d_min,
+                            d_max=w.d_max, eps=w.eps, threads=threads)
+        return time.perf_counter() - t0
+
+    t1 = run(1, 1)  # one (b, h) sequence, single-threaded work
+    per_seq = max(t1, 1e-4)
+    n = int(min(w.B * w.H, max(1, budget_s * threads / per_seq)))
+    nb, nh = max(1, n // w.H), min(w.H, n)
+    secs = run(nb, nh)
+    seqs = nb * nh
+    rate = seqs * w.T / w.H / secs  # layer tokens (each needs H head-sequences) per second
+    return rate, secs, f"{seqs} of {w.B * w.H} (b,h) sequences x T={w.T}, fp64 oracle forward", threads
+
+
+def run_reference(args, w):
+    from preconditioned_delta_rule_gb300 import workloads as W
+
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    inp = W.make_prefill(w)
+    for _ in range(args.warmup):
+        oracle_layer_rate(w, inp, budget_s=1.0)
+    rates, secs = [], []
+    for _ in range(args.steps):
+        rate, s, sample, threads = oracle_layer_rate(w, inp, budget_s=args.ref_budget)
+        rates.append(rate)
+        secs.append(s)
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "K": w.K, "V": w.V,
+                   "chunk": w.chunk, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+def run_ours(args, w):
+    from preconditioned_delta_rule_gb300 import binding
+    from preconditioned_delta_rule_gb300 import workloads as W
+    from preconditioned_delta_rule_gb300.build import build
+
+    ws, rank, local = dist_setup()
+    if rank == 0:
+        build()
+    barrier(ws)
+    binding.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, bf16_peak, peak_src = peaks()
+
+    host = W.make_prefill(w)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
+    kt = torch.empty((B, T, H, K), device=dev, dtype=g["k"].dtype)
+    d_out = torch.empty((B, H, K), device=dev, dtype=torch.float32)
+    o = torch.empty((B, T, H, V), device=dev, dtype=g["v"].dtype)
+    S_out = torch.empty((B, H, V, K), device=dev, dtype=torch.float32)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+
+    def scan():
+        binding.osdn_precond_scan(g["k"], g["beta"], g["r"], None, k_tilde=kt, d_out=d_out,
+                                  eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps,
+                                  beta_aware=w.beta_aware)
+
+    def chunk():
+        binding.osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], None, o=o, S_out=S_out,
+                               chunk=w.chunk)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1.0)
+        scan()
+        chunk()
+    binding.osdn_check()
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(n):
+            flush.fill_(float(i))  # evict the previous step's tensors from L2 (outside the events)
+            ev[i][0].record(stream)
+            scan()
+            ev[i][1].record(stream)
+            chunk()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(ws)
+    binding.osdn_check()
+    scan_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+    chunk_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
+    step_ms = [a + b for a, b in zip(scan_ms, chunk_ms)]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, ws)
+    tokens = B * T * ws * n
+    value = tokens / total_s
+    ms_per_step = 1e3 * total_s / n
+
+    scan_b, chunk_b = layer_bytes(w)
+    scan_avg, chunk_avg = statistics.mean(scan_ms), statistics.mean(chunk_ms)
+    dom = ("osdn_chunk_fwd", chunk_b, chunk_avg) if chunk_avg >= scan_avg else ("osdn_precond_scan", scan_b, scan_avg)
+    ach = dom[1] / (dom[2] * 1e-3) / 1e9
+    roof = {"kernel": dom[0], "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+            "frac": ach / hbm_peak, "traffic": None, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": dom[1], "avg_launch_ms": dom[2]}
+    kernels = {
+        "osdn_precond_scan": {"ms": scan_avg, "bytes": scan_b,
+                              "gbs": scan_b / (scan_avg * 1e-3) / 1e9,
+                              "frac": scan_b / (scan_avg * 1e-3) / 1e9 / hbm_peak},
+        "osdn_chunk_fwd": {"ms": chunk_avg, "bytes": chunk_b,
+                           "gbs": chunk_b / (chunk_avg * 1e-3) / 1e9,
+                           "frac": chunk_b / (chunk_avg * 1e-3) / 1e9 / hbm_peak},
+    }
+
+    e2e = run_e2e(args, w, host, dev, stream, ws)
+    decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, secs, sample, threads = oracle_layer_rate(w, host, budget_s=args.ref_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+               "seconds": secs}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": n,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate/state",
+            "data": "synthetic (seeded; shapes of the pages' 340M layer)",
+            "config": {"workload": w.name, "B": B, "H": H, "T": T, "K": K, "V": V,
+                       "chunk": w.chunk, "eta": w.eta, "box": [w.d_min, w.d_max],
+                       "l2": "flushed between steps (256 MiB write outside the timed events)"},
+            "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "decode": decode, "gpu_launches": 2 * n, "clocks": clk.summary(),
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, host, dev, stream, ws):
+    """Same metric through the public API from pinned host buffers: H2D of q, k, v, beta (r),
+    scan + chunk, D2H of o, S and d, every step, all inside the timed region."""
+    from preconditioned_delta_rule_gb300 import binding
+
+    names = [n for n in ("q", "k", "v", "beta", "r") if host[n] is not None]
+    pinned = {n: host[n].pin_memory() for n in names}
+    dbuf = {n: torch.empty_like(pinned[n], device=dev) for n in names}
+    o_h = torch.empty((w.B, w.T, w.H, w.V), dtype=host["v"].dtype).pin_memory()
+    S_h = torch.empty((w.B, w.H, w.V, w.K), dtype=torch.float32).pin_memory()
+    d_h = torch.empty((w.B, w.H, w.K), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(t.numel() * t.element_size() for t in (o_h, S_h, d_h))
+
+    def step():
+        for n in names:
+            dbuf[n].copy_(pinned[n], non_blocking=True)
+        o, S, d = binding.chunk_osdn(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["beta"], dbuf.get("r"),
+                                     eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps,
+                                     chunk_size=w.chunk)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S, non_blocking=True)
+        d_h.copy_(d, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, ws)
+    return {"value": w.B * w.T * ws * n / secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * secs / n}
+
+
+def run_decode(args, dev, stream, hbm_peak):
+    """The decode workload: B=256, H=16, K=V=128, fp32 state, `steps` sequential tokens with
+    all per-step inputs resident in HBM; the token loop is one CUDA graph."""
+    from preconditioned_delta_rule_gb300 import binding
+    from preconditioned_delta_rule_gb300 import workloads as W
+
+    w = W.DECODE
+    steps = args.decode_steps
+    inp = W.make_decode_steps(w, steps, device=dev)
+    S, d = W.make_decode_state(w, device=dev)
+    S0, d0 = S.clone(), d.clone()
+    o = torch.empty((steps, w.B, w.H, w.V), device=dev, dtype=inp["v"].dtype)
+
+    def loop():
+        for t in range(steps):
+            binding.osdn_decode_step(inp["q"][t], inp["k"][t], inp["v"][t], inp["beta"][t], S, d,
+                                     o=o[t], eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        loop()  # warm-up (also the first pass of the state)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        loop()
+    S.copy_(S0)
+    d.copy_(d0)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.decode_reps)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    times = []
+    for _ in range(reps):
+        S.copy_(S0)
+        d.copy_(d0)
+        ev[0].record(stream)
+        graph.replay()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+    binding.osdn_check()
+    secs = statistics.median(times)
+    per_step = secs / steps
+    b = decode_bytes(w)
+    ach = b / per_step / 1e9
+    return {"workload": w.name, "B": w.B, "H": w.H, "K": w.K, "V": w.V, "steps": steps,
+            "value": steps / secs, "unit": "steps/s", "us_per_step": per_step * 1e6,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": ach / hbm_peak, "algorithmic_bytes_per_launch": b},
+            "l2": "state 268 MB > L2; no flush", "gpu_launches_per_pass": steps,
+            "timing": "CUDA graph of all steps, median of reps"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="layer_340m")
+    ap.add_argument("--decode-steps", type=int, default=1024)
+    ap.add_argument("--decode-reps", type=int, default=3)
+    ap.add_argument("--ref-budget", type=float, default=12.0, help="CPU seconds per oracle sample")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from preconditioned_delta_rule_gb300 import workloads as W
+
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,125 @@
+/*
+ * osdn.h -- C ABI of the GB300 (sm_103a) OSDN forward path.
+ *
+ * OSDN ("OSDN: Improving Delta Rule with Provable Online Preconditioning in Linear Attention",
+ * arXiv:2605.13473) is the delta rule with a diagonal, online-learned right preconditioner d on
+ * the write side.  The forward path has three calls:
+ *
+ *   osdn_precond_scan  phase 1 (Section 4.2, Algorithm 1, Eq. (4); APF retention Eq. (7)):
+ *                      per (batch, head), for t = 0..T-1:
+ *                        k~_t   = d_t . k_t                                  (emitted first)
+ *                        s_t    = k_t . k_t,  n_t = max(sum s_t, eps)
+ *                        b      = beta_t if beta_aware else 1
+ *                        d_{t+1}= clip(r_t d_t + eta b (1 - b <d_t, s_t>) / n_t * s_t, d_min, d_max)
+ *   osdn_chunk_fwd     phase 2 (Section 4.1 Eq. (2), Section 4.3 Eqs. (5)-(6), Appendix A.2
+ *                      Eqs. (8)-(11)): per (batch, head), with the original key on the read side
+ *                      and the write key k~ on the write side,
+ *                        u_t = v_t - S_{t-1} k_t,   S_t = S_{t-1} + beta_t u_t k~_t^T,
+ *                        o_t = scale * S_t q_t      (readout after the write)
+ *                      computed chunkwise (WY/UT form) with an fp32 state.
+ *   osdn_decode_step   one token of both phases in place on (S, d): the recurrent form used at
+ *                      generation time (the pages' single-token kernel, Appendix L).
+ *
+ * Conventions shared by every call
+ *   - Every buffer is caller-owned DEVICE memory (cudaMalloc or equivalent); the library never
+ *     allocates, frees or keeps pointers after the call returns.
+ *   - Layouts are dense row-major: q, k, k~ [B,T,H,K]; v, o [B,T,H,V]; beta, r [B,T,H];
+ *     S [B,H,V,K] (value-major: S[b,h,i,j] multiplies key coordinate j); d [B,H,K].
+ *     Decode drops T: q, k [B,H,K]; v, o [B,H,V]; beta, r [B,H].
+ *   - dtypes: q, k, k~, v, o are OSDN_F32, OSDN_BF16 or OSDN_F16 (one dtype per call, except the
+ *     scan's k~ output dtype which is chosen separately); beta, r, d, S are always fp32.
+ *   - All pointers must be 16-byte aligned.  K and V must each be 64 or 128.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is enqueued
+ *     asynchronously; argument errors are detected on the host and returned before any launch.
+ *   - Errors: OSDN_OK on success; OSDN_ERR_ARG (null pointer where one is required, negative or
+ *     non-finite scalar, d_min > d_max), OSDN_ERR_SHAPE (sizes out of range, T not a multiple of
+ *     the chunk), OSDN_ERR_DTYPE, OSDN_ERR_ALIGN, OSDN_ERR_UNSUPPORTED (valid but not built, e.g.
+ *     K = 96), OSDN_ERR_CUDA (a launch failed; the CUDA error is left for the caller to query),
+ *     OSDN_ERR_TIMEOUT (a device-side bounded wait gave up; reported by osdn_check()).
+ *   - Sizes are `int`; B*T*H*max(K,V) must stay below 2^31 elements per tensor.
+ */
+#ifndef OSDN_H
+#define OSDN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    OSDN_OK = 0,
+    OSDN_ERR_ARG = 1,
+    OSDN_ERR_SHAPE = 2,
+    OSDN_ERR_DTYPE = 3,
+    OSDN_ERR_ALIGN = 4,
+    OSDN_ERR_UNSUPPORTED = 5,
+    OSDN_ERR_CUDA = 6,
+    OSDN_ERR_TIMEOUT = 7
+} osdn_status;
+
+typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1, OSDN_F16 = 2 } osdn_dtype;
+
+/*
+ * Phase 1: preconditioner scan (Algorithm 1 / Eq. (4); Eq. (7) when r != NULL).
+ *   k        [B,T,H,K] keys, dtype k_dtype (read)
+ *   beta     [B,T,H] fp32 write gates in (0,1) (read)
+ *   r        [B,T,H] fp32 APF retention r_{t,h}, broadcast over K; NULL means r = 1 (Eq. (4))
+ *   d0       [B,H,K] fp32 initial preconditioner; NULL means d = 1.  Used as given (not clamped).
+ *   k_tilde  [B,T,H,K] write keys k~_t = d_t . k_t, dtype kt_dtype (written)
+ *   d_out    [B,H,K] fp32 final d_{T} (written; may alias d0)
+ *   eta >= 0; d_min <= d_max (use -INFINITY/+INFINITY to switch the box off); eps > 0 floors
+ *   the SQUARED key norm; beta_aware = 1 feeds beta_t into the step (Listing 1 default),
+ *   0 uses 1 there (the memory write keeps beta either way).
+ *   T may be 0 (then d_out = d0 or 1).
+ */
+osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* beta,
+                              const float* r, const float* d0, void* k_tilde,
+                              osdn_dtype kt_dtype, float* d_out, int B, int T, int H, int K,
+                              float eta, float d_min, float d_max, float eps, int beta_aware,
+                              void* stream);
+
+/*
+ * Phase 2: chunkwise preconditioned delta rule (Eqs. (2), (5), (8)-(11)).
+ *   q, k, k_tilde [B,T,H,K], v [B,T,H,V], all of dtype `dtype` (read)
+ *   beta     [B,T,H] fp32 (read)
+ *   S0       [B,H,V,K] fp32 initial state; NULL means zeros
+ *   o        [B,T,H,V] outputs o_t = scale * S_t q_t, dtype `dtype` (written)
+ *   S_out    [B,H,V,K] fp32 final state (written; may alias S0)
+ *   chunk    chunk length C; 64 is the only value built.  T must be a multiple of C (T = 0 is
+ *            allowed and copies S0 to S_out).
+ *   scale    multiplies q (1.0 gives o_t = S_t q_t as in the equations; Listing 1 uses K^-1/2).
+ * bf16/f16 inputs with K = V = 128 run on the tensor-core kernel (TMA + tcgen05, fp32
+ * accumulation, fp32 state); other shapes and fp32 inputs run an fp32 CUDA-core kernel.
+ */
+osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, const void* v,
+                           osdn_dtype dtype, const float* beta, const float* S0, void* o,
+                           float* S_out, int B, int T, int H, int K, int V, int chunk,
+                           float scale, void* stream);
+
+/*
+ * One decode token for every (batch, head), in place (recurrent form of both phases):
+ *   k~ = d . k (old d); d <- clip(r d + eta b (1 - b <d, k.k>) / max(|k|^2, eps) k.k);
+ *   u = v - S k;  S <- S + beta u k~^T;  o = scale * S q.
+ *   q, k [B,H,K], v [B,H,V] of dtype `dtype`; beta, r [B,H] fp32 (r may be NULL);
+ *   S [B,H,V,K] fp32 and d [B,H,K] fp32 are read and overwritten; o [B,H,V] dtype `dtype`.
+ */
+osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,
+                             const float* beta, const float* r, float* S, float* d, void* o,
+                             int B, int H, int K, int V, float eta, float d_min, float d_max,
+                             float eps, float scale, int beta_aware, void* stream);
+
+/* Waits for `stream`, then reports OSDN_ERR_TIMEOUT if any kernel of this library gave up a
+ * bounded device-side wait since the last check (and clears the flag), OSDN_ERR_CUDA if the
+ * stream holds a CUDA error, else OSDN_OK. */
+osdn_status osdn_check(void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* osdn_status_string(int status);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int osdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSDN_H */

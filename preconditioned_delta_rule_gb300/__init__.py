@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) OSDN forward path: phase-1 preconditioner scan, chunkwise preconditioned
+delta rule, and single-token decode, behind the C ABI of include/osdn.h.
+
+The CUDA library (libosdn.so) is loaded on first use; a missing library raises ImportError.
+"""
+from .binding import (OSDN_BF16, OSDN_F16, OSDN_F32, OsdnError, chunk_osdn, osdn_check,
+                      osdn_chunk_fwd, osdn_decode_step, osdn_precond_scan, osdn_status_string,
+                      osdn_version)
+
+__all__ = ["OSDN_BF16", "OSDN_F16", "OSDN_F32", "OsdnError", "chunk_osdn", "osdn_check",
+           "osdn_chunk_fwd", "osdn_decode_step", "osdn_precond_scan", "osdn_status_string",
+           "osdn_version"]

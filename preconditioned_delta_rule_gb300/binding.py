@@ -1,0 +1,193 @@
+"""Thin ctypes binding over libosdn.so (include/osdn.h): argument marshalling only.
+
+Every function here takes torch CUDA tensors, checks shapes/dtypes/contiguity, allocates any
+output the caller did not pass (PyTorch is only the device-memory and stream provider), and
+calls the C entry point of the same name on the current torch stream.  All arithmetic runs in
+the library's CUDA kernels; there is no CPU or PyTorch fallback.  A missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+from typing import Optional
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libosdn.so"
+
+OSDN_F32, OSDN_BF16, OSDN_F16 = 0, 1, 2
+_DTYPE_CODE = {torch.float32: OSDN_F32, torch.bfloat16: OSDN_BF16, torch.float16: OSDN_F16}
+_STATUS = ["OSDN_OK", "OSDN_ERR_ARG", "OSDN_ERR_SHAPE", "OSDN_ERR_DTYPE", "OSDN_ERR_ALIGN",
+           "OSDN_ERR_UNSUPPORTED", "OSDN_ERR_CUDA", "OSDN_ERR_TIMEOUT"]
+
+_lib = None
+
+
+class OsdnError(RuntimeError):
+    """A non-OK status from the C ABI."""
+
+    def __init__(self, fn: str, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{fn}: {detail} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libosdn.so (built in-tree by ``preconditioned_delta_rule_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not LIB_PATH.exists():
+        raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                          "(python -m preconditioned_delta_rule_gb300.build)")
+    L = ctypes.CDLL(str(LIB_PATH))
+    vp, fp, i, f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.osdn_precond_scan.argtypes = [vp, i, fp, fp, fp, vp, i, fp, i, i, i, i, f, f, f, f, i, vp]
+    L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp]
+    L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
+    L.osdn_check.argtypes = [vp]
+    for fn in ("osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step", "osdn_check"):
+        getattr(L, fn).restype = ctypes.c_int
+    L.osdn_status_string.argtypes = [ctypes.c_int]
+    L.osdn_status_string.restype = ctypes.c_char_p
+    L.osdn_version.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def osdn_status_string(status: int) -> str:
+    return lib().osdn_status_string(int(status)).decode()
+
+
+def osdn_version() -> int:
+    return int(lib().osdn_version())
+
+
+def _raise(fn: str, st: int):
+    if st != 0:
+        raise OsdnError(fn, st, osdn_status_string(st))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device, stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(name, t, shape, dtype=None, device=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def _code(dtype) -> int:
+    if dtype not in _DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {dtype}; use float32, bfloat16 or float16")
+    return _DTYPE_CODE[dtype]
+
+
+def osdn_precond_scan(k, beta, r=None, d0=None, *, k_tilde=None, kt_dtype=None, d_out=None,
+                      eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6, beta_aware=True, stream=None):
+    """Phase 1 (Algorithm 1 / Eq. (4); APF Eq. (7) with r).  k [B,T,H,K] -> (k_tilde, d_out)."""
+    B, T, H, K = k.shape
+    dev = k.device
+    _check("k", k, (B, T, H, K), device=dev)
+    _check("beta", beta, (B, T, H), torch.float32, dev)
+    _check("r", r, (B, T, H), torch.float32, dev)
+    _check("d0", d0, (B, H, K), torch.float32, dev)
+    if k_tilde is None:
+        k_tilde = torch.empty((B, T, H, K), device=dev, dtype=kt_dtype or k.dtype)
+    _check("k_tilde", k_tilde, (B, T, H, K), device=dev)
+    if d_out is None:
+        d_out = torch.empty((B, H, K), device=dev, dtype=torch.float32)
+    _check("d_out", d_out, (B, H, K), torch.float32, dev)
+    st = lib().osdn_precond_scan(_ptr(k), _code(k.dtype), _ptr(beta), _ptr(r), _ptr(d0),
+                                 _ptr(k_tilde), _code(k_tilde.dtype), _ptr(d_out), B, T, H, K,
+                                 float(eta), float(d_min), float(d_max), float(eps),
+                                 int(bool(beta_aware)), _stream(dev, stream))
+    _raise("osdn_precond_scan", st)
+    return k_tilde, d_out
+
+
+def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, o=None, S_out=None, chunk=64, scale=1.0,
+                   stream=None):
+    """Phase 2 (Eqs. (2), (5), (8)-(11)).  Returns (o [B,T,H,V], S_out [B,H,V,K] fp32)."""
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    dev, dt = k.device, k.dtype
+    for name, t, shp in (("q", q, (B, T, H, K)), ("k", k, (B, T, H, K)),
+                         ("k_tilde", k_tilde, (B, T, H, K)), ("v", v, (B, T, H, V))):
+        _check(name, t, shp, dt, dev)
+    _check("beta", beta, (B, T, H), torch.float32, dev)
+    _check("S0", S0, (B, H, V, K), torch.float32, dev)
+    if o is None:
+        o = torch.empty((B, T, H, V), device=dev, dtype=dt)
+    _check("o", o, (B, T, H, V), dt, dev)
+    if S_out is None:
+        S_out = torch.empty((B, H, V, K), device=dev, dtype=torch.float32)
+    _check("S_out", S_out, (B, H, V, K), torch.float32, dev)
+    st = lib().osdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(k_tilde), _ptr(v), _code(dt), _ptr(beta),
+                              _ptr(S0), _ptr(o), _ptr(S_out), B, T, H, K, V, int(chunk),
+                              float(scale), _stream(dev, stream))
+    _raise("osdn_chunk_fwd", st)
+    return o, S_out
+
+
+def osdn_decode_step(q, k, v, beta, S, d, r=None, *, o=None, eta=0.003, d_min=0.5, d_max=2.0,
+                     eps=1e-6, scale=1.0, beta_aware=True, stream=None):
+    """One decode token in place on S [B,H,V,K] and d [B,H,K].  Returns o [B,H,V]."""
+    B, H, K = k.shape
+    V = v.shape[-1]
+    dev, dt = k.device, k.dtype
+    _check("q", q, (B, H, K), dt, dev)
+    _check("v", v, (B, H, V), dt, dev)
+    _check("beta", beta, (B, H), torch.float32, dev)
+    _check("r", r, (B, H), torch.float32, dev)
+    _check("S", S, (B, H, V, K), torch.float32, dev)
+    _check("d", d, (B, H, K), torch.float32, dev)
+    if o is None:
+        o = torch.empty((B, H, V), device=dev, dtype=dt)
+    _check("o", o, (B, H, V), dt, dev)
+    st = lib().osdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r),
+                                _ptr(S), _ptr(d), _ptr(o), B, H, K, V, float(eta), float(d_min),
+                                float(d_max), float(eps), float(scale), int(bool(beta_aware)),
+                                _stream(dev, stream))
+    _raise("osdn_decode_step", st)
+    return o
+
+
+def osdn_check(stream=None, device=None):
+    """Synchronise the stream and raise on a recorded device-side timeout or CUDA error."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _raise("osdn_check", lib().osdn_check(_stream(dev, stream)))
+
+
+def chunk_osdn(q, k, v, beta, precond_retention=None, initial_state=None, initial_d=None, *,
+               chunk_size=64, eta=0.003, beta_aware=True, d_min=0.5, d_max=2.0, eps=1e-6,
+               scale=1.0, kt_dtype=None, stream=None):
+    """Both phases of the layer forward (the pages' ``chunk_osdn`` signature, Listing 1):
+    osdn_precond_scan then osdn_chunk_fwd.  ``scale`` defaults to 1 (o_t = S_t q_t as in the
+    equations; pass K ** -0.5 for the listing's query scaling).  Returns (o, S, d)."""
+    kt, d = osdn_precond_scan(k, beta, precond_retention, initial_d, kt_dtype=kt_dtype or k.dtype,
+                              eta=eta, d_min=-math.inf if d_min is None else d_min,
+                              d_max=math.inf if d_max is None else d_max, eps=eps,
+                              beta_aware=beta_aware, stream=stream)
+    o, S = osdn_chunk_fwd(q, k, kt, v, beta, initial_state, chunk=chunk_size, scale=scale,
+                          stream=stream)
+    return o, S, d

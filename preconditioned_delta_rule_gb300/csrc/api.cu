@@ -1,0 +1,141 @@
+// api.cu -- the extern "C" entry points declared in include/osdn.h: argument validation on the
+// host (no launch on any error), dispatch to the kernels, status reporting.
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dtype_ok(int dt) { return dt == OSDN_F32 || dt == OSDN_BF16 || dt == OSDN_F16; }
+bool head_dim_ok(int x) { return x == 64 || x == 128; }
+
+// Pointer check: required pointers must be non-null; every non-null pointer 16-byte aligned.
+osdn_status ptr(const void* p, bool required) {
+    if (!p) return required ? OSDN_ERR_ARG : OSDN_OK;
+    return aligned16(p) ? OSDN_OK : OSDN_ERR_ALIGN;
+}
+
+#define OSDN_TRY(expr)                       \
+    do {                                     \
+        osdn_status _st = (expr);            \
+        if (_st != OSDN_OK) return _st;      \
+    } while (0)
+
+osdn_status phase1_scalars(float eta, float d_min, float d_max, float eps) {
+    if (!(eta >= 0.f) || !isfinite(eta)) return OSDN_ERR_ARG;
+    if (!(eps > 0.f) || !isfinite(eps)) return OSDN_ERR_ARG;
+    if (isnan(d_min) || isnan(d_max) || d_min > d_max) return OSDN_ERR_ARG;
+    return OSDN_OK;
+}
+
+osdn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* beta,
+                              const float* r, const float* d0, void* k_tilde,
+                              osdn_dtype kt_dtype, float* d_out, int B, int T, int H, int K,
+                              float eta, float d_min, float d_max, float eps, int beta_aware,
+                              void* stream) {
+    if (B < 0 || T < 0 || H < 0) return OSDN_ERR_SHAPE;
+    if (!head_dim_ok(K)) return K > 0 ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
+    if (!dtype_ok(k_dtype) || !dtype_ok(kt_dtype)) return OSDN_ERR_DTYPE;
+    OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
+    if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
+    if (B == 0 || H == 0) return OSDN_OK;
+    const bool seq = T > 0;
+    OSDN_TRY(ptr(k, seq));
+    OSDN_TRY(ptr(beta, seq));
+    OSDN_TRY(ptr(k_tilde, seq));
+    OSDN_TRY(ptr(r, false));
+    OSDN_TRY(ptr(d0, false));
+    OSDN_TRY(ptr(d_out, true));
+    OsdnScanArgs a{k, k_dtype, beta, r, d0, k_tilde, kt_dtype, d_out, B, T, H, K,
+                   eta, d_min, d_max, eps, beta_aware ? 1 : 0};
+    return from_cuda(osdn_launch_scan(a, static_cast<cudaStream_t>(stream)));
+}
+
+osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, const void* v,
+                           osdn_dtype dtype, const float* beta, const float* S0, void* o,
+                           float* S_out, int B, int T, int H, int K, int V, int chunk,
+                           float scale, void* stream) {
+    if (B < 0 || T < 0 || H < 0 || chunk <= 0) return OSDN_ERR_SHAPE;
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return (K > 0 && V > 0) ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
+    if (chunk != 64) return OSDN_ERR_UNSUPPORTED;
+    if (T % chunk != 0) return OSDN_ERR_SHAPE;
+    if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
+    if (!isfinite(scale)) return OSDN_ERR_ARG;
+    if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
+    if (B == 0 || H == 0) return OSDN_OK;
+    const bool seq = T > 0;
+    OSDN_TRY(ptr(q, seq));
+    OSDN_TRY(ptr(k, seq));
+    OSDN_TRY(ptr(k_tilde, seq));
+    OSDN_TRY(ptr(v, seq));
+    OSDN_TRY(ptr(beta, seq));
+    OSDN_TRY(ptr(o, seq));
+    OSDN_TRY(ptr(S0, false));
+    OSDN_TRY(ptr(S_out, true));
+    OsdnChunkArgs a{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (seq && dtype != OSDN_F32 && K == 128 && V == 128) {
+        cudaError_t e = osdn_launch_chunk_tc(a, s);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
+    return from_cuda(osdn_launch_chunk_simt(a, s));
+}
+
+osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,
+                             const float* beta, const float* r, float* S, float* d, void* o,
+                             int B, int H, int K, int V, float eta, float d_min, float d_max,
+                             float eps, float scale, int beta_aware, void* stream) {
+    if (B < 0 || H < 0) return OSDN_ERR_SHAPE;
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return (K > 0 && V > 0) ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
+    if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
+    OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
+    if (!isfinite(scale)) return OSDN_ERR_ARG;
+    if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
+    if (B == 0 || H == 0) return OSDN_OK;
+    OSDN_TRY(ptr(q, true));
+    OSDN_TRY(ptr(k, true));
+    OSDN_TRY(ptr(v, true));
+    OSDN_TRY(ptr(beta, true));
+    OSDN_TRY(ptr(r, false));
+    OSDN_TRY(ptr(S, true));
+    OSDN_TRY(ptr(d, true));
+    OSDN_TRY(ptr(o, true));
+    OsdnDecodeArgs a{q, k, v, dtype, beta, r, S, d, o, B, H, K, V,
+                     eta, d_min, d_max, eps, scale, beta_aware ? 1 : 0};
+    return from_cuda(osdn_launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+osdn_status osdn_check(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int flag = 0;
+    cudaError_t e = osdn_read_and_clear_timeout(&flag, s);
+    if (e != cudaSuccess) return OSDN_ERR_CUDA;
+    if (flag) return OSDN_ERR_TIMEOUT;
+    return OSDN_OK;
+}
+
+const char* osdn_status_string(int status) {
+    switch (status) {
+        case OSDN_OK: return "OSDN_OK";
+        case OSDN_ERR_ARG: return "OSDN_ERR_ARG: invalid argument (null pointer or bad scalar)";
+        case OSDN_ERR_SHAPE: return "OSDN_ERR_SHAPE: invalid sizes (negative, or T not a multiple of the chunk)";
+        case OSDN_ERR_DTYPE: return "OSDN_ERR_DTYPE: unknown dtype";
+        case OSDN_ERR_ALIGN: return "OSDN_ERR_ALIGN: a pointer is not 16-byte aligned";
+        case OSDN_ERR_UNSUPPORTED: return "OSDN_ERR_UNSUPPORTED: valid arguments not covered by a built kernel";
+        case OSDN_ERR_CUDA: return "OSDN_ERR_CUDA: a CUDA call or launch failed";
+        case OSDN_ERR_TIMEOUT: return "OSDN_ERR_TIMEOUT: a device-side bounded wait gave up";
+    }
+    return "OSDN: unknown status";
+}
+
+int osdn_version(void) { return 100; }
+
+}  // extern "C"

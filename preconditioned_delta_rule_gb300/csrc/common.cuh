@@ -1,0 +1,108 @@
+// common.cuh -- internal helpers shared by the OSDN kernels (not part of the public ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "osdn.h"
+
+namespace osdn {
+
+// ---- element load/store in the three storage dtypes -----------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+
+// Load N consecutive elements (N * sizeof(T) bytes, naturally aligned) as floats.
+template <typename T, int N> struct VecIO;
+template <int N> struct VecIO<float, N> {
+    static_assert(N == 2 || N == 4, "");
+    __device__ __forceinline__ static void load(const float* p, float* out) {
+        if constexpr (N == 4) {
+            float4 v = *reinterpret_cast<const float4*>(p);
+            out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+        } else {
+            float2 v = *reinterpret_cast<const float2*>(p);
+            out[0] = v.x; out[1] = v.y;
+        }
+    }
+    __device__ __forceinline__ static void store(float* p, const float* in) {
+        if constexpr (N == 4) *reinterpret_cast<float4*>(p) = make_float4(in[0], in[1], in[2], in[3]);
+        else *reinterpret_cast<float2*>(p) = make_float2(in[0], in[1]);
+    }
+};
+template <typename H, int N> struct VecIO16 {  // 16-bit types
+    static_assert(N == 2 || N == 4, "");
+    __device__ __forceinline__ static void load(const H* p, float* out) {
+        if constexpr (N == 4) {
+            uint2 v = *reinterpret_cast<const uint2*>(p);
+            const H* h = reinterpret_cast<const H*>(&v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) out[i] = to_f32(h[i]);
+        } else {
+            uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+            const H* h = reinterpret_cast<const H*>(&v);
+            out[0] = to_f32(h[0]);
+            out[1] = to_f32(h[1]);
+        }
+    }
+    __device__ __forceinline__ static void store(H* p, const float* in) {
+        if constexpr (N == 4) {
+            uint2 v;
+            H* h = reinterpret_cast<H*>(&v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[i] = from_f32<H>(in[i]);
+            *reinterpret_cast<uint2*>(p) = v;
+        } else {
+            uint32_t v;
+            H* h = reinterpret_cast<H*>(&v);
+            h[0] = from_f32<H>(in[0]);
+            h[1] = from_f32<H>(in[1]);
+            *reinterpret_cast<uint32_t*>(p) = v;
+        }
+    }
+};
+template <int N> struct VecIO<__nv_bfloat16, N> : VecIO16<__nv_bfloat16, N> {};
+template <int N> struct VecIO<__half, N> : VecIO16<__half, N> {};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+}  // namespace osdn
+
+// ---- host-side launchers, one per kernel family (defined in the .cu files) -------------------
+struct OsdnScanArgs {
+    const void* k; osdn_dtype k_dtype; const float* beta; const float* r; const float* d0;
+    void* k_tilde; osdn_dtype kt_dtype; float* d_out;
+    int B, T, H, K; float eta, d_min, d_max, eps; int beta_aware;
+};
+struct OsdnChunkArgs {
+    const void* q; const void* k; const void* k_tilde; const void* v; osdn_dtype dtype;
+    const float* beta; const float* S0; void* o; float* S_out;
+    int B, T, H, K, V, chunk; float scale;
+};
+struct OsdnDecodeArgs {
+    const void* q; const void* k; const void* v; osdn_dtype dtype; const float* beta;
+    const float* r; float* S; float* d; void* o;
+    int B, H, K, V; float eta, d_min, d_max, eps, scale; int beta_aware;
+};
+
+cudaError_t osdn_launch_scan(const OsdnScanArgs& a, cudaStream_t s);
+cudaError_t osdn_launch_chunk_simt(const OsdnChunkArgs& a, cudaStream_t s);
+// Returns cudaErrorNotSupported when the tensor-core kernel does not cover the arguments.
+cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, cudaStream_t s);
+cudaError_t osdn_launch_decode(const OsdnDecodeArgs& a, cudaStream_t s);
+// Reads and clears the device-side timeout word (synchronous on the given stream).
+cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s);

@@ -1,0 +1,165 @@
+// decode.cu -- one recurrent OSDN token for every (batch, head), in place on S and d.
+//
+// "OSDN: Improving Delta Rule with Provable Online Preconditioning in Linear Attention":
+// Algorithm 2 (parts 2a and 2b for a single token) with the APF gate of Eq. (7); the pages'
+// own decode path is a fused single-token kernel (Appendix L).  For one head:
+//   k~ = d . k (old d);  d <- clip(r d + eta b (1 - b <d, k.k>) / max(|k|^2, eps) * k.k)
+//   u_i = v_i - <S_i, k>;  S_i <- S_i + beta u_i k~;  o_i = <S_i_new, q'> = <S_i, q'> + beta u_i <k~, q'>
+// with q' = scale * q, for every row i of S (rows are independent given k, k~, q).
+//
+// The step is HBM-bound: S (V x K fp32) is read once and written once.  One CTA of 256 threads
+// per head; 8 lanes per row, each lane holding 4-float pieces interleaved so that every load
+// and store instruction of a warp covers four full 128-byte row segments.  All rows of a
+// thread are loaded before any is used so that each thread keeps its loads in flight together.
+#include "common.cuh"
+
+namespace osdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kLanesPerRow = 8;
+
+__device__ __forceinline__ float4 ld_stream(const float* p) {
+    float4 v;
+    asm volatile("ld.global.cs.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_stream(float* p, float4 v) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};\n" ::"l"(p), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w) : "memory");
+}
+
+template <int K, int V, typename TIn, bool HAS_R>
+__global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
+    constexpr int P4 = K / 4 / kLanesPerRow;        // float4 pieces per lane per row (4 or 2)
+    constexpr int ROWS_PER_PASS = kThreads / kLanesPerRow;  // 32
+    constexpr int PASSES = V / ROWS_PER_PASS;        // 4 or 2
+    constexpr int E = K / 32;
+    __shared__ __align__(16) float sk[K], skt[K], sq[K];
+    __shared__ float scoef[2];
+
+    const int tid = threadIdx.x;
+    const size_t bh = blockIdx.x;
+    float* S = a.S + bh * (size_t)V * K;
+
+    if (tid < 32) {  // warp 0: phase-1 step of this head, and the shared vectors
+        const TIn* kp = static_cast<const TIn*>(a.k) + bh * K + tid * E;
+        const TIn* qp = static_cast<const TIn*>(a.q) + bh * K + tid * E;
+        float kv[E], qv[E], dv[E];
+        VecIO<TIn, E>::load(kp, kv);
+        VecIO<TIn, E>::load(qp, qv);
+        VecIO<float, E>::load(a.d + bh * K + tid * E, dv);
+        float n = 0.f, al = 0.f, ktq = 0.f, s[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            s[i] = kv[i] * kv[i];
+            n += s[i];
+            al = fmaf(dv[i], s[i], al);
+            const float kt = dv[i] * kv[i];
+            const float qs = a.scale * qv[i];
+            ktq = fmaf(kt, qs, ktq);
+            sk[tid * E + i] = kv[i];
+            skt[tid * E + i] = kt;
+            sq[tid * E + i] = qs;
+        }
+        n = warp_sum(n);
+        al = warp_sum(al);
+        ktq = warp_sum(ktq);
+        const float bt = a.beta[bh];
+        const float rt = HAS_R ? a.r[bh] : 1.f;
+        const float bp = a.beta_aware ? bt : 1.f;
+        const float g = a.eta * bp * (1.f - bp * al) / fmaxf(n, a.eps);
+        float dn[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) dn[i] = fminf(fmaxf(fmaf(g, s[i], rt * dv[i]), a.d_min), a.d_max);
+        VecIO<float, E>::store(a.d + bh * K + tid * E, dn);
+        if (tid == 0) {
+            scoef[0] = bt;
+            scoef[1] = bt * ktq;
+        }
+    }
+    __syncthreads();
+
+    const int sub = tid % kLanesPerRow;
+    const int rg = tid / kLanesPerRow;
+    float kr[P4][4], ktr[P4][4], qr[P4][4];
+#pragma unroll
+    for (int c = 0; c < P4; ++c) {
+        const int col = (c * kLanesPerRow + sub) * 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            kr[c][j] = sk[col + j];
+            ktr[c][j] = skt[col + j];
+            qr[c][j] = sq[col + j];
+        }
+    }
+    const float bt = scoef[0], bktq = scoef[1];
+
+    float4 Sr[PASSES][P4];
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+        const int row = ps * ROWS_PER_PASS + rg;
+#pragma unroll
+        for (int c = 0; c < P4; ++c) Sr[ps][c] = ld_stream(S + (size_t)row * K + (c * kLanesPerRow + sub) * 4);
+    }
+    const TIn* vp = static_cast<const TIn*>(a.v) + bh * V;
+    TIn* op = static_cast<TIn*>(a.o) + bh * V;
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+        const int row = ps * ROWS_PER_PASS + rg;
+        float dk = 0.f, dq = 0.f;
+#pragma unroll
+        for (int c = 0; c < P4; ++c) {
+            const float4 x = Sr[ps][c];
+            dk = fmaf(x.x, kr[c][0], fmaf(x.y, kr[c][1], fmaf(x.z, kr[c][2], fmaf(x.w, kr[c][3], dk))));
+            dq = fmaf(x.x, qr[c][0], fmaf(x.y, qr[c][1], fmaf(x.z, qr[c][2], fmaf(x.w, qr[c][3], dq))));
+        }
+#pragma unroll
+        for (int o = kLanesPerRow / 2; o > 0; o >>= 1) {
+            dk += __shfl_xor_sync(0xffffffffu, dk, o);
+            dq += __shfl_xor_sync(0xffffffffu, dq, o);
+        }
+        const float u = to_f32(vp[row]) - dk;
+        const float bu = bt * u;
+#pragma unroll
+        for (int c = 0; c < P4; ++c) {
+            float4 x = Sr[ps][c];
+            x.x = fmaf(bu, ktr[c][0], x.x);
+            x.y = fmaf(bu, ktr[c][1], x.y);
+            x.z = fmaf(bu, ktr[c][2], x.z);
+            x.w = fmaf(bu, ktr[c][3], x.w);
+            st_stream(S + (size_t)row * K + (c * kLanesPerRow + sub) * 4, x);
+        }
+        if (sub == 0) op[row] = from_f32<TIn>(fmaf(bktq, u, dq));
+    }
+}
+
+template <int K, int V, typename TIn>
+cudaError_t launch3(const OsdnDecodeArgs& a, cudaStream_t s) {
+    dim3 grid((unsigned)(a.B * a.H)), block(kThreads);
+    if (a.r) decode_kernel<K, V, TIn, true><<<grid, block, 0, s>>>(a);
+    else decode_kernel<K, V, TIn, false><<<grid, block, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int K, int V>
+cudaError_t launch2(const OsdnDecodeArgs& a, cudaStream_t s) {
+    switch (a.dtype) {
+        case OSDN_F32: return launch3<K, V, float>(a, s);
+        case OSDN_BF16: return launch3<K, V, __nv_bfloat16>(a, s);
+        case OSDN_F16: return launch3<K, V, __half>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace osdn
+
+cudaError_t osdn_launch_decode(const OsdnDecodeArgs& a, cudaStream_t s) {
+    if (a.K == 128 && a.V == 128) return osdn::launch2<128, 128>(a, s);
+    if (a.K == 128 && a.V == 64) return osdn::launch2<128, 64>(a, s);
+    if (a.K == 64 && a.V == 128) return osdn::launch2<64, 128>(a, s);
+    if (a.K == 64 && a.V == 64) return osdn::launch2<64, 64>(a, s);
+    return cudaErrorInvalidValue;
+}

@@ -1,0 +1,114 @@
+"""Host-only checks of the C ABI (no GPU needed): the library loads, exports every entry point
+that include/osdn.h declares, and rejects bad arguments on the host before any launch.
+
+Every call here is built to be REJECTED by validation (or to have nothing to do), so no kernel
+is ever launched with the fake device addresses used below.
+"""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+import torch
+
+from preconditioned_delta_rule_gb300 import binding
+from preconditioned_delta_rule_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+A = 0x10000  # a fake, 16-byte-aligned "device address" (never dereferenced: see module doc)
+OK, ARG, SHAPE, DTYPE, ALIGN, UNSUP = 0, 1, 2, 3, 4, 5
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return binding.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "osdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(osdn_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = header_functions()
+    assert {"osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"libosdn.so does not export {n}"
+
+
+def test_status_strings_and_version(L):
+    for code in range(8):
+        s = binding.osdn_status_string(code)
+        assert s.startswith(binding._STATUS[code])
+    assert "unknown" in binding.osdn_status_string(99)
+    assert binding.osdn_version() >= 100
+
+
+def scan(L, **kw):
+    a = dict(k=A, kdt=1, beta=A, r=None, d0=None, kt=A, ktdt=1, dout=A, B=2, T=64, H=2, K=128,
+             eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6, ba=1)
+    a.update(kw)
+    return L.osdn_precond_scan(a["k"], a["kdt"], a["beta"], a["r"], a["d0"], a["kt"], a["ktdt"],
+                               a["dout"], a["B"], a["T"], a["H"], a["K"], a["eta"], a["dmin"],
+                               a["dmax"], a["eps"], a["ba"], None)
+
+
+def chunk(L, **kw):
+    a = dict(q=A, k=A, kt=A, v=A, dt=1, beta=A, S0=None, o=A, Sout=A, B=2, T=128, H=2, K=128,
+             V=128, C=64, scale=1.0)
+    a.update(kw)
+    return L.osdn_chunk_fwd(a["q"], a["k"], a["kt"], a["v"], a["dt"], a["beta"], a["S0"], a["o"],
+                            a["Sout"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"], a["scale"],
+                            None)
+
+
+def decode(L, **kw):
+    a = dict(q=A, k=A, v=A, dt=1, beta=A, r=None, S=A, d=A, o=A, B=2, H=2, K=128, V=128,
+             eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6, scale=1.0, ba=1)
+    a.update(kw)
+    return L.osdn_decode_step(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a["S"], a["d"],
+                              a["o"], a["B"], a["H"], a["K"], a["V"], a["eta"], a["dmin"],
+                              a["dmax"], a["eps"], a["scale"], a["ba"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(k=None), ARG), (dict(beta=None), ARG), (dict(kt=None), ARG), (dict(dout=None), ARG),
+    (dict(k=A + 8), ALIGN), (dict(r=A + 4), ALIGN), (dict(d0=A + 2), ALIGN),
+    (dict(K=96), UNSUP), (dict(K=0), SHAPE), (dict(B=-1), SHAPE), (dict(T=-1), SHAPE),
+    (dict(kdt=7), DTYPE), (dict(ktdt=-1), DTYPE),
+    (dict(eta=-0.1), ARG), (dict(eta=math.nan), ARG), (dict(eps=0.0), ARG),
+    (dict(dmin=2.0, dmax=0.5), ARG), (dict(dmin=math.nan), ARG),
+    (dict(B=0), OK), (dict(H=0), OK),
+])
+def test_scan_validation(L, kw, want):
+    assert scan(L, **kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), ARG), (dict(kt=None), ARG), (dict(o=None), ARG), (dict(Sout=None), ARG),
+    (dict(v=A + 8), ALIGN), (dict(S0=A + 4), ALIGN),
+    (dict(T=100), SHAPE), (dict(C=0), SHAPE), (dict(C=32), UNSUP), (dict(K=256), UNSUP),
+    (dict(V=48), UNSUP), (dict(dt=5), DTYPE), (dict(scale=math.inf), ARG),
+    (dict(B=0), OK),
+])
+def test_chunk_validation(L, kw, want):
+    assert chunk(L, **kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(S=None), ARG), (dict(d=None), ARG), (dict(o=None), ARG), (dict(q=A + 1), ALIGN),
+    (dict(K=32), UNSUP), (dict(dt=3), DTYPE), (dict(eps=-1.0), ARG), (dict(scale=math.nan), ARG),
+    (dict(H=0), OK),
+])
+def test_decode_validation(L, kw, want):
+    assert decode(L, **kw) == want
+
+
+def test_binding_rejects_host_tensors(L):
+    k = torch.zeros(1, 64, 1, 64, dtype=torch.bfloat16)
+    beta = torch.zeros(1, 64, 1)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.osdn_precond_scan(k, beta)
