@@ -1,12 +1,546 @@
-// chunk_tc.cu -- tensor-core (TMA + tcgen05/TMEM) kernel for phase 2 of OSDN.
+// chunk_tc.cu -- tensor-core kernel for phase 2 of OSDN: the chunkwise preconditioned delta rule.
+//
+// "OSDN: Improving Delta Rule with Provable Online Preconditioning in Linear Attention",
+// Section 4.3 (Eqs. (5)-(6)) and Appendix A.2 (Eqs. (8)-(11)).  For one chunk of C = 64 tokens
+// with keys K, write keys K~ (C x K), values V (C x V), queries Q and gates beta:
+//   A  = tril(diag(beta) K K~^T, -1)            (Gram with the write key, Eq. (6))
+//   T  = (I + A)^-1,  T' = T diag(beta)          (UT transform, Eq. (8); fp32 forward substitution)
+//   W  = T' K,  U = T' V                         (Eq. (9): the read key stays in W)
+//   X  = U - W S^T                               (the chunk's scaled residuals)
+//   O  = scale * (Q S^T + tril(Q K~^T, 0) X)     (readout after each write: the diagonal is kept)
+//   S <- S + X^T K~                              (Eq. (11))
+// with S carried across chunks in fp32.
+//
+// Design (one CTA per (batch, head, 64 rows of S); rows of S evolve independently given K, K~,
+// beta, so the V dimension splits across CTAs with no exchange):
+//   * TMA (128-byte swizzle) brings the K, Q, K~, V tiles of chunk n+1 into the other of two
+//     shared-memory stages while chunk n is processed.
+//   * Operands are fp16 (10-bit mantissa): bf16 inputs are converted in place (exact for
+//     normal-range values); computed operands (T', W, S, X, L) are rounded to fp16.  All
+//     products accumulate in fp32 in tensor memory.  fp16 rather than bf16 operands keep the
+//     o/S error ~8x smaller at no extra tensor-core work.
+//   * Every product is one tcgen05.mma group with M = 128, stacking two 64-row operands:
+//       [K; Q] K~^T            -> lanes 0-63: K K~^T (Gram),  lanes 64-127: Q K~^T (scores)
+//       [0; T'] K, [0; T'] V   -> lanes 64-127: W, U
+//       [Q; -W] S^T   (+= U)   -> lanes 0-63: Q S^T,        lanes 64-127: X = U - W S^T
+//       [L; 0] X      (+=)     -> lanes 0-63: O
+//       K~^T X        (+= S^T) -> S^T accumulated in tensor memory (fp32, lanes = key dim)
+//   * The triangular inverse is blocked (16 x 16 diagonal blocks by forward substitution, then
+//     three levels of block products) in fp32 on the CUDA cores.
+// All waits on mbarriers are bounded; on expiry the kernel records a timeout (reported by
+// osdn_check), drains what it issued and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <type_traits>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace osdn {
 // Set by any kernel of this library whose bounded device-side wait gave up.
 __device__ unsigned int g_timeout_flag = 0;
+
+namespace {
+
+constexpr int C = 64;          // chunk length
+constexpr int KD = 128;        // key dim
+constexpr int VS = 64;         // rows of S (value dims) per CTA
+constexpr int NTHREADS = 128;
+constexpr uint32_t kMaxPolls = 1u << 22;
+
+// shared memory map (byte offsets from a 1024-byte-aligned base)
+constexpr uint32_t KQW_KB = 3 * 8192;                 // per 64-wide key block: K | Q | -W
+constexpr uint32_t ST_KQW = 0;
+constexpr uint32_t ST_KT = 2 * KQW_KB;                // 49152: K~, 2 key blocks
+constexpr uint32_t ST_V = ST_KT + 2 * 8192;           // 65536: V slice
+constexpr uint32_t STAGE = ST_V + (VS / 64) * 8192;   // 73728
+constexpr uint32_t OFF_LZT = 2 * STAGE;               // L | zeros | T'  (8 KB each)
+constexpr uint32_t OFF_X = OFF_LZT + 3 * 8192;
+constexpr uint32_t OFF_SS = OFF_X + (VS / 64) * 8192;  // fp16 copy of S (MN-major B operand)
+constexpr uint32_t BLK = 16 * 17;                      // one padded 16x16 fp32 block (floats)
+constexpr uint32_t OFF_AM = OFF_SS + (VS / 64) * KD * 128;
+constexpr uint32_t OFF_TM = OFF_AM + 10 * BLK * 4;     // 10 lower-triangular blocks
+constexpr uint32_t OFF_PM = OFF_TM + 10 * BLK * 4;
+constexpr uint32_t OFF_BETA = OFF_PM + 3 * BLK * 4;
+constexpr uint32_t OFF_BAR = OFF_BETA + 2 * C * 4;
+constexpr uint32_t SMEM_USED = OFF_BAR + 64;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+static_assert(OFF_LZT % 1024 == 0 && OFF_X % 1024 == 0 && OFF_SS % 1024 == 0, "swizzle atoms");
+constexpr uint32_t TMA_BYTES = 2 * 2 * 8192 + 2 * 8192 + (VS / 64) * 8192;
+
+// tensor-memory columns
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_G = 0, COL_W = 64, COL_R = 192, COL_ST = 256;
+
+__device__ __forceinline__ int pb(int i, int j) { return i * (i + 1) / 2 + j; }
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Write 8 consecutive values as fp16 into chunk `c` of row `r` of a swizzled atom stack.
+__device__ __forceinline__ void st_row_chunk(unsigned char* base, uint32_t r, uint32_t c,
+                                             const float* v) {
+    uint4 u;
+    u.x = pack_h2(v[0], v[1]);
+    u.y = pack_h2(v[2], v[3]);
+    u.z = pack_h2(v[4], v[5]);
+    u.w = pack_h2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(base + tc::sw128_off(r, c)) = u;
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(NTHREADS, 1)
+chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmKT, const __grid_constant__ CUtensorMap tmV,
+                const float* __restrict__ beta, const float* S0, TIn* __restrict__ out,
+                float* S_out, int T, int H, int V, float scale) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    const int v0 = blockIdx.y * VS;
+    const int N = T / C;
+
+    float* AM = reinterpret_cast<float*>(sm + OFF_AM);
+    float* TM = reinterpret_cast<float*>(sm + OFF_TM);
+    float* PM = reinterpret_cast<float*>(sm + OFF_PM);
+    float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
+    const uint32_t bar_tma0 = tc::smem_u32(sm + OFF_BAR);
+    const uint32_t bar_mma = tc::smem_u32(sm + OFF_BAR + 16);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 24);
+    const uint32_t sbase = tc::smem_u32(sm);
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    // ---- set-up: barriers, zero block, tensor memory, initial state ------------------------
+    if (tid == 0) {
+        tc::mbar_init(bar_tma0, 1);
+        tc::mbar_init(bar_tma0 + 8, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::mbar_init_fence();
+        tc::prefetch_tmap(&tmQ);
+        tc::prefetch_tmap(&tmK);
+        tc::prefetch_tmap(&tmKT);
+        tc::prefetch_tmap(&tmV);
+    }
+    for (int e = tid; e < 8192 / 16; e += NTHREADS)
+        reinterpret_cast<uint4*>(sm + OFF_LZT + 8192)[e] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+
+    auto issue_tma = [&](int m, int s) {
+        const uint32_t bar = bar_tma0 + 8 * s;
+        const uint32_t st = sbase + s * STAGE;
+        const int row = b * T + m * C;
+        tc::mbar_expect_tx(bar, TMA_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tc::tma_load_3d(st + ST_KQW + kb * KQW_KB, &tmK, bar, kb * 64, h, row);
+            tc::tma_load_3d(st + ST_KQW + kb * KQW_KB + 8192, &tmQ, bar, kb * 64, h, row);
+            tc::tma_load_3d(st + ST_KT + kb * 8192, &tmKT, bar, kb * 64, h, row);
+        }
+#pragma unroll
+        for (int vb = 0; vb < VS / 64; ++vb)
+            tc::tma_load_3d(st + ST_V + vb * 8192, &tmV, bar, v0 + vb * 64, h, row);
+    };
+    if (tid == 0 && N > 0) issue_tma(0, 0);
+    if (tid < C && N > 0) sbeta[tid] = beta[(static_cast<size_t>(b) * T + tid) * H + h];
+
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    {  // S0 slice -> S^T in tensor memory (lane = key coordinate) and its fp16 operand copy
+        const int k = tid;
+        float sv[32];
+#pragma unroll
+        for (int half = 0; half < VS / 32; ++half) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int v = half * 32 + j;
+                sv[j] = S0 ? S0[(static_cast<size_t>(bh) * V + v0 + v) * KD + k] : 0.f;
+            }
+            tc::tmem_st32(tbase + lane_base + COL_ST + half * 32, sv);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                st_row_chunk(sm + OFF_SS + ((half * 32) / 64) * (KD * 128), k, ((half * 32) % 64) / 8 + c,
+                             sv + 8 * c);
+        }
+        tc::tmem_st_wait();
+    }
+    tc::fence_proxy_async();
+    tc::tc_fence_before();
+    __syncthreads();
+
+    uint32_t mph = 0;
+    bool aborted = false;
+    bool tma_pending[2] = {N > 0, false};
+    int tma_chunk[2] = {0, 0};  // chunk index of the load last issued into each stage
+    bool mma_pending = false;
+    auto wait_mma = [&]() -> bool {
+        const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
+        const bool all = __syncthreads_and(ok);
+        if (all) {
+            mph ^= 1u;
+            mma_pending = false;
+            tc::tc_fence_after();
+        }
+        return all;
+    };
+
+    const uint32_t id_gram = tc::idesc_f16_f32(128, C, false, false);
+    const uint32_t id_wk = tc::idesc_f16_f32(128, KD, false, true);
+    const uint32_t id_uv = tc::idesc_f16_f32(128, VS, false, true);
+    const uint32_t id_chain = tc::idesc_f16_f32(128, VS, false, true);
+    const uint32_t id_state = tc::idesc_f16_f32(128, VS, true, true);
+
+    for (int n = 0; n < N; ++n) {
+        const int s = n & 1;
+        unsigned char* stg = sm + s * STAGE;
+        const uint32_t stg_a = sbase + s * STAGE;
+        // 1. prefetch chunk n+1 (its stage was last read by chunk n-1, fully retired)
+        if (tid == 0 && n + 1 < N) issue_tma(n + 1, s ^ 1);
+        if (n + 1 < N) {
+            tma_pending[s ^ 1] = true;
+            tma_chunk[s ^ 1] = n + 1;
+        }
+        float beta_next = 0.f;
+        if (tid < C && n + 1 < N)
+            beta_next = beta[(static_cast<size_t>(b) * T + (n + 1) * C + tid) * H + h];
+
+        // 2. wait for this chunk's tiles
+        {
+            const bool ok = tc::mbar_wait(bar_tma0 + 8 * s, (n >> 1) & 1, kMaxPolls);
+            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            tma_pending[s] = false;
+        }
+        // 3. bf16 -> fp16 in place (K, Q, K~, V)
+        if constexpr (!std::is_same<TIn, __half>::value) {
+            for (int e = tid; e < 3584; e += NTHREADS) {
+                uint32_t off;
+                if (e < 2048) off = ST_KQW + (e >> 10) * KQW_KB + (e & 1023) * 16;
+                else if (e < 3072) off = ST_KT + (e - 2048) * 16;
+                else off = ST_V + (e - 3072) * 16;
+                uint4* p = reinterpret_cast<uint4*>(stg + off);
+                uint4 u = *p;
+                uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    w[i] = pack_h2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+                *p = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        tc::fence_proxy_async();
+        __syncthreads();
+
+        // 4. [K; Q] K~^T
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < KD / 16; ++st) {
+                const uint64_t a = tc::sdesc_sw128(stg_a + ST_KQW + (st >> 2) * KQW_KB + (st & 3) * 32, 16, 1024);
+                const uint64_t bd = tc::sdesc_sw128(stg_a + ST_KT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
+                tc::mma_f16(tbase + COL_G, a, bd, id_gram, st > 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        if (!wait_mma()) { aborted = true; break; }
+
+        // 5. A rows (lanes 0-63) to fp32 blocks; score rows L (lanes 64-127) to fp16
+        {
+            float g[64];
+            tc::tmem_ld32(tbase + lane_base + COL_G, *reinterpret_cast<float(*)[32]>(g));
+            tc::tmem_ld32(tbase + lane_base + COL_G + 32, *reinterpret_cast<float(*)[32]>(g + 32));
+            tc::tmem_ld_wait();
+            if (tid < C) {
+                const int i = tid, bi = i >> 4, r = i & 15;
+                const float bt = sbeta[s * C + i];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const int bj = j >> 4;
+                    if (bj <= bi) AM[pb(bi, bj) * BLK + r * 17 + (j & 15)] = (j < i) ? bt * g[j] : 0.f;
+                }
+            } else {
+                const int i = tid - C;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) g[j] = (j <= i) ? g[j] : 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) st_row_chunk(sm + OFF_LZT, i, c, g + 8 * c);
+            }
+        }
+        tc::tc_fence_before();
+        __syncthreads();
+
+        // 6. T = (I + A)^-1 in fp32: diagonal blocks, then three levels of block products
+        if (tid < C) {
+            const int blk = tid >> 4, c = tid & 15;
+            const float* Ab = AM + pb(blk, blk) * BLK;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+#pragma unroll
+                for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-Ab[i * 17 + m], x[m], x[i]);
+            float* Tb = TM + pb(blk, blk) * BLK;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tb[i * 17 + c] = x[i];
+        }
+        __syncthreads();
+        for (int lam = 1; lam < 4; ++lam) {
+            const int nb = 4 - lam;
+            for (int e = tid; e < nb * 256; e += NTHREADS) {
+                const int blk = e >> 8, ii = (e >> 4) & 15, jj = e & 15;
+                const int j = blk, i = j + lam;
+                float acc = 0.f;
+                for (int m = j; m < i; ++m) {
+                    const float* Ar = AM + pb(i, m) * BLK + ii * 17;
+                    const float* Tc = TM + pb(m, j) * BLK + jj;
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) acc = fmaf(Ar[kk], Tc[kk * 17], acc);
+                }
+                PM[blk * BLK + ii * 17 + jj] = acc;
+            }
+            __syncthreads();
+            for (int e = tid; e < nb * 256; e += NTHREADS) {
+                const int blk = e >> 8, ii = (e >> 4) & 15, jj = e & 15;
+                const int j = blk, i = j + lam;
+                const float* Tr = TM + pb(i, i) * BLK + ii * 17;
+                const float* Pc = PM + blk * BLK + jj;
+                float acc = 0.f;
+                for (int kk = 0; kk <= ii; ++kk) acc = fmaf(Tr[kk], Pc[kk * 17], acc);
+                TM[pb(i, j) * BLK + ii * 17 + jj] = -acc;
+            }
+            __syncthreads();
+        }
+        // T' = T diag(beta) -> fp16 rows of the [0; T'] operand
+        {
+            const int i = tid >> 1, half = tid & 1, bi = i >> 4, r = i & 15;
+            float t[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = half * 32 + jj, bj = j >> 4;
+                const float tv = (bj <= bi) ? TM[pb(bi, bj) * BLK + r * 17 + (j & 15)] : 0.f;
+                t[jj] = tv * sbeta[s * C + j];
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) st_row_chunk(sm + OFF_LZT + 16384, i, half * 4 + c, t + 8 * c);
+        }
+        tc::fence_proxy_async();
+        __syncthreads();
+
+        // 7. W = T' K (lanes 64-127 of COL_W), U = T' V (lanes 64-127 of COL_R)
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st) {
+                const uint64_t a = tc::sdesc_sw128(sbase + OFF_LZT + 8192 + st * 32, 16, 1024);
+                const uint64_t bk = tc::sdesc_sw128(stg_a + ST_KQW + st * 2048, KQW_KB, 1024);
+                tc::mma_f16(tbase + COL_W, a, bk, id_wk, st > 0);
+                const uint64_t bv = tc::sdesc_sw128(stg_a + ST_V + st * 2048, 8192, 1024);
+                tc::mma_f16(tbase + COL_R, a, bv, id_uv, st > 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        if (!wait_mma()) { aborted = true; break; }
+
+        // 8. -W -> fp16 rows under Q in each key block
+        if (tid >= C) {
+            const int c = tid - C;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float w[32];
+                tc::tmem_ld32(tbase + lane_base + COL_W + q4 * 32, w);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = -w[j];
+                const int kb = q4 >> 1;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    st_row_chunk(stg + ST_KQW + kb * KQW_KB + 16384, c, (q4 & 1) * 4 + cc, w + 8 * cc);
+            }
+        }
+        tc::fence_proxy_async();
+        tc::tc_fence_before();
+        __syncthreads();
+
+        // 9. [Q; -W] S^T accumulated onto [0; U]
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < KD / 16; ++st) {
+                const uint64_t a = tc::sdesc_sw128(stg_a + ST_KQW + (st >> 2) * KQW_KB + 8192 + (st & 3) * 32, 16, 1024);
+                const uint64_t bs = tc::sdesc_sw128(sbase + OFF_SS + st * 2048, KD * 128, 1024);
+                tc::mma_f16(tbase + COL_R, a, bs, id_chain, 1);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        if (!wait_mma()) { aborted = true; break; }
+
+        // 10. X rows (lanes 64-127) -> fp16 operand
+        if (tid >= C) {
+            const int c = tid - C;
+#pragma unroll
+            for (int q2 = 0; q2 < VS / 32; ++q2) {
+                float x[32];
+                tc::tmem_ld32(tbase + lane_base + COL_R + q2 * 32, x);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    st_row_chunk(sm + OFF_X + ((q2 * 32) / 64) * 8192, c, ((q2 * 32) % 64) / 8 + cc, x + 8 * cc);
+            }
+        }
+        tc::fence_proxy_async();
+        tc::tc_fence_before();
+        __syncthreads();
+
+        // 11. O += L X (lanes 0-63 of COL_R);  S^T += K~^T X
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st) {
+                const uint64_t bx = tc::sdesc_sw128(sbase + OFF_X + st * 2048, 8192, 1024);
+                const uint64_t al = tc::sdesc_sw128(sbase + OFF_LZT + st * 32, 16, 1024);
+                tc::mma_f16(tbase + COL_R, al, bx, id_uv, 1);
+                const uint64_t ak = tc::sdesc_sw128(stg_a + ST_KT + st * 2048, 8192, 1024);
+                tc::mma_f16(tbase + COL_ST, ak, bx, id_state, 1);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        if (!wait_mma()) { aborted = true; break; }
+
+        // 12. outputs of the chunk; fp16 copy of the new S for the next chunk
+        if (tid < C) {
+            const int c = tid;
+            TIn* orow = out + ((static_cast<size_t>(b) * T + n * C + c) * H + h) * V + v0;
+#pragma unroll
+            for (int q2 = 0; q2 < VS / 32; ++q2) {
+                float o[32];
+                tc::tmem_ld32(tbase + lane_base + COL_R + q2 * 32, o);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float ov[4] = {scale * o[j], scale * o[j + 1], scale * o[j + 2], scale * o[j + 3]};
+                    VecIO<TIn, 4>::store(orow + q2 * 32 + j, ov);
+                }
+            }
+        }
+        {
+            const int k = tid;
+#pragma unroll
+            for (int q2 = 0; q2 < VS / 32; ++q2) {
+                float sv[32];
+                tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, sv);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    st_row_chunk(sm + OFF_SS + ((q2 * 32) / 64) * (KD * 128), k, ((q2 * 32) % 64) / 8 + cc, sv + 8 * cc);
+            }
+        }
+        if (tid < C && n + 1 < N) sbeta[(s ^ 1) * C + tid] = beta_next;
+        tc::fence_proxy_async();
+        tc::tc_fence_before();
+        __syncthreads();
+    }
+
+    if (aborted) {
+        if (tid == 0) atomicExch(&g_timeout_flag, 1u);
+        // drain whatever is still in flight (bounded), so the CTA leaves nothing behind
+        for (int s = 0; s < 2; ++s)
+            if (tma_pending[s]) tc::mbar_wait(bar_tma0 + 8 * s, (tma_chunk[s] >> 1) & 1, kMaxPolls >> 4);
+        if (mma_pending) tc::mbar_wait(bar_mma, mph, kMaxPolls >> 4);
+        tc::tc_fence_before();
+        __syncthreads();
+        tc::tc_fence_after();
+    } else {
+        // final state S_out[v0 + v][k] = S^T[k][v]
+        const int k = tid;
+#pragma unroll
+        for (int q2 = 0; q2 < VS / 32; ++q2) {
+            float sv[32];
+            tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, sv);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                S_out[(static_cast<size_t>(bh) * V + v0 + q2 * 32 + j) * KD + k] = sv[j];
+        }
+        tc::tc_fence_before();
+        __syncthreads();
+        tc::tc_fence_after();
+    }
+    if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [B*T rows of H heads of `inner` elements]: dims (inner, H, B*T), box (64, 1, 64).
+bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int inner, int H, long long rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, static_cast<cuuint64_t>(H) * inner * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename TIn>
+cudaError_t launch_tc(const OsdnChunkArgs& a, cudaStream_t s) {
+    const CUtensorMapDataType dt = std::is_same<TIn, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const long long rows = static_cast<long long>(a.B) * a.T;
+    CUtensorMap mq, mk, mkt, mv;
+    if (!make_map(&mq, a.q, dt, a.K, a.H, rows) || !make_map(&mk, a.k, dt, a.K, a.H, rows) ||
+        !make_map(&mkt, a.k_tilde, dt, a.K, a.H, rows) || !make_map(&mv, a.v, dt, a.V, a.H, rows))
+        return cudaErrorNotSupported;
+    static std::once_flag attr_once[2];
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once[std::is_same<TIn, __half>::value ? 1 : 0], [&] {
+        attr_err = cudaFuncSetAttribute(chunk_tc_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_ALLOC);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS)), block(NTHREADS);
+    chunk_tc_kernel<TIn><<<grid, block, SMEM_ALLOC, s>>>(mq, mk, mkt, mv, a.beta, a.S0,
+                                                         static_cast<TIn*>(a.o), a.S_out, a.T, a.H,
+                                                         a.V, a.scale);
+    return cudaGetLastError();
+}
+
+}  // namespace
 }  // namespace osdn
 
-cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, cudaStream_t s) {
+    if (a.K != osdn::KD || a.V % osdn::VS != 0 || a.chunk != osdn::C || a.T <= 0 || a.T % osdn::C)
+        return cudaErrorNotSupported;
+    if (a.dtype == OSDN_BF16) return osdn::launch_tc<__nv_bfloat16>(a, s);
+    if (a.dtype == OSDN_F16) return osdn::launch_tc<__half>(a, s);
+    return cudaErrorNotSupported;
+}
 
 cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s) {
     cudaError_t e = cudaStreamSynchronize(s);
