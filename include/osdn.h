@@ -41,6 +41,8 @@
 #ifndef OSDN_H
 #define OSDN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -87,13 +89,28 @@ osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* be
  *   chunk    chunk length C; 64 is the only value built.  T must be a multiple of C (T = 0 is
  *            allowed and copies S0 to S_out).
  *   scale    multiplies q (1.0 gives o_t = S_t q_t as in the equations; Listing 1 uses K^-1/2).
- * bf16/f16 inputs with K = V = 128 run on the tensor-core kernel (TMA + tcgen05, fp32
- * accumulation, fp32 state); other shapes and fp32 inputs run an fp32 CUDA-core kernel.
+ *   workspace, workspace_bytes
+ *            optional caller-owned device scratch (16-byte aligned).  When it holds at least
+ *            osdn_chunk_fwd_workspace_bytes(...) bytes, the tensor-core path splits into a
+ *            parallel kernel over all chunks (everything that does not depend on S: the UT
+ *            transform T' and W, kept as fp16 in the workspace) and a serial kernel over chunks;
+ *            with NULL or a smaller workspace one fused kernel does both (slower, no scratch).
+ *            Results are the same either way.  The workspace is overwritten; its contents on
+ *            return are unspecified.
+ * bf16/f16 inputs with K = V = 128 run on the tensor-core kernels (TMA + tcgen05, fp16
+ * operands, fp32 accumulation, fp32 state); other shapes and fp32 inputs run an fp32
+ * CUDA-core kernel (which needs no workspace).
  */
 osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, const void* v,
                            osdn_dtype dtype, const float* beta, const float* S0, void* o,
                            float* S_out, int B, int T, int H, int K, int V, int chunk,
-                           float scale, void* stream);
+                           float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace size in bytes that lets osdn_chunk_fwd use its two-kernel tensor-core path for these
+ * arguments (0 when that path does not apply: then no workspace is ever used).  For K = V = 128
+ * and chunk 64 it is B * H * (T / 64) * 24576 bytes (24 KiB per chunk of each head). */
+size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
+                                      osdn_dtype dtype);
 
 /*
  * One decode token for every (batch, head), in place (recurrent form of both phases):

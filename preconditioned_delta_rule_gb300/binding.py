@@ -44,7 +44,10 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(str(LIB_PATH))
     vp, fp, i, f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     L.osdn_precond_scan.argtypes = [vp, i, fp, fp, fp, vp, i, fp, i, i, i, i, f, f, f, f, i, vp]
-    L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp]
+    sz = ctypes.c_size_t
+    L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp, sz, vp]
+    L.osdn_chunk_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    L.osdn_chunk_fwd_workspace_bytes.restype = sz
     L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
     L.osdn_check.argtypes = [vp]
     for fn in ("osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step", "osdn_check"):
@@ -125,9 +128,28 @@ def osdn_precond_scan(k, beta, r=None, d0=None, *, k_tilde=None, kt_dtype=None, 
     return k_tilde, d_out
 
 
+_WS_CACHE = {}
+
+
+def osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16) -> int:
+    return int(lib().osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, _code(dtype)))
+
+
+def _workspace(device, nbytes):
+    """A cached uint8 device buffer of at least nbytes (torch allocates; the library never does)."""
+    buf = _WS_CACHE.get(device)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+        _WS_CACHE[device] = buf
+    return buf
+
+
 def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, o=None, S_out=None, chunk=64, scale=1.0,
-                   stream=None):
-    """Phase 2 (Eqs. (2), (5), (8)-(11)).  Returns (o [B,T,H,V], S_out [B,H,V,K] fp32)."""
+                   workspace=None, stream=None):
+    """Phase 2 (Eqs. (2), (5), (8)-(11)).  Returns (o [B,T,H,V], S_out [B,H,V,K] fp32).
+
+    ``workspace``: None (default) uses a cached torch buffer of the size the library asks for;
+    a uint8 CUDA tensor is used as given; False runs the no-scratch fused kernel."""
     B, T, H, K = k.shape
     V = v.shape[-1]
     dev, dt = k.device, k.dtype
@@ -142,9 +164,20 @@ def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, o=None, S_out=None, chunk
     if S_out is None:
         S_out = torch.empty((B, H, V, K), device=dev, dtype=torch.float32)
     _check("S_out", S_out, (B, H, V, K), torch.float32, dev)
+    need = osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 else 0
+    if workspace is None:
+        ws = _workspace(dev, need) if need else None
+    elif workspace is False:
+        ws = None
+    else:
+        ws = workspace
+        if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_ptr = None if ws is None else ctypes.c_void_p(ws.data_ptr())
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     st = lib().osdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(k_tilde), _ptr(v), _code(dt), _ptr(beta),
                               _ptr(S0), _ptr(o), _ptr(S_out), B, T, H, K, V, int(chunk),
-                              float(scale), _stream(dev, stream))
+                              float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
     _raise("osdn_chunk_fwd", st)
     return o, S_out
 
@@ -180,7 +213,7 @@ def osdn_check(stream=None, device=None):
 
 def chunk_osdn(q, k, v, beta, precond_retention=None, initial_state=None, initial_d=None, *,
                chunk_size=64, eta=0.003, beta_aware=True, d_min=0.5, d_max=2.0, eps=1e-6,
-               scale=1.0, kt_dtype=None, stream=None):
+               scale=1.0, kt_dtype=None, workspace=None, stream=None):
     """Both phases of the layer forward (the pages' ``chunk_osdn`` signature, Listing 1):
     osdn_precond_scan then osdn_chunk_fwd.  ``scale`` defaults to 1 (o_t = S_t q_t as in the
     equations; pass K ** -0.5 for the listing's query scaling).  Returns (o, S, d)."""
@@ -189,5 +222,5 @@ def chunk_osdn(q, k, v, beta, precond_retention=None, initial_state=None, initia
                               d_max=math.inf if d_max is None else d_max, eps=eps,
                               beta_aware=beta_aware, stream=stream)
     o, S = osdn_chunk_fwd(q, k, kt, v, beta, initial_state, chunk=chunk_size, scale=scale,
-                          stream=stream)
+                          workspace=workspace, stream=stream)
     return o, S, d

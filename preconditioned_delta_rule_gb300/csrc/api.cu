@@ -62,7 +62,7 @@ osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* be
 osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, const void* v,
                            osdn_dtype dtype, const float* beta, const float* S0, void* o,
                            float* S_out, int B, int T, int H, int K, int V, int chunk,
-                           float scale, void* stream) {
+                           float scale, void* workspace, size_t workspace_bytes, void* stream) {
     if (B < 0 || T < 0 || H < 0 || chunk <= 0) return OSDN_ERR_SHAPE;
     if (!head_dim_ok(K) || !head_dim_ok(V)) return (K > 0 && V > 0) ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
     if (chunk != 64) return OSDN_ERR_UNSUPPORTED;
@@ -80,13 +80,23 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
     OSDN_TRY(ptr(o, seq));
     OSDN_TRY(ptr(S0, false));
     OSDN_TRY(ptr(S_out, true));
+    OSDN_TRY(ptr(workspace, false));
     OsdnChunkArgs a{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (seq && dtype != OSDN_F32 && K == 128 && V == 128) {
-        cudaError_t e = osdn_launch_chunk_tc(a, s);
+        cudaError_t e = osdn_launch_chunk_tc(a, workspace, workspace_bytes, s);
         if (e != cudaErrorNotSupported) return from_cuda(e);
     }
     return from_cuda(osdn_launch_chunk_simt(a, s));
+}
+
+size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
+                                      osdn_dtype dtype) {
+    if (B <= 0 || T <= 0 || H <= 0 || chunk <= 0 || T % chunk != 0) return 0;
+    if (K != 128 || V != 128) return 0;
+    OsdnChunkArgs a{};
+    a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.chunk = chunk; a.dtype = dtype;
+    return osdn_chunk_tc_workspace_bytes(a);
 }
 
 osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,

@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "tsolve.cuh"
 
 namespace osdn {
 // Set by any kernel of this library whose bounded device-side wait gave up.
@@ -49,6 +50,7 @@ constexpr int VS = 64;         // rows of S (value dims) per CTA
 constexpr int NTHREADS = 128;
 constexpr uint32_t kMaxPolls = 1u << 22;
 
+namespace fused {
 // shared memory map (byte offsets from a 1024-byte-aligned base)
 constexpr uint32_t KQW_KB = 3 * 8192;                 // per 64-wide key block: K | Q | -W
 constexpr uint32_t ST_KQW = 0;
@@ -58,11 +60,10 @@ constexpr uint32_t STAGE = ST_V + (VS / 64) * 8192;   // 73728
 constexpr uint32_t OFF_LZT = 2 * STAGE;               // L | zeros | T'  (8 KB each)
 constexpr uint32_t OFF_X = OFF_LZT + 3 * 8192;
 constexpr uint32_t OFF_SS = OFF_X + (VS / 64) * 8192;  // fp16 copy of S (MN-major B operand)
-constexpr uint32_t BLK = 16 * 17;                      // one padded 16x16 fp32 block (floats)
 constexpr uint32_t OFF_AM = OFF_SS + (VS / 64) * KD * 128;
-constexpr uint32_t OFF_TM = OFF_AM + 10 * BLK * 4;     // 10 lower-triangular blocks
-constexpr uint32_t OFF_PM = OFF_TM + 10 * BLK * 4;
-constexpr uint32_t OFF_BETA = OFF_PM + 3 * BLK * 4;
+constexpr uint32_t OFF_TM = OFF_AM + 10 * kTile * 4;   // 10 packed lower-triangular tiles
+constexpr uint32_t OFF_PM = OFF_TM + 10 * kTile * 4;
+constexpr uint32_t OFF_BETA = OFF_PM + 3 * kTile * 4;
 constexpr uint32_t OFF_BAR = OFF_BETA + 2 * C * 4;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
@@ -73,8 +74,7 @@ constexpr uint32_t TMA_BYTES = 2 * 2 * 8192 + 2 * 8192 + (VS / 64) * 8192;
 // tensor-memory columns
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_G = 0, COL_W = 64, COL_R = 192, COL_ST = 256;
-
-__device__ __forceinline__ int pb(int i, int j) { return i * (i + 1) / 2 + j; }
+}  // namespace fused
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
@@ -98,6 +98,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmKT, const __grid_constant__ CUtensorMap tmV,
                 const float* __restrict__ beta, const float* S0, TIn* __restrict__ out,
                 float* S_out, int T, int H, int V, float scale) {
+    using namespace fused;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -264,7 +265,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
                     const int bj = j >> 4;
-                    if (bj <= bi) AM[pb(bi, bj) * BLK + r * 17 + (j & 15)] = (j < i) ? bt * g[j] : 0.f;
+                    if (bj <= bi) AM[tile_index(bi, bj) * kTile + r * kTileStride + (j & 15)] = (j < i) ? bt * g[j] : 0.f;
                 }
             } else {
                 const int i = tid - C;
@@ -277,48 +278,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tc::tc_fence_before();
         __syncthreads();
 
-        // 6. T = (I + A)^-1 in fp32: diagonal blocks, then three levels of block products
-        if (tid < C) {
-            const int blk = tid >> 4, c = tid & 15;
-            const float* Ab = AM + pb(blk, blk) * BLK;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; ++m)
-#pragma unroll
-                for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-Ab[i * 17 + m], x[m], x[i]);
-            float* Tb = TM + pb(blk, blk) * BLK;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Tb[i * 17 + c] = x[i];
-        }
-        __syncthreads();
-        for (int lam = 1; lam < 4; ++lam) {
-            const int nb = 4 - lam;
-            for (int e = tid; e < nb * 256; e += NTHREADS) {
-                const int blk = e >> 8, ii = (e >> 4) & 15, jj = e & 15;
-                const int j = blk, i = j + lam;
-                float acc = 0.f;
-                for (int m = j; m < i; ++m) {
-                    const float* Ar = AM + pb(i, m) * BLK + ii * 17;
-                    const float* Tc = TM + pb(m, j) * BLK + jj;
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) acc = fmaf(Ar[kk], Tc[kk * 17], acc);
-                }
-                PM[blk * BLK + ii * 17 + jj] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nb * 256; e += NTHREADS) {
-                const int blk = e >> 8, ii = (e >> 4) & 15, jj = e & 15;
-                const int j = blk, i = j + lam;
-                const float* Tr = TM + pb(i, i) * BLK + ii * 17;
-                const float* Pc = PM + blk * BLK + jj;
-                float acc = 0.f;
-                for (int kk = 0; kk <= ii; ++kk) acc = fmaf(Tr[kk], Pc[kk * 17], acc);
-                TM[pb(i, j) * BLK + ii * 17 + jj] = -acc;
-            }
-            __syncthreads();
-        }
+        // 6. T = (I + A)^-1 in fp32 (blocked forward substitution)
+        ut_inverse_64(AM, TM, PM, tid);
         // T' = T diag(beta) -> fp16 rows of the [0; T'] operand
         {
             const int i = tid >> 1, half = tid & 1, bi = i >> 4, r = i & 15;
@@ -326,7 +287,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
                 const int j = half * 32 + jj, bj = j >> 4;
-                const float tv = (bj <= bi) ? TM[pb(bi, bj) * BLK + r * 17 + (j & 15)] : 0.f;
+                const float tv = (bj <= bi) ? TM[tile_index(bi, bj) * kTile + r * kTileStride + (j & 15)] : 0.f;
                 t[jj] = tv * sbeta[s * C + j];
             }
 #pragma unroll
@@ -480,6 +441,469 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
 }
 
+// =============================================================================================
+// Workspace path: a fully parallel prep kernel (everything that does not depend on S) and a
+// serial chain kernel (everything that does).  Per chunk the workspace holds fp16 images, in
+// the exact 128-byte-swizzled shared-memory layout, of T' (8 KB) and -W (two key blocks, 16 KB).
+// =============================================================================================
+constexpr uint32_t WS_CHUNK = 3 * 8192;
+
+template <int NW>
+__device__ __forceinline__ void convert_bf16_to_f16(unsigned char* base, int tid) {
+    // NW uint4 (8 elements) per thread, contiguous region of NW * 128 * 16 bytes
+#pragma unroll
+    for (int r = 0; r < NW; ++r) {
+        uint4* p = reinterpret_cast<uint4*>(base) + r * NTHREADS + tid;
+        uint4 u = *p;
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = pack_h2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+        *p = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+namespace prep {
+constexpr uint32_t OFF_K = 0;          // K, two 64-wide key blocks
+constexpr uint32_t OFF_KT = 16384;     // K~
+constexpr uint32_t OFF_ZT = 32768;     // zeros | T'   ([0; T'] operand)
+constexpr uint32_t OFF_W = 49152;      // -W, two key blocks
+constexpr uint32_t OFF_AM = 65536;
+constexpr uint32_t OFF_TM = OFF_AM + 10 * kTile * 4;
+constexpr uint32_t OFF_PM = OFF_TM + 10 * kTile * 4;
+constexpr uint32_t OFF_BETA = OFF_PM + 3 * kTile * 4;
+constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;
+constexpr uint32_t SMEM_ALLOC = OFF_BAR + 32 + 1024;
+constexpr uint32_t TMEM_COLS = 128;
+static_assert(2 * SMEM_ALLOC <= 232448, "two prep CTAs per SM");
+}  // namespace prep
+
+// One CTA loops over chunks q = blockIdx.x, blockIdx.x + gridDim.x, ...  (q = (b*H + h)*N + n).
+// Gram A = tril(diag(beta) K K~^T, -1) on the tensor cores, T = (I + A)^-1 in fp32,
+// T' = T diag(beta) and W = T' K (tensor cores) -> fp16 images in the workspace.
+template <typename TIn>
+__global__ void __launch_bounds__(NTHREADS, 2)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKT,
+                  const float* __restrict__ beta, unsigned char* __restrict__ ws, int T, int H, int N,
+                  int total) {
+    using namespace prep;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    float* AM = reinterpret_cast<float*>(sm + OFF_AM);
+    float* TM = reinterpret_cast<float*>(sm + OFF_TM);
+    float* PM = reinterpret_cast<float*>(sm + OFF_PM);
+    float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
+    const uint32_t sbase = tc::smem_u32(sm);
+    const uint32_t bar_tma = sbase + OFF_BAR, bar_mma = sbase + OFF_BAR + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    if (tid == 0) {
+        tc::mbar_init(bar_tma, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::mbar_init_fence();
+        tc::prefetch_tmap(&tmK);
+        tc::prefetch_tmap(&tmKT);
+    }
+    for (int e = tid; e < 8192 / 16; e += NTHREADS)
+        reinterpret_cast<uint4*>(sm + OFF_ZT)[e] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t id_gram = tc::idesc_f16_f32(128, C, false, false);
+    const uint32_t id_w = tc::idesc_f16_f32(128, KD, false, true);
+
+    uint32_t tph = 0, mph = 0;
+    bool aborted = false, tma_pending = false, mma_pending = false;
+    for (int q = blockIdx.x; q < total; q += gridDim.x) {
+        const int bh = q / N, n = q - bh * N, b = bh / H, h = bh - b * H;
+        const int row = b * T + n * C;
+        if (tid == 0) {
+            tc::mbar_expect_tx(bar_tma, 4 * 8192);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                tc::tma_load_3d(sbase + OFF_K + kb * 8192, &tmK, bar_tma, kb * 64, h, row);
+                tc::tma_load_3d(sbase + OFF_KT + kb * 8192, &tmKT, bar_tma, kb * 64, h, row);
+            }
+        }
+        tma_pending = true;
+        if (tid < C) sbeta[tid] = beta[(static_cast<size_t>(row) + tid) * H + h];
+        {
+            const bool ok = tc::mbar_wait(bar_tma, tph, kMaxPolls);
+            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            tph ^= 1u;
+            tma_pending = false;
+        }
+        if constexpr (!std::is_same<TIn, __half>::value) convert_bf16_to_f16<16>(sm + OFF_K, tid);
+        tc::fence_proxy_async();
+        __syncthreads();
+
+        // Gram K K~^T (lanes 0-63; lanes 64-127 read the next 64 rows of smem and are unused)
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < KD / 16; ++st) {
+                const uint64_t a = tc::sdesc_sw128(sbase + OFF_K + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
+                const uint64_t bd = tc::sdesc_sw128(sbase + OFF_KT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
+                tc::mma_f16(tbase, a, bd, id_gram, st > 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        {
+            const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
+            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            mph ^= 1u;
+            mma_pending = false;
+            tc::tc_fence_after();
+        }
+        if (tid < C) {
+            float g[64];
+            tc::tmem_ld32(tbase + lane_base, *reinterpret_cast<float(*)[32]>(g));
+            tc::tmem_ld32(tbase + lane_base + 32, *reinterpret_cast<float(*)[32]>(g + 32));
+            tc::tmem_ld_wait();
+            const int i = tid, bi = i >> 4, r = i & 15;
+            const float bt = sbeta[i];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const int bj = j >> 4;
+                if (bj <= bi) AM[tile_index(bi, bj) * kTile + r * kTileStride + (j & 15)] = (j < i) ? bt * g[j] : 0.f;
+            }
+        }
+        tc::tc_fence_before();
+        __syncthreads();
+        ut_inverse_64(AM, TM, PM, tid);
+        // the T' and -W images of the previous chunk must have been read by their bulk stores
+        if (tid == 0) tc::bulk_wait_read_all();
+        __syncthreads();
+        {
+            const int i = tid >> 1, half = tid & 1, bi = i >> 4, r = i & 15;
+            float t[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = half * 32 + jj, bj = j >> 4;
+                const float tv = (bj <= bi) ? TM[tile_index(bi, bj) * kTile + r * kTileStride + (j & 15)] : 0.f;
+                t[jj] = tv * sbeta[j];
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) st_row_chunk(sm + OFF_ZT + 8192, i, half * 4 + c, t + 8 * c);
+        }
+        tc::fence_proxy_async();
+        __syncthreads();
+
+        // W = [0; T'] K  (lanes 64-127, 128 columns)
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st) {
+                const uint64_t a = tc::sdesc_sw128(sbase + OFF_ZT + st * 32, 16, 1024);
+                const uint64_t bk = tc::sdesc_sw128(sbase + OFF_K + st * 2048, 8192, 1024);
+                tc::mma_f16(tbase, a, bk, id_w, st > 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        {
+            const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
+            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            mph ^= 1u;
+            mma_pending = false;
+            tc::tc_fence_after();
+        }
+        if (tid >= C) {
+            const int c = tid - C;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float w[32];
+                tc::tmem_ld32(tbase + lane_base + q4 * 32, w);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = -w[j];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    st_row_chunk(sm + OFF_W + (q4 >> 1) * 8192, c, (q4 & 1) * 4 + cc, w + 8 * cc);
+            }
+        }
+        tc::fence_proxy_async();
+        tc::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            unsigned char* dst = ws + static_cast<size_t>(q) * WS_CHUNK;
+            tc::bulk_store(dst, sbase + OFF_ZT + 8192, 8192);
+            tc::bulk_store(dst + 8192, sbase + OFF_W, 16384);
+            tc::bulk_commit();
+        }
+    }
+    if (aborted) {
+        if (tid == 0) atomicExch(&g_timeout_flag, 1u);
+        if (tma_pending) tc::mbar_wait(bar_tma, tph, kMaxPolls >> 4);
+        if (mma_pending) tc::mbar_wait(bar_mma, mph, kMaxPolls >> 4);
+    }
+    if (tid == 0) tc::bulk_wait_all();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+}
+
+namespace chain {
+constexpr uint32_t ST_QW = 0;                          // per key block: Q | -W  (2 x 16 KB)
+constexpr uint32_t ST_KT = 32768;                      // K~
+constexpr uint32_t ST_V = 49152;                       // V slice
+constexpr uint32_t ST_ZT = ST_V + (VS / 64) * 8192;    // zeros | T'
+constexpr uint32_t STAGE = ST_ZT + 16384;
+constexpr uint32_t OFF_LZ = 2 * STAGE;                 // L | zeros  ([L; 0] operand)
+constexpr uint32_t OFF_X = OFF_LZ + 16384;
+constexpr uint32_t OFF_SS = OFF_X + (VS / 64) * 8192;
+constexpr uint32_t OFF_BAR = OFF_SS + (VS / 64) * KD * 128;
+constexpr uint32_t SMEM_ALLOC = OFF_BAR + 64 + 1024;
+constexpr uint32_t LOAD_BYTES = 2 * 8192 + 2 * 8192 + (VS / 64) * 8192 + 2 * 8192 + 8192;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t COL_R = 0, COL_L = VS, COL_ST = VS + 64;
+static_assert(SMEM_ALLOC <= 232448, "chain shared memory");
+static_assert(STAGE % 1024 == 0 && OFF_X % 1024 == 0 && OFF_SS % 1024 == 0, "swizzle atoms");
+}  // namespace chain
+
+// One CTA per (batch, head, VS rows of S), serial over chunks.  Per chunk: U = T'V,
+// X = U - W S^T and Q S^T ([Q; -W] S^T), L = tril(Q K~^T); then O = Q S^T + L X and
+// S^T += K~^T X.  T' and -W come from the workspace by bulk copy; Q, K~, V by TMA.
+template <typename TIn>
+__global__ void __launch_bounds__(NTHREADS, 1)
+chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKT,
+                   const __grid_constant__ CUtensorMap tmV, const unsigned char* __restrict__ ws,
+                   const float* S0, TIn* __restrict__ out, float* S_out, int T, int H, int V, int N,
+                   float scale) {
+    using namespace chain;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    const int v0 = blockIdx.y * VS;
+    const uint32_t sbase = tc::smem_u32(sm);
+    const uint32_t bar_tma0 = sbase + OFF_BAR, bar_mma = sbase + OFF_BAR + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 24);
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    if (tid == 0) {
+        tc::mbar_init(bar_tma0, 1);
+        tc::mbar_init(bar_tma0 + 8, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::mbar_init_fence();
+        tc::prefetch_tmap(&tmQ);
+        tc::prefetch_tmap(&tmKT);
+        tc::prefetch_tmap(&tmV);
+    }
+    for (int e = tid; e < 8192 / 16; e += NTHREADS) {
+        reinterpret_cast<uint4*>(sm + ST_ZT)[e] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(sm + STAGE + ST_ZT)[e] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(sm + OFF_LZ + 8192)[e] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+
+    auto issue = [&](int m, int s) {
+        const uint32_t bar = bar_tma0 + 8 * s;
+        const uint32_t st = sbase + s * STAGE;
+        const int row = b * T + m * C;
+        const unsigned char* wsc = ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK;
+        tc::mbar_expect_tx(bar, LOAD_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tc::tma_load_3d(st + ST_QW + kb * 16384, &tmQ, bar, kb * 64, h, row);
+            tc::bulk_load(st + ST_QW + kb * 16384 + 8192, wsc + 8192 + kb * 8192, 8192, bar);
+            tc::tma_load_3d(st + ST_KT + kb * 8192, &tmKT, bar, kb * 64, h, row);
+        }
+#pragma unroll
+        for (int vb = 0; vb < VS / 64; ++vb) tc::tma_load_3d(st + ST_V + vb * 8192, &tmV, bar, v0 + vb * 64, h, row);
+        tc::bulk_load(st + ST_ZT + 8192, wsc, 8192, bar);
+    };
+    if (tid == 0 && N > 0) issue(0, 0);
+
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    {  // S0 slice -> S^T in tensor memory (lane = key coordinate) and its fp16 operand copy
+        const int k = tid;
+        float sv[32];
+#pragma unroll
+        for (int half = 0; half < VS / 32; ++half) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                sv[j] = S0 ? S0[(static_cast<size_t>(bh) * V + v0 + half * 32 + j) * KD + k] : 0.f;
+            tc::tmem_st32(tbase + lane_base + COL_ST + half * 32, sv);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                st_row_chunk(sm + OFF_SS + ((half * 32) / 64) * (KD * 128), k, ((half * 32) % 64) / 8 + c, sv + 8 * c);
+        }
+        tc::tmem_st_wait();
+    }
+    tc::fence_proxy_async();
+    tc::tc_fence_before();
+    __syncthreads();
+
+    const uint32_t id_u = tc::idesc_f16_f32(128, VS, false, true);
+    const uint32_t id_l = tc::idesc_f16_f32(128, C, false, false);
+    const uint32_t id_state = tc::idesc_f16_f32(128, VS, true, true);
+    uint32_t mph = 0;
+    bool aborted = false, mma_pending = false;
+    bool tma_pending[2] = {N > 0, false};
+    int tma_chunk[2] = {0, 0};
+
+    for (int n = 0; n < N; ++n) {
+        const int s = n & 1;
+        unsigned char* stg = sm + s * STAGE;
+        const uint32_t stg_a = sbase + s * STAGE;
+        if (n + 1 < N) {
+            if (tid == 0) issue(n + 1, s ^ 1);
+            tma_pending[s ^ 1] = true;
+            tma_chunk[s ^ 1] = n + 1;
+        }
+        {
+            const bool ok = tc::mbar_wait(bar_tma0 + 8 * s, (n >> 1) & 1, kMaxPolls);
+            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            tma_pending[s] = false;
+        }
+        if constexpr (!std::is_same<TIn, __half>::value) {
+            convert_bf16_to_f16<4>(stg + ST_QW, tid);
+            convert_bf16_to_f16<4>(stg + ST_QW + 16384, tid);
+            convert_bf16_to_f16<8>(stg + ST_KT, tid);
+            convert_bf16_to_f16<(VS / 64) * 4>(stg + ST_V, tid);
+        }
+        tc::fence_proxy_async();
+        __syncthreads();
+
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st) {  // U = [0; T'] V  (lanes 64-127)
+                const uint64_t a = tc::sdesc_sw128(stg_a + ST_ZT + st * 32, 16, 1024);
+                const uint64_t bv = tc::sdesc_sw128(stg_a + ST_V + st * 2048, 8192, 1024);
+                tc::mma_f16(tbase + COL_R, a, bv, id_u, st > 0);
+            }
+#pragma unroll
+            for (int st = 0; st < KD / 16; ++st) {  // += [Q; -W] S^T ; L = [Q; -W] K~^T
+                const uint64_t a = tc::sdesc_sw128(stg_a + ST_QW + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
+                const uint64_t bs = tc::sdesc_sw128(sbase + OFF_SS + st * 2048, KD * 128, 1024);
+                tc::mma_f16(tbase + COL_R, a, bs, id_u, 1);
+                const uint64_t bk = tc::sdesc_sw128(stg_a + ST_KT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
+                tc::mma_f16(tbase + COL_L, a, bk, id_l, st > 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        {
+            const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
+            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            mph ^= 1u;
+            mma_pending = false;
+            tc::tc_fence_after();
+        }
+        if (tid >= C) {  // X rows (lanes 64-127)
+            const int c = tid - C;
+#pragma unroll
+            for (int q2 = 0; q2 < VS / 32; ++q2) {
+                float x[32];
+                tc::tmem_ld32(tbase + lane_base + COL_R + q2 * 32, x);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    st_row_chunk(sm + OFF_X + ((q2 * 32) / 64) * 8192, c, ((q2 * 32) % 64) / 8 + cc, x + 8 * cc);
+            }
+        } else {  // L rows: tril(Q K~^T, 0) (lanes 0-63)
+            const int i = tid;
+            float g[64];
+            tc::tmem_ld32(tbase + lane_base + COL_L, *reinterpret_cast<float(*)[32]>(g));
+            tc::tmem_ld32(tbase + lane_base + COL_L + 32, *reinterpret_cast<float(*)[32]>(g + 32));
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 64; ++j) g[j] = (j <= i) ? g[j] : 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) st_row_chunk(sm + OFF_LZ, i, c, g + 8 * c);
+        }
+        tc::fence_proxy_async();
+        tc::tc_fence_before();
+        __syncthreads();
+
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st) {
+                const uint64_t bx = tc::sdesc_sw128(sbase + OFF_X + st * 2048, 8192, 1024);
+                const uint64_t al = tc::sdesc_sw128(sbase + OFF_LZ + st * 32, 16, 1024);
+                tc::mma_f16(tbase + COL_R, al, bx, id_u, 1);
+                const uint64_t ak = tc::sdesc_sw128(stg_a + ST_KT + st * 2048, 8192, 1024);
+                tc::mma_f16(tbase + COL_ST, ak, bx, id_state, 1);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        {
+            const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
+            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            mph ^= 1u;
+            mma_pending = false;
+            tc::tc_fence_after();
+        }
+        if (tid < C) {
+            TIn* orow = out + ((static_cast<size_t>(b) * T + n * C + tid) * H + h) * V + v0;
+#pragma unroll
+            for (int q2 = 0; q2 < VS / 32; ++q2) {
+                float o[32];
+                tc::tmem_ld32(tbase + lane_base + COL_R + q2 * 32, o);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float ov[4] = {scale * o[j], scale * o[j + 1], scale * o[j + 2], scale * o[j + 3]};
+                    VecIO<TIn, 4>::store(orow + q2 * 32 + j, ov);
+                }
+            }
+        }
+        {
+            const int k = tid;
+#pragma unroll
+            for (int q2 = 0; q2 < VS / 32; ++q2) {
+                float sv[32];
+                tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, sv);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    st_row_chunk(sm + OFF_SS + ((q2 * 32) / 64) * (KD * 128), k, ((q2 * 32) % 64) / 8 + cc, sv + 8 * cc);
+            }
+        }
+        tc::fence_proxy_async();
+        tc::tc_fence_before();
+        __syncthreads();
+    }
+
+    if (aborted) {
+        if (tid == 0) atomicExch(&g_timeout_flag, 1u);
+        for (int s = 0; s < 2; ++s)
+            if (tma_pending[s]) tc::mbar_wait(bar_tma0 + 8 * s, (tma_chunk[s] >> 1) & 1, kMaxPolls >> 4);
+        if (mma_pending) tc::mbar_wait(bar_mma, mph, kMaxPolls >> 4);
+    } else {
+        const int k = tid;
+#pragma unroll
+        for (int q2 = 0; q2 < VS / 32; ++q2) {
+            float sv[32];
+            tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, sv);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) S_out[(static_cast<size_t>(bh) * V + v0 + q2 * 32 + j) * KD + k] = sv[j];
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -508,8 +932,25 @@ bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int inner
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int num_sms() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 148;
+    });
+    return n;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, uint32_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
 template <typename TIn>
-cudaError_t launch_tc(const OsdnChunkArgs& a, cudaStream_t s) {
+cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
     const CUtensorMapDataType dt = std::is_same<TIn, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const long long rows = static_cast<long long>(a.B) * a.T;
@@ -517,29 +958,54 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, cudaStream_t s) {
     if (!make_map(&mq, a.q, dt, a.K, a.H, rows) || !make_map(&mk, a.k, dt, a.K, a.H, rows) ||
         !make_map(&mkt, a.k_tilde, dt, a.K, a.H, rows) || !make_map(&mv, a.v, dt, a.V, a.H, rows))
         return cudaErrorNotSupported;
-    static std::once_flag attr_once[2];
-    cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once[std::is_same<TIn, __half>::value ? 1 : 0], [&] {
-        attr_err = cudaFuncSetAttribute(chunk_tc_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SMEM_ALLOC);
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        cudaError_t e1 = set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC);
+        cudaError_t e2 = set_smem(chunk_prep_kernel<TIn>, prep::SMEM_ALLOC);
+        cudaError_t e3 = set_smem(chunk_chain_kernel<TIn>, chain::SMEM_ALLOC);
+        attr_err = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS)), block(NTHREADS);
-    chunk_tc_kernel<TIn><<<grid, block, SMEM_ALLOC, s>>>(mq, mk, mkt, mv, a.beta, a.S0,
-                                                         static_cast<TIn*>(a.o), a.S_out, a.T, a.H,
-                                                         a.V, a.scale);
+    const int N = a.T / C;
+    const size_t need = static_cast<size_t>(a.B) * a.H * N * WS_CHUNK;
+    dim3 block(NTHREADS);
+    if (ws != nullptr && ws_bytes >= need) {
+        const int total = a.B * a.H * N;
+        dim3 gp(static_cast<unsigned>(total < 2 * num_sms() ? total : 2 * num_sms()));
+        chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mk, mkt, a.beta, static_cast<unsigned char*>(ws),
+                                                                  a.T, a.H, N, total);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        dim3 gc(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
+        chunk_chain_kernel<TIn><<<gc, block, chain::SMEM_ALLOC, s>>>(
+            mq, mkt, mv, static_cast<const unsigned char*>(ws), a.S0, static_cast<TIn*>(a.o), a.S_out, a.T, a.H, a.V,
+            N, a.scale);
+        return cudaGetLastError();
+    }
+    dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
+    chunk_tc_kernel<TIn><<<grid, block, fused::SMEM_ALLOC, s>>>(mq, mk, mkt, mv, a.beta, a.S0, static_cast<TIn*>(a.o),
+                                                        a.S_out, a.T, a.H, a.V, a.scale);
     return cudaGetLastError();
+}
+
+bool tc_covers(const OsdnChunkArgs& a) {
+    return a.K == KD && a.V % VS == 0 && a.chunk == C && a.T > 0 && a.T % C == 0 &&
+           (a.dtype == OSDN_BF16 || a.dtype == OSDN_F16);
 }
 
 }  // namespace
 }  // namespace osdn
 
-cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, cudaStream_t s) {
-    if (a.K != osdn::KD || a.V % osdn::VS != 0 || a.chunk != osdn::C || a.T <= 0 || a.T % osdn::C)
-        return cudaErrorNotSupported;
-    if (a.dtype == OSDN_BF16) return osdn::launch_tc<__nv_bfloat16>(a, s);
-    if (a.dtype == OSDN_F16) return osdn::launch_tc<__half>(a, s);
-    return cudaErrorNotSupported;
+size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a) {
+    if (!osdn::tc_covers(a)) return 0;
+    return static_cast<size_t>(a.B) * a.H * (a.T / osdn::C) * osdn::WS_CHUNK;
+}
+
+cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (!osdn::tc_covers(a)) return cudaErrorNotSupported;
+    if (a.dtype == OSDN_BF16) return osdn::launch_tc<__nv_bfloat16>(a, ws, ws_bytes, s);
+    return osdn::launch_tc<__half>(a, ws, ws_bytes, s);
 }
 
 cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s) {

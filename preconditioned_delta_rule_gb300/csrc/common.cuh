@@ -101,8 +101,11 @@ struct OsdnDecodeArgs {
 
 cudaError_t osdn_launch_scan(const OsdnScanArgs& a, cudaStream_t s);
 cudaError_t osdn_launch_chunk_simt(const OsdnChunkArgs& a, cudaStream_t s);
-// Returns cudaErrorNotSupported when the tensor-core kernel does not cover the arguments.
-cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, cudaStream_t s);
+// Tensor-core path.  With a workspace of at least osdn_chunk_tc_workspace_bytes(a) bytes it runs
+// the parallel prep kernel and the serial chain kernel; otherwise one fused kernel.  Returns
+// cudaErrorNotSupported when the tensor-core kernels do not cover the arguments.
+cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a);
 cudaError_t osdn_launch_decode(const OsdnDecodeArgs& a, cudaStream_t s);
 // Reads and clears the device-side timeout word (synchronous on the given stream).
 cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s);

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from preconditioned_delta_rule_gb300 import osdn_chunk_fwd
+from preconditioned_delta_rule_gb300 import osdn_chunk_fwd, osdn_chunk_fwd_workspace_bytes
 from preconditioned_delta_rule_gb300 import workloads as W
 from tests._parity import assert_maxabs, np64, to_dev
 
@@ -22,14 +22,14 @@ def write_keys(inp, w, dtype):
     return torch.from_numpy(kt).to(torch.float32).to(dtype)
 
 
-def check(inp, w, kt, S0=None, scale=1.0, dtype=None, alias=False, heads=None):
+def check(inp, w, kt, S0=None, scale=1.0, dtype=None, alias=False, workspace=None):
     dtype = dtype or inp["k"].dtype
     cast = lambda t: t.to(dtype)
     q, k, v = cast(inp["q"]), cast(inp["k"]), cast(inp["v"])
     dev = dict(q=q.cuda(), k=k.cuda(), kt=kt.to(dtype).cuda(), v=v.cuda(), beta=inp["beta"].cuda())
     S0d = None if S0 is None else S0.clone().cuda()
     o, S = osdn_chunk_fwd(dev["q"], dev["k"], dev["kt"], dev["v"], dev["beta"], S0d,
-                          S_out=S0d if alias else None, scale=scale)
+                          S_out=S0d if alias else None, scale=scale, workspace=workspace)
     torch.cuda.synchronize()
     o_ref, S_ref = oracle.delta_phase2(q, k, kt.to(dtype), v, inp["beta"], S0, scale=scale)
     tol = TOL[dtype]
@@ -44,12 +44,33 @@ def test_chunk_tiny_f32():
     check(inp, w, write_keys(inp, w, torch.float32))
 
 
+@pytest.mark.parametrize("workspace", [None, False], ids=["two_kernel", "fused"])
 @pytest.mark.parametrize("name", ["layer_340m", "layer_1p3b_apf", "longctx_unit"])
-def test_chunk_workloads_full_size(name):
+def test_chunk_workloads_full_size(name, workspace):
     w = W.WORKLOADS[name]
     inp = W.make_prefill(w)
-    eo, es = check(inp, w, write_keys(inp, w, torch.bfloat16))
-    print(f"{name}: max|o err| {eo:.3e} max|S err| {es:.3e}")
+    eo, es = check(inp, w, write_keys(inp, w, torch.bfloat16), workspace=workspace)
+    print(f"{name} ({'fused' if workspace is False else 'two-kernel'}): "
+          f"max|o err| {eo:.3e} max|S err| {es:.3e}")
+
+
+def test_chunk_paths_agree_and_workspace_reuse():
+    """The two tensor-core paths compute the same rounding sequence; a reused (dirty) workspace
+    and an explicitly passed one give identical results."""
+    w = W.WORKLOADS["layer_1p3b_apf"]
+    inp = W.make_prefill(w, B=2, H=3, T=512, seed=13)
+    kt = write_keys(inp, w, torch.bfloat16).cuda()
+    d = to_dev(inp)
+    S0 = torch.randn(2, 3, 128, 128, generator=torch.Generator().manual_seed(7)).cuda() * 0.1
+    o1, S1 = osdn_chunk_fwd(d["q"], d["k"], kt, d["v"], d["beta"], S0, workspace=False)
+    need = osdn_chunk_fwd_workspace_bytes(2, 512, 3, 128, 128)
+    assert need == 2 * 3 * 8 * 24576
+    ws = torch.full((need + 4096,), 0xAB, dtype=torch.uint8, device="cuda")
+    o2, S2 = osdn_chunk_fwd(d["q"], d["k"], kt, d["v"], d["beta"], S0, workspace=ws)
+    o3, S3 = osdn_chunk_fwd(d["q"], d["k"], kt, d["v"], d["beta"], S0, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o3) and torch.equal(S2, S3)
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
 
 
 @pytest.mark.parametrize("T", [64, 128, 448])

@@ -62,7 +62,7 @@ def chunk(L, **kw):
     a.update(kw)
     return L.osdn_chunk_fwd(a["q"], a["k"], a["kt"], a["v"], a["dt"], a["beta"], a["S0"], a["o"],
                             a["Sout"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"], a["scale"],
-                            None)
+                            a.get("ws"), a.get("wsb", 0), None)
 
 
 def decode(L, **kw):
@@ -92,7 +92,7 @@ def test_scan_validation(L, kw, want):
     (dict(v=A + 8), ALIGN), (dict(S0=A + 4), ALIGN),
     (dict(T=100), SHAPE), (dict(C=0), SHAPE), (dict(C=32), UNSUP), (dict(K=256), UNSUP),
     (dict(V=48), UNSUP), (dict(dt=5), DTYPE), (dict(scale=math.inf), ARG),
-    (dict(B=0), OK),
+    (dict(ws=A + 8, wsb=1 << 20), ALIGN), (dict(B=0), OK),
 ])
 def test_chunk_validation(L, kw, want):
     assert chunk(L, **kw) == want
@@ -112,3 +112,12 @@ def test_binding_rejects_host_tensors(L):
     beta = torch.zeros(1, 64, 1)
     with pytest.raises(ValueError, match="CUDA tensor"):
         binding.osdn_precond_scan(k, beta)
+
+
+def test_workspace_size_query(L):
+    f = L.osdn_chunk_fwd_workspace_bytes
+    assert f(8, 2048, 8, 128, 128, 64, 1) == 8 * 8 * 32 * 24576
+    assert f(1, 64, 1, 128, 128, 64, 2) == 24576
+    assert f(1, 64, 1, 64, 64, 64, 1) == 0      # shapes the tensor-core path does not cover
+    assert f(1, 64, 1, 128, 128, 64, 0) == 0    # fp32 inputs use the CUDA-core kernel
+    assert f(1, 100, 1, 128, 128, 64, 1) == 0   # T not a multiple of the chunk
