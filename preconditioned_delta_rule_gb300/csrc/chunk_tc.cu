@@ -1008,8 +1008,13 @@ cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_byt
     return osdn::launch_tc<__half>(a, ws, ws_bytes, s);
 }
 
+cudaError_t osdn_scan_block_read_and_clear_timeout(unsigned int* flag);
+
 cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s) {
     cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    unsigned int scan_flag = 0;
+    e = osdn_scan_block_read_and_clear_timeout(&scan_flag);
     if (e != cudaSuccess) return e;
     e = cudaMemcpyFromSymbol(flag, osdn::g_timeout_flag, sizeof(unsigned int));
     if (e != cudaSuccess) return e;
@@ -1017,5 +1022,6 @@ cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s) {
         const unsigned int zero = 0;
         e = cudaMemcpyToSymbol(osdn::g_timeout_flag, &zero, sizeof(unsigned int));
     }
+    *flag |= scan_flag;
     return e;
 }

@@ -162,8 +162,14 @@ cudaError_t launch_in(const OsdnScanArgs& a, cudaStream_t s) {
 }  // namespace
 }  // namespace osdn
 
+cudaError_t osdn_launch_scan_block(const OsdnScanArgs& a, cudaStream_t s);
+
 cudaError_t osdn_launch_scan(const OsdnScanArgs& a, cudaStream_t s) {
-    if (a.K == 128) return osdn::launch_in<128>(a, s);
+    if (a.K == 128) {
+        cudaError_t e = osdn_launch_scan_block(a, s);  // 16-bit keys: blocked tensor-core scan
+        if (e != cudaErrorNotSupported) return e;
+        return osdn::launch_in<128>(a, s);
+    }
     if (a.K == 64) return osdn::launch_in<64>(a, s);
     return cudaErrorInvalidValue;
 }
