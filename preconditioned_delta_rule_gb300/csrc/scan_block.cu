@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a) {
                 float d = F[F_DST + q * KD + u];
                 TOut* out = ktg + (row0 + static_cast<size_t>(t0) * H) * KD + u;
                 const size_t stride = static_cast<size_t>(H) * KD;
+#pragma unroll 4
                 for (int j = 0; j < jb; ++j) {
                     const float kj = ld_key<TIn>(kt, j, u);
                     out[j * stride] = from_f32<TOut>(d * kj);
@@ -528,9 +529,10 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a) {
                                 }
                                 const float accs = (acc[0] + acc[1]) + (acc[2] + acc[3]);
                                 const float gn = gam[j] * (1.f - bpv[j] * (rho(j) * (F[F_CF + j] + accs) + F[F_CP + j]));
-                                // stop once no g moves by more than about an ulp: each sweep shrinks
-                                // the remaining error by the coupling, |gamma b M| ~ 1e-3
-                                changed = fabsf(gn - gj) > 1.2e-7f * fabsf(gn);
+                                // stop once no g moves by more than a few ulps: each sweep shrinks
+                                // the remaining error by the coupling |gamma b M| (~1e-3 here), so
+                                // what is left is below rounding; a 1-ulp test can cycle on noise
+                                changed = fabsf(gn - gj) > 5e-7f * fabsf(gn) + 1e-30f;
                                 gj = gn;
                             }
                             const bool any = wg_count(1, changed) != 0;
@@ -549,12 +551,18 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a) {
                 float inc = 0.f;  // sum_{l=p}^{63} h_l s_li  (free coordinates)
                 int viol = J;     // first token whose update leaves the assumed regime
                 if (status == 0) {
-                    float bnd = 0.f;
-                    for (int l = p; l < J; ++l) {
-                        const float hs = F[F_H + l] * sf[l * SROW + i];
-                        inc += hs;
-                        bnd += fabsf(hs);
+                    float bnd = 0.f, inc1 = 0.f, bnd1 = 0.f;
+#pragma unroll 8
+                    for (int l = 0; l < J; l += 2) {  // h_l = 0 for l < p
+                        const float hs0 = F[F_H + l] * sf[l * SROW + i];
+                        const float hs1 = F[F_H + l + 1] * sf[(l + 1) * SROW + i];
+                        inc += hs0;
+                        bnd += fabsf(hs0);
+                        inc1 += hs1;
+                        bnd1 += fabsf(hs1);
                     }
+                    inc += inc1;
+                    bnd += bnd1;
                     bnd = bnd * 1.0001f + fabsf(d_lo);  // margin for the fp32 sums
                     // retention gates lie in (0, 1]: rho_j stays within [rho_64, 1]
                     const float rmin = HAS_R ? F[F_RHO + J] : 1.f;
