@@ -35,7 +35,8 @@
  *     non-finite scalar, d_min > d_max), OSDN_ERR_SHAPE (sizes out of range, T not a multiple of
  *     the chunk), OSDN_ERR_DTYPE, OSDN_ERR_ALIGN, OSDN_ERR_UNSUPPORTED (valid but not built, e.g.
  *     K = 96), OSDN_ERR_CUDA (a launch failed; the CUDA error is left for the caller to query),
- *     OSDN_ERR_TIMEOUT (a device-side bounded wait gave up; reported by osdn_check()).
+ *     OSDN_ERR_TIMEOUT (a device-side bounded wait gave up; reported by osdn_check()),
+ *     OSDN_ERR_CAPACITY (the request needs more scratch than osdn_chunk_fwd_static_ws has).
  *   - Sizes are `int`; B*T*H*max(K,V) must stay below 2^31 elements per tensor.
  */
 #ifndef OSDN_H
@@ -55,7 +56,8 @@ typedef enum {
     OSDN_ERR_ALIGN = 4,
     OSDN_ERR_UNSUPPORTED = 5,
     OSDN_ERR_CUDA = 6,
-    OSDN_ERR_TIMEOUT = 7
+    OSDN_ERR_TIMEOUT = 7,
+    OSDN_ERR_CAPACITY = 8
 } osdn_status;
 
 typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1, OSDN_F16 = 2 } osdn_dtype;
@@ -111,6 +113,30 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
  * and chunk 64 it is B * H * (T / 64) * 24576 bytes (24 KiB per chunk of each head). */
 size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
                                       osdn_dtype dtype);
+
+/*
+ * osdn_chunk_fwd for callers that cannot allocate device memory when they call -- for example an
+ * engine that reserves all GPU memory in one plan at start-up and allocates nothing afterwards,
+ * or code that cannot accept an allocator call (its latency, its implicit synchronisation, its
+ * possible failure) in the middle of a step.  No counterpart in the paper: this is a property of
+ * this library's interface, not of the method.
+ *   Same arguments and results as osdn_chunk_fwd without the workspace: the scratch of the
+ *   two-kernel tensor-core path comes from a fixed 24 MiB array in the library's own device
+ *   memory (file-scope; every GPU that loads the library holds it until the process exits).
+ *   Capacity: osdn_chunk_fwd_workspace_bytes(...) <= 24 MiB, i.e. B * H * (T / 64) <= 1024 chunks;
+ *   larger requests return OSDN_ERR_CAPACITY before any launch.  Calls that need no scratch (fp32
+ *   inputs, other head sizes) run the CUDA-core kernel as osdn_chunk_fwd does.
+ *   Neither the library nor this call allocates (no cudaMalloc/cudaFree or allocating routine).
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
+ *   caches it; make that first call before any stream capture.
+ *   All calls share the one array and nothing in it needs to start at zero (each call writes all
+ *   the scratch it reads), but calls whose work overlaps on the GPU -- on different streams, or
+ *   from different threads -- race on it: serialise them.
+ */
+osdn_status osdn_chunk_fwd_static_ws(const void* q, const void* k, const void* k_tilde,
+                                     const void* v, osdn_dtype dtype, const float* beta,
+                                     const float* S0, void* o, float* S_out, int B, int T, int H,
+                                     int K, int V, int chunk, float scale, void* stream);
 
 /*
  * One decode token for every (batch, head), in place (recurrent form of both phases):

@@ -20,7 +20,7 @@ LIB_PATH = _PKG / "libosdn.so"
 OSDN_F32, OSDN_BF16, OSDN_F16 = 0, 1, 2
 _DTYPE_CODE = {torch.float32: OSDN_F32, torch.bfloat16: OSDN_BF16, torch.float16: OSDN_F16}
 _STATUS = ["OSDN_OK", "OSDN_ERR_ARG", "OSDN_ERR_SHAPE", "OSDN_ERR_DTYPE", "OSDN_ERR_ALIGN",
-           "OSDN_ERR_UNSUPPORTED", "OSDN_ERR_CUDA", "OSDN_ERR_TIMEOUT"]
+           "OSDN_ERR_UNSUPPORTED", "OSDN_ERR_CUDA", "OSDN_ERR_TIMEOUT", "OSDN_ERR_CAPACITY"]
 
 _lib = None
 
@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
     L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp, sz, vp]
     L.osdn_chunk_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.osdn_chunk_fwd_workspace_bytes.restype = sz
+    L.osdn_chunk_fwd_static_ws.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp]
+    L.osdn_chunk_fwd_static_ws.restype = ctypes.c_int
     L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
     L.osdn_check.argtypes = [vp]
     for fn in ("osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step", "osdn_check"):

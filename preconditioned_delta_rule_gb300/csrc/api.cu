@@ -142,6 +142,7 @@ const char* osdn_status_string(int status) {
         case OSDN_ERR_UNSUPPORTED: return "OSDN_ERR_UNSUPPORTED: valid arguments not covered by a built kernel";
         case OSDN_ERR_CUDA: return "OSDN_ERR_CUDA: a CUDA call or launch failed";
         case OSDN_ERR_TIMEOUT: return "OSDN_ERR_TIMEOUT: a device-side bounded wait gave up";
+        case OSDN_ERR_CAPACITY: return "OSDN_ERR_CAPACITY: the request needs more scratch than the fixed no-allocation array holds";
     }
     return "OSDN: unknown status";
 }
