@@ -285,6 +285,10 @@ def run_ours(args, w):
     value = tokens / total_s
     ms_per_step = 1e3 * total_s / n
 
+    # kernels per step: the scan is one kernel plus the parallel emission kernel when it has a
+    # workspace; the chunk forward is a prep and a chain kernel when it has one, else one kernel
+    launches_per_step = ((2 if binding.osdn_precond_scan_workspace_bytes(B, T, H, K, g["k"].dtype) else 1)
+                         + (2 if binding.osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, w.chunk, g["k"].dtype) else 1))
     scan_b, chunk_b = layer_bytes(w)
     scan_avg, chunk_avg = statistics.mean(scan_ms), statistics.mean(chunk_ms)
     dom = ("osdn_chunk_fwd", chunk_b, chunk_avg) if chunk_avg >= scan_avg else ("osdn_precond_scan", scan_b, scan_avg)
@@ -318,7 +322,7 @@ def run_ours(args, w):
                        "chunk": w.chunk, "eta": w.eta, "box": [w.d_min, w.d_max],
                        "l2": "flushed between steps (256 MiB write outside the timed events)"},
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "decode": decode, "gpu_launches": 2 * n, "clocks": clk.summary(),
+            "decode": decode, "gpu_launches": launches_per_step * n, "clocks": clk.summary(),
             "wall_s_timed_region": wall,
         }
         print(json.dumps(line), flush=True)

@@ -73,13 +73,26 @@ typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1, OSDN_F16 = 2 } osdn_dtype;
  *   eta >= 0; d_min <= d_max (use -INFINITY/+INFINITY to switch the box off); eps > 0 floors
  *   the SQUARED key norm; beta_aware = 1 feeds beta_t into the step (Listing 1 default),
  *   0 uses 1 there (the memory write keeps beta either way).
+ *   workspace, workspace_bytes
+ *            optional caller-owned device scratch (16-byte aligned).  When it holds at least
+ *            osdn_precond_scan_workspace_bytes(...) bytes, the blocked scan (bf16/f16 keys,
+ *            K = 128) only fixes the step sizes and block-start states and a second, fully
+ *            parallel kernel writes k_tilde from them; with NULL or a smaller workspace the scan
+ *            kernel writes k_tilde itself (slower).  Results are bit-identical either way.  The
+ *            workspace is overwritten; its contents on return are unspecified.
  *   T may be 0 (then d_out = d0 or 1).
  */
 osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* beta,
                               const float* r, const float* d0, void* k_tilde,
                               osdn_dtype kt_dtype, float* d_out, int B, int T, int H, int K,
                               float eta, float d_min, float d_max, float eps, int beta_aware,
-                              void* stream);
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace size in bytes that lets osdn_precond_scan write k_tilde from its parallel kernel (0
+ * when that path does not apply: then no workspace is ever used).  For bf16/f16 keys with K = 128
+ * it is 4 * B * H * (T + 256 * ceil(T / 64)) bytes: one fp32 step size per token and the fp32
+ * (hi, lo) state at the start of each 64-token block. */
+size_t osdn_precond_scan_workspace_bytes(int B, int T, int H, int K, osdn_dtype k_dtype);
 
 /*
  * Phase 2: chunkwise preconditioned delta rule (Eqs. (2), (5), (8)-(11)).

@@ -43,8 +43,10 @@ def lib() -> ctypes.CDLL:
                           "(python -m preconditioned_delta_rule_gb300.build)")
     L = ctypes.CDLL(str(LIB_PATH))
     vp, fp, i, f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    L.osdn_precond_scan.argtypes = [vp, i, fp, fp, fp, vp, i, fp, i, i, i, i, f, f, f, f, i, vp]
     sz = ctypes.c_size_t
+    L.osdn_precond_scan.argtypes = [vp, i, fp, fp, fp, vp, i, fp, i, i, i, i, f, f, f, f, i, vp, sz, vp]
+    L.osdn_precond_scan_workspace_bytes.argtypes = [i, i, i, i, i]
+    L.osdn_precond_scan_workspace_bytes.restype = sz
     L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp, sz, vp]
     L.osdn_chunk_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.osdn_chunk_fwd_workspace_bytes.restype = sz
@@ -108,8 +110,12 @@ def _code(dtype) -> int:
 
 
 def osdn_precond_scan(k, beta, r=None, d0=None, *, k_tilde=None, kt_dtype=None, d_out=None,
-                      eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6, beta_aware=True, stream=None):
-    """Phase 1 (Algorithm 1 / Eq. (4); APF Eq. (7) with r).  k [B,T,H,K] -> (k_tilde, d_out)."""
+                      eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6, beta_aware=True, workspace=None,
+                      stream=None):
+    """Phase 1 (Algorithm 1 / Eq. (4); APF Eq. (7) with r).  k [B,T,H,K] -> (k_tilde, d_out).
+
+    ``workspace``: None (default) uses a cached torch buffer of the size the library asks for;
+    a uint8 CUDA tensor is used as given; False makes the scan kernel write k_tilde itself."""
     B, T, H, K = k.shape
     dev = k.device
     _check("k", k, (B, T, H, K), device=dev)
@@ -122,10 +128,12 @@ def osdn_precond_scan(k, beta, r=None, d0=None, *, k_tilde=None, kt_dtype=None, 
     if d_out is None:
         d_out = torch.empty((B, H, K), device=dev, dtype=torch.float32)
     _check("d_out", d_out, (B, H, K), torch.float32, dev)
+    need = osdn_precond_scan_workspace_bytes(B, T, H, K, k.dtype)
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "scan")
     st = lib().osdn_precond_scan(_ptr(k), _code(k.dtype), _ptr(beta), _ptr(r), _ptr(d0),
                                  _ptr(k_tilde), _code(k_tilde.dtype), _ptr(d_out), B, T, H, K,
                                  float(eta), float(d_min), float(d_max), float(eps),
-                                 int(bool(beta_aware)), _stream(dev, stream))
+                                 int(bool(beta_aware)), ws_ptr, ws_bytes, _stream(dev, stream))
     _raise("osdn_precond_scan", st)
     return k_tilde, d_out
 
@@ -133,17 +141,38 @@ def osdn_precond_scan(k, beta, r=None, d0=None, *, k_tilde=None, kt_dtype=None, 
 _WS_CACHE = {}
 
 
+def osdn_precond_scan_workspace_bytes(B, T, H, K, dtype=torch.bfloat16) -> int:
+    return int(lib().osdn_precond_scan_workspace_bytes(B, T, H, K, _code(dtype)))
+
+
 def osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16) -> int:
     return int(lib().osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, _code(dtype)))
 
 
-def _workspace(device, nbytes):
-    """A cached uint8 device buffer of at least nbytes (torch allocates; the library never does)."""
-    buf = _WS_CACHE.get(device)
+def _workspace(device, nbytes, role):
+    """A cached uint8 device buffer of at least nbytes per (device, role): torch allocates, the
+    library never does.  The scan and the chunk forward keep separate buffers so that a scan
+    on one stream never shares scratch with a chunk forward on another."""
+    buf = _WS_CACHE.get((device, role))
     if buf is None or buf.numel() < nbytes:
         buf = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
-        _WS_CACHE[device] = buf
+        _WS_CACHE[(device, role)] = buf
     return buf
+
+
+def _resolve_workspace(workspace, device, need, role):
+    """(pointer, bytes) for a workspace argument: None = cached buffer, False = none, else a tensor."""
+    if workspace is None:
+        ws = _workspace(device, need, role) if need else None
+    elif workspace is False:
+        ws = None
+    else:
+        ws = workspace
+        if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+    if ws is None:
+        return None, 0
+    return ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size()
 
 
 def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, o=None, S_out=None, chunk=64, scale=1.0,
@@ -167,16 +196,7 @@ def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, o=None, S_out=None, chunk
         S_out = torch.empty((B, H, V, K), device=dev, dtype=torch.float32)
     _check("S_out", S_out, (B, H, V, K), torch.float32, dev)
     need = osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 else 0
-    if workspace is None:
-        ws = _workspace(dev, need) if need else None
-    elif workspace is False:
-        ws = None
-    else:
-        ws = workspace
-        if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.is_contiguous()):
-            raise ValueError("workspace must be a contiguous CUDA tensor")
-    ws_ptr = None if ws is None else ctypes.c_void_p(ws.data_ptr())
-    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "chunk")
     st = lib().osdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(k_tilde), _ptr(v), _code(dt), _ptr(beta),
                               _ptr(S0), _ptr(o), _ptr(S_out), B, T, H, K, V, int(chunk),
                               float(scale), ws_ptr, ws_bytes, _stream(dev, stream))

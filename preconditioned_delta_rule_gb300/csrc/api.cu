@@ -40,7 +40,7 @@ osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* be
                               const float* r, const float* d0, void* k_tilde,
                               osdn_dtype kt_dtype, float* d_out, int B, int T, int H, int K,
                               float eta, float d_min, float d_max, float eps, int beta_aware,
-                              void* stream) {
+                              void* workspace, size_t workspace_bytes, void* stream) {
     if (B < 0 || T < 0 || H < 0) return OSDN_ERR_SHAPE;
     if (!head_dim_ok(K)) return K > 0 ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
     if (!dtype_ok(k_dtype) || !dtype_ok(kt_dtype)) return OSDN_ERR_DTYPE;
@@ -54,9 +54,17 @@ osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* be
     OSDN_TRY(ptr(r, false));
     OSDN_TRY(ptr(d0, false));
     OSDN_TRY(ptr(d_out, true));
+    OSDN_TRY(ptr(workspace, false));
     OsdnScanArgs a{k, k_dtype, beta, r, d0, k_tilde, kt_dtype, d_out, B, T, H, K,
                    eta, d_min, d_max, eps, beta_aware ? 1 : 0};
-    return from_cuda(osdn_launch_scan(a, static_cast<cudaStream_t>(stream)));
+    return from_cuda(osdn_launch_scan(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+size_t osdn_precond_scan_workspace_bytes(int B, int T, int H, int K, osdn_dtype k_dtype) {
+    if (B <= 0 || T <= 0 || H <= 0) return 0;
+    OsdnScanArgs a{};
+    a.B = B; a.T = T; a.H = H; a.K = K; a.k_dtype = k_dtype;
+    return osdn_scan_block_workspace_bytes(a);
 }
 
 osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, const void* v,

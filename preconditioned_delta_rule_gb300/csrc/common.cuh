@@ -99,7 +99,11 @@ struct OsdnDecodeArgs {
     int B, H, K, V; float eta, d_min, d_max, eps, scale; int beta_aware;
 };
 
-cudaError_t osdn_launch_scan(const OsdnScanArgs& a, cudaStream_t s);
+// Phase-1 scan.  16-bit keys with K = 128 use the blocked kernel; with a workspace of at least
+// osdn_scan_block_workspace_bytes(a) bytes its write keys come from a separate parallel kernel.
+cudaError_t osdn_launch_scan(const OsdnScanArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+cudaError_t osdn_launch_scan_block(const OsdnScanArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+size_t osdn_scan_block_workspace_bytes(const OsdnScanArgs& a);
 cudaError_t osdn_launch_chunk_simt(const OsdnChunkArgs& a, cudaStream_t s);
 // Tensor-core path.  With a workspace of at least osdn_chunk_tc_workspace_bytes(a) bytes it runs
 // the parallel prep kernel and the serial chain kernel; otherwise one fused kernel.  Returns

@@ -162,11 +162,9 @@ cudaError_t launch_in(const OsdnScanArgs& a, cudaStream_t s) {
 }  // namespace
 }  // namespace osdn
 
-cudaError_t osdn_launch_scan_block(const OsdnScanArgs& a, cudaStream_t s);
-
-cudaError_t osdn_launch_scan(const OsdnScanArgs& a, cudaStream_t s) {
+cudaError_t osdn_launch_scan(const OsdnScanArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
     if (a.K == 128) {
-        cudaError_t e = osdn_launch_scan_block(a, s);  // 16-bit keys: blocked tensor-core scan
+        cudaError_t e = osdn_launch_scan_block(a, ws, ws_bytes, s);  // 16-bit keys: blocked scan
         if (e != cudaErrorNotSupported) return e;
         return osdn::launch_in<128>(a, s);
     }

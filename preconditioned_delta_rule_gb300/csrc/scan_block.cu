@@ -166,7 +166,7 @@ __device__ __forceinline__ float chain_sum(float v, float* red, int tid) {
 }
 
 template <typename TIn, typename TOut, bool HAS_R>
-__global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a) {
+__global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float* ws_g, float* ws_d) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a) {
                 atomicExch(&s_abort, 1);
                 break;
             }
-            {
+            if (ws_g == nullptr) {  // emit here; with a workspace scan_emit_kernel does it
                 const int q = m & 1;
                 const unsigned char* kt = sm + OFF_KT + (m % 3) * KT_BYTES;
                 const int t0 = m * J, jb = min(J, T - t0);
@@ -373,6 +373,11 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a) {
             const float* rr = F + F_RR + q * J;
             float* gout = F + F_GOUT + q * J;
             F[F_DST + q * KD + i] = d_hi + d_lo;
+            if (ws_d) {
+                float* wd = ws_d + (static_cast<size_t>(bh) * nblk + blk) * (2 * KD);
+                wd[i] = d_hi;
+                wd[KD + i] = d_lo;
+            }
 
             int p = 0, restarts = 0;
             bool abort_now = false;
@@ -611,6 +616,10 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a) {
                 atomicExch(&s_abort, 1);
                 break;
             }
+            if (ws_g) {
+                wg_sync(1);
+                if (tid < J && blk * J + tid < T) ws_g[static_cast<size_t>(bh) * T + blk * J + tid] = gout[tid];
+            }
             mbar_arrive(bars + B_CHAIN + 8 * q);
         }
         a.d_out[static_cast<size_t>(bh) * KD + i] = d_hi + d_lo;
@@ -629,8 +638,41 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a) {
     if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
 }
 
+// Write keys of one 64-token block of one head: thread i replays coordinate i of the clipped
+// recurrence d <- clip(r_t d + g_t k_t^2) from the block's start state with the step sizes g_t the
+// scan fixed, emitting k~_t = d_t k_t.  Fully parallel over (head, block, coordinate).
+template <typename TIn, typename TOut, bool HAS_R>
+__global__ void __launch_bounds__(KD) scan_emit_kernel(OsdnScanArgs a, const float* __restrict__ ws_g,
+                                                       const float* __restrict__ ws_d) {
+    __shared__ float sg[J], sr[J];
+    const int m = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
+    const int b = bh / a.H, h = bh % a.H, T = a.T, H = a.H;
+    const int nblk = gridDim.x, t0 = m * J, jb = min(J, T - t0);
+    const size_t row0 = static_cast<size_t>(b) * T * H + h;
+    if (i < J) {
+        const bool valid = i < jb;
+        sg[i] = valid ? ws_g[static_cast<size_t>(bh) * T + t0 + i] : 0.f;
+        sr[i] = (HAS_R && valid) ? a.r[row0 + static_cast<size_t>(t0 + i) * H] : 1.f;
+    }
+    const float* wd = ws_d + (static_cast<size_t>(bh) * nblk + m) * (2 * KD);
+    float d = wd[i] + wd[KD + i];
+    const TIn* kp = static_cast<const TIn*>(a.k) + (row0 + static_cast<size_t>(t0) * H) * KD + i;
+    TOut* op = static_cast<TOut*>(a.k_tilde) + (row0 + static_cast<size_t>(t0) * H) * KD + i;
+    const size_t stride = static_cast<size_t>(H) * KD;
+    float kv[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) kv[j] = j < jb ? to_f32(kp[j * stride]) : 0.f;
+    __syncthreads();
+    const float dmin = a.d_min, dmax = a.d_max;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        if (j < jb) op[j * stride] = from_f32<TOut>(d * kv[j]);
+        d = fminf(fmaxf(fmaf(sg[j], kv[j] * kv[j], sr[j] * d), dmin), dmax);
+    }
+}
+
 template <typename TIn, typename TOut>
-cudaError_t launch_b(const OsdnScanArgs& a, cudaStream_t s) {
+cudaError_t launch_b(const OsdnScanArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
     static cudaError_t attr = [] {
         cudaError_t e1 = cudaFuncSetAttribute(scan_block_kernel<TIn, TOut, true>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
@@ -640,17 +682,30 @@ cudaError_t launch_b(const OsdnScanArgs& a, cudaStream_t s) {
     }();
     if (attr != cudaSuccess) return attr;
     dim3 grid(static_cast<unsigned>(a.B * a.H)), block(NT);
-    if (a.r) scan_block_kernel<TIn, TOut, true><<<grid, block, SMEM_ALLOC, s>>>(a);
-    else scan_block_kernel<TIn, TOut, false><<<grid, block, SMEM_ALLOC, s>>>(a);
+    const int nblk = (a.T + J - 1) / J;
+    const size_t need = static_cast<size_t>(a.B) * a.H * (static_cast<size_t>(a.T) + static_cast<size_t>(nblk) * 2 * KD) * 4;
+    float* ws_g = nullptr;
+    float* ws_d = nullptr;
+    if (ws != nullptr && ws_bytes >= need) {
+        ws_g = static_cast<float*>(ws);
+        ws_d = ws_g + static_cast<size_t>(a.B) * a.H * a.T;
+    }
+    if (a.r) scan_block_kernel<TIn, TOut, true><<<grid, block, SMEM_ALLOC, s>>>(a, ws_g, ws_d);
+    else scan_block_kernel<TIn, TOut, false><<<grid, block, SMEM_ALLOC, s>>>(a, ws_g, ws_d);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || ws_g == nullptr) return e;
+    dim3 ge(static_cast<unsigned>(nblk), static_cast<unsigned>(a.B * a.H)), be(KD);
+    if (a.r) scan_emit_kernel<TIn, TOut, true><<<ge, be, 0, s>>>(a, ws_g, ws_d);
+    else scan_emit_kernel<TIn, TOut, false><<<ge, be, 0, s>>>(a, ws_g, ws_d);
     return cudaGetLastError();
 }
 
 template <typename TIn>
-cudaError_t launch_bo(const OsdnScanArgs& a, cudaStream_t s) {
+cudaError_t launch_bo(const OsdnScanArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
     switch (a.kt_dtype) {
-        case OSDN_F32: return launch_b<TIn, float>(a, s);
-        case OSDN_BF16: return launch_b<TIn, __nv_bfloat16>(a, s);
-        case OSDN_F16: return launch_b<TIn, __half>(a, s);
+        case OSDN_F32: return launch_b<TIn, float>(a, ws, ws_bytes, s);
+        case OSDN_BF16: return launch_b<TIn, __nv_bfloat16>(a, ws, ws_bytes, s);
+        case OSDN_F16: return launch_b<TIn, __half>(a, ws, ws_bytes, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -667,10 +722,20 @@ cudaError_t osdn_scan_block_read_and_clear_timeout(unsigned int* flag) {
     return e;
 }
 
-// Blocked scan for 16-bit keys with K = 128; cudaErrorNotSupported otherwise.
-cudaError_t osdn_launch_scan_block(const OsdnScanArgs& a, cudaStream_t s) {
-    if (a.K != osdn::KD || a.T <= 0) return cudaErrorNotSupported;
-    if (a.k_dtype == OSDN_BF16) return osdn::launch_bo<__nv_bfloat16>(a, s);
-    if (a.k_dtype == OSDN_F16) return osdn::launch_bo<__half>(a, s);
-    return cudaErrorNotSupported;
+bool osdn_scan_block_covers(const OsdnScanArgs& a) {
+    return a.K == osdn::KD && a.T > 0 && (a.k_dtype == OSDN_BF16 || a.k_dtype == OSDN_F16);
+}
+
+size_t osdn_scan_block_workspace_bytes(const OsdnScanArgs& a) {
+    if (!osdn_scan_block_covers(a)) return 0;
+    const size_t nblk = (static_cast<size_t>(a.T) + osdn::J - 1) / osdn::J;
+    return static_cast<size_t>(a.B) * a.H * (static_cast<size_t>(a.T) + nblk * 2 * osdn::KD) * 4;
+}
+
+// Blocked scan for 16-bit keys with K = 128 (cudaErrorNotSupported otherwise).  With a workspace
+// of osdn_scan_block_workspace_bytes(a) bytes the write keys come from scan_emit_kernel.
+cudaError_t osdn_launch_scan_block(const OsdnScanArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (!osdn_scan_block_covers(a)) return cudaErrorNotSupported;
+    if (a.k_dtype == OSDN_BF16) return osdn::launch_bo<__nv_bfloat16>(a, ws, ws_bytes, s);
+    return osdn::launch_bo<__half>(a, ws, ws_bytes, s);
 }

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from preconditioned_delta_rule_gb300 import osdn_precond_scan
+from preconditioned_delta_rule_gb300 import binding, osdn_precond_scan
 from preconditioned_delta_rule_gb300 import workloads as W
 from tests._parity import assert_rel, np64, to_dev
 
@@ -101,3 +101,31 @@ def test_scan_d_out_aliases_d0():
     torch.cuda.synchronize()
     _, d_ref = oracle.precond_scan(inp["k"], inp["beta"], None, d0, eta=0.1)
     assert_rel(d_dev, d_ref, 1e-5, what="aliased d")
+
+
+@pytest.mark.parametrize("name,T,eta,kt_dtype", [
+    ("layer_1p3b_apf", 1000, None, torch.bfloat16),    # APF retention, ragged last block
+    ("layer_340m", 512, 0.3, torch.float32),           # interior and both faces of the box
+    ("layer_340m", 64, None, torch.float16),
+])
+def test_scan_parallel_emission_matches_in_kernel_emission(name, T, eta, kt_dtype):
+    """With a workspace the write keys come from the parallel emission kernel; without one the
+    scan kernel writes them.  Both replay the same recurrence from the same states: bit-identical."""
+    w = W.WORKLOADS[name]
+    inp = W.make_prefill(w, B=2, H=4, T=T, seed=23)
+    dev = to_dev(inp)
+    kw = dict(kt_dtype=kt_dtype, eta=w.eta if eta is None else eta, d_min=w.d_min, d_max=w.d_max,
+              eps=w.eps, beta_aware=w.beta_aware)
+    kt0, d0 = osdn_precond_scan(dev["k"], dev["beta"], dev["r"], None, workspace=False, **kw)
+    need = binding.osdn_precond_scan_workspace_bytes(2, T, 4, 128, dev["k"].dtype)
+    assert need > 0
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN garbage to start from
+    kt1, d1 = osdn_precond_scan(dev["k"], dev["beta"], dev["r"], None, workspace=ws, **kw)
+    kt2, d2 = osdn_precond_scan(dev["k"], dev["beta"], dev["r"], None, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(kt0, kt1) and torch.equal(kt1, kt2)
+    assert torch.equal(d0, d1) and torch.equal(d1, d2)
+    kt_ref, d_ref = oracle.precond_scan(inp["k"], inp["beta"], inp["r"], None, eta=kw["eta"],
+                                        d_min=w.d_min, d_max=w.d_max, eps=w.eps,
+                                        beta_aware=w.beta_aware)
+    assert_rel(d1, d_ref, 1e-5, what="d")

@@ -53,7 +53,7 @@ def scan(L, **kw):
     a.update(kw)
     return L.osdn_precond_scan(a["k"], a["kdt"], a["beta"], a["r"], a["d0"], a["kt"], a["ktdt"],
                                a["dout"], a["B"], a["T"], a["H"], a["K"], a["eta"], a["dmin"],
-                               a["dmax"], a["eps"], a["ba"], None)
+                               a["dmax"], a["eps"], a["ba"], a.get("ws"), a.get("wsb", 0), None)
 
 
 def chunk(L, **kw):
@@ -78,7 +78,7 @@ def decode(L, **kw):
     (dict(k=None), ARG), (dict(beta=None), ARG), (dict(kt=None), ARG), (dict(dout=None), ARG),
     (dict(k=A + 8), ALIGN), (dict(r=A + 4), ALIGN), (dict(d0=A + 2), ALIGN),
     (dict(K=96), UNSUP), (dict(K=0), SHAPE), (dict(B=-1), SHAPE), (dict(T=-1), SHAPE),
-    (dict(kdt=7), DTYPE), (dict(ktdt=-1), DTYPE),
+    (dict(kdt=7), DTYPE), (dict(ktdt=-1), DTYPE), (dict(ws=A + 4, wsb=1 << 20), ALIGN),
     (dict(eta=-0.1), ARG), (dict(eta=math.nan), ARG), (dict(eps=0.0), ARG),
     (dict(dmin=2.0, dmax=0.5), ARG), (dict(dmin=math.nan), ARG),
     (dict(B=0), OK), (dict(H=0), OK),
@@ -121,3 +121,12 @@ def test_workspace_size_query(L):
     assert f(1, 64, 1, 64, 64, 64, 1) == 0      # shapes the tensor-core path does not cover
     assert f(1, 64, 1, 128, 128, 64, 0) == 0    # fp32 inputs use the CUDA-core kernel
     assert f(1, 100, 1, 128, 128, 64, 1) == 0   # T not a multiple of the chunk
+
+
+def test_scan_workspace_size_query(L):
+    f = L.osdn_precond_scan_workspace_bytes
+    assert f(8, 2048, 8, 128, 1) == 4 * 8 * 8 * (2048 + 32 * 256)
+    assert f(1, 100, 2, 128, 2) == 4 * 2 * (100 + 2 * 256)   # ragged tail: ceil(100 / 64) blocks
+    assert f(1, 64, 1, 64, 1) == 0      # K = 64 runs the warp-per-head scan, no workspace
+    assert f(1, 64, 1, 128, 0) == 0     # fp32 keys likewise
+    assert f(1, 0, 1, 128, 1) == 0
