@@ -444,9 +444,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // =============================================================================================
 // Workspace path: a fully parallel prep kernel (everything that does not depend on S) and a
 // serial chain kernel (everything that does).  Per chunk the workspace holds fp16 images, in
-// the exact 128-byte-swizzled shared-memory layout, of T' (8 KB) and -W (two key blocks, 16 KB).
+// the exact 128-byte-swizzled shared-memory layout, of T' (8 KB), -W (two key blocks, 16 KB)
+// and L = tril(Q K~^T, 0) (8 KB).
 // =============================================================================================
-constexpr uint32_t WS_CHUNK = 3 * 8192;
+constexpr uint32_t WS_T = 0, WS_W = 8192, WS_L = 24576;
+constexpr uint32_t WS_CHUNK = 32768;
 
 template <int NW>
 __device__ __forceinline__ void convert_bf16_to_f16(unsigned char* base, int tid) {
@@ -464,10 +466,10 @@ __device__ __forceinline__ void convert_bf16_to_f16(unsigned char* base, int tid
 }
 
 namespace prep {
-constexpr uint32_t OFF_K = 0;          // K, two 64-wide key blocks
-constexpr uint32_t OFF_KT = 16384;     // K~
-constexpr uint32_t OFF_ZT = 32768;     // zeros | T'   ([0; T'] operand)
-constexpr uint32_t OFF_W = 49152;      // -W, two key blocks
+constexpr uint32_t OFF_KQ = 0;         // per key block: K (64 rows) | Q (64 rows), 2 x 16 KB
+constexpr uint32_t OFF_KT = 32768;     // K~ (two key blocks); after the Gram: the -W image
+constexpr uint32_t OFF_ZT = 49152;     // zeros | T'   ([0; T'] operand and T' image)
+constexpr uint32_t OFF_LI = OFF_KQ + 8192;  // L image, in the Q rows of key block 0 once Q is used
 constexpr uint32_t OFF_AM = 65536;
 constexpr uint32_t OFF_TM = OFF_AM + 10 * kTile * 4;
 constexpr uint32_t OFF_PM = OFF_TM + 10 * kTile * 4;
@@ -479,14 +481,16 @@ static_assert(2 * SMEM_ALLOC <= 232448, "two prep CTAs per SM");
 }  // namespace prep
 
 // One CTA loops over chunks q = blockIdx.x, blockIdx.x + gridDim.x, ...  (q = (b*H + h)*N + n).
-// Gram A = tril(diag(beta) K K~^T, -1) on the tensor cores, T = (I + A)^-1 in fp32,
-// T' = T diag(beta) and W = T' K (tensor cores) -> fp16 images in the workspace.
+// One tensor-core pass over the loaded tiles gives [K; Q] K~^T: the Gram K K~^T (rows 0-63, for
+// A = tril(diag(beta) K K~^T, -1)) and the scores Q K~^T (rows 64-127, for L).  Then
+// T = (I + A)^-1 in fp32, T' = T diag(beta) and W = T' K (tensor cores) -> fp16 images.
 template <typename TIn>
 __global__ void __launch_bounds__(NTHREADS, 2)
-chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKT,
-                  const float* __restrict__ beta, unsigned char* __restrict__ ws, int T, int H, int N,
-                  int total) {
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ beta,
+                  unsigned char* __restrict__ ws, int T, int H, int N, int total) {
     using namespace prep;
+    constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -504,6 +508,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         tc::mbar_init(bar_tma, 1);
         tc::mbar_init(bar_mma, 1);
         tc::mbar_init_fence();
+        tc::prefetch_tmap(&tmQ);
         tc::prefetch_tmap(&tmK);
         tc::prefetch_tmap(&tmKT);
     }
@@ -515,7 +520,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    const uint32_t id_gram = tc::idesc_f16_f32(128, C, false, false);
+    const uint32_t id_gram = kBf16 ? tc::idesc_bf16_f32(128, C, false, false) : tc::idesc_f16_f32(128, C, false, false);
     const uint32_t id_w = tc::idesc_f16_f32(128, KD, false, true);
 
     uint32_t tph = 0, mph = 0;
@@ -524,10 +529,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const int bh = q / N, n = q - bh * N, b = bh / H, h = bh - b * H;
         const int row = b * T + n * C;
         if (tid == 0) {
-            tc::mbar_expect_tx(bar_tma, 4 * 8192);
+            // the previous chunk's images (in the K~, Q and T' regions) must have been read
+            tc::bulk_wait_read_all();
+            tc::mbar_expect_tx(bar_tma, 6 * 8192);
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
-                tc::tma_load_3d(sbase + OFF_K + kb * 8192, &tmK, bar_tma, kb * 64, h, row);
+                tc::tma_load_3d(sbase + OFF_KQ + kb * 16384, &tmK, bar_tma, kb * 64, h, row);
+                tc::tma_load_3d(sbase + OFF_KQ + kb * 16384 + 8192, &tmQ, bar_tma, kb * 64, h, row);
                 tc::tma_load_3d(sbase + OFF_KT + kb * 8192, &tmKT, bar_tma, kb * 64, h, row);
             }
         }
@@ -539,16 +547,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             tph ^= 1u;
             tma_pending = false;
         }
-        if constexpr (!std::is_same<TIn, __half>::value) convert_bf16_to_f16<16>(sm + OFF_K, tid);
-        tc::fence_proxy_async();
-        __syncthreads();
 
-        // Gram K K~^T (lanes 0-63; lanes 64-127 read the next 64 rows of smem and are unused)
+        // [K; Q] K~^T on the loaded 16-bit tiles (exact products, fp32 sums)
         if (tid == 0) {
             tc::tc_fence_after();
 #pragma unroll
             for (int st = 0; st < KD / 16; ++st) {
-                const uint64_t a = tc::sdesc_sw128(sbase + OFF_K + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
+                const uint64_t a = tc::sdesc_sw128(sbase + OFF_KQ + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
                 const uint64_t bd = tc::sdesc_sw128(sbase + OFF_KT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
                 tc::mma_f16(tbase, a, bd, id_gram, st > 0);
             }
@@ -562,25 +567,35 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             mma_pending = false;
             tc::tc_fence_after();
         }
-        if (tid < C) {
+        // K becomes the fp16 B operand of W = T' K
+        if constexpr (kBf16) {
+            convert_bf16_to_f16<4>(sm + OFF_KQ, tid);
+            convert_bf16_to_f16<4>(sm + OFF_KQ + 16384, tid);
+        }
+        {
+            const int i = tid & 63;
             float g[64];
             tc::tmem_ld32(tbase + lane_base, *reinterpret_cast<float(*)[32]>(g));
             tc::tmem_ld32(tbase + lane_base + 32, *reinterpret_cast<float(*)[32]>(g + 32));
             tc::tmem_ld_wait();
-            const int i = tid, bi = i >> 4, r = i & 15;
-            const float bt = sbeta[i];
+            if (tid < C) {  // Gram rows -> strictly lower A = diag(beta) K K~^T
+                const int bi = i >> 4, r = i & 15;
+                const float bt = sbeta[i];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const int bj = j >> 4;
-                if (bj <= bi) AM[tile_index(bi, bj) * kTile + r * kTileStride + (j & 15)] = (j < i) ? bt * g[j] : 0.f;
+                for (int j = 0; j < 64; ++j) {
+                    const int bj = j >> 4;
+                    if (bj <= bi) AM[tile_index(bi, bj) * kTile + r * kTileStride + (j & 15)] = (j < i) ? bt * g[j] : 0.f;
+                }
+            } else {  // score rows -> L = tril(Q K~^T, 0), fp16 image
+#pragma unroll
+                for (int j = 0; j < 64; ++j) g[j] = (j <= i) ? g[j] : 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) st_row_chunk(sm + OFF_LI, i, c, g + 8 * c);
             }
         }
         tc::tc_fence_before();
         __syncthreads();
         ut_inverse_64(AM, TM, PM, tid);
-        // the T' and -W images of the previous chunk must have been read by their bulk stores
-        if (tid == 0) tc::bulk_wait_read_all();
-        __syncthreads();
         {
             const int i = tid >> 1, half = tid & 1, bi = i >> 4, r = i & 15;
             float t[32];
@@ -596,13 +611,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         tc::fence_proxy_async();
         __syncthreads();
 
-        // W = [0; T'] K  (lanes 64-127, 128 columns)
+        // W = [0; T'] K  (lanes 64-127, 128 columns); K's key blocks are 16 KB apart
         if (tid == 0) {
             tc::tc_fence_after();
 #pragma unroll
             for (int st = 0; st < C / 16; ++st) {
                 const uint64_t a = tc::sdesc_sw128(sbase + OFF_ZT + st * 32, 16, 1024);
-                const uint64_t bk = tc::sdesc_sw128(sbase + OFF_K + st * 2048, 8192, 1024);
+                const uint64_t bk = tc::sdesc_sw128(sbase + OFF_KQ + st * 2048, 16384, 1024);
                 tc::mma_f16(tbase, a, bk, id_w, st > 0);
             }
             tc::mma_commit(bar_mma);
@@ -615,7 +630,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             mma_pending = false;
             tc::tc_fence_after();
         }
-        if (tid >= C) {
+        if (tid >= C) {  // -W image into the K~ region (K~ is no longer needed)
             const int c = tid - C;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
@@ -626,7 +641,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 for (int j = 0; j < 32; ++j) w[j] = -w[j];
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                    st_row_chunk(sm + OFF_W + (q4 >> 1) * 8192, c, (q4 & 1) * 4 + cc, w + 8 * cc);
+                    st_row_chunk(sm + OFF_KT + (q4 >> 1) * 8192, c, (q4 & 1) * 4 + cc, w + 8 * cc);
             }
         }
         tc::fence_proxy_async();
@@ -634,8 +649,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         __syncthreads();
         if (tid == 0) {
             unsigned char* dst = ws + static_cast<size_t>(q) * WS_CHUNK;
-            tc::bulk_store(dst, sbase + OFF_ZT + 8192, 8192);
-            tc::bulk_store(dst + 8192, sbase + OFF_W, 16384);
+            tc::bulk_store(dst + WS_T, sbase + OFF_ZT + 8192, 8192);
+            tc::bulk_store(dst + WS_W, sbase + OFF_KT, 16384);
+            tc::bulk_store(dst + WS_L, sbase + OFF_LI, 8192);
             tc::bulk_commit();
         }
     }
@@ -652,252 +668,482 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 }
 
 namespace chain {
-constexpr uint32_t ST_QW = 0;                          // per key block: Q | -W  (2 x 16 KB)
-constexpr uint32_t ST_KT = 32768;                      // K~
-constexpr uint32_t ST_V = 49152;                       // V slice
-constexpr uint32_t ST_ZT = ST_V + (VS / 64) * 8192;    // zeros | T'
-constexpr uint32_t STAGE = ST_ZT + 16384;
-constexpr uint32_t OFF_LZ = 2 * STAGE;                 // L | zeros  ([L; 0] operand)
-constexpr uint32_t OFF_X = OFF_LZ + 16384;
-constexpr uint32_t OFF_SS = OFF_X + (VS / 64) * 8192;
-constexpr uint32_t OFF_BAR = OFF_SS + (VS / 64) * KD * 128;
-constexpr uint32_t SMEM_ALLOC = OFF_BAR + 64 + 1024;
-constexpr uint32_t LOAD_BYTES = 2 * 8192 + 2 * 8192 + (VS / 64) * 8192 + 2 * 8192 + 8192;
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t COL_R = 0, COL_L = VS, COL_ST = VS + 64;
+// Twelve warps with fixed roles (one CTA per (batch, head, 64 rows of S)):
+//   warps 0-3   S^T epilogue (fp32 S^T in tensor memory -> fp16 B operand in shared memory);
+//               warps 0-1 also the X epilogue (X = U - W S^T -> fp16 B operand)
+//   warps 4-7   operand staging into tensor memory: [-W; Q] as fp16, T' as exact high and low
+//               bf16 parts (U = T'V with the bf16 V tile), K~^T as fp16, [*; L] as fp16
+//   warp 8      tcgen05.mma issue (one thread)
+//   warp 9      TMA / bulk-copy producer (one thread)
+//   warps 10-11 O readout (tensor memory -> shared memory -> TMA store)
+// Every MMA takes its A operand from tensor memory; shared memory carries the loaded tiles, the
+// B operands and the two epilogue tiles.  Only the S^T and X epilogues and the two S-dependent
+// MMA groups lie on the serial path from one chunk to the next.
+constexpr int NT = 384;
+constexpr uint32_t ST_Q = 0;                           // Q, two 64-wide key blocks (as loaded)
+constexpr uint32_t ST_W = 16384;                       // -W image (fp16)
+constexpr uint32_t ST_KT = 32768;                      // K~ (as loaded)
+constexpr uint32_t ST_V = 49152;                       // V slice (as loaded)
+constexpr uint32_t ST_T = ST_V + (VS / 64) * 8192;     // T' image (fp16)
+constexpr uint32_t ST_L = ST_T + 8192;                 // L image (fp16)
+constexpr uint32_t STAGE = ST_L + 8192;
+constexpr uint32_t OFF_X = 2 * STAGE;                  // X (64 tokens x VS values), fp16
+constexpr uint32_t OFF_SS = OFF_X + (VS / 64) * 8192;  // S^T (128 key rows x VS values), fp16
+constexpr uint32_t OFF_O = OFF_SS + (VS / 64) * KD * 128;  // O tile for the TMA store
+constexpr uint32_t OFF_BAR = OFF_O + (VS / 64) * 8192;
+constexpr uint32_t SMEM_ALLOC = OFF_BAR + 256 + 1024;
+constexpr uint32_t LOAD_BYTES = 3 * 16384 + (VS / 64) * 8192 + 2 * 8192;
 static_assert(SMEM_ALLOC <= 232448, "chain shared memory");
-static_assert(STAGE % 1024 == 0 && OFF_X % 1024 == 0 && OFF_SS % 1024 == 0, "swizzle atoms");
+static_assert(STAGE % 1024 == 0 && OFF_X % 1024 == 0 && OFF_SS % 1024 == 0 && OFF_O % 1024 == 0,
+              "swizzle atoms");
+// tensor-memory columns (lanes 0-63 carry U / X, lanes 64-127 carry Q S^T / O)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_R = 0;              // R[2] (fp32)
+constexpr uint32_t COL_ST = 2 * VS;        // S^T (fp32, lane = key)
+constexpr uint32_t COL_QW = COL_ST + VS;   // A: [-W; Q] fp16, two buffers of 64 columns
+constexpr uint32_t COL_TH = COL_QW + 128;  // A: [hi(T'); 0], two buffers of 32 columns
+constexpr uint32_t COL_TL = COL_TH + 64;   // A: [lo(T'); 0], two buffers of 32 columns
+constexpr uint32_t COL_KT = COL_TL + 64;   // A: K~^T fp16 (lane = key)
+constexpr uint32_t COL_LH = COL_KT + 32;   // A: [*; L] fp16
+static_assert(COL_LH + 32 <= TMEM_COLS, "tensor memory columns");
+// mbarriers (byte offsets from OFF_BAR) and their arrival counts
+constexpr uint32_t B_FULL = 0;      // [2] stage loaded                       (1 + tx bytes)
+constexpr uint32_t B_FREE = 16;     // [2] stage no longer read               (U commit + 4 warps)
+constexpr uint32_t B_CONVA = 32;    // [2] [-W; Q], T' staged in buffer b     (4 warps)
+constexpr uint32_t B_QS = 48;       // [2] U + [-W; Q] S^T done in R[b]       (commit)
+constexpr uint32_t B_KT = 64;       // K~^T staged                            (4 warps)
+constexpr uint32_t B_LH = 72;       // L staged                               (2 warps)
+constexpr uint32_t B_XRDY = 80;     // fp16 X in shared memory                (2 warps)
+constexpr uint32_t B_ST = 88;       // S^T update done                        (commit)
+constexpr uint32_t B_SRDY = 96;     // fp16 S^T in shared memory              (4 warps)
+constexpr uint32_t B_O = 104;       // [2] O accumulated in R[b]              (commit)
+constexpr uint32_t B_RFREE = 120;   // [2] O read out of R[b]                 (2 warps)
+constexpr uint32_t B_DRAIN = 136;   // final commit before tensor memory is released
+constexpr uint32_t TMEM_SLOT = 144, ABORT = 148;
 }  // namespace chain
 
-// One CTA per (batch, head, VS rows of S), serial over chunks.  Per chunk: U = T'V,
-// X = U - W S^T and Q S^T ([Q; -W] S^T), L = tril(Q K~^T); then O = Q S^T + L X and
-// S^T += K~^T X.  T' and -W come from the workspace by bulk copy; Q, K~, V by TMA.
+// Bounded wait that also gives up as soon as another role has recorded an abort.  Every lane of
+// the calling warp must call it; the result is the same in all lanes.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+    bool ok = false;
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+        if (tc::mbar_try_wait(bar, parity)) { ok = true; break; }
+        if ((i & 63u) == 63u && *abort_flag) break;
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+// Single-thread variant (MMA issuer, producer).
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && *abort_flag) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ void record_abort(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicExch(&g_timeout_flag, 1u);
+}
+// After a warp's writes for the tensor cores (shared memory through the async proxy, or tensor
+// memory through tcgen05.st): make them visible, then one arrival per warp.
+__device__ __forceinline__ void warp_publish(uint32_t bar, int lane) {
+    tc::fence_proxy_async();
+    tc::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar);
+}
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// Two fp16 values -> their exact split into bf16 high parts (hi) and bf16 remainders (lo):
+// an fp16 significand has 11 bits, the high part keeps the top 8, the rest fits a bf16 exactly.
+__device__ __forceinline__ void f16x2_split_bf16(uint32_t w, uint32_t& hi, uint32_t& lo) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    const uint32_t h0 = __float_as_uint(f.x) & 0xffff0000u, h1 = __float_as_uint(f.y) & 0xffff0000u;
+    const uint32_t l0 = __float_as_uint(f.x - __uint_as_float(h0));
+    const uint32_t l1 = __float_as_uint(f.y - __uint_as_float(h1));
+    hi = (h0 >> 16) | h1;
+    lo = (l0 >> 16) | (l1 & 0xffff0000u);
+}
+// Named barrier over the two readout warps; true when any thread passed `pred`.
+__device__ __forceinline__ bool pair_any(bool pred) {
+    uint32_t c;
+    asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %1, 0;\n bar.red.popc.u32 %0, 1, 64, p;\n}\n"
+                 : "=r"(c)
+                 : "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+    return c != 0;
+}
+
+// One CTA per (batch, head, VS rows of S), serial over chunks.  Per chunk: U = T'V and
+// [X; Q S^T] = [U; 0] + [-W; Q] S^T; then S^T += K~^T X and O = Q S^T + L X.  T', -W and L come
+// from the workspace by bulk copy; Q, K~, V by TMA; O leaves by TMA.
 template <typename TIn>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(chain::NT, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKT,
-                   const __grid_constant__ CUtensorMap tmV, const unsigned char* __restrict__ ws,
-                   const float* S0, TIn* __restrict__ out, float* S_out, int T, int H, int V, int N,
-                   float scale) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const unsigned char* __restrict__ ws, const float* S0, float* S_out, int T, int H,
+                   int V, int N, float scale) {
     using namespace chain;
+    constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int v0 = blockIdx.y * VS;
     const uint32_t sbase = tc::smem_u32(sm);
-    const uint32_t bar_tma0 = sbase + OFF_BAR, bar_mma = sbase + OFF_BAR + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 24);
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t bars = sbase + OFF_BAR;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + TMEM_SLOT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_BAR + ABORT);
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
     if (tid == 0) {
-        tc::mbar_init(bar_tma0, 1);
-        tc::mbar_init(bar_tma0 + 8, 1);
-        tc::mbar_init(bar_mma, 1);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(bars + B_FULL + 8 * s, 1);
+            tc::mbar_init(bars + B_FREE + 8 * s, 5);
+            tc::mbar_init(bars + B_CONVA + 8 * s, 4);
+            tc::mbar_init(bars + B_QS + 8 * s, 1);
+            tc::mbar_init(bars + B_O + 8 * s, 1);
+            tc::mbar_init(bars + B_RFREE + 8 * s, 2);
+        }
+        tc::mbar_init(bars + B_KT, 4);
+        tc::mbar_init(bars + B_LH, 2);
+        tc::mbar_init(bars + B_XRDY, 2);
+        tc::mbar_init(bars + B_ST, 1);
+        tc::mbar_init(bars + B_SRDY, 4);
+        tc::mbar_init(bars + B_DRAIN, 1);
+        *abort_flag = 0;
         tc::mbar_init_fence();
         tc::prefetch_tmap(&tmQ);
         tc::prefetch_tmap(&tmKT);
         tc::prefetch_tmap(&tmV);
-    }
-    for (int e = tid; e < 8192 / 16; e += NTHREADS) {
-        reinterpret_cast<uint4*>(sm + ST_ZT)[e] = make_uint4(0, 0, 0, 0);
-        reinterpret_cast<uint4*>(sm + STAGE + ST_ZT)[e] = make_uint4(0, 0, 0, 0);
-        reinterpret_cast<uint4*>(sm + OFF_LZ + 8192)[e] = make_uint4(0, 0, 0, 0);
+        tc::prefetch_tmap(&tmO);
     }
     __syncthreads();
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
-
-    auto issue = [&](int m, int s) {
-        const uint32_t bar = bar_tma0 + 8 * s;
-        const uint32_t st = sbase + s * STAGE;
-        const int row = b * T + m * C;
-        const unsigned char* wsc = ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK;
-        tc::mbar_expect_tx(bar, LOAD_BYTES);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tc::tma_load_3d(st + ST_QW + kb * 16384, &tmQ, bar, kb * 64, h, row);
-            tc::bulk_load(st + ST_QW + kb * 16384 + 8192, wsc + 8192 + kb * 8192, 8192, bar);
-            tc::tma_load_3d(st + ST_KT + kb * 8192, &tmKT, bar, kb * 64, h, row);
-        }
-#pragma unroll
-        for (int vb = 0; vb < VS / 64; ++vb) tc::tma_load_3d(st + ST_V + vb * 8192, &tmV, bar, v0 + vb * 64, h, row);
-        tc::bulk_load(st + ST_ZT + 8192, wsc, 8192, bar);
-    };
-    if (tid == 0 && N > 0) issue(0, 0);
-
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    {  // S0 slice -> S^T in tensor memory (lane = key coordinate) and its fp16 operand copy
-        const int k = tid;
-        float sv[32];
-#pragma unroll
-        for (int half = 0; half < VS / 32; ++half) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                sv[j] = S0 ? S0[(static_cast<size_t>(bh) * V + v0 + half * 32 + j) * KD + k] : 0.f;
-            tc::tmem_st32(tbase + lane_base + COL_ST + half * 32, sv);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                st_row_chunk(sm + OFF_SS + ((half * 32) / 64) * (KD * 128), k, ((half * 32) % 64) / 8 + c, sv + 8 * c);
-        }
-        tc::tmem_st_wait();
-    }
-    tc::fence_proxy_async();
-    tc::tc_fence_before();
-    __syncthreads();
 
-    const uint32_t id_u = tc::idesc_f16_f32(128, VS, false, true);
-    const uint32_t id_l = tc::idesc_f16_f32(128, C, false, false);
-    const uint32_t id_state = tc::idesc_f16_f32(128, VS, true, true);
-    uint32_t mph = 0;
-    bool aborted = false, mma_pending = false;
-    bool tma_pending[2] = {N > 0, false};
-    int tma_chunk[2] = {0, 0};
-
-    for (int n = 0; n < N; ++n) {
-        const int s = n & 1;
-        unsigned char* stg = sm + s * STAGE;
-        const uint32_t stg_a = sbase + s * STAGE;
-        if (n + 1 < N) {
-            if (tid == 0) issue(n + 1, s ^ 1);
-            tma_pending[s ^ 1] = true;
-            tma_chunk[s ^ 1] = n + 1;
-        }
-        {
-            const bool ok = tc::mbar_wait(bar_tma0 + 8 * s, (n >> 1) & 1, kMaxPolls);
-            if (!__syncthreads_and(ok)) { aborted = true; break; }
-            tma_pending[s] = false;
-        }
-        if constexpr (!std::is_same<TIn, __half>::value) {
-            convert_bf16_to_f16<4>(stg + ST_QW, tid);
-            convert_bf16_to_f16<4>(stg + ST_QW + 16384, tid);
-            convert_bf16_to_f16<8>(stg + ST_KT, tid);
-            convert_bf16_to_f16<(VS / 64) * 4>(stg + ST_V, tid);
-        }
-        tc::fence_proxy_async();
-        __syncthreads();
-
-        if (tid == 0) {
-            tc::tc_fence_after();
+    if (warp == 9) {
+        // ================================ producer ============================================
+        if (lane == 0) {
+            int last[2] = {-1, -1};
+            for (int m = 0; m < N; ++m) {
+                const int s = m & 1;
+                if (m >= 2 && !thread_wait(bars + B_FREE + 8 * s, ((m - 2) >> 1) & 1, abort_flag)) {
+                    record_abort(abort_flag);
+                    break;
+                }
+                const uint32_t bar = bars + B_FULL + 8 * s;
+                const uint32_t st = sbase + s * STAGE;
+                const int row = b * T + m * C;
+                const unsigned char* wsc = ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK;
+                tc::mbar_expect_tx(bar, LOAD_BYTES);
 #pragma unroll
-            for (int st = 0; st < C / 16; ++st) {  // U = [0; T'] V  (lanes 64-127)
-                const uint64_t a = tc::sdesc_sw128(stg_a + ST_ZT + st * 32, 16, 1024);
-                const uint64_t bv = tc::sdesc_sw128(stg_a + ST_V + st * 2048, 8192, 1024);
-                tc::mma_f16(tbase + COL_R, a, bv, id_u, st > 0);
+                for (int kb = 0; kb < 2; ++kb) {
+                    tc::tma_load_3d(st + ST_Q + kb * 8192, &tmQ, bar, kb * 64, h, row);
+                    tc::tma_load_3d(st + ST_KT + kb * 8192, &tmKT, bar, kb * 64, h, row);
+                }
+#pragma unroll
+                for (int vb = 0; vb < VS / 64; ++vb)
+                    tc::tma_load_3d(st + ST_V + vb * 8192, &tmV, bar, v0 + vb * 64, h, row);
+                tc::bulk_load(st + ST_W, wsc + WS_W, 16384, bar);
+                tc::bulk_load(st + ST_T, wsc + WS_T, 8192, bar);
+                tc::bulk_load(st + ST_L, wsc + WS_L, 8192, bar);
+                last[s] = m;
             }
+            // nothing may still be landing in shared memory when the CTA exits
+            for (int s = 0; s < 2; ++s)
+                if (last[s] >= 0) tc::mbar_wait(bars + B_FULL + 8 * s, (last[s] >> 1) & 1, kMaxPolls >> 4);
+        }
+    } else if (warp == 8) {
+        // ================================ MMA issuer ==========================================
+        if (lane == 0) {
+            const uint32_t id_u = kBf16 ? tc::idesc_bf16_f32(128, VS, false, true) : tc::idesc_f16_f32(128, VS, false, true);
+            const uint32_t id_h = tc::idesc_f16_f32(128, VS, false, true);  // fp16 A (tensor memory), MN-major B
+            // Descriptors are built once; an operand k steps further is the same descriptor plus
+            // its byte offset / 16 (shared memory stays below 2^18 bytes, so the 14-bit address
+            // field never carries).
+            const uint64_t d_v[2] = {tc::sdesc_sw128(sbase + ST_V, 8192, 1024),
+                                     tc::sdesc_sw128(sbase + STAGE + ST_V, 8192, 1024)};
+            const uint64_t d_ss = tc::sdesc_sw128(sbase + OFF_SS, KD * 128, 1024);
+            const uint64_t d_x = tc::sdesc_sw128(sbase + OFF_X, 8192, 1024);
+            auto off = [](uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); };
+            auto issue_u = [&](int m) {  // R[m & 1] = [hi(T'); 0] V + [lo(T'); 0] V
+                const int bb = m & 1;
+                const uint32_t dR = tbase + COL_R + bb * VS;
 #pragma unroll
-            for (int st = 0; st < KD / 16; ++st) {  // += [Q; -W] S^T ; L = [Q; -W] K~^T
-                const uint64_t a = tc::sdesc_sw128(stg_a + ST_QW + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
-                const uint64_t bs = tc::sdesc_sw128(sbase + OFF_SS + st * 2048, KD * 128, 1024);
-                tc::mma_f16(tbase + COL_R, a, bs, id_u, 1);
-                const uint64_t bk = tc::sdesc_sw128(stg_a + ST_KT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
-                tc::mma_f16(tbase + COL_L, a, bk, id_l, st > 0);
+                for (int k = 0; k < C / 16; ++k)
+                    tc::mma_f16_ts(dR, tbase + COL_TH + bb * 32 + 8 * k, d_v[bb] + off(k * 2048), id_u, k > 0);
+                if constexpr (kBf16) {
+#pragma unroll
+                    for (int k = 0; k < C / 16; ++k)
+                        tc::mma_f16_ts(dR, tbase + COL_TL + bb * 32 + 8 * k, d_v[bb] + off(k * 2048), id_u, 1);
+                }
+                tc::mma_commit(bars + B_FREE + 8 * bb);
+            };
+            // U(m) needs chunk m staged and (from m = 2 on) R[m & 1] read out
+            auto u_ready = [&](int m, bool block) -> bool {
+                const uint32_t cb = bars + B_CONVA + 8 * (m & 1), cp = (m >> 1) & 1;
+                const uint32_t rb = bars + B_RFREE + 8 * (m & 1), rp = ((m - 2) >> 1) & 1;
+                if (!block) return tc::mbar_try_wait(cb, cp) && (m < 2 || tc::mbar_try_wait(rb, rp));
+                return thread_wait(cb, cp, abort_flag) && (m < 2 || thread_wait(rb, rp, abort_flag));
+            };
+            bool ok = u_ready(0, true);
+            if (ok) {
+                tc::tc_fence_after();
+                issue_u(0);
             }
-            tc::mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        {
-            const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
-            if (!__syncthreads_and(ok)) { aborted = true; break; }
-            mph ^= 1u;
-            mma_pending = false;
-            tc::tc_fence_after();
-        }
-        if (tid >= C) {  // X rows (lanes 64-127)
-            const int c = tid - C;
+            for (int n = 0; ok && n < N; ++n) {
+                const int bb = n & 1;
+                const uint32_t dR = tbase + COL_R + bb * VS;
+                // [X; Q S^T] += [-W; Q] S^T: needs the fp16 copy of S after chunk n - 1
+                if (!(ok = thread_wait(bars + B_SRDY, n & 1, abort_flag))) break;
+                tc::tc_fence_after();
 #pragma unroll
-            for (int q2 = 0; q2 < VS / 32; ++q2) {
-                float x[32];
-                tc::tmem_ld32(tbase + lane_base + COL_R + q2 * 32, x);
-                tc::tmem_ld_wait();
+                for (int k = 0; k < KD / 16; ++k)
+                    tc::mma_f16_ts(dR, tbase + COL_QW + bb * 64 + 8 * k, d_ss + off(k * 2048), id_h, 1);
+                tc::mma_commit(bars + B_QS + 8 * bb);
+                // the next chunk's U while the X epilogue runs, if its operands are staged
+                bool u_done = n + 1 >= N;
+                if (!u_done && u_ready(n + 1, false)) {
+                    tc::tc_fence_after();
+                    issue_u(n + 1);
+                    u_done = true;
+                }
+                // S^T += K~^T X
+                if (!(ok = thread_wait(bars + B_XRDY, n & 1, abort_flag) && thread_wait(bars + B_KT, n & 1, abort_flag)))
+                    break;
+                tc::tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    st_row_chunk(sm + OFF_X + ((q2 * 32) / 64) * 8192, c, ((q2 * 32) % 64) / 8 + cc, x + 8 * cc);
+                for (int k = 0; k < C / 16; ++k)
+                    tc::mma_f16_ts(tbase + COL_ST, tbase + COL_KT + 8 * k, d_x + off(k * 2048), id_h, 1);
+                tc::mma_commit(bars + B_ST);
+                // O = Q S^T + L X  (lanes 0-63 of the L operand only touch R rows already read)
+                if (!(ok = thread_wait(bars + B_LH, n & 1, abort_flag))) break;
+                tc::tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < C / 16; ++k)
+                    tc::mma_f16_ts(dR, tbase + COL_LH + 8 * k, d_x + off(k * 2048), id_h, 1);
+                tc::mma_commit(bars + B_O + 8 * bb);
+                if (!u_done) {
+                    if (!(ok = u_ready(n + 1, true))) break;
+                    tc::tc_fence_after();
+                    issue_u(n + 1);
+                }
             }
-        } else {  // L rows: tril(Q K~^T, 0) (lanes 0-63)
-            const int i = tid;
-            float g[64];
-            tc::tmem_ld32(tbase + lane_base + COL_L, *reinterpret_cast<float(*)[32]>(g));
-            tc::tmem_ld32(tbase + lane_base + COL_L + 32, *reinterpret_cast<float(*)[32]>(g + 32));
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 64; ++j) g[j] = (j <= i) ? g[j] : 0.f;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) st_row_chunk(sm + OFF_LZ, i, c, g + 8 * c);
+            if (!ok) record_abort(abort_flag);
+            // no MMA may be in flight when tensor memory is released: one more commit tracks all
+            tc::mma_commit(bars + B_DRAIN);
+            tc::mbar_wait(bars + B_DRAIN, 0, kMaxPolls >> 4);
         }
-        tc::fence_proxy_async();
-        tc::tc_fence_before();
-        __syncthreads();
-
-        if (tid == 0) {
+    } else if (warp >= 10) {
+        // ========================== O readout: TMEM -> smem -> TMA ============================
+        const int r = (warp - 10) * 32 + lane;  // token row; tensor-memory lane 64 + r
+        const bool issuer = warp == 10 && lane == 0;
+        bool ok = true;
+        for (int n = 0; n < N; ++n) {
+            const int bb = n & 1;
+            ok = warp_wait(bars + B_O + 8 * bb, (n >> 1) & 1, abort_flag);
+            if (issuer) tc::bulk_wait_read_all();  // the previous tile has left shared memory
+            if (pair_any(!ok)) { ok = false; break; }
             tc::tc_fence_after();
-#pragma unroll
-            for (int st = 0; st < C / 16; ++st) {
-                const uint64_t bx = tc::sdesc_sw128(sbase + OFF_X + st * 2048, 8192, 1024);
-                const uint64_t al = tc::sdesc_sw128(sbase + OFF_LZ + st * 32, 16, 1024);
-                tc::mma_f16(tbase + COL_R, al, bx, id_u, 1);
-                const uint64_t ak = tc::sdesc_sw128(stg_a + ST_KT + st * 2048, 8192, 1024);
-                tc::mma_f16(tbase + COL_ST, ak, bx, id_state, 1);
-            }
-            tc::mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        {
-            const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
-            if (!__syncthreads_and(ok)) { aborted = true; break; }
-            mph ^= 1u;
-            mma_pending = false;
-            tc::tc_fence_after();
-        }
-        if (tid < C) {
-            TIn* orow = out + ((static_cast<size_t>(b) * T + n * C + tid) * H + h) * V + v0;
 #pragma unroll
             for (int q2 = 0; q2 < VS / 32; ++q2) {
                 float o[32];
-                tc::tmem_ld32(tbase + lane_base + COL_R + q2 * 32, o);
+                tc::tmem_ld32(tbase + lane_base + COL_R + bb * VS + q2 * 32, o);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float ov[4] = {scale * o[j], scale * o[j + 1], scale * o[j + 2], scale * o[j + 3]};
-                    VecIO<TIn, 4>::store(orow + q2 * 32 + j, ov);
+                for (int c = 0; c < 4; ++c) {
+                    float ov[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) ov[j] = scale * o[8 * c + j];
+                    uint4 u;
+                    VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u), ov);
+                    VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u) + 4, ov + 4);
+                    *reinterpret_cast<uint4*>(sm + OFF_O + ((q2 * 32) / 64) * 8192 +
+                                              tc::sw128_off(r, ((q2 * 32) % 64) / 8 + c)) = u;
                 }
             }
-        }
-        {
-            const int k = tid;
+            tc::fence_proxy_async();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bars + B_RFREE + 8 * bb);
+            pair_any(false);  // both warps' rows are in shared memory
+            if (issuer) {
 #pragma unroll
-            for (int q2 = 0; q2 < VS / 32; ++q2) {
-                float sv[32];
-                tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, sv);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    st_row_chunk(sm + OFF_SS + ((q2 * 32) / 64) * (KD * 128), k, ((q2 * 32) % 64) / 8 + cc, sv + 8 * cc);
+                for (int vb = 0; vb < VS / 64; ++vb)
+                    tc::tma_store_3d(&tmO, sbase + OFF_O + vb * 8192, v0 + vb * 64, h, b * T + n * C);
+                tc::bulk_commit();
             }
         }
-        tc::fence_proxy_async();
-        tc::tc_fence_before();
-        __syncthreads();
+        if (issuer) tc::bulk_wait_all();
+        if (!ok) record_abort(abort_flag);
+    } else if (warp >= 4) {
+        // ======================== operand staging into tensor memory ==========================
+        const int w4 = warp - 4;
+        const bool low = w4 < 2;            // lanes 0-63: -W and T' rows; lanes 64-127: Q and L rows
+        const int r = (w4 & 1) * 32 + lane;  // row 0..63 of the 64-row tiles
+        if (!low) {  // [hi(T'); 0] and [lo(T'); 0]: the bottom 64 rows stay zero in both buffers
+            uint32_t z[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::tmem_st32u(tbase + lane_base + COL_TH + 32 * c, z);
+            tc::tmem_st_wait();
+        }
+        bool ok = true;
+        for (int m = 0; ok && m < N; ++m) {
+            const int s = m & 1, bb = m & 1;
+            const unsigned char* stg = sm + s * STAGE;
+            if (!(ok = warp_wait(bars + B_FULL + 8 * s, (m >> 1) & 1, abort_flag))) break;
+            // buffer bb was last read by U and [-W; Q] S^T of chunk m - 2
+            if (m >= 2 && !(ok = warp_wait(bars + B_QS + 8 * bb, ((m - 2) >> 1) & 1, abort_flag))) break;
+            tc::tc_fence_after();
+            if (low) {
+                uint32_t wv[32];
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_W + kb * 8192 + tc::sw128_off(r, c));
+                        wv[c * 4 + 0] = u.x;
+                        wv[c * 4 + 1] = u.y;
+                        wv[c * 4 + 2] = u.z;
+                        wv[c * 4 + 3] = u.w;
+                    }
+                    tc::tmem_st32u(tbase + lane_base + COL_QW + bb * 64 + kb * 32, wv);
+                }
+                uint32_t th[32], tl[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_T + tc::sw128_off(r, c));
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if constexpr (kBf16) {
+                            f16x2_split_bf16(w[j], th[c * 4 + j], tl[c * 4 + j]);
+                        } else {
+                            th[c * 4 + j] = w[j];
+                            tl[c * 4 + j] = 0u;
+                        }
+                    }
+                }
+                tc::tmem_st32u(tbase + lane_base + COL_TH + bb * 32, th);
+                tc::tmem_st32u(tbase + lane_base + COL_TL + bb * 32, tl);
+            } else {
+                uint32_t qh[32];
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_Q + kb * 8192 + tc::sw128_off(r, c));
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) qh[c * 4 + j] = kBf16 ? bf16x2_to_f16x2(w[j]) : w[j];
+                    }
+                    tc::tmem_st32u(tbase + lane_base + COL_QW + bb * 64 + kb * 32, qh);
+                }
+            }
+            tc::tmem_st_wait();
+            warp_publish(bars + B_CONVA + 8 * bb, lane);
+            // K~^T (lane = key); its buffer was last read by the S^T update of chunk m - 1
+            if (m >= 1 && !(ok = warp_wait(bars + B_ST, (m - 1) & 1, abort_flag))) break;
+            tc::tc_fence_after();
+            {
+                const int k = w4 * 32 + lane, kb = k >> 6, c = (k & 63) >> 3, e = k & 7;
+                const unsigned char* kt = stg + ST_KT + kb * 8192 + 2 * e;
+                uint32_t kw[32];
+#pragma unroll
+                for (int t2 = 0; t2 < 32; ++t2) {
+                    const uint32_t a0 = *reinterpret_cast<const uint16_t*>(kt + tc::sw128_off(2 * t2, c));
+                    const uint32_t a1 = *reinterpret_cast<const uint16_t*>(kt + tc::sw128_off(2 * t2 + 1, c));
+                    const uint32_t pr = a0 | (a1 << 16);
+                    kw[t2] = kBf16 ? bf16x2_to_f16x2(pr) : pr;
+                }
+                tc::tmem_st32u(tbase + lane_base + COL_KT, kw);
+                tc::tmem_st_wait();
+                warp_publish(bars + B_KT, lane);
+            }
+            // L rows (lanes 64-127); the L operand was last read by O of chunk m - 1
+            if (!low) {
+                if (m >= 1 && !(ok = warp_wait(bars + B_O + 8 * ((m - 1) & 1), ((m - 1) >> 1) & 1, abort_flag))) break;
+                tc::tc_fence_after();
+                uint32_t lh[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_L + tc::sw128_off(r, c));
+                    lh[c * 4 + 0] = u.x;
+                    lh[c * 4 + 1] = u.y;
+                    lh[c * 4 + 2] = u.z;
+                    lh[c * 4 + 3] = u.w;
+                }
+                tc::tmem_st32u(tbase + lane_base + COL_LH, lh);
+                tc::tmem_st_wait();
+                warp_publish(bars + B_LH, lane);
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bars + B_FREE + 8 * s);  // this warp's reads of stage s are done
+        }
+        if (!ok) record_abort(abort_flag);
+    } else {
+        // ============================ S^T and X epilogues =====================================
+        const int k = tid;  // key coordinate = tensor-memory lane
+        {  // S0 slice -> S^T in tensor memory and its fp16 operand copy
+            float sv[32];
+#pragma unroll
+            for (int half = 0; half < VS / 32; ++half) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    sv[j] = S0 ? S0[(static_cast<size_t>(bh) * V + v0 + half * 32 + j) * KD + k] : 0.f;
+                tc::tmem_st32(tbase + lane_base + COL_ST + half * 32, sv);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    st_row_chunk(sm + OFF_SS + ((half * 32) / 64) * (KD * 128), k, ((half * 32) % 64) / 8 + c, sv + 8 * c);
+            }
+            tc::tmem_st_wait();
+            warp_publish(bars + B_SRDY, lane);
+        }
+        bool ok = true;
+        for (int n = 0; n < N; ++n) {
+            const int bb = n & 1;
+            if (warp < 2) {  // X rows live in tensor-memory lanes 0-63
+                if (!(ok = warp_wait(bars + B_QS + 8 * bb, (n >> 1) & 1, abort_flag))) break;
+                tc::tc_fence_after();
+#pragma unroll
+                for (int q2 = 0; q2 < VS / 32; ++q2) {
+                    float x[32];
+                    tc::tmem_ld32(tbase + lane_base + COL_R + bb * VS + q2 * 32, x);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        st_row_chunk(sm + OFF_X + ((q2 * 32) / 64) * 8192, tid, ((q2 * 32) % 64) / 8 + cc, x + 8 * cc);
+                }
+                warp_publish(bars + B_XRDY, lane);
+            }
+            if (!(ok = warp_wait(bars + B_ST, n & 1, abort_flag))) break;
+            tc::tc_fence_after();
+            float sv[VS];
+#pragma unroll
+            for (int q2 = 0; q2 < VS / 32; ++q2)
+                tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, *reinterpret_cast<float(*)[32]>(sv + q2 * 32));
+            tc::tmem_ld_wait();
+            if (n + 1 < N) {
+#pragma unroll
+                for (int cc = 0; cc < VS / 8; ++cc)
+                    st_row_chunk(sm + OFF_SS + ((cc * 8) / 64) * (KD * 128), k, cc % 8, sv + 8 * cc);
+                warp_publish(bars + B_SRDY, lane);
+            } else {
+#pragma unroll
+                for (int j = 0; j < VS; ++j) S_out[(static_cast<size_t>(bh) * V + v0 + j) * KD + k] = sv[j];
+            }
+        }
+        if (!ok) record_abort(abort_flag);
     }
 
-    if (aborted) {
-        if (tid == 0) atomicExch(&g_timeout_flag, 1u);
-        for (int s = 0; s < 2; ++s)
-            if (tma_pending[s]) tc::mbar_wait(bar_tma0 + 8 * s, (tma_chunk[s] >> 1) & 1, kMaxPolls >> 4);
-        if (mma_pending) tc::mbar_wait(bar_mma, mph, kMaxPolls >> 4);
-    } else {
-        const int k = tid;
-#pragma unroll
-        for (int q2 = 0; q2 < VS / 32; ++q2) {
-            float sv[32];
-            tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, sv);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) S_out[(static_cast<size_t>(bh) * V + v0 + q2 * 32 + j) * KD + k] = sv[j];
-        }
-    }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -954,9 +1200,10 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
     const CUtensorMapDataType dt = std::is_same<TIn, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const long long rows = static_cast<long long>(a.B) * a.T;
-    CUtensorMap mq, mk, mkt, mv;
+    CUtensorMap mq, mk, mkt, mv, mo;
     if (!make_map(&mq, a.q, dt, a.K, a.H, rows) || !make_map(&mk, a.k, dt, a.K, a.H, rows) ||
-        !make_map(&mkt, a.k_tilde, dt, a.K, a.H, rows) || !make_map(&mv, a.v, dt, a.V, a.H, rows))
+        !make_map(&mkt, a.k_tilde, dt, a.K, a.H, rows) || !make_map(&mv, a.v, dt, a.V, a.H, rows) ||
+        !make_map(&mo, a.o, dt, a.V, a.H, rows))
         return cudaErrorNotSupported;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -973,14 +1220,13 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
     if (ws != nullptr && ws_bytes >= need) {
         const int total = a.B * a.H * N;
         dim3 gp(static_cast<unsigned>(total < 2 * num_sms() ? total : 2 * num_sms()));
-        chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mk, mkt, a.beta, static_cast<unsigned char*>(ws),
+        chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta, static_cast<unsigned char*>(ws),
                                                                   a.T, a.H, N, total);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         dim3 gc(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
-        chunk_chain_kernel<TIn><<<gc, block, chain::SMEM_ALLOC, s>>>(
-            mq, mkt, mv, static_cast<const unsigned char*>(ws), a.S0, static_cast<TIn*>(a.o), a.S_out, a.T, a.H, a.V,
-            N, a.scale);
+        chunk_chain_kernel<TIn><<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(
+            mq, mkt, mv, mo, static_cast<const unsigned char*>(ws), a.S0, a.S_out, a.T, a.H, a.V, N, a.scale);
         return cudaGetLastError();
     }
     dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));

@@ -55,8 +55,11 @@ def test_chunk_workloads_full_size(name, workspace):
 
 
 def test_chunk_paths_agree_and_workspace_reuse():
-    """The two tensor-core paths compute the same rounding sequence; a reused (dirty) workspace
-    and an explicitly passed one give identical results."""
+    """The fused kernel and the two-kernel path compute the same products with different operand
+    arrangements (the two-kernel chain forms T'V as hi(T')V + lo(T')V from an exact bf16 split and
+    Q K~^T from the loaded bf16 tiles), so they agree to fp32 summation order, which can move an
+    fp16-rounded operand by one unit; a reused (dirty) workspace and an explicitly passed one give
+    identical results."""
     w = W.WORKLOADS["layer_1p3b_apf"]
     inp = W.make_prefill(w, B=2, H=3, T=512, seed=13)
     kt = write_keys(inp, w, torch.bfloat16).cuda()
@@ -64,13 +67,16 @@ def test_chunk_paths_agree_and_workspace_reuse():
     S0 = torch.randn(2, 3, 128, 128, generator=torch.Generator().manual_seed(7)).cuda() * 0.1
     o1, S1 = osdn_chunk_fwd(d["q"], d["k"], kt, d["v"], d["beta"], S0, workspace=False)
     need = osdn_chunk_fwd_workspace_bytes(2, 512, 3, 128, 128)
-    assert need == 2 * 3 * 8 * 24576
+    assert need == 2 * 3 * 8 * 32768
     ws = torch.full((need + 4096,), 0xAB, dtype=torch.uint8, device="cuda")
     o2, S2 = osdn_chunk_fwd(d["q"], d["k"], kt, d["v"], d["beta"], S0, workspace=ws)
     o3, S3 = osdn_chunk_fwd(d["q"], d["k"], kt, d["v"], d["beta"], S0, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(o2, o3) and torch.equal(S2, S3)
-    assert torch.equal(o1, o2) and torch.equal(S1, S2)
+    # o is bf16: a one-unit flip of its last place (2^-7 relative) is allowed on top
+    g, r = np64(o2), np64(o1)
+    assert np.all(np.abs(g - r) <= 5e-3 + 2.0 ** -7 * np.abs(r)), float(np.max(np.abs(g - r)))
+    assert_maxabs(S2, S1, 5e-3, what="S two-kernel vs fused")
 
 
 @pytest.mark.parametrize("T", [64, 128, 448])
