@@ -57,8 +57,8 @@ def layer_bytes(w):
 # kernels behind it change, until they are captured again.
 NCU_TRAFFIC = {
     "layer_340m": {
-        "osdn_precond_scan": 34.165248e6 + 0.0 + 36.186624e6 + 0.598016e6,   # scan_block + scan_emit
-        "osdn_chunk_fwd": 101.265408e6 + 29.710848e6 + 167.854080e6 + 20.610560e6,  # prep + chain
+        "osdn_precond_scan": None,   # kernels changed since the last capture
+        "osdn_chunk_fwd": None,
     },
 }
 

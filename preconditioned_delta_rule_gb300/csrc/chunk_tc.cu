@@ -671,8 +671,8 @@ namespace chain {
 // Twelve warps with fixed roles (one CTA per (batch, head, 64 rows of S)):
 //   warps 0-3   S^T epilogue (fp32 S^T in tensor memory -> fp16 B operand in shared memory);
 //               warps 0-1 also the X epilogue (X = U - W S^T -> fp16 B operand)
-//   warps 4-7   operand staging into tensor memory: [-W; Q] as fp16, T' as exact high and low
-//               bf16 parts (U = T'V with the bf16 V tile), K~^T as fp16, [*; L] as fp16
+//   warps 4-7   operand staging: [-W; Q], [T'; 0], K~^T and [*; L] into tensor memory as fp16,
+//               and the V tile to fp16 in place (the B operand of U = T'V)
 //   warp 8      tcgen05.mma issue (one thread)
 //   warp 9      TMA / bulk-copy producer (one thread)
 //   warps 10-11 O readout (tensor memory -> shared memory -> TMA store)
@@ -701,16 +701,15 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_R = 0;              // R[2] (fp32)
 constexpr uint32_t COL_ST = 2 * VS;        // S^T (fp32, lane = key)
 constexpr uint32_t COL_QW = COL_ST + VS;   // A: [-W; Q] fp16, two buffers of 64 columns
-constexpr uint32_t COL_TH = COL_QW + 128;  // A: [hi(T'); 0], two buffers of 32 columns
-constexpr uint32_t COL_TL = COL_TH + 64;   // A: [lo(T'); 0], two buffers of 32 columns
-constexpr uint32_t COL_KT = COL_TL + 64;   // A: K~^T fp16 (lane = key)
+constexpr uint32_t COL_TH = COL_QW + 128;  // A: [T'; *] fp16, two buffers of 32 columns
+constexpr uint32_t COL_KT = COL_TH + 64;   // A: K~^T fp16 (lane = key)
 constexpr uint32_t COL_LH = COL_KT + 32;   // A: [*; L] fp16
 static_assert(COL_LH + 32 <= TMEM_COLS, "tensor memory columns");
 // mbarriers (byte offsets from OFF_BAR) and their arrival counts
 constexpr uint32_t B_FULL = 0;      // [2] stage loaded                       (1 + tx bytes)
 constexpr uint32_t B_FREE = 16;     // [2] stage no longer read               (U commit + 4 warps)
-constexpr uint32_t B_CONVA = 32;    // [2] [-W; Q], T' staged in buffer b     (4 warps)
-constexpr uint32_t B_QS = 48;       // [2] U + [-W; Q] S^T done in R[b]       (commit)
+constexpr uint32_t B_CONVA = 32;    // [2] [-W; Q], T', fp16 V staged (buffer b) (4 warps)
+constexpr uint32_t B_QS = 48;       // [2] [-W; Q] S^T done in R[b]           (commit)
 constexpr uint32_t B_KT = 64;       // K~^T staged                            (4 warps)
 constexpr uint32_t B_LH = 72;       // L staged                               (2 warps)
 constexpr uint32_t B_XRDY = 80;     // fp16 X in shared memory                (2 warps)
@@ -754,16 +753,6 @@ __device__ __forceinline__ void warp_publish(uint32_t bar, int lane) {
 }
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-// Two fp16 values -> their exact split into bf16 high parts (hi) and bf16 remainders (lo):
-// an fp16 significand has 11 bits, the high part keeps the top 8, the rest fits a bf16 exactly.
-__device__ __forceinline__ void f16x2_split_bf16(uint32_t w, uint32_t& hi, uint32_t& lo) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
-    const uint32_t h0 = __float_as_uint(f.x) & 0xffff0000u, h1 = __float_as_uint(f.y) & 0xffff0000u;
-    const uint32_t l0 = __float_as_uint(f.x - __uint_as_float(h0));
-    const uint32_t l1 = __float_as_uint(f.y - __uint_as_float(h1));
-    hi = (h0 >> 16) | h1;
-    lo = (l0 >> 16) | (l1 & 0xffff0000u);
 }
 // Named barrier over the two readout warps; true when any thread passed `pred`.
 __device__ __forceinline__ bool pair_any(bool pred) {
@@ -862,7 +851,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     } else if (warp == 8) {
         // ================================ MMA issuer ==========================================
         if (lane == 0) {
-            const uint32_t id_u = kBf16 ? tc::idesc_bf16_f32(128, VS, false, true) : tc::idesc_f16_f32(128, VS, false, true);
             const uint32_t id_h = tc::idesc_f16_f32(128, VS, false, true);  // fp16 A (tensor memory), MN-major B
             // Descriptors are built once; an operand k steps further is the same descriptor plus
             // its byte offset / 16 (shared memory stays below 2^18 bytes, so the 14-bit address
@@ -872,27 +860,21 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const uint64_t d_ss = tc::sdesc_sw128(sbase + OFF_SS, KD * 128, 1024);
             const uint64_t d_x = tc::sdesc_sw128(sbase + OFF_X, 8192, 1024);
             auto off = [](uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); };
-            auto issue_u = [&](int m) {  // R[m & 1] = [hi(T'); 0] V + [lo(T'); 0] V
+            auto issue_u = [&](int m) {  // R[m & 1] = [T'; 0] V
                 const int bb = m & 1;
                 const uint32_t dR = tbase + COL_R + bb * VS;
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    tc::mma_f16_ts(dR, tbase + COL_TH + bb * 32 + 8 * k, d_v[bb] + off(k * 2048), id_u, k > 0);
-                if constexpr (kBf16) {
-#pragma unroll
-                    for (int k = 0; k < C / 16; ++k)
-                        tc::mma_f16_ts(dR, tbase + COL_TL + bb * 32 + 8 * k, d_v[bb] + off(k * 2048), id_u, 1);
-                }
+                    tc::mma_f16_ts(dR, tbase + COL_TH + bb * 32 + 8 * k, d_v[bb] + off(k * 2048), id_h, k > 0);
                 tc::mma_commit(bars + B_FREE + 8 * bb);
             };
             // U(m) needs chunk m staged and (from m = 2 on) R[m & 1] read out
-            auto u_ready = [&](int m, bool block) -> bool {
+            auto u_ready = [&](int m) -> bool {
                 const uint32_t cb = bars + B_CONVA + 8 * (m & 1), cp = (m >> 1) & 1;
                 const uint32_t rb = bars + B_RFREE + 8 * (m & 1), rp = ((m - 2) >> 1) & 1;
-                if (!block) return tc::mbar_try_wait(cb, cp) && (m < 2 || tc::mbar_try_wait(rb, rp));
                 return thread_wait(cb, cp, abort_flag) && (m < 2 || thread_wait(rb, rp, abort_flag));
             };
-            bool ok = u_ready(0, true);
+            bool ok = u_ready(0);
             if (ok) {
                 tc::tc_fence_after();
                 issue_u(0);
@@ -907,13 +889,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int k = 0; k < KD / 16; ++k)
                     tc::mma_f16_ts(dR, tbase + COL_QW + bb * 64 + 8 * k, d_ss + off(k * 2048), id_h, 1);
                 tc::mma_commit(bars + B_QS + 8 * bb);
-                // the next chunk's U while the X epilogue runs, if its operands are staged
-                bool u_done = n + 1 >= N;
-                if (!u_done && u_ready(n + 1, false)) {
-                    tc::tc_fence_after();
-                    issue_u(n + 1);
-                    u_done = true;
-                }
                 // S^T += K~^T X
                 if (!(ok = thread_wait(bars + B_XRDY, n & 1, abort_flag) && thread_wait(bars + B_KT, n & 1, abort_flag)))
                     break;
@@ -929,8 +904,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int k = 0; k < C / 16; ++k)
                     tc::mma_f16_ts(dR, tbase + COL_LH + 8 * k, d_x + off(k * 2048), id_h, 1);
                 tc::mma_commit(bars + B_O + 8 * bb);
-                if (!u_done) {
-                    if (!(ok = u_ready(n + 1, true))) break;
+                if (n + 1 < N) {  // the next chunk's U = T'V, off the serial path
+                    if (!(ok = u_ready(n + 1))) break;
                     tc::tc_fence_after();
                     issue_u(n + 1);
                 }
@@ -987,12 +962,12 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const int w4 = warp - 4;
         const bool low = w4 < 2;            // lanes 0-63: -W and T' rows; lanes 64-127: Q and L rows
         const int r = (w4 & 1) * 32 + lane;  // row 0..63 of the 64-row tiles
-        if (!low) {  // [hi(T'); 0] and [lo(T'); 0]: the bottom 64 rows stay zero in both buffers
+        if (!low) {  // [T'; 0]: the bottom 64 rows stay zero in both buffers
             uint32_t z[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = 0u;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tc::tmem_st32u(tbase + lane_base + COL_TH + 32 * c, z);
+            for (int c = 0; c < 2; ++c) tc::tmem_st32u(tbase + lane_base + COL_TH + 32 * c, z);
             tc::tmem_st_wait();
         }
         bool ok = true;
@@ -1017,23 +992,16 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     }
                     tc::tmem_st32u(tbase + lane_base + COL_QW + bb * 64 + kb * 32, wv);
                 }
-                uint32_t th[32], tl[32];
+                uint32_t th[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_T + tc::sw128_off(r, c));
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if constexpr (kBf16) {
-                            f16x2_split_bf16(w[j], th[c * 4 + j], tl[c * 4 + j]);
-                        } else {
-                            th[c * 4 + j] = w[j];
-                            tl[c * 4 + j] = 0u;
-                        }
-                    }
+                    th[c * 4 + 0] = u.x;
+                    th[c * 4 + 1] = u.y;
+                    th[c * 4 + 2] = u.z;
+                    th[c * 4 + 3] = u.w;
                 }
                 tc::tmem_st32u(tbase + lane_base + COL_TH + bb * 32, th);
-                tc::tmem_st32u(tbase + lane_base + COL_TL + bb * 32, tl);
             } else {
                 uint32_t qh[32];
 #pragma unroll
@@ -1048,12 +1016,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     tc::tmem_st32u(tbase + lane_base + COL_QW + bb * 64 + kb * 32, qh);
                 }
             }
+            // V to fp16 in place (4 x 16 bytes per thread of the four staging warps)
+            if constexpr (kBf16) convert_bf16_to_f16<(VS / 64) * 4>(const_cast<unsigned char*>(stg) + ST_V, w4 * 32 + lane);
             tc::tmem_st_wait();
             warp_publish(bars + B_CONVA + 8 * bb, lane);
             // K~^T (lane = key); its buffer was last read by the S^T update of chunk m - 1
             if (m >= 1 && !(ok = warp_wait(bars + B_ST, (m - 1) & 1, abort_flag))) break;
             tc::tc_fence_after();
-            {
+            {  // thread k gathers key coordinate k of the 64 tokens
                 const int k = w4 * 32 + lane, kb = k >> 6, c = (k & 63) >> 3, e = k & 7;
                 const unsigned char* kt = stg + ST_KT + kb * 8192 + 2 * e;
                 uint32_t kw[32];
