@@ -76,8 +76,12 @@ constexpr uint32_t OFF_BAR = OFF_F + ((F_END * 4 + 127) / 128) * 128;
 // An M = 128 tcgen05.mma reads 128 rows (16 KB) of its A operand even though only the first 64
 // rows are used; the last A window (s_lo, slot 1, second key block) must stay inside the
 // allocation, so the used size is at least OFF_SL + 2 * 16384 + 8192.
-constexpr uint32_t SMEM_USED = (OFF_BAR + 128 > OFF_SL + 2 * 16384 + 8192) ? OFF_BAR + 128
+constexpr uint32_t SMEM_BASE = (OFF_BAR + 128 > OFF_SL + 2 * 16384 + 8192) ? OFF_BAR + 128
                                                                             : OFF_SL + 2 * 16384 + 8192;
+// the all-free Gram of the current block, scaled and masked to l < j, fp32 rows of MROW floats
+constexpr int MROW = J + 4;
+constexpr uint32_t OFF_MT = ((SMEM_BASE + 127) / 128) * 128;
+constexpr uint32_t SMEM_USED = OFF_MT + J * MROW * 4;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(3 * KT_BYTES <= OFF_SF, "key tiles");
 static_assert(OFF_SH % 1024 == 0 && OFF_SL % 1024 == 0, "swizzle atoms");
@@ -87,8 +91,9 @@ constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t COL_G = 0;     // all-free Gram of the block in slot 0 / 1: columns 0 / 64
 constexpr uint32_t COL_GM = 128;  // masked Gram computed by the chain
 
-// mbarriers (offsets from OFF_BAR): gram[2], prep_ready[2], chain_done[2], gram_masked, tmem slot
-constexpr uint32_t B_GRAM = 0, B_PREP = 16, B_CHAIN = 32, B_GM = 48, B_TMEM = 56;
+// mbarriers (offsets from OFF_BAR): gram[2], prep_ready[2], chain_done[2], gram_masked, tmem slot,
+// Gram rows in shared memory
+constexpr uint32_t B_GRAM = 0, B_PREP = 16, B_CHAIN = 32, B_GM = 48, B_TMEM = 56, B_MRDY = 64;
 
 __device__ __forceinline__ void cp_async_16z(void* smem, const void* gmem, bool valid) {
     const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
@@ -193,6 +198,7 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
             tc::mbar_init(bars + B_CHAIN + 8 * q, 128);
         }
         tc::mbar_init(bars + B_GM, 1);
+        tc::mbar_init(bars + B_MRDY, 2);
         tc::mbar_init_fence();
         s_abort = 0;
         s_grams_issued = 0;
@@ -311,6 +317,35 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
             mbar_arrive(bars + B_PREP + 8 * (m & 1));
         };
 
+        // Gram of block m, tensor memory -> shared memory (rows 0-63: warps 4-5), scaled back by
+        // 1 / sig^2 (exact: powers of two) and masked to l < j, for the chain's Jacobi rows
+        float* mt = reinterpret_cast<float*>(sm + OFF_MT);
+        auto copy_gram = [&](int m) {
+            if (u >= J) return;
+            const bool okg = tc::mbar_wait(bars + B_GRAM + 8 * (m & 1), (m >> 1) & 1, kMaxPolls);
+            if (!__all_sync(0xffffffffu, okg)) {
+                atomicExch(&s_abort, 1);
+                return;
+            }
+            if (u == 0) s_grams_used = m + 1;
+            tc::tc_fence_after();
+            const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            float g[64];
+            tc::tmem_ld32(tbase + lane_base + COL_G + (m & 1) * 64, *reinterpret_cast<float(*)[32]>(g));
+            tc::tmem_ld32(tbase + lane_base + COL_G + (m & 1) * 64 + 32, *reinterpret_cast<float(*)[32]>(g + 32));
+            tc::tmem_ld_wait();
+            const float isg = 1.f / F[F_SIGS + (m & 1)];
+            const float inv_sig2 = isg * isg;
+#pragma unroll
+            for (int l = 0; l < 64; l += 4)
+                *reinterpret_cast<float4*>(mt + u * MROW + l) =
+                    make_float4(l < u ? g[l] * inv_sig2 : 0.f, l + 1 < u ? g[l + 1] * inv_sig2 : 0.f,
+                                l + 2 < u ? g[l + 2] * inv_sig2 : 0.f, l + 3 < u ? g[l + 3] * inv_sig2 : 0.f);
+            tc::tc_fence_before();
+            __syncwarp();
+            if ((u & 31) == 0) mbar_arrive(bars + B_MRDY);
+        };
+
         stage(0);
         stage(1);
         stage(2);
@@ -318,6 +353,7 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
             cp_async_wait<2>();
             wg_sync(2);
             prepare(0);
+            copy_gram(0);
         }
         for (int m = 0; m < nblk; ++m) {
             if (m + 1 < nblk) {
@@ -332,6 +368,7 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
                 atomicExch(&s_abort, 1);
                 break;
             }
+            if (m + 1 < nblk) copy_gram(m + 1);  // the chain is done with the Gram rows of block m
             if (ws_g == nullptr) {  // emit here; with a workspace scan_emit_kernel does it
                 const int q = m & 1;
                 const unsigned char* kt = sm + OFF_KT + (m % 3) * KT_BYTES;
@@ -358,15 +395,13 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
         for (int blk = 0; blk < nblk; ++blk) {
             const int q = blk & 1;
             const uint32_t ph = (blk >> 1) & 1;
-            bool ok = tc::mbar_wait(bars + B_PREP + 8 * q, ph, kMaxPolls);
-            ok = ok && tc::mbar_wait(bars + B_GRAM + 8 * q, ph, kMaxPolls);
+            const bool ok = tc::mbar_wait(bars + B_PREP + 8 * q, ph, kMaxPolls);
             const bool bad = !ok || *static_cast<volatile int*>(&s_abort);
             if (wg_count(1, bad) != 0) {  // uniform decision across the warpgroup
                 atomicExch(&s_abort, 1);
                 break;
             }
             tc::tc_fence_after();
-            if (tid == 0) s_grams_used = blk + 1;
             const float* sf = reinterpret_cast<const float*>(sm + OFF_SF + q * SF_BYTES);
             const float* gam = F + F_GAM + q * J;
             const float* bpv = F + F_BP + q * J;
@@ -380,7 +415,7 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
             }
 
             int p = 0, restarts = 0;
-            bool abort_now = false;
+            bool abort_now = false, gram_rows_ready = false;
             while (p < J) {
                 if (restarts > kMaxRestarts) {  // the rest of the block token by token
                     wg_sync(1);
@@ -489,6 +524,16 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
                 }
                 auto rho = [&](int j) -> float { return HAS_R ? F[F_RHO + j] : 1.f; };
                 // ---- Gram of the free coordinates ------------------------------------------
+                // (the all-free Gram MMA of this block has completed once its rows are copied)
+                if (!gram_rows_ready) {
+                    const bool okr = tc::mbar_wait(bars + B_MRDY, blk & 1, kMaxPolls);
+                    if (wg_count(1, okr && !*static_cast<volatile int*>(&s_abort)) != 128) {
+                        abort_now = true;
+                        break;
+                    }
+                    gram_rows_ready = true;
+                    tc::tc_fence_after();
+                }
                 uint32_t gcol = COL_G + q * 64;
                 if (nfree > 0 && nfree < KD) {
                     // masked copy: rewrite this coordinate's column of the s copies
@@ -531,13 +576,25 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
                         if (HAS_R) ir1 = 1.f / rho(tid + 1);
                     }
                     if (nfree > 0 && row_thread) {
-                        tc::tmem_ld32(tbase + lane_base + gcol, *reinterpret_cast<float(*)[32]>(m));
-                        tc::tmem_ld32(tbase + lane_base + gcol + 32, *reinterpret_cast<float(*)[32]>(m + 32));
-                        tc::tmem_ld_wait();
-                        const float isg = 1.f / F[F_SIGS + q];
-                        const float inv_sig2 = isg * isg;  // exact: powers of two
+                        if (gcol == COL_GM) {  // masked Gram: straight from tensor memory
+                            tc::tmem_ld32(tbase + lane_base + gcol, *reinterpret_cast<float(*)[32]>(m));
+                            tc::tmem_ld32(tbase + lane_base + gcol + 32, *reinterpret_cast<float(*)[32]>(m + 32));
+                            tc::tmem_ld_wait();
+                            const float isg = 1.f / F[F_SIGS + q];
+                            const float inv_sig2 = isg * isg;  // exact: powers of two
 #pragma unroll
-                        for (int l = 0; l < 64; ++l) m[l] = (l < tid) ? m[l] * inv_sig2 : 0.f;
+                            for (int l = 0; l < 64; ++l) m[l] = (l < tid) ? m[l] * inv_sig2 : 0.f;
+                        } else {
+                            const float* mrow = reinterpret_cast<const float*>(sm + OFF_MT) + tid * MROW;
+#pragma unroll
+                            for (int l = 0; l < 64; l += 4) {
+                                const float4 v = *reinterpret_cast<const float4*>(mrow + l);
+                                m[l] = v.x;
+                                m[l + 1] = v.y;
+                                m[l + 2] = v.z;
+                                m[l + 3] = v.w;
+                            }
+                        }
                     }
                     float gj = 0.f;
                     if (row_thread) {
