@@ -734,53 +734,56 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
     if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
 }
 
-// Write keys of one 64-token block of one head: thread i replays coordinate i of the clipped
-// recurrence d <- clip(r_t d + g_t k_t^2) from the block's start state with the step sizes g_t the
-// scan fixed, emitting k~_t = d_t k_t.  Fully parallel over (head, block, coordinate).  The block's
-// 64 key rows (256 bytes each) move through shared memory in 16-byte pieces so that every global
-// access is a full, coalesced line; 16-bit write keys overwrite their own key in the tile and
-// leave the same way, fp32 write keys go straight out (a warp writes 128 contiguous bytes per row).
+// Write keys of one 64-token block of one head, EC key coordinates per CTA: thread i replays
+// coordinate c0 + i of the clipped recurrence d <- clip(r_t d + g_t k_t^2) from the block's start
+// state with the step sizes g_t the scan fixed, emitting k~_t = d_t k_t.  Fully parallel over
+// (head, block, coordinate slice); small CTAs keep many blocks in flight so that loads, the
+// dependent 64-step loop and stores of different blocks overlap.  The key slice (64 rows of
+// 2 EC bytes) moves through shared memory in 16-byte pieces; 16-bit write keys overwrite their key
+// in the tile and leave the same way, fp32 write keys go straight out.
+constexpr int EC = 32;
 template <typename TIn, typename TOut, bool HAS_R>
-__global__ void __launch_bounds__(KD) scan_emit_kernel(OsdnScanArgs a, const float* __restrict__ ws_g,
+__global__ void __launch_bounds__(EC) scan_emit_kernel(OsdnScanArgs a, const float* __restrict__ ws_g,
                                                        const float* __restrict__ ws_d) {
     static_assert(sizeof(TIn) == 2, "16-bit keys");
-    constexpr int ROW_U4 = KD * 2 / 16;   // 16-byte pieces per key row
-    __shared__ __align__(16) TIn tile[J * KD];
+    constexpr int ROW_U4 = EC * 2 / 16;   // 16-byte pieces per key row slice
+    __shared__ __align__(16) TIn tile[J * EC];
     __shared__ float sg[J], sr[J];
-    const int m = blockIdx.x, bh = blockIdx.y, i = threadIdx.x;
+    const int m = blockIdx.x, bh = blockIdx.y, c0 = blockIdx.z * EC, i = threadIdx.x;
     const int b = bh / a.H, h = bh % a.H, T = a.T, H = a.H;
     const int nblk = gridDim.x, t0 = m * J, jb = min(J, T - t0);
     const size_t row0 = static_cast<size_t>(b) * T * H + h;
     const size_t stride = static_cast<size_t>(H) * KD;      // elements between consecutive tokens
-    const TIn* kg = static_cast<const TIn*>(a.k) + (row0 + static_cast<size_t>(t0) * H) * KD;
-    TOut* og = static_cast<TOut*>(a.k_tilde) + (row0 + static_cast<size_t>(t0) * H) * KD;
+    const TIn* kg = static_cast<const TIn*>(a.k) + (row0 + static_cast<size_t>(t0) * H) * KD + c0;
+    TOut* og = static_cast<TOut*>(a.k_tilde) + (row0 + static_cast<size_t>(t0) * H) * KD + c0;
     uint4* t4 = reinterpret_cast<uint4*>(tile);
 #pragma unroll
-    for (int e = i; e < J * ROW_U4; e += KD) {
+    for (int e = i; e < J * ROW_U4; e += EC) {
         const int j = e / ROW_U4, c = e % ROW_U4;
         if (j < jb) t4[e] = *reinterpret_cast<const uint4*>(kg + j * stride + c * 8);
     }
-    if (i < J) {
-        const bool valid = i < jb;
-        sg[i] = valid ? ws_g[static_cast<size_t>(bh) * T + t0 + i] : 0.f;
-        sr[i] = (HAS_R && valid) ? a.r[row0 + static_cast<size_t>(t0 + i) * H] : 1.f;
+#pragma unroll
+    for (int jj = i; jj < J; jj += EC) {
+        const bool valid = jj < jb;
+        sg[jj] = valid ? ws_g[static_cast<size_t>(bh) * T + t0 + jj] : 0.f;
+        sr[jj] = (HAS_R && valid) ? a.r[row0 + static_cast<size_t>(t0 + jj) * H] : 1.f;
     }
-    const float* wd = ws_d + (static_cast<size_t>(bh) * nblk + m) * (2 * KD);
+    const float* wd = ws_d + (static_cast<size_t>(bh) * nblk + m) * (2 * KD) + c0;
     float d = wd[i] + wd[KD + i];
     __syncthreads();
     const float dmin = a.d_min, dmax = a.d_max;
 #pragma unroll 8
     for (int j = 0; j < jb; ++j) {
-        const float kj = to_f32(tile[j * KD + i]);
+        const float kj = to_f32(tile[j * EC + i]);
         const float kt = d * kj;
-        if constexpr (sizeof(TOut) == 2) reinterpret_cast<TOut*>(tile)[j * KD + i] = from_f32<TOut>(kt);  // own slot
+        if constexpr (sizeof(TOut) == 2) reinterpret_cast<TOut*>(tile)[j * EC + i] = from_f32<TOut>(kt);  // own slot
         else og[j * stride + i] = kt;
         d = fminf(fmaxf(fmaf(sg[j], kj * kj, sr[j] * d), dmin), dmax);
     }
     if constexpr (sizeof(TOut) == 2) {
         __syncthreads();
 #pragma unroll
-        for (int e = i; e < J * ROW_U4; e += KD) {
+        for (int e = i; e < J * ROW_U4; e += EC) {
             const int j = e / ROW_U4, c = e % ROW_U4;
             if (j < jb) *reinterpret_cast<uint4*>(og + j * stride + c * 8) = t4[e];
         }
@@ -810,7 +813,7 @@ cudaError_t launch_b(const OsdnScanArgs& a, void* ws, size_t ws_bytes, cudaStrea
     else scan_block_kernel<TIn, TOut, false><<<grid, block, SMEM_ALLOC, s>>>(a, ws_g, ws_d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || ws_g == nullptr) return e;
-    dim3 ge(static_cast<unsigned>(nblk), static_cast<unsigned>(a.B * a.H)), be(KD);
+    dim3 ge(static_cast<unsigned>(nblk), static_cast<unsigned>(a.B * a.H), KD / EC), be(EC);
     if (a.r) scan_emit_kernel<TIn, TOut, true><<<ge, be, 0, s>>>(a, ws_g, ws_d);
     else scan_emit_kernel<TIn, TOut, false><<<ge, be, 0, s>>>(a, ws_g, ws_d);
     return cudaGetLastError();
