@@ -1,9 +1,11 @@
 #!/usr/bin/env python
 """Benchmark of the OSDN forward hot path on GB300.
 
-One step = one pass of the layer forward over one batch: osdn_precond_scan (phase 1) then
-osdn_chunk_fwd (phase 2), on the 340M-shaped layer (B=8, H=8, T=2048, K=V=128, bf16 q/k/v,
-fp32 gates and state), inputs resident in HBM.  The decode step (B=256, H=16, 1024 sequential
+One step = one pass of the layer forward over one batch: osdn_layer_fwd (phase 1 and phase 2;
+for this workload one cooperative launch of the scan with the chunk prep, then the chain
+kernel), on the 340M-shaped layer (B=8, H=8, T=2048, K=V=128, bf16 q/k/v, fp32 gates and
+state), inputs resident in HBM.  The two separate entry points (osdn_precond_scan,
+osdn_chunk_fwd) are timed too and reported under "kernels".  The decode step (B=256, H=16, 1024 sequential
 tokens, fp32 state) is measured in the same run and reported under "decode".
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead (the
@@ -43,12 +45,15 @@ def peaks():
 
 
 def layer_bytes(w):
-    """Algorithmic HBM bytes per launch (inputs read once, outputs written once)."""
+    """Algorithmic HBM bytes per call (inputs read once, outputs written once): the scan, the
+    chunk forward, and the whole layer (q, k, v, beta (, r) in; k~, o, S, d out)."""
     th = w.B * w.T * w.H
     e = 2 if w.dtype != "f32" else 4
-    scan = th * (w.K * e + 4 + w.K * e + (4 if w.apf else 0)) + w.B * w.H * w.K * 4
+    r = 4 if w.apf else 0
+    scan = th * (w.K * e + 4 + w.K * e + r) + w.B * w.H * w.K * 4
     chunk = th * (3 * w.K * e + w.V * e + 4 + w.V * e) + w.B * w.H * w.V * w.K * 4
-    return scan, chunk
+    layer = th * (3 * w.K * e + w.V * e + 4 + r + w.V * e) + w.B * w.H * (w.V * w.K + w.K) * 4
+    return scan, chunk, layer
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call of each entry point on the
@@ -57,8 +62,7 @@ def layer_bytes(w):
 # kernels behind it change, until they are captured again.
 NCU_TRAFFIC = {
     "layer_340m": {
-        "osdn_precond_scan": None,   # kernels changed since the last capture
-        "osdn_chunk_fwd": None,
+        "osdn_layer_fwd": None,      # kernels changed since the last capture
     },
 }
 
@@ -260,56 +264,76 @@ def run_ours(args, w):
         binding.osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], None, o=o, S_out=S_out,
                                chunk=w.chunk)
 
+    def layer():
+        binding.osdn_layer_fwd(g["q"], g["k"], g["v"], g["beta"], g["r"], None, None, k_tilde=kt, o=o,
+                               S_out=S_out, d_out=d_out, chunk=w.chunk, eta=w.eta, d_min=w.d_min,
+                               d_max=w.d_max, eps=w.eps, beta_aware=w.beta_aware)
+
     for _ in range(max(3, args.warmup)):
         flush.fill_(1.0)
+        layer()
         scan()
         chunk()
     binding.osdn_check()
 
     n = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t_end = time.perf_counter() + 0.3  # let the sampler start while the GPU is busy
         while time.perf_counter() < t_end:
             flush.fill_(0.0)
-            scan()
-            chunk()
+            layer()
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for i in range(n):
             flush.fill_(float(i))  # evict the previous step's tensors from L2 (outside the events)
             ev[i][0].record(stream)
-            scan()
+            layer()
             ev[i][1].record(stream)
-            chunk()
-            ev[i][2].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     barrier(ws)
     binding.osdn_check()
-    scan_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
-    chunk_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
-    step_ms = [a + b for a, b in zip(scan_ms, chunk_ms)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
     total_s = max_over_ranks(sum(step_ms) / 1e3, ws)
     tokens = B * T * ws * n
     value = tokens / total_s
     ms_per_step = 1e3 * total_s / n
 
-    # kernels per step: the scan is one kernel plus the parallel emission kernel when it has a
-    # workspace; the chunk forward is a prep and a chain kernel when it has one, else one kernel
-    launches_per_step = ((2 if binding.osdn_precond_scan_workspace_bytes(B, T, H, K, g["k"].dtype) else 1)
-                         + (2 if binding.osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, w.chunk, g["k"].dtype) else 1))
-    scan_b, chunk_b = layer_bytes(w)
-    scan_avg, chunk_avg = statistics.mean(scan_ms), statistics.mean(chunk_ms)
-    dom = ("osdn_chunk_fwd", chunk_b, chunk_avg) if chunk_avg >= scan_avg else ("osdn_precond_scan", scan_b, scan_avg)
-    ach = dom[1] / (dom[2] * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC.get(w.name, {}).get(dom[0])
-    roof = {"kernel": dom[0], "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+    # the two separate entry points, for the per-phase breakdown (not part of the headline)
+    m = min(n, 200)
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(m)]
+    for i in range(m):
+        flush.fill_(float(i))
+        ev2[i][0].record(stream)
+        scan()
+        ev2[i][1].record(stream)
+        chunk()
+        ev2[i][2].record(stream)
+    torch.cuda.synchronize()
+    binding.osdn_check()
+    scan_avg = statistics.mean(ev2[i][0].elapsed_time(ev2[i][1]) for i in range(m))
+    chunk_avg = statistics.mean(ev2[i][1].elapsed_time(ev2[i][2]) for i in range(m))
+
+    # our kernels per step: the fused phase-1 / chunk-prep kernel and the chain kernel when the
+    # layer has its workspace and fewer (batch, head) pairs than SMs, else the separate calls'
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    fused = binding.osdn_layer_fwd_workspace_bytes(B, T, H, K, V, w.chunk, g["k"].dtype) > 0 and B * H < n_sm
+    launches_per_step = 2 if fused else (
+        (2 if binding.osdn_precond_scan_workspace_bytes(B, T, H, K, g["k"].dtype) else 1)
+        + (2 if binding.osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, w.chunk, g["k"].dtype) else 1))
+    scan_b, chunk_b, layer_b = layer_bytes(w)
+    layer_avg = statistics.mean(step_ms)
+    ach = layer_b / (layer_avg * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC.get(w.name, {}).get("osdn_layer_fwd")
+    roof = {"kernel": "osdn_layer_fwd", "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
             "frac": ach / hbm_peak, "traffic": traffic, "peak_source": peak_src,
-            "algorithmic_bytes_per_launch": dom[1], "avg_launch_ms": dom[2]}
+            "algorithmic_bytes_per_launch": layer_b, "avg_launch_ms": layer_avg}
     kernels = {
+        "osdn_layer_fwd": {"ms": layer_avg, "bytes": layer_b, "gbs": ach, "frac": ach / hbm_peak,
+                           "launches": launches_per_step},
         "osdn_precond_scan": {"ms": scan_avg, "bytes": scan_b,
                               "gbs": scan_b / (scan_avg * 1e-3) / 1e9,
                               "frac": scan_b / (scan_avg * 1e-3) / 1e9 / hbm_peak},
@@ -346,7 +370,8 @@ def run_ours(args, w):
 
 def run_e2e(args, w, host, dev, stream, ws):
     """Same metric through the public API from pinned host buffers: H2D of q, k, v, beta (r),
-    scan + chunk, D2H of o, S and d, every step, all inside the timed region."""
+    the layer call (chunk_osdn -> osdn_layer_fwd), D2H of o, S and d, every step, all inside the
+    timed region."""
     from preconditioned_delta_rule_gb300 import binding
 
     names = [n for n in ("q", "k", "v", "beta", "r") if host[n] is not None]

@@ -128,6 +128,32 @@ size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
                                       osdn_dtype dtype);
 
 /*
+ * One OSDN layer forward: phase 1 then phase 2, the pages' chunk_osdn (Listing 1: returns o, the
+ * final state S and the final preconditioner d) as one call.  Arguments as osdn_precond_scan and
+ * osdn_chunk_fwd; q, k, v and the write keys share `dtype`.
+ *   k_tilde  [B,T,H,K] write keys, dtype `dtype` (written; the phase-2 input)
+ *   o, S_out as osdn_chunk_fwd; d_out as osdn_precond_scan (both written)
+ *   workspace, workspace_bytes
+ *            optional caller-owned device scratch (16-byte aligned).  With at least
+ *            osdn_layer_fwd_workspace_bytes(...) bytes, bf16/f16 inputs with K = V = 128 and
+ *            fewer than one (batch, head) per SM run phase 1 and the S-independent part of
+ *            phase 2 in one cooperative launch (each chunk's prep starts as soon as phase 1 has
+ *            passed it, on the SMs phase 1 leaves free), then the serial phase-2 kernel.  Other
+ *            cases run osdn_precond_scan then osdn_chunk_fwd, giving each its part of the
+ *            workspace when it fits.  Results equal the two calls' in every case.
+ *   T must be a multiple of `chunk` (64).
+ */
+osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
+                           const float* r, const float* d0, const float* S0, void* k_tilde, void* o,
+                           float* S_out, float* d_out, int B, int T, int H, int K, int V, int chunk,
+                           float eta, float d_min, float d_max, float eps, float scale, int beta_aware,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace size in bytes for osdn_layer_fwd's fastest path with these arguments (0 when no
+ * workspace is ever used). */
+size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype);
+
+/*
  * osdn_chunk_fwd for callers that cannot allocate device memory when they call -- for example an
  * engine that reserves all GPU memory in one plan at start-up and allocates nothing afterwards,
  * or code that cannot accept an allocator call (its latency, its implicit synchronisation, its

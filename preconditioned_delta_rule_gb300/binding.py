@@ -52,6 +52,11 @@ def lib() -> ctypes.CDLL:
     L.osdn_chunk_fwd_workspace_bytes.restype = sz
     L.osdn_chunk_fwd_static_ws.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp]
     L.osdn_chunk_fwd_static_ws.restype = ctypes.c_int
+    L.osdn_layer_fwd.argtypes = [vp, vp, vp, i, fp, fp, fp, fp, vp, vp, fp, fp, i, i, i, i, i, i,
+                                 f, f, f, f, f, i, vp, sz, vp]
+    L.osdn_layer_fwd.restype = ctypes.c_int
+    L.osdn_layer_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    L.osdn_layer_fwd_workspace_bytes.restype = sz
     L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
     L.osdn_check.argtypes = [vp]
     for fn in ("osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step", "osdn_check"):
@@ -233,16 +238,58 @@ def osdn_check(stream=None, device=None):
     _raise("osdn_check", lib().osdn_check(_stream(dev, stream)))
 
 
+def osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16) -> int:
+    return int(lib().osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, _code(dtype)))
+
+
+def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, k_tilde=None, o=None, S_out=None,
+                   d_out=None, chunk=64, eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6, scale=1.0,
+                   beta_aware=True, workspace=None, stream=None):
+    """Phase 1 then phase 2 in one call.  Returns (o, S_out, d_out, k_tilde).
+
+    ``workspace``: None (default) uses a cached torch buffer of the size the library asks for;
+    a uint8 CUDA tensor is used as given; False runs without scratch."""
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    dev, dt = k.device, k.dtype
+    for name, t, shp in (("q", q, (B, T, H, K)), ("k", k, (B, T, H, K)), ("v", v, (B, T, H, V))):
+        _check(name, t, shp, dt, dev)
+    _check("beta", beta, (B, T, H), torch.float32, dev)
+    _check("r", r, (B, T, H), torch.float32, dev)
+    _check("d0", d0, (B, H, K), torch.float32, dev)
+    _check("S0", S0, (B, H, V, K), torch.float32, dev)
+    if k_tilde is None:
+        k_tilde = torch.empty((B, T, H, K), device=dev, dtype=dt)
+    _check("k_tilde", k_tilde, (B, T, H, K), dt, dev)
+    if o is None:
+        o = torch.empty((B, T, H, V), device=dev, dtype=dt)
+    _check("o", o, (B, T, H, V), dt, dev)
+    if S_out is None:
+        S_out = torch.empty((B, H, V, K), device=dev, dtype=torch.float32)
+    _check("S_out", S_out, (B, H, V, K), torch.float32, dev)
+    if d_out is None:
+        d_out = torch.empty((B, H, K), device=dev, dtype=torch.float32)
+    _check("d_out", d_out, (B, H, K), torch.float32, dev)
+    need = osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 and T % chunk == 0 else 0
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "layer")
+    st = lib().osdn_layer_fwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), _ptr(d0),
+                              _ptr(S0), _ptr(k_tilde), _ptr(o), _ptr(S_out), _ptr(d_out), B, T, H, K,
+                              V, int(chunk), float(eta), float(d_min), float(d_max), float(eps),
+                              float(scale), int(bool(beta_aware)), ws_ptr, ws_bytes,
+                              _stream(dev, stream))
+    _raise("osdn_layer_fwd", st)
+    return o, S_out, d_out, k_tilde
+
+
 def chunk_osdn(q, k, v, beta, precond_retention=None, initial_state=None, initial_d=None, *,
                chunk_size=64, eta=0.003, beta_aware=True, d_min=0.5, d_max=2.0, eps=1e-6,
-               scale=1.0, kt_dtype=None, workspace=None, stream=None):
-    """Both phases of the layer forward (the pages' ``chunk_osdn`` signature, Listing 1):
-    osdn_precond_scan then osdn_chunk_fwd.  ``scale`` defaults to 1 (o_t = S_t q_t as in the
-    equations; pass K ** -0.5 for the listing's query scaling).  Returns (o, S, d)."""
-    kt, d = osdn_precond_scan(k, beta, precond_retention, initial_d, kt_dtype=kt_dtype or k.dtype,
-                              eta=eta, d_min=-math.inf if d_min is None else d_min,
-                              d_max=math.inf if d_max is None else d_max, eps=eps,
-                              beta_aware=beta_aware, stream=stream)
-    o, S = osdn_chunk_fwd(q, k, kt, v, beta, initial_state, chunk=chunk_size, scale=scale,
-                          workspace=workspace, stream=stream)
+               scale=1.0, workspace=None, stream=None):
+    """Both phases of the layer forward (the pages' ``chunk_osdn`` signature, Listing 1) through
+    osdn_layer_fwd.  ``scale`` defaults to 1 (o_t = S_t q_t as in the equations; pass K ** -0.5
+    for the listing's query scaling).  Returns (o, S, d)."""
+    o, S, d, _ = osdn_layer_fwd(q, k, v, beta, precond_retention, initial_d, initial_state,
+                                chunk=chunk_size, eta=eta,
+                                d_min=-math.inf if d_min is None else d_min,
+                                d_max=math.inf if d_max is None else d_max, eps=eps, scale=scale,
+                                beta_aware=beta_aware, workspace=workspace, stream=stream)
     return o, S, d

@@ -32,6 +32,17 @@ osdn_status phase1_scalars(float eta, float d_min, float d_max, float eps) {
 
 osdn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA; }
 
+// phase 2 on the tensor cores where they apply, else the fp32 CUDA-core kernel
+cudaError_t chunk_dispatch(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (a.T > 0 && a.dtype != OSDN_F32 && a.K == 128 && a.V == 128) {
+        cudaError_t e = osdn_launch_chunk_tc(a, ws, ws_bytes, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    return osdn_launch_chunk_simt(a, s);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 }  // namespace
 
 extern "C" {
@@ -90,12 +101,7 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
     OSDN_TRY(ptr(S_out, true));
     OSDN_TRY(ptr(workspace, false));
     OsdnChunkArgs a{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (seq && dtype != OSDN_F32 && K == 128 && V == 128) {
-        cudaError_t e = osdn_launch_chunk_tc(a, workspace, workspace_bytes, s);
-        if (e != cudaErrorNotSupported) return from_cuda(e);
-    }
-    return from_cuda(osdn_launch_chunk_simt(a, s));
+    return from_cuda(chunk_dispatch(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
@@ -105,6 +111,71 @@ size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
     OsdnChunkArgs a{};
     a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.chunk = chunk; a.dtype = dtype;
     return osdn_chunk_tc_workspace_bytes(a);
+}
+
+osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
+                           const float* r, const float* d0, const float* S0, void* k_tilde, void* o,
+                           float* S_out, float* d_out, int B, int T, int H, int K, int V, int chunk,
+                           float eta, float d_min, float d_max, float eps, float scale, int beta_aware,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || T < 0 || H < 0 || chunk <= 0) return OSDN_ERR_SHAPE;
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return (K > 0 && V > 0) ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
+    if (chunk != 64) return OSDN_ERR_UNSUPPORTED;
+    if (T % chunk != 0) return OSDN_ERR_SHAPE;
+    if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
+    OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
+    if (!isfinite(scale)) return OSDN_ERR_ARG;
+    if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
+    if (B == 0 || H == 0) return OSDN_OK;
+    const bool seq = T > 0;
+    OSDN_TRY(ptr(q, seq));
+    OSDN_TRY(ptr(k, seq));
+    OSDN_TRY(ptr(v, seq));
+    OSDN_TRY(ptr(beta, seq));
+    OSDN_TRY(ptr(k_tilde, seq));
+    OSDN_TRY(ptr(o, seq));
+    OSDN_TRY(ptr(r, false));
+    OSDN_TRY(ptr(d0, false));
+    OSDN_TRY(ptr(S0, false));
+    OSDN_TRY(ptr(S_out, true));
+    OSDN_TRY(ptr(d_out, true));
+    OSDN_TRY(ptr(workspace, false));
+    OsdnScanArgs sa{k, dtype, beta, r, d0, k_tilde, dtype, d_out, B, T, H, K, eta, d_min, d_max, eps, beta_aware ? 1 : 0};
+    OsdnChunkArgs ca{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (seq) {
+        cudaError_t e = osdn_launch_layer(sa, ca, workspace, workspace_bytes, s);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
+    // the two phases one after the other, each with its part of the workspace when it fits
+    const size_t need_s = osdn_scan_block_workspace_bytes(sa);
+    const size_t need_c = osdn_chunk_tc_workspace_bytes(ca);
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    void* ws_s = nullptr;
+    void* ws_c = nullptr;
+    if (w && workspace_bytes >= align256(need_s) + need_c) {
+        ws_s = need_s ? w : nullptr;
+        ws_c = need_c ? w + align256(need_s) : nullptr;
+    } else if (w && need_c && workspace_bytes >= need_c) {
+        ws_c = w;
+    } else if (w && need_s && workspace_bytes >= need_s) {
+        ws_s = w;
+    }
+    cudaError_t e = osdn_launch_scan(sa, ws_s, ws_s ? need_s : 0, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(chunk_dispatch(ca, ws_c, ws_c ? need_c : 0, s));
+}
+
+size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype) {
+    if (B <= 0 || T <= 0 || H <= 0 || chunk <= 0 || T % chunk != 0) return 0;
+    OsdnScanArgs sa{};
+    sa.B = B; sa.T = T; sa.H = H; sa.K = K; sa.k_dtype = dtype; sa.kt_dtype = dtype;
+    OsdnChunkArgs ca{};
+    ca.B = B; ca.T = T; ca.H = H; ca.K = K; ca.V = V; ca.chunk = chunk; ca.dtype = dtype;
+    const size_t fused = osdn_layer_workspace_bytes(sa, ca);
+    if (fused) return fused;
+    const size_t need_s = osdn_scan_block_workspace_bytes(sa), need_c = osdn_chunk_tc_workspace_bytes(ca);
+    return need_c ? align256(need_s) + need_c : need_s;
 }
 
 osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,

@@ -35,6 +35,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "scan_block_body.cuh"
 #include "tc_ptx.cuh"
 #include "tsolve.cuh"
 
@@ -474,81 +475,123 @@ constexpr uint32_t OFF_AM = 65536;
 constexpr uint32_t OFF_TM = OFF_AM + 10 * kTile * 4;
 constexpr uint32_t OFF_PM = OFF_TM + 10 * kTile * 4;
 constexpr uint32_t OFF_BETA = OFF_PM + 3 * kTile * 4;
-constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;
+constexpr uint32_t OFF_EMIT = OFF_BETA + C * 4;              // step sizes, retention, start state
+constexpr uint32_t OFF_BAR = OFF_EMIT + (2 * C + 2 * KD) * 4;
+constexpr uint32_t REGION = ((OFF_BAR + 32 + 1023) / 1024) * 1024;  // one worker, 1024-aligned
 constexpr uint32_t SMEM_ALLOC = OFF_BAR + 32 + 1024;
 constexpr uint32_t TMEM_COLS = 128;
 static_assert(2 * SMEM_ALLOC <= 232448, "two prep CTAs per SM");
 }  // namespace prep
 
-// One CTA loops over chunks q = blockIdx.x, blockIdx.x + gridDim.x, ...  (q = (b*H + h)*N + n).
+// bar.red.and over the 128 threads of named barrier `bar`.
+__device__ __forceinline__ bool bar_and128(int bar, bool pred) {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %2, 0;\n bar.red.and.pred q, %1, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r)
+                 : "r"(bar), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+    return r != 0;
+}
+
+// The per-chunk work of phase 2 that does not depend on S, for 128 threads sharing a named
+// barrier, a 1024-aligned shared region of prep::REGION bytes and 128 tensor-memory columns.
 // One tensor-core pass over the loaded tiles gives [K; Q] K~^T: the Gram K K~^T (rows 0-63, for
 // A = tril(diag(beta) K K~^T, -1)) and the scores Q K~^T (rows 64-127, for L).  Then
-// T = (I + A)^-1 in fp32, T' = T diag(beta) and W = T' K (tensor cores) -> fp16 images.
+// T = (I + A)^-1 in fp32, T' = T diag(beta) and W = T' K (tensor cores) -> fp16 images of T', -W
+// and L in the workspace.  With EMIT the write keys of the chunk are formed here instead of
+// loaded: phase 1's clipped recurrence replayed per key coordinate from the chunk's start state
+// with the step sizes the scan fixed, k~_t = d_t k_t (the same arithmetic as the emission
+// kernel), and written out as well.
 template <typename TIn>
-__global__ void __launch_bounds__(NTHREADS, 2)
-chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ beta,
-                  unsigned char* __restrict__ ws, int T, int H, int N, int total) {
-    using namespace prep;
-    constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int tid = threadIdx.x, warp = tid >> 5;
-    float* AM = reinterpret_cast<float*>(sm + OFF_AM);
-    float* TM = reinterpret_cast<float*>(sm + OFF_TM);
-    float* PM = reinterpret_cast<float*>(sm + OFF_PM);
-    float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
-    const uint32_t sbase = tc::smem_u32(sm);
-    const uint32_t bar_tma = sbase + OFF_BAR, bar_mma = sbase + OFF_BAR + 8;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+struct PrepWorker {
+    static constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
+    unsigned char* sm;
+    uint32_t sbase, tbase, bar_tma, bar_mma, tph, mph;
+    int tid, bar;
+    bool tma_pending, mma_pending;
 
-    if (tid == 0) {
-        tc::mbar_init(bar_tma, 1);
-        tc::mbar_init(bar_mma, 1);
-        tc::mbar_init_fence();
-        tc::prefetch_tmap(&tmQ);
-        tc::prefetch_tmap(&tmK);
-        tc::prefetch_tmap(&tmKT);
+    __device__ void init(unsigned char* region, int t, int barrier_id) {
+        sm = region;
+        sbase = tc::smem_u32(sm);
+        bar_tma = sbase + prep::OFF_BAR;
+        bar_mma = sbase + prep::OFF_BAR + 8;
+        tid = t;
+        bar = barrier_id;
+        tph = mph = 0;
+        tma_pending = mma_pending = false;
+        if (tid == 0) {
+            tc::mbar_init(bar_tma, 1);
+            tc::mbar_init(bar_mma, 1);
+            tc::mbar_init_fence();
+        }
+        for (int e = tid; e < 8192 / 16; e += NTHREADS)
+            reinterpret_cast<uint4*>(sm + prep::OFF_ZT)[e] = make_uint4(0, 0, 0, 0);
     }
-    for (int e = tid; e < 8192 / 16; e += NTHREADS)
-        reinterpret_cast<uint4*>(sm + OFF_ZT)[e] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
-    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tbase = *tmem_slot;
-    const uint32_t id_gram = kBf16 ? tc::idesc_bf16_f32(128, C, false, false) : tc::idesc_f16_f32(128, C, false, false);
-    const uint32_t id_w = tc::idesc_f16_f32(128, KD, false, true);
 
-    uint32_t tph = 0, mph = 0;
-    bool aborted = false, tma_pending = false, mma_pending = false;
-    for (int q = blockIdx.x; q < total; q += gridDim.x) {
-        const int bh = q / N, n = q - bh * N, b = bh / H, h = bh - b * H;
+    // Chunk n of head (b, h) into workspace slot `slot`.  Emission inputs (EMIT only): g_src[64],
+    // r_src (stride H, or null), d_src[2 * KD] (hi, lo); kt_out: the chunk's first k~ row.
+    template <bool EMIT>
+    __device__ bool run(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmKT,
+                        const float* __restrict__ beta, unsigned char* __restrict__ ws, size_t slot, int b,
+                        int h, int n, int T, int H, const float* g_src, const float* r_src, const float* d_src,
+                        float dmin, float dmax, TIn* kt_out) {
+        using namespace prep;
+        float* AM = reinterpret_cast<float*>(sm + OFF_AM);
+        float* TM = reinterpret_cast<float*>(sm + OFF_TM);
+        float* PM = reinterpret_cast<float*>(sm + OFF_PM);
+        float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
+        float* semit = reinterpret_cast<float*>(sm + OFF_EMIT);
+        const uint32_t lane_base = static_cast<uint32_t>((tid >> 5) * 32) << 16;
+        const uint32_t id_gram = kBf16 ? tc::idesc_bf16_f32(128, C, false, false) : tc::idesc_f16_f32(128, C, false, false);
+        const uint32_t id_w = tc::idesc_f16_f32(128, KD, false, true);
         const int row = b * T + n * C;
         if (tid == 0) {
             // the previous chunk's images (in the K~, Q and T' regions) must have been read
             tc::bulk_wait_read_all();
-            tc::mbar_expect_tx(bar_tma, 6 * 8192);
+            tc::mbar_expect_tx(bar_tma, (EMIT ? 4 : 6) * 8192);
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
-                tc::tma_load_3d(sbase + OFF_KQ + kb * 16384, &tmK, bar_tma, kb * 64, h, row);
-                tc::tma_load_3d(sbase + OFF_KQ + kb * 16384 + 8192, &tmQ, bar_tma, kb * 64, h, row);
-                tc::tma_load_3d(sbase + OFF_KT + kb * 8192, &tmKT, bar_tma, kb * 64, h, row);
+                tc::tma_load_3d(sbase + OFF_KQ + kb * 16384, tmK, bar_tma, kb * 64, h, row);
+                tc::tma_load_3d(sbase + OFF_KQ + kb * 16384 + 8192, tmQ, bar_tma, kb * 64, h, row);
+                if (!EMIT) tc::tma_load_3d(sbase + OFF_KT + kb * 8192, tmKT, bar_tma, kb * 64, h, row);
             }
         }
         tma_pending = true;
         if (tid < C) sbeta[tid] = beta[(static_cast<size_t>(row) + tid) * H + h];
+        if (EMIT) {
+            if (tid < C) {
+                semit[tid] = g_src[tid];
+                semit[C + tid] = r_src ? r_src[static_cast<size_t>(tid) * H] : 1.f;
+            }
+            semit[2 * C + tid] = d_src[tid];
+            semit[2 * C + KD + tid] = d_src[KD + tid];
+        }
         {
             const bool ok = tc::mbar_wait(bar_tma, tph, kMaxPolls);
-            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            if (!bar_and128(bar, ok)) return false;
             tph ^= 1u;
             tma_pending = false;
         }
+        if (EMIT) {  // thread tid: key coordinate tid of the 64 tokens
+            const int i = tid, kb = i >> 6, c = (i & 63) >> 3, e = i & 7;
+            const unsigned char* kin = sm + OFF_KQ + kb * 16384 + 2 * e;
+            unsigned char* kto = sm + OFF_KT + kb * 8192 + 2 * e;
+            TIn* gout = kt_out + i;
+            const size_t stride = static_cast<size_t>(H) * KD;
+            float d = semit[2 * C + i] + semit[2 * C + KD + i];
+#pragma unroll 8
+            for (int j = 0; j < C; ++j) {
+                const float kj = to_f32(*reinterpret_cast<const TIn*>(kin + tc::sw128_off(j, c)));
+                const TIn kt = from_f32<TIn>(d * kj);
+                *reinterpret_cast<TIn*>(kto + tc::sw128_off(j, c)) = kt;
+                gout[j * stride] = kt;
+                d = fminf(fmaxf(fmaf(semit[j], kj * kj, semit[C + j] * d), dmin), dmax);
+            }
+            tc::fence_proxy_async();
+            bar_sync128(bar);
+        }
 
-        // [K; Q] K~^T on the loaded 16-bit tiles (exact products, fp32 sums)
+        // [K; Q] K~^T on the 16-bit tiles (exact products, fp32 sums)
         if (tid == 0) {
             tc::tc_fence_after();
 #pragma unroll
@@ -562,7 +605,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         mma_pending = true;
         {
             const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
-            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            if (!bar_and128(bar, ok)) return false;
             mph ^= 1u;
             mma_pending = false;
             tc::tc_fence_after();
@@ -594,8 +637,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             }
         }
         tc::tc_fence_before();
-        __syncthreads();
-        ut_inverse_64(AM, TM, PM, tid);
+        bar_sync128(bar);
+        ut_inverse_64(AM, TM, PM, tid, bar);
         {
             const int i = tid >> 1, half = tid & 1, bi = i >> 4, r = i & 15;
             float t[32];
@@ -609,7 +652,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             for (int c = 0; c < 4; ++c) st_row_chunk(sm + OFF_ZT + 8192, i, half * 4 + c, t + 8 * c);
         }
         tc::fence_proxy_async();
-        __syncthreads();
+        bar_sync128(bar);
 
         // W = [0; T'] K  (lanes 64-127, 128 columns); K's key blocks are 16 KB apart
         if (tid == 0) {
@@ -625,7 +668,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         mma_pending = true;
         {
             const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
-            if (!__syncthreads_and(ok)) { aborted = true; break; }
+            if (!bar_and128(bar, ok)) return false;
             mph ^= 1u;
             mma_pending = false;
             tc::tc_fence_after();
@@ -646,25 +689,66 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
         tc::fence_proxy_async();
         tc::tc_fence_before();
-        __syncthreads();
+        bar_sync128(bar);
         if (tid == 0) {
-            unsigned char* dst = ws + static_cast<size_t>(q) * WS_CHUNK;
+            unsigned char* dst = ws + slot * WS_CHUNK;
             tc::bulk_store(dst + WS_T, sbase + OFF_ZT + 8192, 8192);
             tc::bulk_store(dst + WS_W, sbase + OFF_KT, 16384);
             tc::bulk_store(dst + WS_L, sbase + OFF_LI, 8192);
             tc::bulk_commit();
         }
+        return true;
     }
-    if (aborted) {
-        if (tid == 0) atomicExch(&g_timeout_flag, 1u);
-        if (tma_pending) tc::mbar_wait(bar_tma, tph, kMaxPolls >> 4);
-        if (mma_pending) tc::mbar_wait(bar_mma, mph, kMaxPolls >> 4);
+
+    // After the last chunk (or an abort): nothing may still be in flight.
+    __device__ void finish(bool aborted) {
+        if (aborted) {
+            if (tid == 0) atomicExch(&g_timeout_flag, 1u);
+            if (tma_pending) tc::mbar_wait(bar_tma, tph, kMaxPolls >> 4);
+            if (mma_pending) tc::mbar_wait(bar_mma, mph, kMaxPolls >> 4);
+        }
+        if (tid == 0) tc::bulk_wait_all();
     }
-    if (tid == 0) tc::bulk_wait_all();
+};
+
+// One CTA loops over chunks q = blockIdx.x, blockIdx.x + gridDim.x, ...  (q = (b*H + h)*N + n).
+template <typename TIn>
+__global__ void __launch_bounds__(NTHREADS, 2)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ beta,
+                  unsigned char* __restrict__ ws, int T, int H, int N, int total) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + prep::OFF_BAR + 16);
+    PrepWorker<TIn> w;
+    w.init(sm, tid, 0);
+    if (tid == 0) {
+        tc::prefetch_tmap(&tmQ);
+        tc::prefetch_tmap(&tmK);
+        tc::prefetch_tmap(&tmKT);
+    }
+    __syncthreads();
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), prep::TMEM_COLS);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+    w.tbase = *tmem_slot;
+    bool aborted = false;
+    for (int q = blockIdx.x; q < total; q += gridDim.x) {
+        const int bh = q / N, n = q - bh * N, b = bh / H, h = bh - b * H;
+        if (!w.template run<false>(&tmQ, &tmK, &tmKT, beta, ws, static_cast<size_t>(q), b, h, n, T, H, nullptr,
+                                   nullptr, nullptr, 0.f, 0.f, nullptr)) {
+            aborted = true;
+            break;
+        }
+    }
+    w.finish(aborted);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(w.tbase, prep::TMEM_COLS);
 }
 
 namespace chain {
@@ -1120,6 +1204,86 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
 }
 
+// =============================================================================================
+// Fused layer forward: phase 1 and the S-independent part of phase 2 in one cooperative launch.
+// CTAs 0 .. BH-1 run the blocked scan of one (batch, head) each and publish every 64-token block
+// (its step sizes and start state) through a flag; every other CTA runs two prep workers that
+// take chunks in block-major order from a counter, wait for their block's flag (bounded), form
+// the chunk's write keys from the published values and do the chunk prep.  Phase 1 keeps 64 SMs
+// busy for its whole duration, so the prep of each chunk hides behind the scan of later blocks.
+// All CTAs are resident at once (cooperative launch), so the waits always end.
+// =============================================================================================
+__device__ __forceinline__ bool wait_flag(const unsigned int* p) {
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+        if (v != 0u) return true;
+        __nanosleep(64);
+    }
+    return false;
+}
+
+template <typename TIn, bool HAS_R>
+__global__ void __launch_bounds__(256, 1)
+layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* flags, unsigned int* counter,
+                       const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       unsigned char* __restrict__ cws, int N, int BH) {
+    extern __shared__ unsigned char smem_raw[];
+    if (static_cast<int>(blockIdx.x) < BH) {
+        scanblk::scan_block_body<TIn, TIn, HAS_R>(sa, ws_g, ws_d, blockIdx.x, smem_raw, &g_timeout_flag, flags);
+        return;
+    }
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
+    const int T = sa.T, H = sa.H;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_q[2];
+    PrepWorker<TIn> pw;
+    pw.init(base + w * prep::REGION, wt, 1 + w);
+    if (tid == 0) {
+        tc::prefetch_tmap(&tmQ);
+        tc::prefetch_tmap(&tmK);
+    }
+    __syncthreads();
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), 2 * prep::TMEM_COLS);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    pw.tbase = s_tmem + w * prep::TMEM_COLS;
+    const int total = BH * N;
+    TIn* kto = static_cast<TIn*>(sa.k_tilde);
+    bool aborted = false;
+    for (;;) {
+        if (wt == 0) s_q[w] = static_cast<int>(atomicAdd(counter, 1u));
+        bar_sync128(1 + w);
+        const int q = s_q[w];
+        if (q >= total) break;
+        const int m = q / BH, bh = q - m * BH, b = bh / H, h = bh - b * H;
+        bool ok = true;
+        if (wt == 0) ok = wait_flag(flags + static_cast<size_t>(bh) * N + m);
+        if (!bar_and128(1 + w, ok)) {  // the acquire above and this barrier order the reads below
+            aborted = true;
+            break;
+        }
+        const size_t row0 = static_cast<size_t>(b) * T * H + h;
+        const float* g_src = ws_g + static_cast<size_t>(bh) * T + m * C;
+        const float* r_src = HAS_R ? sa.r + row0 + static_cast<size_t>(m) * C * H : nullptr;
+        const float* d_src = ws_d + (static_cast<size_t>(bh) * N + m) * (2 * KD);
+        TIn* kt_out = kto + (row0 + static_cast<size_t>(m) * C * H) * KD;
+        if (!pw.template run<true>(&tmQ, &tmK, nullptr, sa.beta, cws, static_cast<size_t>(bh) * N + m, b, h, m, T, H,
+                                   g_src, r_src, d_src, sa.d_min, sa.d_max, kt_out)) {
+            aborted = true;
+            break;
+        }
+    }
+    pw.finish(aborted);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(s_tmem, 2 * prep::TMEM_COLS);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -1166,7 +1330,7 @@ cudaError_t set_smem(K kernel, uint32_t bytes) {
 }
 
 template <typename TIn>
-cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
+cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s, bool chain_only = false) {
     const CUtensorMapDataType dt = std::is_same<TIn, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const long long rows = static_cast<long long>(a.B) * a.T;
@@ -1190,10 +1354,12 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
     if (ws != nullptr && ws_bytes >= need) {
         const int total = a.B * a.H * N;
         dim3 gp(static_cast<unsigned>(total < 2 * num_sms() ? total : 2 * num_sms()));
-        chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta, static_cast<unsigned char*>(ws),
-                                                                  a.T, a.H, N, total);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        if (!chain_only) {
+            chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta,
+                                                                      static_cast<unsigned char*>(ws), a.T, a.H, N, total);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
         dim3 gc(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
         chunk_chain_kernel<TIn><<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(
             mq, mkt, mv, mo, static_cast<const unsigned char*>(ws), a.S0, a.S_out, a.T, a.H, a.V, N, a.scale);
@@ -1210,8 +1376,90 @@ bool tc_covers(const OsdnChunkArgs& a) {
            (a.dtype == OSDN_BF16 || a.dtype == OSDN_F16);
 }
 
+// Workspace of the fused layer: [scan: step sizes, block-start states][chunk images][block flags]
+// [chunk counter], each part 256-byte aligned.
+struct LayerWs {
+    size_t scan, chunk, flags, counter, total;
+};
+LayerWs layer_ws(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    LayerWs l{};
+    const size_t nblk = static_cast<size_t>(ca.T / C);
+    l.scan = 0;
+    l.chunk = up(osdn_scan_block_workspace_bytes(sa));
+    l.flags = l.chunk + up(static_cast<size_t>(ca.B) * ca.H * nblk * WS_CHUNK);
+    l.counter = l.flags + up(static_cast<size_t>(ca.B) * ca.H * nblk * 4);
+    l.total = l.counter + 256;
+    return l;
+}
+
+bool layer_covers(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
+    return tc_covers(ca) && ca.V == KD && sa.K == KD && sa.k_dtype == ca.dtype && sa.kt_dtype == ca.dtype &&
+           ca.B * ca.H < num_sms() && osdn_scan_block_workspace_bytes(sa) > 0;
+}
+
+template <typename TIn, bool HAS_R>
+cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsigned char* ws, cudaStream_t s) {
+    const CUtensorMapDataType dt = std::is_same<TIn, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const long long rows = static_cast<long long>(ca.B) * ca.T;
+    CUtensorMap mq, mk;
+    if (!make_map(&mq, ca.q, dt, ca.K, ca.H, rows) || !make_map(&mk, ca.k, dt, ca.K, ca.H, rows))
+        return cudaErrorNotSupported;
+    auto kernel = layer_scan_prep_kernel<TIn, HAS_R>;
+    const uint32_t smem = scanblk::SMEM_ALLOC > 2 * prep::REGION + 1024 ? scanblk::SMEM_ALLOC : 2 * prep::REGION + 1024;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] { attr_err = set_smem(kernel, smem); });
+    if (attr_err != cudaSuccess) return attr_err;
+    // every CTA must be resident at once: one per SM, phase 1 on BH of them, prep on the rest
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem) != cudaSuccess || per_sm < 1)
+        return cudaErrorNotSupported;
+    const int grid = per_sm * num_sms();
+    if (grid <= ca.B * ca.H) return cudaErrorNotSupported;
+    const LayerWs l = layer_ws(sa, ca);
+    cudaError_t e = cudaMemsetAsync(ws + l.flags, 0, l.total - l.flags, s);
+    if (e != cudaSuccess) return e;
+    OsdnScanArgs sa2 = sa;
+    float* ws_g = reinterpret_cast<float*>(ws + l.scan);
+    float* ws_d = ws_g + static_cast<size_t>(sa.B) * sa.H * sa.T;
+    unsigned int* flags = reinterpret_cast<unsigned int*>(ws + l.flags);
+    unsigned int* counter = reinterpret_cast<unsigned int*>(ws + l.counter);
+    unsigned char* cws = ws + l.chunk;
+    int N = ca.T / C, BH = ca.B * ca.H;
+    void* args[] = {&sa2, &ws_g, &ws_d, &flags, &counter, &mq, &mk, &cws, &N, &BH};
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
+                                    dim3(256), args, smem, s);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer resident CTAs than expected: two calls
+        (void)cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
+    if (e != cudaSuccess) return e;
+    // the serial chain over the chunk images (same kernel as osdn_chunk_fwd's workspace path)
+    return launch_tc<TIn>(ca, cws, l.total, s, /*chain_only=*/true);
+}
+
 }  // namespace
 }  // namespace osdn
+
+size_t osdn_layer_workspace_bytes(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
+    if (!osdn::layer_covers(sa, ca)) return 0;
+    return osdn::layer_ws(sa, ca).total;
+}
+
+// Fused layer (scan + chunk prep in one cooperative launch, then the chain kernel);
+// cudaErrorNotSupported when it does not apply (the caller then runs the two entry points).
+cudaError_t osdn_launch_layer(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, void* ws, size_t ws_bytes,
+                              cudaStream_t s) {
+    if (!osdn::layer_covers(sa, ca) || ws == nullptr || ws_bytes < osdn::layer_ws(sa, ca).total)
+        return cudaErrorNotSupported;
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    if (ca.dtype == OSDN_BF16)
+        return sa.r ? osdn::launch_layer_t<__nv_bfloat16, true>(sa, ca, w, s)
+                    : osdn::launch_layer_t<__nv_bfloat16, false>(sa, ca, w, s);
+    return sa.r ? osdn::launch_layer_t<__half, true>(sa, ca, w, s) : osdn::launch_layer_t<__half, false>(sa, ca, w, s);
+}
 
 size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a) {
     if (!osdn::tc_covers(a)) return 0;

@@ -111,5 +111,9 @@ cudaError_t osdn_launch_chunk_simt(const OsdnChunkArgs& a, cudaStream_t s);
 cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a);
 cudaError_t osdn_launch_decode(const OsdnDecodeArgs& a, cudaStream_t s);
+// Fused layer forward (phase 1 + chunk prep in one cooperative launch, then the chain kernel).
+cudaError_t osdn_launch_layer(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, void* ws, size_t ws_bytes,
+                              cudaStream_t s);
+size_t osdn_layer_workspace_bytes(const OsdnScanArgs& sa, const OsdnChunkArgs& ca);
 // Reads and clears the device-side timeout word (synchronous on the given stream).
 cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s);

@@ -8,10 +8,13 @@
 // The ten lower-triangular tiles of A and T are stored packed (tile (i, j) at index
 // i(i+1)/2 + j), each 16 rows of kTileStride floats (an even stride, so that pairs of columns
 // load as float2, and rows fall on distinct banks).  Every loop has compile-time bounds.
-// Must be called by all 128 threads of the CTA; it synchronises internally.
+// Must be called by 128 threads that share named barrier `bar` (bar 0 with a 128-thread CTA is
+// __syncthreads()); it synchronises internally on that barrier.
 #pragma once
 
 namespace osdn {
+
+__device__ __forceinline__ void bar_sync128(int bar) { asm volatile("bar.sync %0, 128;\n" ::"r"(bar) : "memory"); }
 
 constexpr int kTileStride = 18;
 constexpr int kTile = 16 * kTileStride;  // floats per packed tile
@@ -20,7 +23,7 @@ __device__ __forceinline__ constexpr int tile_index(int i, int j) { return i * (
 
 template <int LAM>
 __device__ __forceinline__ void tsolve_level(const float* __restrict__ AM, float* __restrict__ TM,
-                                             float* __restrict__ PM, int tid) {
+                                             float* __restrict__ PM, int tid, int bar) {
     constexpr int NB = 4 - LAM;  // tiles on this sub-diagonal
     const int ii = tid >> 3, jj = (tid & 7) * 2;
     float acc[NB][2];
@@ -44,7 +47,7 @@ __device__ __forceinline__ void tsolve_level(const float* __restrict__ AM, float
 #pragma unroll
     for (int blk = 0; blk < NB; ++blk)
         *reinterpret_cast<float2*>(PM + blk * kTile + ii * kTileStride + jj) = make_float2(acc[blk][0], acc[blk][1]);
-    __syncthreads();
+    bar_sync128(bar);
 #pragma unroll
     for (int blk = 0; blk < NB; ++blk) {
         const float* Tr = TM + tile_index(blk + LAM, blk + LAM) * kTile + ii * kTileStride;
@@ -60,14 +63,14 @@ __device__ __forceinline__ void tsolve_level(const float* __restrict__ AM, float
         *reinterpret_cast<float2*>(TM + tile_index(blk + LAM, blk) * kTile + ii * kTileStride + jj) =
             make_float2(-r0, -r1);
     }
-    __syncthreads();
+    bar_sync128(bar);
 }
 
 // AM: packed strictly-lower A (the diagonal tiles' upper parts may hold anything; only entries
 // below the diagonal are read).  TM receives T.  PM is scratch of 3 tiles.  Callers must
-// __syncthreads() between writing AM and calling this.
+// synchronise on `bar` between writing AM and calling this.
 __device__ __forceinline__ void ut_inverse_64(const float* __restrict__ AM, float* __restrict__ TM,
-                                              float* __restrict__ PM, int tid) {
+                                              float* __restrict__ PM, int tid, int bar = 0) {
     if (tid < 64) {
         const int blk = tid >> 4, c = tid & 15;
         const float* Ab = AM + tile_index(blk, blk) * kTile;
@@ -82,10 +85,10 @@ __device__ __forceinline__ void ut_inverse_64(const float* __restrict__ AM, floa
 #pragma unroll
         for (int i = 0; i < 16; ++i) Tb[i * kTileStride + c] = x[i];
     }
-    __syncthreads();
-    tsolve_level<1>(AM, TM, PM, tid);
-    tsolve_level<2>(AM, TM, PM, tid);
-    tsolve_level<3>(AM, TM, PM, tid);
+    bar_sync128(bar);
+    tsolve_level<1>(AM, TM, PM, tid, bar);
+    tsolve_level<2>(AM, TM, PM, tid, bar);
+    tsolve_level<3>(AM, TM, PM, tid, bar);
 }
 
 }  // namespace osdn

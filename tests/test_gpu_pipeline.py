@@ -1,5 +1,6 @@
-"""End-to-end GPU parity of the layer forward (osdn_precond_scan -> osdn_chunk_fwd, bf16 write
-keys) against the oracle's interleaved fp64 forward on the workloads' full sizes."""
+"""End-to-end GPU parity of the layer forward (chunk_osdn -> osdn_layer_fwd: the fused phase-1 /
+chunk-prep launch and the chain kernel for bf16 inputs, the two separate calls for fp32) against
+the oracle's interleaved fp64 forward on the workloads' full sizes."""
 import pytest
 import torch
 

@@ -130,3 +130,34 @@ def test_scan_workspace_size_query(L):
     assert f(1, 64, 1, 64, 1) == 0      # K = 64 runs the warp-per-head scan, no workspace
     assert f(1, 64, 1, 128, 0) == 0     # fp32 keys likewise
     assert f(1, 0, 1, 128, 1) == 0
+
+
+def layer(L, **kw):
+    a = dict(q=A, k=A, v=A, dt=1, beta=A, r=None, d0=None, S0=None, kt=A, o=A, Sout=A, dout=A, B=2, T=128,
+             H=2, K=128, V=128, C=64, eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6, scale=1.0, ba=1)
+    a.update(kw)
+    return L.osdn_layer_fwd(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a["d0"], a["S0"], a["kt"],
+                            a["o"], a["Sout"], a["dout"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"],
+                            a["eta"], a["dmin"], a["dmax"], a["eps"], a["scale"], a["ba"], a.get("ws"),
+                            a.get("wsb", 0), None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(kt=None), ARG), (dict(dout=None), ARG), (dict(Sout=None), ARG), (dict(o=None), ARG),
+    (dict(q=A + 2), ALIGN), (dict(ws=A + 8, wsb=1 << 20), ALIGN), (dict(K=96), UNSUP), (dict(C=32), UNSUP),
+    (dict(T=100), SHAPE), (dict(dt=5), DTYPE), (dict(eta=-1.0), ARG), (dict(scale=math.inf), ARG),
+    (dict(B=0), OK),
+])
+def test_layer_validation(L, kw, want):
+    assert layer(L, **kw) == want
+
+
+def test_layer_workspace_size_query(L):
+    f = L.osdn_layer_fwd_workspace_bytes
+    scan = 4 * 8 * 8 * (2048 + 32 * 256)
+    chunk = 8 * 8 * 32 * 32768
+    got = f(8, 2048, 8, 128, 128, 64, 1)
+    assert got >= scan + chunk + 8 * 8 * 32 * 4   # both workspaces, the block flags and a counter
+    assert got < scan + chunk + 8 * 8 * 32 * 4 + 1024
+    assert f(1, 64, 1, 64, 64, 64, 0) == 0        # fp32, K = 64: no workspace is used
+    assert f(1, 100, 1, 128, 128, 64, 1) == 0     # T not a multiple of the chunk
