@@ -1229,16 +1229,20 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        unsigned char* __restrict__ cws, int N, int BH) {
     extern __shared__ unsigned char smem_raw[];
-    if (static_cast<int>(blockIdx.x) < BH) {
-        scanblk::scan_block_body<TIn, TIn, HAS_R>(sa, ws_g, ws_d, blockIdx.x, smem_raw, &g_timeout_flag, flags);
-        return;
-    }
-    unsigned char* base = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
-    const int T = sa.T, H = sa.H;
     __shared__ uint32_t s_tmem;
     __shared__ int s_q[2];
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), 2 * prep::TMEM_COLS);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = s_tmem;
+    // phase 1 for one (batch, head); afterwards this CTA joins the prep workers
+    if (static_cast<int>(blockIdx.x) < BH)
+        scanblk::scan_block_body<TIn, TIn, HAS_R>(sa, ws_g, ws_d, blockIdx.x, smem_raw, tbase, &g_timeout_flag, flags);
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int T = sa.T, H = sa.H;
     PrepWorker<TIn> pw;
     pw.init(base + w * prep::REGION, wt, 1 + w);
     if (tid == 0) {
@@ -1246,11 +1250,7 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
         tc::prefetch_tmap(&tmK);
     }
     __syncthreads();
-    if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), 2 * prep::TMEM_COLS);
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    pw.tbase = s_tmem + w * prep::TMEM_COLS;
+    pw.tbase = tbase + w * prep::TMEM_COLS;
     const int total = BH * N;
     TIn* kto = static_cast<TIn*>(sa.k_tilde);
     bool aborted = false;
@@ -1281,7 +1281,7 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(s_tmem, 2 * prep::TMEM_COLS);
+    if (warp == 0) tc::tmem_dealloc(tbase, 2 * prep::TMEM_COLS);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -43,7 +43,14 @@ __device__ unsigned int g_scan_timeout_flag = 0;
 template <typename TIn, typename TOut, bool HAS_R>
 __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float* ws_g, float* ws_d) {
     extern __shared__ unsigned char smem_raw[];
-    scan_block_body<TIn, TOut, HAS_R>(a, ws_g, ws_d, blockIdx.x, smem_raw, &g_scan_timeout_flag, nullptr);
+    __shared__ uint32_t s_tmem;
+    if (threadIdx.x < 32) tc::tmem_alloc(tc::smem_u32(&s_tmem), TMEM_COLS);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = s_tmem;
+    scan_block_body<TIn, TOut, HAS_R>(a, ws_g, ws_d, blockIdx.x, smem_raw, tbase, &g_scan_timeout_flag, nullptr);
+    if (threadIdx.x < 32) tc::tmem_dealloc(tbase, TMEM_COLS);
 }
 
 // Write keys of one 64-token block of one head, EC key coordinates per CTA: thread i replays

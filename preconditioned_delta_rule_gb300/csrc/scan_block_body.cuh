@@ -177,13 +177,15 @@ __device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) 
 }
 
 // The body of the blocked scan for one (batch, head) `bh`, run by 256 threads of a CTA whose
-// dynamic shared memory starts at smem_raw (SMEM_ALLOC bytes).  A bounded wait that gives up sets
-// *timeout_flag.  With blk_flags != nullptr, blk_flags[bh * nblk + m] is set to 1 (release, GPU
+// dynamic shared memory starts at smem_raw (SMEM_ALLOC bytes) and which holds TMEM_COLS columns
+// of tensor memory at `tbase` (allocated and released by the caller).  On return no asynchronous
+// operation of the body is in flight and its mbarriers are retired, so the caller may reuse the
+// shared and tensor memory.  A bounded wait that gives up sets *timeout_flag.  With blk_flags != nullptr, blk_flags[bh * nblk + m] is set to 1 (release, GPU
 // scope) once the step sizes and the start state of block m are in the workspace.
 template <typename TIn, typename TOut, bool HAS_R>
 __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws_g, float* ws_d, int bh,
-                                                unsigned char* smem_raw, unsigned int* timeout_flag,
-                                                unsigned int* blk_flags) {
+                                                unsigned char* smem_raw, uint32_t tbase,
+                                                unsigned int* timeout_flag, unsigned int* blk_flags) {
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float* F = reinterpret_cast<float*>(sm + OFF_F);
@@ -197,7 +199,6 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
     const int nblk = (T + J - 1) / J;
     const uint32_t sbase = tc::smem_u32(sm);
     const uint32_t bars = sbase + OFF_BAR;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + B_TMEM);
     const float eta = a.eta, dmin = a.d_min, dmax = a.d_max, eps = a.eps;
     __shared__ int s_abort;
     __shared__ int s_grams_issued, s_grams_used;  // all-free Grams issued by warpgroup 1 / consumed
@@ -216,11 +217,6 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
         s_grams_used = 0;
     }
     __syncthreads();
-    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tbase = *tmem_slot;
     const uint32_t idg = tc::idesc_f16_f32(128, J, false, false);
 
     // Gram of the s copies in slot q (three fp16 products: hi.hi + hi.lo + lo.hi) -> TMEM col
@@ -747,7 +743,16 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+    if (tid == 0) {
+        for (int q = 0; q < 2; ++q) {
+            tc::mbar_inval(bars + B_GRAM + 8 * q);
+            tc::mbar_inval(bars + B_PREP + 8 * q);
+            tc::mbar_inval(bars + B_CHAIN + 8 * q);
+        }
+        tc::mbar_inval(bars + B_GM);
+        tc::mbar_inval(bars + B_MRDY);
+    }
+    __syncthreads();
 }
 
 }  // namespace scanblk
