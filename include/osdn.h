@@ -3,7 +3,7 @@
  *
  * OSDN ("OSDN: Improving Delta Rule with Provable Online Preconditioning in Linear Attention",
  * arXiv:2605.13473) is the delta rule with a diagonal, online-learned right preconditioner d on
- * the write side.  The forward path has three calls:
+ * the write side.  The forward path has three calls, and a fourth that chains the first two:
  *
  *   osdn_precond_scan  phase 1 (Section 4.2, Algorithm 1, Eq. (4); APF retention Eq. (7)):
  *                      per (batch, head), for t = 0..T-1:
@@ -19,6 +19,8 @@
  *                      computed chunkwise (WY/UT form) with an fp32 state.
  *   osdn_decode_step   one token of both phases in place on (S, d): the recurrent form used at
  *                      generation time (the pages' single-token kernel, Appendix L).
+ *   osdn_layer_fwd     osdn_precond_scan then osdn_chunk_fwd on its write keys (the pages'
+ *                      chunk_osdn, Listing 1), with the two phases overlapped on the GPU.
  *
  * Conventions shared by every call
  *   - Every buffer is caller-owned DEVICE memory (cudaMalloc or equivalent); the library never

@@ -502,6 +502,20 @@ __device__ __forceinline__ bool bar_and128(int bar, bool pred) {
 // loaded: phase 1's clipped recurrence replayed per key coordinate from the chunk's start state
 // with the step sizes the scan fixed, k~_t = d_t k_t (the same arithmetic as the emission
 // kernel), and written out as well.
+// A workspace word written concurrently by another CTA: the workspace is filled with all-ones
+// before the launch and the writer never stores that pattern, so the first load that differs is
+// the value.  Relaxed GPU-scope loads (not cached in L1); bounded, clears `ok` on giving up.
+__device__ __forceinline__ float poll_word(const float* p, bool& ok) {
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+        uint32_t v;
+        asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+        if (v != 0xffffffffu) return __uint_as_float(v);
+        __nanosleep(64);
+    }
+    ok = false;
+    return 0.f;
+}
+
 template <typename TIn>
 struct PrepWorker {
     static constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
@@ -558,16 +572,17 @@ struct PrepWorker {
         }
         tma_pending = true;
         if (tid < C) sbeta[tid] = beta[(static_cast<size_t>(row) + tid) * H + h];
-        if (EMIT) {
+        bool ready = true;
+        if (EMIT) {  // the scan may still be writing these: poll until they are there (bounded)
             if (tid < C) {
-                semit[tid] = g_src[tid];
+                semit[tid] = poll_word(g_src + tid, ready);
                 semit[C + tid] = r_src ? r_src[static_cast<size_t>(tid) * H] : 1.f;
             }
-            semit[2 * C + tid] = d_src[tid];
-            semit[2 * C + KD + tid] = d_src[KD + tid];
+            semit[2 * C + tid] = poll_word(d_src + tid, ready);
+            semit[2 * C + KD + tid] = poll_word(d_src + KD + tid, ready);
         }
         {
-            const bool ok = tc::mbar_wait(bar_tma, tph, kMaxPolls);
+            const bool ok = tc::mbar_wait(bar_tma, tph, kMaxPolls) && ready;
             if (!bar_and128(bar, ok)) return false;
             tph ^= 1u;
             tma_pending = false;
@@ -1206,26 +1221,18 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
 // =============================================================================================
 // Fused layer forward: phase 1 and the S-independent part of phase 2 in one cooperative launch.
-// CTAs 0 .. BH-1 run the blocked scan of one (batch, head) each and publish every 64-token block
-// (its step sizes and start state) through a flag; every other CTA runs two prep workers that
-// take chunks in block-major order from a counter, wait for their block's flag (bounded), form
-// the chunk's write keys from the published values and do the chunk prep.  Phase 1 keeps 64 SMs
-// busy for its whole duration, so the prep of each chunk hides behind the scan of later blocks.
-// All CTAs are resident at once (cooperative launch), so the waits always end.
+// CTAs 0 .. BH-1 run the blocked scan of one (batch, head) each and store every 64-token block's
+// step sizes and start state to the workspace as soon as it is solved; every other CTA runs two
+// prep workers that take chunks in block-major order from a counter, poll (bounded) for their
+// block's values, form the chunk's write keys from them and do the chunk prep.  Phase 1 keeps B*H
+// SMs busy for its whole duration, so the prep of each chunk hides behind the scan of later
+// blocks.  All CTAs are resident at once (cooperative launch), so the waits always end.  The
+// workspace's scan part and the counter hold all-ones at launch (the counter's first increment
+// wraps it to chunk 0).
 // =============================================================================================
-__device__ __forceinline__ bool wait_flag(const unsigned int* p) {
-    for (uint32_t i = 0; i < kMaxPolls; ++i) {
-        unsigned int v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-        if (v != 0u) return true;
-        __nanosleep(64);
-    }
-    return false;
-}
-
 template <typename TIn, bool HAS_R>
 __global__ void __launch_bounds__(256, 1)
-layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* flags, unsigned int* counter,
+layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* counter,
                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        unsigned char* __restrict__ cws, int N, int BH) {
     extern __shared__ unsigned char smem_raw[];
@@ -1239,7 +1246,7 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
     const uint32_t tbase = s_tmem;
     // phase 1 for one (batch, head); afterwards this CTA joins the prep workers
     if (static_cast<int>(blockIdx.x) < BH)
-        scanblk::scan_block_body<TIn, TIn, HAS_R>(sa, ws_g, ws_d, blockIdx.x, smem_raw, tbase, &g_timeout_flag, flags);
+        scanblk::scan_block_body<TIn, TIn, HAS_R>(sa, ws_g, ws_d, blockIdx.x, smem_raw, tbase, &g_timeout_flag);
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int T = sa.T, H = sa.H;
@@ -1255,17 +1262,11 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
     TIn* kto = static_cast<TIn*>(sa.k_tilde);
     bool aborted = false;
     for (;;) {
-        if (wt == 0) s_q[w] = static_cast<int>(atomicAdd(counter, 1u));
+        if (wt == 0) s_q[w] = static_cast<int>(atomicAdd(counter, 1u) + 1u);
         bar_sync128(1 + w);
         const int q = s_q[w];
         if (q >= total) break;
         const int m = q / BH, bh = q - m * BH, b = bh / H, h = bh - b * H;
-        bool ok = true;
-        if (wt == 0) ok = wait_flag(flags + static_cast<size_t>(bh) * N + m);
-        if (!bar_and128(1 + w, ok)) {  // the acquire above and this barrier order the reads below
-            aborted = true;
-            break;
-        }
         const size_t row0 = static_cast<size_t>(b) * T * H + h;
         const float* g_src = ws_g + static_cast<size_t>(bh) * T + m * C;
         const float* r_src = HAS_R ? sa.r + row0 + static_cast<size_t>(m) * C * H : nullptr;
@@ -1376,20 +1377,19 @@ bool tc_covers(const OsdnChunkArgs& a) {
            (a.dtype == OSDN_BF16 || a.dtype == OSDN_F16);
 }
 
-// Workspace of the fused layer: [scan: step sizes, block-start states][chunk images][block flags]
-// [chunk counter], each part 256-byte aligned.
+// Workspace of the fused layer: [scan: step sizes, block-start states][chunk counter][chunk
+// images], each part 256-byte aligned.
 struct LayerWs {
-    size_t scan, chunk, flags, counter, total;
+    size_t scan, counter, chunk, total;
 };
 LayerWs layer_ws(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     LayerWs l{};
     const size_t nblk = static_cast<size_t>(ca.T / C);
     l.scan = 0;
-    l.chunk = up(osdn_scan_block_workspace_bytes(sa));
-    l.flags = l.chunk + up(static_cast<size_t>(ca.B) * ca.H * nblk * WS_CHUNK);
-    l.counter = l.flags + up(static_cast<size_t>(ca.B) * ca.H * nblk * 4);
-    l.total = l.counter + 256;
+    l.counter = up(osdn_scan_block_workspace_bytes(sa));
+    l.chunk = l.counter + 256;
+    l.total = l.chunk + up(static_cast<size_t>(ca.B) * ca.H * nblk * WS_CHUNK);
     return l;
 }
 
@@ -1419,16 +1419,16 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     const int grid = per_sm * num_sms();
     if (grid <= ca.B * ca.H) return cudaErrorNotSupported;
     const LayerWs l = layer_ws(sa, ca);
-    cudaError_t e = cudaMemsetAsync(ws + l.flags, 0, l.total - l.flags, s);
+    // all-ones over the scan part (nothing published yet) and the counter
+    cudaError_t e = cudaMemsetAsync(ws + l.scan, 0xff, l.counter + 4 - l.scan, s);
     if (e != cudaSuccess) return e;
     OsdnScanArgs sa2 = sa;
     float* ws_g = reinterpret_cast<float*>(ws + l.scan);
     float* ws_d = ws_g + static_cast<size_t>(sa.B) * sa.H * sa.T;
-    unsigned int* flags = reinterpret_cast<unsigned int*>(ws + l.flags);
     unsigned int* counter = reinterpret_cast<unsigned int*>(ws + l.counter);
     unsigned char* cws = ws + l.chunk;
     int N = ca.T / C, BH = ca.B * ca.H;
-    void* args[] = {&sa2, &ws_g, &ws_d, &flags, &counter, &mq, &mk, &cws, &N, &BH};
+    void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &cws, &N, &BH};
     e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
                                     dim3(256), args, smem, s);
     if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer resident CTAs than expected: two calls
@@ -1437,7 +1437,7 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     }
     if (e != cudaSuccess) return e;
     // the serial chain over the chunk images (same kernel as osdn_chunk_fwd's workspace path)
-    return launch_tc<TIn>(ca, cws, l.total, s, /*chain_only=*/true);
+    return launch_tc<TIn>(ca, cws, l.total - l.chunk, s, /*chain_only=*/true);
 }
 
 }  // namespace

@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tbase = s_tmem;
-    scan_block_body<TIn, TOut, HAS_R>(a, ws_g, ws_d, blockIdx.x, smem_raw, tbase, &g_scan_timeout_flag, nullptr);
+    scan_block_body<TIn, TOut, HAS_R>(a, ws_g, ws_d, blockIdx.x, smem_raw, tbase, &g_scan_timeout_flag);
     if (threadIdx.x < 32) tc::tmem_dealloc(tbase, TMEM_COLS);
 }
 

@@ -24,10 +24,13 @@
 // reassociation.  d is carried across blocks as an unevaluated fp32 pair (hi + lo).
 //
 // Mapping: one CTA of 256 threads per (batch, head).  Warpgroup 0 ("chain") runs the serial part
-// above, one key coordinate per thread.  Warpgroup 1 prepares block b+1 (cp.async staging of the
-// keys three blocks ahead, s = k.k in fp32, power-of-two-scaled fp16 hi/lo copies and the Gram on
-// the tensor cores) and emits the write keys of block b by replaying the clipped recurrence with
-// the chain's g values.  The warpgroups hand blocks over through mbarriers.
+// above, one key coordinate per thread, reading s = k.k straight from the staged keys (the square
+// of a 16-bit key is exact in fp32).  Warpgroup 1 prepares block b+1 (cp.async staging of the keys
+// three blocks ahead, the norms |k_t|^2 and gates, power-of-two-scaled fp16 hi/lo copies of s and
+// the Gram on the tensor cores, copied to shared memory as the chain's Jacobi rows), writes the
+// step sizes and start state of block b to the workspace when there is one, and otherwise emits
+// the write keys of block b by replaying the clipped recurrence with the chain's g values.  The
+// warpgroups hand blocks over through mbarriers.
 
 #pragma once
 #include <type_traits>
@@ -44,17 +47,22 @@ constexpr int J = 64;              // tokens per block
 constexpr int KD = 128;            // key dim (one coordinate per thread of each warpgroup)
 constexpr int NT = 256;
 constexpr int KROW = KD * 2 + 16;  // padded raw key row (16-bit elements), bytes
-constexpr int SROW = KD + 8;       // padded fp32 s row, floats
 constexpr uint32_t kMaxPolls = 1u << 22;
 constexpr int kMaxRestarts = 8;
 
 constexpr uint32_t OFF_KT = 0;                             // 3 raw key tiles
 constexpr uint32_t KT_BYTES = J * KROW;                    // 17408
-constexpr uint32_t OFF_SF = 53248;                         // 2 fp32 s tiles
-constexpr uint32_t SF_BYTES = J * SROW * 4;                // 34816
-constexpr uint32_t OFF_SH = OFF_SF + 2 * SF_BYTES;         // 122880: 2 x s_hi (fp16, SW128)
-constexpr uint32_t OFF_SL = OFF_SH + 2 * 16384;            // 2 x s_lo
-constexpr uint32_t OFF_F = OFF_SL + 2 * 16384;             // fp32 scratch
+// Two slots of fp16 copies of s = k.k scaled by a power of two, 128-byte swizzled.  Per key block
+// (coordinates 0-63, 64-127) the 64 hi rows are followed by the 64 lo rows, so that one N = 128
+// operand holds [hi; lo].
+constexpr uint32_t OFF_SHL = 53248;
+constexpr uint32_t SHL_SLOT = 32768, SHL_KB = 16384, SHL_LO = 8192;
+// Two slots of s = k.k in fp32 (rows of SROW floats) for the chain.  SROW = 132: row j's 16-byte
+// piece c sits in bank group (j + c) mod 8, which the chain's two-threads-per-row reads keep apart.
+constexpr int SROW = KD + 4;
+constexpr uint32_t OFF_SF = OFF_SHL + 2 * SHL_SLOT;
+constexpr uint32_t SF_BYTES = J * SROW * 4;                // 33792
+constexpr uint32_t OFF_F = OFF_SF + 2 * SF_BYTES;          // fp32 scratch
 constexpr int F_GAM = 0;              // [2][64] gamma of the block in a slot
 constexpr int F_BP = F_GAM + 128;     // [2][64] feedback beta
 constexpr int F_RR = F_BP + 128;      // [2][64] retention (1 past the end of the sequence)
@@ -63,8 +71,8 @@ constexpr int F_RAWR = F_RAWB + 192;  // [3][64] cp.async destination for r
 constexpr int F_SIGS = F_RAWR + 192;  // [2] power-of-two scale of the fp16 s copies
 constexpr int F_RHO = F_SIGS + 4;     // [65] (chain)
 constexpr int F_G = F_RHO + 68;       // [64] g of the current sub-block (chain)
-constexpr int F_H = F_G + 64;         // [64]
-constexpr int F_CF = F_H + 64;        // [64]
+constexpr int F_H = F_G + 64;         // [2][64] h = g / rho, double-buffered across Jacobi sweeps
+constexpr int F_CF = F_H + 128;       // [64]
 constexpr int F_CP = F_CF + 64;       // [64]
 constexpr int F_DF = F_CP + 64;       // [128] d of free coordinates (0 if pinned)
 constexpr int F_BPV = F_DF + 128;     // [128] bound of pinned coordinates (0 if free)
@@ -72,30 +80,29 @@ constexpr int F_RED = F_BPV + 128;    // [8] chain reductions
 constexpr int F_RED1 = F_RED + 8;     // [8] prep reductions
 constexpr int F_INT = F_RED1 + 8;     // [8] int scratch (chain)
 constexpr int F_GOUT = F_INT + 8;     // [2][64] final g of each token of a block (chain -> emit)
-constexpr int F_DST = F_GOUT + 128;   // [2][128] state at the block start (chain -> emit)
-constexpr int F_END = F_DST + 256;
+constexpr int F_DST = F_GOUT + 128;   // [2][128] state at the block start, hi part (chain -> emit)
+constexpr int F_DSL = F_DST + 256;    // [2][128] state at the block start, lo part
+constexpr int F_NU = F_DSL + 256;     // [2][2] coupling bound of the block in a slot (per copy warp)
+constexpr int F_END = F_NU + 4;
 constexpr uint32_t OFF_BAR = OFF_F + ((F_END * 4 + 127) / 128) * 128;
-// An M = 128 tcgen05.mma reads 128 rows (16 KB) of its A operand even though only the first 64
-// rows are used; the last A window (s_lo, slot 1, second key block) must stay inside the
-// allocation, so the used size is at least OFF_SL + 2 * 16384 + 8192.
-constexpr uint32_t SMEM_BASE = (OFF_BAR + 128 > OFF_SL + 2 * 16384 + 8192) ? OFF_BAR + 128
-                                                                            : OFF_SL + 2 * 16384 + 8192;
-// the all-free Gram of the current block, scaled and masked to l < j, fp32 rows of MROW floats
+constexpr uint32_t SMEM_BASE = OFF_BAR + 128;
+// the all-free Gram of a block (two slots), scaled and masked to l < j, fp32 rows of MROW floats
 constexpr int MROW = J + 4;
+constexpr uint32_t MT_BYTES = J * MROW * 4;
 constexpr uint32_t OFF_MT = ((SMEM_BASE + 127) / 128) * 128;
-constexpr uint32_t SMEM_USED = OFF_MT + J * MROW * 4;
+constexpr uint32_t SMEM_USED = OFF_MT + 2 * MT_BYTES;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-static_assert(3 * KT_BYTES <= OFF_SF, "key tiles");
-static_assert(OFF_SH % 1024 == 0 && OFF_SL % 1024 == 0, "swizzle atoms");
+static_assert(3 * KT_BYTES <= OFF_SHL, "key tiles");
+static_assert(OFF_SHL % 1024 == 0, "swizzle atoms");
 static_assert(SMEM_ALLOC <= 232448, "shared memory");
 
 constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t COL_G = 0;     // all-free Gram of the block in slot 0 / 1: columns 0 / 64
-constexpr uint32_t COL_GM = 128;  // masked Gram computed by the chain
+constexpr uint32_t COL_G = 0;     // all-free Gram products of the block being prepared (128 columns)
+constexpr uint32_t COL_GM = 128;  // masked Gram products computed by the chain (128 columns)
 
-// mbarriers (offsets from OFF_BAR): gram[2], prep_ready[2], chain_done[2], gram_masked, tmem slot,
-// Gram rows in shared memory
-constexpr uint32_t B_GRAM = 0, B_PREP = 16, B_CHAIN = 32, B_GM = 48, B_TMEM = 56, B_MRDY = 64;
+// mbarriers (offsets from OFF_BAR): gram[2], prep_ready[2], chain_done[2], gram_masked, Gram rows
+// in shared memory[2]
+constexpr uint32_t B_GRAM = 0, B_PREP = 16, B_CHAIN = 32, B_GM = 48, B_MRDY = 56;
 
 __device__ __forceinline__ void cp_async_16z(void* smem, const void* gmem, bool valid) {
     const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
@@ -172,20 +179,18 @@ __device__ __forceinline__ float chain_sum(float v, float* red, int tid) {
     return (red[0] + red[1]) + (red[2] + red[3]);
 }
 
-__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
-}
-
 // The body of the blocked scan for one (batch, head) `bh`, run by 256 threads of a CTA whose
 // dynamic shared memory starts at smem_raw (SMEM_ALLOC bytes) and which holds TMEM_COLS columns
 // of tensor memory at `tbase` (allocated and released by the caller).  On return no asynchronous
 // operation of the body is in flight and its mbarriers are retired, so the caller may reuse the
-// shared and tensor memory.  A bounded wait that gives up sets *timeout_flag.  With blk_flags != nullptr, blk_flags[bh * nblk + m] is set to 1 (release, GPU
-// scope) once the step sizes and the start state of block m are in the workspace.
+// shared and tensor memory.  A bounded wait that gives up sets *timeout_flag.  With a workspace
+// (ws_g, ws_d) the step sizes and start state of every block are stored there as soon as the
+// block is solved, each word with one relaxed GPU-scope store and never with the all-ones bit
+// pattern, so a consumer running concurrently may poll for them.
 template <typename TIn, typename TOut, bool HAS_R>
 __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws_g, float* ws_d, int bh,
                                                 unsigned char* smem_raw, uint32_t tbase,
-                                                unsigned int* timeout_flag, unsigned int* blk_flags) {
+                                                unsigned int* timeout_flag) {
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float* F = reinterpret_cast<float*>(sm + OFF_F);
@@ -211,28 +216,51 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
         }
         tc::mbar_init(bars + B_GM, 1);
         tc::mbar_init(bars + B_MRDY, 2);
+        tc::mbar_init(bars + B_MRDY + 8, 2);
         tc::mbar_init_fence();
         s_abort = 0;
         s_grams_issued = 0;
         s_grams_used = 0;
     }
     __syncthreads();
-    const uint32_t idg = tc::idesc_f16_f32(128, J, false, false);
+    const uint32_t id128 = tc::idesc_f16_f32(128, 2 * J, false, false);
+    const uint32_t id64 = tc::idesc_f16_f32(128, J, false, false);
 
-    // Gram of the s copies in slot q (three fp16 products: hi.hi + hi.lo + lo.hi) -> TMEM col
-    auto issue_gram = [&](int q, uint32_t col, uint32_t bar) {
-        const uint32_t sh = sbase + OFF_SH + q * 16384, sl = sbase + OFF_SL + q * 16384;
-        const uint32_t aa[3] = {sh, sh, sl}, bb[3] = {sh, sl, sh};
+    // Gram products of the s copies in slot q into the 128 TMEM columns at `col`:
+    // [hi; lo].[hi; lo]^T (M = N = 128), i.e. lanes 0-63 hold hi.hi^T | hi.lo^T and lanes 64-127
+    // hold lo.hi^T | lo.lo^T, so row j of the Gram is M_j = D_j[0:64] + D_j[64:128] + D_{64+j}[0:64]
+    // (lo.lo^T is below fp32 rounding).  With `lanes_local`, lo.hi^T is accumulated onto the
+    // first 64 columns of lanes 0-63 as well (8 more products), so that M_j = D_j[0:64] + D_j[64:128]
+    // needs no other lane; the extra A window's rows 64-127 land in lanes the readers ignore.
+    auto issue_gram = [&](int q, uint32_t col, uint32_t bar, bool lanes_local) {
+        const uint32_t base = sbase + OFF_SHL + q * SHL_SLOT;
         tc::tc_fence_after();
 #pragma unroll
-        for (int v = 0; v < 3; ++v)
+        for (int st = 0; st < KD / 16; ++st) {
+            const uint64_t d = tc::sdesc_sw128(base + (st >> 2) * SHL_KB + (st & 3) * 32, 16, 1024);
+            tc::mma_f16(tbase + col, d, d, id128, st > 0 ? 1u : 0u);
+        }
+        if (lanes_local) {
 #pragma unroll
             for (int st = 0; st < KD / 16; ++st) {
-                const uint64_t ad = tc::sdesc_sw128(aa[v] + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
-                const uint64_t bd = tc::sdesc_sw128(bb[v] + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
-                tc::mma_f16(tbase + col, ad, bd, idg, (v > 0 || st > 0) ? 1u : 0u);
+                const uint32_t a = base + (st >> 2) * SHL_KB + (st & 3) * 32;
+                tc::mma_f16(tbase + col, tc::sdesc_sw128(a + SHL_LO, 16, 1024), tc::sdesc_sw128(a, 16, 1024), id64, 1u);
             }
+        }
         tc::mma_commit(bar);
+    };
+    // row j of the Gram of the products at `col` (lanes 0-63 only), scaled by 1 / sig^2 and masked
+    // to l < j; `lane_base` selects the calling warp's lanes
+    auto load_gram_row = [&](uint32_t col, uint32_t lane_base, int j, float inv_sig2, float (&mrow)[64]) {
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
+            float x[32], y[32];
+            tc::tmem_ld32(tbase + lane_base + col + hv * 32, x);
+            tc::tmem_ld32(tbase + lane_base + col + 64 + hv * 32, y);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int l = 0; l < 32; ++l) mrow[hv * 32 + l] = (hv * 32 + l < j) ? (x[l] + y[l]) * inv_sig2 : 0.f;
+        }
     };
 
     if (warp >= 4) {
@@ -299,8 +327,8 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             if (bmax > 0.f) frexpf(bmax, &ex);
             const float sig = bmax > 0.f ? ldexpf(1.f, 14 - ex) : 1.f;  // max s * sig < 2^14
             if (u == 0) F[F_SIGS + (m & 1)] = sig;
-            unsigned char* sh = sm + OFF_SH + (m & 1) * 16384 + hf * 8192;
-            unsigned char* sl = sm + OFF_SL + (m & 1) * 16384 + hf * 8192;
+            unsigned char* sh = sm + OFF_SHL + (m & 1) * SHL_SLOT + hf * SHL_KB;
+            unsigned char* sl = sh + SHL_LO;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 float hi[8], lo[8];
@@ -317,40 +345,94 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             }
             tc::fence_proxy_async();
             wg_sync(2);
-            if (u == 0) {
-                issue_gram(m & 1, COL_G + (m & 1) * 64, bars + B_GRAM + 8 * (m & 1));
+            // the chain starts the block on s and the gates; it waits for the Gram rows separately.
+            // The Gram is issued from warp 6: warps 4-5 copy its rows out of tensor memory.
+            mbar_arrive(bars + B_PREP + 8 * (m & 1));
+            if (u == 2 * 32) {
+                issue_gram(m & 1, COL_G, bars + B_GRAM + 8 * (m & 1), false);
                 s_grams_issued = m + 1;
             }
-            mbar_arrive(bars + B_PREP + 8 * (m & 1));
         };
 
-        // Gram of block m, tensor memory -> shared memory (rows 0-63: warps 4-5), scaled back by
-        // 1 / sig^2 (exact: powers of two) and masked to l < j, for the chain's Jacobi rows
-        float* mt = reinterpret_cast<float*>(sm + OFF_MT);
+        // Gram of block m, tensor memory -> shared memory slot m & 1 (warps 4-5, one row per
+        // thread), scaled back by 1 / sig^2 (exact: powers of two) and masked to l < j, for the
+        // chain's Jacobi rows
         auto copy_gram = [&](int m) {
-            if (u >= J) return;
             const bool okg = tc::mbar_wait(bars + B_GRAM + 8 * (m & 1), (m >> 1) & 1, kMaxPolls);
-            if (!__all_sync(0xffffffffu, okg)) {
+            if (wg_count(2, okg) != 128) {  // uniform decision across the warpgroup
                 atomicExch(&s_abort, 1);
                 return;
             }
             if (u == 0) s_grams_used = m + 1;
             tc::tc_fence_after();
-            const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            float g[64];
-            tc::tmem_ld32(tbase + lane_base + COL_G + (m & 1) * 64, *reinterpret_cast<float(*)[32]>(g));
-            tc::tmem_ld32(tbase + lane_base + COL_G + (m & 1) * 64 + 32, *reinterpret_cast<float(*)[32]>(g + 32));
-            tc::tmem_ld_wait();
-            const float isg = 1.f / F[F_SIGS + (m & 1)];
-            const float inv_sig2 = isg * isg;
+            const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            float* mt = reinterpret_cast<float*>(sm + OFF_MT + (m & 1) * MT_BYTES);
+            if (u >= J) {  // warps 6-7: the lo.hi^T rows (lanes 64-127), raw, into the row tile
 #pragma unroll
-            for (int l = 0; l < 64; l += 4)
-                *reinterpret_cast<float4*>(mt + u * MROW + l) =
-                    make_float4(l < u ? g[l] * inv_sig2 : 0.f, l + 1 < u ? g[l + 1] * inv_sig2 : 0.f,
-                                l + 2 < u ? g[l + 2] * inv_sig2 : 0.f, l + 3 < u ? g[l + 3] * inv_sig2 : 0.f);
-            tc::tc_fence_before();
-            __syncwarp();
-            if ((u & 31) == 0) mbar_arrive(bars + B_MRDY);
+                for (int hv = 0; hv < 2; ++hv) {
+                    float x[32];
+                    tc::tmem_ld32(tbase + lb + COL_G + hv * 32, x);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int l = 0; l < 32; l += 4)
+                        *reinterpret_cast<float4*>(mt + (u - J) * MROW + hv * 32 + l) = make_float4(x[l], x[l + 1], x[l + 2], x[l + 3]);
+                }
+                tc::tc_fence_before();
+            }
+            wg_sync(2);
+            if (u < J) {  // warps 4-5: row u = hi.hi^T + hi.lo^T (lanes 0-63) + the parked lo.hi^T
+                const float isg = 1.f / F[F_SIGS + (m & 1)];
+                const float inv_sig2 = isg * isg;
+                float* row = mt + u * MROW;
+                // coupling bound of the block's system: max_j |gamma_j b_j| sum_l M_jl (M >= 0);
+                // infinite when it is not finite or a retention gate exceeds 1
+                float r4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int hv = 0; hv < 2; ++hv) {
+                    float x[32], y[32];
+                    tc::tmem_ld32(tbase + lb + COL_G + hv * 32, x);
+                    tc::tmem_ld32(tbase + lb + COL_G + 64 + hv * 32, y);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int l = 0; l < 32; l += 4) {
+                        float4 z = *reinterpret_cast<const float4*>(row + hv * 32 + l);
+                        float* zz = reinterpret_cast<float*>(&z);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = hv * 32 + l + e;
+                            zz[e] = c < u ? ((x[l + e] + y[l + e]) + zz[e]) * inv_sig2 : 0.f;
+                            r4[e] += zz[e];
+                        }
+                        *reinterpret_cast<float4*>(row + hv * 32 + l) = z;
+                    }
+                }
+                tc::tc_fence_before();
+                float t = fabsf(F[F_GAM + (m & 1) * J + u] * F[F_BP + (m & 1) * J + u]) * ((r4[0] + r4[1]) + (r4[2] + r4[3]));
+                if (!(t <= 3.0e38f) || (HAS_R && F[F_RR + (m & 1) * J + u] > 1.f)) t = INFINITY;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+                if ((u & 31) == 0) F[F_NU + 2 * (m & 1) + (u >> 5)] = t;
+                __syncwarp();
+                if ((u & 31) == 0) mbar_arrive(bars + B_MRDY + 8 * (m & 1));
+            }
+        };
+        // step sizes and start state of block m to the workspace (warps 6-7).  A reader in
+        // another CTA polls each word until it differs from the all-ones pattern the workspace
+        // was filled with, so no fence or flag is needed; a value with that pattern (a NaN) is
+        // written as the canonical NaN.
+        auto publish = [&](int m) {
+            const int v = u - J, q = m & 1;
+            auto put = [](float* p, float x) {
+                uint32_t w = __float_as_uint(x);
+                if (w == 0xffffffffu) w = 0x7fffffffu;
+                asm volatile("st.relaxed.gpu.global.b32 [%0], %1;\n" ::"l"(p), "r"(w) : "memory");
+            };
+            if (m * J + v < T) put(ws_g + static_cast<size_t>(bh) * T + m * J + v, F[F_GOUT + q * J + v]);
+            float* wd = ws_d + (static_cast<size_t>(bh) * nblk + m) * (2 * KD);
+            put(wd + v, F[F_DST + q * KD + v]);
+            put(wd + v + 64, F[F_DST + q * KD + v + 64]);
+            put(wd + KD + v, F[F_DSL + q * KD + v]);
+            put(wd + KD + v + 64, F[F_DSL + q * KD + v + 64]);
         };
 
         stage(0);
@@ -366,21 +448,22 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             if (m + 1 < nblk) {
                 cp_async_wait<1>();  // groups 0..m+2 committed; block m+1's has landed
                 wg_sync(2);
-                prepare(m + 1);
+                prepare(m + 1);  // slot (m + 1) & 1: the chain finished block m - 1 with it
+                copy_gram(m + 1);
             }
-            // emit block m once the chain has fixed its g values
+            // block m once the chain has fixed its g values
             const bool ok = tc::mbar_wait(bars + B_CHAIN + 8 * (m & 1), (m >> 1) & 1, kMaxPolls);
             const bool bad = !ok || *static_cast<volatile int*>(&s_abort);
             if (wg_count(2, bad) != 0) {  // uniform decision across the warpgroup
                 atomicExch(&s_abort, 1);
                 break;
             }
-            if (m + 1 < nblk) copy_gram(m + 1);  // the chain is done with the Gram rows of block m
+            if (ws_g != nullptr && u >= J) publish(m);
             if (ws_g == nullptr) {  // emit here; with a workspace scan_emit_kernel does it
                 const int q = m & 1;
                 const unsigned char* kt = sm + OFF_KT + (m % 3) * KT_BYTES;
                 const int t0 = m * J, jb = min(J, T - t0);
-                float d = F[F_DST + q * KD + u];
+                float d = F[F_DST + q * KD + u] + F[F_DSL + q * KD + u];
                 TOut* out = ktg + (row0 + static_cast<size_t>(t0) * H) * KD + u;
                 const size_t stride = static_cast<size_t>(H) * KD;
 #pragma unroll 4
@@ -410,16 +493,16 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             }
             tc::tc_fence_after();
             const float* sf = reinterpret_cast<const float*>(sm + OFF_SF + q * SF_BYTES);
+            auto s_at = [&](int j, int c) -> float { return sf[j * SROW + c]; };
+            // the 16-byte piece a chain thread reads in step c of a row: thread pairs split the
+            // row so that the eight lanes of a shared-memory phase hit eight bank groups
+            auto piece = [](int c, int hf) -> int { return hf ? 16 + ((c + 4) & 15) : c; };
             const float* gam = F + F_GAM + q * J;
             const float* bpv = F + F_BP + q * J;
             const float* rr = F + F_RR + q * J;
             float* gout = F + F_GOUT + q * J;
-            F[F_DST + q * KD + i] = d_hi + d_lo;
-            if (ws_d) {
-                float* wd = ws_d + (static_cast<size_t>(bh) * nblk + blk) * (2 * KD);
-                wd[i] = d_hi;
-                wd[KD + i] = d_lo;
-            }
+            F[F_DST + q * KD + i] = d_hi;
+            F[F_DSL + q * KD + i] = d_lo;
 
             int p = 0, restarts = 0;
             bool abort_now = false, gram_rows_ready = false;
@@ -427,7 +510,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 if (restarts > kMaxRestarts) {  // the rest of the block token by token
                     wg_sync(1);
                     for (int j = p; j < J; ++j) {
-                        const float sj = sf[j * SROW + i];
+                        const float sj = s_at(j, i);
                         const float al = chain_sum(d_hi * sj, F + F_RED, tid);
                         const float g = gam[j] * (1.f - bpv[j] * al);
                         if (tid == 0) gout[j] = g;
@@ -451,13 +534,18 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     float cf = 0.f;
                     if (j >= p) {
                         const float* row = sf + j * SROW;
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int ii = (2 * c + hf) * 4;
-                            const float4 s4 = *reinterpret_cast<const float4*>(row + ii);
-                            const float4 d4 = *reinterpret_cast<const float4*>(F + F_DF + ii);
-                            cf = fmaf(d4.x, s4.x, fmaf(d4.y, s4.y, fmaf(d4.z, s4.z, fmaf(d4.w, s4.w, cf))));
+                        float c2 = 0.f;
+#pragma unroll 4
+                        for (int c = 0; c < 16; c += 2) {
+                            const int i0 = piece(c, hf) * 4, i1 = piece(c + 1, hf) * 4;
+                            const float4 s0 = *reinterpret_cast<const float4*>(row + i0);
+                            const float4 d0 = *reinterpret_cast<const float4*>(F + F_DF + i0);
+                            const float4 s1 = *reinterpret_cast<const float4*>(row + i1);
+                            const float4 d1 = *reinterpret_cast<const float4*>(F + F_DF + i1);
+                            cf = fmaf(d0.x, s0.x, fmaf(d0.y, s0.y, fmaf(d0.z, s0.z, fmaf(d0.w, s0.w, cf))));
+                            c2 = fmaf(d1.x, s1.x, fmaf(d1.y, s1.y, fmaf(d1.z, s1.z, fmaf(d1.w, s1.w, c2))));
                         }
+                        cf += c2;
                     }
                     cf += __shfl_xor_sync(0xffffffffu, cf, 1);
                     if (hf == 0) {
@@ -467,7 +555,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 }
                 wg_sync(1);
                 // ---- exact first step at p; classify -------------------------------------
-                const float sp = sf[p * SROW + i];
+                const float sp = s_at(p, i);
                 const float gp = gam[p] * (1.f - bpv[p] * F[F_CF + p]);
                 const float x = fmaf(gp, sp, rr[p] * d_hi);
                 const int status = (x < dmin) ? 1 : ((x > dmax) ? 2 : 0);  // free, low, high
@@ -487,7 +575,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         const float* row = sf + j * SROW;
 #pragma unroll 4
                         for (int c = 0; c < 16; ++c) {
-                            const int ii = (2 * c + hf) * 4;
+                            const int ii = piece(c, hf) * 4;
                             const float4 s4 = *reinterpret_cast<const float4*>(row + ii);
                             const float4 d4 = *reinterpret_cast<const float4*>(F + F_DF + ii);
                             const float4 b4 = *reinterpret_cast<const float4*>(F + F_BPV + ii);
@@ -533,7 +621,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 // ---- Gram of the free coordinates ------------------------------------------
                 // (the all-free Gram MMA of this block has completed once its rows are copied)
                 if (!gram_rows_ready) {
-                    const bool okr = tc::mbar_wait(bars + B_MRDY, blk & 1, kMaxPolls);
+                    const bool okr = tc::mbar_wait(bars + B_MRDY + 8 * q, ph, kMaxPolls);
                     if (wg_count(1, okr && !*static_cast<volatile int*>(&s_abort)) != 128) {
                         abort_now = true;
                         break;
@@ -541,15 +629,15 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     gram_rows_ready = true;
                     tc::tc_fence_after();
                 }
-                uint32_t gcol = COL_G + q * 64;
+                bool masked = false;
                 if (nfree > 0 && nfree < KD) {
                     // masked copy: rewrite this coordinate's column of the s copies
                     const int kb = i >> 6, cc = (i & 63) >> 3, e = i & 7;
-                    unsigned char* shb = sm + OFF_SH + q * 16384 + kb * 8192;
-                    unsigned char* slb = sm + OFF_SL + q * 16384 + kb * 8192;
+                    unsigned char* shb = sm + OFF_SHL + q * SHL_SLOT + kb * SHL_KB;
+                    unsigned char* slb = shb + SHL_LO;
                     const float sig = F[F_SIGS + q];
                     for (int j = 0; j < J; ++j) {
-                        const float x2 = status == 0 ? sf[j * SROW + i] * sig : 0.f;
+                        const float x2 = status == 0 ? s_at(j, i) * sig : 0.f;
                         const __half hv = __float2half_rn(x2);
                         const __half lv = __float2half_rn(x2 - __half2float(hv));
                         *reinterpret_cast<__half*>(shb + tc::sw128_off(j, cc) + e * 2) = hv;
@@ -558,7 +646,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     tc::fence_proxy_async();
                     tc::tc_fence_before();
                     wg_sync(1);
-                    if (tid == 0) issue_gram(q, COL_GM, bars + B_GM);
+                    if (tid == 0) issue_gram(q, COL_GM, bars + B_GM, true);
                     const bool okm = tc::mbar_wait(bars + B_GM, gm_phase, kMaxPolls);
                     gm_phase ^= 1u;
                     if (wg_count(1, okm) != 128) {
@@ -566,9 +654,10 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         break;
                     }
                     tc::tc_fence_after();
-                    gcol = COL_GM;
+                    masked = true;
                 }
                 // ---- g_{p+1..63}: Jacobi sweeps on the unit-lower-triangular system --------
+                int hb = 0;  // which half of F_H holds the final h
                 {
                     float m[64];
                     const bool row_thread = tid < J;
@@ -583,16 +672,11 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         if (HAS_R) ir1 = 1.f / rho(tid + 1);
                     }
                     if (nfree > 0 && row_thread) {
-                        if (gcol == COL_GM) {  // masked Gram: straight from tensor memory
-                            tc::tmem_ld32(tbase + lane_base + gcol, *reinterpret_cast<float(*)[32]>(m));
-                            tc::tmem_ld32(tbase + lane_base + gcol + 32, *reinterpret_cast<float(*)[32]>(m + 32));
-                            tc::tmem_ld_wait();
+                        if (masked) {  // masked Gram straight from tensor memory
                             const float isg = 1.f / F[F_SIGS + q];
-                            const float inv_sig2 = isg * isg;  // exact: powers of two
-#pragma unroll
-                            for (int l = 0; l < 64; ++l) m[l] = (l < tid) ? m[l] * inv_sig2 : 0.f;
+                            load_gram_row(COL_GM, lane_base, tid, isg * isg, m);
                         } else {
-                            const float* mrow = reinterpret_cast<const float*>(sm + OFF_MT) + tid * MROW;
+                            const float* mrow = reinterpret_cast<const float*>(sm + OFF_MT + q * MT_BYTES) + tid * MROW;
 #pragma unroll
                             for (int l = 0; l < 64; l += 4) {
                                 const float4 v = *reinterpret_cast<const float4*>(mrow + l);
@@ -612,17 +696,26 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         } else if (j == p) {
                             gj = F[F_G + j];
                         }
-                        F[F_H + j] = j >= p ? gj * ir1 : 0.f;
+                        const float hj = j >= p ? gj * ir1 : 0.f;
+                        F[F_H + j] = hj;
+                        F[F_H + J + j] = hj;
                     }
                     if (nfree > 0) {
-                        for (int it = 0; it < J; ++it) {
-                            wg_sync(1);
+                        // Each sweep shrinks the error by the coupling bound nu (the largest
+                        // |gamma_j b_j| sum_l M_jl; the rho ratios are <= 1), starting from nu |g|:
+                        // a fixed number of sweeps once nu^(K+1) <= 1e-7, else sweep until no g moves.
+                        const float nu = fmaxf(F[F_NU + 2 * q], F[F_NU + 2 * q + 1]);
+                        const float nu2 = nu * nu;
+                        const int K = nu <= 1e-7f ? 0 : nu2 <= 1e-7f ? 1 : nu2 * nu <= 1e-7f ? 2 : nu2 * nu2 <= 1e-7f ? 3 : -1;
+                        wg_sync(1);
+                        for (int it = 0; K < 0 ? it < J : it < K; ++it) {
+                            const float* hc = F + F_H + hb * J;  // h of the previous sweep
                             bool changed = false;
                             if (row_thread && tid > p) {
                                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                                 for (int l = 0; l < 64; l += 4) {
-                                    const float4 h4 = *reinterpret_cast<const float4*>(F + F_H + l);
+                                    const float4 h4 = *reinterpret_cast<const float4*>(hc + l);
                                     acc[0] = fmaf(h4.x, m[l], acc[0]);
                                     acc[1] = fmaf(h4.y, m[l + 1], acc[1]);
                                     acc[2] = fmaf(h4.z, m[l + 2], acc[2]);
@@ -635,19 +728,19 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                                 // what is left is below rounding; a 1-ulp test can cycle on noise
                                 changed = fabsf(gn - gj) > 5e-7f * fabsf(gn) + 1e-30f;
                                 gj = gn;
-                            }
-                            const bool any = wg_count(1, changed) != 0;
-                            if (row_thread && tid > p) {
                                 F[F_G + tid] = gj;
-                                F[F_H + tid] = gj * ir1;
+                                F[F_H + (hb ^ 1) * J + tid] = gj * ir1;
                             }
-                            if (!any) break;
+                            hb ^= 1;
+                            if (K >= 0) wg_sync(1);
+                            else if (wg_count(1, changed) == 0) break;
                         }
                     }
                     tc::tc_fence_before();
                     wg_sync(1);
                 }
                 // ---- block end and verification ------------------------------------------
+                const float* Hf = F + F_H + hb * J;
                 if (tid == 0) FI[0] = J;
                 float inc = 0.f;  // sum_{l=p}^{63} h_l s_li  (free coordinates)
                 int viol = J;     // first token whose update leaves the assumed regime
@@ -655,11 +748,11 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     float bnd = 0.f, inc1 = 0.f, bnd1 = 0.f;
 #pragma unroll 4
                     for (int l = 0; l < J; l += 4) {  // h_l = 0 for l < p
-                        const float4 h4 = *reinterpret_cast<const float4*>(F + F_H + l);
-                        const float hs0 = h4.x * sf[l * SROW + i];
-                        const float hs1 = h4.y * sf[(l + 1) * SROW + i];
-                        const float hs2 = h4.z * sf[(l + 2) * SROW + i];
-                        const float hs3 = h4.w * sf[(l + 3) * SROW + i];
+                        const float4 h4 = *reinterpret_cast<const float4*>(Hf + l);
+                        const float hs0 = h4.x * s_at(l, i);
+                        const float hs1 = h4.y * s_at(l + 1, i);
+                        const float hs2 = h4.z * s_at(l + 2, i);
+                        const float hs3 = h4.w * s_at(l + 3, i);
                         inc += hs0;
                         bnd += fabsf(hs0);
                         inc1 += hs1;
@@ -678,14 +771,14 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     if (!safe) {  // exact trajectory
                         float part = 0.f;
                         for (int j = p; j < J; ++j) {
-                            part += F[F_H + j] * sf[j * SROW + i];
+                            part += Hf[j] * s_at(j, i);
                             const float v = rho(j + 1) * (d_hi + (part + d_lo));
                             if (v < dmin || v > dmax) { viol = j; break; }
                         }
                     }
                 } else {
                     for (int j = p + 1; j < J; ++j) {
-                        const float xn = fmaf(F[F_G + j], sf[j * SROW + i], rr[j] * bound);
+                        const float xn = fmaf(F[F_G + j], s_at(j, i), rr[j] * bound);
                         if (status == 1 ? (xn > dmin) : (xn < dmax)) { viol = j; break; }
                     }
                 }
@@ -702,11 +795,11 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     if (tid < J && tid > p && tid <= jstar) gout[tid] = F[F_G + tid];
                     if (status == 0) {
                         float part = 0.f;
-                        for (int l = p; l <= jstar; ++l) part += F[F_H + l] * sf[l * SROW + i];
+                        for (int l = p; l <= jstar; ++l) part += Hf[l] * s_at(l, i);
                         pair_advance(d_hi, d_lo, part, rho(jstar + 1));
                         pair_clip(d_hi, d_lo, dmin, dmax);
                     } else {
-                        const float xn = fmaf(F[F_G + jstar], sf[jstar * SROW + i], rr[jstar] * bound);
+                        const float xn = fmaf(F[F_G + jstar], s_at(jstar, i), rr[jstar] * bound);
                         d_hi = fminf(fmaxf(xn, dmin), dmax);
                         d_lo = 0.f;
                     }
@@ -718,15 +811,6 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             if (abort_now) {
                 atomicExch(&s_abort, 1);
                 break;
-            }
-            if (ws_g) {
-                wg_sync(1);
-                if (tid < J && blk * J + tid < T) ws_g[static_cast<size_t>(bh) * T + blk * J + tid] = gout[tid];
-                if (blk_flags) {  // publish block blk to the consumers in other CTAs
-                    __threadfence();
-                    wg_sync(1);
-                    if (tid == 0) st_release_gpu(blk_flags + static_cast<size_t>(bh) * nblk + blk, 1u);
-                }
             }
             mbar_arrive(bars + B_CHAIN + 8 * q);
         }
@@ -751,6 +835,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
         }
         tc::mbar_inval(bars + B_GM);
         tc::mbar_inval(bars + B_MRDY);
+        tc::mbar_inval(bars + B_MRDY + 8);
     }
     __syncthreads();
 }
