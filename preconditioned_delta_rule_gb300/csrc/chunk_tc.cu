@@ -594,13 +594,24 @@ struct PrepWorker {
             TIn* gout = kt_out + i;
             const size_t stride = static_cast<size_t>(H) * KD;
             float d = semit[2 * C + i] + semit[2 * C + KD + i];
-#pragma unroll 8
-            for (int j = 0; j < C; ++j) {
-                const float kj = to_f32(*reinterpret_cast<const TIn*>(kin + tc::sw128_off(j, c)));
-                const TIn kt = from_f32<TIn>(d * kj);
-                *reinterpret_cast<TIn*>(kto + tc::sw128_off(j, c)) = kt;
-                gout[j * stride] = kt;
-                d = fminf(fmaxf(fmaf(semit[j], kj * kj, semit[C + j] * d), dmin), dmax);
+            // 32 tokens at a time: the keys first, then the serial steps, then the stores, so
+            // that no load waits behind a store it might alias
+#pragma unroll
+            for (int j0 = 0; j0 < C; j0 += 32) {
+                float kv[32];
+                TIn kt[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) kv[j] = to_f32(*reinterpret_cast<const TIn*>(kin + tc::sw128_off(j0 + j, c)));
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    kt[j] = from_f32<TIn>(d * kv[j]);
+                    d = fminf(fmaxf(fmaf(semit[j0 + j], kv[j] * kv[j], semit[C + j0 + j] * d), dmin), dmax);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    *reinterpret_cast<TIn*>(kto + tc::sw128_off(j0 + j, c)) = kt[j];
+                    gout[(j0 + j) * stride] = kt[j];
+                }
             }
             tc::fence_proxy_async();
             bar_sync128(bar);
@@ -1239,7 +1250,8 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
     const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
     __shared__ uint32_t s_tmem;
     __shared__ int s_q[2];
-    if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), 2 * prep::TMEM_COLS);
+    constexpr uint32_t kCols = scanblk::TMEM_COLS > 2 * prep::TMEM_COLS ? scanblk::TMEM_COLS : 2 * prep::TMEM_COLS;
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), kCols);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -1282,7 +1294,7 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(tbase, 2 * prep::TMEM_COLS);
+    if (warp == 0) tc::tmem_dealloc(tbase, kCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -82,8 +82,8 @@ constexpr int F_INT = F_RED1 + 8;     // [8] int scratch (chain)
 constexpr int F_GOUT = F_INT + 8;     // [2][64] final g of each token of a block (chain -> emit)
 constexpr int F_DST = F_GOUT + 128;   // [2][128] state at the block start, hi part (chain -> emit)
 constexpr int F_DSL = F_DST + 256;    // [2][128] state at the block start, lo part
-constexpr int F_NU = F_DSL + 256;     // [2][2] coupling bound of the block in a slot (per copy warp)
-constexpr int F_END = F_NU + 4;
+constexpr int F_NU = F_DSL + 256;     // [2][4] coupling bound of the block in a slot (per copy warp)
+constexpr int F_END = F_NU + 8;
 constexpr uint32_t OFF_BAR = OFF_F + ((F_END * 4 + 127) / 128) * 128;
 constexpr uint32_t SMEM_BASE = OFF_BAR + 128;
 // the all-free Gram of a block (two slots), scaled and masked to l < j, fp32 rows of MROW floats
@@ -96,9 +96,9 @@ static_assert(3 * KT_BYTES <= OFF_SHL, "key tiles");
 static_assert(OFF_SHL % 1024 == 0, "swizzle atoms");
 static_assert(SMEM_ALLOC <= 232448, "shared memory");
 
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t COL_G = 0;     // all-free Gram products of the block being prepared (128 columns)
-constexpr uint32_t COL_GM = 128;  // masked Gram products computed by the chain (128 columns)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_G = 0;     // all-free Gram products of the block in slot q: columns 128 q ..
+constexpr uint32_t COL_GM = 256;  // masked Gram products computed by the chain (128 columns)
 
 // mbarriers (offsets from OFF_BAR): gram[2], prep_ready[2], chain_done[2], gram_masked, Gram rows
 // in shared memory[2]
@@ -211,46 +211,44 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
     if (tid == 0) {
         for (int q = 0; q < 2; ++q) {
             tc::mbar_init(bars + B_GRAM + 8 * q, 1);
-            tc::mbar_init(bars + B_PREP + 8 * q, 128);
+            tc::mbar_init(bars + B_PREP + 8 * q, 4);
             tc::mbar_init(bars + B_CHAIN + 8 * q, 128);
         }
         tc::mbar_init(bars + B_GM, 1);
-        tc::mbar_init(bars + B_MRDY, 2);
-        tc::mbar_init(bars + B_MRDY + 8, 2);
+        tc::mbar_init(bars + B_MRDY, 4);
+        tc::mbar_init(bars + B_MRDY + 8, 4);
         tc::mbar_init_fence();
         s_abort = 0;
         s_grams_issued = 0;
         s_grams_used = 0;
     }
     __syncthreads();
-    const uint32_t id128 = tc::idesc_f16_f32(128, 2 * J, false, false);
-    const uint32_t id64 = tc::idesc_f16_f32(128, J, false, false);
+    const uint32_t id_hl = tc::idesc_f16_f32(J, 2 * J, false, false);  // M = 64, N = 128
+    const uint32_t id_lh = tc::idesc_f16_f32(J, J, false, false);      // M = 64, N = 64
 
-    // Gram products of the s copies in slot q into the 128 TMEM columns at `col`:
-    // [hi; lo].[hi; lo]^T (M = N = 128), i.e. lanes 0-63 hold hi.hi^T | hi.lo^T and lanes 64-127
-    // hold lo.hi^T | lo.lo^T, so row j of the Gram is M_j = D_j[0:64] + D_j[64:128] + D_{64+j}[0:64]
-    // (lo.lo^T is below fp32 rounding).  With `lanes_local`, lo.hi^T is accumulated onto the
-    // first 64 columns of lanes 0-63 as well (8 more products), so that M_j = D_j[0:64] + D_j[64:128]
-    // needs no other lane; the extra A window's rows 64-127 land in lanes the readers ignore.
-    auto issue_gram = [&](int q, uint32_t col, uint32_t bar, bool lanes_local) {
+    // Gram products of the s copies in slot q into the 128 TMEM columns at `col`, M = 64: first
+    // hi.[hi; lo]^T (N = 128), then lo.hi^T accumulated onto the first 64 columns, so that row j
+    // of the Gram is M_j = D_j[0:64] + D_j[64:128] = hi.hi^T + lo.hi^T + hi.lo^T (lo.lo^T is
+    // below fp32 rounding).  An M = 64 product puts row j in lane 32 (j / 16) + j % 16: rows
+    // 16 w .. 16 w + 15 in the first 16 lanes of warp quadrant w.
+    auto issue_gram = [&](int q, uint32_t col, uint32_t bar) {
         const uint32_t base = sbase + OFF_SHL + q * SHL_SLOT;
         tc::tc_fence_after();
 #pragma unroll
         for (int st = 0; st < KD / 16; ++st) {
             const uint64_t d = tc::sdesc_sw128(base + (st >> 2) * SHL_KB + (st & 3) * 32, 16, 1024);
-            tc::mma_f16(tbase + col, d, d, id128, st > 0 ? 1u : 0u);
+            tc::mma_f16(tbase + col, d, d, id_hl, st > 0 ? 1u : 0u);
         }
-        if (lanes_local) {
 #pragma unroll
-            for (int st = 0; st < KD / 16; ++st) {
-                const uint32_t a = base + (st >> 2) * SHL_KB + (st & 3) * 32;
-                tc::mma_f16(tbase + col, tc::sdesc_sw128(a + SHL_LO, 16, 1024), tc::sdesc_sw128(a, 16, 1024), id64, 1u);
-            }
+        for (int st = 0; st < KD / 16; ++st) {
+            const uint32_t a = base + (st >> 2) * SHL_KB + (st & 3) * 32;
+            tc::mma_f16(tbase + col, tc::sdesc_sw128(a + SHL_LO, 16, 1024), tc::sdesc_sw128(a, 16, 1024), id_lh, 1u);
         }
         tc::mma_commit(bar);
     };
-    // row j of the Gram of the products at `col` (lanes 0-63 only), scaled by 1 / sig^2 and masked
-    // to l < j; `lane_base` selects the calling warp's lanes
+    // The Gram row of the calling lane of a warp of quadrant `lane_base` (row j = 16 w + lane for
+    // lanes 0-15; the other lanes load what they load), scaled by 1 / sig^2 and masked to l < j.
+    // Warp-collective: every lane of the warp must call it.
     auto load_gram_row = [&](uint32_t col, uint32_t lane_base, int j, float inv_sig2, float (&mrow)[64]) {
 #pragma unroll
         for (int hv = 0; hv < 2; ++hv) {
@@ -304,9 +302,6 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     n += sv[c * 8 + e];
                     mx = fmaxf(mx, sv[c * 8 + e]);
                 }
-                float4* dst = reinterpret_cast<float4*>(sf + j * SROW + hf * 64 + c * 8);
-                dst[0] = make_float4(sv[c * 8], sv[c * 8 + 1], sv[c * 8 + 2], sv[c * 8 + 3]);
-                dst[1] = make_float4(sv[c * 8 + 4], sv[c * 8 + 5], sv[c * 8 + 6], sv[c * 8 + 7]);
             }
             n += __shfl_xor_sync(0xffffffffu, n, 1);
 #pragma unroll
@@ -345,76 +340,58 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             }
             tc::fence_proxy_async();
             wg_sync(2);
-            // the chain starts the block on s and the gates; it waits for the Gram rows separately.
-            // The Gram is issued from warp 6: warps 4-5 copy its rows out of tensor memory.
-            mbar_arrive(bars + B_PREP + 8 * (m & 1));
+            // The Gram goes first (its rows are what the chain waits for longest), issued from
+            // warp 6; then the fp32 s tile for the chain, each warp releasing the block once its
+            // rows are stored.
             if (u == 2 * 32) {
-                issue_gram(m & 1, COL_G, bars + B_GRAM + 8 * (m & 1), false);
+                issue_gram(m & 1, COL_G + (m & 1) * 128, bars + B_GRAM + 8 * (m & 1));
                 s_grams_issued = m + 1;
             }
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float4* dst = reinterpret_cast<float4*>(sf + j * SROW + hf * 64 + c * 8);
+                dst[0] = make_float4(sv[c * 8], sv[c * 8 + 1], sv[c * 8 + 2], sv[c * 8 + 3]);
+                dst[1] = make_float4(sv[c * 8 + 4], sv[c * 8 + 5], sv[c * 8 + 6], sv[c * 8 + 7]);
+            }
+            __syncwarp();
+            if ((u & 31) == 0) mbar_arrive(bars + B_PREP + 8 * (m & 1));
         };
 
         // Gram of block m, tensor memory -> shared memory slot m & 1 (warps 4-5, one row per
-        // thread), scaled back by 1 / sig^2 (exact: powers of two) and masked to l < j, for the
-        // chain's Jacobi rows
+        // thread), scaled back by 1 / sig^2 (exact: powers of two) and masked to l < j, with the
+        // coupling bound of the block's system for the chain's sweep count
         auto copy_gram = [&](int m) {
             const bool okg = tc::mbar_wait(bars + B_GRAM + 8 * (m & 1), (m >> 1) & 1, kMaxPolls);
-            if (wg_count(2, okg) != 128) {  // uniform decision across the warpgroup
+            if (!__all_sync(0xffffffffu, okg)) {
                 atomicExch(&s_abort, 1);
                 return;
             }
             if (u == 0) s_grams_used = m + 1;
             tc::tc_fence_after();
-            const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            float* mt = reinterpret_cast<float*>(sm + OFF_MT + (m & 1) * MT_BYTES);
-            if (u >= J) {  // warps 6-7: the lo.hi^T rows (lanes 64-127), raw, into the row tile
+            const int lane = u & 31, j = ((u >> 5) << 4) | (lane & 15);
+            const float isg = 1.f / F[F_SIGS + (m & 1)];
+            float g[64];
+            load_gram_row(COL_G + (m & 1) * 128, static_cast<uint32_t>((warp & 3) * 32) << 16, j, isg * isg, g);
+            tc::tc_fence_before();
+            float t = 0.f;
+            if (lane < 16) {
+                float* row = reinterpret_cast<float*>(sm + OFF_MT + (m & 1) * MT_BYTES) + j * MROW;
 #pragma unroll
-                for (int hv = 0; hv < 2; ++hv) {
-                    float x[32];
-                    tc::tmem_ld32(tbase + lb + COL_G + hv * 32, x);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int l = 0; l < 32; l += 4)
-                        *reinterpret_cast<float4*>(mt + (u - J) * MROW + hv * 32 + l) = make_float4(x[l], x[l + 1], x[l + 2], x[l + 3]);
-                }
-                tc::tc_fence_before();
-            }
-            wg_sync(2);
-            if (u < J) {  // warps 4-5: row u = hi.hi^T + hi.lo^T (lanes 0-63) + the parked lo.hi^T
-                const float isg = 1.f / F[F_SIGS + (m & 1)];
-                const float inv_sig2 = isg * isg;
-                float* row = mt + u * MROW;
-                // coupling bound of the block's system: max_j |gamma_j b_j| sum_l M_jl (M >= 0);
-                // infinite when it is not finite or a retention gate exceeds 1
+                for (int l = 0; l < 64; l += 4) *reinterpret_cast<float4*>(row + l) = make_float4(g[l], g[l + 1], g[l + 2], g[l + 3]);
+                // max_j |gamma_j b_j| sum_l M_jl (M >= 0); infinite when it is not finite or a
+                // retention gate exceeds 1
                 float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int hv = 0; hv < 2; ++hv) {
-                    float x[32], y[32];
-                    tc::tmem_ld32(tbase + lb + COL_G + hv * 32, x);
-                    tc::tmem_ld32(tbase + lb + COL_G + 64 + hv * 32, y);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int l = 0; l < 32; l += 4) {
-                        float4 z = *reinterpret_cast<const float4*>(row + hv * 32 + l);
-                        float* zz = reinterpret_cast<float*>(&z);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = hv * 32 + l + e;
-                            zz[e] = c < u ? ((x[l + e] + y[l + e]) + zz[e]) * inv_sig2 : 0.f;
-                            r4[e] += zz[e];
-                        }
-                        *reinterpret_cast<float4*>(row + hv * 32 + l) = z;
-                    }
-                }
-                tc::tc_fence_before();
-                float t = fabsf(F[F_GAM + (m & 1) * J + u] * F[F_BP + (m & 1) * J + u]) * ((r4[0] + r4[1]) + (r4[2] + r4[3]));
-                if (!(t <= 3.0e38f) || (HAS_R && F[F_RR + (m & 1) * J + u] > 1.f)) t = INFINITY;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
-                if ((u & 31) == 0) F[F_NU + 2 * (m & 1) + (u >> 5)] = t;
-                __syncwarp();
-                if ((u & 31) == 0) mbar_arrive(bars + B_MRDY + 8 * (m & 1));
+                for (int l = 0; l < 64; ++l) r4[l & 3] += g[l];
+                t = fabsf(F[F_GAM + (m & 1) * J + j] * F[F_BP + (m & 1) * J + j]) * ((r4[0] + r4[1]) + (r4[2] + r4[3]));
+                if (!(t <= 3.0e38f) || (HAS_R && F[F_RR + (m & 1) * J + j] > 1.f)) t = INFINITY;
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+            if (lane == 0) F[F_NU + 4 * (m & 1) + (u >> 5)] = t;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + B_MRDY + 8 * (m & 1));
         };
         // step sizes and start state of block m to the workspace (warps 6-7).  A reader in
         // another CTA polls each word until it differs from the all-ones pattern the workspace
@@ -619,7 +596,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 }
                 auto rho = [&](int j) -> float { return HAS_R ? F[F_RHO + j] : 1.f; };
                 // ---- Gram of the free coordinates ------------------------------------------
-                // (the all-free Gram MMA of this block has completed once its rows are copied)
+                // (the masked copy below may rewrite the s copies once the all-free product is done)
                 if (!gram_rows_ready) {
                     const bool okr = tc::mbar_wait(bars + B_MRDY + 8 * q, ph, kMaxPolls);
                     if (wg_count(1, okr && !*static_cast<volatile int*>(&s_abort)) != 128) {
@@ -646,7 +623,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     tc::fence_proxy_async();
                     tc::tc_fence_before();
                     wg_sync(1);
-                    if (tid == 0) issue_gram(q, COL_GM, bars + B_GM, true);
+                    if (tid == 0) issue_gram(q, COL_GM, bars + B_GM);
                     const bool okm = tc::mbar_wait(bars + B_GM, gm_phase, kMaxPolls);
                     gm_phase ^= 1u;
                     if (wg_count(1, okm) != 128) {
@@ -660,23 +637,25 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 int hb = 0;  // which half of F_H holds the final h
                 {
                     float m[64];
-                    const bool row_thread = tid < J;
+                    // row jr of the system on lanes 0-15 of each chain warp (the lanes of an M = 64 product)
+                    const int jr = (warp << 4) | (tid & 15);
+                    const bool row_thread = (tid & 31) < 16;
                     // this row's coefficients, read once for all sweeps
                     float ga = 0.f, gb = 0.f, rj = 1.f, cfj = 0.f, cpj = 0.f, ir1 = 1.f;
                     if (row_thread) {
-                        ga = gam[tid];
-                        gb = bpv[tid];
-                        rj = rho(tid);
-                        cfj = F[F_CF + tid];
-                        cpj = F[F_CP + tid];
-                        if (HAS_R) ir1 = 1.f / rho(tid + 1);
+                        ga = gam[jr];
+                        gb = bpv[jr];
+                        rj = rho(jr);
+                        cfj = F[F_CF + jr];
+                        cpj = F[F_CP + jr];
+                        if (HAS_R) ir1 = 1.f / rho(jr + 1);
                     }
-                    if (nfree > 0 && row_thread) {
-                        if (masked) {  // masked Gram straight from tensor memory
+                    if (nfree > 0) {
+                        if (masked) {  // masked Gram straight from tensor memory (all lanes)
                             const float isg = 1.f / F[F_SIGS + q];
-                            load_gram_row(COL_GM, lane_base, tid, isg * isg, m);
-                        } else {
-                            const float* mrow = reinterpret_cast<const float*>(sm + OFF_MT + q * MT_BYTES) + tid * MROW;
+                            load_gram_row(COL_GM, lane_base, jr, isg * isg, m);
+                        } else if (row_thread) {
+                            const float* mrow = reinterpret_cast<const float*>(sm + OFF_MT + q * MT_BYTES) + jr * MROW;
 #pragma unroll
                             for (int l = 0; l < 64; l += 4) {
                                 const float4 v = *reinterpret_cast<const float4*>(mrow + l);
@@ -689,7 +668,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     }
                     float gj = 0.f;
                     if (row_thread) {
-                        const int j = tid;
+                        const int j = jr;
                         if (j > p) {
                             gj = ga * (1.f - gb * (rj * cfj + cpj));
                             F[F_G + j] = gj;
@@ -704,14 +683,15 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         // Each sweep shrinks the error by the coupling bound nu (the largest
                         // |gamma_j b_j| sum_l M_jl; the rho ratios are <= 1), starting from nu |g|:
                         // a fixed number of sweeps once nu^(K+1) <= 1e-7, else sweep until no g moves.
-                        const float nu = fmaxf(F[F_NU + 2 * q], F[F_NU + 2 * q + 1]);
+                        // (the masked Gram's entries are bounded by the all-free ones: the same bound)
+                        const float nu = fmaxf(fmaxf(F[F_NU + 4 * q], F[F_NU + 4 * q + 1]), fmaxf(F[F_NU + 4 * q + 2], F[F_NU + 4 * q + 3]));
                         const float nu2 = nu * nu;
                         const int K = nu <= 1e-7f ? 0 : nu2 <= 1e-7f ? 1 : nu2 * nu <= 1e-7f ? 2 : nu2 * nu2 <= 1e-7f ? 3 : -1;
                         wg_sync(1);
                         for (int it = 0; K < 0 ? it < J : it < K; ++it) {
                             const float* hc = F + F_H + hb * J;  // h of the previous sweep
                             bool changed = false;
-                            if (row_thread && tid > p) {
+                            if (row_thread && jr > p) {
                                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                                 for (int l = 0; l < 64; l += 4) {
@@ -728,8 +708,8 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                                 // what is left is below rounding; a 1-ulp test can cycle on noise
                                 changed = fabsf(gn - gj) > 5e-7f * fabsf(gn) + 1e-30f;
                                 gj = gn;
-                                F[F_G + tid] = gj;
-                                F[F_H + (hb ^ 1) * J + tid] = gj * ir1;
+                                F[F_G + jr] = gj;
+                                F[F_H + (hb ^ 1) * J + jr] = gj * ir1;
                             }
                             hb ^= 1;
                             if (K >= 0) wg_sync(1);
