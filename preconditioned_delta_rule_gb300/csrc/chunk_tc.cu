@@ -64,7 +64,7 @@ constexpr uint32_t OFF_SS = OFF_X + (VS / 64) * 8192;  // fp16 copy of S (MN-maj
 constexpr uint32_t OFF_AM = OFF_SS + (VS / 64) * KD * 128;
 constexpr uint32_t OFF_TM = OFF_AM + 10 * kTile * 4;   // 10 packed lower-triangular tiles
 constexpr uint32_t OFF_PM = OFF_TM + 10 * kTile * 4;
-constexpr uint32_t OFF_BETA = OFF_PM + 3 * kTile * 4;
+constexpr uint32_t OFF_BETA = OFF_PM + kUtScratchTiles * kTile * 4;
 constexpr uint32_t OFF_BAR = OFF_BETA + 2 * C * 4;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
@@ -474,7 +474,7 @@ constexpr uint32_t OFF_LI = OFF_KQ + 8192;  // L image, in the Q rows of key blo
 constexpr uint32_t OFF_AM = 65536;
 constexpr uint32_t OFF_TM = OFF_AM + 10 * kTile * 4;
 constexpr uint32_t OFF_PM = OFF_TM + 10 * kTile * 4;
-constexpr uint32_t OFF_BETA = OFF_PM + 3 * kTile * 4;
+constexpr uint32_t OFF_BETA = OFF_PM + kUtScratchTiles * kTile * 4;
 constexpr uint32_t OFF_EMIT = OFF_BETA + C * 4;              // step sizes, retention, start state
 constexpr uint32_t OFF_BAR = OFF_EMIT + (2 * C + 2 * KD) * 4;
 constexpr uint32_t REGION = ((OFF_BAR + 32 + 1023) / 1024) * 1024;  // one worker, 1024-aligned
@@ -543,12 +543,12 @@ struct PrepWorker {
     }
 
     // Chunk n of head (b, h) into workspace slot `slot`.  Emission inputs (EMIT only): g_src[64],
-    // r_src (stride H, or null), d_src[2 * KD] (hi, lo); kt_out: the chunk's first k~ row.
+    // r_src (stride H, or null), d_src[2 * KD] (hi, lo); tmKTout: tensor map of the k~ output.
     template <bool EMIT>
     __device__ bool run(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmKT,
                         const float* __restrict__ beta, unsigned char* __restrict__ ws, size_t slot, int b,
                         int h, int n, int T, int H, const float* g_src, const float* r_src, const float* d_src,
-                        float dmin, float dmax, TIn* kt_out) {
+                        float dmin, float dmax, const CUtensorMap* tmKTout) {
         using namespace prep;
         float* AM = reinterpret_cast<float*>(sm + OFF_AM);
         float* TM = reinterpret_cast<float*>(sm + OFF_TM);
@@ -591,30 +591,33 @@ struct PrepWorker {
             const int i = tid, kb = i >> 6, c = (i & 63) >> 3, e = i & 7;
             const unsigned char* kin = sm + OFF_KQ + kb * 16384 + 2 * e;
             unsigned char* kto = sm + OFF_KT + kb * 8192 + 2 * e;
-            TIn* gout = kt_out + i;
-            const size_t stride = static_cast<size_t>(H) * KD;
             float d = semit[2 * C + i] + semit[2 * C + KD + i];
             // 32 tokens at a time: the keys first, then the serial steps, then the stores, so
-            // that no load waits behind a store it might alias
+            // that no load waits behind a store it might alias; the tile leaves by TMA
 #pragma unroll
             for (int j0 = 0; j0 < C; j0 += 32) {
                 float kv[32];
                 TIn kt[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) kv[j] = to_f32(*reinterpret_cast<const TIn*>(kin + tc::sw128_off(j0 + j, c)));
+                float inc[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) inc[j] = replay_inc(semit[j0 + j], kv[j]);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     kt[j] = from_f32<TIn>(d * kv[j]);
-                    d = fminf(fmaxf(fmaf(semit[j0 + j], kv[j] * kv[j], semit[C + j0 + j] * d), dmin), dmax);
+                    d = replay_step(d, semit[C + j0 + j], inc[j], dmin, dmax);
                 }
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    *reinterpret_cast<TIn*>(kto + tc::sw128_off(j0 + j, c)) = kt[j];
-                    gout[(j0 + j) * stride] = kt[j];
-                }
+                for (int j = 0; j < 32; ++j) *reinterpret_cast<TIn*>(kto + tc::sw128_off(j0 + j, c)) = kt[j];
             }
             tc::fence_proxy_async();
             bar_sync128(bar);
+            if (tid == 0) {  // k~ of the chunk to HBM (read before the -W image reuses the tile)
+                tc::tma_store_3d(tmKTout, sbase + OFF_KT, 0, h, row);
+                tc::tma_store_3d(tmKTout, sbase + OFF_KT + 8192, 64, h, row);
+                tc::bulk_commit();
+            }
         }
 
         // [K; Q] K~^T on the 16-bit tiles (exact products, fp32 sums)
@@ -692,6 +695,7 @@ struct PrepWorker {
             tc::mma_commit(bar_mma);
         }
         mma_pending = true;
+        if (EMIT && tid == 0) tc::bulk_wait_read_all();  // the k~ store has read the tile
         {
             const bool ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
             if (!bar_and128(bar, ok)) return false;
@@ -1245,6 +1249,7 @@ template <typename TIn, bool HAS_R>
 __global__ void __launch_bounds__(256, 1)
 layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* counter,
                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmKT,
                        unsigned char* __restrict__ cws, int N, int BH) {
     extern __shared__ unsigned char smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
@@ -1267,11 +1272,11 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
     if (tid == 0) {
         tc::prefetch_tmap(&tmQ);
         tc::prefetch_tmap(&tmK);
+        tc::prefetch_tmap(&tmKT);
     }
     __syncthreads();
     pw.tbase = tbase + w * prep::TMEM_COLS;
     const int total = BH * N;
-    TIn* kto = static_cast<TIn*>(sa.k_tilde);
     bool aborted = false;
     for (;;) {
         if (wt == 0) s_q[w] = static_cast<int>(atomicAdd(counter, 1u) + 1u);
@@ -1283,9 +1288,8 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
         const float* g_src = ws_g + static_cast<size_t>(bh) * T + m * C;
         const float* r_src = HAS_R ? sa.r + row0 + static_cast<size_t>(m) * C * H : nullptr;
         const float* d_src = ws_d + (static_cast<size_t>(bh) * N + m) * (2 * KD);
-        TIn* kt_out = kto + (row0 + static_cast<size_t>(m) * C * H) * KD;
         if (!pw.template run<true>(&tmQ, &tmK, nullptr, sa.beta, cws, static_cast<size_t>(bh) * N + m, b, h, m, T, H,
-                                   g_src, r_src, d_src, sa.d_min, sa.d_max, kt_out)) {
+                                   g_src, r_src, d_src, sa.d_min, sa.d_max, &tmKT)) {
             aborted = true;
             break;
         }
@@ -1415,8 +1419,9 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     const CUtensorMapDataType dt = std::is_same<TIn, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const long long rows = static_cast<long long>(ca.B) * ca.T;
-    CUtensorMap mq, mk;
-    if (!make_map(&mq, ca.q, dt, ca.K, ca.H, rows) || !make_map(&mk, ca.k, dt, ca.K, ca.H, rows))
+    CUtensorMap mq, mk, mkt;
+    if (!make_map(&mq, ca.q, dt, ca.K, ca.H, rows) || !make_map(&mk, ca.k, dt, ca.K, ca.H, rows) ||
+        !make_map(&mkt, sa.k_tilde, dt, ca.K, ca.H, rows))
         return cudaErrorNotSupported;
     auto kernel = layer_scan_prep_kernel<TIn, HAS_R>;
     const uint32_t smem = scanblk::SMEM_ALLOC > 2 * prep::REGION + 1024 ? scanblk::SMEM_ALLOC : 2 * prep::REGION + 1024;
@@ -1440,7 +1445,7 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     unsigned int* counter = reinterpret_cast<unsigned int*>(ws + l.counter);
     unsigned char* cws = ws + l.chunk;
     int N = ca.T / C, BH = ca.B * ca.H;
-    void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &cws, &N, &BH};
+    void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &mkt, &cws, &N, &BH};
     e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
                                     dim3(256), args, smem, s);
     if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer resident CTAs than expected: two calls

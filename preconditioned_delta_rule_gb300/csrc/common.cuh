@@ -74,6 +74,17 @@ template <typename H, int N> struct VecIO16 {  // 16-bit types
 template <int N> struct VecIO<__nv_bfloat16, N> : VecIO16<__nv_bfloat16, N> {};
 template <int N> struct VecIO<__half, N> : VecIO16<__half, N> {};
 
+// One token of the preconditioner replay for one key coordinate ("OSDN: Improving Delta Rule with
+// Provable Online Preconditioning in Linear Attention", Algorithm 1, Eq. (4)): with the step size
+// g_t fixed by the scan, d <- clip(r_t d + g_t k_t^2, d_min, d_max).  The increment g_t k_t^2 is
+// rounded once by itself (k_t^2 is exact for 16-bit keys), so that it is formed ahead of the
+// serial dependency on d; every kernel that replays the recurrence uses these two functions, so
+// all of them produce the same write keys.
+__device__ __forceinline__ float replay_inc(float g, float k) { return g * (k * k); }
+__device__ __forceinline__ float replay_step(float d, float r, float inc, float dmin, float dmax) {
+    return fminf(fmaxf(fmaf(r, d, inc), dmin), dmax);
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

@@ -91,13 +91,27 @@ __global__ void __launch_bounds__(EC) scan_emit_kernel(OsdnScanArgs a, const flo
     float d = wd[i] + wd[KD + i];
     __syncthreads();
     const float dmin = a.d_min, dmax = a.d_max;
-#pragma unroll 8
-    for (int j = 0; j < jb; ++j) {
-        const float kj = to_f32(tile[j * EC + i]);
-        const float kt = d * kj;
-        if constexpr (sizeof(TOut) == 2) reinterpret_cast<TOut*>(tile)[j * EC + i] = from_f32<TOut>(kt);  // own slot
-        else og[j * stride + i] = kt;
-        d = fminf(fmaxf(fmaf(sg[j], kj * kj, sr[j] * d), dmin), dmax);
+    // 32 tokens at a time: keys and increments first, then the serial steps, then the stores
+#pragma unroll
+    for (int j0 = 0; j0 < J; j0 += 32) {
+        float kv[32], inc[32], kt[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            kv[j] = j0 + j < jb ? to_f32(tile[(j0 + j) * EC + i]) : 0.f;
+            inc[j] = replay_inc(sg[j0 + j], kv[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            kt[j] = d * kv[j];
+            d = replay_step(d, sr[j0 + j], inc[j], dmin, dmax);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j0 + j < jb) {
+                if constexpr (sizeof(TOut) == 2) reinterpret_cast<TOut*>(tile)[(j0 + j) * EC + i] = from_f32<TOut>(kt[j]);  // own slot
+                else og[(j0 + j) * stride + i] = kt[j];
+            }
+        }
     }
     if constexpr (sizeof(TOut) == 2) {
         __syncthreads();

@@ -447,7 +447,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 for (int j = 0; j < jb; ++j) {
                     const float kj = ld_key<TIn>(kt, j, u);
                     out[j * stride] = from_f32<TOut>(d * kj);
-                    d = fminf(fmaxf(fmaf(F[F_GOUT + q * J + j], kj * kj, F[F_RR + q * J + j] * d), dmin), dmax);
+                    d = replay_step(d, F[F_RR + q * J + j], replay_inc(F[F_GOUT + q * J + j], kj), dmin, dmax);
                 }
             }
             wg_sync(2);
