@@ -603,10 +603,21 @@ struct PrepWorker {
                 float inc[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) inc[j] = replay_inc(semit[j0 + j], kv[j]);
+                if (r_src != nullptr) {
+                    float rv[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    kt[j] = from_f32<TIn>(d * kv[j]);
-                    d = replay_step(d, semit[C + j0 + j], inc[j], dmin, dmax);
+                    for (int j = 0; j < 32; ++j) rv[j] = semit[C + j0 + j];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        kt[j] = from_f32<TIn>(d * kv[j]);
+                        d = replay_step(d, rv[j], inc[j], dmin, dmax);
+                    }
+                } else {  // no retention gates: r = 1 (the same value replay_step would compute)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        kt[j] = from_f32<TIn>(d * kv[j]);
+                        d = replay_step(d, 1.f, inc[j], dmin, dmax);
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) *reinterpret_cast<TIn*>(kto + tc::sw128_off(j0 + j, c)) = kt[j];
@@ -751,6 +762,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5;
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the chain kernel may set up
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + prep::OFF_BAR + 16);
     PrepWorker<TIn> w;
     w.init(sm, tid, 0);
@@ -929,6 +941,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    // Launched as a programmatic dependent of the kernel that writes the chunk images and k~
+    // (the setup above overlaps that kernel's tail): wait until its results are visible.  A
+    // no-op when launched without the attribute.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     if (warp == 9) {
         // ================================ producer ============================================
@@ -1253,6 +1269,7 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
                        unsigned char* __restrict__ cws, int N, int BH) {
     extern __shared__ unsigned char smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the chain kernel may set up
     __shared__ uint32_t s_tmem;
     __shared__ int s_q[2];
     constexpr uint32_t kCols = scanblk::TMEM_COLS > 2 * prep::TMEM_COLS ? scanblk::TMEM_COLS : 2 * prep::TMEM_COLS;
@@ -1378,9 +1395,28 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
             if (e != cudaSuccess) return e;
         }
         dim3 gc(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
-        chunk_chain_kernel<TIn><<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(
-            mq, mkt, mv, mo, static_cast<const unsigned char*>(ws), a.S0, a.S_out, a.T, a.H, a.V, N, a.scale);
-        return cudaGetLastError();
+        // programmatic dependent launch: the chain CTAs take SMs as the previous kernel's CTAs
+        // leave and wait (griddepcontrol.wait) for its results
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = gc;
+        cfg.blockDim = dim3(chain::NT);
+        cfg.dynamicSmemBytes = chain::SMEM_ALLOC;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const unsigned char* wsc = static_cast<const unsigned char*>(ws);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, chunk_chain_kernel<TIn>, mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T,
+                                           a.H, a.V, N, a.scale);
+        if (e == cudaErrorNotSupported) {  // no dependent launch here: an ordinary one
+            (void)cudaGetLastError();
+            chunk_chain_kernel<TIn><<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(mq, mkt, mv, mo, wsc, a.S0,
+                                                                                   a.S_out, a.T, a.H, a.V, N, a.scale);
+            e = cudaGetLastError();
+        }
+        return e;
     }
     dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
     chunk_tc_kernel<TIn><<<grid, block, fused::SMEM_ALLOC, s>>>(mq, mk, mkt, mv, a.beta, a.S0, static_cast<TIn*>(a.o),
