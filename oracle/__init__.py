@@ -53,10 +53,10 @@ def _load():
         path = build()
         lib = ctypes.CDLL(str(path))
         i, d = ctypes.c_int, ctypes.c_double
-        lib.oracle_precond_scan.argtypes = [_dp] * 7 + [i] * 4 + [d] * 4 + [i, i]
+        lib.oracle_precond_scan.argtypes = [_dp] * 3 + [i] + [_dp] * 4 + [i] * 4 + [d] * 4 + [i, i]
         lib.oracle_delta_phase2.argtypes = [_dp] * 8 + [i] * 5 + [d, i]
-        lib.oracle_osdn_forward.argtypes = [_dp] * 13 + [i] * 5 + [d] * 4 + [i, d, i]
-        lib.oracle_decode_step.argtypes = [_dp] * 8 + [i] * 4 + [d] * 4 + [i, d, i]
+        lib.oracle_osdn_forward.argtypes = [_dp] * 5 + [i] + [_dp] * 8 + [i] * 5 + [d] * 4 + [i, d, i]
+        lib.oracle_decode_step.argtypes = [_dp] * 5 + [i] + [_dp] * 3 + [i] * 4 + [d] * 4 + [i, d, i]
         for f in ("oracle_precond_scan", "oracle_delta_phase2", "oracle_osdn_forward",
                   "oracle_decode_step"):
             getattr(lib, f).restype = ctypes.c_int
@@ -82,15 +82,28 @@ def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
+def _per_key(r, k) -> int:
+    """1 when r carries one retention per key coordinate (the layout of k), 0 for one per head."""
+    if r is None:
+        return 0
+    if r.shape == k.shape:
+        return 1
+    if r.shape != k.shape[:-1]:
+        raise ValueError(f"retention of shape {r.shape} fits neither {k.shape[:-1]} nor {k.shape}")
+    return 0
+
+
 def precond_scan(k, beta, r=None, d0=None, *, eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6,
                  beta_aware=True, threads=0, return_a=False):
-    """Phase 1 (Algorithm 1 / Eq. (4); Eq. (7) with r).  k [B,T,H,K] -> (k_tilde, d_out[, a])."""
+    """Phase 1 (Algorithm 1 / Eq. (4); Eq. (7) with r).  k [B,T,H,K] -> (k_tilde, d_out[, a]).
+    r [B,T,H] is the per-head retention of Eq. (7); r [B,T,H,K] the vector retention diag(r_t)
+    (Appendix A.5)."""
     k, beta, r, d0 = _in(k), _in(beta), _in(r), _in(d0)
     B, T, H, K = k.shape
     kt = np.empty_like(k)
     dout = np.empty((B, H, K))
     a = np.empty((B, T, H)) if return_a else None
-    rc = _load().oracle_precond_scan(_p(k), _p(beta), _p(r), _p(d0), _p(kt), _p(dout), _p(a),
+    rc = _load().oracle_precond_scan(_p(k), _p(beta), _p(r), _per_key(r, k), _p(d0), _p(kt), _p(dout), _p(a),
                                      B, T, H, K, eta, d_min, d_max, eps, int(beta_aware), threads)
     if rc:
         raise ValueError("oracle_precond_scan: bad arguments")
@@ -123,7 +136,7 @@ def osdn_forward(q, k, v, beta, r=None, d0=None, S0=None, *, eta=0.003, d_min=0.
     kt = np.empty((B, T, H, K))
     a = np.empty((B, T, H))
     u2 = np.empty((B, T, H))
-    rc = _load().oracle_osdn_forward(_p(q), _p(k), _p(v), _p(beta), _p(r), _p(d0), _p(S0), _p(o),
+    rc = _load().oracle_osdn_forward(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(d0), _p(S0), _p(o),
                                      _p(S), _p(d), _p(kt), _p(a), _p(u2), B, T, H, K, V, eta,
                                      d_min, d_max, eps, int(beta_aware), scale, threads)
     if rc:
@@ -141,7 +154,7 @@ def decode_step(q, k, v, beta, S, d, r=None, *, eta=0.003, d_min=0.5, d_max=2.0,
     B, H, K = k.shape
     V = v.shape[-1]
     o = np.empty((B, H, V))
-    rc = _load().oracle_decode_step(_p(q), _p(k), _p(v), _p(beta), _p(r), _p(S), _p(d), _p(o),
+    rc = _load().oracle_decode_step(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(S), _p(d), _p(o),
                                     B, H, K, V, eta, d_min, d_max, eps, int(beta_aware), scale,
                                     threads)
     if rc:

@@ -15,12 +15,15 @@
  *     with b = beta_t ("beta-aware", Listing 1 default) or b = 1 (the non-beta-aware 1.3B form,
  *     Appendix B); the memory write always keeps beta_t.
  *   - APF, Section 4.4 Eq. (7): d_{t+1} = clip(r_{t,h} d_t + same step), the step using the old d_t.
+ *     Vector retention, Appendix A.5 (Prop. A.3): r_{t,h} I becomes diag(r_t), one gate per key
+ *     coordinate (r_per_key = 1: r has the layout of k).
  *   - readout o_t = S_t q_t after the write (Section 4.1; the intra-chunk score of Listing 1 keeps
  *     the diagonal).  An optional scale multiplies q (Listing 1 uses K^-1/2; the equations use 1).
  *
  * Everything is a per-(batch, head) loop over tokens.  OpenMP runs independent heads in
  * parallel; within a head the arithmetic follows the definition above in order, in double.
- * Layouts (row-major, contiguous): q, k, k~ [B,T,H,K]; v, o [B,T,H,V]; beta, r [B,T,H];
+ * Layouts (row-major, contiguous): q, k, k~ [B,T,H,K]; v, o [B,T,H,V]; beta, r [B,T,H] (r [B,T,H,K]
+ * with r_per_key);
  * S [B,H,V,K]; d [B,H,K].  For a decode step T is absent: q, k [B,H,K], v, o [B,H,V], beta, r [B,H].
  * Clamp: min(max(x, d_min), d_max) with IEEE fmin/fmax; +-inf bounds disable it.
  */
@@ -41,10 +44,11 @@ static double clip(double x, double lo, double hi) { return fmin(fmax(x, lo), hi
 
 /* One phase-1 step on d (length K) for key k (length K): writes k~ = d . k (old d), then
  * updates d in place (Algorithm 1 lines "materialise write key" and "hypergradient step";
- * Eq. (7) when r != 1).  Returns a_t = beta <d_t, k_t^2> for diagnostics. */
+ * Eq. (7) when r is given: r[0] for every coordinate, or r[i] for coordinate i with r_per_key).
+ * Returns a_t = beta <d_t, k_t^2> for diagnostics. */
 static double phase1_step(double *d, const double *k, double *kt_out, int K, double beta,
-                          double r, double eta, double dmin, double dmax, double eps,
-                          int beta_aware)
+                          const double *r, int r_per_key, double eta, double dmin, double dmax,
+                          double eps, int beta_aware)
 {
     double n = 0.0, align = 0.0;
     for (int i = 0; i < K; ++i) {
@@ -58,7 +62,8 @@ static double phase1_step(double *d, const double *k, double *kt_out, int K, dou
     double step = eta * bp * (1.0 - bp * align) / nbar;
     for (int i = 0; i < K; ++i) {
         double s = k[i] * k[i];
-        d[i] = clip(r * d[i] + step * s, dmin, dmax);
+        double ri = r ? r[r_per_key ? i : 0] : 1.0;
+        d[i] = clip(ri * d[i] + step * s, dmin, dmax);
     }
     return beta * align;
 }
@@ -102,10 +107,10 @@ static int set_threads(int nthreads)
 /* Phase 1 alone (Algorithm 1 with the per-step clamp; Eq. (7) when r is given).
  * k_tilde [B,T,H,K] and d_out [B,H,K] are written; a_out [B,T,H] (optional) gets
  * a_t = beta_t <d_t, k_t^2>.  r and d0 may be NULL (r = 1, d0 = 1). */
-int oracle_precond_scan(const double *k, const double *beta, const double *r, const double *d0,
-                        double *k_tilde, double *d_out, double *a_out, int B, int T, int H, int K,
-                        double eta, double dmin, double dmax, double eps, int beta_aware,
-                        int nthreads)
+int oracle_precond_scan(const double *k, const double *beta, const double *r, int r_per_key,
+                        const double *d0, double *k_tilde, double *d_out, double *a_out, int B,
+                        int T, int H, int K, double eta, double dmin, double dmax, double eps,
+                        int beta_aware, int nthreads)
 {
     if (B < 0 || T < 0 || H < 0 || K <= 0) return 1;
     int nt = set_threads(nthreads);
@@ -118,8 +123,9 @@ int oracle_precond_scan(const double *k, const double *beta, const double *r, co
         for (long t = 0; t < T; ++t) {
             size_t kk = ix4(b, t, h, 0, T, H, K);
             size_t gg = ix4(b, t, h, 0, T, H, 1);
-            double a = phase1_step(d, k + kk, k_tilde + kk, K, beta[gg], r ? r[gg] : 1.0, eta,
-                                   dmin, dmax, eps, beta_aware);
+            double a = phase1_step(d, k + kk, k_tilde + kk, K, beta[gg],
+                                   r ? r + (r_per_key ? kk : gg) : NULL, r_per_key, eta, dmin, dmax,
+                                   eps, beta_aware);
             if (a_out) a_out[gg] = a;
         }
         memcpy(d_out + (size_t)bh * K, d, sizeof(double) * K);
@@ -161,7 +167,7 @@ int oracle_delta_phase2(const double *q, const double *k, const double *k_tilde,
  * emit k~_t with d_t, step d, read u_t with the ORIGINAL k_t, write with k~_t, read out o_t.
  * Optional diagnostics: a_out [B,T,H] = beta_t <d_t, k_t^2>, u2_out [B,T,H] = |u_t|^2. */
 int oracle_osdn_forward(const double *q, const double *k, const double *v, const double *beta,
-                        const double *r, const double *d0, const double *S0, double *o,
+                        const double *r, int r_per_key, const double *d0, const double *S0, double *o,
                         double *S_out, double *d_out, double *k_tilde, double *a_out,
                         double *u2_out, int B, int T, int H, int K, int V, double eta,
                         double dmin, double dmax, double eps, int beta_aware, double scale,
@@ -184,8 +190,8 @@ int oracle_osdn_forward(const double *q, const double *k, const double *v, const
         for (long t = 0; t < T; ++t) {
             size_t kk = ix4(b, t, h, 0, T, H, K), vv = ix4(b, t, h, 0, T, H, V);
             size_t gg = ix4(b, t, h, 0, T, H, 1);
-            double a = phase1_step(d, k + kk, kt, K, beta[gg], r ? r[gg] : 1.0, eta, dmin, dmax,
-                                   eps, beta_aware);
+            double a = phase1_step(d, k + kk, kt, K, beta[gg], r ? r + (r_per_key ? kk : gg) : NULL,
+                                   r_per_key, eta, dmin, dmax, eps, beta_aware);
             if (k_tilde) memcpy(k_tilde + kk, kt, sizeof(double) * K);
             double u2 = phase2_step(S, q + kk, k + kk, kt, v + vv, beta[gg], o + vv, K, V, scale, u);
             if (a_out) a_out[gg] = a;
@@ -202,9 +208,10 @@ int oracle_osdn_forward(const double *q, const double *k, const double *v, const
 }
 
 /* One recurrent decode step, in place on S [B,H,V,K] and d [B,H,K]: the forward above for a
- * single token.  q, k [B,H,K]; v, o [B,H,V]; beta, r [B,H] (r may be NULL). */
+ * single token.  q, k [B,H,K]; v, o [B,H,V]; beta, r [B,H] (r [B,H,K] with r_per_key; r may be
+ * NULL). */
 int oracle_decode_step(const double *q, const double *k, const double *v, const double *beta,
-                       const double *r, double *S, double *d, double *o, int B, int H, int K,
+                       const double *r, int r_per_key, double *S, double *d, double *o, int B, int H, int K,
                        int V, double eta, double dmin, double dmax, double eps, int beta_aware,
                        double scale, int nthreads)
 {
@@ -216,8 +223,9 @@ int oracle_decode_step(const double *q, const double *k, const double *v, const 
         size_t sz = (size_t)V * K;
         double *kt = malloc(sizeof(double) * K);
         double *u = malloc(sizeof(double) * V);
-        phase1_step(d + (size_t)bh * K, k + (size_t)bh * K, kt, K, beta[bh], r ? r[bh] : 1.0, eta,
-                    dmin, dmax, eps, beta_aware);
+        phase1_step(d + (size_t)bh * K, k + (size_t)bh * K, kt, K, beta[bh],
+                    r ? r + (r_per_key ? (size_t)bh * K : (size_t)bh) : NULL, r_per_key, eta, dmin,
+                    dmax, eps, beta_aware);
         phase2_step(S + (size_t)bh * sz, q + (size_t)bh * K, k + (size_t)bh * K, kt,
                     v + (size_t)bh * V, beta[bh], o + (size_t)bh * V, K, V, scale, u);
         free(u);

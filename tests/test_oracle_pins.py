@@ -382,3 +382,53 @@ def test_scale_multiplies_readout():
     b = oracle.osdn_forward(q, k, v, beta, scale=0.125)
     np.testing.assert_allclose(b["o"], 0.125 * a["o"], rtol=1e-15, atol=0)
     np.testing.assert_array_equal(a["S"], b["S"])
+
+
+# ---------------------------------------------------------------------------------------------
+# Vector retention (Appendix A.5, Prop. A.3): r_{t,h} I becomes diag(r_t), one gate per key
+# coordinate, with the rest of the step unchanged.
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("beta_aware", [True, False])
+def test_vector_retention_step_is_the_affine_matrix_form(beta_aware):
+    """Prop. A.3 written as a matrix: d' = (diag(r) - eta b^2 / n s s^T) d + eta b / n s."""
+    g = rng(21)
+    K = 7
+    for trial in range(5):
+        k = g.standard_normal(K)
+        beta = float(1 / (1 + np.exp(-g.standard_normal())))
+        r = 1 / (1 + np.exp(-(1.5 + g.standard_normal(K))))
+        d0 = g.uniform(0.6, 1.8, size=K)
+        eta = 0.3
+        b = beta if beta_aware else 1.0
+        s = k * k
+        n = max(s.sum(), 1e-6)
+        want = (np.diag(r) - eta * b * b / n * np.outer(s, s)) @ d0 + eta * b / n * s
+        kt, d1 = oracle.precond_scan(k[None, None, None], np.array([[[beta]]]), r[None, None, None],
+                                     d0[None, None], eta=eta, d_min=-INF, d_max=INF, beta_aware=beta_aware)
+        np.testing.assert_allclose(d1[0, 0], want, rtol=1e-13, atol=1e-15)
+        np.testing.assert_array_equal(kt[0, 0, 0], d0 * k)  # emitted with the old d
+        _, d1c = oracle.precond_scan(k[None, None, None], np.array([[[beta]]]), r[None, None, None],
+                                     d0[None, None], eta=eta, d_min=0.9, d_max=1.2, beta_aware=beta_aware)
+        np.testing.assert_allclose(d1c[0, 0], np.clip(want, 0.9, 1.2), rtol=1e-13, atol=1e-15)
+
+
+def test_vector_retention_with_equal_gates_is_the_scalar_gate():
+    q, k, v, beta, r = rand_problem(22, B=2, T=24, H=2, K=8, V=5, apf=True)
+    a = oracle.osdn_forward(q, k, v, beta, r, eta=0.2)
+    b = oracle.osdn_forward(q, k, v, beta, np.repeat(r[..., None], k.shape[-1], axis=-1), eta=0.2)
+    for key in ("o", "S", "d", "k_tilde"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_vector_retention_eta0_is_a_product_of_gates():
+    """eta = 0: d_t = d_0 . prod_{s<t} r_s per coordinate (inside the box), k~_t = d_t . k_t."""
+    g = rng(23)
+    B, T, H, K = 1, 12, 2, 5
+    k = g.standard_normal((B, T, H, K))
+    beta = np.full((B, T, H), 0.5)
+    r = g.uniform(0.8, 1.0, size=(B, T, H, K))
+    d0 = g.uniform(0.8, 1.5, size=(B, H, K))
+    kt, d = oracle.precond_scan(k, beta, r, d0, eta=0.0, d_min=0.0, d_max=INF)
+    prod = np.concatenate([np.ones((B, 1, H, K)), np.cumprod(r, axis=1)], axis=1)  # prod_{s<t}
+    np.testing.assert_allclose(kt, d0[:, None] * prod[:, :T] * k, rtol=1e-13)
+    np.testing.assert_allclose(d, d0 * prod[:, T], rtol=1e-13)
