@@ -345,6 +345,7 @@ def run_ours(args, w):
 
     e2e = run_e2e(args, w, host, dev, stream, ws)
     decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak)
+    vret = None if args.no_vector_retention else run_vector_retention(args, dev, stream, hbm_peak)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, secs, sample, threads = oracle_layer_rate(w, host, budget_s=args.ref_budget)
@@ -360,7 +361,8 @@ def run_ours(args, w):
                        "chunk": w.chunk, "eta": w.eta, "box": [w.d_min, w.d_max],
                        "l2": "flushed between steps (256 MiB write outside the timed events)"},
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "decode": decode, "gpu_launches": launches_per_step * n, "clocks": clk.summary(),
+            "decode": decode, "vector_retention": vret,
+            "gpu_launches": launches_per_step * n, "clocks": clk.summary(),
             "wall_s_timed_region": wall,
         }
         print(json.dumps(line), flush=True)
@@ -466,6 +468,51 @@ def run_decode(args, dev, stream, hbm_peak):
             "timing": "CUDA graph of all steps, median of reps"}
 
 
+def run_vector_retention(args, dev, stream, hbm_peak):
+    """Phase 1 with one APF gate per key coordinate (diag(r_t), the pages' Appendix A.5) on the
+    1.3B-shaped workload (B=4, H=16, T=4096, bf16 keys): the token-by-token scan kernel, gates
+    sigmoid(4 + N(0, 1)) in fp32 resident in HBM, L2 flushed between reps.  The per-head gate's
+    blocked scan on the same inputs is timed beside it."""
+    from preconditioned_delta_rule_gb300 import binding
+    from preconditioned_delta_rule_gb300 import workloads as W
+
+    w = W.WORKLOADS["layer_1p3b_apf"]
+    inp = W.make_prefill(w)
+    k, beta, r_head = inp["k"].to(dev), inp["beta"].to(dev), inp["r"].to(dev)
+    g = torch.Generator().manual_seed(4)
+    r_vec = torch.sigmoid(4.0 + torch.randn(w.B, w.T, w.H, w.K, generator=g)).to(dev)
+    kt = torch.empty_like(k)
+    dout = torch.empty((w.B, w.H, w.K), device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    kw = dict(k_tilde=kt, d_out=dout, eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+
+    def timed(r):
+        binding.osdn_precond_scan(k, beta, r, **kw)  # warm-up
+        times = []
+        for i in range(max(3, args.decode_reps)):
+            flush.fill_(float(i))
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record(stream)
+            binding.osdn_precond_scan(k, beta, r, **kw)
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+        binding.osdn_check()
+        return statistics.median(times)
+
+    secs_v = timed(r_vec)
+    secs_h = timed(r_head)
+    th = w.B * w.T * w.H
+    b = th * (2 * w.K + 4 + 4 * w.K + 2 * w.K) + w.B * w.H * 2 * w.K * 4  # k, beta, r, k~; d0/d
+    ach = b / secs_v / 1e9
+    return {"workload": w.name + "_vector_retention", "B": w.B, "H": w.H, "T": w.T, "K": w.K,
+            "value": th / secs_v / w.H, "unit": "tokens/s", "ms": secs_v * 1e3,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": ach / hbm_peak, "algorithmic_bytes_per_launch": b},
+            "per_head_gate_ms": secs_h * 1e3, "kernel": "scan_warp_kernel (token by token)",
+            "l2": "flushed between reps (256 MiB write outside the timed events)"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,6 +524,7 @@ def main():
     ap.add_argument("--decode-reps", type=int, default=3)
     ap.add_argument("--ref-budget", type=float, default=12.0, help="CPU seconds per oracle sample")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-vector-retention", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -68,7 +68,11 @@ typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1, OSDN_F16 = 2 } osdn_dtype;
  * Phase 1: preconditioner scan (Algorithm 1 / Eq. (4); Eq. (7) when r != NULL).
  *   k        [B,T,H,K] keys, dtype k_dtype (read)
  *   beta     [B,T,H] fp32 write gates in (0,1) (read)
- *   r        [B,T,H] fp32 APF retention r_{t,h}, broadcast over K; NULL means r = 1 (Eq. (4))
+ *   r        fp32 APF retention; NULL means r = 1 (Eq. (4)).  r_per_key = 0: [B,T,H], one
+ *            r_{t,h} broadcast over K (Eq. (7)); r_per_key = 1: [B,T,H,K], the vector retention
+ *            diag(r_t) of Appendix A.5 (Prop. A.3), one gate per key coordinate.  Other values of
+ *            r_per_key return OSDN_ERR_ARG.  The blocked scan covers one gate per head; vector
+ *            retention runs the token-by-token kernel.
  *   d0       [B,H,K] fp32 initial preconditioner; NULL means d = 1.  Used as given (not clamped).
  *   k_tilde  [B,T,H,K] write keys k~_t = d_t . k_t, dtype kt_dtype (written)
  *   d_out    [B,H,K] fp32 final d_{T} (written; may alias d0)
@@ -85,7 +89,7 @@ typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1, OSDN_F16 = 2 } osdn_dtype;
  *   T may be 0 (then d_out = d0 or 1).
  */
 osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* beta,
-                              const float* r, const float* d0, void* k_tilde,
+                              const float* r, int r_per_key, const float* d0, void* k_tilde,
                               osdn_dtype kt_dtype, float* d_out, int B, int T, int H, int K,
                               float eta, float d_min, float d_max, float eps, int beta_aware,
                               void* workspace, size_t workspace_bytes, void* stream);
@@ -135,6 +139,7 @@ size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
  * osdn_chunk_fwd; q, k, v and the write keys share `dtype`.
  *   k_tilde  [B,T,H,K] write keys, dtype `dtype` (written; the phase-2 input)
  *   o, S_out as osdn_chunk_fwd; d_out as osdn_precond_scan (both written)
+ *   r, r_per_key as osdn_precond_scan (vector retention always takes the two separate calls)
  *   workspace, workspace_bytes
  *            optional caller-owned device scratch (16-byte aligned).  With at least
  *            osdn_layer_fwd_workspace_bytes(...) bytes, bf16/f16 inputs with K = V = 128 and
@@ -146,7 +151,7 @@ size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
  *   T must be a multiple of `chunk` (64).
  */
 osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
-                           const float* r, const float* d0, const float* S0, void* k_tilde, void* o,
+                           const float* r, int r_per_key, const float* d0, const float* S0, void* k_tilde, void* o,
                            float* S_out, float* d_out, int B, int T, int H, int K, int V, int chunk,
                            float eta, float d_min, float d_max, float eps, float scale, int beta_aware,
                            void* workspace, size_t workspace_bytes, void* stream);
@@ -183,11 +188,12 @@ osdn_status osdn_chunk_fwd_static_ws(const void* q, const void* k, const void* k
  * One decode token for every (batch, head), in place (recurrent form of both phases):
  *   k~ = d . k (old d); d <- clip(r d + eta b (1 - b <d, k.k>) / max(|k|^2, eps) k.k);
  *   u = v - S k;  S <- S + beta u k~^T;  o = scale * S q.
- *   q, k [B,H,K], v [B,H,V] of dtype `dtype`; beta, r [B,H] fp32 (r may be NULL);
+ *   q, k [B,H,K], v [B,H,V] of dtype `dtype`; beta [B,H] fp32; r fp32 or NULL: [B,H] with
+ *   r_per_key = 0, or [B,H,K] (one gate per key coordinate, diag(r_t)) with r_per_key = 1;
  *   S [B,H,V,K] fp32 and d [B,H,K] fp32 are read and overwritten; o [B,H,V] dtype `dtype`.
  */
 osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,
-                             const float* beta, const float* r, float* S, float* d, void* o,
+                             const float* beta, const float* r, int r_per_key, float* S, float* d, void* o,
                              int B, int H, int K, int V, float eta, float d_min, float d_max,
                              float eps, float scale, int beta_aware, void* stream);
 

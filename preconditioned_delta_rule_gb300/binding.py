@@ -44,7 +44,7 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(str(LIB_PATH))
     vp, fp, i, f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     sz = ctypes.c_size_t
-    L.osdn_precond_scan.argtypes = [vp, i, fp, fp, fp, vp, i, fp, i, i, i, i, f, f, f, f, i, vp, sz, vp]
+    L.osdn_precond_scan.argtypes = [vp, i, fp, fp, i, fp, vp, i, fp, i, i, i, i, f, f, f, f, i, vp, sz, vp]
     L.osdn_precond_scan_workspace_bytes.argtypes = [i, i, i, i, i]
     L.osdn_precond_scan_workspace_bytes.restype = sz
     L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp, sz, vp]
@@ -52,12 +52,12 @@ def lib() -> ctypes.CDLL:
     L.osdn_chunk_fwd_workspace_bytes.restype = sz
     L.osdn_chunk_fwd_static_ws.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp]
     L.osdn_chunk_fwd_static_ws.restype = ctypes.c_int
-    L.osdn_layer_fwd.argtypes = [vp, vp, vp, i, fp, fp, fp, fp, vp, vp, fp, fp, i, i, i, i, i, i,
+    L.osdn_layer_fwd.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, vp, vp, fp, fp, i, i, i, i, i, i,
                                  f, f, f, f, f, i, vp, sz, vp]
     L.osdn_layer_fwd.restype = ctypes.c_int
     L.osdn_layer_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.osdn_layer_fwd_workspace_bytes.restype = sz
-    L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
+    L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
     L.osdn_check.argtypes = [vp]
     for fn in ("osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step", "osdn_check"):
         getattr(L, fn).restype = ctypes.c_int
@@ -114,10 +114,21 @@ def _code(dtype) -> int:
     return _DTYPE_CODE[dtype]
 
 
+def _retention(r, head_shape, K, dev):
+    """Check the retention and say its layout: 0 for one gate per head (``head_shape``, Eq. (7)),
+    1 for one per key coordinate (``head_shape + (K,)``, the vector retention diag(r_t))."""
+    if r is None:
+        return 0
+    per_key = tuple(r.shape) == tuple(head_shape) + (K,)
+    _check("r", r, tuple(head_shape) + ((K,) if per_key else ()), torch.float32, dev)
+    return int(per_key)
+
+
 def osdn_precond_scan(k, beta, r=None, d0=None, *, k_tilde=None, kt_dtype=None, d_out=None,
                       eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6, beta_aware=True, workspace=None,
                       stream=None):
     """Phase 1 (Algorithm 1 / Eq. (4); APF Eq. (7) with r).  k [B,T,H,K] -> (k_tilde, d_out).
+    r is [B,T,H] (one retention per head) or [B,T,H,K] (vector retention, one per coordinate).
 
     ``workspace``: None (default) uses a cached torch buffer of the size the library asks for;
     a uint8 CUDA tensor is used as given; False makes the scan kernel write k_tilde itself."""
@@ -125,7 +136,7 @@ def osdn_precond_scan(k, beta, r=None, d0=None, *, k_tilde=None, kt_dtype=None, 
     dev = k.device
     _check("k", k, (B, T, H, K), device=dev)
     _check("beta", beta, (B, T, H), torch.float32, dev)
-    _check("r", r, (B, T, H), torch.float32, dev)
+    r_per_key = _retention(r, (B, T, H), K, dev)
     _check("d0", d0, (B, H, K), torch.float32, dev)
     if k_tilde is None:
         k_tilde = torch.empty((B, T, H, K), device=dev, dtype=kt_dtype or k.dtype)
@@ -135,7 +146,7 @@ def osdn_precond_scan(k, beta, r=None, d0=None, *, k_tilde=None, kt_dtype=None, 
     _check("d_out", d_out, (B, H, K), torch.float32, dev)
     need = osdn_precond_scan_workspace_bytes(B, T, H, K, k.dtype)
     ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "scan")
-    st = lib().osdn_precond_scan(_ptr(k), _code(k.dtype), _ptr(beta), _ptr(r), _ptr(d0),
+    st = lib().osdn_precond_scan(_ptr(k), _code(k.dtype), _ptr(beta), _ptr(r), r_per_key, _ptr(d0),
                                  _ptr(k_tilde), _code(k_tilde.dtype), _ptr(d_out), B, T, H, K,
                                  float(eta), float(d_min), float(d_max), float(eps),
                                  int(bool(beta_aware)), ws_ptr, ws_bytes, _stream(dev, stream))
@@ -211,20 +222,21 @@ def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, o=None, S_out=None, chunk
 
 def osdn_decode_step(q, k, v, beta, S, d, r=None, *, o=None, eta=0.003, d_min=0.5, d_max=2.0,
                      eps=1e-6, scale=1.0, beta_aware=True, stream=None):
-    """One decode token in place on S [B,H,V,K] and d [B,H,K].  Returns o [B,H,V]."""
+    """One decode token in place on S [B,H,V,K] and d [B,H,K].  Returns o [B,H,V].  r is [B,H]
+    or [B,H,K] (vector retention)."""
     B, H, K = k.shape
     V = v.shape[-1]
     dev, dt = k.device, k.dtype
     _check("q", q, (B, H, K), dt, dev)
     _check("v", v, (B, H, V), dt, dev)
     _check("beta", beta, (B, H), torch.float32, dev)
-    _check("r", r, (B, H), torch.float32, dev)
+    r_per_key = _retention(r, (B, H), K, dev)
     _check("S", S, (B, H, V, K), torch.float32, dev)
     _check("d", d, (B, H, K), torch.float32, dev)
     if o is None:
         o = torch.empty((B, H, V), device=dev, dtype=dt)
     _check("o", o, (B, H, V), dt, dev)
-    st = lib().osdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r),
+    st = lib().osdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key,
                                 _ptr(S), _ptr(d), _ptr(o), B, H, K, V, float(eta), float(d_min),
                                 float(d_max), float(eps), float(scale), int(bool(beta_aware)),
                                 _stream(dev, stream))
@@ -255,7 +267,7 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, k_tilde=None, o=N
     for name, t, shp in (("q", q, (B, T, H, K)), ("k", k, (B, T, H, K)), ("v", v, (B, T, H, V))):
         _check(name, t, shp, dt, dev)
     _check("beta", beta, (B, T, H), torch.float32, dev)
-    _check("r", r, (B, T, H), torch.float32, dev)
+    r_per_key = _retention(r, (B, T, H), K, dev)
     _check("d0", d0, (B, H, K), torch.float32, dev)
     _check("S0", S0, (B, H, V, K), torch.float32, dev)
     if k_tilde is None:
@@ -272,7 +284,7 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, k_tilde=None, o=N
     _check("d_out", d_out, (B, H, K), torch.float32, dev)
     need = osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 and T % chunk == 0 else 0
     ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "layer")
-    st = lib().osdn_layer_fwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), _ptr(d0),
+    st = lib().osdn_layer_fwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, _ptr(d0),
                               _ptr(S0), _ptr(k_tilde), _ptr(o), _ptr(S_out), _ptr(d_out), B, T, H, K,
                               V, int(chunk), float(eta), float(d_min), float(d_max), float(eps),
                               float(scale), int(bool(beta_aware)), ws_ptr, ws_bytes,

@@ -48,7 +48,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 extern "C" {
 
 osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* beta,
-                              const float* r, const float* d0, void* k_tilde,
+                              const float* r, int r_per_key, const float* d0, void* k_tilde,
                               osdn_dtype kt_dtype, float* d_out, int B, int T, int H, int K,
                               float eta, float d_min, float d_max, float eps, int beta_aware,
                               void* workspace, size_t workspace_bytes, void* stream) {
@@ -56,6 +56,7 @@ osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* be
     if (!head_dim_ok(K)) return K > 0 ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
     if (!dtype_ok(k_dtype) || !dtype_ok(kt_dtype)) return OSDN_ERR_DTYPE;
     OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
+    if (r_per_key != 0 && r_per_key != 1) return OSDN_ERR_ARG;
     if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
     if (B == 0 || H == 0) return OSDN_OK;
     const bool seq = T > 0;
@@ -67,7 +68,7 @@ osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* be
     OSDN_TRY(ptr(d_out, true));
     OSDN_TRY(ptr(workspace, false));
     OsdnScanArgs a{k, k_dtype, beta, r, d0, k_tilde, kt_dtype, d_out, B, T, H, K,
-                   eta, d_min, d_max, eps, beta_aware ? 1 : 0};
+                   eta, d_min, d_max, eps, beta_aware ? 1 : 0, r != nullptr ? r_per_key : 0};
     return from_cuda(osdn_launch_scan(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
@@ -114,7 +115,7 @@ size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
 }
 
 osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
-                           const float* r, const float* d0, const float* S0, void* k_tilde, void* o,
+                           const float* r, int r_per_key, const float* d0, const float* S0, void* k_tilde, void* o,
                            float* S_out, float* d_out, int B, int T, int H, int K, int V, int chunk,
                            float eta, float d_min, float d_max, float eps, float scale, int beta_aware,
                            void* workspace, size_t workspace_bytes, void* stream) {
@@ -125,6 +126,7 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
     if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
     OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
     if (!isfinite(scale)) return OSDN_ERR_ARG;
+    if (r_per_key != 0 && r_per_key != 1) return OSDN_ERR_ARG;
     if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
     if (B == 0 || H == 0) return OSDN_OK;
     const bool seq = T > 0;
@@ -140,7 +142,8 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
     OSDN_TRY(ptr(S_out, true));
     OSDN_TRY(ptr(d_out, true));
     OSDN_TRY(ptr(workspace, false));
-    OsdnScanArgs sa{k, dtype, beta, r, d0, k_tilde, dtype, d_out, B, T, H, K, eta, d_min, d_max, eps, beta_aware ? 1 : 0};
+    OsdnScanArgs sa{k, dtype, beta, r, d0, k_tilde, dtype, d_out, B, T, H, K, eta, d_min, d_max, eps, beta_aware ? 1 : 0,
+                    r != nullptr ? r_per_key : 0};
     OsdnChunkArgs ca{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (seq) {
@@ -179,7 +182,7 @@ size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
 }
 
 osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,
-                             const float* beta, const float* r, float* S, float* d, void* o,
+                             const float* beta, const float* r, int r_per_key, float* S, float* d, void* o,
                              int B, int H, int K, int V, float eta, float d_min, float d_max,
                              float eps, float scale, int beta_aware, void* stream) {
     if (B < 0 || H < 0) return OSDN_ERR_SHAPE;
@@ -187,6 +190,7 @@ osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_d
     if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
     OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
     if (!isfinite(scale)) return OSDN_ERR_ARG;
+    if (r_per_key != 0 && r_per_key != 1) return OSDN_ERR_ARG;
     if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
     if (B == 0 || H == 0) return OSDN_OK;
     OSDN_TRY(ptr(q, true));
@@ -198,7 +202,7 @@ osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_d
     OSDN_TRY(ptr(d, true));
     OSDN_TRY(ptr(o, true));
     OsdnDecodeArgs a{q, k, v, dtype, beta, r, S, d, o, B, H, K, V,
-                     eta, d_min, d_max, eps, scale, beta_aware ? 1 : 0};
+                     eta, d_min, d_max, eps, scale, beta_aware ? 1 : 0, r != nullptr ? r_per_key : 0};
     return from_cuda(osdn_launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 

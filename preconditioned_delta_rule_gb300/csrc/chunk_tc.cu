@@ -1446,7 +1446,7 @@ LayerWs layer_ws(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
 }
 
 bool layer_covers(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
-    return tc_covers(ca) && ca.V == KD && sa.K == KD && sa.k_dtype == ca.dtype && sa.kt_dtype == ca.dtype &&
+    return tc_covers(ca) && ca.V == KD && sa.K == KD && sa.k_dtype == ca.dtype && sa.kt_dtype == ca.dtype && !sa.r_per_key &&
            ca.B * ca.H < num_sms() && osdn_scan_block_workspace_bytes(sa) > 0;
 }
 

@@ -98,6 +98,7 @@ struct OsdnScanArgs {
     const void* k; osdn_dtype k_dtype; const float* beta; const float* r; const float* d0;
     void* k_tilde; osdn_dtype kt_dtype; float* d_out;
     int B, T, H, K; float eta, d_min, d_max, eps; int beta_aware;
+    int r_per_key;  // 1: r [B,T,H,K], one retention per key coordinate (vector retention)
 };
 struct OsdnChunkArgs {
     const void* q; const void* k; const void* k_tilde; const void* v; osdn_dtype dtype;
@@ -108,6 +109,7 @@ struct OsdnDecodeArgs {
     const void* q; const void* k; const void* v; osdn_dtype dtype; const float* beta;
     const float* r; float* S; float* d; void* o;
     int B, H, K, V; float eta, d_min, d_max, eps, scale; int beta_aware;
+    int r_per_key;  // 1: r [B,H,K], one retention per key coordinate (vector retention)
 };
 
 // Phase-1 scan.  16-bit keys with K = 128 use the blocked kernel; with a workspace of at least

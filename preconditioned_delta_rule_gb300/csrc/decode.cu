@@ -30,7 +30,8 @@ __device__ __forceinline__ void st_stream(float* p, float4 v) {
                  "f"(v.z), "f"(v.w) : "memory");
 }
 
-template <int K, int V, typename TIn, bool HAS_R>
+// RMODE: 0 no retention, 1 one per head (Eq. (7)), 2 one per key coordinate (diag(r_t), Appendix A.5)
+template <int K, int V, typename TIn, int RMODE>
 __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
     constexpr int P4 = K / 4 / kLanesPerRow;        // float4 pieces per lane per row (4 or 2)
     constexpr int ROWS_PER_PASS = kThreads / kLanesPerRow;  // 32
@@ -67,12 +68,18 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
         al = warp_sum(al);
         ktq = warp_sum(ktq);
         const float bt = a.beta[bh];
-        const float rt = HAS_R ? a.r[bh] : 1.f;
+        float rv[E];
+        if (RMODE == 2) {
+            VecIO<float, E>::load(a.r + bh * K + tid * E, rv);
+        } else {
+#pragma unroll
+            for (int i = 0; i < E; ++i) rv[i] = RMODE == 1 ? a.r[bh] : 1.f;
+        }
         const float bp = a.beta_aware ? bt : 1.f;
         const float g = a.eta * bp * (1.f - bp * al) / fmaxf(n, a.eps);
         float dn[E];
 #pragma unroll
-        for (int i = 0; i < E; ++i) dn[i] = fminf(fmaxf(fmaf(g, s[i], rt * dv[i]), a.d_min), a.d_max);
+        for (int i = 0; i < E; ++i) dn[i] = fminf(fmaxf(fmaf(g, s[i], rv[i] * dv[i]), a.d_min), a.d_max);
         VecIO<float, E>::store(a.d + bh * K + tid * E, dn);
         if (tid == 0) {
             scoef[0] = bt;
@@ -138,8 +145,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
 template <int K, int V, typename TIn>
 cudaError_t launch3(const OsdnDecodeArgs& a, cudaStream_t s) {
     dim3 grid((unsigned)(a.B * a.H)), block(kThreads);
-    if (a.r) decode_kernel<K, V, TIn, true><<<grid, block, 0, s>>>(a);
-    else decode_kernel<K, V, TIn, false><<<grid, block, 0, s>>>(a);
+    if (a.r && a.r_per_key) decode_kernel<K, V, TIn, 2><<<grid, block, 0, s>>>(a);
+    else if (a.r) decode_kernel<K, V, TIn, 1><<<grid, block, 0, s>>>(a);
+    else decode_kernel<K, V, TIn, 0><<<grid, block, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -51,14 +51,19 @@ __device__ __forceinline__ void d_step(float& hi, float& lo, float r, float g, f
     lo = l2;
 }
 
-template <int K, typename TIn, typename TOut, bool HAS_R>
+// RMODE: 0 no retention, 1 one retention per head and token (Eq. (7)), 2 one per key coordinate
+// (vector retention diag(r_t), Appendix A.5), staged with the keys, 16 tokens at a time.
+template <int K, typename TIn, typename TOut, int RMODE>
 __global__ void __launch_bounds__(32) scan_warp_kernel(OsdnScanArgs a) {
+    constexpr bool HAS_R = RMODE != 0;
+    constexpr int NST = RMODE == 2 ? kStageTokens / 2 : kStageTokens;
     constexpr int E = K / 32;
     constexpr int ROWB = K * (int)sizeof(TIn);
     constexpr int PIECES = ROWB / 16;
-    __shared__ __align__(16) unsigned char kbuf[2][kStageTokens * ROWB];
-    __shared__ float bbuf[2][kStageTokens];
-    __shared__ float rbuf[2][kStageTokens];
+    constexpr int RROW = RMODE == 2 ? K : 1;  // retention floats per token
+    __shared__ __align__(16) unsigned char kbuf[2][NST * ROWB];
+    __shared__ float bbuf[2][NST];
+    __shared__ __align__(16) float rbuf[2][NST * RROW];
 
     const int lane = threadIdx.x;
     const int bh = blockIdx.x;
@@ -76,34 +81,43 @@ __global__ void __launch_bounds__(32) scan_warp_kernel(OsdnScanArgs a) {
     }
 
     auto stage = [&](int buf, int t0) {
-        const int nt = min(kStageTokens, T - t0);
+        const int nt = min(NST, T - t0);
         for (int i = lane; i < nt * PIECES; i += 32) {
             const int tt = i / PIECES, c = i - tt * PIECES;
             const unsigned char* src =
                 reinterpret_cast<const unsigned char*>(kg + (row0 + (size_t)(t0 + tt) * H) * K) + c * 16;
             cp_async_16(&kbuf[buf][tt * ROWB + c * 16], src);
         }
+        if (RMODE == 2) {  // K fp32 per token, 16-byte pieces
+            for (int i = lane; i < nt * (K / 4); i += 32) {
+                const int tt = i / (K / 4), c = i - tt * (K / 4);
+                cp_async_16(&rbuf[buf][tt * K + c * 4], a.r + (row0 + (size_t)(t0 + tt) * H) * K + c * 4);
+            }
+        }
         if (lane < nt) {
             cp_async_4(&bbuf[buf][lane], a.beta + row0 + (size_t)(t0 + lane) * H);
-            if (HAS_R) cp_async_4(&rbuf[buf][lane], a.r + row0 + (size_t)(t0 + lane) * H);
+            if (RMODE == 1) cp_async_4(&rbuf[buf][lane], a.r + row0 + (size_t)(t0 + lane) * H);
         }
         cp_async_commit();
     };
 
     if (T > 0) stage(0, 0);
-    for (int t0 = 0, it = 0; t0 < T; t0 += kStageTokens, ++it) {
+    for (int t0 = 0, it = 0; t0 < T; t0 += NST, ++it) {
         const int buf = it & 1;
-        if (t0 + kStageTokens < T) stage(buf ^ 1, t0 + kStageTokens);
+        if (t0 + NST < T) stage(buf ^ 1, t0 + NST);
         else cp_async_commit();
         cp_async_wait_1();
         __syncwarp();
-        const int nt = min(kStageTokens, T - t0);
+        const int nt = min(NST, T - t0);
 #pragma unroll 2
         for (int tt = 0; tt < nt; ++tt) {
             float kv[E];
             VecIO<TIn, E>::load(reinterpret_cast<const TIn*>(&kbuf[buf][tt * ROWB]) + lane * E, kv);
             const float bt = bbuf[buf][tt];
-            const float rt = HAS_R ? rbuf[buf][tt] : 1.f;
+            float rv[E];
+#pragma unroll
+            for (int i = 0; i < E; ++i)
+                rv[i] = RMODE == 2 ? rbuf[buf][tt * RROW + lane * E + i] : (HAS_R ? rbuf[buf][tt] : 1.f);
             float s[E], n = 0.f, al = 0.f, ko[E];
 #pragma unroll
             for (int i = 0; i < E; ++i) {
@@ -122,7 +136,7 @@ __global__ void __launch_bounds__(32) scan_warp_kernel(OsdnScanArgs a) {
             const float bp = a.beta_aware ? bt : 1.f;
             const float g = a.eta * bp * (1.f - bp * al) / nbar;
 #pragma unroll
-            for (int i = 0; i < E; ++i) d_step(dh[i], dl[i], rt, g, s[i], a.d_min, a.d_max);
+            for (int i = 0; i < E; ++i) d_step(dh[i], dl[i], rv[i], g, s[i], a.d_min, a.d_max);
         }
         __syncwarp();
     }
@@ -134,8 +148,9 @@ __global__ void __launch_bounds__(32) scan_warp_kernel(OsdnScanArgs a) {
 template <int K, typename TIn, typename TOut>
 cudaError_t launch_k(const OsdnScanArgs& a, cudaStream_t s) {
     dim3 grid((unsigned)(a.B * a.H)), block(32);
-    if (a.r) scan_warp_kernel<K, TIn, TOut, true><<<grid, block, 0, s>>>(a);
-    else scan_warp_kernel<K, TIn, TOut, false><<<grid, block, 0, s>>>(a);
+    if (a.r && a.r_per_key) scan_warp_kernel<K, TIn, TOut, 2><<<grid, block, 0, s>>>(a);
+    else if (a.r) scan_warp_kernel<K, TIn, TOut, 1><<<grid, block, 0, s>>>(a);
+    else scan_warp_kernel<K, TIn, TOut, 0><<<grid, block, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -175,7 +175,8 @@ cudaError_t osdn_scan_block_read_and_clear_timeout(unsigned int* flag) {
 }
 
 bool osdn_scan_block_covers(const OsdnScanArgs& a) {
-    return a.K == osdn::KD && a.T > 0 && (a.k_dtype == OSDN_BF16 || a.k_dtype == OSDN_F16);
+    // (one retention per head: the blocked solve scales the Gram by scalar products of gates)
+    return a.K == osdn::KD && a.T > 0 && (a.k_dtype == OSDN_BF16 || a.k_dtype == OSDN_F16) && !a.r_per_key;
 }
 
 size_t osdn_scan_block_workspace_bytes(const OsdnScanArgs& a) {
