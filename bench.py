@@ -346,6 +346,7 @@ def run_ours(args, w):
     e2e = run_e2e(args, w, host, dev, stream, ws)
     decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak)
     vret = None if args.no_vector_retention else run_vector_retention(args, dev, stream, hbm_peak)
+    configs = None if args.no_configs else run_configs(args, dev, stream, hbm_peak)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, secs, sample, threads = oracle_layer_rate(w, host, budget_s=args.ref_budget)
@@ -361,7 +362,7 @@ def run_ours(args, w):
                        "chunk": w.chunk, "eta": w.eta, "box": [w.d_min, w.d_max],
                        "l2": "flushed between steps (256 MiB write outside the timed events)"},
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "decode": decode, "vector_retention": vret,
+            "decode": decode, "other_configs": configs, "vector_retention": vret,
             "gpu_launches": launches_per_step * n, "clocks": clk.summary(),
             "wall_s_timed_region": wall,
         }
@@ -468,6 +469,59 @@ def run_decode(args, dev, stream, hbm_peak):
             "timing": "CUDA graph of all steps, median of reps"}
 
 
+def run_configs(args, dev, stream, hbm_peak, names=("layer_1p3b_apf", "longctx_raw", "longctx_unit")):
+    """The other prefill configs: osdn_layer_fwd (and, for the breakdown, osdn_precond_scan and
+    osdn_chunk_fwd) on each full-size workload, median of reps, L2 flushed between reps.  The
+    long-context config as written (raw keys) overflows in phase 2; its timing does not depend on
+    the values except through phase 1's clipping, so it is timed as written and with unit keys
+    (the variant its parity tests use)."""
+    from preconditioned_delta_rule_gb300 import binding
+    from preconditioned_delta_rule_gb300 import workloads as W
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    out = []
+    for name in names:
+        w = W.WORKLOADS[name]
+        g = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in W.make_prefill(w).items()}
+        kt = torch.empty_like(g["k"])
+        kw = dict(eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+
+        def layer():
+            binding.osdn_layer_fwd(g["q"], g["k"], g["v"], g["beta"], g["r"], k_tilde=kt, **kw)
+
+        def scan():
+            binding.osdn_precond_scan(g["k"], g["beta"], g["r"], k_tilde=kt, **kw)
+
+        def chunk():
+            binding.osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"])
+
+        def med(fn):
+            fn()
+            times = []
+            for i in range(max(3, args.decode_reps)):
+                flush.fill_(float(i))
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                ev[0].record(stream)
+                fn()
+                ev[1].record(stream)
+                torch.cuda.synchronize()
+                times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+            binding.osdn_check()
+            return statistics.median(times)
+
+        t_layer, t_scan, t_chunk = med(layer), med(scan), med(chunk)
+        b_scan, b_chunk, b_layer = layer_bytes(w)
+        frac = lambda b, t: b / t / 1e9 / hbm_peak
+        out.append({"workload": name, "B": w.B, "H": w.H, "T": w.T, "apf": w.apf,
+                    "layer_ms": t_layer * 1e3, "tokens_per_s": w.B * w.T / t_layer,
+                    "layer_roofline_frac": frac(b_layer, t_layer),
+                    "scan_ms": t_scan * 1e3, "scan_roofline_frac": frac(b_scan, t_scan),
+                    "chunk_ms": t_chunk * 1e3, "chunk_roofline_frac": frac(b_chunk, t_chunk)})
+        del g, kt
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_vector_retention(args, dev, stream, hbm_peak):
     """Phase 1 with one APF gate per key coordinate (diag(r_t), the pages' Appendix A.5) on the
     1.3B-shaped workload (B=4, H=16, T=4096, bf16 keys): the token-by-token scan kernel, gates
@@ -525,6 +579,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=12.0, help="CPU seconds per oracle sample")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-vector-retention", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other prefill configs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -18,10 +18,13 @@
 // as d_64 = rho_64 (d_p + sum_l h_l s_l).  The assumption is checked per coordinate: a cheap
 // sufficient bound on the free trajectory (d_p +- sum_l |h_l| s_l, scaled by the extreme rho),
 // otherwise the exact trajectory; pinned coordinates must keep being clipped at every step.  At
-// the first violation the tokens before it are accepted, the state after it is formed with the
-// clip, and the block restarts there with the new classification (after 8 restarts in a block
-// the rest of the block runs token by token).  The result is the sequential algorithm's, up to
-// reassociation.  d is carried across blocks as an unevaluated fp32 pair (hi + lo).
+// the first violation the tokens before it are accepted and the state after it is formed with
+// the clip.  The rest of the block, and every block that starts with free and pinned coordinates
+// together, is solved by Jacobi sweeps on the clipped recurrence itself: each coordinate runs its
+// own clipped trajectory under a guess of the g's and the products d_j s_j, summed across the
+// coordinates, give the next guess.  The clip is 1-Lipschitz, so the same coupling bound fixes
+// the number of sweeps.  The result is the sequential algorithm's, up to reassociation.  d is
+// carried across blocks as an unevaluated fp32 pair (hi + lo).
 //
 // Mapping: one CTA of 256 threads per (batch, head).  Warpgroup 0 ("chain") runs the serial part
 // above, one key coordinate per thread, reading s = k.k straight from the staged keys (the square
@@ -48,7 +51,6 @@ constexpr int KD = 128;            // key dim (one coordinate per thread of each
 constexpr int NT = 256;
 constexpr int KROW = KD * 2 + 16;  // padded raw key row (16-bit elements), bytes
 constexpr uint32_t kMaxPolls = 1u << 22;
-constexpr int kMaxRestarts = 8;
 
 constexpr uint32_t OFF_KT = 0;                             // 3 raw key tiles
 constexpr uint32_t KT_BYTES = J * KROW;                    // 17408
@@ -96,13 +98,12 @@ static_assert(3 * KT_BYTES <= OFF_SHL, "key tiles");
 static_assert(OFF_SHL % 1024 == 0, "swizzle atoms");
 static_assert(SMEM_ALLOC <= 232448, "shared memory");
 
-constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t COL_G = 0;     // all-free Gram products of the block in slot q: columns 128 q ..
-constexpr uint32_t COL_GM = 256;  // masked Gram products computed by the chain (128 columns)
 
-// mbarriers (offsets from OFF_BAR): gram[2], prep_ready[2], chain_done[2], gram_masked, Gram rows
-// in shared memory[2]
-constexpr uint32_t B_GRAM = 0, B_PREP = 16, B_CHAIN = 32, B_GM = 48, B_MRDY = 56;
+// mbarriers (offsets from OFF_BAR): gram[2], prep_ready[2], chain_done[2], Gram rows in shared
+// memory[2]
+constexpr uint32_t B_GRAM = 0, B_PREP = 16, B_CHAIN = 32, B_MRDY = 48;
 
 __device__ __forceinline__ void cp_async_16z(void* smem, const void* gmem, bool valid) {
     const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
@@ -170,13 +171,19 @@ __device__ __forceinline__ void pair_clip(float& hi, float& lo, float dmin, floa
     if (hi > dmax || (hi == dmax && lo > 0.f)) { hi = dmax; lo = 0.f; }
 }
 
-// Sum over warpgroup 0; every chain thread gets the result.
-__device__ __forceinline__ float chain_sum(float v, float* red, int tid) {
-    v = warp_sum(v);
-    wg_sync(1);
-    if ((tid & 31) == 0) red[tid >> 5] = v;
-    wg_sync(1);
-    return (red[0] + red[1]) + (red[2] + red[3]);
+// One halving step of a sum over the lanes of a warp of L values held by each lane: the lanes
+// with bit O set keep the upper half, the others the lower half, each adding its partner's copy of
+// the half it keeps.  After the steps for O = 16, 8, 4, 2, 1 (L = 64 .. 4) lane l holds in v[0],
+// v[1] the warp sums of entries 2 l and 2 l + 1.
+template <int L, int O>
+__device__ __forceinline__ void rs_level(float (&v)[64], int lane) {
+    const bool up = (lane & O) != 0;
+#pragma unroll
+    for (int t = 0; t < L / 2; ++t) {
+        const float keep = up ? v[t + L / 2] : v[t];
+        const float send = up ? v[t] : v[t + L / 2];
+        v[t] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+    }
 }
 
 // The body of the blocked scan for one (batch, head) `bh`, run by 256 threads of a CTA whose
@@ -214,7 +221,6 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             tc::mbar_init(bars + B_PREP + 8 * q, 4);
             tc::mbar_init(bars + B_CHAIN + 8 * q, 128);
         }
-        tc::mbar_init(bars + B_GM, 1);
         tc::mbar_init(bars + B_MRDY, 4);
         tc::mbar_init(bars + B_MRDY + 8, 4);
         tc::mbar_init_fence();
@@ -456,9 +462,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
     } else {
         // =========================== warpgroup 0: the serial chain =============================
         const int i = tid;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         float d_hi = a.d0 ? a.d0[static_cast<size_t>(bh) * KD + i] : 1.f, d_lo = 0.f;
-        uint32_t gm_phase = 0;
         for (int blk = 0; blk < nblk; ++blk) {
             const int q = blk & 1;
             const uint32_t ph = (blk >> 1) & 1;
@@ -481,17 +485,92 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             F[F_DST + q * KD + i] = d_hi;
             F[F_DSL + q * KD + i] = d_lo;
 
-            int p = 0, restarts = 0;
-            bool abort_now = false, gram_rows_ready = false;
+            int p = 0;
+            bool abort_now = false, gram_rows_ready = false, clipped = false;
+            // the all-free Gram rows and the coupling bound nu of this block (copied by warpgroup 1)
+            auto gram_ready = [&]() -> bool {
+                if (gram_rows_ready) return true;
+                const bool okr = tc::mbar_wait(bars + B_MRDY + 8 * q, ph, kMaxPolls);
+                if (wg_count(1, okr && !*static_cast<volatile int*>(&s_abort)) != 128) return false;
+                gram_rows_ready = true;
+                tc::tc_fence_after();
+                return true;
+            };
+            // Sweeps needed by the bound nu: each Jacobi sweep shrinks the error by nu (the largest
+            // |gamma_j b_j| sum_l M_jl), so K more sweeps after an estimate within nu |g| leave
+            // nu^(K+1) |g| <= 1e-7 |g|; -1: sweep until no g moves.
+            auto sweeps_for_nu = [&]() -> int {
+                const float nu = fmaxf(fmaxf(F[F_NU + 4 * q], F[F_NU + 4 * q + 1]), fmaxf(F[F_NU + 4 * q + 2], F[F_NU + 4 * q + 3]));
+                const float nu2 = nu * nu;
+                return nu <= 1e-7f ? 0 : nu2 <= 1e-7f ? 1 : nu2 * nu <= 1e-7f ? 2 : nu2 * nu2 <= 1e-7f ? 3 : -1;
+            };
             while (p < J) {
-                if (restarts > kMaxRestarts) {  // the rest of the block token by token
+                if (clipped) {
+                    // ---- Jacobi sweeps on the clipped recurrence itself, tokens p..63 ----------
+                    // From a guess of the g's every coordinate runs its own clipped trajectory
+                    // d_{j+1} = clip(r_j d_j + g_j s_j) and the products d_j s_j summed over the
+                    // coordinates give a_j and the next guess g_j = gamma_j (1 - b_j a_j).  Sweep n
+                    // fixes g_p .. g_{p+n-1} exactly (the trajectory up to j needs only the g's
+                    // before j); and since the clip is 1-Lipschitz and r <= 1, g's that are off by e
+                    // move a_j by at most e sum_l M_jl, so each sweep shrinks the error by nu as on
+                    // the unclipped system.  Starting from g = 0 (error |g|) K + 1 sweeps suffice.
+                    if (!gram_ready()) {
+                        abort_now = true;
+                        break;
+                    }
+                    const int K = sweeps_for_nu();
+                    const int nsw = K >= 0 ? min(K + 1, J - p) : J - p;
+                    float* red = F + F_DF;  // [4][64] per-warp partial sums (F_DF, F_BPV: free here)
+                    const int lane = tid & 31;
                     wg_sync(1);
+                    if (tid < J) F[F_G + tid] = 0.f;  // tokens before p then leave d unchanged
+                    wg_sync(1);
+                    for (int it = 0; it < nsw; ++it) {
+                        float v[J];
+                        float x = d_hi;
+#pragma unroll
+                        for (int j4 = 0; j4 < J; j4 += 4) {
+                            const float4 g4 = *reinterpret_cast<const float4*>(F + F_G + j4);
+                            const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+                            float r4[4] = {1.f, 1.f, 1.f, 1.f};
+                            if (HAS_R) {
+                                const float4 t4 = *reinterpret_cast<const float4*>(rr + j4);
+                                r4[0] = t4.x;
+                                r4[1] = t4.y;
+                                r4[2] = t4.z;
+                                r4[3] = t4.w;
+                            }
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = j4 + e;
+                                const float sj = s_at(j, i);
+                                v[j] = x * sj;
+                                const float rj = j >= p ? r4[e] : 1.f;
+                                x = fminf(fmaxf(fmaf(rj, x, gg[e] * sj), dmin), dmax);
+                            }
+                        }
+                        // sum over the warp: lane l keeps the sums for tokens 2 l and 2 l + 1
+                        rs_level<64, 16>(v, lane);
+                        rs_level<32, 8>(v, lane);
+                        rs_level<16, 4>(v, lane);
+                        rs_level<8, 2>(v, lane);
+                        rs_level<4, 1>(v, lane);
+                        *reinterpret_cast<float2*>(red + warp * J + 2 * lane) = make_float2(v[0], v[1]);
+                        wg_sync(1);
+                        bool changed = false;
+                        if (tid >= p && tid < J) {
+                            const float aj = (red[tid] + red[J + tid]) + (red[2 * J + tid] + red[3 * J + tid]);
+                            const float gn = gam[tid] * (1.f - bpv[tid] * aj);
+                            changed = fabsf(gn - F[F_G + tid]) > 5e-7f * fabsf(gn) + 1e-30f;
+                            F[F_G + tid] = gn;
+                        }
+                        if (K >= 0) wg_sync(1);
+                        else if (wg_count(1, changed) == 0) break;
+                    }
+                    if (tid >= p && tid < J) gout[tid] = F[F_G + tid];
+                    // the block end with the final g's, carried as a (hi, lo) pair
                     for (int j = p; j < J; ++j) {
-                        const float sj = s_at(j, i);
-                        const float al = chain_sum(d_hi * sj, F + F_RED, tid);
-                        const float g = gam[j] * (1.f - bpv[j] * al);
-                        if (tid == 0) gout[j] = g;
-                        const float r = rr[j];
+                        const float sj = s_at(j, i), g = F[F_G + j], r = HAS_R ? rr[j] : 1.f;
                         float p1 = r * d_hi, ep = fmaf(r, d_hi, -p1), q1 = g * sj, s1, e1;
                         two_sum(p1, q1, s1, e1);
                         const float l1 = fmaf(r, d_lo, ep + e1);
@@ -499,6 +578,8 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         d_lo = l1 - (d_hi - s1);
                         pair_clip(d_hi, d_lo, dmin, dmax);
                     }
+                    p = J;
+                    wg_sync(1);
                     break;
                 }
                 // ---- c_j = <d_p, s_j> over all coordinates, j >= p (2 threads per row) ----------
@@ -542,28 +623,28 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     F[F_G + p] = gp;
                     gout[p] = gp;
                 }
-                if (nfree < KD) {  // some coordinate is pinned: split cF / cP by status
-                    F[F_DF + i] = status == 0 ? d_hi : 0.f;
-                    F[F_BPV + i] = status == 0 ? 0.f : bound;
+                if (nfree > 0 && nfree < KD) {  // free and pinned coordinates: clipped sweeps
+                    clipped = true;
+                    continue;
+                }
+                if (nfree == 0) {  // every coordinate pinned: cF = 0, cP_j = <b, s_j>
+                    F[F_BPV + i] = bound;
                     wg_sync(1);
                     const int j = tid >> 1, hf = tid & 1;
-                    float cf = 0.f, cpv = 0.f;
+                    float cpv = 0.f;
                     if (j > p) {
                         const float* row = sf + j * SROW;
 #pragma unroll 4
                         for (int c = 0; c < 16; ++c) {
                             const int ii = piece(c, hf) * 4;
                             const float4 s4 = *reinterpret_cast<const float4*>(row + ii);
-                            const float4 d4 = *reinterpret_cast<const float4*>(F + F_DF + ii);
                             const float4 b4 = *reinterpret_cast<const float4*>(F + F_BPV + ii);
-                            cf = fmaf(d4.x, s4.x, fmaf(d4.y, s4.y, fmaf(d4.z, s4.z, fmaf(d4.w, s4.w, cf))));
                             cpv = fmaf(b4.x, s4.x, fmaf(b4.y, s4.y, fmaf(b4.z, s4.z, fmaf(b4.w, s4.w, cpv))));
                         }
                     }
-                    cf += __shfl_xor_sync(0xffffffffu, cf, 1);
                     cpv += __shfl_xor_sync(0xffffffffu, cpv, 1);
                     if (hf == 0 && j > p) {
-                        F[F_CF + j] = cf;
+                        F[F_CF + j] = 0.f;
                         F[F_CP + j] = cpv;
                     }
                 }
@@ -588,51 +669,12 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         if (lane == 31) F[F_RHO + J] = incl;
                     }
                     wg_sync(1);
-                    if (!(F[F_RHO + J] > 1e-30f)) {  // retention products too small: token by token
-                        restarts = kMaxRestarts + 1;
-                        wg_sync(1);
+                    if (!(F[F_RHO + J] > 1e-30f)) {  // retention products too small: clipped sweeps
+                        clipped = true;
                         continue;
                     }
                 }
                 auto rho = [&](int j) -> float { return HAS_R ? F[F_RHO + j] : 1.f; };
-                // ---- Gram of the free coordinates ------------------------------------------
-                // (the masked copy below may rewrite the s copies once the all-free product is done)
-                if (!gram_rows_ready) {
-                    const bool okr = tc::mbar_wait(bars + B_MRDY + 8 * q, ph, kMaxPolls);
-                    if (wg_count(1, okr && !*static_cast<volatile int*>(&s_abort)) != 128) {
-                        abort_now = true;
-                        break;
-                    }
-                    gram_rows_ready = true;
-                    tc::tc_fence_after();
-                }
-                bool masked = false;
-                if (nfree > 0 && nfree < KD) {
-                    // masked copy: rewrite this coordinate's column of the s copies
-                    const int kb = i >> 6, cc = (i & 63) >> 3, e = i & 7;
-                    unsigned char* shb = sm + OFF_SHL + q * SHL_SLOT + kb * SHL_KB;
-                    unsigned char* slb = shb + SHL_LO;
-                    const float sig = F[F_SIGS + q];
-                    for (int j = 0; j < J; ++j) {
-                        const float x2 = status == 0 ? s_at(j, i) * sig : 0.f;
-                        const __half hv = __float2half_rn(x2);
-                        const __half lv = __float2half_rn(x2 - __half2float(hv));
-                        *reinterpret_cast<__half*>(shb + tc::sw128_off(j, cc) + e * 2) = hv;
-                        *reinterpret_cast<__half*>(slb + tc::sw128_off(j, cc) + e * 2) = lv;
-                    }
-                    tc::fence_proxy_async();
-                    tc::tc_fence_before();
-                    wg_sync(1);
-                    if (tid == 0) issue_gram(q, COL_GM, bars + B_GM);
-                    const bool okm = tc::mbar_wait(bars + B_GM, gm_phase, kMaxPolls);
-                    gm_phase ^= 1u;
-                    if (wg_count(1, okm) != 128) {
-                        abort_now = true;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    masked = true;
-                }
                 // ---- g_{p+1..63}: Jacobi sweeps on the unit-lower-triangular system --------
                 int hb = 0;  // which half of F_H holds the final h
                 {
@@ -650,11 +692,12 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         cpj = F[F_CP + jr];
                         if (HAS_R) ir1 = 1.f / rho(jr + 1);
                     }
-                    if (nfree > 0) {
-                        if (masked) {  // masked Gram straight from tensor memory (all lanes)
-                            const float isg = 1.f / F[F_SIGS + q];
-                            load_gram_row(COL_GM, lane_base, jr, isg * isg, m);
-                        } else if (row_thread) {
+                    if (nfree == KD) {
+                        if (!gram_ready()) {
+                            abort_now = true;
+                            break;
+                        }
+                        if (row_thread) {
                             const float* mrow = reinterpret_cast<const float*>(sm + OFF_MT + q * MT_BYTES) + jr * MROW;
 #pragma unroll
                             for (int l = 0; l < 64; l += 4) {
@@ -679,14 +722,9 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         F[F_H + j] = hj;
                         F[F_H + J + j] = hj;
                     }
-                    if (nfree > 0) {
-                        // Each sweep shrinks the error by the coupling bound nu (the largest
-                        // |gamma_j b_j| sum_l M_jl; the rho ratios are <= 1), starting from nu |g|:
-                        // a fixed number of sweeps once nu^(K+1) <= 1e-7, else sweep until no g moves.
-                        // (the masked Gram's entries are bounded by the all-free ones: the same bound)
-                        const float nu = fmaxf(fmaxf(F[F_NU + 4 * q], F[F_NU + 4 * q + 1]), fmaxf(F[F_NU + 4 * q + 2], F[F_NU + 4 * q + 3]));
-                        const float nu2 = nu * nu;
-                        const int K = nu <= 1e-7f ? 0 : nu2 <= 1e-7f ? 1 : nu2 * nu <= 1e-7f ? 2 : nu2 * nu2 <= 1e-7f ? 3 : -1;
+                    if (nfree == KD) {
+                        // from the estimate above (within nu |g|; the rho ratios are <= 1)
+                        const int K = sweeps_for_nu();
                         wg_sync(1);
                         for (int it = 0; K < 0 ? it < J : it < K; ++it) {
                             const float* hc = F + F_H + hb * J;  // h of the previous sweep
@@ -784,7 +822,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         d_lo = 0.f;
                     }
                     p = jstar + 1;
-                    ++restarts;
+                    clipped = true;  // the rest of the block by clipped sweeps
                 }
                 wg_sync(1);
             }
@@ -813,7 +851,6 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             tc::mbar_inval(bars + B_PREP + 8 * q);
             tc::mbar_inval(bars + B_CHAIN + 8 * q);
         }
-        tc::mbar_inval(bars + B_GM);
         tc::mbar_inval(bars + B_MRDY);
         tc::mbar_inval(bars + B_MRDY + 8);
     }
