@@ -12,6 +12,9 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   delta_phase2   pinned (textbook DeltaNet at d = 1, residual identity, chunk-form identity)
   osdn_forward   pinned (decoupling into the two phases, continuation, Cor. D.8 identity)
   decode_step    pinned (equals the forward on one token; decode x T equals forward on T)
+  alpha (the OSGDN state gate, any of the three phase-2 functions): pinned (alpha = 1 is the
+                 ungated rule; eta = 0 is a separately written Gated DeltaNet; the chunk form of
+                 Eqs. (13)-(15) equals the recurrence; a zero gate forgets the state)
 """
 from __future__ import annotations
 
@@ -54,9 +57,9 @@ def _load():
         lib = ctypes.CDLL(str(path))
         i, d = ctypes.c_int, ctypes.c_double
         lib.oracle_precond_scan.argtypes = [_dp] * 3 + [i] + [_dp] * 4 + [i] * 4 + [d] * 4 + [i, i]
-        lib.oracle_delta_phase2.argtypes = [_dp] * 8 + [i] * 5 + [d, i]
-        lib.oracle_osdn_forward.argtypes = [_dp] * 5 + [i] + [_dp] * 8 + [i] * 5 + [d] * 4 + [i, d, i]
-        lib.oracle_decode_step.argtypes = [_dp] * 5 + [i] + [_dp] * 3 + [i] * 4 + [d] * 4 + [i, d, i]
+        lib.oracle_delta_phase2.argtypes = [_dp] * 9 + [i] * 5 + [d, i]
+        lib.oracle_osdn_forward.argtypes = [_dp] * 5 + [i] + [_dp] * 9 + [i] * 5 + [d] * 4 + [i, d, i]
+        lib.oracle_decode_step.argtypes = [_dp] * 5 + [i] + [_dp] * 4 + [i] * 4 + [d] * 4 + [i, d, i]
         for f in ("oracle_precond_scan", "oracle_delta_phase2", "oracle_osdn_forward",
                   "oracle_decode_step"):
             getattr(lib, f).restype = ctypes.c_int
@@ -110,24 +113,26 @@ def precond_scan(k, beta, r=None, d0=None, *, eta=0.003, d_min=0.5, d_max=2.0, e
     return (kt, dout, a) if return_a else (kt, dout)
 
 
-def delta_phase2(q, k, k_tilde, v, beta, S0=None, *, scale=1.0, threads=0):
-    """Phase 2 (Eq. (2)/(5)) token by token with the supplied write key -> (o, S_out)."""
-    q, k, kt, v, beta, S0 = _in(q), _in(k), _in(k_tilde), _in(v), _in(beta), _in(S0)
+def delta_phase2(q, k, k_tilde, v, beta, S0=None, *, alpha=None, scale=1.0, threads=0):
+    """Phase 2 (Eq. (2)/(5)) token by token with the supplied write key -> (o, S_out).  alpha
+    [B,T,H]: the OSGDN state gate (Appendix B.1, post-gate residual)."""
+    q, k, kt, v, beta, S0, alpha = map(_in, (q, k, k_tilde, v, beta, S0, alpha))
     B, T, H, K = k.shape
     V = v.shape[-1]
     o = np.empty((B, T, H, V))
     S = np.empty((B, H, V, K))
-    rc = _load().oracle_delta_phase2(_p(q), _p(k), _p(kt), _p(v), _p(beta), _p(S0), _p(o), _p(S),
+    rc = _load().oracle_delta_phase2(_p(q), _p(k), _p(kt), _p(v), _p(beta), _p(alpha), _p(S0), _p(o), _p(S),
                                      B, T, H, K, V, scale, threads)
     if rc:
         raise ValueError("oracle_delta_phase2: bad arguments")
     return o, S
 
 
-def osdn_forward(q, k, v, beta, r=None, d0=None, S0=None, *, eta=0.003, d_min=0.5, d_max=2.0,
-                 eps=1e-6, beta_aware=True, scale=1.0, threads=0):
-    """Both phases interleaved per token.  Returns dict(o, S, d, k_tilde, a, u2)."""
-    q, k, v, beta, r, d0, S0 = map(_in, (q, k, v, beta, r, d0, S0))
+def osdn_forward(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, eta=0.003, d_min=0.5,
+                 d_max=2.0, eps=1e-6, beta_aware=True, scale=1.0, threads=0):
+    """Both phases interleaved per token.  Returns dict(o, S, d, k_tilde, a, u2).  alpha [B,T,H]:
+    the OSGDN state gate (Appendix B.1)."""
+    q, k, v, beta, r, d0, S0, alpha = map(_in, (q, k, v, beta, r, d0, S0, alpha))
     B, T, H, K = k.shape
     V = v.shape[-1]
     o = np.empty((B, T, H, V))
@@ -136,7 +141,8 @@ def osdn_forward(q, k, v, beta, r=None, d0=None, S0=None, *, eta=0.003, d_min=0.
     kt = np.empty((B, T, H, K))
     a = np.empty((B, T, H))
     u2 = np.empty((B, T, H))
-    rc = _load().oracle_osdn_forward(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(d0), _p(S0), _p(o),
+    rc = _load().oracle_osdn_forward(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(alpha), _p(d0),
+                                     _p(S0), _p(o),
                                      _p(S), _p(d), _p(kt), _p(a), _p(u2), B, T, H, K, V, eta,
                                      d_min, d_max, eps, int(beta_aware), scale, threads)
     if rc:
@@ -144,17 +150,18 @@ def osdn_forward(q, k, v, beta, r=None, d0=None, S0=None, *, eta=0.003, d_min=0.
     return {"o": o, "S": S, "d": d, "k_tilde": kt, "a": a, "u2": u2}
 
 
-def decode_step(q, k, v, beta, S, d, r=None, *, eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6,
-                beta_aware=True, scale=1.0, threads=0):
-    """One decode token.  q, k [B,H,K], v [B,H,V], beta/r [B,H]; S [B,H,V,K], d [B,H,K] are
+def decode_step(q, k, v, beta, S, d, r=None, *, alpha=None, eta=0.003, d_min=0.5, d_max=2.0,
+                eps=1e-6, beta_aware=True, scale=1.0, threads=0):
+    """One decode token.  q, k [B,H,K], v [B,H,V], beta/r/alpha [B,H]; S [B,H,V,K], d [B,H,K] are
     copied, stepped and returned: (o, S_new, d_new)."""
-    q, k, v, beta, r = map(_in, (q, k, v, beta, r))
+    q, k, v, beta, r, alpha = map(_in, (q, k, v, beta, r, alpha))
     S = _in(S).copy()
     d = _in(d).copy()
     B, H, K = k.shape
     V = v.shape[-1]
     o = np.empty((B, H, V))
-    rc = _load().oracle_decode_step(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(S), _p(d), _p(o),
+    rc = _load().oracle_decode_step(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(alpha), _p(S), _p(d),
+                                    _p(o),
                                     B, H, K, V, eta, d_min, d_max, eps, int(beta_aware), scale,
                                     threads)
     if rc:

@@ -432,3 +432,120 @@ def test_vector_retention_eta0_is_a_product_of_gates():
     prod = np.concatenate([np.ones((B, 1, H, K)), np.cumprod(r, axis=1)], axis=1)  # prod_{s<t}
     np.testing.assert_allclose(kt, d0[:, None] * prod[:, :T] * k, rtol=1e-13)
     np.testing.assert_allclose(d, d0 * prod[:, T], rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------------
+# The OSGDN state gate (Appendix B.1): S_t = alpha_t S_{t-1} (I - beta_t k_t k~_t^T)
+# + beta_t v_t k~_t^T, post-gate residual; phase 1 unchanged.
+# ---------------------------------------------------------------------------------------------
+def gates(seed, shape, lo=0.6):
+    return rng(seed).uniform(lo, 1.0, size=shape)
+
+
+def textbook_gated_deltanet(q, k, v, beta, alpha):
+    """Gated DeltaNet in its transition-matrix form S_t = S_{t-1} (alpha_t (I - beta_t k_t k_t^T))
+    + beta_t v_t k_t^T, o_t = S_t q_t (written independently of the oracle's residual form)."""
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.zeros((B, T, H, V))
+    S_all = np.zeros((B, H, V, K))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((V, K))
+            for t in range(T):
+                kk = k[b, t, h]
+                S = S @ (alpha[b, t, h] * (np.eye(K) - beta[b, t, h] * np.outer(kk, kk))) \
+                    + beta[b, t, h] * np.outer(v[b, t, h], kk)
+                o[b, t, h] = S @ q[b, t, h]
+            S_all[b, h] = S
+    return o, S_all
+
+
+def gated_chunk_form(q, k, kt, v, beta, alpha, S0, C):
+    """Eqs. (13)-(15) with the readout of each chunk: with gamma_i the gate product from the chunk
+    start through token i, A_ij = beta_i (gamma_i / gamma_j) <k_i, k~_j> (j < i),
+    M = (I + A)^-1 diag(beta), W = M (gamma . K), U = M V, X = U - W S^T,
+    O = diag(gamma) Q S^T + (tril(Q K~^T, 0) . gamma_i / gamma_j) X,
+    S <- gamma_C S + X^T (rho . K~), rho_j = gamma_C / gamma_j."""
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.zeros((B, T, H, V))
+    S_out = np.zeros((B, H, V, K))
+    for b in range(B):
+        for h in range(H):
+            S = S0[b, h].copy()
+            for c0 in range(0, T, C):
+                sl = slice(c0, c0 + C)
+                Kc, Ktc, Vc, Qc, bc = k[b, sl, h], kt[b, sl, h], v[b, sl, h], q[b, sl, h], beta[b, sl, h]
+                gam = np.cumprod(alpha[b, sl, h])
+                ratio = gam[:, None] / gam[None, :]
+                n = Kc.shape[0]
+                A = np.tril(bc[:, None] * ratio * (Kc @ Ktc.T), -1)
+                M = np.linalg.inv(np.eye(n) + A) @ np.diag(bc)        # Eq. (13)
+                W = M @ (gam[:, None] * Kc)                           # Eq. (14)
+                U = M @ Vc
+                X = U - W @ S.T
+                o[b, sl, h] = gam[:, None] * (Qc @ S.T) + (np.tril(Qc @ Ktc.T, 0) * ratio) @ X
+                S = gam[-1] * S + X.T @ ((gam[-1] / gam)[:, None] * Ktc)  # Eq. (15)
+            S_out[b, h] = S
+    return o, S_out
+
+
+def test_gate_one_is_the_ungated_rule():
+    q, k, v, beta, r = rand_problem(31, B=2, T=40, H=2, K=8, V=6, apf=True)
+    a = oracle.osdn_forward(q, k, v, beta, r, eta=0.2)
+    b = oracle.osdn_forward(q, k, v, beta, r, alpha=np.ones_like(beta), eta=0.2)
+    for key in ("o", "S", "d", "k_tilde"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_gated_eta0_is_textbook_gated_deltanet():
+    q, k, v, beta, _ = rand_problem(32, B=2, T=48, H=3, K=8, V=6)
+    alpha = gates(33, beta.shape)
+    out = oracle.osdn_forward(q, k, v, beta, alpha=alpha, eta=0.0)
+    o_ref, S_ref = textbook_gated_deltanet(q, k, v, beta, alpha)
+    np.testing.assert_allclose(out["o"], o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out["S"], S_ref, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(out["k_tilde"], k)
+
+
+@pytest.mark.parametrize("C", [16, 64])
+def test_gated_chunk_form_equals_sequential(C):
+    q, k, v, beta, r = rand_problem(34, B=1, T=256, H=2, K=16, V=12, apf=True)
+    alpha = gates(35, beta.shape, lo=0.3)
+    S0 = rng(36).standard_normal((1, 2, 12, 16)) * 0.1
+    kt, _ = oracle.precond_scan(k, beta, r, None, eta=0.3)
+    o_seq, S_seq = oracle.delta_phase2(q, k, kt, v, beta, S0, alpha=alpha)
+    o_chk, S_chk = gated_chunk_form(q, k, kt, v, beta, alpha, S0, C)
+    np.testing.assert_allclose(o_seq, o_chk, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(S_seq, S_chk, rtol=0, atol=1e-11)
+
+
+def test_zero_gate_forgets_the_state():
+    """alpha_t = 0: the post-gate reference is empty, so S_t = beta_t v_t k~_t^T and everything
+    after t is the rule started from S = 0 at t."""
+    q, k, v, beta, _ = rand_problem(37, B=1, T=30, H=2, K=8, V=6)
+    alpha = gates(38, beta.shape)
+    alpha[:, 12] = 0.0
+    S0 = rng(39).standard_normal((1, 2, 6, 8))
+    kt, _ = oracle.precond_scan(k, beta, None, None, eta=0.2)
+    o, S = oracle.delta_phase2(q, k, kt, v, beta, S0, alpha=alpha)
+    o2, S2 = oracle.delta_phase2(q[:, 12:], k[:, 12:], kt[:, 12:], v[:, 12:], beta[:, 12:], None,
+                                 alpha=alpha[:, 12:])
+    np.testing.assert_array_equal(o[:, 12:], o2)
+    np.testing.assert_array_equal(S, S2)
+
+
+def test_gated_decode_steps_equal_forward():
+    q, k, v, beta, r = rand_problem(40, B=2, T=6, H=2, K=8, V=5, apf=True)
+    alpha = gates(41, beta.shape)
+    g = rng(42)
+    S = g.standard_normal((2, 2, 5, 8)) * 0.1
+    d = g.uniform(0.6, 1.8, size=(2, 2, 8))
+    full = oracle.osdn_forward(q, k, v, beta, r, d, S, alpha=alpha, eta=0.2)
+    for t in range(6):
+        o, S, d = oracle.decode_step(q[:, t], k[:, t], v[:, t], beta[:, t], S, d, r[:, t],
+                                     alpha=alpha[:, t], eta=0.2)
+        np.testing.assert_allclose(o, full["o"][:, t], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(S, full["S"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(d, full["d"], rtol=0, atol=1e-15)
