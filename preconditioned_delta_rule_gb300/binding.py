@@ -47,17 +47,17 @@ def lib() -> ctypes.CDLL:
     L.osdn_precond_scan.argtypes = [vp, i, fp, fp, i, fp, vp, i, fp, i, i, i, i, f, f, f, f, i, vp, sz, vp]
     L.osdn_precond_scan_workspace_bytes.argtypes = [i, i, i, i, i]
     L.osdn_precond_scan_workspace_bytes.restype = sz
-    L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp, sz, vp]
+    L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, fp, vp, fp, i, i, i, i, i, i, f, vp, sz, vp]
     L.osdn_chunk_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.osdn_chunk_fwd_workspace_bytes.restype = sz
-    L.osdn_chunk_fwd_static_ws.argtypes = [vp, vp, vp, vp, i, fp, fp, vp, fp, i, i, i, i, i, i, f, vp]
+    L.osdn_chunk_fwd_static_ws.argtypes = [vp, vp, vp, vp, i, fp, fp, fp, vp, fp, i, i, i, i, i, i, f, vp]
     L.osdn_chunk_fwd_static_ws.restype = ctypes.c_int
-    L.osdn_layer_fwd.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, vp, vp, fp, fp, i, i, i, i, i, i,
+    L.osdn_layer_fwd.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, fp, vp, vp, fp, fp, i, i, i, i, i, i,
                                  f, f, f, f, f, i, vp, sz, vp]
     L.osdn_layer_fwd.restype = ctypes.c_int
     L.osdn_layer_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.osdn_layer_fwd_workspace_bytes.restype = sz
-    L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
+    L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
     L.osdn_check.argtypes = [vp]
     for fn in ("osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step", "osdn_check"):
         getattr(L, fn).restype = ctypes.c_int
@@ -191,9 +191,10 @@ def _resolve_workspace(workspace, device, need, role):
     return ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size()
 
 
-def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, o=None, S_out=None, chunk=64, scale=1.0,
-                   workspace=None, stream=None):
+def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, alpha=None, o=None, S_out=None, chunk=64,
+                   scale=1.0, workspace=None, stream=None):
     """Phase 2 (Eqs. (2), (5), (8)-(11)).  Returns (o [B,T,H,V], S_out [B,H,V,K] fp32).
+    ``alpha`` [B,T,H] fp32: the OSGDN state gate (Appendix B.1, Eqs. (13)-(15)); None for none.
 
     ``workspace``: None (default) uses a cached torch buffer of the size the library asks for;
     a uint8 CUDA tensor is used as given; False runs the no-scratch fused kernel."""
@@ -204,6 +205,7 @@ def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, o=None, S_out=None, chunk
                          ("k_tilde", k_tilde, (B, T, H, K)), ("v", v, (B, T, H, V))):
         _check(name, t, shp, dt, dev)
     _check("beta", beta, (B, T, H), torch.float32, dev)
+    _check("alpha", alpha, (B, T, H), torch.float32, dev)
     _check("S0", S0, (B, H, V, K), torch.float32, dev)
     if o is None:
         o = torch.empty((B, T, H, V), device=dev, dtype=dt)
@@ -214,16 +216,16 @@ def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, o=None, S_out=None, chunk
     need = osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 else 0
     ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "chunk")
     st = lib().osdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(k_tilde), _ptr(v), _code(dt), _ptr(beta),
-                              _ptr(S0), _ptr(o), _ptr(S_out), B, T, H, K, V, int(chunk),
+                              _ptr(alpha), _ptr(S0), _ptr(o), _ptr(S_out), B, T, H, K, V, int(chunk),
                               float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
     _raise("osdn_chunk_fwd", st)
     return o, S_out
 
 
-def osdn_decode_step(q, k, v, beta, S, d, r=None, *, o=None, eta=0.003, d_min=0.5, d_max=2.0,
-                     eps=1e-6, scale=1.0, beta_aware=True, stream=None):
+def osdn_decode_step(q, k, v, beta, S, d, r=None, *, alpha=None, o=None, eta=0.003, d_min=0.5,
+                     d_max=2.0, eps=1e-6, scale=1.0, beta_aware=True, stream=None):
     """One decode token in place on S [B,H,V,K] and d [B,H,K].  Returns o [B,H,V].  r is [B,H]
-    or [B,H,K] (vector retention)."""
+    or [B,H,K] (vector retention); alpha [B,H] the OSGDN state gate (None: none)."""
     B, H, K = k.shape
     V = v.shape[-1]
     dev, dt = k.device, k.dtype
@@ -231,13 +233,14 @@ def osdn_decode_step(q, k, v, beta, S, d, r=None, *, o=None, eta=0.003, d_min=0.
     _check("v", v, (B, H, V), dt, dev)
     _check("beta", beta, (B, H), torch.float32, dev)
     r_per_key = _retention(r, (B, H), K, dev)
+    _check("alpha", alpha, (B, H), torch.float32, dev)
     _check("S", S, (B, H, V, K), torch.float32, dev)
     _check("d", d, (B, H, K), torch.float32, dev)
     if o is None:
         o = torch.empty((B, H, V), device=dev, dtype=dt)
     _check("o", o, (B, H, V), dt, dev)
     st = lib().osdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key,
-                                _ptr(S), _ptr(d), _ptr(o), B, H, K, V, float(eta), float(d_min),
+                                _ptr(alpha), _ptr(S), _ptr(d), _ptr(o), B, H, K, V, float(eta), float(d_min),
                                 float(d_max), float(eps), float(scale), int(bool(beta_aware)),
                                 _stream(dev, stream))
     _raise("osdn_decode_step", st)
@@ -254,10 +257,11 @@ def osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16
     return int(lib().osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, _code(dtype)))
 
 
-def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, k_tilde=None, o=None, S_out=None,
-                   d_out=None, chunk=64, eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6, scale=1.0,
-                   beta_aware=True, workspace=None, stream=None):
-    """Phase 1 then phase 2 in one call.  Returns (o, S_out, d_out, k_tilde).
+def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, k_tilde=None, o=None,
+                   S_out=None, d_out=None, chunk=64, eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6,
+                   scale=1.0, beta_aware=True, workspace=None, stream=None):
+    """Phase 1 then phase 2 in one call.  Returns (o, S_out, d_out, k_tilde).  ``alpha`` [B,T,H]:
+    the OSGDN state gate of phase 2 (Appendix B.1); None for the ungated rule.
 
     ``workspace``: None (default) uses a cached torch buffer of the size the library asks for;
     a uint8 CUDA tensor is used as given; False runs without scratch."""
@@ -268,6 +272,7 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, k_tilde=None, o=N
         _check(name, t, shp, dt, dev)
     _check("beta", beta, (B, T, H), torch.float32, dev)
     r_per_key = _retention(r, (B, T, H), K, dev)
+    _check("alpha", alpha, (B, T, H), torch.float32, dev)
     _check("d0", d0, (B, H, K), torch.float32, dev)
     _check("S0", S0, (B, H, V, K), torch.float32, dev)
     if k_tilde is None:
@@ -284,7 +289,8 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, k_tilde=None, o=N
     _check("d_out", d_out, (B, H, K), torch.float32, dev)
     need = osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 and T % chunk == 0 else 0
     ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "layer")
-    st = lib().osdn_layer_fwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, _ptr(d0),
+    st = lib().osdn_layer_fwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, _ptr(alpha),
+                              _ptr(d0),
                               _ptr(S0), _ptr(k_tilde), _ptr(o), _ptr(S_out), _ptr(d_out), B, T, H, K,
                               V, int(chunk), float(eta), float(d_min), float(d_max), float(eps),
                               float(scale), int(bool(beta_aware)), ws_ptr, ws_bytes,

@@ -80,7 +80,7 @@ size_t osdn_precond_scan_workspace_bytes(int B, int T, int H, int K, osdn_dtype 
 }
 
 osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, const void* v,
-                           osdn_dtype dtype, const float* beta, const float* S0, void* o,
+                           osdn_dtype dtype, const float* beta, const float* alpha, const float* S0, void* o,
                            float* S_out, int B, int T, int H, int K, int V, int chunk,
                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
     if (B < 0 || T < 0 || H < 0 || chunk <= 0) return OSDN_ERR_SHAPE;
@@ -97,11 +97,12 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
     OSDN_TRY(ptr(k_tilde, seq));
     OSDN_TRY(ptr(v, seq));
     OSDN_TRY(ptr(beta, seq));
+    OSDN_TRY(ptr(alpha, false));
     OSDN_TRY(ptr(o, seq));
     OSDN_TRY(ptr(S0, false));
     OSDN_TRY(ptr(S_out, true));
     OSDN_TRY(ptr(workspace, false));
-    OsdnChunkArgs a{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale};
+    OsdnChunkArgs a{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale, alpha};
     return from_cuda(chunk_dispatch(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
@@ -115,7 +116,8 @@ size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
 }
 
 osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
-                           const float* r, int r_per_key, const float* d0, const float* S0, void* k_tilde, void* o,
+                           const float* r, int r_per_key, const float* alpha, const float* d0, const float* S0,
+                           void* k_tilde, void* o,
                            float* S_out, float* d_out, int B, int T, int H, int K, int V, int chunk,
                            float eta, float d_min, float d_max, float eps, float scale, int beta_aware,
                            void* workspace, size_t workspace_bytes, void* stream) {
@@ -137,6 +139,7 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
     OSDN_TRY(ptr(k_tilde, seq));
     OSDN_TRY(ptr(o, seq));
     OSDN_TRY(ptr(r, false));
+    OSDN_TRY(ptr(alpha, false));
     OSDN_TRY(ptr(d0, false));
     OSDN_TRY(ptr(S0, false));
     OSDN_TRY(ptr(S_out, true));
@@ -144,7 +147,7 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
     OSDN_TRY(ptr(workspace, false));
     OsdnScanArgs sa{k, dtype, beta, r, d0, k_tilde, dtype, d_out, B, T, H, K, eta, d_min, d_max, eps, beta_aware ? 1 : 0,
                     r != nullptr ? r_per_key : 0};
-    OsdnChunkArgs ca{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale};
+    OsdnChunkArgs ca{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale, alpha};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (seq) {
         cudaError_t e = osdn_launch_layer(sa, ca, workspace, workspace_bytes, s);
@@ -182,7 +185,8 @@ size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
 }
 
 osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,
-                             const float* beta, const float* r, int r_per_key, float* S, float* d, void* o,
+                             const float* beta, const float* r, int r_per_key, const float* alpha, float* S,
+                             float* d, void* o,
                              int B, int H, int K, int V, float eta, float d_min, float d_max,
                              float eps, float scale, int beta_aware, void* stream) {
     if (B < 0 || H < 0) return OSDN_ERR_SHAPE;
@@ -198,11 +202,12 @@ osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_d
     OSDN_TRY(ptr(v, true));
     OSDN_TRY(ptr(beta, true));
     OSDN_TRY(ptr(r, false));
+    OSDN_TRY(ptr(alpha, false));
     OSDN_TRY(ptr(S, true));
     OSDN_TRY(ptr(d, true));
     OSDN_TRY(ptr(o, true));
     OsdnDecodeArgs a{q, k, v, dtype, beta, r, S, d, o, B, H, K, V,
-                     eta, d_min, d_max, eps, scale, beta_aware ? 1 : 0, r != nullptr ? r_per_key : 0};
+                     eta, d_min, d_max, eps, scale, beta_aware ? 1 : 0, r != nullptr ? r_per_key : 0, alpha};
     return from_cuda(osdn_launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -230,6 +235,6 @@ const char* osdn_status_string(int status) {
     return "OSDN: unknown status";
 }
 
-int osdn_version(void) { return 100; }
+int osdn_version(void) { return 200; }
 
 }  // extern "C"

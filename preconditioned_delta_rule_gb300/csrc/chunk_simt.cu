@@ -5,6 +5,8 @@
 //   u_t = v_t - S_{t-1} k_t   (original key: read side)
 //   S_t = S_{t-1} + beta_t u_t k~_t^T   (write key)
 //   o_t = scale * S_t q_t   (readout after the write)
+// With the OSGDN state gate (Appendix B.1, post-gate residual) S_{t-1} is first scaled by
+// alpha_t (alpha = 1 without the gate: an exact no-op).
 // This kernel evaluates the recurrence token by token in fp32 (FFMA only), which is exact up to
 // fp32 rounding for any input dtype.  It serves fp32 inputs (where bf16/f16 tensor-core
 // operands could not meet a 1e-4 tolerance) and the head sizes the tensor-core kernel is not
@@ -42,7 +44,7 @@ __global__ void __launch_bounds__(256) chunk_recurrent_kernel(OsdnChunkArgs a) {
     }
 
     const size_t row0 = (size_t)b * T * H + h;
-    float kv[E], ktv[E], qv[E], vv[kRowsPerWarp], bt = 0.f;
+    float kv[E], ktv[E], qv[E], vv[kRowsPerWarp], bt = 0.f, al = 1.f;
     auto load = [&](int t) {
         const size_t r = row0 + (size_t)t * H;
         VecIO<TIn, E>::load(kg + r * K + lane * E, kv);
@@ -51,6 +53,7 @@ __global__ void __launch_bounds__(256) chunk_recurrent_kernel(OsdnChunkArgs a) {
 #pragma unroll
         for (int j = 0; j < kRowsPerWarp; ++j) vv[j] = to_f32(vg[r * V + row_base + j]);
         bt = a.beta[r];
+        al = a.alpha ? a.alpha[r] : 1.f;
     };
     if (T > 0) load(0);
     for (int t = 0; t < T; ++t) {
@@ -59,14 +62,17 @@ __global__ void __launch_bounds__(256) chunk_recurrent_kernel(OsdnChunkArgs a) {
         for (int i = 0; i < E; ++i) { ck[i] = kv[i]; ckt[i] = ktv[i]; cq[i] = qv[i]; }
 #pragma unroll
         for (int j = 0; j < kRowsPerWarp; ++j) cv[j] = vv[j];
-        const float cb = bt;
+        const float cb = bt, ca = al;
         if (t + 1 < T) load(t + 1);
         const size_t r = row0 + (size_t)t * H;
 #pragma unroll
         for (int j = 0; j < kRowsPerWarp; ++j) {
             float sk = 0.f;
 #pragma unroll
-            for (int i = 0; i < E; ++i) sk = fmaf(S[j][i], ck[i], sk);
+            for (int i = 0; i < E; ++i) {
+                S[j][i] *= ca;
+                sk = fmaf(S[j][i], ck[i], sk);
+            }
             sk = warp_sum(sk);
             const float bu = cb * (cv[j] - sk);
             float sq = 0.f;

@@ -1505,7 +1505,7 @@ size_t osdn_layer_workspace_bytes(const OsdnScanArgs& sa, const OsdnChunkArgs& c
 // cudaErrorNotSupported when it does not apply (the caller then runs the two entry points).
 cudaError_t osdn_launch_layer(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, void* ws, size_t ws_bytes,
                               cudaStream_t s) {
-    if (!osdn::layer_covers(sa, ca) || ws == nullptr || ws_bytes < osdn::layer_ws(sa, ca).total)
+    if (!osdn::layer_covers(sa, ca) || ws == nullptr || ws_bytes < osdn::layer_ws(sa, ca).total || ca.alpha)
         return cudaErrorNotSupported;
     unsigned char* w = static_cast<unsigned char*>(ws);
     if (ca.dtype == OSDN_BF16)
@@ -1520,7 +1520,7 @@ size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a) {
 }
 
 cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
-    if (!osdn::tc_covers(a)) return cudaErrorNotSupported;
+    if (!osdn::tc_covers(a) || a.alpha) return cudaErrorNotSupported;
     if (a.dtype == OSDN_BF16) return osdn::launch_tc<__nv_bfloat16>(a, ws, ws_bytes, s);
     return osdn::launch_tc<__half>(a, ws, ws_bytes, s);
 }

@@ -104,12 +104,14 @@ struct OsdnChunkArgs {
     const void* q; const void* k; const void* k_tilde; const void* v; osdn_dtype dtype;
     const float* beta; const float* S0; void* o; float* S_out;
     int B, T, H, K, V, chunk; float scale;
+    const float* alpha;  // [B,T,H] OSGDN state gate (Appendix B.1), or null: no gate
 };
 struct OsdnDecodeArgs {
     const void* q; const void* k; const void* v; osdn_dtype dtype; const float* beta;
     const float* r; float* S; float* d; void* o;
     int B, H, K, V; float eta, d_min, d_max, eps, scale; int beta_aware;
     int r_per_key;  // 1: r [B,H,K], one retention per key coordinate (vector retention)
+    const float* alpha;  // [B,H] OSGDN state gate (Appendix B.1), or null: no gate
 };
 
 // Phase-1 scan.  16-bit keys with K = 128 use the blocked kernel; with a workspace of at least

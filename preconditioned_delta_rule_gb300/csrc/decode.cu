@@ -5,7 +5,9 @@
 // own decode path is a fused single-token kernel (Appendix L).  For one head:
 //   k~ = d . k (old d);  d <- clip(r d + eta b (1 - b <d, k.k>) / max(|k|^2, eps) * k.k)
 //   u_i = v_i - <S_i, k>;  S_i <- S_i + beta u_i k~;  o_i = <S_i_new, q'> = <S_i, q'> + beta u_i <k~, q'>
-// with q' = scale * q, for every row i of S (rows are independent given k, k~, q).
+// with q' = scale * q, for every row i of S (rows are independent given k, k~, q).  With the OSGDN
+// state gate (Appendix B.1, post-gate residual) S is first scaled by alpha: S <- alpha S, then the
+// same step (alpha = 1 without the gate: an exact no-op).
 //
 // The step is HBM-bound: S (V x K fp32) is read once and written once.  One CTA of 256 threads
 // per head; 8 lanes per row, each lane holding 4-float pieces interleaved so that every load
@@ -102,6 +104,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
         }
     }
     const float bt = scoef[0], bktq = scoef[1];
+    const float ag = a.alpha ? a.alpha[bh] : 1.f;
 
     float4 Sr[PASSES][P4];
 #pragma unroll
@@ -118,6 +121,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
         float dk = 0.f, dq = 0.f;
 #pragma unroll
         for (int c = 0; c < P4; ++c) {
+            Sr[ps][c].x *= ag;
+            Sr[ps][c].y *= ag;
+            Sr[ps][c].z *= ag;
+            Sr[ps][c].w *= ag;
             const float4 x = Sr[ps][c];
             dk = fmaf(x.x, kr[c][0], fmaf(x.y, kr[c][1], fmaf(x.z, kr[c][2], fmaf(x.w, kr[c][3], dk))));
             dq = fmaf(x.x, qr[c][0], fmaf(x.y, qr[c][1], fmaf(x.z, qr[c][2], fmaf(x.w, qr[c][3], dq))));

@@ -60,7 +60,7 @@ def chunk(L, **kw):
     a = dict(q=A, k=A, kt=A, v=A, dt=1, beta=A, S0=None, o=A, Sout=A, B=2, T=128, H=2, K=128,
              V=128, C=64, scale=1.0)
     a.update(kw)
-    return L.osdn_chunk_fwd(a["q"], a["k"], a["kt"], a["v"], a["dt"], a["beta"], a["S0"], a["o"],
+    return L.osdn_chunk_fwd(a["q"], a["k"], a["kt"], a["v"], a["dt"], a["beta"], a.get("alpha"), a["S0"], a["o"],
                             a["Sout"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"], a["scale"],
                             a.get("ws"), a.get("wsb", 0), None)
 
@@ -69,7 +69,8 @@ def decode(L, **kw):
     a = dict(q=A, k=A, v=A, dt=1, beta=A, r=None, S=A, d=A, o=A, B=2, H=2, K=128, V=128,
              eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6, scale=1.0, ba=1)
     a.update(kw)
-    return L.osdn_decode_step(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a.get("rpk", 0), a["S"], a["d"],
+    return L.osdn_decode_step(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a.get("rpk", 0), a.get("alpha"),
+                              a["S"], a["d"],
                               a["o"], a["B"], a["H"], a["K"], a["V"], a["eta"], a["dmin"],
                               a["dmax"], a["eps"], a["scale"], a["ba"], None)
 
@@ -92,7 +93,7 @@ def test_scan_validation(L, kw, want):
     (dict(v=A + 8), ALIGN), (dict(S0=A + 4), ALIGN),
     (dict(T=100), SHAPE), (dict(C=0), SHAPE), (dict(C=32), UNSUP), (dict(K=256), UNSUP),
     (dict(V=48), UNSUP), (dict(dt=5), DTYPE), (dict(scale=math.inf), ARG),
-    (dict(ws=A + 8, wsb=1 << 20), ALIGN), (dict(B=0), OK),
+    (dict(ws=A + 8, wsb=1 << 20), ALIGN), (dict(alpha=A + 4), ALIGN), (dict(B=0), OK),
 ])
 def test_chunk_validation(L, kw, want):
     assert chunk(L, **kw) == want
@@ -101,7 +102,7 @@ def test_chunk_validation(L, kw, want):
 @pytest.mark.parametrize("kw,want", [
     (dict(S=None), ARG), (dict(d=None), ARG), (dict(o=None), ARG), (dict(q=A + 1), ALIGN),
     (dict(K=32), UNSUP), (dict(dt=3), DTYPE), (dict(eps=-1.0), ARG), (dict(scale=math.nan), ARG),
-    (dict(rpk=-1), ARG), (dict(H=0), OK),
+    (dict(rpk=-1), ARG), (dict(alpha=A + 8), ALIGN), (dict(H=0), OK),
 ])
 def test_decode_validation(L, kw, want):
     assert decode(L, **kw) == want
@@ -136,7 +137,8 @@ def layer(L, **kw):
     a = dict(q=A, k=A, v=A, dt=1, beta=A, r=None, d0=None, S0=None, kt=A, o=A, Sout=A, dout=A, B=2, T=128,
              H=2, K=128, V=128, C=64, eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6, scale=1.0, ba=1)
     a.update(kw)
-    return L.osdn_layer_fwd(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a.get("rpk", 0), a["d0"], a["S0"], a["kt"],
+    return L.osdn_layer_fwd(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a.get("rpk", 0), a.get("alpha"),
+                            a["d0"], a["S0"], a["kt"],
                             a["o"], a["Sout"], a["dout"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"],
                             a["eta"], a["dmin"], a["dmax"], a["eps"], a["scale"], a["ba"], a.get("ws"),
                             a.get("wsb", 0), None)
@@ -146,7 +148,7 @@ def layer(L, **kw):
     (dict(kt=None), ARG), (dict(dout=None), ARG), (dict(Sout=None), ARG), (dict(o=None), ARG),
     (dict(q=A + 2), ALIGN), (dict(ws=A + 8, wsb=1 << 20), ALIGN), (dict(K=96), UNSUP), (dict(C=32), UNSUP),
     (dict(T=100), SHAPE), (dict(dt=5), DTYPE), (dict(eta=-1.0), ARG), (dict(scale=math.inf), ARG),
-    (dict(rpk=3), ARG), (dict(B=0), OK),
+    (dict(rpk=3), ARG), (dict(alpha=A + 12), ALIGN), (dict(B=0), OK),
 ])
 def test_layer_validation(L, kw, want):
     assert layer(L, **kw) == want
