@@ -469,14 +469,16 @@ __device__ __forceinline__ void convert_bf16_to_f16(unsigned char* base, int tid
 namespace prep {
 constexpr uint32_t OFF_KQ = 0;         // per key block: K (64 rows) | Q (64 rows), 2 x 16 KB
 constexpr uint32_t OFF_KT = 32768;     // K~ (two key blocks); after the Gram: the -W image
-constexpr uint32_t OFF_ZT = 49152;     // zeros | T'   ([0; T'] operand and T' image)
+constexpr uint32_t OFF_ZT = 49152;     // zeros | T'   ([0; T'] operand and T' image); gated: T' | T''
 constexpr uint32_t OFF_LI = OFF_KQ + 8192;  // L image, in the Q rows of key block 0 once Q is used
 constexpr uint32_t OFF_AM = 65536;
 constexpr uint32_t OFF_TM = OFF_AM + 10 * kTile * 4;
 constexpr uint32_t OFF_PM = OFF_TM + 10 * kTile * 4;
 constexpr uint32_t OFF_BETA = OFF_PM + kUtScratchTiles * kTile * 4;
 constexpr uint32_t OFF_EMIT = OFF_BETA + C * 4;              // step sizes, retention, start state
-constexpr uint32_t OFF_BAR = OFF_EMIT + (2 * C + 2 * KD) * 4;
+constexpr uint32_t OFF_ALPHA = OFF_EMIT + (2 * C + 2 * KD) * 4;  // state gates of the chunk (+ pad)
+constexpr uint32_t OFF_GAM = OFF_ALPHA + (C + 4) * 4;          // their prefix products gamma
+constexpr uint32_t OFF_BAR = OFF_GAM + C * 4;
 constexpr uint32_t REGION = ((OFF_BAR + 32 + 1023) / 1024) * 1024;  // one worker, 1024-aligned
 constexpr uint32_t SMEM_ALLOC = OFF_BAR + 32 + 1024;
 constexpr uint32_t TMEM_COLS = 128;
@@ -498,7 +500,11 @@ __device__ __forceinline__ bool bar_and128(int bar, bool pred) {
 // One tensor-core pass over the loaded tiles gives [K; Q] K~^T: the Gram K K~^T (rows 0-63, for
 // A = tril(diag(beta) K K~^T, -1)) and the scores Q K~^T (rows 64-127, for L).  Then
 // T = (I + A)^-1 in fp32, T' = T diag(beta) and W = T' K (tensor cores) -> fp16 images of T', -W
-// and L in the workspace.  With EMIT the write keys of the chunk are formed here instead of
+// and L in the workspace.  With the OSGDN state gate (Appendix B.1, Eqs. (13)-(15)) the Gram and
+// score entries (i, j) carry the decay ratio gamma_i / gamma_j = prod_{j < l <= i} alpha_l (formed
+// as a running product along each row, so a zero gate gives zeros, never 0/0), and W takes
+// T diag(beta gamma) while the workspace's T' stays T diag(beta) (for U = T'V).  With EMIT the
+// write keys of the chunk are formed here instead of
 // loaded: phase 1's clipped recurrence replayed per key coordinate from the chunk's start state
 // with the step sizes the scan fixed, k~_t = d_t k_t (the same arithmetic as the emission
 // kernel), and written out as well.
@@ -546,7 +552,8 @@ struct PrepWorker {
     // r_src (stride H, or null), d_src[2 * KD] (hi, lo); tmKTout: tensor map of the k~ output.
     template <bool EMIT>
     __device__ bool run(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmKT,
-                        const float* __restrict__ beta, unsigned char* __restrict__ ws, size_t slot, int b,
+                        const float* __restrict__ beta, const float* __restrict__ alpha,
+                        unsigned char* __restrict__ ws, size_t slot, int b,
                         int h, int n, int T, int H, const float* g_src, const float* r_src, const float* d_src,
                         float dmin, float dmax, const CUtensorMap* tmKTout) {
         using namespace prep;
@@ -555,6 +562,9 @@ struct PrepWorker {
         float* PM = reinterpret_cast<float*>(sm + OFF_PM);
         float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
         float* semit = reinterpret_cast<float*>(sm + OFF_EMIT);
+        float* salpha = reinterpret_cast<float*>(sm + OFF_ALPHA);
+        float* sgam = reinterpret_cast<float*>(sm + OFF_GAM);
+        const bool gated = alpha != nullptr;
         const uint32_t lane_base = static_cast<uint32_t>((tid >> 5) * 32) << 16;
         const uint32_t id_gram = kBf16 ? tc::idesc_bf16_f32(128, C, false, false) : tc::idesc_f16_f32(128, C, false, false);
         const uint32_t id_w = tc::idesc_f16_f32(128, KD, false, true);
@@ -572,6 +582,7 @@ struct PrepWorker {
         }
         tma_pending = true;
         if (tid < C) sbeta[tid] = beta[(static_cast<size_t>(row) + tid) * H + h];
+        if (gated && tid < C) salpha[tid] = alpha[(static_cast<size_t>(row) + tid) * H + h];
         bool ready = true;
         if (EMIT) {  // the scan may still be writing these: poll until they are there (bounded)
             if (tid < C) {
@@ -586,6 +597,20 @@ struct PrepWorker {
             if (!bar_and128(bar, ok)) return false;
             tph ^= 1u;
             tma_pending = false;
+        }
+        if (gated && tid < 32) {  // gamma_j = prod_{l <= j} alpha_l: lane l forms tokens 2l, 2l + 1
+            const float a0 = salpha[2 * tid], a1 = salpha[2 * tid + 1];
+            float incl = a0 * a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl *= y;
+            }
+            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+            if (tid == 0) excl = 1.f;
+            const float g0 = excl * a0;
+            sgam[2 * tid] = g0;
+            sgam[2 * tid + 1] = g0 * a1;
         }
         if (EMIT) {  // thread tid: key coordinate tid of the 64 tokens
             const int i = tid, kb = i >> 6, c = (i & 63) >> 3, e = i & 7;
@@ -661,6 +686,16 @@ struct PrepWorker {
             tc::tmem_ld32(tbase + lane_base, *reinterpret_cast<float(*)[32]>(g));
             tc::tmem_ld32(tbase + lane_base + 32, *reinterpret_cast<float(*)[32]>(g + 32));
             tc::tmem_ld_wait();
+            if (gated) {  // decay ratios gamma_i / gamma_j along row i, j descending from i
+                float rr = 1.f;
+#pragma unroll
+                for (int j = 63; j >= 0; --j) {
+                    if (j < i) {
+                        rr *= salpha[j + 1];
+                        g[j] *= rr;
+                    }
+                }
+            }
             if (tid < C) {  // Gram rows -> strictly lower A = diag(beta) K K~^T
                 const int bi = i >> 4, r = i & 15;
                 const float bt = sbeta[i];
@@ -688,13 +723,20 @@ struct PrepWorker {
                 const float tv = (bj <= bi) ? TM[tile_index(bi, bj) * kTile + r * kTileStride + (j & 15)] : 0.f;
                 t[jj] = tv * sbeta[j];
             }
+            if (gated) {  // T' = T diag(beta) for the workspace, T'' = T diag(beta gamma) for W
+#pragma unroll
+                for (int c = 0; c < 4; ++c) st_row_chunk(sm + OFF_ZT, i, half * 4 + c, t + 8 * c);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) t[jj] *= sgam[half * 32 + jj];
+            }
 #pragma unroll
             for (int c = 0; c < 4; ++c) st_row_chunk(sm + OFF_ZT + 8192, i, half * 4 + c, t + 8 * c);
         }
         tc::fence_proxy_async();
         bar_sync128(bar);
 
-        // W = [0; T'] K  (lanes 64-127, 128 columns); K's key blocks are 16 KB apart
+        // W = [0; T'] K  (lanes 64-127, 128 columns); K's key blocks are 16 KB apart.  Gated:
+        // [T'; T''] K, whose lanes 0-63 are not used
         if (tid == 0) {
             tc::tc_fence_after();
 #pragma unroll
@@ -733,7 +775,7 @@ struct PrepWorker {
         bar_sync128(bar);
         if (tid == 0) {
             unsigned char* dst = ws + slot * WS_CHUNK;
-            tc::bulk_store(dst + WS_T, sbase + OFF_ZT + 8192, 8192);
+            tc::bulk_store(dst + WS_T, sbase + OFF_ZT + (gated ? 0 : 8192), 8192);
             tc::bulk_store(dst + WS_W, sbase + OFF_KT, 16384);
             tc::bulk_store(dst + WS_L, sbase + OFF_LI, 8192);
             tc::bulk_commit();
@@ -757,7 +799,8 @@ template <typename TIn>
 __global__ void __launch_bounds__(NTHREADS, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ beta,
-                  unsigned char* __restrict__ ws, int T, int H, int N, int total) {
+                  const float* __restrict__ alpha, unsigned char* __restrict__ ws, int T, int H, int N,
+                  int total) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -780,7 +823,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     bool aborted = false;
     for (int q = blockIdx.x; q < total; q += gridDim.x) {
         const int bh = q / N, n = q - bh * N, b = bh / H, h = bh - b * H;
-        if (!w.template run<false>(&tmQ, &tmK, &tmKT, beta, ws, static_cast<size_t>(q), b, h, n, T, H, nullptr,
+        if (!w.template run<false>(&tmQ, &tmK, &tmKT, beta, alpha, ws, static_cast<size_t>(q), b, h, n, T, H, nullptr,
                                    nullptr, nullptr, 0.f, 0.f, nullptr)) {
             aborted = true;
             break;
@@ -845,6 +888,7 @@ constexpr uint32_t B_O = 104;       // [2] O accumulated in R[b]              (c
 constexpr uint32_t B_RFREE = 120;   // [2] O read out of R[b]                 (2 warps)
 constexpr uint32_t B_DRAIN = 136;   // final commit before tensor memory is released
 constexpr uint32_t TMEM_SLOT = 144, ABORT = 148;
+constexpr uint32_t B_SSCL = 152;    // gated: S^T in TMEM scaled by the next chunk's gamma_C (4 warps)
 }  // namespace chain
 
 // Bounded wait that also gives up as soon as another role has recorded an abort.  Every lane of
@@ -890,15 +934,61 @@ __device__ __forceinline__ bool pair_any(bool pred) {
     return c != 0;
 }
 
+// Two 16-bit values (bf16 or fp16, as loaded) scaled by s0 (low half) and s1 (high half), packed
+// as fp16x2 (round to nearest).
+template <bool kBf16In>
+__device__ __forceinline__ uint32_t scale_to_f16x2(uint32_t w, float s0, float s1) {
+    float lo, hi;
+    if (kBf16In) {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xffff0000u);
+    } else {
+        const __half2 hv = *reinterpret_cast<const __half2*>(&w);
+        const float2 f = __half22float2(hv);
+        lo = f.x;
+        hi = f.y;
+    }
+    return pack_h2(lo * s0, hi * s1);
+}
+// Gate products of one chunk from its 64 state gates, two per lane (tokens 2 lane, 2 lane + 1):
+// prefix gamma_t = prod_{l <= t} alpha_l and suffix rho_t = prod_{l > t} alpha_l, by warp scans
+// (no division: a zero gate gives zeros).  Returns gamma_C = gamma_63 in every lane.
+__device__ __forceinline__ float chunk_gates(float a0, float a1, int lane, float& g0, float& g1, float& r0,
+                                             float& r1) {
+    const float p = a0 * a1;
+    float incl = p, sufx = p;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl *= y;
+        const float z = __shfl_down_sync(0xffffffffu, sufx, o);
+        if (lane + o < 32) sufx *= z;
+    }
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    float sexc = __shfl_down_sync(0xffffffffu, sufx, 1);
+    if (lane == 0) excl = 1.f;
+    if (lane == 31) sexc = 1.f;
+    g0 = excl * a0;
+    g1 = g0 * a1;
+    r1 = sexc;
+    r0 = a1 * sexc;
+    return __shfl_sync(0xffffffffu, incl, 31);
+}
+
 // One CTA per (batch, head, VS rows of S), serial over chunks.  Per chunk: U = T'V and
 // [X; Q S^T] = [U; 0] + [-W; Q] S^T; then S^T += K~^T X and O = Q S^T + L X.  T', -W and L come
 // from the workspace by bulk copy; Q, K~, V by TMA; O leaves by TMA.
-template <typename TIn>
+// GATED (OSGDN, Appendix B.1, Eqs. (13)-(15)): with gamma_t / rho_t the gate products from the
+// chunk start through t / after t, the staging warps scale the rows of Q by gamma (O = diag(gamma)
+// Q S^T + L X, the ratios being in L) and the tokens of K~ by rho (S^T <- gamma_C S^T +
+// (rho . K~)^T X); the S^T epilogue stores the unscaled fp16 copy for the S-dependent products and
+// then scales the fp32 state in tensor memory by the next chunk's gamma_C before its update.
+template <typename TIn, bool GATED>
 __global__ void __launch_bounds__(chain::NT, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKT,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                   const unsigned char* __restrict__ ws, const float* S0, float* S_out, int T, int H,
-                   int V, int N, float scale) {
+                   const unsigned char* __restrict__ ws, const float* S0, float* S_out,
+                   const float* __restrict__ alpha, int T, int H, int V, int N, float scale) {
     using namespace chain;
     constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
     extern __shared__ unsigned char smem_raw[];
@@ -928,6 +1018,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tc::mbar_init(bars + B_ST, 1);
         tc::mbar_init(bars + B_SRDY, 4);
         tc::mbar_init(bars + B_DRAIN, 1);
+        if (GATED) tc::mbar_init(bars + B_SSCL, 4);
         *abort_flag = 0;
         tc::mbar_init_fence();
         tc::prefetch_tmap(&tmQ);
@@ -1019,9 +1110,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int k = 0; k < KD / 16; ++k)
                     tc::mma_f16_ts(dR, tbase + COL_QW + bb * 64 + 8 * k, d_ss + off(k * 2048), id_h, 1);
                 tc::mma_commit(bars + B_QS + 8 * bb);
-                // S^T += K~^T X
+                // S^T += K~^T X  (gated: onto gamma_C S^T)
                 if (!(ok = thread_wait(bars + B_XRDY, n & 1, abort_flag) && thread_wait(bars + B_KT, n & 1, abort_flag)))
                     break;
+                if (GATED && !(ok = thread_wait(bars + B_SSCL, n & 1, abort_flag))) break;
                 tc::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
@@ -1104,6 +1196,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         for (int m = 0; ok && m < N; ++m) {
             const int s = m & 1, bb = m & 1;
             const unsigned char* stg = sm + s * STAGE;
+            float gm0 = 1.f, gm1 = 1.f, rh0 = 1.f, rh1 = 1.f;  // gamma, rho of tokens 2 lane, 2 lane + 1
+            if (GATED) {
+                const size_t ar = (static_cast<size_t>(b) * T + m * C + 2 * lane) * H + h;
+                chunk_gates(alpha[ar], alpha[ar + H], lane, gm0, gm1, rh0, rh1);
+            }
             if (!(ok = warp_wait(bars + B_FULL + 8 * s, (m >> 1) & 1, abort_flag))) break;
             // buffer bb was last read by U and [-W; Q] S^T of chunk m - 2
             if (m >= 2 && !(ok = warp_wait(bars + B_QS + 8 * bb, ((m - 2) >> 1) & 1, abort_flag))) break;
@@ -1134,6 +1231,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 tc::tmem_st32u(tbase + lane_base + COL_TH + bb * 32, th);
             } else {
                 uint32_t qh[32];
+                float gq = 1.f;  // gated: row r of Q scaled by gamma_r
+                if (GATED) {
+                    const float ge = __shfl_sync(0xffffffffu, gm0, r >> 1), go = __shfl_sync(0xffffffffu, gm1, r >> 1);
+                    gq = (r & 1) ? go : ge;
+                }
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll
@@ -1141,7 +1243,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_Q + kb * 8192 + tc::sw128_off(r, c));
                         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) qh[c * 4 + j] = kBf16 ? bf16x2_to_f16x2(w[j]) : w[j];
+                        for (int j = 0; j < 4; ++j)
+                            qh[c * 4 + j] = GATED ? scale_to_f16x2<kBf16>(w[j], gq, gq) : (kBf16 ? bf16x2_to_f16x2(w[j]) : w[j]);
                     }
                     tc::tmem_st32u(tbase + lane_base + COL_QW + bb * 64 + kb * 32, qh);
                 }
@@ -1162,7 +1265,12 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     const uint32_t a0 = *reinterpret_cast<const uint16_t*>(kt + tc::sw128_off(2 * t2, c));
                     const uint32_t a1 = *reinterpret_cast<const uint16_t*>(kt + tc::sw128_off(2 * t2 + 1, c));
                     const uint32_t pr = a0 | (a1 << 16);
-                    kw[t2] = kBf16 ? bf16x2_to_f16x2(pr) : pr;
+                    if (GATED) {  // tokens 2 t2, 2 t2 + 1 scaled by their rho
+                        const float q0 = __shfl_sync(0xffffffffu, rh0, t2), q1 = __shfl_sync(0xffffffffu, rh1, t2);
+                        kw[t2] = scale_to_f16x2<kBf16>(pr, q0, q1);
+                    } else {
+                        kw[t2] = kBf16 ? bf16x2_to_f16x2(pr) : pr;
+                    }
                 }
                 tc::tmem_st32u(tbase + lane_base + COL_KT, kw);
                 tc::tmem_st_wait();
@@ -1192,24 +1300,37 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     } else {
         // ============================ S^T and X epilogues =====================================
         const int k = tid;  // key coordinate = tensor-memory lane
-        {  // S0 slice -> S^T in tensor memory and its fp16 operand copy
+        // gated: gamma_C of chunk m (the product of its 64 state gates)
+        auto gamma_c = [&](int m) -> float {
+            const size_t ar = (static_cast<size_t>(b) * T + m * C + 2 * lane) * H + h;
+            float g0, g1, r0, r1;
+            return chunk_gates(alpha[ar], alpha[ar + H], lane, g0, g1, r0, r1);
+        };
+        {  // S0 slice -> S^T in tensor memory (gated: times gamma_C of chunk 0) and its fp16 operand copy
+            const float gc0 = GATED ? gamma_c(0) : 1.f;
             float sv[32];
 #pragma unroll
             for (int half = 0; half < VS / 32; ++half) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     sv[j] = S0 ? S0[(static_cast<size_t>(bh) * V + v0 + half * 32 + j) * KD + k] : 0.f;
-                tc::tmem_st32(tbase + lane_base + COL_ST + half * 32, sv);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     st_row_chunk(sm + OFF_SS + ((half * 32) / 64) * (KD * 128), k, ((half * 32) % 64) / 8 + c, sv + 8 * c);
+                if (GATED) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sv[j] *= gc0;
+                }
+                tc::tmem_st32(tbase + lane_base + COL_ST + half * 32, sv);
             }
             tc::tmem_st_wait();
             warp_publish(bars + B_SRDY, lane);
+            if (GATED) warp_publish(bars + B_SSCL, lane);
         }
         bool ok = true;
         for (int n = 0; n < N; ++n) {
             const int bb = n & 1;
+            const float gcn = (GATED && n + 1 < N) ? gamma_c(n + 1) : 1.f;  // read ahead of the waits
             if (warp < 2) {  // X rows live in tensor-memory lanes 0-63
                 if (!(ok = warp_wait(bars + B_QS + 8 * bb, (n >> 1) & 1, abort_flag))) break;
                 tc::tc_fence_after();
@@ -1236,6 +1357,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int cc = 0; cc < VS / 8; ++cc)
                     st_row_chunk(sm + OFF_SS + ((cc * 8) / 64) * (KD * 128), k, cc % 8, sv + 8 * cc);
                 warp_publish(bars + B_SRDY, lane);
+                if (GATED) {  // the next update accumulates onto gamma_C S^T (off the serial path)
+#pragma unroll
+                    for (int j = 0; j < VS; ++j) sv[j] *= gcn;
+#pragma unroll
+                    for (int q2 = 0; q2 < VS / 32; ++q2)
+                        tc::tmem_st32(tbase + lane_base + COL_ST + q2 * 32, *reinterpret_cast<float(*)[32]>(sv + q2 * 32));
+                    tc::tmem_st_wait();
+                    warp_publish(bars + B_SSCL, lane);
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < VS; ++j) S_out[(static_cast<size_t>(bh) * V + v0 + j) * KD + k] = sv[j];
@@ -1265,7 +1395,7 @@ template <typename TIn, bool HAS_R>
 __global__ void __launch_bounds__(256, 1)
 layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* counter,
                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmKT,
+                       const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ alpha,
                        unsigned char* __restrict__ cws, int N, int BH) {
     extern __shared__ unsigned char smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
@@ -1305,7 +1435,7 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
         const float* g_src = ws_g + static_cast<size_t>(bh) * T + m * C;
         const float* r_src = HAS_R ? sa.r + row0 + static_cast<size_t>(m) * C * H : nullptr;
         const float* d_src = ws_d + (static_cast<size_t>(bh) * N + m) * (2 * KD);
-        if (!pw.template run<true>(&tmQ, &tmK, nullptr, sa.beta, cws, static_cast<size_t>(bh) * N + m, b, h, m, T, H,
+        if (!pw.template run<true>(&tmQ, &tmK, nullptr, sa.beta, alpha, cws, static_cast<size_t>(bh) * N + m, b, h, m, T, H,
                                    g_src, r_src, d_src, sa.d_min, sa.d_max, &tmKT)) {
             aborted = true;
             break;
@@ -1378,8 +1508,9 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
     std::call_once(attr_once, [] {
         cudaError_t e1 = set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC);
         cudaError_t e2 = set_smem(chunk_prep_kernel<TIn>, prep::SMEM_ALLOC);
-        cudaError_t e3 = set_smem(chunk_chain_kernel<TIn>, chain::SMEM_ALLOC);
-        attr_err = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+        cudaError_t e3 = set_smem(chunk_chain_kernel<TIn, false>, chain::SMEM_ALLOC);
+        cudaError_t e4 = set_smem(chunk_chain_kernel<TIn, true>, chain::SMEM_ALLOC);
+        attr_err = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : (e3 != cudaSuccess ? e3 : e4));
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int N = a.T / C;
@@ -1389,7 +1520,7 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
         const int total = a.B * a.H * N;
         dim3 gp(static_cast<unsigned>(total < 2 * num_sms() ? total : 2 * num_sms()));
         if (!chain_only) {
-            chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta,
+            chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta, a.alpha,
                                                                       static_cast<unsigned char*>(ws), a.T, a.H, N, total);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return e;
@@ -1408,16 +1539,18 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         const unsigned char* wsc = static_cast<const unsigned char*>(ws);
-        cudaError_t e = cudaLaunchKernelEx(&cfg, chunk_chain_kernel<TIn>, mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T,
+        auto chain_kernel = a.alpha ? chunk_chain_kernel<TIn, true> : chunk_chain_kernel<TIn, false>;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel, mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.alpha, a.T,
                                            a.H, a.V, N, a.scale);
         if (e == cudaErrorNotSupported) {  // no dependent launch here: an ordinary one
             (void)cudaGetLastError();
-            chunk_chain_kernel<TIn><<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(mq, mkt, mv, mo, wsc, a.S0,
-                                                                                   a.S_out, a.T, a.H, a.V, N, a.scale);
+            chain_kernel<<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.alpha,
+                                                                       a.T, a.H, a.V, N, a.scale);
             e = cudaGetLastError();
         }
         return e;
     }
+    if (a.alpha) return cudaErrorNotSupported;  // the gate is carried by the two-kernel path only
     dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
     chunk_tc_kernel<TIn><<<grid, block, fused::SMEM_ALLOC, s>>>(mq, mk, mkt, mv, a.beta, a.S0, static_cast<TIn*>(a.o),
                                                         a.S_out, a.T, a.H, a.V, a.scale);
@@ -1481,7 +1614,8 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     unsigned int* counter = reinterpret_cast<unsigned int*>(ws + l.counter);
     unsigned char* cws = ws + l.chunk;
     int N = ca.T / C, BH = ca.B * ca.H;
-    void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &mkt, &cws, &N, &BH};
+    const float* alpha = ca.alpha;
+    void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &mkt, &alpha, &cws, &N, &BH};
     e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
                                     dim3(256), args, smem, s);
     if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer resident CTAs than expected: two calls
@@ -1505,7 +1639,7 @@ size_t osdn_layer_workspace_bytes(const OsdnScanArgs& sa, const OsdnChunkArgs& c
 // cudaErrorNotSupported when it does not apply (the caller then runs the two entry points).
 cudaError_t osdn_launch_layer(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, void* ws, size_t ws_bytes,
                               cudaStream_t s) {
-    if (!osdn::layer_covers(sa, ca) || ws == nullptr || ws_bytes < osdn::layer_ws(sa, ca).total || ca.alpha)
+    if (!osdn::layer_covers(sa, ca) || ws == nullptr || ws_bytes < osdn::layer_ws(sa, ca).total)
         return cudaErrorNotSupported;
     unsigned char* w = static_cast<unsigned char*>(ws);
     if (ca.dtype == OSDN_BF16)
@@ -1520,7 +1654,7 @@ size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a) {
 }
 
 cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
-    if (!osdn::tc_covers(a) || a.alpha) return cudaErrorNotSupported;
+    if (!osdn::tc_covers(a)) return cudaErrorNotSupported;
     if (a.dtype == OSDN_BF16) return osdn::launch_tc<__nv_bfloat16>(a, ws, ws_bytes, s);
     return osdn::launch_tc<__half>(a, ws, ws_bytes, s);
 }

@@ -136,3 +136,23 @@ def test_gated_decode_continues_the_gated_prefill():
     assert_maxabs(o1, ref["o"][:, T], 2e-2, what="decoded o")
     assert_maxabs(S, ref["S"], 2e-2, what="S after decode")
     assert np.isfinite(np64(o)).all()
+
+
+@pytest.mark.parametrize("name,B,H,T", [("layer_340m", 2, 4, 512), ("layer_1p3b_apf", 1, 6, 640)])
+def test_gated_layer_equals_two_calls(name, B, H, T):
+    """The fused layer call (phase 1 and the gated chunk prep in one launch, then the gated chain)
+    replays the same arithmetic as osdn_precond_scan then osdn_chunk_fwd: identical results."""
+    w = W.WORKLOADS[name]
+    inp = W.make_prefill(w, B=B, H=H, T=T, seed=62)
+    alpha = state_gates((B, T, H), 63, lo=0.6).cuda()
+    d = to_dev(inp)
+    S0 = (torch.randn(B, H, 128, 128, generator=torch.Generator().manual_seed(64)) * 0.05).cuda()
+    o, S, dd, kt = osdn_layer_fwd(d["q"], d["k"], d["v"], d["beta"], d["r"], None, S0, alpha=alpha, eta=0.05,
+                                  d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+    kt2, dd2 = osdn_precond_scan(d["k"], d["beta"], d["r"], None, kt_dtype=d["k"].dtype, eta=0.05, d_min=w.d_min,
+                                 d_max=w.d_max, eps=w.eps)
+    o2, S2 = osdn_chunk_fwd(d["q"], d["k"], kt2, d["v"], d["beta"], S0, alpha=alpha)
+    torch.cuda.synchronize()
+    assert torch.equal(kt, kt2) and torch.equal(dd, dd2)
+    assert torch.equal(o, o2), "o differs"
+    assert torch.equal(S, S2), "S differs"
