@@ -133,7 +133,8 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
 
 /* Workspace size in bytes that lets osdn_chunk_fwd use its two-kernel tensor-core path for these
  * arguments (0 when that path does not apply: then no workspace is ever used).  For K = V = 128
- * and chunk 64 it is B * H * (T / 64) * 32768 bytes (32 KiB per chunk of each head). */
+ * and chunk 64 it is B * H * (T / 64) * 33280 bytes per call: for each chunk of each head 32 KiB
+ * of fp16 images and the chunk's decay factors of the gated variant. */
 size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
                                       osdn_dtype dtype);
 
@@ -175,7 +176,7 @@ size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
  *   Same arguments and results as osdn_chunk_fwd without the workspace: the scratch of the
  *   two-kernel tensor-core path comes from a fixed 32 MiB array in the library's own device
  *   memory (file-scope; every GPU that loads the library holds it until the process exits).
- *   Capacity: osdn_chunk_fwd_workspace_bytes(...) <= 32 MiB, i.e. B * H * (T / 64) <= 1024 chunks;
+ *   Capacity: osdn_chunk_fwd_workspace_bytes(...) <= 32 MiB, i.e. B * H * (T / 64) <= 1008 chunks;
  *   larger requests return OSDN_ERR_CAPACITY before any launch.  Calls that need no scratch (fp32
  *   inputs, other head sizes) run the CUDA-core kernel as osdn_chunk_fwd does.
  *   Neither the library nor this call allocates (no cudaMalloc/cudaFree or allocating routine).

@@ -1,6 +1,6 @@
 // chunk_static_ws.cu -- osdn_chunk_fwd_static_ws: the chunk forward with no allocation at all.
 //
-// osdn_chunk_fwd's fast tensor-core path needs 32 KiB of scratch per chunk of each head, which the
+// osdn_chunk_fwd's fast tensor-core path needs 32.5 KiB of scratch per chunk of each head, which the
 // caller normally passes in.  Some callers cannot allocate device memory when they call: an
 // engine that reserves all GPU memory in one plan at start-up and must not allocate afterwards,
 // or code that cannot accept an allocator call (its latency, its implicit synchronisation, or its
@@ -12,7 +12,7 @@
 
 namespace {
 
-// Capacity: 1024 chunks of one head (32 KiB each), e.g. 16 heads x 4096 tokens.
+// Capacity: 1008 chunks of one head (33280 bytes each), e.g. 15 heads x 4096 tokens.
 constexpr size_t kStaticWsBytes = static_cast<size_t>(32) << 20;
 
 // File-scope device scratch.  Every GPU that loads this library holds these 32 MiB until the

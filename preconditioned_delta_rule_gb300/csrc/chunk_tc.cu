@@ -449,7 +449,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // and L = tril(Q K~^T, 0) (8 KB).
 // =============================================================================================
 constexpr uint32_t WS_T = 0, WS_W = 8192, WS_L = 24576;
-constexpr uint32_t WS_CHUNK = 32768;
+// gated (OSGDN) chunks also carry their decay factors: gamma_t = prod_{l <= t} alpha_l and
+// rho_t = prod_{l > t} alpha_l as 32 fp16 pairs each (tokens 2i, 2i + 1), then gamma_C (fp32)
+constexpr uint32_t WS_GATE = 32768, WS_GAM = 0, WS_RHO = 128, WS_GC = 256;
+constexpr uint32_t WS_CHUNK = 33280;  // a multiple of 128 bytes
 
 template <int NW>
 __device__ __forceinline__ void convert_bf16_to_f16(unsigned char* base, int tid) {
@@ -520,6 +523,42 @@ __device__ __forceinline__ float poll_word(const float* p, bool& ok) {
     }
     ok = false;
     return 0.f;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// Two 16-bit values as loaded (bf16 or fp16) converted to fp16 and multiplied by the fp16 pair s
+// (one rounding of the product; the converted values are exact in the fp16 normal range).
+template <bool kBf16In>
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t w, uint32_t s) {
+    const uint32_t h = kBf16In ? bf16x2_to_f16x2(w) : w;
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&h), *reinterpret_cast<const __half2*>(&s));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+// Gate products of one chunk from its 64 state gates, two per lane (tokens 2 lane, 2 lane + 1):
+// prefix gamma_t = prod_{l <= t} alpha_l and suffix rho_t = prod_{l > t} alpha_l, by warp scans
+// (no division: a zero gate gives zeros).  Returns gamma_C = gamma_63 in every lane.
+__device__ __forceinline__ float chunk_gates(float a0, float a1, int lane, float& g0, float& g1, float& r0,
+                                             float& r1) {
+    const float p = a0 * a1;
+    float incl = p, sufx = p;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl *= y;
+        const float z = __shfl_down_sync(0xffffffffu, sufx, o);
+        if (lane + o < 32) sufx *= z;
+    }
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    float sexc = __shfl_down_sync(0xffffffffu, sufx, 1);
+    if (lane == 0) excl = 1.f;
+    if (lane == 31) sexc = 1.f;
+    g0 = excl * a0;
+    g1 = g0 * a1;
+    r1 = sexc;
+    r0 = a1 * sexc;
+    return __shfl_sync(0xffffffffu, incl, 31);
 }
 
 template <typename TIn>
@@ -598,19 +637,16 @@ struct PrepWorker {
             tph ^= 1u;
             tma_pending = false;
         }
-        if (gated && tid < 32) {  // gamma_j = prod_{l <= j} alpha_l: lane l forms tokens 2l, 2l + 1
-            const float a0 = salpha[2 * tid], a1 = salpha[2 * tid + 1];
-            float incl = a0 * a1;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o) incl *= y;
-            }
-            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-            if (tid == 0) excl = 1.f;
-            const float g0 = excl * a0;
-            sgam[2 * tid] = g0;
-            sgam[2 * tid + 1] = g0 * a1;
+        if (gated && (tid >> 5) == 1) {  // warp 1 (warp 0 issues the Gram): the chunk's decay factors
+            const int l = tid & 31;
+            float g0, g1, r0, r1;
+            const float gc = chunk_gates(salpha[2 * l], salpha[2 * l + 1], l, g0, g1, r0, r1);
+            sgam[2 * l] = g0;
+            sgam[2 * l + 1] = g1;
+            uint32_t* wg = reinterpret_cast<uint32_t*>(ws + slot * WS_CHUNK + WS_GATE);
+            wg[(WS_GAM >> 2) + l] = pack_h2(g0, g1);
+            wg[(WS_RHO >> 2) + l] = pack_h2(r0, r1);
+            if (l == 0) reinterpret_cast<float*>(wg)[WS_GC >> 2] = gc;
         }
         if (EMIT) {  // thread tid: key coordinate tid of the 64 tokens
             const int i = tid, kb = i >> 6, c = (i & 63) >> 3, e = i & 7;
@@ -888,7 +924,6 @@ constexpr uint32_t B_O = 104;       // [2] O accumulated in R[b]              (c
 constexpr uint32_t B_RFREE = 120;   // [2] O read out of R[b]                 (2 warps)
 constexpr uint32_t B_DRAIN = 136;   // final commit before tensor memory is released
 constexpr uint32_t TMEM_SLOT = 144, ABORT = 148;
-constexpr uint32_t B_SSCL = 152;    // gated: S^T in TMEM scaled by the next chunk's gamma_C (4 warps)
 }  // namespace chain
 
 // Bounded wait that also gives up as soon as another role has recorded an abort.  Every lane of
@@ -921,9 +956,6 @@ __device__ __forceinline__ void warp_publish(uint32_t bar, int lane) {
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(bar);
 }
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-    return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
 // Named barrier over the two readout warps; true when any thread passed `pred`.
 __device__ __forceinline__ bool pair_any(bool pred) {
     uint32_t c;
@@ -934,61 +966,21 @@ __device__ __forceinline__ bool pair_any(bool pred) {
     return c != 0;
 }
 
-// Two 16-bit values (bf16 or fp16, as loaded) scaled by s0 (low half) and s1 (high half), packed
-// as fp16x2 (round to nearest).
-template <bool kBf16In>
-__device__ __forceinline__ uint32_t scale_to_f16x2(uint32_t w, float s0, float s1) {
-    float lo, hi;
-    if (kBf16In) {
-        lo = __uint_as_float(w << 16);
-        hi = __uint_as_float(w & 0xffff0000u);
-    } else {
-        const __half2 hv = *reinterpret_cast<const __half2*>(&w);
-        const float2 f = __half22float2(hv);
-        lo = f.x;
-        hi = f.y;
-    }
-    return pack_h2(lo * s0, hi * s1);
-}
-// Gate products of one chunk from its 64 state gates, two per lane (tokens 2 lane, 2 lane + 1):
-// prefix gamma_t = prod_{l <= t} alpha_l and suffix rho_t = prod_{l > t} alpha_l, by warp scans
-// (no division: a zero gate gives zeros).  Returns gamma_C = gamma_63 in every lane.
-__device__ __forceinline__ float chunk_gates(float a0, float a1, int lane, float& g0, float& g1, float& r0,
-                                             float& r1) {
-    const float p = a0 * a1;
-    float incl = p, sufx = p;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl *= y;
-        const float z = __shfl_down_sync(0xffffffffu, sufx, o);
-        if (lane + o < 32) sufx *= z;
-    }
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    float sexc = __shfl_down_sync(0xffffffffu, sufx, 1);
-    if (lane == 0) excl = 1.f;
-    if (lane == 31) sexc = 1.f;
-    g0 = excl * a0;
-    g1 = g0 * a1;
-    r1 = sexc;
-    r0 = a1 * sexc;
-    return __shfl_sync(0xffffffffu, incl, 31);
-}
-
 // One CTA per (batch, head, VS rows of S), serial over chunks.  Per chunk: U = T'V and
 // [X; Q S^T] = [U; 0] + [-W; Q] S^T; then S^T += K~^T X and O = Q S^T + L X.  T', -W and L come
 // from the workspace by bulk copy; Q, K~, V by TMA; O leaves by TMA.
 // GATED (OSGDN, Appendix B.1, Eqs. (13)-(15)): with gamma_t / rho_t the gate products from the
-// chunk start through t / after t, the staging warps scale the rows of Q by gamma (O = diag(gamma)
-// Q S^T + L X, the ratios being in L) and the tokens of K~ by rho (S^T <- gamma_C S^T +
-// (rho . K~)^T X); the S^T epilogue stores the unscaled fp16 copy for the S-dependent products and
-// then scales the fp32 state in tensor memory by the next chunk's gamma_C before its update.
+// chunk start through t / after t (formed by the prep, read from the workspace a chunk ahead), the
+// staging warps scale the rows of Q by gamma (O = diag(gamma) Q S^T + L X, the ratios being in L)
+// and the tokens of K~ by rho (S^T <- gamma_C S^T + (rho . K~)^T X); the S^T epilogue stores the
+// fp16 copy for the S-dependent products from the fp32 state it carries in registers, formed as
+// gamma_C S^T + Y from the update product Y = (rho . K~)^T X that the tensor cores leave on its own.
 template <typename TIn, bool GATED>
 __global__ void __launch_bounds__(chain::NT, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKT,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                   const unsigned char* __restrict__ ws, const float* S0, float* S_out,
-                   const float* __restrict__ alpha, int T, int H, int V, int N, float scale) {
+                   const unsigned char* __restrict__ ws, const float* S0, float* S_out, int T, int H,
+                   int V, int N, float scale) {
     using namespace chain;
     constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
     extern __shared__ unsigned char smem_raw[];
@@ -1018,7 +1010,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tc::mbar_init(bars + B_ST, 1);
         tc::mbar_init(bars + B_SRDY, 4);
         tc::mbar_init(bars + B_DRAIN, 1);
-        if (GATED) tc::mbar_init(bars + B_SSCL, 4);
         *abort_flag = 0;
         tc::mbar_init_fence();
         tc::prefetch_tmap(&tmQ);
@@ -1110,14 +1101,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int k = 0; k < KD / 16; ++k)
                     tc::mma_f16_ts(dR, tbase + COL_QW + bb * 64 + 8 * k, d_ss + off(k * 2048), id_h, 1);
                 tc::mma_commit(bars + B_QS + 8 * bb);
-                // S^T += K~^T X  (gated: onto gamma_C S^T)
+                // S^T += K~^T X  (gated: Y = (rho . K~)^T X on its own; the epilogue adds gamma_C S^T)
                 if (!(ok = thread_wait(bars + B_XRDY, n & 1, abort_flag) && thread_wait(bars + B_KT, n & 1, abort_flag)))
                     break;
-                if (GATED && !(ok = thread_wait(bars + B_SSCL, n & 1, abort_flag))) break;
                 tc::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    tc::mma_f16_ts(tbase + COL_ST, tbase + COL_KT + 8 * k, d_x + off(k * 2048), id_h, 1);
+                    tc::mma_f16_ts(tbase + COL_ST, tbase + COL_KT + 8 * k, d_x + off(k * 2048), id_h,
+                                   (GATED && k == 0) ? 0u : 1u);
                 tc::mma_commit(bars + B_ST);
                 // O = Q S^T + L X  (lanes 0-63 of the L operand only touch R rows already read)
                 if (!(ok = thread_wait(bars + B_LH, n & 1, abort_flag))) break;
@@ -1193,14 +1184,22 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             tc::tmem_st_wait();
         }
         bool ok = true;
+        // gated: gamma and rho of tokens 2 lane, 2 lane + 1 of a chunk as fp16 pairs (formed by
+        // the prep), read from the workspace one chunk ahead
+        uint32_t gpair = 0, rpair = 0, gnext = 0, rnext = 0;
+        auto gates_of = [&](int m) {
+            const uint32_t* wg = reinterpret_cast<const uint32_t*>(ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK + WS_GATE);
+            gnext = wg[(WS_GAM >> 2) + lane];
+            rnext = wg[(WS_RHO >> 2) + lane];
+        };
+        if (GATED) {
+            gates_of(0);
+            gpair = gnext;
+            rpair = rnext;
+        }
         for (int m = 0; ok && m < N; ++m) {
             const int s = m & 1, bb = m & 1;
             const unsigned char* stg = sm + s * STAGE;
-            float gm0 = 1.f, gm1 = 1.f, rh0 = 1.f, rh1 = 1.f;  // gamma, rho of tokens 2 lane, 2 lane + 1
-            if (GATED) {
-                const size_t ar = (static_cast<size_t>(b) * T + m * C + 2 * lane) * H + h;
-                chunk_gates(alpha[ar], alpha[ar + H], lane, gm0, gm1, rh0, rh1);
-            }
             if (!(ok = warp_wait(bars + B_FULL + 8 * s, (m >> 1) & 1, abort_flag))) break;
             // buffer bb was last read by U and [-W; Q] S^T of chunk m - 2
             if (m >= 2 && !(ok = warp_wait(bars + B_QS + 8 * bb, ((m - 2) >> 1) & 1, abort_flag))) break;
@@ -1231,10 +1230,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 tc::tmem_st32u(tbase + lane_base + COL_TH + bb * 32, th);
             } else {
                 uint32_t qh[32];
-                float gq = 1.f;  // gated: row r of Q scaled by gamma_r
+                uint32_t gq = 0;  // gated: row r of Q scaled by gamma_r (an fp16 pair of it)
                 if (GATED) {
-                    const float ge = __shfl_sync(0xffffffffu, gm0, r >> 1), go = __shfl_sync(0xffffffffu, gm1, r >> 1);
-                    gq = (r & 1) ? go : ge;
+                    const uint32_t gp = __shfl_sync(0xffffffffu, gpair, r >> 1);
+                    const uint32_t g16 = (r & 1) ? (gp >> 16) : (gp & 0xffffu);
+                    gq = g16 | (g16 << 16);
                 }
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
@@ -1244,7 +1244,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            qh[c * 4 + j] = GATED ? scale_to_f16x2<kBf16>(w[j], gq, gq) : (kBf16 ? bf16x2_to_f16x2(w[j]) : w[j]);
+                            qh[c * 4 + j] = GATED ? mul_f16x2<kBf16>(w[j], gq) : (kBf16 ? bf16x2_to_f16x2(w[j]) : w[j]);
                     }
                     tc::tmem_st32u(tbase + lane_base + COL_QW + bb * 64 + kb * 32, qh);
                 }
@@ -1253,6 +1253,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             if constexpr (kBf16) convert_bf16_to_f16<(VS / 64) * 4>(const_cast<unsigned char*>(stg) + ST_V, w4 * 32 + lane);
             tc::tmem_st_wait();
             warp_publish(bars + B_CONVA + 8 * bb, lane);
+            if (GATED && m + 1 < N) gates_of(m + 1);
             // K~^T (lane = key); its buffer was last read by the S^T update of chunk m - 1
             if (m >= 1 && !(ok = warp_wait(bars + B_ST, (m - 1) & 1, abort_flag))) break;
             tc::tc_fence_after();
@@ -1266,8 +1267,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     const uint32_t a1 = *reinterpret_cast<const uint16_t*>(kt + tc::sw128_off(2 * t2 + 1, c));
                     const uint32_t pr = a0 | (a1 << 16);
                     if (GATED) {  // tokens 2 t2, 2 t2 + 1 scaled by their rho
-                        const float q0 = __shfl_sync(0xffffffffu, rh0, t2), q1 = __shfl_sync(0xffffffffu, rh1, t2);
-                        kw[t2] = scale_to_f16x2<kBf16>(pr, q0, q1);
+                        kw[t2] = mul_f16x2<kBf16>(pr, __shfl_sync(0xffffffffu, rpair, t2));
                     } else {
                         kw[t2] = kBf16 ? bf16x2_to_f16x2(pr) : pr;
                     }
@@ -1295,19 +1295,21 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bars + B_FREE + 8 * s);  // this warp's reads of stage s are done
+            gpair = gnext;
+            rpair = rnext;
         }
         if (!ok) record_abort(abort_flag);
     } else {
         // ============================ S^T and X epilogues =====================================
         const int k = tid;  // key coordinate = tensor-memory lane
-        // gated: gamma_C of chunk m (the product of its 64 state gates)
+        // gated: gamma_C of a chunk (the product of its 64 state gates, formed by the prep)
         auto gamma_c = [&](int m) -> float {
-            const size_t ar = (static_cast<size_t>(b) * T + m * C + 2 * lane) * H + h;
-            float g0, g1, r0, r1;
-            return chunk_gates(alpha[ar], alpha[ar + H], lane, g0, g1, r0, r1);
+            return *reinterpret_cast<const float*>(ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK + WS_GATE + WS_GC);
         };
-        {  // S0 slice -> S^T in tensor memory (gated: times gamma_C of chunk 0) and its fp16 operand copy
-            const float gc0 = GATED ? gamma_c(0) : 1.f;
+        // gated: this lane's row of S^T (fp32) carried in registers; the update MMA leaves
+        // Y = (rho . K~)^T X in tensor memory and S^T <- gamma_C S^T + Y is formed here
+        float st[GATED ? VS : 1];
+        {  // S0 slice -> S^T (tensor memory, or registers when gated) and its fp16 operand copy
             float sv[32];
 #pragma unroll
             for (int half = 0; half < VS / 32; ++half) {
@@ -1319,18 +1321,18 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     st_row_chunk(sm + OFF_SS + ((half * 32) / 64) * (KD * 128), k, ((half * 32) % 64) / 8 + c, sv + 8 * c);
                 if (GATED) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) sv[j] *= gc0;
+                    for (int j = 0; j < 32; ++j) st[half * 32 + j] = sv[j];
+                } else {
+                    tc::tmem_st32(tbase + lane_base + COL_ST + half * 32, sv);
                 }
-                tc::tmem_st32(tbase + lane_base + COL_ST + half * 32, sv);
             }
-            tc::tmem_st_wait();
+            if (!GATED) tc::tmem_st_wait();
             warp_publish(bars + B_SRDY, lane);
-            if (GATED) warp_publish(bars + B_SSCL, lane);
         }
         bool ok = true;
         for (int n = 0; n < N; ++n) {
             const int bb = n & 1;
-            const float gcn = (GATED && n + 1 < N) ? gamma_c(n + 1) : 1.f;  // read ahead of the waits
+            const float gcn = GATED ? gamma_c(n) : 1.f;  // gamma_C of this chunk, used after its update
             if (warp < 2) {  // X rows live in tensor-memory lanes 0-63
                 if (!(ok = warp_wait(bars + B_QS + 8 * bb, (n >> 1) & 1, abort_flag))) break;
                 tc::tc_fence_after();
@@ -1352,20 +1354,18 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             for (int q2 = 0; q2 < VS / 32; ++q2)
                 tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, *reinterpret_cast<float(*)[32]>(sv + q2 * 32));
             tc::tmem_ld_wait();
+            if (GATED) {
+#pragma unroll
+                for (int j = 0; j < VS; ++j) {
+                    st[j] = fmaf(gcn, st[j], sv[j]);
+                    sv[j] = st[j];
+                }
+            }
             if (n + 1 < N) {
 #pragma unroll
                 for (int cc = 0; cc < VS / 8; ++cc)
                     st_row_chunk(sm + OFF_SS + ((cc * 8) / 64) * (KD * 128), k, cc % 8, sv + 8 * cc);
                 warp_publish(bars + B_SRDY, lane);
-                if (GATED) {  // the next update accumulates onto gamma_C S^T (off the serial path)
-#pragma unroll
-                    for (int j = 0; j < VS; ++j) sv[j] *= gcn;
-#pragma unroll
-                    for (int q2 = 0; q2 < VS / 32; ++q2)
-                        tc::tmem_st32(tbase + lane_base + COL_ST + q2 * 32, *reinterpret_cast<float(*)[32]>(sv + q2 * 32));
-                    tc::tmem_st_wait();
-                    warp_publish(bars + B_SSCL, lane);
-                }
             } else {
 #pragma unroll
                 for (int j = 0; j < VS; ++j) S_out[(static_cast<size_t>(bh) * V + v0 + j) * KD + k] = sv[j];
@@ -1540,12 +1540,12 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
         cfg.numAttrs = 1;
         const unsigned char* wsc = static_cast<const unsigned char*>(ws);
         auto chain_kernel = a.alpha ? chunk_chain_kernel<TIn, true> : chunk_chain_kernel<TIn, false>;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel, mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.alpha, a.T,
-                                           a.H, a.V, N, a.scale);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel, mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T, a.H, a.V,
+                                           N, a.scale);
         if (e == cudaErrorNotSupported) {  // no dependent launch here: an ordinary one
             (void)cudaGetLastError();
-            chain_kernel<<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.alpha,
-                                                                       a.T, a.H, a.V, N, a.scale);
+            chain_kernel<<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T,
+                                                                       a.H, a.V, N, a.scale);
             e = cudaGetLastError();
         }
         return e;

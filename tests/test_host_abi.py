@@ -117,8 +117,8 @@ def test_binding_rejects_host_tensors(L):
 
 def test_workspace_size_query(L):
     f = L.osdn_chunk_fwd_workspace_bytes
-    assert f(8, 2048, 8, 128, 128, 64, 1) == 8 * 8 * 32 * 32768
-    assert f(1, 64, 1, 128, 128, 64, 2) == 32768
+    assert f(8, 2048, 8, 128, 128, 64, 1) == 8 * 8 * 32 * 33280
+    assert f(1, 64, 1, 128, 128, 64, 2) == 33280
     assert f(1, 64, 1, 64, 64, 64, 1) == 0      # shapes the tensor-core path does not cover
     assert f(1, 64, 1, 128, 128, 64, 0) == 0    # fp32 inputs use the CUDA-core kernel
     assert f(1, 100, 1, 128, 128, 64, 1) == 0   # T not a multiple of the chunk
@@ -157,7 +157,7 @@ def test_layer_validation(L, kw, want):
 def test_layer_workspace_size_query(L):
     f = L.osdn_layer_fwd_workspace_bytes
     scan = 4 * 8 * 8 * (2048 + 32 * 256)
-    chunk = 8 * 8 * 32 * 32768
+    chunk = 8 * 8 * 32 * 33280
     got = f(8, 2048, 8, 128, 128, 64, 1)
     assert got >= scan + chunk + 4               # both workspaces and a chunk counter
     assert got < scan + chunk + 1024

@@ -50,7 +50,7 @@ def test_static_scratch_matches_workspace_path_twice():
 
 
 def test_static_scratch_rejects_requests_over_capacity():
-    """1037 chunk-heads need 1037 x 32 KiB > 32 MiB: refused before any launch."""
+    """1037 chunk-heads need 1037 x 33280 B > 32 MiB: refused before any launch."""
     B, T, H = 1, 64 * 61, 17
     e = lambda *s: torch.zeros(*s, dtype=torch.bfloat16, device="cuda")
     q, k, kt, v = e(B, T, H, 128), e(B, T, H, 128), e(B, T, H, 128), e(B, T, H, 128)
