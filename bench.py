@@ -62,8 +62,8 @@ def layer_bytes(w):
 # kernels behind it change, until they are captured again.
 NCU_TRAFFIC = {
     "layer_340m": {
-        # layer_scan_prep_kernel 68.79 + 51.95 MB, chunk_chain_kernel 167.85 + 21.13 MB
-        "osdn_layer_fwd": 309.72e6,
+        # layer_scan_prep_kernel 68.17 + 51.40 MB, chunk_chain_kernel 167.86 + 21.36 MB
+        "osdn_layer_fwd": 308.79e6,
     },
 }
 
@@ -347,6 +347,7 @@ def run_ours(args, w):
     decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak)
     vret = None if args.no_vector_retention else run_vector_retention(args, dev, stream, hbm_peak)
     configs = None if args.no_configs else run_configs(args, dev, stream, hbm_peak)
+    gated = None if args.no_gated else run_gated(args, dev, stream, hbm_peak)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, secs, sample, threads = oracle_layer_rate(w, host, budget_s=args.ref_budget)
@@ -362,7 +363,7 @@ def run_ours(args, w):
                        "chunk": w.chunk, "eta": w.eta, "box": [w.d_min, w.d_max],
                        "l2": "flushed between steps (256 MiB write outside the timed events)"},
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "decode": decode, "other_configs": configs, "vector_retention": vret,
+            "decode": decode, "other_configs": configs, "gated": gated, "vector_retention": vret,
             "gpu_launches": launches_per_step * n, "clocks": clk.summary(),
             "wall_s_timed_region": wall,
         }
@@ -414,9 +415,10 @@ def run_e2e(args, w, host, dev, stream, ws):
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * secs / n}
 
 
-def run_decode(args, dev, stream, hbm_peak):
+def run_decode(args, dev, stream, hbm_peak, gated=False):
     """The decode workload: B=256, H=16, K=V=128, fp32 state, `steps` sequential tokens with
-    all per-step inputs resident in HBM; the token loop is one CUDA graph."""
+    all per-step inputs resident in HBM; the token loop is one CUDA graph.  gated: with an OSGDN
+    state gate per token and head (sigmoid(4 + N(0, 1)), resident in HBM like the other inputs)."""
     from preconditioned_delta_rule_gb300 import binding
     from preconditioned_delta_rule_gb300 import workloads as W
 
@@ -426,11 +428,16 @@ def run_decode(args, dev, stream, hbm_peak):
     S, d = W.make_decode_state(w, device=dev)
     S0, d0 = S.clone(), d.clone()
     o = torch.empty((steps, w.B, w.H, w.V), device=dev, dtype=inp["v"].dtype)
+    alpha = None
+    if gated:
+        g = torch.Generator().manual_seed(6)
+        alpha = torch.sigmoid(4.0 + torch.randn(steps, w.B, w.H, generator=g)).to(dev)
 
     def loop():
         for t in range(steps):
             binding.osdn_decode_step(inp["q"][t], inp["k"][t], inp["v"][t], inp["beta"][t], S, d,
-                                     o=o[t], eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+                                     alpha=None if alpha is None else alpha[t], o=o[t], eta=w.eta,
+                                     d_min=w.d_min, d_max=w.d_max, eps=w.eps)
 
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
@@ -459,9 +466,9 @@ def run_decode(args, dev, stream, hbm_peak):
     binding.osdn_check()
     secs = statistics.median(times)
     per_step = secs / steps
-    b = decode_bytes(w)
+    b = decode_bytes(w) + (w.B * w.H * 4 if gated else 0)
     ach = b / per_step / 1e9
-    return {"workload": w.name, "B": w.B, "H": w.H, "K": w.K, "V": w.V, "steps": steps,
+    return {"workload": w.name + ("_gated" if gated else ""), "B": w.B, "H": w.H, "K": w.K, "V": w.V, "steps": steps,
             "value": steps / secs, "unit": "steps/s", "us_per_step": per_step * 1e6,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
                          "frac": ach / hbm_peak, "algorithmic_bytes_per_launch": b},
@@ -522,6 +529,54 @@ def run_configs(args, dev, stream, hbm_peak, names=("layer_1p3b_apf", "longctx_r
     return out
 
 
+def run_gated(args, dev, stream, hbm_peak):
+    """The gated variant (OSGDN, Appendix B.1): osdn_layer_fwd and osdn_chunk_fwd on the
+    340M-shaped layer (B=8, H=8, T=2048) with a state gate alpha = sigmoid(4 + N(0, 1)) per token
+    and head, median of reps with L2 flushed between them; and the gated decode step on the
+    decode workload."""
+    from preconditioned_delta_rule_gb300 import binding
+    from preconditioned_delta_rule_gb300 import workloads as W
+
+    w = W.WORKLOADS["layer_340m"]
+    g = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in W.make_prefill(w).items()}
+    gen = torch.Generator().manual_seed(5)
+    alpha = torch.sigmoid(4.0 + torch.randn(w.B, w.T, w.H, generator=gen)).to(dev)
+    kt = torch.empty_like(g["k"])
+    kw = dict(eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    binding.osdn_precond_scan(g["k"], g["beta"], g["r"], k_tilde=kt, **kw)
+
+    def med(fn):
+        fn()
+        times = []
+        for i in range(max(3, args.decode_reps)):
+            flush.fill_(float(i))
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record(stream)
+            fn()
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+        binding.osdn_check()
+        return statistics.median(times)
+
+    t_layer = med(lambda: binding.osdn_layer_fwd(g["q"], g["k"], g["v"], g["beta"], g["r"], alpha=alpha,
+                                                 k_tilde=kt, **kw))
+    t_chunk = med(lambda: binding.osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], alpha=alpha))
+    _, b_chunk, b_layer = layer_bytes(w)
+    th = w.B * w.T * w.H
+    b_chunk += 4 * th
+    b_layer += 4 * th
+    frac = lambda b, t: b / t / 1e9 / hbm_peak
+    dec = None if args.no_decode else run_decode(args, dev, stream, hbm_peak, gated=True)
+    return {"workload": w.name + "_gated", "B": w.B, "H": w.H, "T": w.T,
+            "gate": "alpha = sigmoid(4 + N(0, 1)) per token and head",
+            "layer_ms": t_layer * 1e3, "tokens_per_s": th / w.H / t_layer,
+            "layer_roofline_frac": frac(b_layer, t_layer),
+            "chunk_ms": t_chunk * 1e3, "chunk_roofline_frac": frac(b_chunk, t_chunk),
+            "decode": dec}
+
+
 def run_vector_retention(args, dev, stream, hbm_peak):
     """Phase 1 with one APF gate per key coordinate (diag(r_t), the pages' Appendix A.5) on the
     1.3B-shaped workload (B=4, H=16, T=4096, bf16 keys): the token-by-token scan kernel, gates
@@ -580,6 +635,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-vector-retention", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other prefill configs")
+    ap.add_argument("--no-gated", action="store_true", help="skip the gated variant (OSGDN)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
