@@ -168,6 +168,38 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
 size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype);
 
 /*
+ * The layer forward over packed variable-length sequences (cu_seqlens).  N sequences are
+ * concatenated along the token axis: sequence n owns rows cu_seqlens[n] .. cu_seqlens[n+1]-1 of
+ * q, k, v [total, H, K|V] (dtype `dtype`), beta, alpha [total, H] fp32, r [total, H] (or
+ * [total, H, K] with r_per_key = 1); it starts from d0[n] [H, K] and S0[n] [H, V, K] (NULL: ones,
+ * zeros) and ends in d_out[n], S_out[n] ([N, H, K] and [N, H, V, K], fp32, written).  k_tilde
+ * [total, H, K] and o [total, H, V] are written.  Each sequence gets exactly the result it would
+ * get alone (Algorithm 1 and Eqs. (2), (4), (7), and Appendix B.1 with alpha, per sequence).
+ *   cu_seqlens  device int32 [N + 1], non-decreasing from 0 to total (read on the device; a
+ *               sequence whose range is not within [0, total] or is longer than max_len is
+ *               skipped and the next osdn_check reports OSDN_ERR_SHAPE)
+ *   total       packed tokens (rows of q); max_len >= every sequence length (host value)
+ *   workspace, workspace_bytes
+ *               required: at least osdn_layer_fwd_varlen_workspace_bytes(...) bytes, 16-byte
+ *               aligned (OSDN_ERR_ARG when missing or smaller).  It holds the sequences scattered
+ *               into an [N, Tp, H, .] batch, Tp = max_len rounded up to the chunk, with padding
+ *               tokens that leave d and S unchanged (k = q = v = 0, beta = 0, retention and state
+ *               gate 1), and the batched layer's own workspace; the outputs are gathered back.
+ * Other arguments as osdn_layer_fwd.  A sequence of length 0 returns d0 and S0 unchanged.
+ */
+osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
+                                  const float* r, int r_per_key, const float* alpha, const int* cu_seqlens, int N,
+                                  long long total, int max_len, const float* d0, const float* S0, void* k_tilde,
+                                  void* o, float* S_out, float* d_out, int H, int K, int V, int chunk, float eta,
+                                  float d_min, float d_max, float eps, float scale, int beta_aware, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* Workspace size for osdn_layer_fwd_varlen: r_mode 0 (no retention), 1 (one per head) or 2 (one
+ * per key coordinate); gated nonzero when alpha is passed.  0 for invalid arguments. */
+size_t osdn_layer_fwd_varlen_workspace_bytes(int N, int max_len, int H, int K, int V, int chunk, osdn_dtype dtype,
+                                             int r_mode, int gated);
+
+/*
  * osdn_chunk_fwd for callers that cannot allocate device memory when they call -- for example an
  * engine that reserves all GPU memory in one plan at start-up and allocates nothing afterwards,
  * or code that cannot accept an allocator call (its latency, its implicit synchronisation, its
@@ -208,8 +240,9 @@ osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_d
                              float eps, float scale, int beta_aware, void* stream);
 
 /* Waits for `stream`, then reports OSDN_ERR_TIMEOUT if any kernel of this library gave up a
- * bounded device-side wait since the last check (and clears the flag), OSDN_ERR_CUDA if the
- * stream holds a CUDA error, else OSDN_OK. */
+ * bounded device-side wait since the last check, OSDN_ERR_SHAPE if a varlen call met an invalid
+ * cu_seqlens range (both flags are cleared), OSDN_ERR_CUDA if the stream holds a CUDA error, else
+ * OSDN_OK. */
 osdn_status osdn_check(void* stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */

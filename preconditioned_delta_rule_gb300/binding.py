@@ -57,6 +57,12 @@ def lib() -> ctypes.CDLL:
     L.osdn_layer_fwd.restype = ctypes.c_int
     L.osdn_layer_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.osdn_layer_fwd_workspace_bytes.restype = sz
+    ll = ctypes.c_longlong
+    L.osdn_layer_fwd_varlen.argtypes = [vp, vp, vp, i, fp, fp, i, fp, vp, i, ll, i, fp, fp, vp, vp, fp, fp, i, i, i,
+                                        i, f, f, f, f, f, i, vp, sz, vp]
+    L.osdn_layer_fwd_varlen.restype = ctypes.c_int
+    L.osdn_layer_fwd_varlen_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i]
+    L.osdn_layer_fwd_varlen_workspace_bytes.restype = sz
     L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
     L.osdn_check.argtypes = [vp]
     for fn in ("osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step", "osdn_check"):
@@ -296,6 +302,71 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, k_til
                               float(scale), int(bool(beta_aware)), ws_ptr, ws_bytes,
                               _stream(dev, stream))
     _raise("osdn_layer_fwd", st)
+    return o, S_out, d_out, k_tilde
+
+
+def osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk=64, dtype=torch.bfloat16, r_mode=0,
+                                          gated=False) -> int:
+    return int(lib().osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk, _code(dtype), int(r_mode),
+                                                           int(bool(gated))))
+
+
+def osdn_layer_fwd_varlen(q, k, v, beta, cu_seqlens, *, max_len=None, r=None, alpha=None, d0=None, S0=None,
+                          k_tilde=None, o=None, S_out=None, d_out=None, chunk=64, eta=0.003, d_min=0.5, d_max=2.0,
+                          eps=1e-6, scale=1.0, beta_aware=True, workspace=None, stream=None):
+    """The layer forward over N packed variable-length sequences.  q, k [total,H,K] and v [total,H,V]
+    (a leading batch dimension of 1 is accepted), beta and alpha [total,H], r [total,H] or
+    [total,H,K]; cu_seqlens: int32 CUDA tensor [N+1] of sequence offsets; d0 [N,H,K], S0 [N,H,V,K]
+    per sequence.  ``max_len`` (the longest sequence) is read from cu_seqlens when None, which
+    synchronises.  Returns (o [total,H,V], S_out [N,H,V,K], d_out [N,H,K], k_tilde [total,H,K])."""
+    squeeze = k.dim() == 4
+    if squeeze:
+        if k.shape[0] != 1:
+            raise ValueError("packed sequences take a leading batch dimension of 1 at most")
+        q, k, v, beta = q[0], k[0], v[0], beta[0]
+        r = None if r is None else r[0]
+        alpha = None if alpha is None else alpha[0]
+    total, H, K = k.shape
+    V = v.shape[-1]
+    dev, dt = k.device, k.dtype
+    for name, t, shp in (("q", q, (total, H, K)), ("k", k, (total, H, K)), ("v", v, (total, H, V))):
+        _check(name, t, shp, dt, dev)
+    _check("beta", beta, (total, H), torch.float32, dev)
+    r_per_key = _retention(r, (total, H), K, dev)
+    _check("alpha", alpha, (total, H), torch.float32, dev)
+    _check("cu_seqlens", cu_seqlens, (cu_seqlens.shape[0],), torch.int32, dev)
+    N = cu_seqlens.shape[0] - 1
+    if N < 0:
+        raise ValueError("cu_seqlens needs at least one entry")
+    if max_len is None:
+        max_len = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 0
+    _check("d0", d0, (N, H, K), torch.float32, dev)
+    _check("S0", S0, (N, H, V, K), torch.float32, dev)
+    if k_tilde is None:
+        k_tilde = torch.empty((total, H, K), device=dev, dtype=dt)
+    _check("k_tilde", k_tilde, (total, H, K), dt, dev)
+    if o is None:
+        o = torch.empty((total, H, V), device=dev, dtype=dt)
+    _check("o", o, (total, H, V), dt, dev)
+    if S_out is None:
+        S_out = torch.empty((N, H, V, K), device=dev, dtype=torch.float32)
+    _check("S_out", S_out, (N, H, V, K), torch.float32, dev)
+    if d_out is None:
+        d_out = torch.empty((N, H, K), device=dev, dtype=torch.float32)
+    _check("d_out", d_out, (N, H, K), torch.float32, dev)
+    r_mode = 0 if r is None else 1 + r_per_key
+    need = osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk, dt, r_mode, alpha is not None) if N else 0
+    if workspace is False:
+        raise ValueError("osdn_layer_fwd_varlen needs a workspace")
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "varlen")
+    st = lib().osdn_layer_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, _ptr(alpha),
+                                     _ptr(cu_seqlens), N, int(total), int(max_len), _ptr(d0), _ptr(S0), _ptr(k_tilde),
+                                     _ptr(o), _ptr(S_out), _ptr(d_out), H, K, V, int(chunk), float(eta), float(d_min),
+                                     float(d_max), float(eps), float(scale), int(bool(beta_aware)), ws_ptr, ws_bytes,
+                                     _stream(dev, stream))
+    _raise("osdn_layer_fwd_varlen", st)
+    if squeeze:
+        return o[None], S_out, d_out, k_tilde[None]
     return o, S_out, d_out, k_tilde
 
 

@@ -43,6 +43,33 @@ cudaError_t chunk_dispatch(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cu
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// phase 1 then phase 2: the fused layer path when it applies, else the two calls, each with its
+// part of the workspace when it fits
+cudaError_t layer_dispatch(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, void* workspace, size_t workspace_bytes,
+                           cudaStream_t s) {
+    if (sa.T > 0) {
+        cudaError_t e = osdn_launch_layer(sa, ca, workspace, workspace_bytes, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    const size_t need_s = osdn_scan_block_workspace_bytes(sa);
+    const size_t need_c = osdn_chunk_tc_workspace_bytes(ca);
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    void* ws_s = nullptr;
+    void* ws_c = nullptr;
+    if (w && workspace_bytes >= align256(need_s) + need_c) {
+        ws_s = need_s ? w : nullptr;
+        ws_c = need_c ? w + align256(need_s) : nullptr;
+    } else if (w && need_c && workspace_bytes >= need_c) {
+        ws_c = w;
+    } else if (w && need_s && workspace_bytes >= need_s) {
+        ws_s = w;
+    }
+    cudaError_t e = osdn_launch_scan(sa, ws_s, ws_s ? need_s : 0, s);
+    if (e != cudaSuccess) return e;
+    return chunk_dispatch(ca, ws_c, ws_c ? need_c : 0, s);
+}
+
+
 }  // namespace
 
 extern "C" {
@@ -148,28 +175,7 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
     OsdnScanArgs sa{k, dtype, beta, r, d0, k_tilde, dtype, d_out, B, T, H, K, eta, d_min, d_max, eps, beta_aware ? 1 : 0,
                     r != nullptr ? r_per_key : 0};
     OsdnChunkArgs ca{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale, alpha};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (seq) {
-        cudaError_t e = osdn_launch_layer(sa, ca, workspace, workspace_bytes, s);
-        if (e != cudaErrorNotSupported) return from_cuda(e);
-    }
-    // the two phases one after the other, each with its part of the workspace when it fits
-    const size_t need_s = osdn_scan_block_workspace_bytes(sa);
-    const size_t need_c = osdn_chunk_tc_workspace_bytes(ca);
-    unsigned char* w = static_cast<unsigned char*>(workspace);
-    void* ws_s = nullptr;
-    void* ws_c = nullptr;
-    if (w && workspace_bytes >= align256(need_s) + need_c) {
-        ws_s = need_s ? w : nullptr;
-        ws_c = need_c ? w + align256(need_s) : nullptr;
-    } else if (w && need_c && workspace_bytes >= need_c) {
-        ws_c = w;
-    } else if (w && need_s && workspace_bytes >= need_s) {
-        ws_s = w;
-    }
-    cudaError_t e = osdn_launch_scan(sa, ws_s, ws_s ? need_s : 0, s);
-    if (e != cudaSuccess) return from_cuda(e);
-    return from_cuda(chunk_dispatch(ca, ws_c, ws_c ? need_c : 0, s));
+    return from_cuda(layer_dispatch(sa, ca, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype) {
@@ -182,6 +188,98 @@ size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
     if (fused) return fused;
     const size_t need_s = osdn_scan_block_workspace_bytes(sa), need_c = osdn_chunk_tc_workspace_bytes(ca);
     return need_c ? align256(need_s) + need_c : need_s;
+}
+
+static OsdnVarlenShape varlen_shape(int N, int max_len, int H, int K, int V, int chunk, osdn_dtype dtype,
+                                    int r_mode, int gated, long long total) {
+    OsdnVarlenShape v{};
+    v.N = N;
+    v.Tp = max_len <= chunk ? chunk : ((max_len + chunk - 1) / chunk) * chunk;
+    v.H = H;
+    v.K = K;
+    v.V = V;
+    v.total = total;
+    v.elt = dtype == OSDN_F32 ? 4 : 2;
+    v.r_mode = r_mode;
+    v.gated = gated;
+    return v;
+}
+
+size_t osdn_layer_fwd_varlen_workspace_bytes(int N, int max_len, int H, int K, int V, int chunk, osdn_dtype dtype,
+                                             int r_mode, int gated) {
+    if (N <= 0 || max_len < 0 || H <= 0 || chunk <= 0 || !head_dim_ok(K) || !head_dim_ok(V) || !dtype_ok(dtype))
+        return 0;
+    if (r_mode < 0 || r_mode > 2) return 0;
+    const OsdnVarlenShape v = varlen_shape(N, max_len, H, K, V, chunk, dtype, r_mode, gated ? 1 : 0, 0);
+    return align256(osdn_varlen_pad_bytes(v)) + osdn_layer_fwd_workspace_bytes(N, v.Tp, H, K, V, chunk, dtype);
+}
+
+osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
+                                  const float* r, int r_per_key, const float* alpha, const int* cu_seqlens, int N,
+                                  long long total, int max_len, const float* d0, const float* S0, void* k_tilde,
+                                  void* o, float* S_out, float* d_out, int H, int K, int V, int chunk, float eta,
+                                  float d_min, float d_max, float eps, float scale, int beta_aware, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    if (N < 0 || total < 0 || max_len < 0 || H < 0 || chunk <= 0) return OSDN_ERR_SHAPE;
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return (K > 0 && V > 0) ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
+    if (chunk != 64) return OSDN_ERR_UNSUPPORTED;
+    if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
+    OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
+    if (!isfinite(scale)) return OSDN_ERR_ARG;
+    if (r_per_key != 0 && r_per_key != 1) return OSDN_ERR_ARG;
+    if ((long long)N * H > 0x7fffffffLL || total > 0x7fffffffLL) return OSDN_ERR_SHAPE;
+    if (N == 0 || H == 0) return OSDN_OK;
+    const bool seq = total > 0;
+    OSDN_TRY(ptr(cu_seqlens, true));
+    OSDN_TRY(ptr(q, seq));
+    OSDN_TRY(ptr(k, seq));
+    OSDN_TRY(ptr(v, seq));
+    OSDN_TRY(ptr(beta, seq));
+    OSDN_TRY(ptr(k_tilde, seq));
+    OSDN_TRY(ptr(o, seq));
+    OSDN_TRY(ptr(r, false));
+    OSDN_TRY(ptr(alpha, false));
+    OSDN_TRY(ptr(d0, false));
+    OSDN_TRY(ptr(S0, false));
+    OSDN_TRY(ptr(S_out, true));
+    OSDN_TRY(ptr(d_out, true));
+    OSDN_TRY(ptr(workspace, true));
+    const int r_mode = r ? (r_per_key ? 2 : 1) : 0;
+    const OsdnVarlenShape vs = varlen_shape(N, max_len, H, K, V, chunk, dtype, r_mode, alpha ? 1 : 0, total);
+    const size_t pad = align256(osdn_varlen_pad_bytes(vs));
+    const size_t need_layer = osdn_layer_fwd_workspace_bytes(N, vs.Tp, H, K, V, chunk, dtype);
+    if (workspace_bytes < pad + need_layer) return OSDN_ERR_ARG;
+    // the padded batch, each part 256-byte aligned, then the batched layer's own workspace
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    const size_t rows = static_cast<size_t>(N) * vs.Tp;
+    auto take = [&](size_t bytes) {
+        unsigned char* p = w;
+        w += align256(bytes);
+        return p;
+    };
+    OsdnVarlenIo io{};
+    io.cu = cu_seqlens;
+    io.q = q; io.k = k; io.v = v; io.beta = beta; io.r = r; io.alpha = alpha;
+    io.k_tilde = k_tilde; io.o = o; io.d0 = d0; io.d_out = d_out;
+    io.pq = take(rows * H * K * vs.elt);
+    io.pk = take(rows * H * K * vs.elt);
+    io.pkt = take(rows * H * K * vs.elt);
+    io.pv = take(rows * H * V * vs.elt);
+    io.po = take(rows * H * V * vs.elt);
+    io.pbeta = reinterpret_cast<float*>(take(rows * H * 4));
+    if (r_mode) io.pr = reinterpret_cast<float*>(take(rows * H * (r_mode == 2 ? K : 1) * 4));
+    if (alpha) io.palpha = reinterpret_cast<float*>(take(rows * H * 4));
+    unsigned char* wl = static_cast<unsigned char*>(workspace) + pad;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = osdn_launch_varlen_pack(io, vs, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    OsdnScanArgs sa{io.pk, dtype, io.pbeta, io.pr, d0, io.pkt, dtype, d_out, N, vs.Tp, H, K, eta, d_min, d_max, eps,
+                    beta_aware ? 1 : 0, r_mode == 2 ? 1 : 0};
+    OsdnChunkArgs ca{io.pq, io.pk, io.pkt, io.pv, dtype, io.pbeta, S0, io.po, S_out, N, vs.Tp, H, K, V, chunk, scale,
+                     io.palpha};
+    e = layer_dispatch(sa, ca, wl, need_layer, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(osdn_launch_varlen_unpack(io, vs, s));
 }
 
 osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,
@@ -213,10 +311,12 @@ osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_d
 
 osdn_status osdn_check(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned int flag = 0;
+    unsigned int flag = 0, bad = 0;
     cudaError_t e = osdn_read_and_clear_timeout(&flag, s);
     if (e != cudaSuccess) return OSDN_ERR_CUDA;
+    if (osdn_varlen_read_and_clear_flag(&bad) != cudaSuccess) return OSDN_ERR_CUDA;
     if (flag) return OSDN_ERR_TIMEOUT;
+    if (bad) return OSDN_ERR_SHAPE;
     return OSDN_OK;
 }
 

@@ -126,6 +126,26 @@ cudaError_t osdn_launch_chunk_simt(const OsdnChunkArgs& a, cudaStream_t s);
 cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a);
 cudaError_t osdn_launch_decode(const OsdnDecodeArgs& a, cudaStream_t s);
+// Packed variable-length sequences: scatter into an [N, Tp, H, .] batch and gather back.
+struct OsdnVarlenShape {
+    int N, Tp, H, K, V;
+    long long total;  // packed tokens
+    int elt;          // bytes per q/k/v/o/k~ element
+    int r_mode;       // 0 no retention, 1 one per head, 2 one per key coordinate
+    int gated;        // alpha given
+};
+struct OsdnVarlenIo {
+    const int* cu;                                        // [N + 1] sequence offsets
+    const void* q; const void* k; const void* v;          // packed inputs [total, H, .]
+    const float* beta; const float* r; const float* alpha;
+    void* k_tilde; void* o;                               // packed outputs
+    const float* d0; float* d_out;                        // [N, H, K]
+    void* pq; void* pk; void* pv; float* pbeta; float* pr; float* palpha; void* pkt; void* po;  // padded
+};
+size_t osdn_varlen_pad_bytes(const OsdnVarlenShape& v);
+cudaError_t osdn_launch_varlen_pack(const OsdnVarlenIo& io, const OsdnVarlenShape& v, cudaStream_t s);
+cudaError_t osdn_launch_varlen_unpack(const OsdnVarlenIo& io, const OsdnVarlenShape& v, cudaStream_t s);
+cudaError_t osdn_varlen_read_and_clear_flag(unsigned int* flag);
 // Fused layer forward (phase 1 + chunk prep in one cooperative launch, then the chain kernel).
 cudaError_t osdn_launch_layer(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, void* ws, size_t ws_bytes,
                               cudaStream_t s);

@@ -163,3 +163,38 @@ def test_layer_workspace_size_query(L):
     assert got < scan + chunk + 1024
     assert f(1, 64, 1, 64, 64, 64, 0) == 0        # fp32, K = 64: no workspace is used
     assert f(1, 100, 1, 128, 128, 64, 1) == 0     # T not a multiple of the chunk
+
+
+def varlen(L, **kw):
+    a = dict(q=A, k=A, v=A, dt=1, beta=A, r=None, rpk=0, alpha=None, cu=A, N=3, total=300, maxlen=128, d0=None,
+             S0=None, kt=A, o=A, Sout=A, dout=A, H=2, K=128, V=128, C=64, eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6,
+             scale=1.0, ba=1, ws=A, wsb=1 << 40)
+    a.update(kw)
+    return L.osdn_layer_fwd_varlen(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a["rpk"], a["alpha"], a["cu"],
+                                   a["N"], a["total"], a["maxlen"], a["d0"], a["S0"], a["kt"], a["o"], a["Sout"],
+                                   a["dout"], a["H"], a["K"], a["V"], a["C"], a["eta"], a["dmin"], a["dmax"], a["eps"],
+                                   a["scale"], a["ba"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(cu=None), ARG), (dict(ws=None), ARG), (dict(wsb=1024), ARG), (dict(cu=A + 4), ALIGN),
+    (dict(q=A + 2), ALIGN), (dict(alpha=A + 8), ALIGN), (dict(dout=None), ARG), (dict(K=96), UNSUP),
+    (dict(C=32), UNSUP), (dict(N=-1), SHAPE), (dict(total=-1), SHAPE), (dict(maxlen=-1), SHAPE),
+    (dict(dt=9), DTYPE), (dict(rpk=2), ARG), (dict(eta=math.nan), ARG), (dict(N=0), OK), (dict(H=0), OK),
+])
+def test_varlen_validation(L, kw, want):
+    assert varlen(L, **kw) == want
+
+
+def test_varlen_workspace_size_query(L):
+    f = L.osdn_layer_fwd_varlen_workspace_bytes
+    lay = L.osdn_layer_fwd_workspace_bytes
+    up = lambda x: (x + 255) // 256 * 256
+    N, H, Tp = 4, 8, 320                       # max_len 300 rounds up to 320
+    rows = N * Tp
+    pad = 3 * up(rows * H * 128 * 2) + 2 * up(rows * H * 128 * 2) + up(rows * H * 4)
+    assert f(N, 300, H, 128, 128, 64, 1, 0, 0) == up(pad) + lay(N, Tp, H, 128, 128, 64, 1)
+    assert f(N, 300, H, 128, 128, 64, 1, 1, 1) == up(pad + 2 * up(rows * H * 4)) + lay(N, Tp, H, 128, 128, 64, 1)
+    assert f(N, 0, H, 128, 128, 64, 1, 0, 0) > 0   # all empty: one chunk of padding each
+    assert f(0, 300, H, 128, 128, 64, 1, 0, 0) == 0
+    assert f(N, 300, H, 128, 128, 64, 1, 3, 0) == 0
