@@ -348,6 +348,7 @@ def run_ours(args, w):
     vret = None if args.no_vector_retention else run_vector_retention(args, dev, stream, hbm_peak)
     configs = None if args.no_configs else run_configs(args, dev, stream, hbm_peak)
     gated = None if args.no_gated else run_gated(args, dev, stream, hbm_peak)
+    varlen = None if args.no_varlen else run_varlen(args, dev, stream, hbm_peak)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, secs, sample, threads = oracle_layer_rate(w, host, budget_s=args.ref_budget)
@@ -363,7 +364,8 @@ def run_ours(args, w):
                        "chunk": w.chunk, "eta": w.eta, "box": [w.d_min, w.d_max],
                        "l2": "flushed between steps (256 MiB write outside the timed events)"},
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "decode": decode, "other_configs": configs, "gated": gated, "vector_retention": vret,
+            "decode": decode, "other_configs": configs, "gated": gated, "varlen": varlen,
+            "vector_retention": vret,
             "gpu_launches": launches_per_step * n, "clocks": clk.summary(),
             "wall_s_timed_region": wall,
         }
@@ -577,6 +579,56 @@ def run_gated(args, dev, stream, hbm_peak):
             "decode": dec}
 
 
+def run_varlen(args, dev, stream, hbm_peak):
+    """Packed variable-length prefill (cu_seqlens): 16 sequences with lengths uniform in
+    [256, 2048] (seeded), H = 8, K = V = 128, bf16, the 340M layer's key/value recipe, through
+    osdn_layer_fwd_varlen; median of reps with L2 flushed between them.  Reported beside it: the
+    same tokens as a dense batch padded to the longest sequence through osdn_layer_fwd."""
+    import numpy as np
+    from preconditioned_delta_rule_gb300 import binding
+    from preconditioned_delta_rule_gb300 import workloads as W
+
+    w = W.WORKLOADS["layer_340m"]
+    rng = np.random.Generator(np.random.PCG64(11))
+    lengths = rng.integers(256, 2049, size=16)
+    total, N, H = int(lengths.sum()), len(lengths), w.H
+    inp = W.make_prefill(w, B=1, H=H, T=total, seed=11)
+    g = {n: v[0].contiguous().to(dev) for n, v in inp.items() if isinstance(v, torch.Tensor) and v.dim() >= 3}
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device=dev)
+    max_len = int(lengths.max())
+    kw = dict(eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+
+    def med(fn):
+        fn()
+        times = []
+        for i in range(max(3, args.decode_reps)):
+            flush.fill_(float(i))
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record(stream)
+            fn()
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+        binding.osdn_check()
+        return statistics.median(times)
+
+    t_var = med(lambda: binding.osdn_layer_fwd_varlen(g["q"], g["k"], g["v"], g["beta"], cu, max_len=max_len, **kw))
+    Tp = (max_len + 63) // 64 * 64
+    dense = {n: torch.zeros((N, Tp) + tuple(t.shape[1:]), dtype=t.dtype, device=dev) for n, t in g.items()}
+    for n in range(N):
+        for name in dense:
+            dense[name][n, :lengths[n]] = g[name][int(cu[n]):int(cu[n + 1])]
+    t_dense = med(lambda: binding.osdn_layer_fwd(dense["q"], dense["k"], dense["v"], dense["beta"], **kw))
+    wv = W.PrefillWorkload("varlen", B=1, H=H, T=total, K=w.K, V=w.V, dtype=w.dtype)
+    b = layer_bytes(wv)[2] + (N - 1) * H * (w.V * w.K + w.K) * 4
+    return {"workload": "layer_340m_varlen", "sequences": N, "H": H, "tokens": total, "max_len": max_len,
+            "padded_tokens": N * Tp, "ms": t_var * 1e3, "tokens_per_s": total / t_var,
+            "roofline_frac": b / t_var / 1e9 / hbm_peak,
+            "dense_padded_batch_ms": t_dense * 1e3,
+            "note": "osdn_layer_fwd_varlen = scatter into the padded batch + the batched layer + gather"}
+
+
 def run_vector_retention(args, dev, stream, hbm_peak):
     """Phase 1 with one APF gate per key coordinate (diag(r_t), the pages' Appendix A.5) on the
     1.3B-shaped workload (B=4, H=16, T=4096, bf16 keys): the token-by-token scan kernel, gates
@@ -636,6 +688,7 @@ def main():
     ap.add_argument("--no-vector-retention", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other prefill configs")
     ap.add_argument("--no-gated", action="store_true", help="skip the gated variant (OSGDN)")
+    ap.add_argument("--no-varlen", action="store_true", help="skip packed variable-length prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -56,41 +56,44 @@ __device__ __forceinline__ int seq_len(const int* cu, int n, long long total, in
 }
 
 template <typename W>
-__device__ __forceinline__ void copy_row(const unsigned char* src, unsigned char* dst, long long bytes) {
+__device__ __forceinline__ void copy_words(const unsigned char* src, unsigned char* dst, long long bytes, int lane) {
     const W* s = reinterpret_cast<const W*>(src);
     W* d = reinterpret_cast<W*>(dst);
-    for (long long w = threadIdx.x; w < bytes / static_cast<long long>(sizeof(W)); w += blockDim.x) d[w] = s[w];
+    const int n = static_cast<int>(bytes / static_cast<long long>(sizeof(W)));
+    for (int w = lane; w < n; w += 32) d[w] = s[w];
 }
 template <typename W>
-__device__ __forceinline__ void fill_row(unsigned char* dst, long long bytes, uint32_t fill) {
+__device__ __forceinline__ void fill_words(unsigned char* dst, long long bytes, uint32_t fill, int lane) {
     W v;
     uint32_t* p = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
     for (int i = 0; i < static_cast<int>(sizeof(W) / 4); ++i) p[i] = fill;
     W* d = reinterpret_cast<W*>(dst);
-    for (long long w = threadIdx.x; w < bytes / static_cast<long long>(sizeof(W)); w += blockDim.x) d[w] = v;
+    const int n = static_cast<int>(bytes / static_cast<long long>(sizeof(W)));
+    for (int w = lane; w < n; w += 32) d[w] = v;
 }
 
-// One CTA per padded token row (n, t), grid-stride: every tensor's row is copied from the packed
-// layout (t < length of sequence n) or filled with its padding word.
+// One warp per padded row p = (n, t), grid-stride over the rows: every tensor's row is copied from
+// packed row cu[n] + t when t is within sequence n, else filled with its padding word.
 __global__ void __launch_bounds__(kThreads) pack_kernel(PackArgs a) {
+    const int lane = threadIdx.x & 31;
     const long long rows = static_cast<long long>(a.N) * a.Tp;
-    for (long long p = blockIdx.x; p < rows; p += gridDim.x) {
-        const int n = static_cast<int>(p / a.Tp), t = static_cast<int>(p % a.Tp);
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); p < rows; p += warps) {
+        const int n = static_cast<int>(p / a.Tp), t = static_cast<int>(p - static_cast<long long>(n) * a.Tp);
         int start = 0;
         const int len = seq_len(a.cu, n, a.total, a.Tp, start);
-        const bool real = t < len;
         for (int i = 0; i < a.nt; ++i) {
             const PackTensor& x = a.t[i];
             unsigned char* dst = x.padded + p * x.row_bytes;
             const bool v16 = (x.row_bytes & 15) == 0;
-            if (real) {
+            if (t < len) {
                 const unsigned char* src = x.packed + (static_cast<long long>(start) + t) * x.row_bytes;
-                if (v16) copy_row<uint4>(src, dst, x.row_bytes);
-                else copy_row<uint32_t>(src, dst, x.row_bytes);
+                if (v16) copy_words<uint4>(src, dst, x.row_bytes, lane);
+                else copy_words<uint32_t>(src, dst, x.row_bytes, lane);
             } else {
-                if (v16) fill_row<uint4>(dst, x.row_bytes, x.fill);
-                else fill_row<uint32_t>(dst, x.row_bytes, x.fill);
+                if (v16) fill_words<uint4>(dst, x.row_bytes, x.fill, lane);
+                else fill_words<uint32_t>(dst, x.row_bytes, x.fill, lane);
             }
         }
     }
@@ -107,15 +110,18 @@ struct UnpackArgs {
     int HK;
 };
 
-// The real rows of o and k~ back to the packed layout; for a sequence of length 0, d_out = d0.
+// The real rows of o and k~ back to the packed layout (one warp per padded row); for a sequence
+// of length 0, d_out = d0.
 __global__ void __launch_bounds__(kThreads) unpack_kernel(UnpackArgs a) {
+    const int lane = threadIdx.x & 31;
     const long long rows = static_cast<long long>(a.N) * a.Tp;
-    for (long long p = blockIdx.x; p < rows; p += gridDim.x) {
-        const int n = static_cast<int>(p / a.Tp), t = static_cast<int>(p % a.Tp);
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); p < rows; p += warps) {
+        const int n = static_cast<int>(p / a.Tp), t = static_cast<int>(p - static_cast<long long>(n) * a.Tp);
         int start = 0;
         const int len = seq_len(a.cu, n, a.total, a.Tp, start);
         if (t == 0 && len == 0) {
-            for (int e = threadIdx.x; e < a.HK; e += blockDim.x)
+            for (int e = lane; e < a.HK; e += 32)
                 a.d_out[static_cast<long long>(n) * a.HK + e] = a.d0 ? a.d0[static_cast<long long>(n) * a.HK + e] : 1.f;
         }
         if (t >= len) continue;
@@ -123,17 +129,18 @@ __global__ void __launch_bounds__(kThreads) unpack_kernel(UnpackArgs a) {
             const PackTensor& x = a.t[i];
             const unsigned char* src = x.padded + p * x.row_bytes;
             unsigned char* dst = const_cast<unsigned char*>(x.packed) + (static_cast<long long>(start) + t) * x.row_bytes;
-            if ((x.row_bytes & 15) == 0) copy_row<uint4>(src, dst, x.row_bytes);
-            else copy_row<uint32_t>(src, dst, x.row_bytes);
+            if ((x.row_bytes & 15) == 0) copy_words<uint4>(src, dst, x.row_bytes, lane);
+            else copy_words<uint32_t>(src, dst, x.row_bytes, lane);
         }
     }
 }
 
-int grid_for(long long rows) {
+int grid_for(long long rows) {  // one warp per row, grid-stride
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long cap = static_cast<long long>(sms) * 8;
-    return static_cast<int>(rows < cap ? (rows > 0 ? rows : 1) : cap);
+    const long long need = (rows + kThreads / 32 - 1) / (kThreads / 32);
+    return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
 }
 
 }  // namespace
