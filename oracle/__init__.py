@@ -15,6 +15,9 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   alpha (the OSGDN state gate, any of the three phase-2 functions): pinned (alpha = 1 is the
                  ungated rule; eta = 0 is a separately written Gated DeltaNet; the chunk form of
                  Eqs. (13)-(15) equals the recurrence; a zero gate forgets the state)
+  backward.layer_backward (oracle/backward.py, the gradients of the layer forward by reverse-mode
+                 differentiation of a plain fp64 PyTorch token loop): pinned (its forward equals
+                 this library's; every gradient equals central finite differences of it)
 """
 from __future__ import annotations
 

@@ -549,3 +549,75 @@ def test_gated_decode_steps_equal_forward():
         np.testing.assert_allclose(o, full["o"][:, t], rtol=0, atol=1e-13)
     np.testing.assert_allclose(S, full["S"], rtol=0, atol=1e-13)
     np.testing.assert_allclose(d, full["d"], rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------------------------
+# The backward reference (oracle/backward.py): its forward is the C oracle's, and its gradients
+# are central finite differences of the C oracle's forward (independent of autograd).
+# ---------------------------------------------------------------------------------------------
+from oracle import backward as obw  # noqa: E402
+
+
+def bw_problem(seed, T=12, K=4, V=3, H=2, apf=False, gated=False, per_key=False):
+    q, k, v, beta, r = rand_problem(seed, B=1, T=T, H=H, K=K, V=V, apf=apf)
+    g = rng(seed + 100)
+    if apf and per_key:
+        r = g.uniform(0.6, 1.0, size=k.shape)
+    alpha = g.uniform(0.6, 1.0, size=beta.shape) if gated else None
+    d0 = g.uniform(0.7, 1.6, size=(1, H, K))
+    S0 = g.standard_normal((1, H, V, K)) * 0.3
+    return dict(q=q, k=k, v=v, beta=beta, r=r, d0=d0, S0=S0, alpha=alpha)
+
+
+@pytest.mark.parametrize("apf,gated,per_key,beta_aware", [
+    (False, False, False, True), (True, False, False, True), (True, False, True, False), (False, True, False, True)])
+def test_backward_reference_forward_is_the_oracle(apf, gated, per_key, beta_aware):
+    p = bw_problem(81, T=20, K=8, V=5, apf=apf, gated=gated, per_key=per_key)
+    kw = dict(eta=0.3, d_min=0.5, d_max=2.0, eps=1e-6, beta_aware=beta_aware, scale=0.7)
+    ref = oracle.osdn_forward(p["q"], p["k"], p["v"], p["beta"], p["r"], p["d0"], p["S0"], alpha=p["alpha"], **kw)
+    t = {n: obw._t(x) for n, x in p.items()}
+    o, S, d, kt = obw.forward(t["q"], t["k"], t["v"], t["beta"], t["r"], t["d0"], t["S0"], t["alpha"], **kw)
+    np.testing.assert_allclose(o.numpy(), ref["o"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(S.numpy(), ref["S"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(d.numpy(), ref["d"], rtol=1e-14)
+    np.testing.assert_allclose(kt.numpy(), ref["k_tilde"], rtol=1e-14)
+
+
+@pytest.mark.parametrize("apf,gated,per_key,beta_aware", [
+    (False, False, False, True), (True, False, False, False), (True, False, True, True), (False, True, False, True)])
+def test_backward_reference_equals_finite_differences(apf, gated, per_key, beta_aware):
+    """<grad_X L, delta> against (L(X + h delta) - L(X - h delta)) / 2h with the C oracle's forward,
+    for every input X and a random direction delta; the upstream gradients weight o, S_T, d_T, k~."""
+    p = bw_problem(82, T=14, K=5, V=3, apf=apf, gated=gated, per_key=per_key)
+    kw = dict(eta=0.3, d_min=0.5, d_max=2.0, eps=1e-6, beta_aware=beta_aware, scale=0.9)
+    g = rng(83)
+    up = dict(do=g.standard_normal(p["v"].shape), dS=g.standard_normal(p["S0"].shape),
+              dd=g.standard_normal(p["d0"].shape), dkt=g.standard_normal(p["k"].shape))
+
+    def loss(pp):
+        f = oracle.osdn_forward(pp["q"], pp["k"], pp["v"], pp["beta"], pp["r"], pp["d0"], pp["S0"], alpha=pp["alpha"],
+                                **kw)
+        return (np.sum(f["o"] * up["do"]) + np.sum(f["S"] * up["dS"]) + np.sum(f["d"] * up["dd"])
+                + np.sum(f["k_tilde"] * up["dkt"]))
+
+    grads = obw.layer_backward(p["q"], p["k"], p["v"], p["beta"], p["r"], p["d0"], p["S0"], p["alpha"], **up, **kw)
+    h = 1e-6
+    for name in ("q", "k", "v", "beta", "r", "d0", "S0", "alpha"):
+        if p[name] is None:
+            continue
+        delta = g.standard_normal(p[name].shape)
+        plus = dict(p, **{name: p[name] + h * delta})
+        minus = dict(p, **{name: p[name] - h * delta})
+        fd = (loss(plus) - loss(minus)) / (2 * h)
+        an = float(np.sum(grads["d" + name] * delta))
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_backward_reference_clipped_coordinates_pass_no_gradient():
+    """A coordinate that stays clipped at every step: d_T does not depend on d0 there."""
+    p = bw_problem(84, T=10, K=4, V=3)
+    p["d0"][..., 0] = 0.1   # below d_min = 0.5, with eta = 0 the first step clips it to 0.5 for good
+    grads = obw.layer_backward(p["q"], p["k"], p["v"], p["beta"], None, p["d0"], p["S0"],
+                               dd=np.ones_like(p["d0"]), eta=0.0, d_min=0.5, d_max=2.0)
+    assert np.all(grads["dd0"][..., 0] == 0.0)
+    np.testing.assert_allclose(grads["dd0"][..., 1:], 1.0, rtol=0, atol=0)  # eta = 0: d_T = d0 inside the box
