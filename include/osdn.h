@@ -200,6 +200,31 @@ size_t osdn_layer_fwd_varlen_workspace_bytes(int N, int max_len, int H, int K, i
                                              int r_mode, int gated);
 
 /*
+ * The layer backward: gradients of a loss through osdn_layer_fwd's outputs o, S_out and d_out
+ * with respect to q, k, v, beta, r, d0 and S0 (the pages' training path; the reverse sweep of the
+ * projected d recurrence passes no gradient through a clipped coordinate: the clip's derivative
+ * is 1 on [d_min, d_max] and 0 outside).  Inputs as osdn_layer_fwd (alpha must be NULL: the gated
+ * variant's backward is not built, OSDN_ERR_UNSUPPORTED); upstream gradients fp32:
+ *   dout [B,T,H,V] (required), dS [B,H,V,K] and dd [B,H,K] (NULL: zero).
+ * Outputs fp32 (written): dq, dk [B,T,H,K], dv [B,T,H,V], dbeta [B,T,H], dr (the layout of r;
+ * required when r is given), dd0 [B,H,K] and dS0 [B,H,V,K] (NULL: not written).
+ *   workspace  required, at least osdn_layer_bwd_workspace_bytes(...) bytes (fp32 write keys,
+ *              their gradient, the state at every 64-token chunk start and d at every block
+ *              start).
+ * The sweeps are token-recurrent fp32 on the CUDA cores (S checkpointed per chunk and rebuilt
+ * backward within it): exact to fp32 rounding, not fast.
+ */
+osdn_status osdn_layer_bwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
+                           const float* r, int r_per_key, const float* alpha, const float* d0, const float* S0,
+                           const float* dout, const float* dS, const float* dd, float* dq, float* dk, float* dv,
+                           float* dbeta, float* dr, float* dd0, float* dS0, int B, int T, int H, int K, int V,
+                           float eta, float d_min, float d_max, float eps, float scale, int beta_aware,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace size for osdn_layer_bwd (0 for unsupported head sizes or empty problems). */
+size_t osdn_layer_bwd_workspace_bytes(int B, int T, int H, int K, int V);
+
+/*
  * osdn_chunk_fwd for callers that cannot allocate device memory when they call -- for example an
  * engine that reserves all GPU memory in one plan at start-up and allocates nothing afterwards,
  * or code that cannot accept an allocator call (its latency, its implicit synchronisation, its

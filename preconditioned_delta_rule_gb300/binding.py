@@ -63,6 +63,11 @@ def lib() -> ctypes.CDLL:
     L.osdn_layer_fwd_varlen.restype = ctypes.c_int
     L.osdn_layer_fwd_varlen_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i]
     L.osdn_layer_fwd_varlen_workspace_bytes.restype = sz
+    L.osdn_layer_bwd.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
+                                 i, i, i, i, i, f, f, f, f, f, i, vp, sz, vp]
+    L.osdn_layer_bwd.restype = ctypes.c_int
+    L.osdn_layer_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
+    L.osdn_layer_bwd_workspace_bytes.restype = sz
     L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
     L.osdn_check.argtypes = [vp]
     for fn in ("osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step", "osdn_check"):
@@ -368,6 +373,45 @@ def osdn_layer_fwd_varlen(q, k, v, beta, cu_seqlens, *, max_len=None, r=None, al
     if squeeze:
         return o[None], S_out, d_out, k_tilde[None]
     return o, S_out, d_out, k_tilde
+
+
+def osdn_layer_bwd_workspace_bytes(B, T, H, K, V) -> int:
+    return int(lib().osdn_layer_bwd_workspace_bytes(B, T, H, K, V))
+
+
+def osdn_layer_bwd(q, k, v, beta, do, r=None, d0=None, S0=None, *, dS=None, dd=None, eta=0.003, d_min=0.5,
+                   d_max=2.0, eps=1e-6, scale=1.0, beta_aware=True, workspace=None, stream=None):
+    """Gradients of a loss through osdn_layer_fwd's o, S_out and d_out: ``do`` [B,T,H,V] and the
+    optional ``dS`` [B,H,V,K], ``dd`` [B,H,K] (fp32) are the loss's gradients with respect to them.
+    Returns a dict of fp32 tensors dq, dk, dv, dbeta, dr (None without r), dd0, dS0."""
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    dev, dt = k.device, k.dtype
+    for name, t, shp in (("q", q, (B, T, H, K)), ("k", k, (B, T, H, K)), ("v", v, (B, T, H, V))):
+        _check(name, t, shp, dt, dev)
+    _check("beta", beta, (B, T, H), torch.float32, dev)
+    r_per_key = _retention(r, (B, T, H), K, dev)
+    _check("d0", d0, (B, H, K), torch.float32, dev)
+    _check("S0", S0, (B, H, V, K), torch.float32, dev)
+    _check("do", do, (B, T, H, V), torch.float32, dev)
+    _check("dS", dS, (B, H, V, K), torch.float32, dev)
+    _check("dd", dd, (B, H, K), torch.float32, dev)
+    f32 = dict(device=dev, dtype=torch.float32)
+    g = {"dq": torch.empty((B, T, H, K), **f32), "dk": torch.empty((B, T, H, K), **f32),
+         "dv": torch.empty((B, T, H, V), **f32), "dbeta": torch.empty((B, T, H), **f32),
+         "dr": None if r is None else torch.empty(tuple(r.shape), **f32),
+         "dd0": torch.empty((B, H, K), **f32), "dS0": torch.empty((B, H, V, K), **f32)}
+    need = osdn_layer_bwd_workspace_bytes(B, T, H, K, V)
+    if workspace is False:
+        raise ValueError("osdn_layer_bwd needs a workspace")
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "bwd")
+    st = lib().osdn_layer_bwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, None, _ptr(d0),
+                              _ptr(S0), _ptr(do), _ptr(dS), _ptr(dd), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                              _ptr(g["dbeta"]), _ptr(g["dr"]), _ptr(g["dd0"]), _ptr(g["dS0"]), B, T, H, K, V,
+                              float(eta), float(d_min), float(d_max), float(eps), float(scale),
+                              int(bool(beta_aware)), ws_ptr, ws_bytes, _stream(dev, stream))
+    _raise("osdn_layer_bwd", st)
+    return g
 
 
 def chunk_osdn(q, k, v, beta, precond_retention=None, initial_state=None, initial_d=None, *,

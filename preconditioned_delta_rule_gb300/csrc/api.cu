@@ -282,6 +282,60 @@ osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, o
     return from_cuda(osdn_launch_varlen_unpack(io, vs, s));
 }
 
+size_t osdn_layer_bwd_workspace_bytes(int B, int T, int H, int K, int V) {
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return 0;
+    return osdn_bwd_workspace_bytes(B, T, H, K, V);
+}
+
+osdn_status osdn_layer_bwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
+                           const float* r, int r_per_key, const float* alpha, const float* d0, const float* S0,
+                           const float* dout, const float* dS, const float* dd, float* dq, float* dk, float* dv,
+                           float* dbeta, float* dr, float* dd0, float* dS0, int B, int T, int H, int K, int V,
+                           float eta, float d_min, float d_max, float eps, float scale, int beta_aware,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || T < 0 || H < 0) return OSDN_ERR_SHAPE;
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return (K > 0 && V > 0) ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
+    if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
+    OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
+    if (!isfinite(scale)) return OSDN_ERR_ARG;
+    if (r_per_key != 0 && r_per_key != 1) return OSDN_ERR_ARG;
+    if (alpha) return OSDN_ERR_UNSUPPORTED;  // the gated variant's backward is not built
+    if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
+    if (B == 0 || H == 0 || T == 0) {
+        // nothing flows through the tokens: the initial states' gradients are the final ones'
+        const size_t ns = static_cast<size_t>(B) * H * V * K, nd = static_cast<size_t>(B) * H * K;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if (B == 0 || H == 0) return OSDN_OK;
+        if (dS0 && (dS ? cudaMemcpyAsync(dS0, dS, ns * 4, cudaMemcpyDeviceToDevice, s)
+                       : cudaMemsetAsync(dS0, 0, ns * 4, s)) != cudaSuccess) return OSDN_ERR_CUDA;
+        if (dd0 && (dd ? cudaMemcpyAsync(dd0, dd, nd * 4, cudaMemcpyDeviceToDevice, s)
+                       : cudaMemsetAsync(dd0, 0, nd * 4, s)) != cudaSuccess) return OSDN_ERR_CUDA;
+        return OSDN_OK;
+    }
+    OSDN_TRY(ptr(q, true));
+    OSDN_TRY(ptr(k, true));
+    OSDN_TRY(ptr(v, true));
+    OSDN_TRY(ptr(beta, true));
+    OSDN_TRY(ptr(dout, true));
+    OSDN_TRY(ptr(dq, true));
+    OSDN_TRY(ptr(dk, true));
+    OSDN_TRY(ptr(dv, true));
+    OSDN_TRY(ptr(dbeta, true));
+    OSDN_TRY(ptr(r, false));
+    OSDN_TRY(ptr(dr, r != nullptr));
+    OSDN_TRY(ptr(d0, false));
+    OSDN_TRY(ptr(S0, false));
+    OSDN_TRY(ptr(dS, false));
+    OSDN_TRY(ptr(dd, false));
+    OSDN_TRY(ptr(dd0, false));
+    OSDN_TRY(ptr(dS0, false));
+    OSDN_TRY(ptr(workspace, true));
+    if (workspace_bytes < osdn_bwd_workspace_bytes(B, T, H, K, V)) return OSDN_ERR_ARG;
+    OsdnBwdArgs a{q, k, v, dtype, beta, r, r ? r_per_key : 0, d0, S0, dout, dS, dd, dq, dk, dv, dbeta, dr, dd0, dS0,
+                  B, T, H, K, V, eta, d_min, d_max, eps, scale, beta_aware ? 1 : 0};
+    return from_cuda(osdn_launch_bwd(a, workspace, static_cast<cudaStream_t>(stream)));
+}
+
 osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,
                              const float* beta, const float* r, int r_per_key, const float* alpha, float* S,
                              float* d, void* o,

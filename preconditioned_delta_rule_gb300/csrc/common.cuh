@@ -146,6 +146,18 @@ size_t osdn_varlen_pad_bytes(const OsdnVarlenShape& v);
 cudaError_t osdn_launch_varlen_pack(const OsdnVarlenIo& io, const OsdnVarlenShape& v, cudaStream_t s);
 cudaError_t osdn_launch_varlen_unpack(const OsdnVarlenIo& io, const OsdnVarlenShape& v, cudaStream_t s);
 cudaError_t osdn_varlen_read_and_clear_flag(unsigned int* flag);
+// Layer backward (token-recurrent fp32 reverse sweeps of both phases).
+struct OsdnBwdArgs {
+    const void* q; const void* k; const void* v; osdn_dtype dtype;
+    const float* beta; const float* r; int r_per_key; const float* d0; const float* S0;
+    const float* dout;  // [B,T,H,V] fp32
+    const float* dS;    // [B,H,V,K] fp32 or null
+    const float* dd;    // [B,H,K] fp32 or null
+    float* dq; float* dk; float* dv; float* dbeta; float* dr; float* dd0; float* dS0;
+    int B, T, H, K, V; float eta, d_min, d_max, eps, scale; int beta_aware;
+};
+size_t osdn_bwd_workspace_bytes(int B, int T, int H, int K, int V);
+cudaError_t osdn_launch_bwd(const OsdnBwdArgs& a, void* ws, cudaStream_t s);
 // Fused layer forward (phase 1 + chunk prep in one cooperative launch, then the chain kernel).
 cudaError_t osdn_launch_layer(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, void* ws, size_t ws_bytes,
                               cudaStream_t s);
