@@ -349,6 +349,7 @@ def run_ours(args, w):
     configs = None if args.no_configs else run_configs(args, dev, stream, hbm_peak)
     gated = None if args.no_gated else run_gated(args, dev, stream, hbm_peak)
     varlen = None if args.no_varlen else run_varlen(args, dev, stream, hbm_peak)
+    backward = None if args.no_backward else run_backward(args, dev, stream, hbm_peak)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, secs, sample, threads = oracle_layer_rate(w, host, budget_s=args.ref_budget)
@@ -364,7 +365,7 @@ def run_ours(args, w):
                        "chunk": w.chunk, "eta": w.eta, "box": [w.d_min, w.d_max],
                        "l2": "flushed between steps (256 MiB write outside the timed events)"},
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "decode": decode, "other_configs": configs, "gated": gated, "varlen": varlen,
+            "decode": decode, "other_configs": configs, "gated": gated, "varlen": varlen, "backward": backward,
             "vector_retention": vret,
             "gpu_launches": launches_per_step * n, "clocks": clk.summary(),
             "wall_s_timed_region": wall,
@@ -629,6 +630,48 @@ def run_varlen(args, dev, stream, hbm_peak):
             "note": "osdn_layer_fwd_varlen = scatter into the padded batch + the batched layer + gather"}
 
 
+def run_backward(args, dev, stream, hbm_peak):
+    """The layer backward (osdn_layer_bwd) on the 340M-shaped layer (B=8, H=8, T=2048, bf16): the
+    loss's gradients with respect to o (fp32, N(0, 1)), S_out and d_out given; median of reps with
+    L2 flushed between them.  Algorithmic bytes: q, k, v, beta and do read once, dq, dk, dv
+    (fp32) and dbeta written once, the per-head states and their gradients."""
+    from preconditioned_delta_rule_gb300 import binding
+    from preconditioned_delta_rule_gb300 import workloads as W
+
+    w = W.WORKLOADS["layer_340m"]
+    g = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in W.make_prefill(w).items()}
+    gen = torch.Generator().manual_seed(9)
+    do = torch.randn(w.B, w.T, w.H, w.V, generator=gen).to(dev)
+    dS = (0.1 * torch.randn(w.B, w.H, w.V, w.K, generator=gen)).to(dev)
+    dd = torch.randn(w.B, w.H, w.K, generator=gen).to(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    kw = dict(eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+
+    def call():
+        binding.osdn_layer_bwd(g["q"], g["k"], g["v"], g["beta"], do, dS=dS, dd=dd, **kw)
+
+    call()
+    times = []
+    for i in range(3):
+        flush.fill_(float(i))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        call()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        times.append(ev[0].elapsed_time(ev[1]) / 1e3)
+    binding.osdn_check()
+    secs = statistics.median(times)
+    th = w.B * w.T * w.H
+    b = th * (3 * w.K * 2 + 4 + 4 * w.V + 4 * (2 * w.K + w.V) + 4) + w.B * w.H * 4 * 3 * (w.V * w.K + w.K)
+    ach = b / secs / 1e9
+    return {"workload": w.name + "_backward", "B": w.B, "H": w.H, "T": w.T, "ms": secs * 1e3,
+            "tokens_per_s": w.B * w.T / secs,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                         "algorithmic_bytes_per_launch": b},
+            "kernels": "scan (write keys, fp32) + bwd_phase2_kernel + bwd_phase1_kernel, token-recurrent fp32"}
+
+
 def run_vector_retention(args, dev, stream, hbm_peak):
     """Phase 1 with one APF gate per key coordinate (diag(r_t), the pages' Appendix A.5) on the
     1.3B-shaped workload (B=4, H=16, T=4096, bf16 keys): the token-by-token scan kernel, gates
@@ -689,6 +732,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the other prefill configs")
     ap.add_argument("--no-gated", action="store_true", help="skip the gated variant (OSGDN)")
     ap.add_argument("--no-varlen", action="store_true", help="skip packed variable-length prefill")
+    ap.add_argument("--no-backward", action="store_true", help="skip the layer backward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

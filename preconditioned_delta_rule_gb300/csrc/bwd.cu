@@ -237,16 +237,31 @@ __global__ void __launch_bounds__(32) bwd_phase1_kernel(OsdnBwdArgs a, const flo
 #pragma unroll
     for (int i = 0; i < E; ++i) d[i] = a.d0 ? a.d0[static_cast<size_t>(bh) * K + lane * E + i] : 1.f;
 
-    struct Step {
-        float s[E], g, n, bb, a_, r[E];
+    // a token's operands (key, gate inputs, and in the reverse sweep dL/dk~), loaded a token ahead
+    struct In {
+        float kv[E], bb, r[E], dkt[E];
     };
-    // the forward step's quantities at token t from d_t
-    auto step_of = [&](int t, const float (&dt)[E], const float (&kv)[E], Step& st) {
+    auto load_in = [&](int t, In& f, bool with_dkt) {
         const size_t r = row0 + static_cast<size_t>(t) * H;
+        VecIO<TIn, E>::load(kg + r * K + lane * E, f.kv);
+        f.bb = a.beta_aware ? a.beta[r] : 1.f;
+        if (RMODE == 2) {
+            VecIO<float, E>::load(a.r + r * K + lane * E, f.r);
+        } else {
+#pragma unroll
+            for (int i = 0; i < E; ++i) f.r[i] = RMODE == 1 ? a.r[r] : 1.f;
+        }
+        if (with_dkt) VecIO<float, E>::load(dkt + r * K + lane * E, f.dkt);
+    };
+    struct Step {
+        float s[E], g, n, a_;
+    };
+    // the forward step's quantities at a token from d_t
+    auto step_of = [&](const float (&dt)[E], const In& f, Step& st) {
         float n = 0.f, al = 0.f;
 #pragma unroll
         for (int i = 0; i < E; ++i) {
-            st.s[i] = kv[i] * kv[i];
+            st.s[i] = f.kv[i] * f.kv[i];
             n += st.s[i];
             al = fmaf(dt[i], st.s[i], al);
         }
@@ -254,26 +269,23 @@ __global__ void __launch_bounds__(32) bwd_phase1_kernel(OsdnBwdArgs a, const flo
         al = warp_sum(al);
         st.n = n;
         st.a_ = al;
-        st.bb = a.beta_aware ? a.beta[r] : 1.f;
-        st.g = a.eta * st.bb * (1.f - st.bb * al) / fmaxf(n, a.eps);
-        if (RMODE == 2) {
-            VecIO<float, E>::load(a.r + r * K + lane * E, st.r);
-        } else {
-#pragma unroll
-            for (int i = 0; i < E; ++i) st.r[i] = RMODE == 1 ? a.r[r] : 1.f;
-        }
+        st.g = a.eta * f.bb * (1.f - f.bb * al) / fmaxf(n, a.eps);
     };
-    for (int c = 0; c < nch; ++c) {
+    {
+        In nx;
+        if (T > 0) load_in(0, nx, false);
+        for (int c = 0; c < nch; ++c) {
 #pragma unroll
-        for (int i = 0; i < E; ++i) ck[static_cast<size_t>(c) * K + lane * E + i] = d[i];
-        const int t1 = min(T, (c + 1) * kChunk);
-        for (int t = c * kChunk; t < t1; ++t) {
-            float kv[E];
-            VecIO<TIn, E>::load(kg + (row0 + static_cast<size_t>(t) * H) * K + lane * E, kv);
-            Step st;
-            step_of(t, d, kv, st);
+            for (int i = 0; i < E; ++i) ck[static_cast<size_t>(c) * K + lane * E + i] = d[i];
+            const int t1 = min(T, (c + 1) * kChunk);
+            for (int t = c * kChunk; t < t1; ++t) {
+                const In cur = nx;
+                if (t + 1 < T) load_in(t + 1, nx, false);
+                Step st;
+                step_of(d, cur, st);
 #pragma unroll
-            for (int i = 0; i < E; ++i) d[i] = fminf(fmaxf(fmaf(st.g, st.s[i], st.r[i] * d[i]), a.d_min), a.d_max);
+                for (int i = 0; i < E; ++i) d[i] = fminf(fmaxf(fmaf(st.g, st.s[i], cur.r[i] * d[i]), a.d_min), a.d_max);
+            }
         }
     }
     float e[E];  // dL/dd_{t+1}
@@ -283,32 +295,40 @@ __global__ void __launch_bounds__(32) bwd_phase1_kernel(OsdnBwdArgs a, const flo
         const int t0 = c * kChunk, t1 = min(T, t0 + kChunk);
 #pragma unroll
         for (int i = 0; i < E; ++i) d[i] = ck[static_cast<size_t>(c) * K + lane * E + i];
-        for (int t = t0; t < t1; ++t) {
+        {
+            In nx;
+            load_in(t0, nx, false);
+            for (int t = t0; t < t1; ++t) {
 #pragma unroll
-            for (int i = 0; i < E; ++i) sd[t - t0][lane * E + i] = d[i];
-            float kv[E];
-            VecIO<TIn, E>::load(kg + (row0 + static_cast<size_t>(t) * H) * K + lane * E, kv);
-            Step st;
-            step_of(t, d, kv, st);
+                for (int i = 0; i < E; ++i) sd[t - t0][lane * E + i] = d[i];
+                const In cur = nx;
+                if (t + 1 < t1) load_in(t + 1, nx, false);
+                Step st;
+                step_of(d, cur, st);
 #pragma unroll
-            for (int i = 0; i < E; ++i) d[i] = fminf(fmaxf(fmaf(st.g, st.s[i], st.r[i] * d[i]), a.d_min), a.d_max);
+                for (int i = 0; i < E; ++i) d[i] = fminf(fmaxf(fmaf(st.g, st.s[i], cur.r[i] * d[i]), a.d_min), a.d_max);
+            }
         }
         __syncwarp();
+        In bnx;
+        load_in(t1 - 1, bnx, true);
         for (int t = t1 - 1; t >= t0; --t) {
             const size_t r = row0 + static_cast<size_t>(t) * H;
-            float dt[E], kv[E], dktv[E];
+            const In cur = bnx;
+            if (t - 1 >= t0) load_in(t - 1, bnx, true);
+            float dt[E];
 #pragma unroll
             for (int i = 0; i < E; ++i) dt[i] = sd[t - t0][lane * E + i];
-            VecIO<TIn, E>::load(kg + r * K + lane * E, kv);
-            VecIO<float, E>::load(dkt + r * K + lane * E, dktv);
+            const float(&kv)[E] = cur.kv;
+            const float(&dktv)[E] = cur.dkt;
             Step st;
-            step_of(t, dt, kv, st);
+            step_of(dt, cur, st);
             float dd[E], ds[E], dg = 0.f, dr = 0.f;
 #pragma unroll
             for (int i = 0; i < E; ++i) {
-                const float x = fmaf(st.g, st.s[i], st.r[i] * dt[i]);
+                const float x = fmaf(st.g, st.s[i], cur.r[i] * dt[i]);
                 const float ex = (x >= a.d_min && x <= a.d_max) ? e[i] : 0.f;
-                dd[i] = st.r[i] * ex + dktv[i] * kv[i];
+                dd[i] = cur.r[i] * ex + dktv[i] * kv[i];
                 dg = fmaf(ex, st.s[i], dg);
                 ds[i] = st.g * ex;
                 if (RMODE == 2) a.dr[r * K + lane * E + i] = ex * dt[i];
@@ -320,8 +340,8 @@ __global__ void __launch_bounds__(32) bwd_phase1_kernel(OsdnBwdArgs a, const flo
                 if (lane == 0) a.dr[r] = dr;
             }
             const float nb = fmaxf(st.n, a.eps), cc = a.eta / nb;
-            const float da = -cc * st.bb * st.bb * dg;
-            const float db = cc * (1.f - 2.f * st.bb * st.a_) * dg;
+            const float da = -cc * cur.bb * cur.bb * dg;
+            const float db = cc * (1.f - 2.f * cur.bb * st.a_) * dg;
             const float dn = st.n > a.eps ? -(st.g / nb) * dg : 0.f;
             float dkl[E];
 #pragma unroll
@@ -331,10 +351,11 @@ __global__ void __launch_bounds__(32) bwd_phase1_kernel(OsdnBwdArgs a, const flo
                 dkl[i] = 2.f * kv[i] * ds[i] + dktv[i] * dt[i];
                 e[i] = dd[i];
             }
+            // added without reading back (no stall on the load; nothing else writes these words now)
             float* dkp = a.dk + r * K + lane * E;
 #pragma unroll
-            for (int i = 0; i < E; ++i) dkp[i] += dkl[i];
-            if (a.beta_aware && lane == 0) a.dbeta[r] += db;
+            for (int i = 0; i < E; ++i) atomicAdd(dkp + i, dkl[i]);
+            if (a.beta_aware && lane == 0) atomicAdd(a.dbeta + r, db);
         }
         __syncwarp();
     }
