@@ -12,6 +12,8 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   delta_phase2   pinned (textbook DeltaNet at d = 1, residual identity, chunk-form identity)
   osdn_forward   pinned (decoupling into the two phases, continuation, Cor. D.8 identity)
   decode_step    pinned (equals the forward on one token; decode x T equals forward on T)
+  alpha [B,T,H,K] (one state gate per key channel, OSKDA): pinned (a textbook KDA recurrence in
+                 its own K x V convention at eta = 0; equal channel gates reproduce the head gate)
   alpha (the OSGDN state gate, any of the three phase-2 functions): pinned (alpha = 1 is the
                  ungated rule; eta = 0 is a separately written Gated DeltaNet; the chunk form of
                  Eqs. (13)-(15) equals the recurrence; a zero gate forgets the state)
@@ -60,9 +62,9 @@ def _load():
         lib = ctypes.CDLL(str(path))
         i, d = ctypes.c_int, ctypes.c_double
         lib.oracle_precond_scan.argtypes = [_dp] * 3 + [i] + [_dp] * 4 + [i] * 4 + [d] * 4 + [i, i]
-        lib.oracle_delta_phase2.argtypes = [_dp] * 9 + [i] * 5 + [d, i]
-        lib.oracle_osdn_forward.argtypes = [_dp] * 5 + [i] + [_dp] * 9 + [i] * 5 + [d] * 4 + [i, d, i]
-        lib.oracle_decode_step.argtypes = [_dp] * 5 + [i] + [_dp] * 4 + [i] * 4 + [d] * 4 + [i, d, i]
+        lib.oracle_delta_phase2.argtypes = [_dp] * 6 + [i] + [_dp] * 3 + [i] * 5 + [d, i]
+        lib.oracle_osdn_forward.argtypes = [_dp] * 5 + [i, _dp, i] + [_dp] * 8 + [i] * 5 + [d] * 4 + [i, d, i]
+        lib.oracle_decode_step.argtypes = [_dp] * 5 + [i, _dp, i] + [_dp] * 3 + [i] * 4 + [d] * 4 + [i, d, i]
         for f in ("oracle_precond_scan", "oracle_delta_phase2", "oracle_osdn_forward",
                   "oracle_decode_step"):
             getattr(lib, f).restype = ctypes.c_int
@@ -124,7 +126,8 @@ def delta_phase2(q, k, k_tilde, v, beta, S0=None, *, alpha=None, scale=1.0, thre
     V = v.shape[-1]
     o = np.empty((B, T, H, V))
     S = np.empty((B, H, V, K))
-    rc = _load().oracle_delta_phase2(_p(q), _p(k), _p(kt), _p(v), _p(beta), _p(alpha), _p(S0), _p(o), _p(S),
+    rc = _load().oracle_delta_phase2(_p(q), _p(k), _p(kt), _p(v), _p(beta), _p(alpha), _per_key(alpha, k), _p(S0),
+                                     _p(o), _p(S),
                                      B, T, H, K, V, scale, threads)
     if rc:
         raise ValueError("oracle_delta_phase2: bad arguments")
@@ -144,7 +147,8 @@ def osdn_forward(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, eta=0.0
     kt = np.empty((B, T, H, K))
     a = np.empty((B, T, H))
     u2 = np.empty((B, T, H))
-    rc = _load().oracle_osdn_forward(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(alpha), _p(d0),
+    rc = _load().oracle_osdn_forward(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(alpha),
+                                     _per_key(alpha, k), _p(d0),
                                      _p(S0), _p(o),
                                      _p(S), _p(d), _p(kt), _p(a), _p(u2), B, T, H, K, V, eta,
                                      d_min, d_max, eps, int(beta_aware), scale, threads)
@@ -163,7 +167,8 @@ def decode_step(q, k, v, beta, S, d, r=None, *, alpha=None, eta=0.003, d_min=0.5
     B, H, K = k.shape
     V = v.shape[-1]
     o = np.empty((B, H, V))
-    rc = _load().oracle_decode_step(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(alpha), _p(S), _p(d),
+    rc = _load().oracle_decode_step(_p(q), _p(k), _p(v), _p(beta), _p(r), _per_key(r, k), _p(alpha),
+                                    _per_key(alpha, k), _p(S), _p(d),
                                     _p(o),
                                     B, H, K, V, eta, d_min, d_max, eps, int(beta_aware), scale,
                                     threads)

@@ -59,8 +59,8 @@ def forward(q, k, v, beta, r=None, d0=None, S0=None, alpha=None, *, eta=0.003, d
         else:
             rd = (r[:, t] if per_key else r[:, t][..., None]) * d
         d = torch.clamp(rd + g[..., None] * s, min=d_min, max=d_max)
-        if alpha is not None:
-            S = alpha[:, t][..., None, None] * S
+        if alpha is not None:  # one gate per head (Appendix B.1) or per key channel (B.2)
+            S = (alpha[:, t][..., None, :] if alpha.dim() == 4 else alpha[:, t][..., None, None]) * S
         u = v[:, t] - torch.einsum("bhvk,bhk->bhv", S, kk)
         S = S + beta[:, t][..., None, None] * u[..., :, None] * kt[..., None, :]
         outs.append(scale * torch.einsum("bhvk,bhk->bhv", S, q[:, t]))

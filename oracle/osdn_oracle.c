@@ -23,6 +23,10 @@
  *     state gate alpha_t in the post-gate residual form, Sbar = alpha_t S_{t-1},
  *     e_t = v_t - Sbar k_t, S_t = Sbar + beta_t e_t k~_t^T (phase 1 unchanged, Eq. (12)).
  *     alpha = NULL is the ungated rule (alpha = 1).
+ *   - Kimi Delta Attention with online scaling (OSKDA), Appendix B.2: one state gate per key
+ *     channel, Sbar = Diag(alpha_t) S_{t-1} in KDA's K x V convention; the state here is stored
+ *     V x K (its transpose), so the gate scales column i of S by alpha_{t,i} (alpha_per_key = 1:
+ *     alpha has the layout of k).  The write key k~ and the read key k keep their roles.
  *
  * Everything is a per-(batch, head) loop over tokens.  OpenMP runs independent heads in
  * parallel; within a head the arithmetic follows the definition above in order, in double.
@@ -74,14 +78,16 @@ static double phase1_step(double *d, const double *k, double *kt_out, int K, dou
 }
 
 /* One phase-2 step on S (V x K): S <- alpha S (the state gate, Appendix B.1; alpha = 1 without
- * it), then u = v - S k; S += beta u kt^T; o = scale * S q.  Returns |u|^2 for diagnostics. */
+ * it), or column i of S times alpha[i] with a gate per key channel (Appendix B.2), then
+ * u = v - S k; S += beta u kt^T; o = scale * S q.  alpha may be NULL.  Returns |u|^2. */
 static double phase2_step(double *S, const double *q, const double *k, const double *kt,
-                          const double *v, double beta, double alpha, double *o, int K, int V,
-                          double scale, double *u /* scratch, length V */)
+                          const double *v, double beta, const double *alpha, int alpha_per_key,
+                          double *o, int K, int V, double scale, double *u /* scratch, length V */)
 {
     double u2 = 0.0;
-    if (alpha != 1.0)
-        for (size_t e = 0; e < (size_t)V * K; ++e) S[e] *= alpha;
+    if (alpha)
+        for (int a = 0; a < V; ++a)
+            for (int i = 0; i < K; ++i) S[(size_t)a * K + i] *= alpha[alpha_per_key ? i : 0];
     for (int a = 0; a < V; ++a) {
         double sk = 0.0;
         for (int i = 0; i < K; ++i) sk += S[(size_t)a * K + i] * k[i];
@@ -145,7 +151,7 @@ int oracle_precond_scan(const double *k, const double *beta, const double *r, in
  * by alpha when it is given (Appendix B.1).  o [B,T,H,V] and S_out [B,H,V,K] are written; S0 and
  * alpha may be NULL (zeros, no gate). */
 int oracle_delta_phase2(const double *q, const double *k, const double *k_tilde, const double *v,
-                        const double *beta, const double *alpha, const double *S0, double *o,
+                        const double *beta, const double *alpha, int alpha_per_key, const double *S0, double *o,
                         double *S_out, int B,
                         int T, int H, int K, int V, double scale, int nthreads)
 {
@@ -163,8 +169,9 @@ int oracle_delta_phase2(const double *q, const double *k, const double *k_tilde,
         for (long t = 0; t < T; ++t) {
             size_t kk = ix4(b, t, h, 0, T, H, K), vv = ix4(b, t, h, 0, T, H, V);
             size_t gg = ix4(b, t, h, 0, T, H, 1);
-            phase2_step(S, q + kk, k + kk, k_tilde + kk, v + vv, beta[gg], alpha ? alpha[gg] : 1.0,
-                        o + vv, K, V, scale, u);
+            phase2_step(S, q + kk, k + kk, k_tilde + kk, v + vv, beta[gg],
+                        alpha ? alpha + (alpha_per_key ? kk : gg) : NULL, alpha_per_key, o + vv, K, V,
+                        scale, u);
         }
         memcpy(S_out + (size_t)bh * sz, S, sizeof(double) * sz);
         free(u);
@@ -177,8 +184,8 @@ int oracle_delta_phase2(const double *q, const double *k, const double *k_tilde,
  * emit k~_t with d_t, step d, read u_t with the ORIGINAL k_t, write with k~_t, read out o_t.
  * Optional diagnostics: a_out [B,T,H] = beta_t <d_t, k_t^2>, u2_out [B,T,H] = |u_t|^2. */
 int oracle_osdn_forward(const double *q, const double *k, const double *v, const double *beta,
-                        const double *r, int r_per_key, const double *alpha, const double *d0,
-                        const double *S0, double *o,
+                        const double *r, int r_per_key, const double *alpha, int alpha_per_key,
+                        const double *d0, const double *S0, double *o,
                         double *S_out, double *d_out, double *k_tilde, double *a_out,
                         double *u2_out, int B, int T, int H, int K, int V, double eta,
                         double dmin, double dmax, double eps, int beta_aware, double scale,
@@ -204,7 +211,8 @@ int oracle_osdn_forward(const double *q, const double *k, const double *v, const
             double a = phase1_step(d, k + kk, kt, K, beta[gg], r ? r + (r_per_key ? kk : gg) : NULL,
                                    r_per_key, eta, dmin, dmax, eps, beta_aware);
             if (k_tilde) memcpy(k_tilde + kk, kt, sizeof(double) * K);
-            double u2 = phase2_step(S, q + kk, k + kk, kt, v + vv, beta[gg], alpha ? alpha[gg] : 1.0,
+            double u2 = phase2_step(S, q + kk, k + kk, kt, v + vv, beta[gg],
+                                    alpha ? alpha + (alpha_per_key ? kk : gg) : NULL, alpha_per_key,
                                     o + vv, K, V, scale, u);
             if (a_out) a_out[gg] = a;
             if (u2_out) u2_out[gg] = u2;
@@ -223,7 +231,8 @@ int oracle_osdn_forward(const double *q, const double *k, const double *v, const
  * single token.  q, k [B,H,K]; v, o [B,H,V]; beta, r, alpha [B,H] (r [B,H,K] with r_per_key; r
  * and alpha may be NULL). */
 int oracle_decode_step(const double *q, const double *k, const double *v, const double *beta,
-                       const double *r, int r_per_key, const double *alpha, double *S, double *d,
+                       const double *r, int r_per_key, const double *alpha, int alpha_per_key, double *S,
+                       double *d,
                        double *o, int B, int H, int K,
                        int V, double eta, double dmin, double dmax, double eps, int beta_aware,
                        double scale, int nthreads)
@@ -240,8 +249,9 @@ int oracle_decode_step(const double *q, const double *k, const double *v, const 
                     r ? r + (r_per_key ? (size_t)bh * K : (size_t)bh) : NULL, r_per_key, eta, dmin,
                     dmax, eps, beta_aware);
         phase2_step(S + (size_t)bh * sz, q + (size_t)bh * K, k + (size_t)bh * K, kt,
-                    v + (size_t)bh * V, beta[bh], alpha ? alpha[bh] : 1.0, o + (size_t)bh * V, K, V,
-                    scale, u);
+                    v + (size_t)bh * V, beta[bh],
+                    alpha ? alpha + (alpha_per_key ? (size_t)bh * K : (size_t)bh) : NULL, alpha_per_key,
+                    o + (size_t)bh * V, K, V, scale, u);
         free(u);
         free(kt);
     }

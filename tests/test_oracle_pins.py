@@ -563,14 +563,15 @@ def bw_problem(seed, T=12, K=4, V=3, H=2, apf=False, gated=False, per_key=False)
     g = rng(seed + 100)
     if apf and per_key:
         r = g.uniform(0.6, 1.0, size=k.shape)
-    alpha = g.uniform(0.6, 1.0, size=beta.shape) if gated else None
+    alpha = g.uniform(0.6, 1.0, size=(k.shape if gated == "key" else beta.shape)) if gated else None
     d0 = g.uniform(0.7, 1.6, size=(1, H, K))
     S0 = g.standard_normal((1, H, V, K)) * 0.3
     return dict(q=q, k=k, v=v, beta=beta, r=r, d0=d0, S0=S0, alpha=alpha)
 
 
 @pytest.mark.parametrize("apf,gated,per_key,beta_aware", [
-    (False, False, False, True), (True, False, False, True), (True, False, True, False), (False, True, False, True)])
+    (False, False, False, True), (True, False, False, True), (True, False, True, False), (False, True, False, True),
+    (False, "key", False, True)])
 def test_backward_reference_forward_is_the_oracle(apf, gated, per_key, beta_aware):
     p = bw_problem(81, T=20, K=8, V=5, apf=apf, gated=gated, per_key=per_key)
     kw = dict(eta=0.3, d_min=0.5, d_max=2.0, eps=1e-6, beta_aware=beta_aware, scale=0.7)
@@ -584,7 +585,8 @@ def test_backward_reference_forward_is_the_oracle(apf, gated, per_key, beta_awar
 
 
 @pytest.mark.parametrize("apf,gated,per_key,beta_aware", [
-    (False, False, False, True), (True, False, False, False), (True, False, True, True), (False, True, False, True)])
+    (False, False, False, True), (True, False, False, False), (True, False, True, True), (False, True, False, True),
+    (False, "key", False, True)])
 def test_backward_reference_equals_finite_differences(apf, gated, per_key, beta_aware):
     """<grad_X L, delta> against (L(X + h delta) - L(X - h delta)) / 2h with the C oracle's forward,
     for every input X and a random direction delta; the upstream gradients weight o, S_T, d_T, k~."""
@@ -621,3 +623,57 @@ def test_backward_reference_clipped_coordinates_pass_no_gradient():
                                dd=np.ones_like(p["d0"]), eta=0.0, d_min=0.5, d_max=2.0)
     assert np.all(grads["dd0"][..., 0] == 0.0)
     np.testing.assert_allclose(grads["dd0"][..., 1:], 1.0, rtol=0, atol=0)  # eta = 0: d_T = d0 inside the box
+
+
+# ---------------------------------------------------------------------------------------------
+# One state gate per key channel (OSKDA, Appendix B.2): KDA's K x V state S_t =
+# (I - beta_t k~_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k~_t v_t^T, o_t = S_t^T q_t; this library
+# stores the V x K transpose.
+# ---------------------------------------------------------------------------------------------
+def textbook_kda(q, k, kt, v, beta, alpha):
+    """KDA with the write key on the left, in its own K x V convention (written independently)."""
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.zeros((B, T, H, V))
+    S_all = np.zeros((B, H, K, V))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((K, V))
+            for t in range(T):
+                a = (np.eye(K) - beta[b, t, h] * np.outer(kt[b, t, h], k[b, t, h])) @ np.diag(alpha[b, t, h])
+                S = a @ S + beta[b, t, h] * np.outer(kt[b, t, h], v[b, t, h])
+                o[b, t, h] = S.T @ q[b, t, h]
+            S_all[b, h] = S
+    return o, S_all
+
+
+def test_channel_gates_follow_textbook_kda():
+    q, k, v, beta, _ = rand_problem(91, B=2, T=30, H=2, K=6, V=4)
+    alpha = gates(92, k.shape, lo=0.5)
+    kt, _ = oracle.precond_scan(k, beta, None, None, eta=0.3)
+    o, S = oracle.delta_phase2(q, k, kt, v, beta, None, alpha=alpha)
+    o_ref, S_ref = textbook_kda(q, k, kt, v, beta, alpha)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(np.swapaxes(S, -1, -2), S_ref, rtol=0, atol=1e-12)
+
+
+def test_equal_channel_gates_are_the_head_gate():
+    q, k, v, beta, r = rand_problem(93, B=1, T=25, H=2, K=6, V=4, apf=True)
+    alpha = gates(94, beta.shape)
+    a = oracle.osdn_forward(q, k, v, beta, r, alpha=alpha, eta=0.2)
+    b = oracle.osdn_forward(q, k, v, beta, r, alpha=np.repeat(alpha[..., None], k.shape[-1], axis=-1), eta=0.2)
+    for key in ("o", "S", "d", "k_tilde"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_channel_gated_decode_steps_equal_forward():
+    q, k, v, beta, r = rand_problem(95, B=2, T=5, H=2, K=8, V=5, apf=True)
+    alpha = gates(96, k.shape)
+    g = rng(97)
+    S = g.standard_normal((2, 2, 5, 8)) * 0.1
+    d = g.uniform(0.6, 1.8, size=(2, 2, 8))
+    full = oracle.osdn_forward(q, k, v, beta, r, d, S, alpha=alpha, eta=0.2)
+    for t in range(5):
+        o, S, d = oracle.decode_step(q[:, t], k[:, t], v[:, t], beta[:, t], S, d, r[:, t], alpha=alpha[:, t], eta=0.2)
+        np.testing.assert_allclose(o, full["o"][:, t], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(S, full["S"], rtol=0, atol=1e-13)
