@@ -108,6 +108,11 @@ size_t osdn_precond_scan_workspace_bytes(int B, int T, int H, int K, osdn_dtype 
  *            or NULL for none.  With it every token first scales the state, Sbar = alpha_t S_{t-1},
  *            then e_t = v_t - Sbar k_t, S_t = Sbar + beta_t e_t k~_t^T (post-gate residual).
  *            Gates are read as given (the pages' gates lie in (0, 1]).
+ *   alpha_per_key
+ *            1: alpha is [B,T,H,K], one state gate per key channel (OSKDA, Appendix B.2: KDA's
+ *            K x V state Diag(alpha_t) S_{t-1}; the state here is its V x K transpose, so column i
+ *            is scaled by alpha_{t,i}); such calls run the fp32 CUDA-core kernel.  0: one per head
+ *            (OSGDN).  Ignored without alpha; other values OSDN_ERR_ARG.
  *   S0       [B,H,V,K] fp32 initial state; NULL means zeros
  *   o        [B,T,H,V] outputs o_t = scale * S_t q_t, dtype `dtype` (written)
  *   S_out    [B,H,V,K] fp32 final state (written; may alias S0)
@@ -127,7 +132,8 @@ size_t osdn_precond_scan_workspace_bytes(int B, int T, int H, int K, osdn_dtype 
  * CUDA-core kernel (which needs no workspace).
  */
 osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, const void* v,
-                           osdn_dtype dtype, const float* beta, const float* alpha, const float* S0, void* o,
+                           osdn_dtype dtype, const float* beta, const float* alpha, int alpha_per_key,
+                           const float* S0, void* o,
                            float* S_out, int B, int T, int H, int K, int V, int chunk,
                            float scale, void* workspace, size_t workspace_bytes, void* stream);
 
@@ -145,7 +151,7 @@ size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
  *   k_tilde  [B,T,H,K] write keys, dtype `dtype` (written; the phase-2 input)
  *   o, S_out as osdn_chunk_fwd; d_out as osdn_precond_scan (both written)
  *   r, r_per_key as osdn_precond_scan (vector retention always takes the two separate calls)
- *   alpha    as osdn_chunk_fwd (the OSGDN state gate; phase 1 does not use it)
+ *   alpha, alpha_per_key as osdn_chunk_fwd (the OSGDN / OSKDA state gate; phase 1 does not use it)
  *   workspace, workspace_bytes
  *            optional caller-owned device scratch (16-byte aligned).  With at least
  *            osdn_layer_fwd_workspace_bytes(...) bytes, bf16/f16 inputs with K = V = 128 and
@@ -157,8 +163,8 @@ size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
  *   T must be a multiple of `chunk` (64).
  */
 osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
-                           const float* r, int r_per_key, const float* alpha, const float* d0, const float* S0,
-                           void* k_tilde, void* o,
+                           const float* r, int r_per_key, const float* alpha, int alpha_per_key, const float* d0,
+                           const float* S0, void* k_tilde, void* o,
                            float* S_out, float* d_out, int B, int T, int H, int K, int V, int chunk,
                            float eta, float d_min, float d_max, float eps, float scale, int beta_aware,
                            void* workspace, size_t workspace_bytes, void* stream);
@@ -188,14 +194,16 @@ size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
  * Other arguments as osdn_layer_fwd.  A sequence of length 0 returns d0 and S0 unchanged.
  */
 osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
-                                  const float* r, int r_per_key, const float* alpha, const int* cu_seqlens, int N,
+                                  const float* r, int r_per_key, const float* alpha, int alpha_per_key,
+                                  const int* cu_seqlens, int N,
                                   long long total, int max_len, const float* d0, const float* S0, void* k_tilde,
                                   void* o, float* S_out, float* d_out, int H, int K, int V, int chunk, float eta,
                                   float d_min, float d_max, float eps, float scale, int beta_aware, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
 /* Workspace size for osdn_layer_fwd_varlen: r_mode 0 (no retention), 1 (one per head) or 2 (one
- * per key coordinate); gated nonzero when alpha is passed.  0 for invalid arguments. */
+ * per key coordinate); gated 0 (no alpha), 1 (one per head) or 2 (one per key channel).  0 for
+ * invalid arguments. */
 size_t osdn_layer_fwd_varlen_workspace_bytes(int N, int max_len, int H, int K, int V, int chunk, osdn_dtype dtype,
                                              int r_mode, int gated);
 
@@ -245,7 +253,7 @@ size_t osdn_layer_bwd_workspace_bytes(int B, int T, int H, int K, int V);
  */
 osdn_status osdn_chunk_fwd_static_ws(const void* q, const void* k, const void* k_tilde,
                                      const void* v, osdn_dtype dtype, const float* beta,
-                                     const float* alpha, const float* S0, void* o, float* S_out, int B, int T, int H,
+                                     const float* alpha, int alpha_per_key, const float* S0, void* o, float* S_out, int B, int T, int H,
                                      int K, int V, int chunk, float scale, void* stream);
 
 /*
@@ -255,12 +263,12 @@ osdn_status osdn_chunk_fwd_static_ws(const void* q, const void* k, const void* k
  *   u = v - S k;  S <- S + beta u k~^T;  o = scale * S q.
  *   q, k [B,H,K], v [B,H,V] of dtype `dtype`; beta [B,H] fp32; r fp32 or NULL: [B,H] with
  *   r_per_key = 0, or [B,H,K] (one gate per key coordinate, diag(r_t)) with r_per_key = 1;
- *   alpha [B,H] fp32 or NULL;
+ *   alpha [B,H] fp32 or NULL ([B,H,K] with alpha_per_key = 1: one gate per key channel, OSKDA);
  *   S [B,H,V,K] fp32 and d [B,H,K] fp32 are read and overwritten; o [B,H,V] dtype `dtype`.
  */
 osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,
-                             const float* beta, const float* r, int r_per_key, const float* alpha, float* S,
-                             float* d, void* o,
+                             const float* beta, const float* r, int r_per_key, const float* alpha,
+                             int alpha_per_key, float* S, float* d, void* o,
                              int B, int H, int K, int V, float eta, float d_min, float d_max,
                              float eps, float scale, int beta_aware, void* stream);
 

@@ -47,18 +47,18 @@ def lib() -> ctypes.CDLL:
     L.osdn_precond_scan.argtypes = [vp, i, fp, fp, i, fp, vp, i, fp, i, i, i, i, f, f, f, f, i, vp, sz, vp]
     L.osdn_precond_scan_workspace_bytes.argtypes = [i, i, i, i, i]
     L.osdn_precond_scan_workspace_bytes.restype = sz
-    L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, fp, vp, fp, i, i, i, i, i, i, f, vp, sz, vp]
+    L.osdn_chunk_fwd.argtypes = [vp, vp, vp, vp, i, fp, fp, i, fp, vp, fp, i, i, i, i, i, i, f, vp, sz, vp]
     L.osdn_chunk_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.osdn_chunk_fwd_workspace_bytes.restype = sz
-    L.osdn_chunk_fwd_static_ws.argtypes = [vp, vp, vp, vp, i, fp, fp, fp, vp, fp, i, i, i, i, i, i, f, vp]
+    L.osdn_chunk_fwd_static_ws.argtypes = [vp, vp, vp, vp, i, fp, fp, i, fp, vp, fp, i, i, i, i, i, i, f, vp]
     L.osdn_chunk_fwd_static_ws.restype = ctypes.c_int
-    L.osdn_layer_fwd.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, fp, vp, vp, fp, fp, i, i, i, i, i, i,
+    L.osdn_layer_fwd.argtypes = [vp, vp, vp, i, fp, fp, i, fp, i, fp, fp, vp, vp, fp, fp, i, i, i, i, i, i,
                                  f, f, f, f, f, i, vp, sz, vp]
     L.osdn_layer_fwd.restype = ctypes.c_int
     L.osdn_layer_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.osdn_layer_fwd_workspace_bytes.restype = sz
     ll = ctypes.c_longlong
-    L.osdn_layer_fwd_varlen.argtypes = [vp, vp, vp, i, fp, fp, i, fp, vp, i, ll, i, fp, fp, vp, vp, fp, fp, i, i, i,
+    L.osdn_layer_fwd_varlen.argtypes = [vp, vp, vp, i, fp, fp, i, fp, i, vp, i, ll, i, fp, fp, vp, vp, fp, fp, i, i, i,
                                         i, f, f, f, f, f, i, vp, sz, vp]
     L.osdn_layer_fwd_varlen.restype = ctypes.c_int
     L.osdn_layer_fwd_varlen_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i]
@@ -68,7 +68,7 @@ def lib() -> ctypes.CDLL:
     L.osdn_layer_bwd.restype = ctypes.c_int
     L.osdn_layer_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
     L.osdn_layer_bwd_workspace_bytes.restype = sz
-    L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
+    L.osdn_decode_step.argtypes = [vp, vp, vp, i, fp, fp, i, fp, i, fp, fp, vp, i, i, i, i, f, f, f, f, f, i, vp]
     L.osdn_check.argtypes = [vp]
     for fn in ("osdn_precond_scan", "osdn_chunk_fwd", "osdn_decode_step", "osdn_check"):
         getattr(L, fn).restype = ctypes.c_int
@@ -123,6 +123,16 @@ def _code(dtype) -> int:
     if dtype not in _DTYPE_CODE:
         raise ValueError(f"unsupported dtype {dtype}; use float32, bfloat16 or float16")
     return _DTYPE_CODE[dtype]
+
+
+def _state_gate(alpha, head_shape, K, dev):
+    """Check the state gate and say its layout: 0 for one gate per head (``head_shape``, OSGDN), 1
+    for one per key channel (``head_shape + (K,)``, OSKDA)."""
+    if alpha is None:
+        return 0
+    per_key = tuple(alpha.shape) == tuple(head_shape) + (K,)
+    _check("alpha", alpha, tuple(head_shape) + ((K,) if per_key else ()), torch.float32, dev)
+    return int(per_key)
 
 
 def _retention(r, head_shape, K, dev):
@@ -216,7 +226,7 @@ def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, alpha=None, o=None, S_out
                          ("k_tilde", k_tilde, (B, T, H, K)), ("v", v, (B, T, H, V))):
         _check(name, t, shp, dt, dev)
     _check("beta", beta, (B, T, H), torch.float32, dev)
-    _check("alpha", alpha, (B, T, H), torch.float32, dev)
+    a_per_key = _state_gate(alpha, (B, T, H), K, dev)
     _check("S0", S0, (B, H, V, K), torch.float32, dev)
     if o is None:
         o = torch.empty((B, T, H, V), device=dev, dtype=dt)
@@ -227,7 +237,7 @@ def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, alpha=None, o=None, S_out
     need = osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 else 0
     ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "chunk")
     st = lib().osdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(k_tilde), _ptr(v), _code(dt), _ptr(beta),
-                              _ptr(alpha), _ptr(S0), _ptr(o), _ptr(S_out), B, T, H, K, V, int(chunk),
+                              _ptr(alpha), a_per_key, _ptr(S0), _ptr(o), _ptr(S_out), B, T, H, K, V, int(chunk),
                               float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
     _raise("osdn_chunk_fwd", st)
     return o, S_out
@@ -244,14 +254,14 @@ def osdn_decode_step(q, k, v, beta, S, d, r=None, *, alpha=None, o=None, eta=0.0
     _check("v", v, (B, H, V), dt, dev)
     _check("beta", beta, (B, H), torch.float32, dev)
     r_per_key = _retention(r, (B, H), K, dev)
-    _check("alpha", alpha, (B, H), torch.float32, dev)
+    a_per_key = _state_gate(alpha, (B, H), K, dev)
     _check("S", S, (B, H, V, K), torch.float32, dev)
     _check("d", d, (B, H, K), torch.float32, dev)
     if o is None:
         o = torch.empty((B, H, V), device=dev, dtype=dt)
     _check("o", o, (B, H, V), dt, dev)
     st = lib().osdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key,
-                                _ptr(alpha), _ptr(S), _ptr(d), _ptr(o), B, H, K, V, float(eta), float(d_min),
+                                _ptr(alpha), a_per_key, _ptr(S), _ptr(d), _ptr(o), B, H, K, V, float(eta), float(d_min),
                                 float(d_max), float(eps), float(scale), int(bool(beta_aware)),
                                 _stream(dev, stream))
     _raise("osdn_decode_step", st)
@@ -283,7 +293,7 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, k_til
         _check(name, t, shp, dt, dev)
     _check("beta", beta, (B, T, H), torch.float32, dev)
     r_per_key = _retention(r, (B, T, H), K, dev)
-    _check("alpha", alpha, (B, T, H), torch.float32, dev)
+    a_per_key = _state_gate(alpha, (B, T, H), K, dev)
     _check("d0", d0, (B, H, K), torch.float32, dev)
     _check("S0", S0, (B, H, V, K), torch.float32, dev)
     if k_tilde is None:
@@ -301,7 +311,7 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, k_til
     need = osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 and T % chunk == 0 else 0
     ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "layer")
     st = lib().osdn_layer_fwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, _ptr(alpha),
-                              _ptr(d0),
+                              a_per_key, _ptr(d0),
                               _ptr(S0), _ptr(k_tilde), _ptr(o), _ptr(S_out), _ptr(d_out), B, T, H, K,
                               V, int(chunk), float(eta), float(d_min), float(d_max), float(eps),
                               float(scale), int(bool(beta_aware)), ws_ptr, ws_bytes,
@@ -311,9 +321,10 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, k_til
 
 
 def osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk=64, dtype=torch.bfloat16, r_mode=0,
-                                          gated=False) -> int:
+                                          gated=0) -> int:
+    """gated: 0 no state gate, 1 one per head, 2 one per key channel."""
     return int(lib().osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk, _code(dtype), int(r_mode),
-                                                           int(bool(gated))))
+                                                           int(gated)))
 
 
 def osdn_layer_fwd_varlen(q, k, v, beta, cu_seqlens, *, max_len=None, r=None, alpha=None, d0=None, S0=None,
@@ -338,7 +349,7 @@ def osdn_layer_fwd_varlen(q, k, v, beta, cu_seqlens, *, max_len=None, r=None, al
         _check(name, t, shp, dt, dev)
     _check("beta", beta, (total, H), torch.float32, dev)
     r_per_key = _retention(r, (total, H), K, dev)
-    _check("alpha", alpha, (total, H), torch.float32, dev)
+    a_per_key = _state_gate(alpha, (total, H), K, dev)
     _check("cu_seqlens", cu_seqlens, (cu_seqlens.shape[0],), torch.int32, dev)
     N = cu_seqlens.shape[0] - 1
     if N < 0:
@@ -360,12 +371,13 @@ def osdn_layer_fwd_varlen(q, k, v, beta, cu_seqlens, *, max_len=None, r=None, al
         d_out = torch.empty((N, H, K), device=dev, dtype=torch.float32)
     _check("d_out", d_out, (N, H, K), torch.float32, dev)
     r_mode = 0 if r is None else 1 + r_per_key
-    need = osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk, dt, r_mode, alpha is not None) if N else 0
+    g_mode = 0 if alpha is None else 1 + a_per_key
+    need = osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk, dt, r_mode, g_mode) if N else 0
     if workspace is False:
         raise ValueError("osdn_layer_fwd_varlen needs a workspace")
     ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "varlen")
     st = lib().osdn_layer_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, _ptr(alpha),
-                                     _ptr(cu_seqlens), N, int(total), int(max_len), _ptr(d0), _ptr(S0), _ptr(k_tilde),
+                                     a_per_key, _ptr(cu_seqlens), N, int(total), int(max_len), _ptr(d0), _ptr(S0), _ptr(k_tilde),
                                      _ptr(o), _ptr(S_out), _ptr(d_out), H, K, V, int(chunk), float(eta), float(d_min),
                                      float(d_max), float(eps), float(scale), int(bool(beta_aware)), ws_ptr, ws_bytes,
                                      _stream(dev, stream))

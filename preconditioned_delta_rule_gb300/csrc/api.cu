@@ -107,7 +107,8 @@ size_t osdn_precond_scan_workspace_bytes(int B, int T, int H, int K, osdn_dtype 
 }
 
 osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, const void* v,
-                           osdn_dtype dtype, const float* beta, const float* alpha, const float* S0, void* o,
+                           osdn_dtype dtype, const float* beta, const float* alpha, int alpha_per_key,
+                           const float* S0, void* o,
                            float* S_out, int B, int T, int H, int K, int V, int chunk,
                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
     if (B < 0 || T < 0 || H < 0 || chunk <= 0) return OSDN_ERR_SHAPE;
@@ -116,6 +117,7 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
     if (T % chunk != 0) return OSDN_ERR_SHAPE;
     if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
     if (!isfinite(scale)) return OSDN_ERR_ARG;
+    if (alpha_per_key != 0 && alpha_per_key != 1) return OSDN_ERR_ARG;
     if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
     if (B == 0 || H == 0) return OSDN_OK;
     const bool seq = T > 0;
@@ -129,7 +131,8 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
     OSDN_TRY(ptr(S0, false));
     OSDN_TRY(ptr(S_out, true));
     OSDN_TRY(ptr(workspace, false));
-    OsdnChunkArgs a{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale, alpha};
+    OsdnChunkArgs a{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale, alpha,
+                    alpha ? alpha_per_key : 0};
     return from_cuda(chunk_dispatch(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
@@ -143,8 +146,8 @@ size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chu
 }
 
 osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
-                           const float* r, int r_per_key, const float* alpha, const float* d0, const float* S0,
-                           void* k_tilde, void* o,
+                           const float* r, int r_per_key, const float* alpha, int alpha_per_key, const float* d0,
+                           const float* S0, void* k_tilde, void* o,
                            float* S_out, float* d_out, int B, int T, int H, int K, int V, int chunk,
                            float eta, float d_min, float d_max, float eps, float scale, int beta_aware,
                            void* workspace, size_t workspace_bytes, void* stream) {
@@ -156,6 +159,7 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
     OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
     if (!isfinite(scale)) return OSDN_ERR_ARG;
     if (r_per_key != 0 && r_per_key != 1) return OSDN_ERR_ARG;
+    if (alpha_per_key != 0 && alpha_per_key != 1) return OSDN_ERR_ARG;
     if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
     if (B == 0 || H == 0) return OSDN_OK;
     const bool seq = T > 0;
@@ -174,7 +178,8 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
     OSDN_TRY(ptr(workspace, false));
     OsdnScanArgs sa{k, dtype, beta, r, d0, k_tilde, dtype, d_out, B, T, H, K, eta, d_min, d_max, eps, beta_aware ? 1 : 0,
                     r != nullptr ? r_per_key : 0};
-    OsdnChunkArgs ca{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale, alpha};
+    OsdnChunkArgs ca{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale, alpha,
+                     alpha ? alpha_per_key : 0};
     return from_cuda(layer_dispatch(sa, ca, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
@@ -209,13 +214,14 @@ size_t osdn_layer_fwd_varlen_workspace_bytes(int N, int max_len, int H, int K, i
                                              int r_mode, int gated) {
     if (N <= 0 || max_len < 0 || H <= 0 || chunk <= 0 || !head_dim_ok(K) || !head_dim_ok(V) || !dtype_ok(dtype))
         return 0;
-    if (r_mode < 0 || r_mode > 2) return 0;
-    const OsdnVarlenShape v = varlen_shape(N, max_len, H, K, V, chunk, dtype, r_mode, gated ? 1 : 0, 0);
+    if (r_mode < 0 || r_mode > 2 || gated < 0 || gated > 2) return 0;
+    const OsdnVarlenShape v = varlen_shape(N, max_len, H, K, V, chunk, dtype, r_mode, gated, 0);
     return align256(osdn_varlen_pad_bytes(v)) + osdn_layer_fwd_workspace_bytes(N, v.Tp, H, K, V, chunk, dtype);
 }
 
 osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
-                                  const float* r, int r_per_key, const float* alpha, const int* cu_seqlens, int N,
+                                  const float* r, int r_per_key, const float* alpha, int alpha_per_key,
+                                  const int* cu_seqlens, int N,
                                   long long total, int max_len, const float* d0, const float* S0, void* k_tilde,
                                   void* o, float* S_out, float* d_out, int H, int K, int V, int chunk, float eta,
                                   float d_min, float d_max, float eps, float scale, int beta_aware, void* workspace,
@@ -245,7 +251,9 @@ osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, o
     OSDN_TRY(ptr(d_out, true));
     OSDN_TRY(ptr(workspace, true));
     const int r_mode = r ? (r_per_key ? 2 : 1) : 0;
-    const OsdnVarlenShape vs = varlen_shape(N, max_len, H, K, V, chunk, dtype, r_mode, alpha ? 1 : 0, total);
+    if (alpha_per_key != 0 && alpha_per_key != 1) return OSDN_ERR_ARG;
+    const int g_mode = alpha ? (alpha_per_key ? 2 : 1) : 0;
+    const OsdnVarlenShape vs = varlen_shape(N, max_len, H, K, V, chunk, dtype, r_mode, g_mode, total);
     const size_t pad = align256(osdn_varlen_pad_bytes(vs));
     const size_t need_layer = osdn_layer_fwd_workspace_bytes(N, vs.Tp, H, K, V, chunk, dtype);
     if (workspace_bytes < pad + need_layer) return OSDN_ERR_ARG;
@@ -268,7 +276,7 @@ osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, o
     io.po = take(rows * H * V * vs.elt);
     io.pbeta = reinterpret_cast<float*>(take(rows * H * 4));
     if (r_mode) io.pr = reinterpret_cast<float*>(take(rows * H * (r_mode == 2 ? K : 1) * 4));
-    if (alpha) io.palpha = reinterpret_cast<float*>(take(rows * H * 4));
+    if (alpha) io.palpha = reinterpret_cast<float*>(take(rows * H * (g_mode == 2 ? K : 1) * 4));
     unsigned char* wl = static_cast<unsigned char*>(workspace) + pad;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = osdn_launch_varlen_pack(io, vs, s);
@@ -276,7 +284,7 @@ osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, o
     OsdnScanArgs sa{io.pk, dtype, io.pbeta, io.pr, d0, io.pkt, dtype, d_out, N, vs.Tp, H, K, eta, d_min, d_max, eps,
                     beta_aware ? 1 : 0, r_mode == 2 ? 1 : 0};
     OsdnChunkArgs ca{io.pq, io.pk, io.pkt, io.pv, dtype, io.pbeta, S0, io.po, S_out, N, vs.Tp, H, K, V, chunk, scale,
-                     io.palpha};
+                     io.palpha, g_mode == 2 ? 1 : 0};
     e = layer_dispatch(sa, ca, wl, need_layer, s);
     if (e != cudaSuccess) return from_cuda(e);
     return from_cuda(osdn_launch_varlen_unpack(io, vs, s));
@@ -337,8 +345,8 @@ osdn_status osdn_layer_bwd(const void* q, const void* k, const void* v, osdn_dty
 }
 
 osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_dtype dtype,
-                             const float* beta, const float* r, int r_per_key, const float* alpha, float* S,
-                             float* d, void* o,
+                             const float* beta, const float* r, int r_per_key, const float* alpha,
+                             int alpha_per_key, float* S, float* d, void* o,
                              int B, int H, int K, int V, float eta, float d_min, float d_max,
                              float eps, float scale, int beta_aware, void* stream) {
     if (B < 0 || H < 0) return OSDN_ERR_SHAPE;
@@ -347,6 +355,7 @@ osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_d
     OSDN_TRY(phase1_scalars(eta, d_min, d_max, eps));
     if (!isfinite(scale)) return OSDN_ERR_ARG;
     if (r_per_key != 0 && r_per_key != 1) return OSDN_ERR_ARG;
+    if (alpha_per_key != 0 && alpha_per_key != 1) return OSDN_ERR_ARG;
     if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
     if (B == 0 || H == 0) return OSDN_OK;
     OSDN_TRY(ptr(q, true));
@@ -359,7 +368,8 @@ osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_d
     OSDN_TRY(ptr(d, true));
     OSDN_TRY(ptr(o, true));
     OsdnDecodeArgs a{q, k, v, dtype, beta, r, S, d, o, B, H, K, V,
-                     eta, d_min, d_max, eps, scale, beta_aware ? 1 : 0, r != nullptr ? r_per_key : 0, alpha};
+                     eta, d_min, d_max, eps, scale, beta_aware ? 1 : 0, r != nullptr ? r_per_key : 0, alpha,
+                     alpha ? alpha_per_key : 0};
     return from_cuda(osdn_launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 

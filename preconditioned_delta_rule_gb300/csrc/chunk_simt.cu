@@ -6,7 +6,8 @@
 //   S_t = S_{t-1} + beta_t u_t k~_t^T   (write key)
 //   o_t = scale * S_t q_t   (readout after the write)
 // With the OSGDN state gate (Appendix B.1, post-gate residual) S_{t-1} is first scaled by
-// alpha_t (alpha = 1 without the gate: an exact no-op).
+// alpha_t (alpha = 1 without the gate: an exact no-op), or each column i by alpha_{t,i} with one
+// gate per key channel (OSKDA, Appendix B.2, in the transpose of its K x V convention).
 // This kernel evaluates the recurrence token by token in fp32 (FFMA only), which is exact up to
 // fp32 rounding for any input dtype.  It serves fp32 inputs (where bf16/f16 tensor-core
 // operands could not meet a 1e-4 tolerance) and the head sizes the tensor-core kernel is not
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(256) chunk_recurrent_kernel(OsdnChunkArgs a) {
     }
 
     const size_t row0 = (size_t)b * T * H + h;
-    float kv[E], ktv[E], qv[E], vv[kRowsPerWarp], bt = 0.f, al = 1.f;
+    float kv[E], ktv[E], qv[E], vv[kRowsPerWarp], bt = 0.f, al[E];
     auto load = [&](int t) {
         const size_t r = row0 + (size_t)t * H;
         VecIO<TIn, E>::load(kg + r * K + lane * E, kv);
@@ -53,7 +54,12 @@ __global__ void __launch_bounds__(256) chunk_recurrent_kernel(OsdnChunkArgs a) {
 #pragma unroll
         for (int j = 0; j < kRowsPerWarp; ++j) vv[j] = to_f32(vg[r * V + row_base + j]);
         bt = a.beta[r];
-        al = a.alpha ? a.alpha[r] : 1.f;
+        if (a.alpha && a.alpha_per_key) {
+            VecIO<float, E>::load(a.alpha + r * K + lane * E, al);
+        } else {
+#pragma unroll
+            for (int i = 0; i < E; ++i) al[i] = a.alpha ? a.alpha[r] : 1.f;
+        }
     };
     if (T > 0) load(0);
     for (int t = 0; t < T; ++t) {
@@ -62,7 +68,10 @@ __global__ void __launch_bounds__(256) chunk_recurrent_kernel(OsdnChunkArgs a) {
         for (int i = 0; i < E; ++i) { ck[i] = kv[i]; ckt[i] = ktv[i]; cq[i] = qv[i]; }
 #pragma unroll
         for (int j = 0; j < kRowsPerWarp; ++j) cv[j] = vv[j];
-        const float cb = bt, ca = al;
+        const float cb = bt;
+        float ca[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) ca[i] = al[i];
         if (t + 1 < T) load(t + 1);
         const size_t r = row0 + (size_t)t * H;
 #pragma unroll
@@ -70,7 +79,7 @@ __global__ void __launch_bounds__(256) chunk_recurrent_kernel(OsdnChunkArgs a) {
             float sk = 0.f;
 #pragma unroll
             for (int i = 0; i < E; ++i) {
-                S[j][i] *= ca;
+                S[j][i] *= ca[i];
                 sk = fmaf(S[j][i], ck[i], sk);
             }
             sk = warp_sum(sk);

@@ -46,7 +46,7 @@ cudaError_t static_ws_address(void** out) {
 extern "C" {
 
 osdn_status osdn_chunk_fwd_static_ws(const void* q, const void* k, const void* k_tilde, const void* v,
-                                     osdn_dtype dtype, const float* beta, const float* alpha,
+                                     osdn_dtype dtype, const float* beta, const float* alpha, int alpha_per_key,
                                      const float* S0, void* o,
                                      float* S_out, int B, int T, int H, int K, int V, int chunk,
                                      float scale, void* stream) {
@@ -58,7 +58,8 @@ osdn_status osdn_chunk_fwd_static_ws(const void* q, const void* k, const void* k
         // so nothing needs clearing between calls.
         if (static_ws_address(&ws) != cudaSuccess) return OSDN_ERR_CUDA;
     }
-    return osdn_chunk_fwd(q, k, k_tilde, v, dtype, beta, alpha, S0, o, S_out, B, T, H, K, V, chunk, scale, ws,
+    return osdn_chunk_fwd(q, k, k_tilde, v, dtype, beta, alpha, alpha_per_key, S0, o, S_out, B, T, H, K, V, chunk,
+                          scale, ws,
                           need, stream);
 }
 

@@ -1558,8 +1558,9 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
 }
 
 bool tc_covers(const OsdnChunkArgs& a) {
+    // (one state gate per key channel puts the decay inside the Gram's contraction: not built here)
     return a.K == KD && a.V % VS == 0 && a.chunk == C && a.T > 0 && a.T % C == 0 &&
-           (a.dtype == OSDN_BF16 || a.dtype == OSDN_F16);
+           (a.dtype == OSDN_BF16 || a.dtype == OSDN_F16) && !(a.alpha && a.alpha_per_key);
 }
 
 // Workspace of the fused layer: [scan: step sizes, block-start states][chunk counter][chunk

@@ -105,6 +105,7 @@ struct OsdnChunkArgs {
     const float* beta; const float* S0; void* o; float* S_out;
     int B, T, H, K, V, chunk; float scale;
     const float* alpha;  // [B,T,H] OSGDN state gate (Appendix B.1), or null: no gate
+    int alpha_per_key;   // 1: alpha [B,T,H,K], one gate per key channel (OSKDA, Appendix B.2)
 };
 struct OsdnDecodeArgs {
     const void* q; const void* k; const void* v; osdn_dtype dtype; const float* beta;
@@ -112,6 +113,7 @@ struct OsdnDecodeArgs {
     int B, H, K, V; float eta, d_min, d_max, eps, scale; int beta_aware;
     int r_per_key;  // 1: r [B,H,K], one retention per key coordinate (vector retention)
     const float* alpha;  // [B,H] OSGDN state gate (Appendix B.1), or null: no gate
+    int alpha_per_key;   // 1: alpha [B,H,K], one gate per key channel (OSKDA, Appendix B.2)
 };
 
 // Phase-1 scan.  16-bit keys with K = 128 use the blocked kernel; with a workspace of at least
@@ -132,7 +134,7 @@ struct OsdnVarlenShape {
     long long total;  // packed tokens
     int elt;          // bytes per q/k/v/o/k~ element
     int r_mode;       // 0 no retention, 1 one per head, 2 one per key coordinate
-    int gated;        // alpha given
+    int gated;        // 0 no state gate, 1 one per head, 2 one per key channel
 };
 struct OsdnVarlenIo {
     const int* cu;                                        // [N + 1] sequence offsets

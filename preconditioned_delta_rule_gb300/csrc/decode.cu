@@ -7,7 +7,9 @@
 //   u_i = v_i - <S_i, k>;  S_i <- S_i + beta u_i k~;  o_i = <S_i_new, q'> = <S_i, q'> + beta u_i <k~, q'>
 // with q' = scale * q, for every row i of S (rows are independent given k, k~, q).  With the OSGDN
 // state gate (Appendix B.1, post-gate residual) S is first scaled by alpha: S <- alpha S, then the
-// same step (alpha = 1 without the gate: an exact no-op).
+// same step (alpha = 1 without the gate: an exact no-op); with one gate per key channel (OSKDA,
+// Appendix B.2, the state stored as the transpose of its K x V convention) column i of S is scaled
+// by alpha_i.
 //
 // The step is HBM-bound: S (V x K fp32) is read once and written once.  One CTA of 256 threads
 // per head; 8 lanes per row, each lane holding 4-float pieces interleaved so that every load
@@ -104,7 +106,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
         }
     }
     const float bt = scoef[0], bktq = scoef[1];
-    const float ag = a.alpha ? a.alpha[bh] : 1.f;
+    // state gate of this thread's columns: one per head, one per key channel, or 1
+    float ga[P4][4];
+#pragma unroll
+    for (int c = 0; c < P4; ++c)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            ga[c][j] = !a.alpha ? 1.f : (a.alpha_per_key ? a.alpha[bh * K + (c * kLanesPerRow + sub) * 4 + j] : a.alpha[bh]);
 
     float4 Sr[PASSES][P4];
 #pragma unroll
@@ -121,10 +129,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
         float dk = 0.f, dq = 0.f;
 #pragma unroll
         for (int c = 0; c < P4; ++c) {
-            Sr[ps][c].x *= ag;
-            Sr[ps][c].y *= ag;
-            Sr[ps][c].z *= ag;
-            Sr[ps][c].w *= ag;
+            Sr[ps][c].x *= ga[c][0];
+            Sr[ps][c].y *= ga[c][1];
+            Sr[ps][c].z *= ga[c][2];
+            Sr[ps][c].w *= ga[c][3];
             const float4 x = Sr[ps][c];
             dk = fmaf(x.x, kr[c][0], fmaf(x.y, kr[c][1], fmaf(x.z, kr[c][2], fmaf(x.w, kr[c][3], dk))));
             dq = fmaf(x.x, qr[c][0], fmaf(x.y, qr[c][1], fmaf(x.z, qr[c][2], fmaf(x.w, qr[c][3], dq))));

@@ -156,7 +156,7 @@ size_t osdn_varlen_pad_bytes(const OsdnVarlenShape& v) {
     b += up(rows * v.H * 4);                    // beta
     if (v.r_mode == 1) b += up(rows * v.H * 4);
     if (v.r_mode == 2) b += up(rows * v.H * v.K * 4);
-    if (v.gated) b += up(rows * v.H * 4);       // alpha
+    if (v.gated) b += up(rows * v.H * (v.gated == 2 ? v.K : 1) * 4);  // alpha
     return b;
 }
 
@@ -173,7 +173,7 @@ cudaError_t osdn_launch_varlen_pack(const OsdnVarlenIo& io, const OsdnVarlenShap
     if (io.r) a.t[i++] = {reinterpret_cast<const unsigned char*>(io.r), reinterpret_cast<unsigned char*>(io.pr),
                           v.H * (v.r_mode == 2 ? v.K : 1) * 4LL, one};
     if (io.alpha) a.t[i++] = {reinterpret_cast<const unsigned char*>(io.alpha), reinterpret_cast<unsigned char*>(io.palpha),
-                              v.H * 4LL, one};
+                              v.H * (v.gated == 2 ? v.K : 1) * 4LL, one};
     a.nt = i;
     a.cu = io.cu;
     a.N = v.N;

@@ -60,7 +60,8 @@ def chunk(L, **kw):
     a = dict(q=A, k=A, kt=A, v=A, dt=1, beta=A, S0=None, o=A, Sout=A, B=2, T=128, H=2, K=128,
              V=128, C=64, scale=1.0)
     a.update(kw)
-    return L.osdn_chunk_fwd(a["q"], a["k"], a["kt"], a["v"], a["dt"], a["beta"], a.get("alpha"), a["S0"], a["o"],
+    return L.osdn_chunk_fwd(a["q"], a["k"], a["kt"], a["v"], a["dt"], a["beta"], a.get("alpha"), a.get("apk", 0), a["S0"],
+                            a["o"],
                             a["Sout"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"], a["scale"],
                             a.get("ws"), a.get("wsb", 0), None)
 
@@ -70,7 +71,7 @@ def decode(L, **kw):
              eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6, scale=1.0, ba=1)
     a.update(kw)
     return L.osdn_decode_step(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a.get("rpk", 0), a.get("alpha"),
-                              a["S"], a["d"],
+                              a.get("apk", 0), a["S"], a["d"],
                               a["o"], a["B"], a["H"], a["K"], a["V"], a["eta"], a["dmin"],
                               a["dmax"], a["eps"], a["scale"], a["ba"], None)
 
@@ -93,7 +94,7 @@ def test_scan_validation(L, kw, want):
     (dict(v=A + 8), ALIGN), (dict(S0=A + 4), ALIGN),
     (dict(T=100), SHAPE), (dict(C=0), SHAPE), (dict(C=32), UNSUP), (dict(K=256), UNSUP),
     (dict(V=48), UNSUP), (dict(dt=5), DTYPE), (dict(scale=math.inf), ARG),
-    (dict(ws=A + 8, wsb=1 << 20), ALIGN), (dict(alpha=A + 4), ALIGN), (dict(B=0), OK),
+    (dict(ws=A + 8, wsb=1 << 20), ALIGN), (dict(alpha=A + 4), ALIGN), (dict(apk=2), ARG), (dict(B=0), OK),
 ])
 def test_chunk_validation(L, kw, want):
     assert chunk(L, **kw) == want
@@ -102,7 +103,7 @@ def test_chunk_validation(L, kw, want):
 @pytest.mark.parametrize("kw,want", [
     (dict(S=None), ARG), (dict(d=None), ARG), (dict(o=None), ARG), (dict(q=A + 1), ALIGN),
     (dict(K=32), UNSUP), (dict(dt=3), DTYPE), (dict(eps=-1.0), ARG), (dict(scale=math.nan), ARG),
-    (dict(rpk=-1), ARG), (dict(alpha=A + 8), ALIGN), (dict(H=0), OK),
+    (dict(rpk=-1), ARG), (dict(alpha=A + 8), ALIGN), (dict(apk=-1), ARG), (dict(H=0), OK),
 ])
 def test_decode_validation(L, kw, want):
     assert decode(L, **kw) == want
@@ -138,7 +139,7 @@ def layer(L, **kw):
              H=2, K=128, V=128, C=64, eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6, scale=1.0, ba=1)
     a.update(kw)
     return L.osdn_layer_fwd(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a.get("rpk", 0), a.get("alpha"),
-                            a["d0"], a["S0"], a["kt"],
+                            a.get("apk", 0), a["d0"], a["S0"], a["kt"],
                             a["o"], a["Sout"], a["dout"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"],
                             a["eta"], a["dmin"], a["dmax"], a["eps"], a["scale"], a["ba"], a.get("ws"),
                             a.get("wsb", 0), None)
@@ -148,7 +149,7 @@ def layer(L, **kw):
     (dict(kt=None), ARG), (dict(dout=None), ARG), (dict(Sout=None), ARG), (dict(o=None), ARG),
     (dict(q=A + 2), ALIGN), (dict(ws=A + 8, wsb=1 << 20), ALIGN), (dict(K=96), UNSUP), (dict(C=32), UNSUP),
     (dict(T=100), SHAPE), (dict(dt=5), DTYPE), (dict(eta=-1.0), ARG), (dict(scale=math.inf), ARG),
-    (dict(rpk=3), ARG), (dict(alpha=A + 12), ALIGN), (dict(B=0), OK),
+    (dict(rpk=3), ARG), (dict(alpha=A + 12), ALIGN), (dict(apk=5), ARG), (dict(B=0), OK),
 ])
 def test_layer_validation(L, kw, want):
     assert layer(L, **kw) == want
@@ -170,7 +171,8 @@ def varlen(L, **kw):
              S0=None, kt=A, o=A, Sout=A, dout=A, H=2, K=128, V=128, C=64, eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6,
              scale=1.0, ba=1, ws=A, wsb=1 << 40)
     a.update(kw)
-    return L.osdn_layer_fwd_varlen(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a["rpk"], a["alpha"], a["cu"],
+    return L.osdn_layer_fwd_varlen(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a["rpk"], a["alpha"],
+                                   a.get("apk", 0), a["cu"],
                                    a["N"], a["total"], a["maxlen"], a["d0"], a["S0"], a["kt"], a["o"], a["Sout"],
                                    a["dout"], a["H"], a["K"], a["V"], a["C"], a["eta"], a["dmin"], a["dmax"], a["eps"],
                                    a["scale"], a["ba"], a["ws"], a["wsb"], None)
@@ -198,3 +200,5 @@ def test_varlen_workspace_size_query(L):
     assert f(N, 0, H, 128, 128, 64, 1, 0, 0) > 0   # all empty: one chunk of padding each
     assert f(0, 300, H, 128, 128, 64, 1, 0, 0) == 0
     assert f(N, 300, H, 128, 128, 64, 1, 3, 0) == 0
+    assert f(N, 300, H, 128, 128, 64, 1, 0, 2) == up(pad + up(rows * H * 128 * 4)) + lay(N, Tp, H, 128, 128, 64, 1)
+    assert f(N, 300, H, 128, 128, 64, 1, 0, 3) == 0

@@ -27,7 +27,7 @@ def call_static(q, k, kt, v, beta, S0, o, S_out, scale=1.0):
     p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return binding.lib().osdn_chunk_fwd_static_ws(
-        p(q), p(k), p(kt), p(v), binding._code(k.dtype), p(beta), None, p(S0), p(o), p(S_out),
+        p(q), p(k), p(kt), p(v), binding._code(k.dtype), p(beta), None, 0, p(S0), p(o), p(S_out),
         B, T, H, K, V, 64, float(scale), stream)
 
 
