@@ -565,6 +565,10 @@ def run_gated(args, dev, stream, hbm_peak):
 
     t_layer = med(lambda: binding.osdn_layer_fwd(g["q"], g["k"], g["v"], g["beta"], g["r"], alpha=alpha,
                                                  k_tilde=kt, **kw))
+    # one gate per key channel (OSKDA, Appendix B.2): the CUDA-core chunk kernel
+    alpha_k = torch.sigmoid(4.0 + torch.randn(w.B, w.T, w.H, w.K, generator=gen)).to(dev)
+    t_kda = med(lambda: binding.osdn_layer_fwd(g["q"], g["k"], g["v"], g["beta"], g["r"], alpha=alpha_k,
+                                               k_tilde=kt, **kw))
     t_chunk = med(lambda: binding.osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], alpha=alpha))
     _, b_chunk, b_layer = layer_bytes(w)
     th = w.B * w.T * w.H
@@ -577,6 +581,8 @@ def run_gated(args, dev, stream, hbm_peak):
             "layer_ms": t_layer * 1e3, "tokens_per_s": th / w.H / t_layer,
             "layer_roofline_frac": frac(b_layer, t_layer),
             "chunk_ms": t_chunk * 1e3, "chunk_roofline_frac": frac(b_chunk, t_chunk),
+            "channel_gated_layer_ms": t_kda * 1e3,
+            "channel_gated_layer_roofline_frac": frac(b_layer + 4 * th * (w.K - 1), t_kda),
             "decode": dec}
 
 
