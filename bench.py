@@ -145,6 +145,13 @@ def barrier(ws):
         dist.barrier()
 
 
+def whole_job(local_seconds, tokens_per_rank_step, steps, ws):
+    """Whole-job throughput of `steps` timed steps on every rank: all ranks' tokens over the
+    slowest rank's time (max over ranks).  Returns (tokens/s, ms per step)."""
+    total_s = max_over_ranks(local_seconds, ws)
+    return tokens_per_rank_step * ws * steps / total_s, 1e3 * total_s / steps
+
+
 def max_over_ranks(x, ws):
     if ws == 1:
         return x
@@ -298,10 +305,7 @@ def run_ours(args, w):
     barrier(ws)
     binding.osdn_check()
     step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
-    total_s = max_over_ranks(sum(step_ms) / 1e3, ws)
-    tokens = B * T * ws * n
-    value = tokens / total_s
-    ms_per_step = 1e3 * total_s / n
+    value, ms_per_step = whole_job(sum(step_ms) / 1e3, B * T, n, ws)
 
     # the two separate entry points, for the per-phase breakdown (not part of the headline)
     m = min(n, 200)
