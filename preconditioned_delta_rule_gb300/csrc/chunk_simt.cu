@@ -12,8 +12,9 @@
 // fp32 rounding for any input dtype.  It serves fp32 inputs (where bf16/f16 tensor-core
 // operands could not meet a 1e-4 tolerance) and the head sizes the tensor-core kernel is not
 // built for.  Mapping: one CTA per (batch, head, 32 rows of S); each warp owns 4 rows; a row's
-// K entries are spread over the 32 lanes (E = K/32 each) and its two dot products are warp
-// butterflies.  Token t+1's operands are loaded while token t is processed.
+// K entries are spread over the 32 lanes (E = K/32 each).  Per token the dot products <S_i, k>,
+// <S_i, q> of every row and <k~, q> share one warp butterfly, and o_t = S_t q is formed as
+// <Sbar_i, q> + beta u_i <k~, q>.  Token t+1's operands are loaded while token t is processed.
 #include "common.cuh"
 
 namespace osdn {
@@ -74,24 +75,37 @@ __global__ void __launch_bounds__(256) chunk_recurrent_kernel(OsdnChunkArgs a) {
         for (int i = 0; i < E; ++i) ca[i] = al[i];
         if (t + 1 < T) load(t + 1);
         const size_t r = row0 + (size_t)t * H;
+        // <S_i, k>, <S_i, q> of the gated state and <k~, q> in one butterfly (independent sums);
+        // then S_t q = Sbar q + beta u <k~, q>, so the readout needs no second pass over S
+        float sk[kRowsPerWarp], sq[kRowsPerWarp], ktq = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) ktq = fmaf(ckt[i], cq[i], ktq);
 #pragma unroll
         for (int j = 0; j < kRowsPerWarp; ++j) {
-            float sk = 0.f;
+            sk[j] = 0.f;
+            sq[j] = 0.f;
 #pragma unroll
             for (int i = 0; i < E; ++i) {
                 S[j][i] *= ca[i];
-                sk = fmaf(S[j][i], ck[i], sk);
+                sk[j] = fmaf(S[j][i], ck[i], sk[j]);
+                sq[j] = fmaf(S[j][i], cq[i], sq[j]);
             }
-            sk = warp_sum(sk);
-            const float bu = cb * (cv[j] - sk);
-            float sq = 0.f;
+        }
 #pragma unroll
-            for (int i = 0; i < E; ++i) {
-                S[j][i] = fmaf(bu, ckt[i], S[j][i]);
-                sq = fmaf(S[j][i], cq[i], sq);
+        for (int o = 16; o > 0; o >>= 1) {
+            ktq += __shfl_xor_sync(0xffffffffu, ktq, o);
+#pragma unroll
+            for (int j = 0; j < kRowsPerWarp; ++j) {
+                sk[j] += __shfl_xor_sync(0xffffffffu, sk[j], o);
+                sq[j] += __shfl_xor_sync(0xffffffffu, sq[j], o);
             }
-            sq = warp_sum(sq);
-            if (lane == 0) og[r * V + row_base + j] = from_f32<TIn>(a.scale * sq);
+        }
+#pragma unroll
+        for (int j = 0; j < kRowsPerWarp; ++j) {
+            const float bu = cb * (cv[j] - sk[j]);
+#pragma unroll
+            for (int i = 0; i < E; ++i) S[j][i] = fmaf(bu, ckt[i], S[j][i]);
+            if (lane == 0) og[r * V + row_base + j] = from_f32<TIn>(a.scale * fmaf(bu, ktq, sq[j]));
         }
     }
 #pragma unroll
