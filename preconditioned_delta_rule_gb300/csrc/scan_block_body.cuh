@@ -795,9 +795,20 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         }
                     }
                 } else {
-                    for (int j = p + 1; j < J; ++j) {
-                        const float xn = fmaf(F[F_G + j], s_at(j, i), rr[j] * bound);
-                        if (status == 1 ? (xn > dmin) : (xn < dmax)) { viol = j; break; }
+                    // the first token after p whose step would leave the face: all 64 at once, no
+                    // early exit (g and r four at a time, so the loads pipeline)
+#pragma unroll 4
+                    for (int j4 = 0; j4 < J; j4 += 4) {
+                        const float4 g4 = *reinterpret_cast<const float4*>(F + F_G + j4);
+                        const float4 r4 = *reinterpret_cast<const float4*>(rr + j4);
+                        const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = j4 + e;
+                            const float xn = fmaf(gg[e], s_at(j, i), rv[e] * bound);
+                            const bool off = j > p && (status == 1 ? (xn > dmin) : (xn < dmax));
+                            viol = off ? min(viol, j) : viol;
+                        }
                     }
                 }
                 wg_sync(1);
