@@ -85,7 +85,8 @@ constexpr int F_GOUT = F_INT + 8;     // [2][64] final g of each token of a bloc
 constexpr int F_DST = F_GOUT + 128;   // [2][128] state at the block start, hi part (chain -> emit)
 constexpr int F_DSL = F_DST + 256;    // [2][128] state at the block start, lo part
 constexpr int F_NU = F_DSL + 256;     // [2][4] coupling bound of the block in a slot (per copy warp)
-constexpr int F_END = F_NU + 8;
+constexpr int F_NRM = F_NU + 8;       // [2][64] |k_j|^2 of the block in a slot
+constexpr int F_END = F_NRM + 128;
 constexpr uint32_t OFF_BAR = OFF_F + ((F_END * 4 + 127) / 128) * 128;
 constexpr uint32_t SMEM_BASE = OFF_BAR + 128;
 // the all-free Gram of a block (two slots), scaled and masked to l < j, fp32 rows of MROW floats
@@ -319,6 +320,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 const float bt = F[F_RAWB + (m % 3) * J + j];
                 const float bp = a.beta_aware ? bt : 1.f;
                 F[F_GAM + q * J + j] = valid ? eta * bp / fmaxf(n, eps) : 0.f;
+                F[F_NRM + q * J + j] = n;
                 F[F_BP + q * J + j] = bp;
                 F[F_RR + q * J + j] = (HAS_R && valid) ? F[F_RAWR + (m % 3) * J + j] : 1.f;
             }
@@ -628,24 +630,33 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     continue;
                 }
                 if (nfree == 0) {  // every coordinate pinned: cF = 0, cP_j = <b, s_j>
-                    F[F_BPV + i] = bound;
-                    wg_sync(1);
-                    const int j = tid >> 1, hf = tid & 1;
-                    float cpv = 0.f;
-                    if (j > p) {
-                        const float* row = sf + j * SROW;
-#pragma unroll 4
-                        for (int c = 0; c < 16; ++c) {
-                            const int ii = piece(c, hf) * 4;
-                            const float4 s4 = *reinterpret_cast<const float4*>(row + ii);
-                            const float4 b4 = *reinterpret_cast<const float4*>(F + F_BPV + ii);
-                            cpv = fmaf(b4.x, s4.x, fmaf(b4.y, s4.y, fmaf(b4.z, s4.z, fmaf(b4.w, s4.w, cpv))));
+                    const int nlow = wg_count(1, status == 1);
+                    if (nlow == KD || nlow == 0) {  // all on one face: cP_j = b |k_j|^2
+                        const float bd = nlow == KD ? dmin : dmax;
+                        if (tid < J && tid > p) {
+                            F[F_CF + tid] = 0.f;
+                            F[F_CP + tid] = bd * F[F_NRM + q * J + tid];
                         }
-                    }
-                    cpv += __shfl_xor_sync(0xffffffffu, cpv, 1);
-                    if (hf == 0 && j > p) {
-                        F[F_CF + j] = 0.f;
-                        F[F_CP + j] = cpv;
+                    } else {
+                        F[F_BPV + i] = bound;
+                        wg_sync(1);
+                        const int j = tid >> 1, hf = tid & 1;
+                        float cpv = 0.f;
+                        if (j > p) {
+                            const float* row = sf + j * SROW;
+#pragma unroll 4
+                            for (int c = 0; c < 16; ++c) {
+                                const int ii = piece(c, hf) * 4;
+                                const float4 s4 = *reinterpret_cast<const float4*>(row + ii);
+                                const float4 b4 = *reinterpret_cast<const float4*>(F + F_BPV + ii);
+                                cpv = fmaf(b4.x, s4.x, fmaf(b4.y, s4.y, fmaf(b4.z, s4.z, fmaf(b4.w, s4.w, cpv))));
+                            }
+                        }
+                        cpv += __shfl_xor_sync(0xffffffffu, cpv, 1);
+                        if (hf == 0 && j > p) {
+                            F[F_CF + j] = 0.f;
+                            F[F_CP + j] = cpv;
+                        }
                     }
                 }
                 wg_sync(1);  // F_G / F_CF / F_CP are read by other chain threads below
