@@ -86,7 +86,8 @@ constexpr int F_DST = F_GOUT + 128;   // [2][128] state at the block start, hi p
 constexpr int F_DSL = F_DST + 256;    // [2][128] state at the block start, lo part
 constexpr int F_NU = F_DSL + 256;     // [2][4] coupling bound of the block in a slot (per copy warp)
 constexpr int F_NRM = F_NU + 8;       // [2][64] |k_j|^2 of the block in a slot
-constexpr int F_END = F_NRM + 128;
+constexpr int F_SMX = F_NRM + 128;    // [2][64] max_i k_{j,i}^2 of the block in a slot
+constexpr int F_END = F_SMX + 128;
 constexpr uint32_t OFF_BAR = OFF_F + ((F_END * 4 + 127) / 128) * 128;
 constexpr uint32_t SMEM_BASE = OFF_BAR + 128;
 // the all-free Gram of a block (two slots), scaled and masked to l < j, fp32 rows of MROW floats
@@ -311,6 +312,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 }
             }
             n += __shfl_xor_sync(0xffffffffu, n, 1);
+            const float rowmx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             if ((u & 31) == 0) F[F_RED1 + (u >> 5)] = mx;
@@ -321,6 +323,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 const float bp = a.beta_aware ? bt : 1.f;
                 F[F_GAM + q * J + j] = valid ? eta * bp / fmaxf(n, eps) : 0.f;
                 F[F_NRM + q * J + j] = n;
+                F[F_SMX + q * J + j] = rowmx;
                 F[F_BP + q * J + j] = bp;
                 F[F_RR + q * J + j] = (HAS_R && valid) ? F[F_RAWR + (m % 3) * J + j] : 1.f;
             }
@@ -629,8 +632,10 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     clipped = true;
                     continue;
                 }
+                bool all_low = false;  // every coordinate clipped at d_min
                 if (nfree == 0) {  // every coordinate pinned: cF = 0, cP_j = <b, s_j>
                     const int nlow = wg_count(1, status == 1);
+                    all_low = nlow == KD;
                     if (nlow == KD || nlow == 0) {  // all on one face: cP_j = b |k_j|^2
                         const float bd = nlow == KD ? dmin : dmax;
                         if (tid < J && tid > p) {
@@ -805,6 +810,24 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                             if (v < dmin || v > dmax) { viol = j; break; }
                         }
                     }
+                } else if (all_low) {
+                    // every coordinate on d_min: for g_j > 0 the step r_j d_min + g_j s_j is
+                    // largest at the largest s_j (fmaf is monotone in s), so that coordinate decides
+                    // exactly; for g_j <= 0 the step is at most r_j d_min (a gate above 1 counts as
+                    // leaving; the sweeps then take the rest of the block).  The same for every
+                    // thread: each lane checks two tokens, then a warp minimum.
+                    const int lane = tid & 31;
+                    int v = J;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int j = 2 * lane + e;
+                        const float g = F[F_G + j], c = rr[j] * dmin;
+                        const bool off = j > p && (g > 0.f ? fmaf(g, F[F_SMX + q * J + j], c) > dmin : c > dmin);
+                        v = off ? min(v, j) : v;
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+                    viol = v;
                 } else {
                     // the first token after p whose step would leave the face: all 64 at once, no
                     // early exit (g and r four at a time, so the loads pipeline)
