@@ -14,7 +14,10 @@
 // The step is HBM-bound: S (V x K fp32) is read once and written once.  One CTA of 256 threads
 // per head; 8 lanes per row, each lane holding 4-float pieces interleaved so that every load
 // and store instruction of a warp covers four full 128-byte row segments.  All rows of a
-// thread are loaded before any is used so that each thread keeps its loads in flight together.
+// thread are loaded before any is used, and before the phase-1 step, so that each thread keeps its
+// loads in flight together and their latency overlaps the step's.  The per-column vectors (k, k~,
+// q and the gate) sit in shared memory and are read at use, which keeps the kernel within the 128
+// registers a thread that two resident CTAs per SM allow.
 #include "common.cuh"
 
 namespace osdn {
@@ -36,25 +39,46 @@ __device__ __forceinline__ void st_stream(float* p, float4 v) {
 
 // RMODE: 0 no retention, 1 one per head (Eq. (7)), 2 one per key coordinate (diag(r_t), Appendix A.5)
 template <int K, int V, typename TIn, int RMODE>
-__global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(OsdnDecodeArgs a) {
     constexpr int P4 = K / 4 / kLanesPerRow;        // float4 pieces per lane per row (4 or 2)
     constexpr int ROWS_PER_PASS = kThreads / kLanesPerRow;  // 32
     constexpr int PASSES = V / ROWS_PER_PASS;        // 4 or 2
     constexpr int E = K / 32;
-    __shared__ __align__(16) float sk[K], skt[K], sq[K];
+    // sk, sq: k and scale * q with the state gate of their column folded in (<alpha o S_i, k> =
+    // <S_i, alpha o k>); sga: the gate of each column (1 without one); skt: k~
+    __shared__ __align__(16) float sk[K], skt[K], sq[K], sga[K];
     __shared__ float scoef[2];
 
     const int tid = threadIdx.x;
     const size_t bh = blockIdx.x;
     float* S = a.S + bh * (size_t)V * K;
+    const int sub = tid % kLanesPerRow;
+    const int rg = tid / kLanesPerRow;
+
+    // The state does not depend on the phase-1 step: its loads go out first, so that their latency
+    // overlaps the step's own loads and reductions.
+    float4 Sr[PASSES][P4];
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+        const int row = ps * ROWS_PER_PASS + rg;
+#pragma unroll
+        for (int c = 0; c < P4; ++c) Sr[ps][c] = ld_stream(S + (size_t)row * K + (c * kLanesPerRow + sub) * 4);
+    }
 
     if (tid < 32) {  // warp 0: phase-1 step of this head, and the shared vectors
         const TIn* kp = static_cast<const TIn*>(a.k) + bh * K + tid * E;
         const TIn* qp = static_cast<const TIn*>(a.q) + bh * K + tid * E;
-        float kv[E], qv[E], dv[E];
+        float kv[E], qv[E], dv[E], gv[E];
         VecIO<TIn, E>::load(kp, kv);
         VecIO<TIn, E>::load(qp, qv);
         VecIO<float, E>::load(a.d + bh * K + tid * E, dv);
+        if (a.alpha && a.alpha_per_key) {
+            VecIO<float, E>::load(a.alpha + bh * K + tid * E, gv);
+        } else {
+            const float g1 = a.alpha ? a.alpha[bh] : 1.f;
+#pragma unroll
+            for (int i = 0; i < E; ++i) gv[i] = g1;
+        }
         float n = 0.f, al = 0.f, ktq = 0.f, s[E];
 #pragma unroll
         for (int i = 0; i < E; ++i) {
@@ -64,9 +88,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
             const float kt = dv[i] * kv[i];
             const float qs = a.scale * qv[i];
             ktq = fmaf(kt, qs, ktq);
-            sk[tid * E + i] = kv[i];
+            sk[tid * E + i] = gv[i] * kv[i];
             skt[tid * E + i] = kt;
-            sq[tid * E + i] = qs;
+            sq[tid * E + i] = gv[i] * qs;
+            sga[tid * E + i] = gv[i];
         }
         n = warp_sum(n);
         al = warp_sum(al);
@@ -92,35 +117,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
     }
     __syncthreads();
 
-    const int sub = tid % kLanesPerRow;
-    const int rg = tid / kLanesPerRow;
-    float kr[P4][4], ktr[P4][4], qr[P4][4];
-#pragma unroll
-    for (int c = 0; c < P4; ++c) {
-        const int col = (c * kLanesPerRow + sub) * 4;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            kr[c][j] = sk[col + j];
-            ktr[c][j] = skt[col + j];
-            qr[c][j] = sq[col + j];
-        }
-    }
     const float bt = scoef[0], bktq = scoef[1];
-    // state gate of this thread's columns: one per head, one per key channel, or 1
-    float ga[P4][4];
-#pragma unroll
-    for (int c = 0; c < P4; ++c)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            ga[c][j] = !a.alpha ? 1.f : (a.alpha_per_key ? a.alpha[bh * K + (c * kLanesPerRow + sub) * 4 + j] : a.alpha[bh]);
-
-    float4 Sr[PASSES][P4];
-#pragma unroll
-    for (int ps = 0; ps < PASSES; ++ps) {
-        const int row = ps * ROWS_PER_PASS + rg;
-#pragma unroll
-        for (int c = 0; c < P4; ++c) Sr[ps][c] = ld_stream(S + (size_t)row * K + (c * kLanesPerRow + sub) * 4);
-    }
     const TIn* vp = static_cast<const TIn*>(a.v) + bh * V;
     TIn* op = static_cast<TIn*>(a.o) + bh * V;
 #pragma unroll
@@ -129,13 +126,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
         float dk = 0.f, dq = 0.f;
 #pragma unroll
         for (int c = 0; c < P4; ++c) {
-            Sr[ps][c].x *= ga[c][0];
-            Sr[ps][c].y *= ga[c][1];
-            Sr[ps][c].z *= ga[c][2];
-            Sr[ps][c].w *= ga[c][3];
+            const int col = (c * kLanesPerRow + sub) * 4;
             const float4 x = Sr[ps][c];
-            dk = fmaf(x.x, kr[c][0], fmaf(x.y, kr[c][1], fmaf(x.z, kr[c][2], fmaf(x.w, kr[c][3], dk))));
-            dq = fmaf(x.x, qr[c][0], fmaf(x.y, qr[c][1], fmaf(x.z, qr[c][2], fmaf(x.w, qr[c][3], dq))));
+            const float4 kk = *reinterpret_cast<const float4*>(sk + col);
+            const float4 qq = *reinterpret_cast<const float4*>(sq + col);
+            dk = fmaf(x.x, kk.x, fmaf(x.y, kk.y, fmaf(x.z, kk.z, fmaf(x.w, kk.w, dk))));
+            dq = fmaf(x.x, qq.x, fmaf(x.y, qq.y, fmaf(x.z, qq.z, fmaf(x.w, qq.w, dq))));
         }
 #pragma unroll
         for (int o = kLanesPerRow / 2; o > 0; o >>= 1) {
@@ -146,12 +142,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(OsdnDecodeArgs a) {
         const float bu = bt * u;
 #pragma unroll
         for (int c = 0; c < P4; ++c) {
+            const int col = (c * kLanesPerRow + sub) * 4;
+            const float4 kt = *reinterpret_cast<const float4*>(skt + col);
+            const float4 ga = *reinterpret_cast<const float4*>(sga + col);
             float4 x = Sr[ps][c];
-            x.x = fmaf(bu, ktr[c][0], x.x);
-            x.y = fmaf(bu, ktr[c][1], x.y);
-            x.z = fmaf(bu, ktr[c][2], x.z);
-            x.w = fmaf(bu, ktr[c][3], x.w);
-            st_stream(S + (size_t)row * K + (c * kLanesPerRow + sub) * 4, x);
+            x.x = fmaf(bu, kt.x, ga.x * x.x);
+            x.y = fmaf(bu, kt.y, ga.y * x.y);
+            x.z = fmaf(bu, kt.z, ga.z * x.z);
+            x.w = fmaf(bu, kt.w, ga.w * x.w);
+            st_stream(S + (size_t)row * K + col, x);
         }
         if (sub == 0) op[row] = from_f32<TIn>(fmaf(bktq, u, dq));
     }
