@@ -14,10 +14,12 @@
 // The step is HBM-bound: S (V x K fp32) is read once and written once.  One CTA of 256 threads
 // per head; 8 lanes per row, each lane holding 4-float pieces interleaved so that every load
 // and store instruction of a warp covers four full 128-byte row segments.  All rows of a
-// thread are loaded before any is used, and before the phase-1 step, so that each thread keeps its
-// loads in flight together and their latency overlaps the step's.  The per-column vectors (k, k~,
-// q and the gate) sit in shared memory and are read at use, which keeps the kernel within the 128
-// registers a thread that two resident CTAs per SM allow.
+// thread are loaded before any is used, and before the phase-1 step is computed (only that step's
+// own operands are requested earlier), so that each thread keeps its loads in flight together and
+// their latency overlaps the step's.  k and q (with the
+// gate folded in) are held in registers; k~ and the gate are read from shared memory in the store
+// loop, which keeps the kernel within the 128 registers a thread that two resident CTAs per SM
+// allow.
 #include "common.cuh"
 
 namespace osdn {
@@ -55,8 +57,30 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(OsdnDecodeArgs a) {
     const int sub = tid % kLanesPerRow;
     const int rg = tid / kLanesPerRow;
 
-    // The state does not depend on the phase-1 step: its loads go out first, so that their latency
-    // overlaps the step's own loads and reductions.
+    // Warp 0's operands of the phase-1 step are loaded first, then every thread's slice of the
+    // state (which does not depend on the step), so that the step's loads do not queue behind the
+    // state's and its latency overlaps theirs.
+    float kv[E], qv[E], dv[E], gv[E], rv[E], bt0 = 0.f;
+    if (tid < 32) {
+        VecIO<TIn, E>::load(static_cast<const TIn*>(a.k) + bh * K + tid * E, kv);
+        VecIO<TIn, E>::load(static_cast<const TIn*>(a.q) + bh * K + tid * E, qv);
+        VecIO<float, E>::load(a.d + bh * K + tid * E, dv);
+        if (a.alpha && a.alpha_per_key) {
+            VecIO<float, E>::load(a.alpha + bh * K + tid * E, gv);
+        } else {
+            const float g1 = a.alpha ? a.alpha[bh] : 1.f;
+#pragma unroll
+            for (int i = 0; i < E; ++i) gv[i] = g1;
+        }
+        if (RMODE == 2) {
+            VecIO<float, E>::load(a.r + bh * K + tid * E, rv);
+        } else {
+            const float r1 = RMODE == 1 ? a.r[bh] : 1.f;
+#pragma unroll
+            for (int i = 0; i < E; ++i) rv[i] = r1;
+        }
+        bt0 = a.beta[bh];
+    }
     float4 Sr[PASSES][P4];
 #pragma unroll
     for (int ps = 0; ps < PASSES; ++ps) {
@@ -66,19 +90,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(OsdnDecodeArgs a) {
     }
 
     if (tid < 32) {  // warp 0: phase-1 step of this head, and the shared vectors
-        const TIn* kp = static_cast<const TIn*>(a.k) + bh * K + tid * E;
-        const TIn* qp = static_cast<const TIn*>(a.q) + bh * K + tid * E;
-        float kv[E], qv[E], dv[E], gv[E];
-        VecIO<TIn, E>::load(kp, kv);
-        VecIO<TIn, E>::load(qp, qv);
-        VecIO<float, E>::load(a.d + bh * K + tid * E, dv);
-        if (a.alpha && a.alpha_per_key) {
-            VecIO<float, E>::load(a.alpha + bh * K + tid * E, gv);
-        } else {
-            const float g1 = a.alpha ? a.alpha[bh] : 1.f;
-#pragma unroll
-            for (int i = 0; i < E; ++i) gv[i] = g1;
-        }
         float n = 0.f, al = 0.f, ktq = 0.f, s[E];
 #pragma unroll
         for (int i = 0; i < E; ++i) {
@@ -96,28 +107,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(OsdnDecodeArgs a) {
         n = warp_sum(n);
         al = warp_sum(al);
         ktq = warp_sum(ktq);
-        const float bt = a.beta[bh];
-        float rv[E];
-        if (RMODE == 2) {
-            VecIO<float, E>::load(a.r + bh * K + tid * E, rv);
-        } else {
-#pragma unroll
-            for (int i = 0; i < E; ++i) rv[i] = RMODE == 1 ? a.r[bh] : 1.f;
-        }
-        const float bp = a.beta_aware ? bt : 1.f;
+        const float bp = a.beta_aware ? bt0 : 1.f;
         const float g = a.eta * bp * (1.f - bp * al) / fmaxf(n, a.eps);
         float dn[E];
 #pragma unroll
         for (int i = 0; i < E; ++i) dn[i] = fminf(fmaxf(fmaf(g, s[i], rv[i] * dv[i]), a.d_min), a.d_max);
         VecIO<float, E>::store(a.d + bh * K + tid * E, dn);
         if (tid == 0) {
-            scoef[0] = bt;
-            scoef[1] = bt * ktq;
+            scoef[0] = bt0;
+            scoef[1] = bt0 * ktq;
         }
     }
     __syncthreads();
 
     const float bt = scoef[0], bktq = scoef[1];
+    float4 kr[P4], qr[P4];
+#pragma unroll
+    for (int c = 0; c < P4; ++c) {
+        const int col = (c * kLanesPerRow + sub) * 4;
+        kr[c] = *reinterpret_cast<const float4*>(sk + col);
+        qr[c] = *reinterpret_cast<const float4*>(sq + col);
+    }
     const TIn* vp = static_cast<const TIn*>(a.v) + bh * V;
     TIn* op = static_cast<TIn*>(a.o) + bh * V;
 #pragma unroll
@@ -126,10 +136,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(OsdnDecodeArgs a) {
         float dk = 0.f, dq = 0.f;
 #pragma unroll
         for (int c = 0; c < P4; ++c) {
-            const int col = (c * kLanesPerRow + sub) * 4;
             const float4 x = Sr[ps][c];
-            const float4 kk = *reinterpret_cast<const float4*>(sk + col);
-            const float4 qq = *reinterpret_cast<const float4*>(sq + col);
+            const float4 kk = kr[c];
+            const float4 qq = qr[c];
             dk = fmaf(x.x, kk.x, fmaf(x.y, kk.y, fmaf(x.z, kk.z, fmaf(x.w, kk.w, dk))));
             dq = fmaf(x.x, qq.x, fmaf(x.y, qq.y, fmaf(x.z, qq.z, fmaf(x.w, qq.w, dq))));
         }
