@@ -62,8 +62,8 @@ def layer_bytes(w):
 # kernels behind it change, until they are captured again.
 NCU_TRAFFIC = {
     "layer_340m": {
-        # layer_scan_prep_kernel 68.17 + 51.40 MB, chunk_chain_kernel 167.86 + 21.36 MB
-        "osdn_layer_fwd": 308.79e6,
+        # layer_scan_prep_kernel 68.06 + 50.65 MB, chunk_chain_kernel 167.88 + 21.52 MB
+        "osdn_layer_fwd": 308.11e6,
     },
 }
 
