@@ -21,10 +21,12 @@
  *                      generation time (the pages' single-token kernel, Appendix L).
  *   osdn_layer_fwd     osdn_precond_scan then osdn_chunk_fwd on its write keys (the pages'
  *                      chunk_osdn, Listing 1), with the two phases overlapped on the GPU.
+ *   osdn_layer_fwd_host the same from HOST buffers, the copies overlapped with the compute.
  *
  * Conventions shared by every call
- *   - Every buffer is caller-owned DEVICE memory (cudaMalloc or equivalent); the library never
- *     allocates, frees or keeps pointers after the call returns.
+ *   - Every buffer is caller-owned DEVICE memory (cudaMalloc or equivalent; osdn_layer_fwd_host's
+ *     inputs and outputs are the one exception, host memory); the library never allocates device
+ *     memory, frees, or keeps pointers after the call returns.
  *   - Layouts are dense row-major: q, k, k~ [B,T,H,K]; v, o [B,T,H,V]; beta, r [B,T,H];
  *     S [B,H,V,K] (value-major: S[b,h,i,j] multiplies key coordinate j); d [B,H,K].
  *     Decode drops T: q, k [B,H,K]; v, o [B,H,V]; beta, r [B,H].
@@ -206,6 +208,50 @@ osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, o
  * invalid arguments. */
 size_t osdn_layer_fwd_varlen_workspace_bytes(int N, int max_len, int H, int K, int V, int chunk, osdn_dtype dtype,
                                              int r_mode, int gated);
+
+/*
+ * The layer forward on HOST buffers (the pages' chunk_osdn, Listing 1, as one call from host
+ * memory), with the copies overlapped with the compute.  Algorithm 1 and Eqs. (2), (4), (7) are
+ * recurrences over the token axis that carry only (d, S), so the call splits the sequence into
+ * `segments` consecutive pieces of T / segments tokens and runs osdn_layer_fwd on piece i from
+ * piece i-1's final (d, S), kept on the device.  Piece i+1's inputs are copied in on `h2d_stream`
+ * while piece i computes on `stream`, and piece i's o is copied out on `d2h_stream` meanwhile.
+ *   q, k, v, beta, r, alpha, d0, S0
+ *            HOST arrays, layouts and meaning as osdn_layer_fwd (NULL d0 / S0: ones / zeros; NULL
+ *            r / alpha: none).  They must stay unchanged until the call's work on `stream` is
+ *            complete.  Page-locked memory lets the copies overlap the compute; pageable memory
+ *            gives the same results without the overlap.
+ *   o, S_out, d_out
+ *            HOST arrays [B,T,H,V] (dtype), [B,H,V,K] and [B,H,K] fp32 (written; valid once
+ *            `stream` has completed the call's work).  The write keys are not returned.
+ *   segments number of pieces; T / segments must be a whole number of chunks (OSDN_ERR_SHAPE
+ *            otherwise; segments <= 0: OSDN_ERR_ARG).  1 runs copy-in, compute, copy-out in turn.
+ *            Each piece boundary rounds the carried d to fp32 once (within the call d is carried
+ *            as an fp32 pair), so results can differ from one osdn_layer_fwd call in the last bits.
+ *   workspace, workspace_bytes
+ *            required caller-owned DEVICE scratch, 256-byte aligned (OSDN_ERR_ALIGN otherwise), of
+ *            at least osdn_layer_fwd_host_workspace_bytes(...) bytes (OSDN_ERR_ARG otherwise):
+ *            two (d, S) state buffers, two staging slots of one piece's inputs and outputs, and
+ *            the per-piece layer workspace.
+ *   stream, h2d_stream, d2h_stream
+ *            the compute stream and two copy streams (NULL copy streams mean `stream`: correct,
+ *            without overlap).  Work queued on `stream` before the call comes first; everything the
+ *            call queues is complete once `stream` reaches the point after the call.
+ * T = 0 waits for `stream`, then writes d_out = d0 (or ones) and S_out = S0 (or zeros) on the
+ * host.  Errors: the argument checks of osdn_layer_fwd, then OSDN_ERR_CUDA if a copy or an event
+ * call fails.
+ */
+osdn_status osdn_layer_fwd_host(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
+                                const float* r, int r_per_key, const float* alpha, int alpha_per_key,
+                                const float* d0, const float* S0, void* o, float* S_out, float* d_out, int B,
+                                int T, int H, int K, int V, int chunk, float eta, float d_min, float d_max,
+                                float eps, float scale, int beta_aware, int segments, void* workspace,
+                                size_t workspace_bytes, void* stream, void* h2d_stream, void* d2h_stream);
+
+/* Device workspace size for osdn_layer_fwd_host: r_mode 0 / 1 / 2 and gated 0 / 1 / 2 as for
+ * osdn_layer_fwd_varlen_workspace_bytes.  0 for invalid arguments (including T = 0). */
+size_t osdn_layer_fwd_host_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype,
+                                           int r_mode, int gated, int segments);
 
 /*
  * The layer backward: gradients of a loss through osdn_layer_fwd's outputs o, S_out and d_out

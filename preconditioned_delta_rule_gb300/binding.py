@@ -63,6 +63,11 @@ def lib() -> ctypes.CDLL:
     L.osdn_layer_fwd_varlen.restype = ctypes.c_int
     L.osdn_layer_fwd_varlen_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i]
     L.osdn_layer_fwd_varlen_workspace_bytes.restype = sz
+    L.osdn_layer_fwd_host.argtypes = [vp, vp, vp, i, fp, fp, i, fp, i, fp, fp, vp, fp, fp, i, i, i, i, i, i,
+                                      f, f, f, f, f, i, i, vp, sz, vp, vp, vp]
+    L.osdn_layer_fwd_host.restype = ctypes.c_int
+    L.osdn_layer_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i, i]
+    L.osdn_layer_fwd_host_workspace_bytes.restype = sz
     L.osdn_layer_bwd.argtypes = [vp, vp, vp, i, fp, fp, i, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
                                  i, i, i, i, i, f, f, f, f, f, i, vp, sz, vp]
     L.osdn_layer_bwd.restype = ctypes.c_int
@@ -102,12 +107,19 @@ def _stream(device, stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+_HOST = object()  # device argument of _check for host (CPU) arrays
+
+
 def _check(name, t, shape, dtype=None, device=None):
     if t is None:
         return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
+    if device is _HOST:  # the host-buffer entry point's arrays
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host (CPU) tensor")
+        device = torch.device("cpu")
+    elif not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
     if device is not None and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
@@ -325,6 +337,73 @@ def osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk=64, dtype=t
     """gated: 0 no state gate, 1 one per head, 2 one per key channel."""
     return int(lib().osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk, _code(dtype), int(r_mode),
                                                            int(gated)))
+
+
+_COPY_STREAMS = {}
+
+
+def _copy_streams(device):
+    """The two copy streams osdn_layer_fwd_host overlaps with the compute, one pair per device."""
+    s = _COPY_STREAMS.get(device)
+    if s is None:
+        s = (torch.cuda.Stream(device), torch.cuda.Stream(device))
+        _COPY_STREAMS[device] = s
+    return s
+
+
+def osdn_layer_fwd_host_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16, r_mode=0, gated=0,
+                                        segments=4) -> int:
+    return int(lib().osdn_layer_fwd_host_workspace_bytes(B, T, H, K, V, chunk, _code(dtype), r_mode, gated,
+                                                         segments))
+
+
+def osdn_layer_fwd_host(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, o=None, S_out=None, d_out=None,
+                        segments=4, chunk=64, eta=0.003, d_min=0.5, d_max=2.0, eps=1e-6, scale=1.0,
+                        beta_aware=True, device=None, workspace=None, stream=None, synchronize=True):
+    """The layer forward (both phases, the pages' chunk_osdn) from HOST tensors: the sequence runs
+    as ``segments`` consecutive pieces whose input copies overlap the previous piece's compute,
+    with (d, S) carried on the device.  q, k [B,T,H,K], v [B,T,H,V], beta [B,T,H], r [B,T,H] or
+    [B,T,H,K], alpha [B,T,H] or [B,T,H,K], d0 [B,H,K], S0 [B,H,V,K]: CPU tensors (page-locked for
+    the overlap).  Returns CPU tensors (o, S_out, d_out), page-locked when allocated here.  With
+    ``synchronize`` False the outputs are valid once ``stream`` has passed the call, and the
+    inputs must stay unchanged until then."""
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    dt = k.dtype
+    cpu = _HOST
+    for name, t, shp in (("q", q, (B, T, H, K)), ("k", k, (B, T, H, K)), ("v", v, (B, T, H, V))):
+        _check(name, t, shp, dt, cpu)
+    _check("beta", beta, (B, T, H), torch.float32, cpu)
+    r_per_key = _retention(r, (B, T, H), K, cpu)
+    a_per_key = _state_gate(alpha, (B, T, H), K, cpu)
+    _check("d0", d0, (B, H, K), torch.float32, cpu)
+    _check("S0", S0, (B, H, V, K), torch.float32, cpu)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if o is None:
+        o = torch.empty((B, T, H, V), dtype=dt, pin_memory=True)
+    if S_out is None:
+        S_out = torch.empty((B, H, V, K), dtype=torch.float32, pin_memory=True)
+    if d_out is None:
+        d_out = torch.empty((B, H, K), dtype=torch.float32, pin_memory=True)
+    _check("o", o, (B, T, H, V), dt, cpu)
+    _check("S_out", S_out, (B, H, V, K), torch.float32, cpu)
+    _check("d_out", d_out, (B, H, K), torch.float32, cpu)
+    r_mode = 0 if r is None else (2 if r_per_key else 1)
+    g_mode = 0 if alpha is None else (2 if a_per_key else 1)
+    need = osdn_layer_fwd_host_workspace_bytes(B, T, H, K, V, chunk, dt, r_mode, g_mode, segments) if T > 0 else 0
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "host")
+    h2d, d2h = _copy_streams(dev)
+    st = lib().osdn_layer_fwd_host(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key,
+                                   _ptr(alpha), a_per_key, _ptr(d0), _ptr(S0), _ptr(o), _ptr(S_out), _ptr(d_out),
+                                   B, T, H, K, V, int(chunk), float(eta),
+                                   float(-math.inf if d_min is None else d_min),
+                                   float(math.inf if d_max is None else d_max), float(eps), float(scale),
+                                   int(bool(beta_aware)), int(segments), ws_ptr, ws_bytes, _stream(dev, stream),
+                                   ctypes.c_void_p(h2d.cuda_stream), ctypes.c_void_p(d2h.cuda_stream))
+    _raise("osdn_layer_fwd_host", st)
+    if synchronize:
+        (stream if stream is not None else torch.cuda.current_stream(dev)).synchronize()
+    return o, S_out, d_out
 
 
 def osdn_layer_fwd_varlen(q, k, v, beta, cu_seqlens, *, max_len=None, r=None, alpha=None, d0=None, S0=None,

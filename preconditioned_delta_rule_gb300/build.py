@@ -16,7 +16,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libosdn.so"
-SOURCES = ["api.cu", "scan.cu", "scan_block.cu", "decode.cu", "chunk_simt.cu", "chunk_tc.cu", "chunk_static_ws.cu", "varlen.cu", "bwd.cu"]
+SOURCES = ["api.cu", "scan.cu", "scan_block.cu", "decode.cu", "chunk_simt.cu", "chunk_tc.cu", "chunk_static_ws.cu", "varlen.cu", "bwd.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

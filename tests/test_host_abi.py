@@ -202,3 +202,49 @@ def test_varlen_workspace_size_query(L):
     assert f(N, 300, H, 128, 128, 64, 1, 3, 0) == 0
     assert f(N, 300, H, 128, 128, 64, 1, 0, 2) == up(pad + up(rows * H * 128 * 4)) + lay(N, Tp, H, 128, 128, 64, 1)
     assert f(N, 300, H, 128, 128, 64, 1, 0, 3) == 0
+
+
+def host_layer(L, **kw):
+    a = dict(q=A, k=A, v=A, dt=1, beta=A, r=None, rpk=0, alpha=None, apk=0, d0=None, S0=None, o=A, Sout=A, dout=A,
+             B=2, T=256, H=2, K=128, V=128, C=64, eta=0.003, dmin=0.5, dmax=2.0, eps=1e-6, scale=1.0, ba=1, seg=4,
+             ws=ctypes.c_void_p(1 << 20), wsb=1 << 40)
+    a.update(kw)
+    return L.osdn_layer_fwd_host(a["q"], a["k"], a["v"], a["dt"], a["beta"], a["r"], a["rpk"], a["alpha"], a["apk"],
+                                 a["d0"], a["S0"], a["o"], a["Sout"], a["dout"], a["B"], a["T"], a["H"], a["K"],
+                                 a["V"], a["C"], a["eta"], a["dmin"], a["dmax"], a["eps"], a["scale"], a["ba"],
+                                 a["seg"], a["ws"], a["wsb"], None, None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(seg=0), ARG), (dict(seg=3), SHAPE), (dict(seg=8), SHAPE), (dict(T=100, seg=1), SHAPE),
+    (dict(ws=None), ARG), (dict(wsb=1024), ARG), (dict(ws=ctypes.c_void_p((1 << 20) + 128)), ALIGN),
+    (dict(q=None), ARG), (dict(Sout=None), ARG), (dict(K=96), UNSUP), (dict(C=32), UNSUP), (dict(dt=9), DTYPE),
+    (dict(rpk=2), ARG), (dict(apk=2), ARG), (dict(dmin=3.0), ARG), (dict(eta=math.nan), ARG), (dict(B=-1), SHAPE),
+    (dict(B=0), OK), (dict(H=0), OK),
+])
+def test_host_layer_validation(L, kw, want):
+    """Every argument error is returned before any CUDA call (host buffers need no alignment)."""
+    assert host_layer(L, **kw) == want
+
+
+def test_host_layer_workspace_size_query(L):
+    f = L.osdn_layer_fwd_host_workspace_bytes
+    lay = L.osdn_layer_fwd_workspace_bytes
+    up = lambda x: (x + 255) // 256 * 256
+    B, T, H, seg = 8, 2048, 8, 4
+    rows = B * (T // seg) * H
+    state = 2 * (up(B * H * 128 * 4) + up(B * H * 128 * 128 * 4))
+    slot = 5 * up(rows * 128 * 2) + up(rows * 4)  # q, k, v, k~, o and beta
+    assert f(B, T, H, 128, 128, 64, 1, 0, 0, seg) == state + 2 * slot + lay(B, T // seg, H, 128, 128, 64, 1)
+    assert f(B, T, H, 128, 128, 64, 1, 2, 1, seg) == (state + 2 * (slot + up(rows * 128 * 4) + up(rows * 4))
+                                                      + lay(B, T // seg, H, 128, 128, 64, 1))
+    assert f(B, T, H, 128, 128, 64, 1, 0, 0, 3) == 0      # 2048 / 3 is not whole
+    assert f(B, T, H, 128, 128, 64, 1, 0, 0, 64) == 0     # 32 tokens: not a whole chunk
+    assert f(B, 0, H, 128, 128, 64, 1, 0, 0, 1) == 0
+    assert f(B, T, H, 128, 128, 64, 1, 3, 0, seg) == 0
+
+
+def test_host_binding_rejects_device_side_arguments(L):
+    k = torch.zeros(1, 64, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="shape"):
+        binding.osdn_layer_fwd_host(k, k, k, torch.zeros(1, 64, 2))
