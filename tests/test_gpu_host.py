@@ -89,3 +89,19 @@ def test_no_tokens_returns_the_start_state():
                                   inp["S0"], segments=1)
     assert o.shape[1] == 0
     assert torch.equal(S, inp["S0"]) and torch.equal(d, inp["d0"])
+
+
+@pytest.mark.parametrize("name,segments", [("layer_340m", 4), ("layer_1p3b_apf", 4)])
+def test_host_layer_full_size(name, segments):
+    """The host-buffer call as the bench times it (full workload, seeded inputs, pinned buffers)
+    against the oracle's forward."""
+    w = W.WORKLOADS[name]
+    inp = W.make_prefill(w)
+    x = pinned(inp)
+    o, S, d = osdn_layer_fwd_host(x["q"], x["k"], x["v"], x["beta"], x["r"], segments=segments, eta=w.eta,
+                                  d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+    ref = oracle.osdn_forward(inp["q"], inp["k"], inp["v"], inp["beta"], inp["r"], eta=w.eta, d_min=w.d_min,
+                              d_max=w.d_max, eps=w.eps)
+    assert_rel(d, ref["d"], 1e-5, what=f"{name} d")
+    assert_maxabs(o, ref["o"], 2e-2, what=f"{name} o")
+    assert_maxabs(S, ref["S"], 2e-2, what=f"{name} S")
