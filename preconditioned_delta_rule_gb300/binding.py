@@ -178,7 +178,7 @@ def osdn_precond_scan(k, beta, r=None, d0=None, *, k_tilde=None, kt_dtype=None, 
         d_out = torch.empty((B, H, K), device=dev, dtype=torch.float32)
     _check("d_out", d_out, (B, H, K), torch.float32, dev)
     need = osdn_precond_scan_workspace_bytes(B, T, H, K, k.dtype)
-    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "scan")
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "scan", stream)
     st = lib().osdn_precond_scan(_ptr(k), _code(k.dtype), _ptr(beta), _ptr(r), r_per_key, _ptr(d0),
                                  _ptr(k_tilde), _code(k_tilde.dtype), _ptr(d_out), B, T, H, K,
                                  float(eta), float(d_min), float(d_max), float(eps),
@@ -198,21 +198,26 @@ def osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16
     return int(lib().osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, _code(dtype)))
 
 
-def _workspace(device, nbytes, role):
-    """A cached uint8 device buffer of at least nbytes per (device, role): torch allocates, the
-    library never does.  The scan and the chunk forward keep separate buffers so that a scan
-    on one stream never shares scratch with a chunk forward on another."""
-    buf = _WS_CACHE.get((device, role))
+def _workspace(device, nbytes, role, stream=None):
+    """A cached uint8 device buffer of at least nbytes per (device, role, stream): torch
+    allocates, the library never does.  Calls on one stream run in order, so they can share a
+    buffer; each entry point and each stream has its own, so that no two calls that may run at
+    the same time on the GPU share scratch."""
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (device, role, s.cuda_stream)
+    buf = _WS_CACHE.get(key)
     if buf is None or buf.numel() < nbytes:
+        if buf is not None:  # the old buffer may still be in use by work queued on s
+            buf.record_stream(s)
         buf = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
-        _WS_CACHE[(device, role)] = buf
+        _WS_CACHE[key] = buf
     return buf
 
 
-def _resolve_workspace(workspace, device, need, role):
+def _resolve_workspace(workspace, device, need, role, stream=None):
     """(pointer, bytes) for a workspace argument: None = cached buffer, False = none, else a tensor."""
     if workspace is None:
-        ws = _workspace(device, need, role) if need else None
+        ws = _workspace(device, need, role, stream) if need else None
     elif workspace is False:
         ws = None
     else:
@@ -247,7 +252,7 @@ def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, alpha=None, o=None, S_out
         S_out = torch.empty((B, H, V, K), device=dev, dtype=torch.float32)
     _check("S_out", S_out, (B, H, V, K), torch.float32, dev)
     need = osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 else 0
-    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "chunk")
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "chunk", stream)
     st = lib().osdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(k_tilde), _ptr(v), _code(dt), _ptr(beta),
                               _ptr(alpha), a_per_key, _ptr(S0), _ptr(o), _ptr(S_out), B, T, H, K, V, int(chunk),
                               float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
@@ -321,7 +326,7 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, k_til
         d_out = torch.empty((B, H, K), device=dev, dtype=torch.float32)
     _check("d_out", d_out, (B, H, K), torch.float32, dev)
     need = osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 and T % chunk == 0 else 0
-    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "layer")
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "layer", stream)
     st = lib().osdn_layer_fwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, _ptr(alpha),
                               a_per_key, _ptr(d0),
                               _ptr(S0), _ptr(k_tilde), _ptr(o), _ptr(S_out), _ptr(d_out), B, T, H, K,
@@ -391,7 +396,7 @@ def osdn_layer_fwd_host(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, 
     r_mode = 0 if r is None else (2 if r_per_key else 1)
     g_mode = 0 if alpha is None else (2 if a_per_key else 1)
     need = osdn_layer_fwd_host_workspace_bytes(B, T, H, K, V, chunk, dt, r_mode, g_mode, segments) if T > 0 else 0
-    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "host")
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "host", stream)
     h2d, d2h = _copy_streams(dev)
     st = lib().osdn_layer_fwd_host(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key,
                                    _ptr(alpha), a_per_key, _ptr(d0), _ptr(S0), _ptr(o), _ptr(S_out), _ptr(d_out),
@@ -454,7 +459,7 @@ def osdn_layer_fwd_varlen(q, k, v, beta, cu_seqlens, *, max_len=None, r=None, al
     need = osdn_layer_fwd_varlen_workspace_bytes(N, max_len, H, K, V, chunk, dt, r_mode, g_mode) if N else 0
     if workspace is False:
         raise ValueError("osdn_layer_fwd_varlen needs a workspace")
-    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "varlen")
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "varlen", stream)
     st = lib().osdn_layer_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, _ptr(alpha),
                                      a_per_key, _ptr(cu_seqlens), N, int(total), int(max_len), _ptr(d0), _ptr(S0), _ptr(k_tilde),
                                      _ptr(o), _ptr(S_out), _ptr(d_out), H, K, V, int(chunk), float(eta), float(d_min),
@@ -495,7 +500,7 @@ def osdn_layer_bwd(q, k, v, beta, do, r=None, d0=None, S0=None, *, dS=None, dd=N
     need = osdn_layer_bwd_workspace_bytes(B, T, H, K, V)
     if workspace is False:
         raise ValueError("osdn_layer_bwd needs a workspace")
-    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "bwd")
+    ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "bwd", stream)
     st = lib().osdn_layer_bwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, None, _ptr(d0),
                               _ptr(S0), _ptr(do), _ptr(dS), _ptr(dd), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
                               _ptr(g["dbeta"]), _ptr(g["dr"]), _ptr(g["dd0"]), _ptr(g["dS0"]), B, T, H, K, V,

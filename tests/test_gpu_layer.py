@@ -88,3 +88,25 @@ def test_layer_fallback_fp32_and_empty(name, T):
     o2, S2, dd2, kt2 = two_calls(d, w, S0, d0, eta=0.1)
     torch.cuda.synchronize()
     assert torch.equal(kt, kt2) and torch.equal(dd, dd2) and torch.equal(o, o2) and torch.equal(S, S2)
+
+
+def test_chunk_calls_on_two_streams_get_separate_scratch():
+    """Two chunk forwards queued on two streams may run at the same time: each stream gets its own
+    cached workspace, so both give what they give one after the other."""
+    w = W.WORKLOADS["layer_340m"]
+    prob = []
+    for seed in (71, 72):
+        d = to_dev(W.make_prefill(w, B=2, H=4, T=512, seed=seed))
+        kt, _ = osdn_precond_scan(d["k"], d["beta"], None, None, kt_dtype=d["k"].dtype, eta=w.eta)
+        prob.append((d, kt))
+    ref = [osdn_chunk_fwd(d["q"], d["k"], kt, d["v"], d["beta"]) for d, kt in prob]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    out = []
+    for (d, kt), s in zip(prob, streams):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            out.append(osdn_chunk_fwd(d["q"], d["k"], kt, d["v"], d["beta"], stream=s))
+    torch.cuda.synchronize()
+    for (o, S), (o2, S2) in zip(ref, out):
+        assert torch.equal(o, o2) and torch.equal(S, S2)
