@@ -12,6 +12,7 @@
 // `stream` runs the layer on piece i-1 from the other slot, and `d2h` copies piece i-1's outputs
 // back.  The (d, S) state stays on the device, in two buffers used alternately.  Events order the
 // reuse of a slot: piece i+2's inputs go into slot i % 2 only after piece i's outputs have left it.
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -116,8 +117,9 @@ extern "C" osdn_status osdn_layer_fwd_host(const void* q, const void* k, const v
     if (dtype != OSDN_F32 && dtype != OSDN_BF16 && dtype != OSDN_F16) return OSDN_ERR_DTYPE;
     if (r_per_key != 0 && r_per_key != 1) return OSDN_ERR_ARG;
     if (alpha_per_key != 0 && alpha_per_key != 1) return OSDN_ERR_ARG;
-    if (!(eta >= 0.f) || !(eps > 0.f) || d_min != d_min || d_max != d_max || d_min > d_max || scale != scale)
-        return OSDN_ERR_ARG;
+    // the scalar checks of osdn_layer_fwd, here so that no copy is queued for a call it would reject
+    if (!(eta >= 0.f) || !isfinite(eta) || !(eps > 0.f) || !isfinite(eps)) return OSDN_ERR_ARG;
+    if (isnan(d_min) || isnan(d_max) || d_min > d_max || !isfinite(scale)) return OSDN_ERR_ARG;
     if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
     if (B == 0 || H == 0) return OSDN_OK;
     if (!S_out || !d_out) return OSDN_ERR_ARG;

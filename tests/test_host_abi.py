@@ -220,7 +220,8 @@ def host_layer(L, **kw):
     (dict(ws=None), ARG), (dict(wsb=1024), ARG), (dict(ws=ctypes.c_void_p((1 << 20) + 128)), ALIGN),
     (dict(q=None), ARG), (dict(Sout=None), ARG), (dict(K=96), UNSUP), (dict(C=32), UNSUP), (dict(dt=9), DTYPE),
     (dict(rpk=2), ARG), (dict(apk=2), ARG), (dict(dmin=3.0), ARG), (dict(eta=math.nan), ARG), (dict(B=-1), SHAPE),
-    (dict(B=0), OK), (dict(H=0), OK),
+    (dict(eta=math.inf), ARG), (dict(eps=0.0), ARG), (dict(eps=math.inf), ARG), (dict(scale=math.inf), ARG),
+    (dict(dmin=math.nan), ARG), (dict(B=0), OK), (dict(H=0), OK),
 ])
 def test_host_layer_validation(L, kw, want):
     """Every argument error is returned before any CUDA call (host buffers need no alignment)."""
