@@ -206,6 +206,13 @@ def oracle_layer_rate(w, inp, budget_s=12.0):
     return rate, secs, sample, threads
 
 
+def workload_config(w):
+    """The `config` object of both arms' JSON lines (identical, so that they compare)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "K": w.K, "V": w.V, "chunk": w.chunk,
+            "eta": w.eta, "box": [w.d_min, w.d_max],
+            "l2": "GPU arm: flushed between steps (256 MiB write outside the timed events); CPU arm: n/a"}
+
+
 def run_reference(args, w):
     from preconditioned_delta_rule_gb300 import workloads as W
 
@@ -227,8 +234,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "K": w.K, "V": w.V,
-                   "chunk": w.chunk, "l2": "n/a (CPU)"},
+        "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -365,9 +371,7 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate/state",
             "data": "synthetic (seeded; shapes of the pages' 340M layer)",
-            "config": {"workload": w.name, "B": B, "H": H, "T": T, "K": K, "V": V,
-                       "chunk": w.chunk, "eta": w.eta, "box": [w.d_min, w.d_max],
-                       "l2": "flushed between steps (256 MiB write outside the timed events)"},
+            "config": workload_config(w),
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "decode": decode, "other_configs": configs, "gated": gated, "varlen": varlen, "backward": backward,
             "vector_retention": vret,

@@ -291,8 +291,12 @@ size_t osdn_layer_bwd_workspace_bytes(int B, int T, int H, int K, int V);
  *   larger requests return OSDN_ERR_CAPACITY before any launch.  Calls that need no scratch (fp32
  *   inputs, other head sizes) run the CUDA-core kernel as osdn_chunk_fwd does.
  *   Neither the library nor this call allocates (no cudaMalloc/cudaFree or allocating routine).
- *   The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
- *   caches it; make that first call before any stream capture.
+ *   Every call looks up the array's device address on the current device
+ *   (cudaGetSymbolAddress, which allocates nothing); the first call on a device also loads the
+ *   library's device code there, so make that first call before any stream capture.  The
+ *   argument checks are osdn_chunk_fwd's and come before the capacity test; only calls that take
+ *   the tensor-core path need scratch, so a per-channel gate (alpha_per_key = 1) or fp32 inputs are
+ *   never refused for capacity.
  *   All calls share the one array and nothing in it needs to start at zero (each call writes all
  *   the scratch it reads), but calls whose work overlaps on the GPU -- on different streams, or
  *   from different threads -- race on it: serialise them.
@@ -323,6 +327,16 @@ osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_d
  * cu_seqlens range (both flags are cleared), OSDN_ERR_CUDA if the stream holds a CUDA error, else
  * OSDN_OK. */
 osdn_status osdn_check(void* stream);
+
+/*
+ * Failure-detection hook (not a method parameter; the paper has no counterpart).  Sets how many
+ * times the fused layer call's chunk-prep workers poll for a value that its phase-1 CTAs publish
+ * before they give up (0 restores the default, about 2-4 s of polling).  A small limit makes those
+ * bounded waits run out while phase 1 is still working: the kernels then drain what they issued
+ * and exit normally, the call's results are invalid, and osdn_check reports OSDN_ERR_TIMEOUT.
+ * Process-wide; meant for tests, never needed in normal use.
+ */
+void osdn_set_poll_limit(unsigned int polls);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* osdn_status_string(int status);

@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
     L.osdn_status_string.argtypes = [ctypes.c_int]
     L.osdn_status_string.restype = ctypes.c_char_p
     L.osdn_version.restype = ctypes.c_int
+    L.osdn_set_poll_limit.argtypes = [ctypes.c_uint]
+    L.osdn_set_poll_limit.restype = None
     _lib = L
     return L
 
@@ -90,6 +92,11 @@ def osdn_status_string(status: int) -> str:
 
 def osdn_version() -> int:
     return int(lib().osdn_version())
+
+
+def osdn_set_poll_limit(polls: int) -> None:
+    """Failure-detection hook: poll limit of the fused layer's prep workers (0: the default)."""
+    lib().osdn_set_poll_limit(int(polls))
 
 
 def _raise(fn: str, st: int):

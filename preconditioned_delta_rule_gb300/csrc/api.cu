@@ -72,6 +72,47 @@ cudaError_t layer_dispatch(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, void
 
 }  // namespace
 
+// Argument checks of osdn_chunk_fwd (everything but the workspace), shared with the entry
+// points that call it; `empty` is set when there is nothing to compute (B or H zero).
+osdn_status osdn_chunk_validate(const void* q, const void* k, const void* k_tilde, const void* v, osdn_dtype dtype,
+                                const float* beta, const float* alpha, int alpha_per_key, const float* S0, void* o,
+                                float* S_out, int B, int T, int H, int K, int V, int chunk, float scale,
+                                OsdnChunkArgs* out, bool* empty) {
+    *empty = false;
+    if (B < 0 || T < 0 || H < 0 || chunk <= 0) return OSDN_ERR_SHAPE;
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return (K > 0 && V > 0) ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
+    if (chunk != 64) return OSDN_ERR_UNSUPPORTED;
+    if (T % chunk != 0) return OSDN_ERR_SHAPE;
+    if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
+    if (!isfinite(scale)) return OSDN_ERR_ARG;
+    if (alpha_per_key != 0 && alpha_per_key != 1) return OSDN_ERR_ARG;
+    if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
+    if (B == 0 || H == 0) {
+        *empty = true;
+        return OSDN_OK;
+    }
+    const bool seq = T > 0;
+    OSDN_TRY(ptr(q, seq));
+    OSDN_TRY(ptr(k, seq));
+    OSDN_TRY(ptr(k_tilde, seq));
+    OSDN_TRY(ptr(v, seq));
+    OSDN_TRY(ptr(beta, seq));
+    OSDN_TRY(ptr(alpha, false));
+    OSDN_TRY(ptr(o, seq));
+    OSDN_TRY(ptr(S0, false));
+    OSDN_TRY(ptr(S_out, true));
+    *out = OsdnChunkArgs{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale, alpha,
+                         alpha ? alpha_per_key : 0};
+    return OSDN_OK;
+}
+
+// Scratch the dispatch below would use for these (validated) arguments: the tensor-core path's
+// workspace where that path applies, else 0.
+size_t osdn_chunk_scratch_bytes(const OsdnChunkArgs& a) {
+    if (a.T > 0 && a.dtype != OSDN_F32 && a.K == 128 && a.V == 128) return osdn_chunk_tc_workspace_bytes(a);
+    return 0;
+}
+
 extern "C" {
 
 osdn_status osdn_precond_scan(const void* k, osdn_dtype k_dtype, const float* beta,
@@ -111,28 +152,12 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
                            const float* S0, void* o,
                            float* S_out, int B, int T, int H, int K, int V, int chunk,
                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
-    if (B < 0 || T < 0 || H < 0 || chunk <= 0) return OSDN_ERR_SHAPE;
-    if (!head_dim_ok(K) || !head_dim_ok(V)) return (K > 0 && V > 0) ? OSDN_ERR_UNSUPPORTED : OSDN_ERR_SHAPE;
-    if (chunk != 64) return OSDN_ERR_UNSUPPORTED;
-    if (T % chunk != 0) return OSDN_ERR_SHAPE;
-    if (!dtype_ok(dtype)) return OSDN_ERR_DTYPE;
-    if (!isfinite(scale)) return OSDN_ERR_ARG;
-    if (alpha_per_key != 0 && alpha_per_key != 1) return OSDN_ERR_ARG;
-    if ((long long)B * H > 0x7fffffffLL) return OSDN_ERR_SHAPE;
-    if (B == 0 || H == 0) return OSDN_OK;
-    const bool seq = T > 0;
-    OSDN_TRY(ptr(q, seq));
-    OSDN_TRY(ptr(k, seq));
-    OSDN_TRY(ptr(k_tilde, seq));
-    OSDN_TRY(ptr(v, seq));
-    OSDN_TRY(ptr(beta, seq));
-    OSDN_TRY(ptr(alpha, false));
-    OSDN_TRY(ptr(o, seq));
-    OSDN_TRY(ptr(S0, false));
-    OSDN_TRY(ptr(S_out, true));
+    OsdnChunkArgs a{};
+    bool empty = false;
+    OSDN_TRY(osdn_chunk_validate(q, k, k_tilde, v, dtype, beta, alpha, alpha_per_key, S0, o, S_out, B, T, H, K, V,
+                                 chunk, scale, &a, &empty));
+    if (empty) return OSDN_OK;
     OSDN_TRY(ptr(workspace, false));
-    OsdnChunkArgs a{q, k, k_tilde, v, dtype, beta, S0, o, S_out, B, T, H, K, V, chunk, scale, alpha,
-                    alpha ? alpha_per_key : 0};
     return from_cuda(chunk_dispatch(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 

@@ -6,8 +6,6 @@
 // or code that cannot accept an allocator call (its latency, its implicit synchronisation, or its
 // possible failure) in the middle of a step.  For them this entry point uses a fixed scratch
 // array that lives in the library's own device memory instead.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace {
@@ -16,30 +14,10 @@ namespace {
 constexpr size_t kStaticWsBytes = static_cast<size_t>(32) << 20;
 
 // File-scope device scratch.  Every GPU that loads this library holds these 32 MiB until the
-// process exits.  In host code `g_chunk_ws` only names the symbol: its device address comes from
-// cudaGetSymbolAddress, once per device (below).
+// process exits.  In host code `g_chunk_ws` only names the symbol: its device address on the
+// current device comes from cudaGetSymbolAddress, looked up on every call (it allocates nothing,
+// and a fresh lookup stays valid if the device's context was torn down and made again).
 static __device__ __align__(256) unsigned char g_chunk_ws[kStaticWsBytes];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_ws_mu;
-void* g_ws_ptr[kMaxDevices] = {};
-
-// Device address of g_chunk_ws on the current device; resolved on the first call per device.
-cudaError_t static_ws_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_ws_mu);
-    if (g_ws_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_chunk_ws);
-        if (e != cudaSuccess) return e;
-        g_ws_ptr[dev] = p;
-    }
-    *out = g_ws_ptr[dev];
-    return cudaSuccess;
-}
 
 }  // namespace
 
@@ -50,17 +28,24 @@ osdn_status osdn_chunk_fwd_static_ws(const void* q, const void* k, const void* k
                                      const float* S0, void* o,
                                      float* S_out, int B, int T, int H, int K, int V, int chunk,
                                      float scale, void* stream) {
-    const size_t need = osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, dtype);
+    // the same argument checks as osdn_chunk_fwd, before the capacity test
+    OsdnChunkArgs a{};
+    bool empty = false;
+    const osdn_status st = osdn_chunk_validate(q, k, k_tilde, v, dtype, beta, alpha, alpha_per_key, S0, o, S_out, B,
+                                               T, H, K, V, chunk, scale, &a, &empty);
+    if (st != OSDN_OK || empty) return st;
+    // scratch only where the tensor-core path runs (a channel gate or fp32 inputs take the
+    // CUDA-core kernel, which needs none)
+    const size_t need = osdn_chunk_scratch_bytes(a);
     if (need > kStaticWsBytes) return OSDN_ERR_CAPACITY;
     void* ws = nullptr;
     if (need > 0) {
         // Everything the two kernels read from the scratch is written earlier in the same call,
         // so nothing needs clearing between calls.
-        if (static_ws_address(&ws) != cudaSuccess) return OSDN_ERR_CUDA;
+        if (cudaGetSymbolAddress(&ws, g_chunk_ws) != cudaSuccess) return OSDN_ERR_CUDA;
     }
     return osdn_chunk_fwd(q, k, k_tilde, v, dtype, beta, alpha, alpha_per_key, S0, o, S_out, B, T, H, K, V, chunk,
-                          scale, ws,
-                          need, stream);
+                          scale, ws, need, stream);
 }
 
 }  // extern "C"

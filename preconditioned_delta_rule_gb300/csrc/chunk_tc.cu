@@ -31,6 +31,7 @@
 // osdn_check), drains what it issued and exits.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -514,8 +515,10 @@ __device__ __forceinline__ bool bar_and128(int bar, bool pred) {
 // A workspace word written concurrently by another CTA: the workspace is filled with all-ones
 // before the launch and the writer never stores that pattern, so the first load that differs is
 // the value.  Relaxed GPU-scope loads (not cached in L1); bounded, clears `ok` on giving up.
-__device__ __forceinline__ float poll_word(const float* p, bool& ok) {
-    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+// `limit` is the number of polls (kMaxPolls unless a failure-detection test lowered it); each
+// poll is one L2 round trip plus a 64 ns back-off, so the default gives up after about 2-4 s.
+__device__ __forceinline__ float poll_word(const float* p, bool& ok, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t v;
         asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
         if (v != 0xffffffffu) return __uint_as_float(v);
@@ -594,7 +597,7 @@ struct PrepWorker {
                         const float* __restrict__ beta, const float* __restrict__ alpha,
                         unsigned char* __restrict__ ws, size_t slot, int b,
                         int h, int n, int T, int H, const float* g_src, const float* r_src, const float* d_src,
-                        float dmin, float dmax, const CUtensorMap* tmKTout) {
+                        float dmin, float dmax, const CUtensorMap* tmKTout, uint32_t poll_limit = kMaxPolls) {
         using namespace prep;
         float* AM = reinterpret_cast<float*>(sm + OFF_AM);
         float* TM = reinterpret_cast<float*>(sm + OFF_TM);
@@ -625,11 +628,11 @@ struct PrepWorker {
         bool ready = true;
         if (EMIT) {  // the scan may still be writing these: poll until they are there (bounded)
             if (tid < C) {
-                semit[tid] = poll_word(g_src + tid, ready);
+                semit[tid] = poll_word(g_src + tid, ready, poll_limit);
                 semit[C + tid] = r_src ? r_src[static_cast<size_t>(tid) * H] : 1.f;
             }
-            semit[2 * C + tid] = poll_word(d_src + tid, ready);
-            semit[2 * C + KD + tid] = poll_word(d_src + KD + tid, ready);
+            semit[2 * C + tid] = poll_word(d_src + tid, ready, poll_limit);
+            semit[2 * C + KD + tid] = poll_word(d_src + KD + tid, ready, poll_limit);
         }
         {
             const bool ok = tc::mbar_wait(bar_tma, tph, kMaxPolls) && ready;
@@ -1396,7 +1399,7 @@ __global__ void __launch_bounds__(256, 1)
 layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* counter,
                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ alpha,
-                       unsigned char* __restrict__ cws, int N, int BH) {
+                       unsigned char* __restrict__ cws, int N, int BH, uint32_t poll_limit) {
     extern __shared__ unsigned char smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the chain kernel may set up
@@ -1436,7 +1439,7 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
         const float* r_src = HAS_R ? sa.r + row0 + static_cast<size_t>(m) * C * H : nullptr;
         const float* d_src = ws_d + (static_cast<size_t>(bh) * N + m) * (2 * KD);
         if (!pw.template run<true>(&tmQ, &tmK, nullptr, sa.beta, alpha, cws, static_cast<size_t>(bh) * N + m, b, h, m, T, H,
-                                   g_src, r_src, d_src, sa.d_min, sa.d_max, &tmKT)) {
+                                   g_src, r_src, d_src, sa.d_min, sa.d_max, &tmKT, poll_limit)) {
             aborted = true;
             break;
         }
@@ -1447,6 +1450,10 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
     tc::tc_fence_after();
     if (warp == 0) tc::tmem_dealloc(tbase, kCols);
 }
+
+// Poll limit of the fused layer's prep workers (0: the default kMaxPolls); lowered only by
+// osdn_set_poll_limit, for failure-detection tests.
+std::atomic<uint32_t> g_poll_limit{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1616,7 +1623,9 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     unsigned char* cws = ws + l.chunk;
     int N = ca.T / C, BH = ca.B * ca.H;
     const float* alpha = ca.alpha;
-    void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &mkt, &alpha, &cws, &N, &BH};
+    uint32_t poll_limit = g_poll_limit.load();
+    if (poll_limit == 0) poll_limit = kMaxPolls;
+    void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &mkt, &alpha, &cws, &N, &BH, &poll_limit};
     e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
                                     dim3(256), args, smem, s);
     if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer resident CTAs than expected: two calls
@@ -1677,3 +1686,5 @@ cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s) {
     *flag |= scan_flag;
     return e;
 }
+
+extern "C" void osdn_set_poll_limit(unsigned int polls) { osdn::g_poll_limit.store(polls); }

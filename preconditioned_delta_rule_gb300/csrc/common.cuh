@@ -128,6 +128,13 @@ cudaError_t osdn_launch_chunk_simt(const OsdnChunkArgs& a, cudaStream_t s);
 cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a);
 cudaError_t osdn_launch_decode(const OsdnDecodeArgs& a, cudaStream_t s);
+// Argument checks of osdn_chunk_fwd (all but the workspace); fills `out`, or sets `empty` when B
+// or H is zero.  Scratch the chunk dispatch uses for validated arguments (0: none).
+osdn_status osdn_chunk_validate(const void* q, const void* k, const void* k_tilde, const void* v, osdn_dtype dtype,
+                                const float* beta, const float* alpha, int alpha_per_key, const float* S0, void* o,
+                                float* S_out, int B, int T, int H, int K, int V, int chunk, float scale,
+                                OsdnChunkArgs* out, bool* empty);
+size_t osdn_chunk_scratch_bytes(const OsdnChunkArgs& a);
 // Packed variable-length sequences: scatter into an [N, Tp, H, .] batch and gather back.
 struct OsdnVarlenShape {
     int N, Tp, H, K, V;

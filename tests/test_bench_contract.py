@@ -31,6 +31,11 @@ def _check_line(line, n):
     assert line["n_gpus"] == n and line["steps"] == 1 and line["warmup"] == 3
     assert line["value"] > 0 and line["higher_is_better"] is True and line["vs_baseline"] is None
     assert line["config"]["workload"] == "tiny_f32"
+    # the GPU arm prints the same object (bench.workload_config), so the two lines compare
+    sys.path.insert(0, str(ROOT))
+    import bench
+    from preconditioned_delta_rule_gb300 import workloads as W
+    assert line["config"] == json.loads(json.dumps(bench.workload_config(W.WORKLOADS["tiny_f32"])))
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
     e2e = line["e2e"]
