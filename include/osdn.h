@@ -38,9 +38,18 @@
  *   - Errors: OSDN_OK on success; OSDN_ERR_ARG (null pointer where one is required, negative or
  *     non-finite scalar, d_min > d_max), OSDN_ERR_SHAPE (sizes out of range, T not a multiple of
  *     the chunk), OSDN_ERR_DTYPE, OSDN_ERR_ALIGN, OSDN_ERR_UNSUPPORTED (valid but not built, e.g.
- *     K = 96), OSDN_ERR_CUDA (a launch failed; the CUDA error is left for the caller to query),
+ *     K = 96), OSDN_ERR_CUDA (a launch failed; osdn_last_cuda_error() names the CUDA error),
  *     OSDN_ERR_TIMEOUT (a device-side bounded wait gave up; reported by osdn_check()),
- *     OSDN_ERR_CAPACITY (the request needs more scratch than osdn_chunk_fwd_static_ws has).
+ *     OSDN_ERR_CAPACITY (the request needs more scratch than osdn_chunk_fwd_static_ws has),
+ *     OSDN_ERR_RANGE (reported by osdn_check(): a 16-bit tensor-core chunk call produced an inf or
+ *     NaN in o or the final S, i.e. an input, the state or an intermediate left fp16's range).
+ *   - Numeric range of the 16-bit tensor-core chunk path (K = V = 128, bf16/f16 inputs): its
+ *     operands are fp16 (bf16 inputs convert exactly in fp16's normal range), so every input
+ *     element, every entry of the state S and of the chunk intermediates T', W, U, X and L must
+ *     stay below 65504 in magnitude.  Elements below fp16's normal range (6.1e-5) keep an absolute
+ *     precision of 6e-8.  A call that left the range returns invalid results and osdn_check()
+ *     reports OSDN_ERR_RANGE; rerun it with fp32 inputs (the fp32 CUDA-core path), or scale v and
+ *     S0 by a power of two and o and S back (the rule is linear in (v, S0)).
  *   - Sizes are `int`; B*T*H*max(K,V) must stay below 2^31 elements per tensor.
  */
 #ifndef OSDN_H
@@ -61,7 +70,8 @@ typedef enum {
     OSDN_ERR_UNSUPPORTED = 5,
     OSDN_ERR_CUDA = 6,
     OSDN_ERR_TIMEOUT = 7,
-    OSDN_ERR_CAPACITY = 8
+    OSDN_ERR_CAPACITY = 8,
+    OSDN_ERR_RANGE = 9
 } osdn_status;
 
 typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1, OSDN_F16 = 2 } osdn_dtype;
@@ -324,7 +334,8 @@ osdn_status osdn_decode_step(const void* q, const void* k, const void* v, osdn_d
 
 /* Waits for `stream`, then reports OSDN_ERR_TIMEOUT if any kernel of this library gave up a
  * bounded device-side wait since the last check, OSDN_ERR_SHAPE if a varlen call met an invalid
- * cu_seqlens range (both flags are cleared), OSDN_ERR_CUDA if the stream holds a CUDA error, else
+ * cu_seqlens range, OSDN_ERR_RANGE if a 16-bit tensor-core chunk call produced a non-finite
+ * output (all three flags are cleared), OSDN_ERR_CUDA if the stream holds a CUDA error, else
  * OSDN_OK. */
 osdn_status osdn_check(void* stream);
 
@@ -340,6 +351,10 @@ void osdn_set_poll_limit(unsigned int polls);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* osdn_status_string(int status);
+
+/* Name of the CUDA error behind the calling thread's most recent OSDN_ERR_CUDA return
+ * ("cudaSuccess" if there was none); static storage, never NULL. */
+const char* osdn_last_cuda_error(void);
 
 /* ABI version: major * 10000 + minor * 100 + patch. */
 int osdn_version(void);

@@ -20,7 +20,8 @@ LIB_PATH = _PKG / "libosdn.so"
 OSDN_F32, OSDN_BF16, OSDN_F16 = 0, 1, 2
 _DTYPE_CODE = {torch.float32: OSDN_F32, torch.bfloat16: OSDN_BF16, torch.float16: OSDN_F16}
 _STATUS = ["OSDN_OK", "OSDN_ERR_ARG", "OSDN_ERR_SHAPE", "OSDN_ERR_DTYPE", "OSDN_ERR_ALIGN",
-           "OSDN_ERR_UNSUPPORTED", "OSDN_ERR_CUDA", "OSDN_ERR_TIMEOUT", "OSDN_ERR_CAPACITY"]
+           "OSDN_ERR_UNSUPPORTED", "OSDN_ERR_CUDA", "OSDN_ERR_TIMEOUT", "OSDN_ERR_CAPACITY",
+           "OSDN_ERR_RANGE"]
 
 _lib = None
 
@@ -80,6 +81,7 @@ def lib() -> ctypes.CDLL:
     L.osdn_status_string.argtypes = [ctypes.c_int]
     L.osdn_status_string.restype = ctypes.c_char_p
     L.osdn_version.restype = ctypes.c_int
+    L.osdn_last_cuda_error.restype = ctypes.c_char_p
     L.osdn_set_poll_limit.argtypes = [ctypes.c_uint]
     L.osdn_set_poll_limit.restype = None
     _lib = L
@@ -101,7 +103,10 @@ def osdn_set_poll_limit(polls: int) -> None:
 
 def _raise(fn: str, st: int):
     if st != 0:
-        raise OsdnError(fn, st, osdn_status_string(st))
+        detail = osdn_status_string(st)
+        if st == 6:  # OSDN_ERR_CUDA: name the CUDA error
+            detail += f" [{lib().osdn_last_cuda_error().decode()}]"
+        raise OsdnError(fn, st, detail)
 
 
 def _ptr(t: Optional[torch.Tensor]):

@@ -30,7 +30,13 @@ osdn_status phase1_scalars(float eta, float d_min, float d_max, float eps) {
     return OSDN_OK;
 }
 
-osdn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA; }
+// The CUDA error behind this thread's last OSDN_ERR_CUDA (reported by osdn_last_cuda_error).
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+osdn_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return OSDN_OK;
+    t_last_cuda_error = e;
+    return OSDN_ERR_CUDA;
+}
 
 // phase 2 on the tensor cores where they apply, else the fp32 CUDA-core kernel
 cudaError_t chunk_dispatch(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
@@ -402,10 +408,15 @@ osdn_status osdn_check(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned int flag = 0, bad = 0;
     cudaError_t e = osdn_read_and_clear_timeout(&flag, s);
-    if (e != cudaSuccess) return OSDN_ERR_CUDA;
-    if (osdn_varlen_read_and_clear_flag(&bad) != cudaSuccess) return OSDN_ERR_CUDA;
+    if (e != cudaSuccess) return from_cuda(e);
+    e = osdn_varlen_read_and_clear_flag(&bad);
+    if (e != cudaSuccess) return from_cuda(e);
+    unsigned int range = 0;
+    e = osdn_read_and_clear_range(&range);
+    if (e != cudaSuccess) return from_cuda(e);
     if (flag) return OSDN_ERR_TIMEOUT;
     if (bad) return OSDN_ERR_SHAPE;
+    if (range) return OSDN_ERR_RANGE;
     return OSDN_OK;
 }
 
@@ -420,10 +431,15 @@ const char* osdn_status_string(int status) {
         case OSDN_ERR_CUDA: return "OSDN_ERR_CUDA: a CUDA call or launch failed";
         case OSDN_ERR_TIMEOUT: return "OSDN_ERR_TIMEOUT: a device-side bounded wait gave up";
         case OSDN_ERR_CAPACITY: return "OSDN_ERR_CAPACITY: the request needs more scratch than the fixed no-allocation array holds";
+        case OSDN_ERR_RANGE: return "OSDN_ERR_RANGE: a 16-bit tensor-core call produced a non-finite output (a value left fp16's range)";
     }
     return "OSDN: unknown status";
 }
 
 int osdn_version(void) { return 200; }
+
+const char* osdn_last_cuda_error(void) {
+    return t_last_cuda_error == cudaSuccess ? "cudaSuccess" : cudaGetErrorName(t_last_cuda_error);
+}
 
 }  // extern "C"

@@ -38,11 +38,15 @@
 #include "common.cuh"
 #include "scan_block_body.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 #include "tsolve.cuh"
 
 namespace osdn {
 // Set by any kernel of this library whose bounded device-side wait gave up.
 __device__ unsigned int g_timeout_flag = 0;
+// Set by the 16-bit tensor-core kernels when an output (o or the final S) is not finite: an fp16
+// operand (input, state copy or intermediate) left fp16's range, and the call's results are invalid.
+__device__ unsigned int g_range_flag = 0;
 
 namespace {
 
@@ -83,6 +87,13 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// True when any of the 32 values is inf or NaN (one pass of compares, no branches).
+__device__ __forceinline__ bool any_nonfinite32(const float (&v)[32]) {
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) bad |= !isfinite(v[j]);
+    return bad;
+}
 // Write 8 consecutive values as fp16 into chunk `c` of row `r` of a swizzled atom stack.
 __device__ __forceinline__ void st_row_chunk(unsigned char* base, uint32_t r, uint32_t c,
                                              const float* v) {
@@ -182,6 +193,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     uint32_t mph = 0;
     bool aborted = false;
+    bool nonfinite = false;  // an output of this thread was inf or NaN
     bool tma_pending[2] = {N > 0, false};
     int tma_chunk[2] = {0, 0};  // chunk index of the load last issued into each stage
     bool mma_pending = false;
@@ -390,6 +402,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 float o[32];
                 tc::tmem_ld32(tbase + lane_base + COL_R + q2 * 32, o);
                 tc::tmem_ld_wait();
+                nonfinite |= any_nonfinite32(o);
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
                     float ov[4] = {scale * o[j], scale * o[j + 1], scale * o[j + 2], scale * o[j + 3]};
@@ -432,10 +445,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             float sv[32];
             tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, sv);
             tc::tmem_ld_wait();
+            nonfinite |= any_nonfinite32(sv);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 S_out[(static_cast<size_t>(bh) * V + v0 + q2 * 32 + j) * KD + k] = sv[j];
         }
+        if (nonfinite) atomicOr(&g_range_flag, 1u);
         tc::tc_fence_before();
         __syncthreads();
         tc::tc_fence_after();
@@ -1135,7 +1150,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // ========================== O readout: TMEM -> smem -> TMA ============================
         const int r = (warp - 10) * 32 + lane;  // token row; tensor-memory lane 64 + r
         const bool issuer = warp == 10 && lane == 0;
-        bool ok = true;
+        bool ok = true, nonfinite = false;
         for (int n = 0; n < N; ++n) {
             const int bb = n & 1;
             ok = warp_wait(bars + B_O + 8 * bb, (n >> 1) & 1, abort_flag);
@@ -1147,6 +1162,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 float o[32];
                 tc::tmem_ld32(tbase + lane_base + COL_R + bb * VS + q2 * 32, o);
                 tc::tmem_ld_wait();
+                nonfinite |= any_nonfinite32(o);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float ov[8];
@@ -1172,6 +1188,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
         }
         if (issuer) tc::bulk_wait_all();
+        if (nonfinite) atomicOr(&g_range_flag, 1u);
         if (!ok) record_abort(abort_flag);
     } else if (warp >= 4) {
         // ======================== operand staging into tensor memory ==========================
@@ -1370,8 +1387,13 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     st_row_chunk(sm + OFF_SS + ((cc * 8) / 64) * (KD * 128), k, cc % 8, sv + 8 * cc);
                 warp_publish(bars + B_SRDY, lane);
             } else {
+                bool bad = false;
 #pragma unroll
-                for (int j = 0; j < VS; ++j) S_out[(static_cast<size_t>(bh) * V + v0 + j) * KD + k] = sv[j];
+                for (int j = 0; j < VS; ++j) {
+                    bad |= !isfinite(sv[j]);
+                    S_out[(static_cast<size_t>(bh) * V + v0 + j) * KD + k] = sv[j];
+                }
+                if (bad) atomicOr(&g_range_flag, 1u);
             }
         }
         if (!ok) record_abort(abort_flag);
@@ -1638,6 +1660,12 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
 }
 
 }  // namespace
+
+bool make_row_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int inner, int H, long long rows) {
+    return make_map(m, ptr, dt, inner, H, rows);
+}
+int device_sm_count() { return num_sms(); }
+
 }  // namespace osdn
 
 size_t osdn_layer_workspace_bytes(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
@@ -1671,12 +1699,20 @@ cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_byt
 
 cudaError_t osdn_scan_block_read_and_clear_timeout(unsigned int* flag);
 
+cudaError_t osdn_read_and_clear_range(unsigned int* flag) {
+    cudaError_t e = cudaMemcpyFromSymbol(flag, osdn::g_range_flag, sizeof(unsigned int));
+    if (e != cudaSuccess || *flag == 0) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(osdn::g_range_flag, &zero, sizeof(unsigned int));
+}
+
 cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s) {
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return e;
     unsigned int scan_flag = 0;
     e = osdn_scan_block_read_and_clear_timeout(&scan_flag);
     if (e != cudaSuccess) return e;
+
     e = cudaMemcpyFromSymbol(flag, osdn::g_timeout_flag, sizeof(unsigned int));
     if (e != cudaSuccess) return e;
     if (*flag) {

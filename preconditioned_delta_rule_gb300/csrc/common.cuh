@@ -171,5 +171,8 @@ cudaError_t osdn_launch_bwd(const OsdnBwdArgs& a, void* ws, cudaStream_t s);
 cudaError_t osdn_launch_layer(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, void* ws, size_t ws_bytes,
                               cudaStream_t s);
 size_t osdn_layer_workspace_bytes(const OsdnScanArgs& sa, const OsdnChunkArgs& ca);
+// Reads and clears the device-side word set when a 16-bit tensor-core kernel produced a non-finite
+// output (call after the stream is synchronised).
+cudaError_t osdn_read_and_clear_range(unsigned int* flag);
 // Reads and clears the device-side timeout word (synchronous on the given stream).
 cudaError_t osdn_read_and_clear_timeout(unsigned int* flag, cudaStream_t s);

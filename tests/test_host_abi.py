@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    for code in range(8):
+    for code in range(10):
         s = binding.osdn_status_string(code)
         assert s.startswith(binding._STATUS[code])
     assert "unknown" in binding.osdn_status_string(99)
