@@ -687,7 +687,8 @@ def run_backward(args, dev, stream, hbm_peak):
             "tokens_per_s": w.B * w.T / secs,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
                          "algorithmic_bytes_per_launch": b},
-            "kernels": "scan (write keys, fp32) + bwd_phase2_kernel + bwd_phase1_kernel, token-recurrent fp32"}
+            "kernels": "scan (write keys fp32, its record of step sizes and block states) + bwd_phase2_st_kernel "
+                       "+ bwd_phase1_blk_kernel, token-recurrent fp32 with staged inputs"}
 
 
 def run_vector_retention(args, dev, stream, hbm_peak):
