@@ -486,14 +486,18 @@ __device__ __forceinline__ void convert_bf16_to_f16(unsigned char* base, int tid
 }
 
 namespace prep {
+// One worker's shared memory (byte offsets from a 1024-aligned base), 72 KB so that three workers
+// fit on an SM.  Buffers that die early host later ones:
 constexpr uint32_t OFF_KQ = 0;         // per key block: K (64 rows) | Q (64 rows), 2 x 16 KB
-constexpr uint32_t OFF_KT = 32768;     // K~ (two key blocks); after the Gram: the -W image
-constexpr uint32_t OFF_ZT = 49152;     // zeros | T'   ([0; T'] operand and T' image); gated: T' | T''
-constexpr uint32_t OFF_LI = OFF_KQ + 8192;  // L image, in the Q rows of key block 0 once Q is used
-constexpr uint32_t OFF_AM = 65536;
-constexpr uint32_t OFF_TM = OFF_AM + 10 * kTile * 4;
-constexpr uint32_t OFF_PM = OFF_TM + 10 * kTile * 4;
-constexpr uint32_t OFF_BETA = OFF_PM + kUtScratchTiles * kTile * 4;
+constexpr uint32_t OFF_Q0 = 8192;      //   Q rows of key block 0; after the Gram: gated T' image
+constexpr uint32_t OFF_PM = 24576;     //   Q rows of key block 1; after the Gram: UT scratch A'
+constexpr uint32_t OFF_KT = 32768;     // K~ (two key blocks); after the Gram: A's packed tiles, then
+                                       //   T's off-diagonal tiles over them; last the -W image
+constexpr uint32_t OFF_ZT = 49152;     // [L | T'] (L rows 0-63: the score image and the rows 0-63
+                                       //   of W's A operand; T' rows 64-127; gated: T'' there)
+constexpr uint32_t OFF_AM = OFF_KT;
+constexpr uint32_t OFF_TD = 65536;     // T's four diagonal tiles
+constexpr uint32_t OFF_BETA = OFF_TD + 4 * kTile * 4;
 constexpr uint32_t OFF_EMIT = OFF_BETA + C * 4;              // step sizes, retention, start state
 constexpr uint32_t OFF_ALPHA = OFF_EMIT + (2 * C + 2 * KD) * 4;  // state gates of the chunk (+ pad)
 constexpr uint32_t OFF_GAM = OFF_ALPHA + (C + 4) * 4;          // their prefix products gamma
@@ -501,7 +505,8 @@ constexpr uint32_t OFF_BAR = OFF_GAM + C * 4;
 constexpr uint32_t REGION = ((OFF_BAR + 32 + 1023) / 1024) * 1024;  // one worker, 1024-aligned
 constexpr uint32_t SMEM_ALLOC = OFF_BAR + 32 + 1024;
 constexpr uint32_t TMEM_COLS = 128;
-static_assert(2 * SMEM_ALLOC <= 232448, "two prep CTAs per SM");
+static_assert(10 * kTile * 4 <= 16384 && kUtScratchTiles * kTile * 4 <= 8192, "UT scratch in dead buffers");
+static_assert(3 * SMEM_ALLOC <= 233472 && 3 * REGION + 1024 <= 232448, "three prep workers per SM");
 }  // namespace prep
 
 // bar.red.and over the 128 threads of named barrier `bar`.
@@ -601,8 +606,6 @@ struct PrepWorker {
             tc::mbar_init(bar_mma, 1);
             tc::mbar_init_fence();
         }
-        for (int e = tid; e < 8192 / 16; e += NTHREADS)
-            reinterpret_cast<uint4*>(sm + prep::OFF_ZT)[e] = make_uint4(0, 0, 0, 0);
     }
 
     // Chunk n of head (b, h) into workspace slot `slot`.  Emission inputs (EMIT only): g_src[64],
@@ -615,7 +618,7 @@ struct PrepWorker {
                         float dmin, float dmax, const CUtensorMap* tmKTout, uint32_t poll_limit = kMaxPolls) {
         using namespace prep;
         float* AM = reinterpret_cast<float*>(sm + OFF_AM);
-        float* TM = reinterpret_cast<float*>(sm + OFF_TM);
+        float* TD = reinterpret_cast<float*>(sm + OFF_TD);
         float* PM = reinterpret_cast<float*>(sm + OFF_PM);
         float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
         float* semit = reinterpret_cast<float*>(sm + OFF_EMIT);
@@ -734,6 +737,10 @@ struct PrepWorker {
             convert_bf16_to_f16<4>(sm + OFF_KQ, tid);
             convert_bf16_to_f16<4>(sm + OFF_KQ + 16384, tid);
         }
+        if (EMIT) {  // A's tiles go over K~: the k~ store must have read it
+            if (tid == 0) tc::bulk_wait_read_all();
+            bar_sync128(bar);
+        }
         {
             const int i = tid & 63;
             float g[64];
@@ -762,24 +769,24 @@ struct PrepWorker {
 #pragma unroll
                 for (int j = 0; j < 64; ++j) g[j] = (j <= i) ? g[j] : 0.f;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) st_row_chunk(sm + OFF_LI, i, c, g + 8 * c);
+                for (int c = 0; c < 8; ++c) st_row_chunk(sm + OFF_ZT, i, c, g + 8 * c);
             }
         }
         tc::tc_fence_before();
         bar_sync128(bar);
-        ut_inverse_64(AM, TM, PM, tid, bar);
+        ut_inverse_64_aliased(AM, TD, PM, tid, bar);
         {
             const int i = tid >> 1, half = tid & 1, bi = i >> 4, r = i & 15;
             float t[32];
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
                 const int j = half * 32 + jj, bj = j >> 4;
-                const float tv = (bj <= bi) ? TM[tile_index(bi, bj) * kTile + r * kTileStride + (j & 15)] : 0.f;
+                const float tv = (bj <= bi) ? ut_tile(AM, TD, bi, bj)[r * kTileStride + (j & 15)] : 0.f;
                 t[jj] = tv * sbeta[j];
             }
             if (gated) {  // T' = T diag(beta) for the workspace, T'' = T diag(beta gamma) for W
 #pragma unroll
-                for (int c = 0; c < 4; ++c) st_row_chunk(sm + OFF_ZT, i, half * 4 + c, t + 8 * c);
+                for (int c = 0; c < 4; ++c) st_row_chunk(sm + OFF_Q0, i, half * 4 + c, t + 8 * c);
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) t[jj] *= sgam[half * 32 + jj];
             }
@@ -789,8 +796,9 @@ struct PrepWorker {
         tc::fence_proxy_async();
         bar_sync128(bar);
 
-        // W = [0; T'] K  (lanes 64-127, 128 columns); K's key blocks are 16 KB apart.  Gated:
-        // [T'; T''] K, whose lanes 0-63 are not used
+        // W = [L; T'] K, read from lanes 64-127 (128 columns; rows 0-63 of the operand are the L
+        // image, whose products land in lanes 0-63 and are not read); K's key blocks are 16 KB
+        // apart.  Gated: [L; T''] K
         if (tid == 0) {
             tc::tc_fence_after();
 #pragma unroll
@@ -829,9 +837,9 @@ struct PrepWorker {
         bar_sync128(bar);
         if (tid == 0) {
             unsigned char* dst = ws + slot * WS_CHUNK;
-            tc::bulk_store(dst + WS_T, sbase + OFF_ZT + (gated ? 0 : 8192), 8192);
+            tc::bulk_store(dst + WS_T, sbase + (gated ? OFF_Q0 : OFF_ZT + 8192), 8192);
             tc::bulk_store(dst + WS_W, sbase + OFF_KT, 16384);
-            tc::bulk_store(dst + WS_L, sbase + OFF_LI, 8192);
+            tc::bulk_store(dst + WS_L, sbase + OFF_ZT, 8192);
             tc::bulk_commit();
         }
         return true;
@@ -850,7 +858,7 @@ struct PrepWorker {
 
 // One CTA loops over chunks q = blockIdx.x, blockIdx.x + gridDim.x, ...  (q = (b*H + h)*N + n).
 template <typename TIn>
-__global__ void __launch_bounds__(NTHREADS, 2)
+__global__ void __launch_bounds__(NTHREADS, 3)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ beta,
                   const float* __restrict__ alpha, unsigned char* __restrict__ ws, int T, int H, int N,
@@ -1416,8 +1424,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 // workspace's scan part and the counter hold all-ones at launch (the counter's first increment
 // wraps it to chunk 0).
 // =============================================================================================
+constexpr int LAYER_NT = 384;      // phase 1 on threads 0-255 of the first B*H CTAs; three prep workers
+constexpr int LAYER_WORKERS = 3;
+
 template <typename TIn, bool HAS_R>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(LAYER_NT, 1)
 layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* counter,
                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ alpha,
@@ -1426,16 +1437,18 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
     const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the chain kernel may set up
     __shared__ uint32_t s_tmem;
-    __shared__ int s_q[2];
-    constexpr uint32_t kCols = scanblk::TMEM_COLS > 2 * prep::TMEM_COLS ? scanblk::TMEM_COLS : 2 * prep::TMEM_COLS;
+    __shared__ int s_q[LAYER_WORKERS];
+    constexpr uint32_t kCols = 512;  // >= the scan's 256 and the workers' 3 x 128, a power of two
+    static_assert(kCols >= scanblk::TMEM_COLS && kCols >= LAYER_WORKERS * prep::TMEM_COLS, "tensor memory");
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), kCols);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tbase = s_tmem;
     // phase 1 for one (batch, head); afterwards this CTA joins the prep workers
-    if (static_cast<int>(blockIdx.x) < BH)
+    if (static_cast<int>(blockIdx.x) < BH && tid < scanblk::NT)
         scanblk::scan_block_body<TIn, TIn, HAS_R>(sa, ws_g, ws_d, blockIdx.x, smem_raw, tbase, &g_timeout_flag);
+    __syncthreads();  // the scan's shared memory becomes the workers' regions
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int T = sa.T, H = sa.H;
@@ -1547,7 +1560,7 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
     dim3 block(NTHREADS);
     if (ws != nullptr && ws_bytes >= need) {
         const int total = a.B * a.H * N;
-        dim3 gp(static_cast<unsigned>(total < 2 * num_sms() ? total : 2 * num_sms()));
+        dim3 gp(static_cast<unsigned>(total < 3 * num_sms() ? total : 3 * num_sms()));
         if (!chain_only) {
             chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta, a.alpha,
                                                                       static_cast<unsigned char*>(ws), a.T, a.H, N, total);
@@ -1623,14 +1636,15 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
         !make_map(&mkt, sa.k_tilde, dt, ca.K, ca.H, rows))
         return cudaErrorNotSupported;
     auto kernel = layer_scan_prep_kernel<TIn, HAS_R>;
-    const uint32_t smem = scanblk::SMEM_ALLOC > 2 * prep::REGION + 1024 ? scanblk::SMEM_ALLOC : 2 * prep::REGION + 1024;
+    constexpr uint32_t kWorkSmem = LAYER_WORKERS * prep::REGION + 1024;
+    const uint32_t smem = scanblk::SMEM_ALLOC > kWorkSmem ? scanblk::SMEM_ALLOC : kWorkSmem;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] { attr_err = set_smem(kernel, smem); });
     if (attr_err != cudaSuccess) return attr_err;
     // every CTA must be resident at once: one per SM, phase 1 on BH of them, prep on the rest
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem) != cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, LAYER_NT, smem) != cudaSuccess || per_sm < 1)
         return cudaErrorNotSupported;
     const int grid = per_sm * num_sms();
     if (grid <= ca.B * ca.H) return cudaErrorNotSupported;
@@ -1649,7 +1663,7 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     if (poll_limit == 0) poll_limit = kMaxPolls;
     void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &mkt, &alpha, &cws, &N, &BH, &poll_limit};
     e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
-                                    dim3(256), args, smem, s);
+                                    dim3(LAYER_NT), args, smem, s);
     if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer resident CTAs than expected: two calls
         (void)cudaGetLastError();
         return cudaErrorNotSupported;

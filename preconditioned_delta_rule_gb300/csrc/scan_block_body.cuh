@@ -123,6 +123,8 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // Barrier over one warpgroup (128 threads) with hardware barrier `id` (1 or 2).
 __device__ __forceinline__ void wg_sync(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
+// All NT threads of the scan (a CTA may carry more threads that do not take part in the scan).
+__device__ __forceinline__ void scan_sync() { asm volatile("bar.sync 4, 256;\n" ::: "memory"); }
 // Barrier over one warpgroup that also counts the threads with `pred` set.
 __device__ __forceinline__ int wg_count(int id, bool pred) {
     int c;
@@ -230,7 +232,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
         s_grams_issued = 0;
         s_grams_used = 0;
     }
-    __syncthreads();
+    scan_sync();
     const uint32_t id_hl = tc::idesc_f16_f32(J, 2 * J, false, false);  // M = 64, N = 128
     const uint32_t id_lh = tc::idesc_f16_f32(J, J, false, false);      // M = 64, N = 64
 
@@ -880,7 +882,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
         a.d_out[static_cast<size_t>(bh) * KD + i] = d_hi + d_lo;
     }
     if (tid >= 128) cp_async_wait<0>();
-    __syncthreads();
+    scan_sync();
     if (tid == 0 && s_abort) {
         atomicExch(timeout_flag, 1u);
         // drain all-free Grams the chain never consumed before tensor memory is released
@@ -888,7 +890,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             tc::mbar_wait(bars + B_GRAM + 8 * (m & 1), (m >> 1) & 1, kMaxPolls >> 4);
     }
     tc::tc_fence_before();
-    __syncthreads();
+    scan_sync();
     tc::tc_fence_after();
     if (tid == 0) {
         for (int q = 0; q < 2; ++q) {
@@ -899,7 +901,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
         tc::mbar_inval(bars + B_MRDY);
         tc::mbar_inval(bars + B_MRDY + 8);
     }
-    __syncthreads();
+    scan_sync();
 }
 
 }  // namespace scanblk
