@@ -517,6 +517,11 @@ def run_configs(args, dev, stream, hbm_peak, names=("layer_1p3b_apf", "longctx_r
         def chunk():
             binding.osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"])
 
+        # the raw-key long-context outputs overflow (the config diverges as written), so the
+        # 16-bit path's range check fires there: expected, and reported rather than raised
+        diverges = name == "longctx_raw"
+        range_flags = []
+
         def med(fn):
             fn()
             times = []
@@ -528,7 +533,12 @@ def run_configs(args, dev, stream, hbm_peak, names=("layer_1p3b_apf", "longctx_r
                 ev[1].record(stream)
                 torch.cuda.synchronize()
                 times.append(ev[0].elapsed_time(ev[1]) / 1e3)
-            binding.osdn_check()
+            try:
+                binding.osdn_check()
+            except binding.OsdnError as e:
+                if not (diverges and e.status == binding.OSDN_ERR_RANGE):
+                    raise
+                range_flags.append(fn.__name__)
             return statistics.median(times)
 
         t_layer, t_scan, t_chunk = med(layer), med(scan), med(chunk)
@@ -538,7 +548,10 @@ def run_configs(args, dev, stream, hbm_peak, names=("layer_1p3b_apf", "longctx_r
                     "layer_ms": t_layer * 1e3, "tokens_per_s": w.B * w.T / t_layer,
                     "layer_roofline_frac": frac(b_layer, t_layer),
                     "scan_ms": t_scan * 1e3, "scan_roofline_frac": frac(b_scan, t_scan),
-                    "chunk_ms": t_chunk * 1e3, "chunk_roofline_frac": frac(b_chunk, t_chunk)})
+                    "chunk_ms": t_chunk * 1e3, "chunk_roofline_frac": frac(b_chunk, t_chunk),
+                    **({"range_status": {"calls": range_flags,
+                                         "note": "non-finite o/S expected: phase 2 diverges on raw keys"}}
+                       if diverges else {})})
         del g, kt
         torch.cuda.empty_cache()
     return out

@@ -22,6 +22,7 @@ _DTYPE_CODE = {torch.float32: OSDN_F32, torch.bfloat16: OSDN_BF16, torch.float16
 _STATUS = ["OSDN_OK", "OSDN_ERR_ARG", "OSDN_ERR_SHAPE", "OSDN_ERR_DTYPE", "OSDN_ERR_ALIGN",
            "OSDN_ERR_UNSUPPORTED", "OSDN_ERR_CUDA", "OSDN_ERR_TIMEOUT", "OSDN_ERR_CAPACITY",
            "OSDN_ERR_RANGE"]
+OSDN_ERR_TIMEOUT, OSDN_ERR_RANGE = _STATUS.index("OSDN_ERR_TIMEOUT"), _STATUS.index("OSDN_ERR_RANGE")
 
 _lib = None
 
