@@ -468,7 +468,6 @@ constexpr uint32_t WS_T = 0, WS_W = 8192, WS_L = 24576;
 // gated (OSGDN) chunks also carry their decay factors: gamma_t = prod_{l <= t} alpha_l and
 // rho_t = prod_{l > t} alpha_l as 32 fp16 pairs each (tokens 2i, 2i + 1), then gamma_C (fp32)
 constexpr uint32_t WS_GATE = 32768, WS_GAM = 0, WS_RHO = 128, WS_GC = 256;
-constexpr uint32_t WS_RDY = WS_GATE + 384;  // the chunk's ready word (all-ones until its images are stored)
 constexpr uint32_t WS_CHUNK = 33280;  // a multiple of 128 bytes
 
 template <int NW>
@@ -592,7 +591,6 @@ struct PrepWorker {
     uint32_t sbase, tbase, bar_tma, bar_mma, tph, mph;
     int tid, bar;
     bool tma_pending, mma_pending;
-    unsigned int* ready_pending;  // ready word of the last chunk whose images are still being stored
 
     __device__ void init(unsigned char* region, int t, int barrier_id) {
         sm = region;
@@ -603,7 +601,6 @@ struct PrepWorker {
         bar = barrier_id;
         tph = mph = 0;
         tma_pending = mma_pending = false;
-        ready_pending = nullptr;
         if (tid == 0) {
             tc::mbar_init(bar_tma, 1);
             tc::mbar_init(bar_mma, 1);
@@ -611,28 +608,14 @@ struct PrepWorker {
         }
     }
 
-    // Thread 0: once every store of the previous chunk has completed, its ready word is published
-    // (release, after a proxy fence: the stores went through the async proxy).
-    __device__ void publish_pending() {
-        if (ready_pending != nullptr) {
-            tc::bulk_wait_all();
-            asm volatile("fence.proxy.async.global;\n" ::: "memory");
-            asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(ready_pending), "r"(1u) : "memory");
-            ready_pending = nullptr;
-        }
-    }
-
     // Chunk n of head (b, h) into workspace slot `slot`.  Emission inputs (EMIT only): g_src[64],
     // r_src (stride H, or null), d_src[2 * KD] (hi, lo); tmKTout: tensor map of the k~ output.
-    // `ready_word` (or null): the chunk's ready word, set to 1 once its images (and k~) are stored;
-    // it is published at the start of the worker's next chunk, or by finish().
     template <bool EMIT>
     __device__ bool run(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmKT,
                         const float* __restrict__ beta, const float* __restrict__ alpha,
                         unsigned char* __restrict__ ws, size_t slot, int b,
                         int h, int n, int T, int H, const float* g_src, const float* r_src, const float* d_src,
-                        float dmin, float dmax, const CUtensorMap* tmKTout, uint32_t poll_limit = kMaxPolls,
-                        unsigned int* ready_word = nullptr, int next_h = -1, int next_row = 0) {
+                        float dmin, float dmax, const CUtensorMap* tmKTout, uint32_t poll_limit = kMaxPolls) {
         using namespace prep;
         float* AM = reinterpret_cast<float*>(sm + OFF_AM);
         float* TD = reinterpret_cast<float*>(sm + OFF_TD);
@@ -656,15 +639,6 @@ struct PrepWorker {
                 tc::tma_load_3d(sbase + OFF_KQ + kb * 16384 + 8192, tmQ, bar_tma, kb * 64, h, row);
                 if (!EMIT) tc::tma_load_3d(sbase + OFF_KT + kb * 8192, tmKT, bar_tma, kb * 64, h, row);
             }
-            if (next_h >= 0) {  // the worker's next chunk: its tiles into L2 while this one runs
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-                    tc::tma_prefetch_3d(tmK, kb * 64, next_h, next_row);
-                    tc::tma_prefetch_3d(tmQ, kb * 64, next_h, next_row);
-                    if (!EMIT) tc::tma_prefetch_3d(tmKT, kb * 64, next_h, next_row);
-                }
-            }
-            publish_pending();  // overlaps the wait for this chunk's tiles
         }
         tma_pending = true;
         if (tid < C) sbeta[tid] = beta[(static_cast<size_t>(row) + tid) * H + h];
@@ -867,7 +841,6 @@ struct PrepWorker {
             tc::bulk_store(dst + WS_W, sbase + OFF_KT, 16384);
             tc::bulk_store(dst + WS_L, sbase + OFF_ZT, 8192);
             tc::bulk_commit();
-            ready_pending = ready_word;
         }
         return true;
     }
@@ -879,141 +852,104 @@ struct PrepWorker {
             if (tma_pending) tc::mbar_wait(bar_tma, tph, kMaxPolls >> 4);
             if (mma_pending) tc::mbar_wait(bar_mma, mph, kMaxPolls >> 4);
         }
-        if (tid == 0) {
-            tc::bulk_wait_all();
-            if (!aborted) publish_pending();
-        }
+        if (tid == 0) tc::bulk_wait_all();
     }
 };
 
-// Persistent prep: three workers per CTA (one CTA per SM), chunks in chunk-major order (chunk q is
-// chunk n = q / BH of head bh = q % BH, so every head's early chunks come first); worker
-// g = 3 blockIdx.x + w takes q = g, g + 3 gridDim.x, ...  Each worker first sets the ready words of
-// its own chunks to all-ones and publishes each one after the chunk's images are stored; the chain
-// kernel, a programmatic dependent of this one, may start only after every CTA has done the reset.
-constexpr int PREP_NT = 384;
-constexpr int PREP_WORKERS = 3;
-constexpr uint32_t PREP_SMEM = PREP_WORKERS * prep::REGION + 1024;
+// One CTA loops over chunks q = blockIdx.x, blockIdx.x + gridDim.x, ...  (q = (b*H + h)*N + n).
 template <typename TIn>
-__global__ void __launch_bounds__(PREP_NT, 1)
+__global__ void __launch_bounds__(NTHREADS, 3)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ beta,
                   const float* __restrict__ alpha, unsigned char* __restrict__ ws, int T, int H, int N,
-                  int BH) {
+                  int total) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* base = reinterpret_cast<unsigned char*>(
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
-    __shared__ uint32_t s_tmem;
-    const int total = BH * N;
-    const int nworkers = static_cast<int>(gridDim.x) * PREP_WORKERS;
-    const int g = static_cast<int>(blockIdx.x) * PREP_WORKERS + w;
-    for (int q = g + wt * nworkers; q < total; q += 128 * nworkers) {
-        const int n = q / BH, bh = q - n * BH;
-        *reinterpret_cast<unsigned int*>(ws + (static_cast<size_t>(bh) * N + n) * WS_CHUNK + WS_RDY) = 0xffffffffu;
-    }
-    __threadfence();
-    __syncthreads();
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the chain kernel may start
-    constexpr uint32_t kCols = 512;  // >= 3 x 128, a power of two
-    static_assert(kCols >= PREP_WORKERS * prep::TMEM_COLS, "tensor memory");
-    if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), kCols);
-    PrepWorker<TIn> pw;
-    pw.init(base + w * prep::REGION, wt, 1 + w);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the chain kernel may set up
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + prep::OFF_BAR + 16);
+    PrepWorker<TIn> w;
+    w.init(sm, tid, 0);
     if (tid == 0) {
         tc::prefetch_tmap(&tmQ);
         tc::prefetch_tmap(&tmK);
         tc::prefetch_tmap(&tmKT);
     }
+    __syncthreads();
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), prep::TMEM_COLS);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tbase = s_tmem;
-    pw.tbase = tbase + w * prep::TMEM_COLS;
+    w.tbase = *tmem_slot;
     bool aborted = false;
-    for (int q = g; q < total; q += nworkers) {
-        const int n = q / BH, bh = q - n * BH, b = bh / H, h = bh - b * H;
-        const size_t slot = static_cast<size_t>(bh) * N + n;
-        unsigned int* rdy = reinterpret_cast<unsigned int*>(ws + slot * WS_CHUNK + WS_RDY);
-        int next_h = -1, next_row = 0;
-        if (q + nworkers < total) {
-            const int q2 = q + nworkers, n2 = q2 / BH, bh2 = q2 - n2 * BH;
-            next_h = bh2 % H;
-            next_row = (bh2 / H) * T + n2 * C;
-        }
-        if (!pw.template run<false>(&tmQ, &tmK, &tmKT, beta, alpha, ws, slot, b, h, n, T, H, nullptr, nullptr,
-                                    nullptr, 0.f, 0.f, nullptr, kMaxPolls, rdy, next_h, next_row)) {
+    for (int q = blockIdx.x; q < total; q += gridDim.x) {
+        const int bh = q / N, n = q - bh * N, b = bh / H, h = bh - b * H;
+        if (!w.template run<false>(&tmQ, &tmK, &tmKT, beta, alpha, ws, static_cast<size_t>(q), b, h, n, T, H, nullptr,
+                                   nullptr, nullptr, 0.f, 0.f, nullptr)) {
             aborted = true;
             break;
         }
     }
-    pw.finish(aborted);
+    w.finish(aborted);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(tbase, kCols);
+    if (warp == 0) tc::tmem_dealloc(w.tbase, prep::TMEM_COLS);
 }
 
-// Shared-memory and tensor-memory layout of the chain kernel for VS_ rows of S per CTA (64 or 128).
-// Twelve warps with fixed roles (one CTA per (batch, head, VS rows of S)):
+namespace chain {
+// Twelve warps with fixed roles (one CTA per (batch, head, 64 rows of S)):
 //   warps 0-3   S^T epilogue (fp32 S^T in tensor memory -> fp16 B operand in shared memory);
 //               warps 0-1 also the X epilogue (X = U - W S^T -> fp16 B operand)
-//   warps 4-7   operand staging: [-W; Q], [T'; 0] and [*; L] into tensor memory as fp16, and the
-//               V and K~ tiles to fp16 in place (V is the B operand of U = T'V, K~ the MN-major A
-//               operand of the state update K~^T X)
+//   warps 4-7   operand staging: [-W; Q], [T'; 0], K~^T and [*; L] into tensor memory as fp16,
+//               and the V tile to fp16 in place (the B operand of U = T'V)
 //   warp 8      tcgen05.mma issue (one thread)
 //   warp 9      TMA / bulk-copy producer (one thread)
 //   warps 10-11 O readout (tensor memory -> shared memory -> TMA store)
-// Only the S^T and X epilogues and the two S-dependent MMA groups lie on the serial path from one
-// chunk to the next.  With VS = 128 (one CTA per head) the A operands in tensor memory are single-
-// buffered so that S^T and the two accumulators R fit the 512 columns.
-template <int VS_>
-struct ChainCfg {
-    static constexpr int VSZ = VS_;
-    static constexpr int NVB = VS_ / 64;                    // 64-wide value blocks
-    static constexpr bool kSingle = VS_ > 64;               // single-buffered A operands
-    static constexpr uint32_t ST_Q = 0;                     // Q, two 64-wide key blocks (as loaded)
-    static constexpr uint32_t ST_W = 16384;                 // -W image (fp16)
-    static constexpr uint32_t ST_KT = 32768;                // K~ (as loaded; fp16 after staging)
-    static constexpr uint32_t ST_V = 49152;                 // V slice (as loaded; fp16 after staging)
-    static constexpr uint32_t ST_T = ST_V + NVB * 8192;     // T' image (fp16)
-    static constexpr uint32_t ST_L = ST_T + 8192;           // L image (fp16)
-    static constexpr uint32_t STAGE = ST_L + 8192;
-    static constexpr uint32_t OFF_X = 2 * STAGE;            // X (64 tokens x VS values), fp16
-    static constexpr uint32_t OFF_SS = OFF_X + NVB * 8192;  // S^T (128 key rows x VS values), fp16
-    static constexpr uint32_t OFF_O = OFF_SS + NVB * KD * 128;  // O tile for the TMA store
-    static constexpr uint32_t OFF_BAR = OFF_O + NVB * 8192;
-    static constexpr uint32_t SMEM_ALLOC = OFF_BAR + 256 + 1024;
-    static constexpr uint32_t LOAD_BYTES = 3 * 16384 + NVB * 8192 + 2 * 8192;
-    static_assert(SMEM_ALLOC <= 232448, "chain shared memory");
-    static_assert(STAGE % 1024 == 0 && OFF_X % 1024 == 0 && OFF_SS % 1024 == 0 && OFF_O % 1024 == 0,
-                  "swizzle atoms");
-    // tensor-memory columns (lanes 0-63 carry U / X, lanes 64-127 carry Q S^T / O)
-    static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_R = 0;                                  // R[2] (fp32)
-    static constexpr uint32_t COL_ST = 2 * VS_;                           // S^T (fp32, lane = key)
-    static constexpr uint32_t COL_QW = COL_ST + VS_;                      // A: [-W; Q], 64 columns a buffer
-    static constexpr uint32_t COL_TH = COL_QW + (kSingle ? 64 : 128);     // A: [T'; 0], 32 columns a buffer
-    static constexpr uint32_t COL_LH = COL_TH + (kSingle ? 32 : 64);      // A: [*; L]
-    static_assert(COL_LH + 32 <= TMEM_COLS, "tensor memory columns");
-    __device__ static constexpr uint32_t qw(int bb) { return COL_QW + (kSingle ? 0u : 64u * bb); }
-    __device__ static constexpr uint32_t th(int bb) { return COL_TH + (kSingle ? 0u : 32u * bb); }
-};
-namespace chain {
+// Every MMA takes its A operand from tensor memory; shared memory carries the loaded tiles, the
+// B operands and the two epilogue tiles.  Only the S^T and X epilogues and the two S-dependent
+// MMA groups lie on the serial path from one chunk to the next.
+constexpr int NT = 384;
+constexpr uint32_t ST_Q = 0;                           // Q, two 64-wide key blocks (as loaded)
+constexpr uint32_t ST_W = 16384;                       // -W image (fp16)
+constexpr uint32_t ST_KT = 32768;                      // K~ (as loaded)
+constexpr uint32_t ST_V = 49152;                       // V slice (as loaded)
+constexpr uint32_t ST_T = ST_V + (VS / 64) * 8192;     // T' image (fp16)
+constexpr uint32_t ST_L = ST_T + 8192;                 // L image (fp16)
+constexpr uint32_t STAGE = ST_L + 8192;
+constexpr uint32_t OFF_X = 2 * STAGE;                  // X (64 tokens x VS values), fp16
+constexpr uint32_t OFF_SS = OFF_X + (VS / 64) * 8192;  // S^T (128 key rows x VS values), fp16
+constexpr uint32_t OFF_O = OFF_SS + (VS / 64) * KD * 128;  // O tile for the TMA store
+constexpr uint32_t OFF_BAR = OFF_O + (VS / 64) * 8192;
+constexpr uint32_t SMEM_ALLOC = OFF_BAR + 256 + 1024;
+constexpr uint32_t LOAD_BYTES = 3 * 16384 + (VS / 64) * 8192 + 2 * 8192;
+static_assert(SMEM_ALLOC <= 232448, "chain shared memory");
+static_assert(STAGE % 1024 == 0 && OFF_X % 1024 == 0 && OFF_SS % 1024 == 0 && OFF_O % 1024 == 0,
+              "swizzle atoms");
+// tensor-memory columns (lanes 0-63 carry U / X, lanes 64-127 carry Q S^T / O)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_R = 0;              // R[2] (fp32)
+constexpr uint32_t COL_ST = 2 * VS;        // S^T (fp32, lane = key)
+constexpr uint32_t COL_QW = COL_ST + VS;   // A: [-W; Q] fp16, two buffers of 64 columns
+constexpr uint32_t COL_TH = COL_QW + 128;  // A: [T'; *] fp16, two buffers of 32 columns
+constexpr uint32_t COL_KT = COL_TH + 64;   // A: K~^T fp16 (lane = key)
+constexpr uint32_t COL_LH = COL_KT + 32;   // A: [*; L] fp16
+static_assert(COL_LH + 32 <= TMEM_COLS, "tensor memory columns");
 // mbarriers (byte offsets from OFF_BAR) and their arrival counts
 constexpr uint32_t B_FULL = 0;      // [2] stage loaded                       (1 + tx bytes)
-constexpr uint32_t B_FREE = 16;     // [2] stage no longer read               (update commit + 4 warps)
-constexpr uint32_t B_CONVA = 32;    // [2] [-W; Q], T', fp16 V staged (chunk parity) (4 warps)
+constexpr uint32_t B_FREE = 16;     // [2] stage no longer read               (U commit + 4 warps)
+constexpr uint32_t B_CONVA = 32;    // [2] [-W; Q], T', fp16 V staged (buffer b) (4 warps)
 constexpr uint32_t B_QS = 48;       // [2] [-W; Q] S^T done in R[b]           (commit)
-constexpr uint32_t B_KT = 64;       // [2] K~ in fp16 in its stage            (4 warps)
-constexpr uint32_t B_LH = 80;       // L staged                               (2 warps)
-constexpr uint32_t B_XRDY = 88;     // fp16 X in shared memory                (2 warps)
-constexpr uint32_t B_ST = 96;       // S^T update done                        (commit)
-constexpr uint32_t B_SRDY = 104;    // fp16 S^T in shared memory              (4 warps)
-constexpr uint32_t B_O = 112;       // [2] O accumulated in R[b]              (commit)
-constexpr uint32_t B_RFREE = 128;   // [2] O read out of R[b]                 (2 warps)
-constexpr uint32_t B_DRAIN = 144;   // final commit before tensor memory is released
-constexpr uint32_t TMEM_SLOT = 152, ABORT = 156;
+constexpr uint32_t B_KT = 64;       // K~^T staged                            (4 warps)
+constexpr uint32_t B_LH = 72;       // L staged                               (2 warps)
+constexpr uint32_t B_XRDY = 80;     // fp16 X in shared memory                (2 warps)
+constexpr uint32_t B_ST = 88;       // S^T update done                        (commit)
+constexpr uint32_t B_SRDY = 96;     // fp16 S^T in shared memory              (4 warps)
+constexpr uint32_t B_O = 104;       // [2] O accumulated in R[b]              (commit)
+constexpr uint32_t B_RFREE = 120;   // [2] O read out of R[b]                 (2 warps)
+constexpr uint32_t B_DRAIN = 136;   // final commit before tensor memory is released
+constexpr uint32_t TMEM_SLOT = 144, ABORT = 148;
 }  // namespace chain
 
 // Bounded wait that also gives up as soon as another role has recorded an abort.  Every lane of
@@ -1031,22 +967,6 @@ __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const
     for (uint32_t i = 0; i < kMaxPolls; ++i) {
         if (tc::mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 63u && *abort_flag) return false;
-    }
-    return false;
-}
-// A chunk's ready word, published by the prep worker that wrote its images (all-ones until then):
-// acquire loads, bounded, giving up early on an abort.  On success the async proxy (the TMA and
-// bulk loads that follow) is ordered after the acquire.
-__device__ __forceinline__ bool wait_ready(const unsigned int* p, const volatile int* abort_flag) {
-    for (uint32_t i = 0; i < kMaxPolls; ++i) {
-        uint32_t v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-        if (v != 0xffffffffu) {
-            asm volatile("fence.proxy.async.global;\n" ::: "memory");
-            return true;
-        }
-        if ((i & 63u) == 63u && *abort_flag) return false;
-        __nanosleep(32);
     }
     return false;
 }
@@ -1075,36 +995,30 @@ __device__ __forceinline__ bool pair_any(bool pred) {
 // One CTA per (batch, head, VS rows of S), serial over chunks.  Per chunk: U = T'V and
 // [X; Q S^T] = [U; 0] + [-W; Q] S^T; then S^T += K~^T X and O = Q S^T + L X.  T', -W and L come
 // from the workspace by bulk copy; Q, K~, V by TMA; O leaves by TMA.
-// Chunk m's images are read once its ready word (ready + (bh N + m) ready_stride) differs from
-// all-ones, so the chain can run while the prep is still producing later chunks; with ready ==
-// nullptr the kernel instead waits (griddepcontrol.wait) for the whole preceding kernel.
 // GATED (OSGDN, Appendix B.1, Eqs. (13)-(15)): with gamma_t / rho_t the gate products from the
 // chunk start through t / after t (formed by the prep, read from the workspace a chunk ahead), the
 // staging warps scale the rows of Q by gamma (O = diag(gamma) Q S^T + L X, the ratios being in L)
 // and the tokens of K~ by rho (S^T <- gamma_C S^T + (rho . K~)^T X); the S^T epilogue stores the
 // fp16 copy for the S-dependent products from the fp32 state it carries in registers, formed as
 // gamma_C S^T + Y from the update product Y = (rho . K~)^T X that the tensor cores leave on its own.
-template <typename TIn, bool GATED, int VS_>
-__global__ void __launch_bounds__(384, 1)
+template <typename TIn, bool GATED>
+__global__ void __launch_bounds__(chain::NT, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKT,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                   const unsigned char* __restrict__ ws, const unsigned int* ready, int ready_stride,
-                   const float* S0, float* S_out, int T, int H, int V, int N, float scale) {
-    using Cfg = ChainCfg<VS_>;
+                   const unsigned char* __restrict__ ws, const float* S0, float* S_out, int T, int H,
+                   int V, int N, float scale) {
     using namespace chain;
-    static_assert(!GATED || VS_ == 64, "the gated state is carried in registers: 64 rows of S per CTA");
-    constexpr int VSZ = VS_;
     constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int v0 = blockIdx.y * VSZ;
+    const int v0 = blockIdx.y * VS;
     const uint32_t sbase = tc::smem_u32(sm);
-    const uint32_t bars = sbase + Cfg::OFF_BAR;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Cfg::OFF_BAR + TMEM_SLOT);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Cfg::OFF_BAR + ABORT);
+    const uint32_t bars = sbase + OFF_BAR;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + TMEM_SLOT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_BAR + ABORT);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
     if (tid == 0) {
@@ -1115,8 +1029,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             tc::mbar_init(bars + B_QS + 8 * s, 1);
             tc::mbar_init(bars + B_O + 8 * s, 1);
             tc::mbar_init(bars + B_RFREE + 8 * s, 2);
-            tc::mbar_init(bars + B_KT + 8 * s, 4);
         }
+        tc::mbar_init(bars + B_KT, 4);
         tc::mbar_init(bars + B_LH, 2);
         tc::mbar_init(bars + B_XRDY, 2);
         tc::mbar_init(bars + B_ST, 1);
@@ -1130,15 +1044,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tc::prefetch_tmap(&tmO);
     }
     __syncthreads();
-    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    // Without ready words: launched as a programmatic dependent of the kernel that writes the
-    // chunk images and k~ (the setup above overlaps that kernel's tail), wait until its results
-    // are visible.  A no-op when launched without the attribute.
-    if (ready == nullptr) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // Launched as a programmatic dependent of the kernel that writes the chunk images and k~
+    // (the setup above overlaps that kernel's tail): wait until its results are visible.  A
+    // no-op when launched without the attribute.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     if (warp == 9) {
         // ================================ producer ============================================
@@ -1150,39 +1064,23 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     record_abort(abort_flag);
                     break;
                 }
-                if (ready != nullptr &&
-                    !wait_ready(ready + (static_cast<size_t>(bh) * N + m) * ready_stride, abort_flag)) {
-                    record_abort(abort_flag);
-                    break;
-                }
                 const uint32_t bar = bars + B_FULL + 8 * s;
-                const uint32_t st = sbase + s * Cfg::STAGE;
+                const uint32_t st = sbase + s * STAGE;
                 const int row = b * T + m * C;
                 const unsigned char* wsc = ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK;
-                tc::mbar_expect_tx(bar, Cfg::LOAD_BYTES);
+                tc::mbar_expect_tx(bar, LOAD_BYTES);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
-                    tc::tma_load_3d(st + Cfg::ST_Q + kb * 8192, &tmQ, bar, kb * 64, h, row);
-                    tc::tma_load_3d(st + Cfg::ST_KT + kb * 8192, &tmKT, bar, kb * 64, h, row);
+                    tc::tma_load_3d(st + ST_Q + kb * 8192, &tmQ, bar, kb * 64, h, row);
+                    tc::tma_load_3d(st + ST_KT + kb * 8192, &tmKT, bar, kb * 64, h, row);
                 }
 #pragma unroll
-                for (int vb = 0; vb < Cfg::NVB; ++vb)
-                    tc::tma_load_3d(st + Cfg::ST_V + vb * 8192, &tmV, bar, v0 + vb * 64, h, row);
-                tc::bulk_load(st + Cfg::ST_W, wsc + WS_W, 16384, bar);
-                tc::bulk_load(st + Cfg::ST_T, wsc + WS_T, 8192, bar);
-                tc::bulk_load(st + Cfg::ST_L, wsc + WS_L, 8192, bar);
+                for (int vb = 0; vb < VS / 64; ++vb)
+                    tc::tma_load_3d(st + ST_V + vb * 8192, &tmV, bar, v0 + vb * 64, h, row);
+                tc::bulk_load(st + ST_W, wsc + WS_W, 16384, bar);
+                tc::bulk_load(st + ST_T, wsc + WS_T, 8192, bar);
+                tc::bulk_load(st + ST_L, wsc + WS_L, 8192, bar);
                 last[s] = m;
-                if (m + 2 < N) {  // the inputs two chunks on into L2 (the images once they are ready)
-                    const int row2 = row + 2 * C;
-#pragma unroll
-                    for (int kb = 0; kb < 2; ++kb) {
-                        tc::tma_prefetch_3d(&tmQ, kb * 64, h, row2);
-                        tc::tma_prefetch_3d(&tmKT, kb * 64, h, row2);
-                    }
-#pragma unroll
-                    for (int vb = 0; vb < Cfg::NVB; ++vb) tc::tma_prefetch_3d(&tmV, v0 + vb * 64, h, row2);
-                    if (ready == nullptr) tc::bulk_prefetch_l2(wsc + 2 * WS_CHUNK, WS_GATE);
-                }
             }
             // nothing may still be landing in shared memory when the CTA exits
             for (int s = 0; s < 2; ++s)
@@ -1191,25 +1089,22 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     } else if (warp == 8) {
         // ================================ MMA issuer ==========================================
         if (lane == 0) {
-            const uint32_t id_h = tc::idesc_f16_f32(128, VSZ, false, true);   // fp16 A (tensor memory), MN-major B
-            const uint32_t id_kt = tc::idesc_f16_f32(128, VSZ, true, true);   // K~^T: MN-major A in shared memory
+            const uint32_t id_h = tc::idesc_f16_f32(128, VS, false, true);  // fp16 A (tensor memory), MN-major B
             // Descriptors are built once; an operand k steps further is the same descriptor plus
             // its byte offset / 16 (shared memory stays below 2^18 bytes, so the 14-bit address
-            // field never carries).  MN-major operands: 64-element atoms 8 KB apart (16 KB for
-            // the S^T copy), 8-row groups along K 1 KB apart.
-            const uint64_t d_v[2] = {tc::sdesc_sw128(sbase + Cfg::ST_V, 8192, 1024),
-                                     tc::sdesc_sw128(sbase + Cfg::STAGE + Cfg::ST_V, 8192, 1024)};
-            const uint64_t d_kt[2] = {tc::sdesc_sw128(sbase + Cfg::ST_KT, 8192, 1024),
-                                      tc::sdesc_sw128(sbase + Cfg::STAGE + Cfg::ST_KT, 8192, 1024)};
-            const uint64_t d_ss = tc::sdesc_sw128(sbase + Cfg::OFF_SS, KD * 128, 1024);
-            const uint64_t d_x = tc::sdesc_sw128(sbase + Cfg::OFF_X, 8192, 1024);
+            // field never carries).
+            const uint64_t d_v[2] = {tc::sdesc_sw128(sbase + ST_V, 8192, 1024),
+                                     tc::sdesc_sw128(sbase + STAGE + ST_V, 8192, 1024)};
+            const uint64_t d_ss = tc::sdesc_sw128(sbase + OFF_SS, KD * 128, 1024);
+            const uint64_t d_x = tc::sdesc_sw128(sbase + OFF_X, 8192, 1024);
             auto off = [](uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); };
             auto issue_u = [&](int m) {  // R[m & 1] = [T'; 0] V
                 const int bb = m & 1;
-                const uint32_t dR = tbase + Cfg::COL_R + bb * VSZ;
+                const uint32_t dR = tbase + COL_R + bb * VS;
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    tc::mma_f16_ts(dR, tbase + Cfg::th(bb) + 8 * k, d_v[bb] + off(k * 2048), id_h, k > 0);
+                    tc::mma_f16_ts(dR, tbase + COL_TH + bb * 32 + 8 * k, d_v[bb] + off(k * 2048), id_h, k > 0);
+                tc::mma_commit(bars + B_FREE + 8 * bb);
             };
             // U(m) needs chunk m staged and (from m = 2 on) R[m & 1] read out
             auto u_ready = [&](int m) -> bool {
@@ -1224,30 +1119,29 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
             for (int n = 0; ok && n < N; ++n) {
                 const int bb = n & 1;
-                const uint32_t dR = tbase + Cfg::COL_R + bb * VSZ;
+                const uint32_t dR = tbase + COL_R + bb * VS;
                 // [X; Q S^T] += [-W; Q] S^T: needs the fp16 copy of S after chunk n - 1
                 if (!(ok = thread_wait(bars + B_SRDY, n & 1, abort_flag))) break;
                 tc::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < KD / 16; ++k)
-                    tc::mma_f16_ts(dR, tbase + Cfg::qw(bb) + 8 * k, d_ss + off(k * 2048), id_h, 1);
+                    tc::mma_f16_ts(dR, tbase + COL_QW + bb * 64 + 8 * k, d_ss + off(k * 2048), id_h, 1);
                 tc::mma_commit(bars + B_QS + 8 * bb);
                 // S^T += K~^T X  (gated: Y = (rho . K~)^T X on its own; the epilogue adds gamma_C S^T)
-                if (!(ok = thread_wait(bars + B_XRDY, n & 1, abort_flag) && thread_wait(bars + B_KT + 8 * bb, (n >> 1) & 1, abort_flag)))
+                if (!(ok = thread_wait(bars + B_XRDY, n & 1, abort_flag) && thread_wait(bars + B_KT, n & 1, abort_flag)))
                     break;
                 tc::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    tc::mma_f16(tbase + Cfg::COL_ST, d_kt[bb] + off(k * 2048), d_x + off(k * 2048), id_kt,
-                                (GATED && k == 0) ? 0u : 1u);
+                    tc::mma_f16_ts(tbase + COL_ST, tbase + COL_KT + 8 * k, d_x + off(k * 2048), id_h,
+                                   (GATED && k == 0) ? 0u : 1u);
                 tc::mma_commit(bars + B_ST);
-                tc::mma_commit(bars + B_FREE + 8 * bb);  // the last MMA reading stage n & 1
                 // O = Q S^T + L X  (lanes 0-63 of the L operand only touch R rows already read)
                 if (!(ok = thread_wait(bars + B_LH, n & 1, abort_flag))) break;
                 tc::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    tc::mma_f16_ts(dR, tbase + Cfg::COL_LH + 8 * k, d_x + off(k * 2048), id_h, 1);
+                    tc::mma_f16_ts(dR, tbase + COL_LH + 8 * k, d_x + off(k * 2048), id_h, 1);
                 tc::mma_commit(bars + B_O + 8 * bb);
                 if (n + 1 < N) {  // the next chunk's U = T'V, off the serial path
                     if (!(ok = u_ready(n + 1))) break;
@@ -1272,9 +1166,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             if (pair_any(!ok)) { ok = false; break; }
             tc::tc_fence_after();
 #pragma unroll
-            for (int q2 = 0; q2 < VSZ / 32; ++q2) {
+            for (int q2 = 0; q2 < VS / 32; ++q2) {
                 float o[32];
-                tc::tmem_ld32(tbase + lane_base + Cfg::COL_R + bb * VSZ + q2 * 32, o);
+                tc::tmem_ld32(tbase + lane_base + COL_R + bb * VS + q2 * 32, o);
                 tc::tmem_ld_wait();
                 nonfinite |= any_nonfinite32(o);
 #pragma unroll
@@ -1285,7 +1179,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     uint4 u;
                     VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u), ov);
                     VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u) + 4, ov + 4);
-                    *reinterpret_cast<uint4*>(sm + Cfg::OFF_O + ((q2 * 32) / 64) * 8192 +
+                    *reinterpret_cast<uint4*>(sm + OFF_O + ((q2 * 32) / 64) * 8192 +
                                               tc::sw128_off(r, ((q2 * 32) % 64) / 8 + c)) = u;
                 }
             }
@@ -1296,8 +1190,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             pair_any(false);  // both warps' rows are in shared memory
             if (issuer) {
 #pragma unroll
-                for (int vb = 0; vb < Cfg::NVB; ++vb)
-                    tc::tma_store_3d(&tmO, sbase + Cfg::OFF_O + vb * 8192, v0 + vb * 64, h, b * T + n * C);
+                for (int vb = 0; vb < VS / 64; ++vb)
+                    tc::tma_store_3d(&tmO, sbase + OFF_O + vb * 8192, v0 + vb * 64, h, b * T + n * C);
                 tc::bulk_commit();
             }
         }
@@ -1309,12 +1203,12 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const int w4 = warp - 4;
         const bool low = w4 < 2;            // lanes 0-63: -W and T' rows; lanes 64-127: Q and L rows
         const int r = (w4 & 1) * 32 + lane;  // row 0..63 of the 64-row tiles
-        if (!low) {  // [T'; 0]: the bottom 64 rows stay zero in every buffer
+        if (!low) {  // [T'; 0]: the bottom 64 rows stay zero in both buffers
             uint32_t z[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = 0u;
 #pragma unroll
-            for (int c = 0; c < (Cfg::kSingle ? 1 : 2); ++c) tc::tmem_st32u(tbase + lane_base + Cfg::COL_TH + 32 * c, z);
+            for (int c = 0; c < 2; ++c) tc::tmem_st32u(tbase + lane_base + COL_TH + 32 * c, z);
             tc::tmem_st_wait();
         }
         bool ok = true;
@@ -1333,15 +1227,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         for (int m = 0; ok && m < N; ++m) {
             const int s = m & 1, bb = m & 1;
-            unsigned char* stg = sm + s * Cfg::STAGE;
+            const unsigned char* stg = sm + s * STAGE;
             if (!(ok = warp_wait(bars + B_FULL + 8 * s, (m >> 1) & 1, abort_flag))) break;
-            // the A buffers were last read by U and [-W; Q] S^T of chunk m - 1 (single buffers)
-            // or m - 2 (double buffers)
-            constexpr int kLag = Cfg::kSingle ? 1 : 2;
-            if (m >= kLag) {
-                const int mp = m - kLag;
-                if (!(ok = warp_wait(bars + B_QS + 8 * (mp & 1), (mp >> 1) & 1, abort_flag))) break;
-            }
+            // buffer bb was last read by U and [-W; Q] S^T of chunk m - 2
+            if (m >= 2 && !(ok = warp_wait(bars + B_QS + 8 * bb, ((m - 2) >> 1) & 1, abort_flag))) break;
             tc::tc_fence_after();
             if (low) {
                 uint32_t wv[32];
@@ -1349,24 +1238,24 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(stg + Cfg::ST_W + kb * 8192 + tc::sw128_off(r, c));
+                        const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_W + kb * 8192 + tc::sw128_off(r, c));
                         wv[c * 4 + 0] = u.x;
                         wv[c * 4 + 1] = u.y;
                         wv[c * 4 + 2] = u.z;
                         wv[c * 4 + 3] = u.w;
                     }
-                    tc::tmem_st32u(tbase + lane_base + Cfg::qw(bb) + kb * 32, wv);
+                    tc::tmem_st32u(tbase + lane_base + COL_QW + bb * 64 + kb * 32, wv);
                 }
                 uint32_t th[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 u = *reinterpret_cast<const uint4*>(stg + Cfg::ST_T + tc::sw128_off(r, c));
+                    const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_T + tc::sw128_off(r, c));
                     th[c * 4 + 0] = u.x;
                     th[c * 4 + 1] = u.y;
                     th[c * 4 + 2] = u.z;
                     th[c * 4 + 3] = u.w;
                 }
-                tc::tmem_st32u(tbase + lane_base + Cfg::th(bb), th);
+                tc::tmem_st32u(tbase + lane_base + COL_TH + bb * 32, th);
             } else {
                 uint32_t qh[32];
                 uint32_t gq = 0;  // gated: row r of Q scaled by gamma_r (an fp16 pair of it)
@@ -1379,44 +1268,42 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(stg + Cfg::ST_Q + kb * 8192 + tc::sw128_off(r, c));
+                        const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_Q + kb * 8192 + tc::sw128_off(r, c));
                         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             qh[c * 4 + j] = GATED ? mul_f16x2<kBf16>(w[j], gq) : (kBf16 ? bf16x2_to_f16x2(w[j]) : w[j]);
                     }
-                    tc::tmem_st32u(tbase + lane_base + Cfg::qw(bb) + kb * 32, qh);
+                    tc::tmem_st32u(tbase + lane_base + COL_QW + bb * 64 + kb * 32, qh);
                 }
             }
-            // V to fp16 in place (NVB x 4 x 16 bytes per thread of the four staging warps)
-            if constexpr (kBf16) convert_bf16_to_f16<Cfg::NVB * 4>(stg + Cfg::ST_V, w4 * 32 + lane);
+            // V to fp16 in place (4 x 16 bytes per thread of the four staging warps)
+            if constexpr (kBf16) convert_bf16_to_f16<(VS / 64) * 4>(const_cast<unsigned char*>(stg) + ST_V, w4 * 32 + lane);
             tc::tmem_st_wait();
             warp_publish(bars + B_CONVA + 8 * bb, lane);
-            // K~ to fp16 in place (gated: token t scaled by rho_t), the MN-major A operand of the
-            // state update; uint4 i of thread j covers token (i % 4) * 16 + j / 8 of its key block
-            if (kBf16 || GATED) {
-                const int j = w4 * 32 + lane;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    uint4* p = reinterpret_cast<uint4*>(stg + Cfg::ST_KT) + i * 128 + j;
-                    uint4 u = *p;
-                    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                    if (GATED) {
-                        const int t = (i & 3) * 16 + (j >> 3);
-                        const uint32_t rp = __shfl_sync(0xffffffffu, rpair, t >> 1);
-                        const uint32_t r16 = (t & 1) ? (rp >> 16) : (rp & 0xffffu);
-                        const uint32_t rr = r16 | (r16 << 16);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) w[e] = mul_f16x2<kBf16>(w[e], rr);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) w[e] = bf16x2_to_f16x2(w[e]);
-                    }
-                    *p = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            warp_publish(bars + B_KT + 8 * s, lane);
             if (GATED && m + 1 < N) gates_of(m + 1);
+            // K~^T (lane = key); its buffer was last read by the S^T update of chunk m - 1
+            if (m >= 1 && !(ok = warp_wait(bars + B_ST, (m - 1) & 1, abort_flag))) break;
+            tc::tc_fence_after();
+            {  // thread k gathers key coordinate k of the 64 tokens
+                const int k = w4 * 32 + lane, kb = k >> 6, c = (k & 63) >> 3, e = k & 7;
+                const unsigned char* kt = stg + ST_KT + kb * 8192 + 2 * e;
+                uint32_t kw[32];
+#pragma unroll
+                for (int t2 = 0; t2 < 32; ++t2) {
+                    const uint32_t a0 = *reinterpret_cast<const uint16_t*>(kt + tc::sw128_off(2 * t2, c));
+                    const uint32_t a1 = *reinterpret_cast<const uint16_t*>(kt + tc::sw128_off(2 * t2 + 1, c));
+                    const uint32_t pr = a0 | (a1 << 16);
+                    if (GATED) {  // tokens 2 t2, 2 t2 + 1 scaled by their rho
+                        kw[t2] = mul_f16x2<kBf16>(pr, __shfl_sync(0xffffffffu, rpair, t2));
+                    } else {
+                        kw[t2] = kBf16 ? bf16x2_to_f16x2(pr) : pr;
+                    }
+                }
+                tc::tmem_st32u(tbase + lane_base + COL_KT, kw);
+                tc::tmem_st_wait();
+                warp_publish(bars + B_KT, lane);
+            }
             // L rows (lanes 64-127); the L operand was last read by O of chunk m - 1
             if (!low) {
                 if (m >= 1 && !(ok = warp_wait(bars + B_O + 8 * ((m - 1) & 1), ((m - 1) >> 1) & 1, abort_flag))) break;
@@ -1424,13 +1311,13 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 uint32_t lh[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 u = *reinterpret_cast<const uint4*>(stg + Cfg::ST_L + tc::sw128_off(r, c));
+                    const uint4 u = *reinterpret_cast<const uint4*>(stg + ST_L + tc::sw128_off(r, c));
                     lh[c * 4 + 0] = u.x;
                     lh[c * 4 + 1] = u.y;
                     lh[c * 4 + 2] = u.z;
                     lh[c * 4 + 3] = u.w;
                 }
-                tc::tmem_st32u(tbase + lane_base + Cfg::COL_LH, lh);
+                tc::tmem_st32u(tbase + lane_base + COL_LH, lh);
                 tc::tmem_st_wait();
                 warp_publish(bars + B_LH, lane);
             }
@@ -1449,22 +1336,22 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         };
         // gated: this lane's row of S^T (fp32) carried in registers; the update MMA leaves
         // Y = (rho . K~)^T X in tensor memory and S^T <- gamma_C S^T + Y is formed here
-        float st[GATED ? VSZ : 1];
+        float st[GATED ? VS : 1];
         {  // S0 slice -> S^T (tensor memory, or registers when gated) and its fp16 operand copy
             float sv[32];
 #pragma unroll
-            for (int half = 0; half < VSZ / 32; ++half) {
+            for (int half = 0; half < VS / 32; ++half) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     sv[j] = S0 ? S0[(static_cast<size_t>(bh) * V + v0 + half * 32 + j) * KD + k] : 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    st_row_chunk(sm + Cfg::OFF_SS + ((half * 32) / 64) * (KD * 128), k, ((half * 32) % 64) / 8 + c, sv + 8 * c);
-                if constexpr (GATED) {
+                    st_row_chunk(sm + OFF_SS + ((half * 32) / 64) * (KD * 128), k, ((half * 32) % 64) / 8 + c, sv + 8 * c);
+                if (GATED) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) st[half * 32 + j] = sv[j];
                 } else {
-                    tc::tmem_st32(tbase + lane_base + Cfg::COL_ST + half * 32, sv);
+                    tc::tmem_st32(tbase + lane_base + COL_ST + half * 32, sv);
                 }
             }
             if (!GATED) tc::tmem_st_wait();
@@ -1478,47 +1365,44 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 if (!(ok = warp_wait(bars + B_QS + 8 * bb, (n >> 1) & 1, abort_flag))) break;
                 tc::tc_fence_after();
 #pragma unroll
-                for (int q2 = 0; q2 < VSZ / 32; ++q2) {
+                for (int q2 = 0; q2 < VS / 32; ++q2) {
                     float x[32];
-                    tc::tmem_ld32(tbase + lane_base + Cfg::COL_R + bb * VSZ + q2 * 32, x);
+                    tc::tmem_ld32(tbase + lane_base + COL_R + bb * VS + q2 * 32, x);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc)
-                        st_row_chunk(sm + Cfg::OFF_X + ((q2 * 32) / 64) * 8192, tid, ((q2 * 32) % 64) / 8 + cc, x + 8 * cc);
+                        st_row_chunk(sm + OFF_X + ((q2 * 32) / 64) * 8192, tid, ((q2 * 32) % 64) / 8 + cc, x + 8 * cc);
                 }
                 warp_publish(bars + B_XRDY, lane);
             }
             if (!(ok = warp_wait(bars + B_ST, n & 1, abort_flag))) break;
             tc::tc_fence_after();
-            bool bad = false;
-            // 64 columns of S^T at a time (tensor memory -> fp16 operand copy, or S_out at the end)
+            float sv[VS];
 #pragma unroll
-            for (int vb = 0; vb < VSZ / 64; ++vb) {
-                float sv[64];
-                tc::tmem_ld32(tbase + lane_base + Cfg::COL_ST + vb * 64, *reinterpret_cast<float(*)[32]>(sv));
-                tc::tmem_ld32(tbase + lane_base + Cfg::COL_ST + vb * 64 + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
-                tc::tmem_ld_wait();
-                if constexpr (GATED) {
+            for (int q2 = 0; q2 < VS / 32; ++q2)
+                tc::tmem_ld32(tbase + lane_base + COL_ST + q2 * 32, *reinterpret_cast<float(*)[32]>(sv + q2 * 32));
+            tc::tmem_ld_wait();
+            if (GATED) {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        st[vb * 64 + j] = fmaf(gcn, st[vb * 64 + j], sv[j]);
-                        sv[j] = st[vb * 64 + j];
-                    }
-                }
-                if (n + 1 < N) {
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        st_row_chunk(sm + Cfg::OFF_SS + vb * (KD * 128), k, cc, sv + 8 * cc);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        bad |= !isfinite(sv[j]);
-                        S_out[(static_cast<size_t>(bh) * V + v0 + vb * 64 + j) * KD + k] = sv[j];
-                    }
+                for (int j = 0; j < VS; ++j) {
+                    st[j] = fmaf(gcn, st[j], sv[j]);
+                    sv[j] = st[j];
                 }
             }
-            if (n + 1 < N) warp_publish(bars + B_SRDY, lane);
-            if (bad) atomicOr(&g_range_flag, 1u);
+            if (n + 1 < N) {
+#pragma unroll
+                for (int cc = 0; cc < VS / 8; ++cc)
+                    st_row_chunk(sm + OFF_SS + ((cc * 8) / 64) * (KD * 128), k, cc % 8, sv + 8 * cc);
+                warp_publish(bars + B_SRDY, lane);
+            } else {
+                bool bad = false;
+#pragma unroll
+                for (int j = 0; j < VS; ++j) {
+                    bad |= !isfinite(sv[j]);
+                    S_out[(static_cast<size_t>(bh) * V + v0 + j) * KD + k] = sv[j];
+                }
+                if (bad) atomicOr(&g_range_flag, 1u);
+            }
         }
         if (!ok) record_abort(abort_flag);
     }
@@ -1526,24 +1410,19 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(tbase, Cfg::TMEM_COLS);
-    // The kernel that produced the images may have CTAs still finishing after their last ready
-    // word: this grid completes only after it, so that later work on the stream sees both done.
-    if (ready != nullptr) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
 }
 
 // =============================================================================================
 // Fused layer forward: phase 1 and the S-independent part of phase 2 in one cooperative launch.
 // CTAs 0 .. BH-1 run the blocked scan of one (batch, head) each and store every 64-token block's
-// step sizes and start state to the workspace as soon as it is solved; every other CTA runs three
+// step sizes and start state to the workspace as soon as it is solved; every other CTA runs two
 // prep workers that take chunks in block-major order from a counter, poll (bounded) for their
-// block's values, form the chunk's write keys from them and do the chunk prep, then publish the
-// chunk's ready word.  Phase 1 keeps B*H SMs busy for its whole duration, so the prep of each chunk
-// hides behind the scan of later blocks.  A scan CTA whose head is done either joins the prep
-// workers (`join`) or leaves, handing its SM to the chain kernel that follows the ready words.
-// All CTAs are resident at once (cooperative launch), so the waits always end.  The workspace's
-// scan part, the ready words and the counter hold all-ones at launch (the counter's first
-// increment wraps it to chunk 0).
+// block's values, form the chunk's write keys from them and do the chunk prep.  Phase 1 keeps B*H
+// SMs busy for its whole duration, so the prep of each chunk hides behind the scan of later
+// blocks.  All CTAs are resident at once (cooperative launch), so the waits always end.  The
+// workspace's scan part and the counter hold all-ones at launch (the counter's first increment
+// wraps it to chunk 0).
 // =============================================================================================
 constexpr int LAYER_NT = 384;      // phase 1 on threads 0-255 of the first B*H CTAs; three prep workers
 constexpr int LAYER_WORKERS = 3;
@@ -1553,8 +1432,7 @@ __global__ void __launch_bounds__(LAYER_NT, 1)
 layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* counter,
                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ alpha,
-                       unsigned char* __restrict__ cws, unsigned int* ready, int join, int N, int BH,
-                       uint32_t poll_limit) {
+                       unsigned char* __restrict__ cws, int N, int BH, uint32_t poll_limit) {
     extern __shared__ unsigned char smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, w = tid >> 7, wt = tid & 127;
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the chain kernel may set up
@@ -1585,10 +1463,7 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
     pw.tbase = tbase + w * prep::TMEM_COLS;
     const int total = BH * N;
     bool aborted = false;
-    // without `join` a scan CTA leaves when its head is done, so that the chain kernel (a
-    // programmatic dependent following the ready words) can take its SM
-    const bool work = join || static_cast<int>(blockIdx.x) >= BH;
-    while (work) {
+    for (;;) {
         if (wt == 0) s_q[w] = static_cast<int>(atomicAdd(counter, 1u) + 1u);
         bar_sync128(1 + w);
         const int q = s_q[w];
@@ -1599,8 +1474,7 @@ layer_scan_prep_kernel(OsdnScanArgs sa, float* ws_g, float* ws_d, unsigned int* 
         const float* r_src = HAS_R ? sa.r + row0 + static_cast<size_t>(m) * C * H : nullptr;
         const float* d_src = ws_d + (static_cast<size_t>(bh) * N + m) * (2 * KD);
         if (!pw.template run<true>(&tmQ, &tmK, nullptr, sa.beta, alpha, cws, static_cast<size_t>(bh) * N + m, b, h, m, T, H,
-                                   g_src, r_src, d_src, sa.d_min, sa.d_max, &tmKT, poll_limit,
-                                   ready + static_cast<size_t>(bh) * N + m)) {
+                                   g_src, r_src, d_src, sa.d_min, sa.d_max, &tmKT, poll_limit)) {
             aborted = true;
             break;
         }
@@ -1661,54 +1535,8 @@ cudaError_t set_smem(K kernel, uint32_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
-// Rows of S per chain CTA: 128 (one CTA per head) when the heads leave at least 16 SMs to the
-// prep kernel running beside the chain, else 64.  The same rule serves the chunk and layer calls,
-// so both run the same chain kernel on a given shape.  The gated chain carries S in registers and
-// keeps 64 rows.
-int chain_vs(const OsdnChunkArgs& a) {
-    const int heads = a.B * a.H;
-    if (!a.alpha && a.V % 128 == 0 && heads * (a.V / 128) <= num_sms() - 16) return 128;
-    return 64;
-}
-
 template <typename TIn>
-cudaError_t launch_chain(const OsdnChunkArgs& a, const CUtensorMap& mq, const CUtensorMap& mkt, const CUtensorMap& mv,
-                         const CUtensorMap& mo, const unsigned char* wsc, const unsigned int* ready, int ready_stride,
-                         cudaStream_t s) {
-    const int N = a.T / C;
-    const int vs = chain_vs(a);
-    auto kernel = a.alpha ? chunk_chain_kernel<TIn, true, 64>
-                          : (vs == 128 ? chunk_chain_kernel<TIn, false, 128> : chunk_chain_kernel<TIn, false, 64>);
-    const uint32_t smem = vs == 128 ? ChainCfg<128>::SMEM_ALLOC : ChainCfg<64>::SMEM_ALLOC;
-    dim3 gc(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / vs));
-    // programmatic dependent launch: the chain CTAs take SMs as they become free and follow the
-    // ready words (or, without them, wait with griddepcontrol.wait for the previous kernel)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = gc;
-    cfg.blockDim = dim3(384);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, mq, mkt, mv, mo, wsc, ready, ready_stride, a.S0, a.S_out, a.T,
-                                       a.H, a.V, N, a.scale);
-    if (e == cudaErrorNotSupported) {  // no dependent launch here: an ordinary one
-        (void)cudaGetLastError();
-        kernel<<<gc, dim3(384), smem, s>>>(mq, mkt, mv, mo, wsc, ready, ready_stride, a.S0, a.S_out, a.T, a.H, a.V, N,
-                                           a.scale);
-        e = cudaGetLastError();
-    }
-    return e;
-}
-
-// With a workspace: the prep kernel and the chain kernel.  chain_only (the layer call, whose
-// cooperative kernel did the prep): only the chain, following `layer_ready` (one word per chunk).
-template <typename TIn>
-cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s, bool chain_only = false,
-                      const unsigned int* layer_ready = nullptr) {
+cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s, bool chain_only = false) {
     const CUtensorMapDataType dt = std::is_same<TIn, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const long long rows = static_cast<long long>(a.B) * a.T;
@@ -1720,38 +1548,52 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        cudaError_t e[5] = {set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC),
-                            set_smem(chunk_prep_kernel<TIn>, PREP_SMEM),
-                            set_smem(chunk_chain_kernel<TIn, false, 64>, ChainCfg<64>::SMEM_ALLOC),
-                            set_smem(chunk_chain_kernel<TIn, true, 64>, ChainCfg<64>::SMEM_ALLOC),
-                            set_smem(chunk_chain_kernel<TIn, false, 128>, ChainCfg<128>::SMEM_ALLOC)};
-        for (cudaError_t x : e)
-            if (x != cudaSuccess && attr_err == cudaSuccess) attr_err = x;
+        cudaError_t e1 = set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC);
+        cudaError_t e2 = set_smem(chunk_prep_kernel<TIn>, prep::SMEM_ALLOC);
+        cudaError_t e3 = set_smem(chunk_chain_kernel<TIn, false>, chain::SMEM_ALLOC);
+        cudaError_t e4 = set_smem(chunk_chain_kernel<TIn, true>, chain::SMEM_ALLOC);
+        attr_err = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : (e3 != cudaSuccess ? e3 : e4));
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int N = a.T / C;
     const size_t need = static_cast<size_t>(a.B) * a.H * N * WS_CHUNK;
-    const bool gated = a.alpha != nullptr;
+    dim3 block(NTHREADS);
     if (ws != nullptr && ws_bytes >= need) {
-        unsigned char* w = static_cast<unsigned char*>(ws);
-        if (chain_only)
-            return launch_chain<TIn>(a, mq, mkt, mv, mo, w, gated ? nullptr : layer_ready, 1, s);
         const int total = a.B * a.H * N;
-        const int chain_ctas = a.B * a.H * (a.V / chain_vs(a));
-        // the prep leaves the chain's SMs free when they fit beside it (ungated); one CTA per SM
-        int gp = (!gated && chain_ctas <= num_sms() - 16) ? num_sms() - chain_ctas : num_sms();
-        const int need_ctas = (total + PREP_WORKERS - 1) / PREP_WORKERS;
-        if (gp > need_ctas) gp = need_ctas;
-        chunk_prep_kernel<TIn><<<dim3(static_cast<unsigned>(gp)), dim3(PREP_NT), PREP_SMEM, s>>>(
-            mq, mk, mkt, a.beta, a.alpha, w, a.T, a.H, N, a.B * a.H);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        const unsigned int* rdy = gated ? nullptr : reinterpret_cast<const unsigned int*>(w + WS_RDY);
-        return launch_chain<TIn>(a, mq, mkt, mv, mo, w, rdy, static_cast<int>(WS_CHUNK / 4), s);
+        dim3 gp(static_cast<unsigned>(total < 3 * num_sms() ? total : 3 * num_sms()));
+        if (!chain_only) {
+            chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta, a.alpha,
+                                                                      static_cast<unsigned char*>(ws), a.T, a.H, N, total);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        dim3 gc(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
+        // programmatic dependent launch: the chain CTAs take SMs as the previous kernel's CTAs
+        // leave and wait (griddepcontrol.wait) for its results
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = gc;
+        cfg.blockDim = dim3(chain::NT);
+        cfg.dynamicSmemBytes = chain::SMEM_ALLOC;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const unsigned char* wsc = static_cast<const unsigned char*>(ws);
+        auto chain_kernel = a.alpha ? chunk_chain_kernel<TIn, true> : chunk_chain_kernel<TIn, false>;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel, mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T, a.H, a.V,
+                                           N, a.scale);
+        if (e == cudaErrorNotSupported) {  // no dependent launch here: an ordinary one
+            (void)cudaGetLastError();
+            chain_kernel<<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T,
+                                                                       a.H, a.V, N, a.scale);
+            e = cudaGetLastError();
+        }
+        return e;
     }
     if (a.alpha) return cudaErrorNotSupported;  // the gate is carried by the two-kernel path only
     dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
-    dim3 block(NTHREADS);
     chunk_tc_kernel<TIn><<<grid, block, fused::SMEM_ALLOC, s>>>(mq, mk, mkt, mv, a.beta, a.S0, static_cast<TIn*>(a.o),
                                                         a.S_out, a.T, a.H, a.V, a.scale);
     return cudaGetLastError();
@@ -1763,18 +1605,17 @@ bool tc_covers(const OsdnChunkArgs& a) {
            (a.dtype == OSDN_BF16 || a.dtype == OSDN_F16) && !(a.alpha && a.alpha_per_key);
 }
 
-// Workspace of the fused layer: [scan: step sizes, block-start states][chunk ready words][chunk
-// counter][chunk images], each part 256-byte aligned.
+// Workspace of the fused layer: [scan: step sizes, block-start states][chunk counter][chunk
+// images], each part 256-byte aligned.
 struct LayerWs {
-    size_t scan, ready, counter, chunk, total;
+    size_t scan, counter, chunk, total;
 };
 LayerWs layer_ws(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     LayerWs l{};
     const size_t nblk = static_cast<size_t>(ca.T / C);
     l.scan = 0;
-    l.ready = up(osdn_scan_block_workspace_bytes(sa));
-    l.counter = l.ready + up(static_cast<size_t>(ca.B) * ca.H * nblk * 4);
+    l.counter = up(osdn_scan_block_workspace_bytes(sa));
     l.chunk = l.counter + 256;
     l.total = l.chunk + up(static_cast<size_t>(ca.B) * ca.H * nblk * WS_CHUNK);
     return l;
@@ -1808,7 +1649,7 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     const int grid = per_sm * num_sms();
     if (grid <= ca.B * ca.H) return cudaErrorNotSupported;
     const LayerWs l = layer_ws(sa, ca);
-    // all-ones over the scan part (nothing published yet), the ready words and the counter
+    // all-ones over the scan part (nothing published yet) and the counter
     cudaError_t e = cudaMemsetAsync(ws + l.scan, 0xff, l.counter + 4 - l.scan, s);
     if (e != cudaSuccess) return e;
     OsdnScanArgs sa2 = sa;
@@ -1816,14 +1657,11 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     float* ws_d = ws_g + static_cast<size_t>(sa.B) * sa.H * sa.T;
     unsigned int* counter = reinterpret_cast<unsigned int*>(ws + l.counter);
     unsigned char* cws = ws + l.chunk;
-    unsigned int* ready = reinterpret_cast<unsigned int*>(ws + l.ready);
     int N = ca.T / C, BH = ca.B * ca.H;
     const float* alpha = ca.alpha;
-    // the gated chain waits for the whole kernel, so the scan CTAs then help with the prep
-    int join = alpha != nullptr ? 1 : 0;
     uint32_t poll_limit = g_poll_limit.load();
     if (poll_limit == 0) poll_limit = kMaxPolls;
-    void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &mkt, &alpha, &cws, &ready, &join, &N, &BH, &poll_limit};
+    void* args[] = {&sa2, &ws_g, &ws_d, &counter, &mq, &mk, &mkt, &alpha, &cws, &N, &BH, &poll_limit};
     e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
                                     dim3(LAYER_NT), args, smem, s);
     if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer resident CTAs than expected: two calls
@@ -1832,7 +1670,7 @@ cudaError_t launch_layer_t(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, unsi
     }
     if (e != cudaSuccess) return e;
     // the serial chain over the chunk images (same kernel as osdn_chunk_fwd's workspace path)
-    return launch_tc<TIn>(ca, cws, l.total - l.chunk, s, /*chain_only=*/true, ready);
+    return launch_tc<TIn>(ca, cws, l.total - l.chunk, s, /*chain_only=*/true);
 }
 
 }  // namespace

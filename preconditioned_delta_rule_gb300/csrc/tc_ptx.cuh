@@ -118,11 +118,6 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
                  "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
-// Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-                 : "memory");
-}
 // Tiled TMA store shared -> global, tracked by the issuing thread's bulk groups.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
