@@ -133,12 +133,18 @@ size_t osdn_precond_scan_workspace_bytes(int B, int T, int H, int K, osdn_dtype 
  *   scale    multiplies q (1.0 gives o_t = S_t q_t as in the equations; Listing 1 uses K^-1/2).
  *   workspace, workspace_bytes
  *            optional caller-owned device scratch (16-byte aligned).  When it holds at least
- *            osdn_chunk_fwd_workspace_bytes(...) bytes, the tensor-core path splits into a
- *            parallel kernel over all chunks (everything that does not depend on S: the UT
- *            transform T' and W, kept as fp16 in the workspace) and a serial kernel over chunks;
- *            with NULL or a smaller workspace one fused kernel does both (slower, no scratch).
- *            Results are the same either way.  The workspace is overwritten; its contents on
- *            return are unspecified.
+ *            B * H * (T / 64) * 33280 bytes, the tensor-core path splits into a parallel kernel
+ *            over all chunks (everything that does not depend on S: the UT transform T' and W,
+ *            kept as fp16 in the workspace) and a serial kernel over chunks; with NULL or a
+ *            smaller workspace one fused kernel does both (slower, no scratch).  With few heads
+ *            (B*H*(V/64) CTAs leave most SMs idle) and at least 32 chunks, a workspace of
+ *            osdn_chunk_fwd_workspace_bytes(...) bytes (more than the above) also lets the serial
+ *            pass run in segments side by side: each later segment starts from a zero state
+ *            beside a pass that carries the product of the chunk transitions (I - K~^T W)
+ *            (Appendix A.2, Eq. (10)); the segment start states are chained afterwards and the
+ *            later segments' outputs corrected.  The paths agree to the fp16 operand rounding
+ *            (o may differ by one unit of its last place).  The workspace is overwritten; its
+ *            contents on return are unspecified.
  * bf16/f16 inputs with K = V = 128 run on the tensor-core kernels (TMA + tcgen05, fp16
  * operands, fp32 accumulation, fp32 state); other shapes and fp32 inputs run an fp32
  * CUDA-core kernel (which needs no workspace).
@@ -149,10 +155,13 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
                            float* S_out, int B, int T, int H, int K, int V, int chunk,
                            float scale, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace size in bytes that lets osdn_chunk_fwd use its two-kernel tensor-core path for these
+/* Workspace size in bytes that lets osdn_chunk_fwd use its fastest tensor-core path for these
  * arguments (0 when that path does not apply: then no workspace is ever used).  For K = V = 128
- * and chunk 64 it is B * H * (T / 64) * 33280 bytes per call: for each chunk of each head 32 KiB
- * of fp16 images and the chunk's decay factors of the gated variant. */
+ * and chunk 64 it is B * H * (T / 64) * 33280 bytes (for each chunk of each head 32 KiB of fp16
+ * images and the chunk's decay factors of the gated variant), plus, where the serial pass runs
+ * in segments (few heads, long sequences; depends on the device's SM count), the segment scratch:
+ * the transition pass's fp16 outputs (B*T*H*K*2 bytes) and three fp32 states per head and
+ * segment. */
 size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
                                       osdn_dtype dtype);
 
@@ -294,10 +303,11 @@ size_t osdn_layer_bwd_workspace_bytes(int B, int T, int H, int K, int V);
  * or code that cannot accept an allocator call (its latency, its implicit synchronisation, its
  * possible failure) in the middle of a step.  No counterpart in the paper: this is a property of
  * this library's interface, not of the method.
- *   Same arguments and results as osdn_chunk_fwd without the workspace: the scratch of the
- *   two-kernel tensor-core path comes from a fixed 32 MiB array in the library's own device
+ *   Same arguments as osdn_chunk_fwd without the workspace, and the results osdn_chunk_fwd gives
+ *   with a workspace of B * H * (T / 64) * 33280 bytes (its two-kernel tensor-core path, without
+ *   the segment split): that scratch comes from a fixed 32 MiB array in the library's own device
  *   memory (file-scope; every GPU that loads the library holds it until the process exits).
- *   Capacity: osdn_chunk_fwd_workspace_bytes(...) <= 32 MiB, i.e. B * H * (T / 64) <= 1008 chunks;
+ *   Capacity: B * H * (T / 64) * 33280 <= 32 MiB, i.e. B * H * (T / 64) <= 1008 chunks;
  *   larger requests return OSDN_ERR_CAPACITY before any launch.  Calls that need no scratch (fp32
  *   inputs, other head sizes) run the CUDA-core kernel as osdn_chunk_fwd does.
  *   Neither the library nor this call allocates (no cudaMalloc/cudaFree or allocating routine).

@@ -112,10 +112,10 @@ osdn_status osdn_chunk_validate(const void* q, const void* k, const void* k_tild
     return OSDN_OK;
 }
 
-// Scratch the dispatch below would use for these (validated) arguments: the tensor-core path's
-// workspace where that path applies, else 0.
+// Scratch of the two-kernel tensor-core path for these (validated) arguments, without the
+// segment split of the state pass (which needs more): 0 where that path does not apply.
 size_t osdn_chunk_scratch_bytes(const OsdnChunkArgs& a) {
-    if (a.T > 0 && a.dtype != OSDN_F32 && a.K == 128 && a.V == 128) return osdn_chunk_tc_workspace_bytes(a);
+    if (a.T > 0 && a.dtype != OSDN_F32 && a.K == 128 && a.V == 128) return osdn_chunk_tc_plain_workspace_bytes(a);
     return 0;
 }
 

@@ -992,6 +992,22 @@ __device__ __forceinline__ bool pair_any(bool pred) {
     return c != 0;
 }
 
+// Segment-parallel state pass (Appendix A.2, Eq. (10): the chunk transition is affine in S,
+// S^T_n = P_n S^T_{n-1} + Z_n with P_n = I - K~_n^T W_n).  The chunks of a head are cut into
+// segments of n_seg chunks; segment 0 runs from S0, every later one from a zero state,
+// and beside its value slices it runs as many transition slices: the same pass with
+// zero values (U = 0) and the identity as its start (64 of its key columns per CTA).  Those carry
+// Phi_n = P_n ... P_first, write G_n = scale (Q_n - L_n W_n) Phi_{n-1} (the readout of a transition
+// slice) through tmG in fp16, and end in Phi of the segment.  With S_start of each segment known
+// afterwards, S_end = S_start Phi^T-product + Z (seg_combine_kernel) and the outputs of a later
+// segment gain G_n S_start^T (seg_correct_kernel).  Unsegmented: n_seg = N, no transition slices.
+struct ChainSeg {
+    int n_seg;    // chunks per segment
+    int vslices;  // value slices per head (V / VS); slices from here on are transition slices
+    float* Z;     // [G][B H][V][K]: end state of each segment's value slices (null: S_out directly)
+    float* P;     // [G][B H][K][K]: end state of each later segment's transition slices
+};
+
 // One CTA per (batch, head, VS rows of S), serial over chunks.  Per chunk: U = T'V and
 // [X; Q S^T] = [U; 0] + [-W; Q] S^T; then S^T += K~^T X and O = Q S^T + L X.  T', -W and L come
 // from the workspace by bulk copy; Q, K~, V by TMA; O leaves by TMA.
@@ -1001,20 +1017,38 @@ __device__ __forceinline__ bool pair_any(bool pred) {
 // and the tokens of K~ by rho (S^T <- gamma_C S^T + (rho . K~)^T X); the S^T epilogue stores the
 // fp16 copy for the S-dependent products from the fp32 state it carries in registers, formed as
 // gamma_C S^T + Y from the update product Y = (rho . K~)^T X that the tensor cores leave on its own.
-template <typename TIn, bool GATED>
-__global__ void __launch_bounds__(chain::NT, 1)
-chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKT,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                   const unsigned char* __restrict__ ws, const float* S0, float* S_out, int T, int H,
-                   int V, int N, float scale) {
+template <typename TIn, bool GATED, bool SEG>
+__device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtensorMap& tmKT, const CUtensorMap& tmV,
+                                           const CUtensorMap& tmO, const CUtensorMap& tmG, const ChainSeg& sg,
+                                           const unsigned char* __restrict__ ws, const float* S0, float* S_out,
+                                           int T, int H, int V, int N, float scale) {
     using namespace chain;
     constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
+    // This CTA's segment of chunks [m0, m0 + NL) and slice (value rows, or key columns of Phi).
+    // SEG: blockIdx.y enumerates the first segment's value slices, then for each later segment
+    // its value slices and its transition slices (the first segment starts from S0 itself), so
+    // that no CTA leaves early (an early exit here slows every CTA's loop); every segment is
+    // non-empty.  SEG = false: one segment of value slices (the compiler drops the rest).
+    const int ys = static_cast<int>(blockIdx.y) - sg.vslices;
+    const int seg = (SEG && ys >= 0) ? 1 + ys / (2 * sg.vslices) : 0;
+    const int slice = !SEG || ys < 0 ? static_cast<int>(blockIdx.y) : ys % (2 * sg.vslices);
+    const bool phi = SEG && slice >= sg.vslices;
+    const int m0 = SEG ? seg * sg.n_seg : 0;
+    const int NL = SEG ? min(N - m0, sg.n_seg) : N;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int v0 = blockIdx.y * VS;
+    const int v0 = (phi ? slice - sg.vslices : slice) * VS;
+    const int BH = static_cast<int>(gridDim.x);
+    // start state: S0 for the first segment's value slices, zero for later ones, the identity for
+    // transition slices; end state: S_out, or the segment's slot in Z or P
+    const float* S0c = (seg == 0) ? S0 : nullptr;
+    float* S_end = !SEG ? S_out + static_cast<size_t>(bh) * V * KD
+                   : phi ? sg.P + (static_cast<size_t>(seg) * BH + bh) * KD * KD
+                         : sg.Z + (static_cast<size_t>(seg) * BH + bh) * V * KD;
+    const CUtensorMap* tmOut = phi ? &tmG : &tmO;
     const uint32_t sbase = tc::smem_u32(sm);
     const uint32_t bars = sbase + OFF_BAR;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + TMEM_SLOT);
@@ -1058,7 +1092,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // ================================ producer ============================================
         if (lane == 0) {
             int last[2] = {-1, -1};
-            for (int m = 0; m < N; ++m) {
+            for (int m = 0; m < NL; ++m) {
                 const int s = m & 1;
                 if (m >= 2 && !thread_wait(bars + B_FREE + 8 * s, ((m - 2) >> 1) & 1, abort_flag)) {
                     record_abort(abort_flag);
@@ -1066,17 +1100,19 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 }
                 const uint32_t bar = bars + B_FULL + 8 * s;
                 const uint32_t st = sbase + s * STAGE;
-                const int row = b * T + m * C;
-                const unsigned char* wsc = ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK;
-                tc::mbar_expect_tx(bar, LOAD_BYTES);
+                const int row = b * T + (m0 + m) * C;
+                const unsigned char* wsc = ws + (static_cast<size_t>(bh) * N + m0 + m) * WS_CHUNK;
+                tc::mbar_expect_tx(bar, phi ? LOAD_BYTES - (VS / 64) * 8192 : LOAD_BYTES);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
                     tc::tma_load_3d(st + ST_Q + kb * 8192, &tmQ, bar, kb * 64, h, row);
                     tc::tma_load_3d(st + ST_KT + kb * 8192, &tmKT, bar, kb * 64, h, row);
                 }
+                if (!phi) {  // a transition slice has zero values
 #pragma unroll
-                for (int vb = 0; vb < VS / 64; ++vb)
-                    tc::tma_load_3d(st + ST_V + vb * 8192, &tmV, bar, v0 + vb * 64, h, row);
+                    for (int vb = 0; vb < VS / 64; ++vb)
+                        tc::tma_load_3d(st + ST_V + vb * 8192, &tmV, bar, v0 + vb * 64, h, row);
+                }
                 tc::bulk_load(st + ST_W, wsc + WS_W, 16384, bar);
                 tc::bulk_load(st + ST_T, wsc + WS_T, 8192, bar);
                 tc::bulk_load(st + ST_L, wsc + WS_L, 8192, bar);
@@ -1098,12 +1134,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const uint64_t d_ss = tc::sdesc_sw128(sbase + OFF_SS, KD * 128, 1024);
             const uint64_t d_x = tc::sdesc_sw128(sbase + OFF_X, 8192, 1024);
             auto off = [](uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); };
-            auto issue_u = [&](int m) {  // R[m & 1] = [T'; 0] V
+            auto issue_u = [&](int m) {  // R[m & 1] = [T'; 0] V  (a transition slice has U = 0)
                 const int bb = m & 1;
                 const uint32_t dR = tbase + COL_R + bb * VS;
+                if (!phi) {
 #pragma unroll
-                for (int k = 0; k < C / 16; ++k)
-                    tc::mma_f16_ts(dR, tbase + COL_TH + bb * 32 + 8 * k, d_v[bb] + off(k * 2048), id_h, k > 0);
+                    for (int k = 0; k < C / 16; ++k)
+                        tc::mma_f16_ts(dR, tbase + COL_TH + bb * 32 + 8 * k, d_v[bb] + off(k * 2048), id_h, k > 0);
+                }
                 tc::mma_commit(bars + B_FREE + 8 * bb);
             };
             // U(m) needs chunk m staged and (from m = 2 on) R[m & 1] read out
@@ -1117,7 +1155,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 tc::tc_fence_after();
                 issue_u(0);
             }
-            for (int n = 0; ok && n < N; ++n) {
+            for (int n = 0; ok && n < NL; ++n) {
                 const int bb = n & 1;
                 const uint32_t dR = tbase + COL_R + bb * VS;
                 // [X; Q S^T] += [-W; Q] S^T: needs the fp16 copy of S after chunk n - 1
@@ -1125,7 +1163,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 tc::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < KD / 16; ++k)
-                    tc::mma_f16_ts(dR, tbase + COL_QW + bb * 64 + 8 * k, d_ss + off(k * 2048), id_h, 1);
+                    tc::mma_f16_ts(dR, tbase + COL_QW + bb * 64 + 8 * k, d_ss + off(k * 2048), id_h,
+                                   (phi && k == 0) ? 0u : 1u);
                 tc::mma_commit(bars + B_QS + 8 * bb);
                 // S^T += K~^T X  (gated: Y = (rho . K~)^T X on its own; the epilogue adds gamma_C S^T)
                 if (!(ok = thread_wait(bars + B_XRDY, n & 1, abort_flag) && thread_wait(bars + B_KT, n & 1, abort_flag)))
@@ -1143,7 +1182,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int k = 0; k < C / 16; ++k)
                     tc::mma_f16_ts(dR, tbase + COL_LH + 8 * k, d_x + off(k * 2048), id_h, 1);
                 tc::mma_commit(bars + B_O + 8 * bb);
-                if (n + 1 < N) {  // the next chunk's U = T'V, off the serial path
+                if (n + 1 < NL) {  // the next chunk's U = T'V, off the serial path
                     if (!(ok = u_ready(n + 1))) break;
                     tc::tc_fence_after();
                     issue_u(n + 1);
@@ -1159,7 +1198,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const int r = (warp - 10) * 32 + lane;  // token row; tensor-memory lane 64 + r
         const bool issuer = warp == 10 && lane == 0;
         bool ok = true, nonfinite = false;
-        for (int n = 0; n < N; ++n) {
+        for (int n = 0; n < NL; ++n) {
             const int bb = n & 1;
             ok = warp_wait(bars + B_O + 8 * bb, (n >> 1) & 1, abort_flag);
             if (issuer) tc::bulk_wait_read_all();  // the previous tile has left shared memory
@@ -1177,8 +1216,13 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
                     for (int j = 0; j < 8; ++j) ov[j] = scale * o[8 * c + j];
                     uint4 u;
-                    VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u), ov);
-                    VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u) + 4, ov + 4);
+                    if (phi) {  // G_n in fp16
+                        u = make_uint4(pack_h2(ov[0], ov[1]), pack_h2(ov[2], ov[3]), pack_h2(ov[4], ov[5]),
+                                       pack_h2(ov[6], ov[7]));
+                    } else {
+                        VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u), ov);
+                        VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u) + 4, ov + 4);
+                    }
                     *reinterpret_cast<uint4*>(sm + OFF_O + ((q2 * 32) / 64) * 8192 +
                                               tc::sw128_off(r, ((q2 * 32) % 64) / 8 + c)) = u;
                 }
@@ -1191,7 +1235,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             if (issuer) {
 #pragma unroll
                 for (int vb = 0; vb < VS / 64; ++vb)
-                    tc::tma_store_3d(&tmO, sbase + OFF_O + vb * 8192, v0 + vb * 64, h, b * T + n * C);
+                    tc::tma_store_3d(tmOut, sbase + OFF_O + vb * 8192, v0 + vb * 64, h, b * T + (m0 + n) * C);
                 tc::bulk_commit();
             }
         }
@@ -1215,7 +1259,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // gated: gamma and rho of tokens 2 lane, 2 lane + 1 of a chunk as fp16 pairs (formed by
         // the prep), read from the workspace one chunk ahead
         uint32_t gpair = 0, rpair = 0, gnext = 0, rnext = 0;
-        auto gates_of = [&](int m) {
+        auto gates_of = [&](int m) {  // (the gated chain is never segmented: m0 = 0)
             const uint32_t* wg = reinterpret_cast<const uint32_t*>(ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK + WS_GATE);
             gnext = wg[(WS_GAM >> 2) + lane];
             rnext = wg[(WS_RHO >> 2) + lane];
@@ -1225,7 +1269,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             gpair = gnext;
             rpair = rnext;
         }
-        for (int m = 0; ok && m < N; ++m) {
+        for (int m = 0; ok && m < NL; ++m) {
             const int s = m & 1, bb = m & 1;
             const unsigned char* stg = sm + s * STAGE;
             if (!(ok = warp_wait(bars + B_FULL + 8 * s, (m >> 1) & 1, abort_flag))) break;
@@ -1278,10 +1322,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 }
             }
             // V to fp16 in place (4 x 16 bytes per thread of the four staging warps)
-            if constexpr (kBf16) convert_bf16_to_f16<(VS / 64) * 4>(const_cast<unsigned char*>(stg) + ST_V, w4 * 32 + lane);
+            if (kBf16 && !phi) convert_bf16_to_f16<(VS / 64) * 4>(const_cast<unsigned char*>(stg) + ST_V, w4 * 32 + lane);
             tc::tmem_st_wait();
             warp_publish(bars + B_CONVA + 8 * bb, lane);
-            if (GATED && m + 1 < N) gates_of(m + 1);
+            if (GATED && m + 1 < NL) gates_of(m + 1);
             // K~^T (lane = key); its buffer was last read by the S^T update of chunk m - 1
             if (m >= 1 && !(ok = warp_wait(bars + B_ST, (m - 1) & 1, abort_flag))) break;
             tc::tc_fence_after();
@@ -1343,7 +1387,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             for (int half = 0; half < VS / 32; ++half) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    sv[j] = S0 ? S0[(static_cast<size_t>(bh) * V + v0 + half * 32 + j) * KD + k] : 0.f;
+                    sv[j] = phi ? (k == v0 + half * 32 + j ? 1.f : 0.f)
+                                : (S0c ? S0c[(static_cast<size_t>(bh) * V + v0 + half * 32 + j) * KD + k] : 0.f);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     st_row_chunk(sm + OFF_SS + ((half * 32) / 64) * (KD * 128), k, ((half * 32) % 64) / 8 + c, sv + 8 * c);
@@ -1358,7 +1403,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             warp_publish(bars + B_SRDY, lane);
         }
         bool ok = true;
-        for (int n = 0; n < N; ++n) {
+        for (int n = 0; n < NL; ++n) {
             const int bb = n & 1;
             const float gcn = GATED ? gamma_c(n) : 1.f;  // gamma_C of this chunk, used after its update
             if (warp < 2) {  // X rows live in tensor-memory lanes 0-63
@@ -1389,7 +1434,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     sv[j] = st[j];
                 }
             }
-            if (n + 1 < N) {
+            if (n + 1 < NL) {
 #pragma unroll
                 for (int cc = 0; cc < VS / 8; ++cc)
                     st_row_chunk(sm + OFF_SS + ((cc * 8) / 64) * (KD * 128), k, cc % 8, sv + 8 * cc);
@@ -1399,7 +1444,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
                 for (int j = 0; j < VS; ++j) {
                     bad |= !isfinite(sv[j]);
-                    S_out[(static_cast<size_t>(bh) * V + v0 + j) * KD + k] = sv[j];
+                    S_end[static_cast<size_t>(v0 + j) * KD + k] = sv[j];
                 }
                 if (bad) atomicOr(&g_range_flag, 1u);
             }
@@ -1411,6 +1456,178 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     __syncthreads();
     tc::tc_fence_after();
     if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+}
+
+template <typename TIn, bool GATED>
+__global__ void __launch_bounds__(chain::NT, 1)
+chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKT,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const unsigned char* __restrict__ ws, const float* S0, float* S_out, int T, int H,
+                   int V, int N, float scale) {
+    chain_body<TIn, GATED, false>(tmQ, tmKT, tmV, tmO, tmO, ChainSeg{N, 0, nullptr, nullptr}, ws, S0, S_out, T, H, V,
+                                  N, scale);
+}
+// The segmented pass: grid (B H, value slices x (2 G - 1)), see chain_body.
+template <typename TIn>
+__global__ void __launch_bounds__(chain::NT, 1)
+chunk_chain_seg_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKT,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                       const __grid_constant__ CUtensorMap tmG, ChainSeg sg, const unsigned char* __restrict__ ws,
+                       const float* S0, float* S_out, int T, int H, int V, int N, float scale) {
+    chain_body<TIn, false, true>(tmQ, tmKT, tmV, tmO, tmG, sg, ws, S0, S_out, T, H, V, N, scale);
+}
+
+// Start states of the segments and the final state.  Row v of S evolves on its own across a
+// segment boundary: S_start(g + 1)[v][k] = sum_j S_start(g)[v][j] P_g[j][k] + Z_g[v][k] (P_g[j][k] =
+// Phi_g[k][j], the transition slices' end state), so each CTA carries 16 rows of one head through
+// all boundaries in fp32.  Sst[g] (g >= 1) receives S_start(g) for the output correction.
+// Grid (B H, V / 16), 256 threads.
+__global__ void __launch_bounds__(256)
+seg_combine_kernel(const float* __restrict__ Z, const float* __restrict__ P, float* __restrict__ Sst,
+                   float* __restrict__ S_out, int G, int V) {
+    __shared__ float cur[16][KD];
+    const int bh = blockIdx.x, BH = gridDim.x, r0 = blockIdx.y * 16, tid = threadIdx.x;
+    const int k = tid & (KD - 1), rh = tid >> 7;  // column k, rows rh * 8 .. rh * 8 + 7
+    auto row_of = [&](int g, int r) {  // offset of row r of head bh in slot g of a [G][BH][V][K] array
+        return ((static_cast<size_t>(g) * BH + bh) * V + r0 + r) * KD;
+    };
+    for (int i = tid; i < 16 * KD; i += 256) cur[i / KD][i % KD] = Z[row_of(0, i / KD) + i % KD];
+    __syncthreads();
+    for (int g = 1; g < G; ++g) {
+        for (int i = tid; i < 16 * KD; i += 256) Sst[row_of(g, i / KD) + i % KD] = cur[i / KD][i % KD];
+        const float* Pg = P + (static_cast<size_t>(g) * BH + bh) * KD * KD;
+        float acc[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) acc[r] = Z[row_of(g, rh * 8 + r) + k];
+        for (int j = 0; j < KD; ++j) {
+            const float pj = Pg[static_cast<size_t>(j) * KD + k];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = fmaf(cur[rh * 8 + r][j], pj, acc[r]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 8; ++r) cur[rh * 8 + r][k] = acc[r];
+        __syncthreads();
+    }
+    for (int i = tid; i < 16 * KD; i += 256)
+        S_out[(static_cast<size_t>(bh) * V + r0 + i / KD) * KD + i % KD] = cur[i / KD][i % KD];
+}
+
+// Output correction of the later segments: o_n += G_n S_start(g)^T, G_n (64 tokens x K, fp16) from
+// the transition slices.  One CTA per (head, segment g >= 1, group of chunk pairs): S_start(g) in
+// fp16 as the K-major B operand (N = V = 128 rows), two chunks of G stacked as the M = 128 A
+// operand (TMA), fp32 accumulator in tensor memory; each thread then adds its token row to o.
+// 128 threads, one pair of chunks at a time.
+namespace segc {
+constexpr uint32_t OFF_A = 0;          // per key block: chunk c rows | chunk c + 1 rows (16 KB)
+constexpr uint32_t OFF_B = 32768;      // S_start^T operand: per key block 128 rows x 128 bytes
+constexpr uint32_t OFF_BAR = 65536;
+constexpr uint32_t SMEM_ALLOC = OFF_BAR + 64 + 1024;
+}  // namespace segc
+template <typename TIn>
+__global__ void __launch_bounds__(128, 1)
+seg_correct_kernel(const __grid_constant__ CUtensorMap tmG, const float* __restrict__ Sst, TIn* __restrict__ o,
+                   int T, int H, int V, int N, int n_seg) {
+    using namespace segc;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int bh = blockIdx.x, b = bh / H, h = bh % H, BH = gridDim.x;
+    const int g = blockIdx.y + 1;
+    const int m0 = g * n_seg, NL = min(N - m0, n_seg);
+    const int npairs = (NL + 1) / 2;
+    const uint32_t sbase = tc::smem_u32(sm);
+    const uint32_t bar_tma = sbase + OFF_BAR, bar_mma = sbase + OFF_BAR + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
+    if (tid == 0) {
+        tc::mbar_init(bar_tma, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::mbar_init_fence();
+        tc::prefetch_tmap(&tmG);
+    }
+    // S_start(g) rows v (thread v) -> fp16 K-major operand
+    {
+        const float* srow = Sst + ((static_cast<size_t>(g) * BH + bh) * V + tid) * KD;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float v8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v8[e] = srow[kb * 64 + c * 8 + e];
+                st_row_chunk(sm + OFF_B + kb * 16384, tid, c, v8);
+            }
+        }
+    }
+    tc::fence_proxy_async();
+    __syncthreads();
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 128);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t idesc = tc::idesc_f16_f32(128, 128, false, false);
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int p = blockIdx.z; ok && p < npairs; p += gridDim.z) {
+        const int c = m0 + 2 * p;
+        const bool two = 2 * p + 1 < NL;
+        if (tid == 0) {
+            tc::mbar_expect_tx(bar_tma, (two ? 4 : 2) * 8192);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                tc::tma_load_3d(sbase + OFF_A + kb * 16384, &tmG, bar_tma, kb * 64, h, b * T + c * C);
+                if (two) tc::tma_load_3d(sbase + OFF_A + kb * 16384 + 8192, &tmG, bar_tma, kb * 64, h, b * T + (c + 1) * C);
+            }
+        }
+        ok = tc::mbar_wait(bar_tma, ph, kMaxPolls);
+        if (!__syncthreads_and(ok)) break;
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < KD / 16; ++k) {
+                const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
+                tc::mma_f16(tbase, tc::sdesc_sw128(sbase + OFF_A + koff, 16, 1024),
+                            tc::sdesc_sw128(sbase + OFF_B + koff, 16, 1024), idesc, k > 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        ok = tc::mbar_wait(bar_mma, ph, kMaxPolls);
+        if (!__syncthreads_and(ok)) break;
+        ph ^= 1u;
+        tc::tc_fence_after();
+        const int tok = (tid < 64 ? c * C : (c + 1) * C - 64) + tid;  // this thread's token row
+        TIn* orow = o + ((static_cast<size_t>(b) * T + tok) * H + h) * V;
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+            float acc[32];
+            tc::tmem_ld32(tbase + lane_base + q2 * 32, acc);
+            tc::tmem_ld_wait();
+            if (tid < 64 || two) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    float cur[4];
+                    VecIO<TIn, 4>::load(orow + q2 * 32 + e, cur);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cur[i] += acc[e + i];
+                    VecIO<TIn, 4>::store(orow + q2 * 32 + e, cur);
+                }
+            }
+        }
+        tc::tc_fence_before();
+        __syncthreads();  // the A tiles and the accumulator are reused by the next pair
+    }
+    if (!ok && tid == 0) {  // a wait gave up: record it, let what was issued land, then leave
+        atomicExch(&g_timeout_flag, 1u);
+        tc::mbar_wait(bar_tma, ph, kMaxPolls >> 4);
+        tc::mbar_wait(bar_mma, ph, kMaxPolls >> 4);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tbase, 128);
 }
 
 // =============================================================================================
@@ -1535,12 +1752,44 @@ cudaError_t set_smem(K kernel, uint32_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
+// Segments of the state pass (see ChainSeg): more than one when a head's chain would leave most
+// SMs idle, i.e. few heads and long sequences.  Each later segment adds as many transition-slice
+// CTAs as value-slice CTAs; all CTAs must fit on the GPU at once, and segments keep >= 16 chunks.
+int seg_count(int B, int H, int T, int V) {
+    const int BH = B * H, N = T / C, vsl = V / VS;
+    if (V != KD) return 1;
+    int G = 1;
+    for (int g = 2; g <= 8; ++g) {
+        if (BH * (vsl + (g - 1) * 2 * vsl) > num_sms() || N < g * 16) break;
+        G = g;
+    }
+    return G;
+}
+// Workspace of the segmented pass: [chunk images][G_n, fp16 rows like q][Z][P][S_start], 256-aligned.
+struct SegWs {
+    size_t gbuf, z, p, sst, total;
+};
+SegWs seg_ws(const OsdnChunkArgs& a, int G) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t BH = static_cast<size_t>(a.B) * a.H, N = static_cast<size_t>(a.T / C);
+    SegWs s{};
+    s.gbuf = up(BH * N * WS_CHUNK);
+    s.z = s.gbuf + up(static_cast<size_t>(a.B) * a.T * a.H * KD * 2);
+    s.p = s.z + up(static_cast<size_t>(G) * BH * a.V * KD * 4);
+    s.sst = s.p + up(static_cast<size_t>(G) * BH * KD * KD * 4);
+    s.total = s.sst + up(static_cast<size_t>(G) * BH * a.V * KD * 4);
+    return s;
+}
+
+// With a workspace: the prep kernel (unless chain_only: the layer call's cooperative kernel did
+// it) and the chain kernel, segmented when seg_count > 1 and the workspace holds the segment
+// scratch, then the segment combine and the output correction.  Without: one fused kernel.
 template <typename TIn>
 cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s, bool chain_only = false) {
     const CUtensorMapDataType dt = std::is_same<TIn, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const long long rows = static_cast<long long>(a.B) * a.T;
-    CUtensorMap mq, mk, mkt, mv, mo;
+    CUtensorMap mq, mk, mkt, mv, mo, mg;
     if (!make_map(&mq, a.q, dt, a.K, a.H, rows) || !make_map(&mk, a.k, dt, a.K, a.H, rows) ||
         !make_map(&mkt, a.k_tilde, dt, a.K, a.H, rows) || !make_map(&mv, a.v, dt, a.V, a.H, rows) ||
         !make_map(&mo, a.o, dt, a.V, a.H, rows))
@@ -1548,26 +1797,42 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        cudaError_t e1 = set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC);
-        cudaError_t e2 = set_smem(chunk_prep_kernel<TIn>, prep::SMEM_ALLOC);
-        cudaError_t e3 = set_smem(chunk_chain_kernel<TIn, false>, chain::SMEM_ALLOC);
-        cudaError_t e4 = set_smem(chunk_chain_kernel<TIn, true>, chain::SMEM_ALLOC);
-        attr_err = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : (e3 != cudaSuccess ? e3 : e4));
+        cudaError_t e[6] = {set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC),
+                            set_smem(chunk_prep_kernel<TIn>, prep::SMEM_ALLOC),
+                            set_smem(chunk_chain_kernel<TIn, false>, chain::SMEM_ALLOC),
+                            set_smem(chunk_chain_kernel<TIn, true>, chain::SMEM_ALLOC),
+                            set_smem(chunk_chain_seg_kernel<TIn>, chain::SMEM_ALLOC),
+                            set_smem(seg_correct_kernel<TIn>, segc::SMEM_ALLOC)};
+        for (cudaError_t x : e)
+            if (x != cudaSuccess && attr_err == cudaSuccess) attr_err = x;
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int N = a.T / C;
     const size_t need = static_cast<size_t>(a.B) * a.H * N * WS_CHUNK;
     dim3 block(NTHREADS);
     if (ws != nullptr && ws_bytes >= need) {
-        const int total = a.B * a.H * N;
-        dim3 gp(static_cast<unsigned>(total < 3 * num_sms() ? total : 3 * num_sms()));
+        unsigned char* w = static_cast<unsigned char*>(ws);
+        const int BH = a.B * a.H;
+        const int total = BH * N;
+        int G = a.alpha ? 1 : seg_count(a.B, a.H, a.T, a.V);
+        SegWs sw{};
+        if (G > 1) {
+            sw = seg_ws(a, G);
+            if (ws_bytes < sw.total || !make_map(&mg, w + sw.gbuf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, KD, a.H, rows)) G = 1;
+        }
+        if (G == 1) mg = mo;  // (unused)
+        const int n_seg = (N + G - 1) / G;
         if (!chain_only) {
-            chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta, a.alpha,
-                                                                      static_cast<unsigned char*>(ws), a.T, a.H, N, total);
+            dim3 gp(static_cast<unsigned>(total < 3 * num_sms() ? total : 3 * num_sms()));
+            chunk_prep_kernel<TIn><<<gp, block, prep::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta, a.alpha, w, a.T, a.H, N,
+                                                                      total);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return e;
         }
-        dim3 gc(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
+        ChainSeg sg{n_seg, a.V / VS, G > 1 ? reinterpret_cast<float*>(w + sw.z) : nullptr,
+                    G > 1 ? reinterpret_cast<float*>(w + sw.p) : nullptr};
+        static_assert(KD == 2 * 64, "transition slices: as many as value slices when V = K");
+        dim3 gc(static_cast<unsigned>(BH), static_cast<unsigned>((a.V / VS) * (2 * G - 1)));
         // programmatic dependent launch: the chain CTAs take SMs as the previous kernel's CTAs
         // leave and wait (griddepcontrol.wait) for its results
         cudaLaunchConfig_t cfg = {};
@@ -1580,17 +1845,41 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const unsigned char* wsc = static_cast<const unsigned char*>(ws);
-        auto chain_kernel = a.alpha ? chunk_chain_kernel<TIn, true> : chunk_chain_kernel<TIn, false>;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel, mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T, a.H, a.V,
-                                           N, a.scale);
+        const unsigned char* wsc = w;
+        cudaError_t e;
+        if (G > 1) {
+            e = cudaLaunchKernelEx(&cfg, chunk_chain_seg_kernel<TIn>, mq, mkt, mv, mo, mg, sg, wsc, a.S0, a.S_out, a.T,
+                                   a.H, a.V, N, a.scale);
+        } else {
+            auto chain_kernel = a.alpha ? chunk_chain_kernel<TIn, true> : chunk_chain_kernel<TIn, false>;
+            e = cudaLaunchKernelEx(&cfg, chain_kernel, mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T, a.H, a.V, N, a.scale);
+        }
         if (e == cudaErrorNotSupported) {  // no dependent launch here: an ordinary one
             (void)cudaGetLastError();
-            chain_kernel<<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T,
-                                                                       a.H, a.V, N, a.scale);
+            if (G > 1) {
+                chunk_chain_seg_kernel<TIn><<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(
+                    mq, mkt, mv, mo, mg, sg, wsc, a.S0, a.S_out, a.T, a.H, a.V, N, a.scale);
+            } else {
+                auto chain_kernel = a.alpha ? chunk_chain_kernel<TIn, true> : chunk_chain_kernel<TIn, false>;
+                chain_kernel<<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T,
+                                                                           a.H, a.V, N, a.scale);
+            }
             e = cudaGetLastError();
         }
-        return e;
+        if (e != cudaSuccess || G == 1) return e;
+        // the segments' start states (and S_out), then the later segments' output correction
+        float* sst = reinterpret_cast<float*>(w + sw.sst);
+        seg_combine_kernel<<<dim3(static_cast<unsigned>(BH), static_cast<unsigned>(a.V / 16)), 256, 0, s>>>(
+            sg.Z, sg.P, sst, a.S_out, G, a.V);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const int per = (2 * num_sms() + BH * (G - 1) - 1) / (BH * (G - 1));  // about two CTAs per SM
+        const int pairs = (n_seg + 1) / 2;
+        dim3 gr(static_cast<unsigned>(BH), static_cast<unsigned>(G - 1),
+                static_cast<unsigned>(per < pairs ? (per > 0 ? per : 1) : pairs));
+        seg_correct_kernel<TIn><<<gr, 128, segc::SMEM_ALLOC, s>>>(mg, sst, static_cast<TIn*>(a.o), a.T, a.H, a.V, N,
+                                                                 n_seg);
+        return cudaGetLastError();
     }
     if (a.alpha) return cudaErrorNotSupported;  // the gate is carried by the two-kernel path only
     dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
@@ -1617,7 +1906,8 @@ LayerWs layer_ws(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
     l.scan = 0;
     l.counter = up(osdn_scan_block_workspace_bytes(sa));
     l.chunk = l.counter + 256;
-    l.total = l.chunk + up(static_cast<size_t>(ca.B) * ca.H * nblk * WS_CHUNK);
+    l.total = l.chunk + up(osdn_chunk_tc_workspace_bytes(ca));
+    (void)nblk;
     return l;
 }
 
@@ -1700,9 +1990,18 @@ cudaError_t osdn_launch_layer(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, v
     return sa.r ? osdn::launch_layer_t<__half, true>(sa, ca, w, s) : osdn::launch_layer_t<__half, false>(sa, ca, w, s);
 }
 
-size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a) {
+size_t osdn_chunk_tc_plain_workspace_bytes(const OsdnChunkArgs& a) {
     if (!osdn::tc_covers(a)) return 0;
     return static_cast<size_t>(a.B) * a.H * (a.T / osdn::C) * osdn::WS_CHUNK;
+}
+
+// With the segment scratch where the shape would use segments (whatever the gate: the size
+// query does not see it).
+size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a) {
+    if (!osdn::tc_covers(a)) return 0;
+    const int G = osdn::seg_count(a.B, a.H, a.T, a.V);
+    if (G > 1) return osdn::seg_ws(a, G).total;
+    return osdn_chunk_tc_plain_workspace_bytes(a);
 }
 
 cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {

@@ -127,6 +127,8 @@ cudaError_t osdn_launch_chunk_simt(const OsdnChunkArgs& a, cudaStream_t s);
 // cudaErrorNotSupported when the tensor-core kernels do not cover the arguments.
 cudaError_t osdn_launch_chunk_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a);
+// The same path's scratch without the segment split of the state pass (the prep images only).
+size_t osdn_chunk_tc_plain_workspace_bytes(const OsdnChunkArgs& a);
 cudaError_t osdn_launch_decode(const OsdnDecodeArgs& a, cudaStream_t s);
 // Argument checks of osdn_chunk_fwd (all but the workspace); fills `out`, or sets `empty` when B
 // or H is zero.  Scratch the chunk dispatch uses for validated arguments (0: none).

@@ -3,8 +3,9 @@ device memory when they call (an engine that plans all GPU memory once at start-
 cannot take an allocator call -- its latency, synchronisation or possible failure -- mid-step).
 
 The entry point is called through the C ABI.  It runs the same kernels as osdn_chunk_fwd given a
-workspace, only on a fixed scratch array, so its results must be bit-identical to that path on
-two calls in a row (the array is shared by every call and keeps the previous call's contents);
+workspace of the chunk images' size (the two-kernel path without the segment split), only on a
+fixed scratch array, so its results must be bit-identical to that path on two calls in a row (the
+array is shared by every call and keeps the previous call's contents);
 one call is also checked against the oracle at the chunk tests' tolerance.  The capacity edge
 (exactly 1008 chunk-heads accepted, 1009 refused) and a gated call are covered too.  This file is
 collected last on purpose.
@@ -44,6 +45,14 @@ def _inputs(B, H, T, seed):
     return inp, g, kt
 
 
+def _workspace_path(g, kt, S0, **kw):
+    """osdn_chunk_fwd on a workspace of exactly the chunk images' size (B H (T / 64) x 33280 bytes):
+    the two-kernel path the static scratch runs."""
+    B, T, H, _ = g["k"].shape
+    ws = torch.empty(B * H * (T // 64) * 33280, dtype=torch.uint8, device="cuda")
+    return osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], S0, workspace=ws, **kw)
+
+
 def _run_static(g, kt, S0, scale=1.0, alpha=None, alpha_per_key=0, like=None):
     o = torch.full_like(like[0], float("nan"))
     S = torch.full_like(like[1], float("nan"))
@@ -58,7 +67,7 @@ def _run_static(g, kt, S0, scale=1.0, alpha=None, alpha_per_key=0, like=None):
 def test_static_scratch_matches_workspace_path_twice():
     inp, g, kt = _inputs(2, 4, 512, seed=17)
     S0 = torch.randn(2, 4, 128, 128, generator=torch.Generator().manual_seed(5)).cuda() * 0.1
-    o_ref, S_ref = osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], S0, scale=0.5)
+    o_ref, S_ref = _workspace_path(g, kt, S0, scale=0.5)
     for call in range(2):
         o, S = _run_static(g, kt, S0, scale=0.5, like=(o_ref, S_ref))
         assert torch.equal(o, o_ref), f"o differs from the workspace path (call {call})"
@@ -74,7 +83,7 @@ def test_static_scratch_gated_matches_workspace_path():
     inp, g, kt = _inputs(1, 4, 256, seed=23)
     gen = torch.Generator().manual_seed(29)
     alpha = torch.sigmoid(4.0 + torch.randn(1, 256, 4, generator=gen)).cuda()
-    o_ref, S_ref = osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], None, alpha=alpha)
+    o_ref, S_ref = _workspace_path(g, kt, None, alpha=alpha)
     for call in range(2):
         o, S = _run_static(g, kt, None, alpha=alpha, like=(o_ref, S_ref))
         assert torch.equal(o, o_ref), f"gated o differs (call {call})"
@@ -85,7 +94,7 @@ def test_static_scratch_exact_capacity():
     """B=1, H=16, T=4032: 16 x 63 = 1008 chunk-heads, the whole array; the last slots must hold
     correct results too."""
     inp, g, kt = _inputs(1, 16, 4032, seed=31)
-    o_ref, S_ref = osdn_chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], None)
+    o_ref, S_ref = _workspace_path(g, kt, None)
     o, S = _run_static(g, kt, None, like=(o_ref, S_ref))
     assert torch.equal(o, o_ref) and torch.equal(S, S_ref)
 
