@@ -1480,35 +1480,40 @@ chunk_chain_seg_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
 // Start states of the segments and the final state.  Row v of S evolves on its own across a
 // segment boundary: S_start(g + 1)[v][k] = sum_j S_start(g)[v][j] P_g[j][k] + Z_g[v][k] (P_g[j][k] =
 // Phi_g[k][j], the transition slices' end state), so each CTA carries 16 rows of one head through
-// all boundaries in fp32.  Sst[g] (g >= 1) receives S_start(g) for the output correction.
-// Grid (B H, V / 16), 256 threads.
+// all boundaries in fp32, with P_g staged in shared memory.  Sst[g] (g >= 1) receives S_start(g)
+// for the output correction.  Grid (B H, V / 16), 256 threads, 72 KB of shared memory.
+constexpr uint32_t COMBINE_SMEM = (KD * KD + 16 * KD) * 4;
 __global__ void __launch_bounds__(256)
 seg_combine_kernel(const float* __restrict__ Z, const float* __restrict__ P, float* __restrict__ Sst,
                    float* __restrict__ S_out, int G, int V) {
-    __shared__ float cur[16][KD];
+    extern __shared__ float cmb[];
+    float* Ps = cmb;                   // P_g, [j][k]
+    float(*cur)[KD] = reinterpret_cast<float(*)[KD]>(cmb + KD * KD);
     const int bh = blockIdx.x, BH = gridDim.x, r0 = blockIdx.y * 16, tid = threadIdx.x;
     const int k = tid & (KD - 1), rh = tid >> 7;  // column k, rows rh * 8 .. rh * 8 + 7
     auto row_of = [&](int g, int r) {  // offset of row r of head bh in slot g of a [G][BH][V][K] array
         return ((static_cast<size_t>(g) * BH + bh) * V + r0 + r) * KD;
     };
     for (int i = tid; i < 16 * KD; i += 256) cur[i / KD][i % KD] = Z[row_of(0, i / KD) + i % KD];
-    __syncthreads();
     for (int g = 1; g < G; ++g) {
+        const float4* Pg = reinterpret_cast<const float4*>(P + (static_cast<size_t>(g) * BH + bh) * KD * KD);
+        for (int i = tid; i < KD * KD / 4; i += 256) reinterpret_cast<float4*>(Ps)[i] = Pg[i];
+        __syncthreads();
         for (int i = tid; i < 16 * KD; i += 256) Sst[row_of(g, i / KD) + i % KD] = cur[i / KD][i % KD];
-        const float* Pg = P + (static_cast<size_t>(g) * BH + bh) * KD * KD;
         float acc[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) acc[r] = Z[row_of(g, rh * 8 + r) + k];
+#pragma unroll 8
         for (int j = 0; j < KD; ++j) {
-            const float pj = Pg[static_cast<size_t>(j) * KD + k];
+            const float pj = Ps[j * KD + k];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = fmaf(cur[rh * 8 + r][j], pj, acc[r]);
         }
         __syncthreads();
 #pragma unroll
         for (int r = 0; r < 8; ++r) cur[rh * 8 + r][k] = acc[r];
-        __syncthreads();
     }
+    __syncthreads();
     for (int i = tid; i < 16 * KD; i += 256)
         S_out[(static_cast<size_t>(bh) * V + r0 + i / KD) * KD + i % KD] = cur[i / KD][i % KD];
 }
@@ -1516,18 +1521,19 @@ seg_combine_kernel(const float* __restrict__ Z, const float* __restrict__ P, flo
 // Output correction of the later segments: o_n += G_n S_start(g)^T, G_n (64 tokens x K, fp16) from
 // the transition slices.  One CTA per (head, segment g >= 1, group of chunk pairs): S_start(g) in
 // fp16 as the K-major B operand (N = V = 128 rows), two chunks of G stacked as the M = 128 A
-// operand (TMA), fp32 accumulator in tensor memory; each thread then adds its token row to o.
-// 128 threads, one pair of chunks at a time.
+// operand, the same two chunks of o (TMA), fp32 accumulator in tensor memory; each thread adds its
+// token row to the o tile in shared memory, which leaves by TMA.  128 threads, one pair at a time.
 namespace segc {
 constexpr uint32_t OFF_A = 0;          // per key block: chunk c rows | chunk c + 1 rows (16 KB)
 constexpr uint32_t OFF_B = 32768;      // S_start^T operand: per key block 128 rows x 128 bytes
-constexpr uint32_t OFF_BAR = 65536;
+constexpr uint32_t OFF_O = 65536;      // o: per 64-wide value block, chunk c rows | chunk c + 1 rows
+constexpr uint32_t OFF_BAR = 98304;
 constexpr uint32_t SMEM_ALLOC = OFF_BAR + 64 + 1024;
 }  // namespace segc
 template <typename TIn>
 __global__ void __launch_bounds__(128, 1)
-seg_correct_kernel(const __grid_constant__ CUtensorMap tmG, const float* __restrict__ Sst, TIn* __restrict__ o,
-                   int T, int H, int V, int N, int n_seg) {
+seg_correct_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmO,
+                   const float* __restrict__ Sst, int T, int H, int V, int N, int n_seg) {
     using namespace segc;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -1545,19 +1551,18 @@ seg_correct_kernel(const __grid_constant__ CUtensorMap tmG, const float* __restr
         tc::mbar_init(bar_mma, 1);
         tc::mbar_init_fence();
         tc::prefetch_tmap(&tmG);
+        tc::prefetch_tmap(&tmO);
     }
-    // S_start(g) rows v (thread v) -> fp16 K-major operand
+    // S_start(g) -> fp16 K-major operand; unit u: row u / 16, eight columns 8 (u % 16), so that
+    // sixteen threads read one 512-byte row
     {
-        const float* srow = Sst + ((static_cast<size_t>(g) * BH + bh) * V + tid) * KD;
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float v8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v8[e] = srow[kb * 64 + c * 8 + e];
-                st_row_chunk(sm + OFF_B + kb * 16384, tid, c, v8);
-            }
+        const float* S = Sst + (static_cast<size_t>(g) * BH + bh) * V * KD;
+        for (int u = tid; u < V * 16; u += 128) {
+            const int row = u >> 4, c16 = u & 15;
+            const float4 x = *reinterpret_cast<const float4*>(S + row * KD + c16 * 8);
+            const float4 y = *reinterpret_cast<const float4*>(S + row * KD + c16 * 8 + 4);
+            const float v8[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+            st_row_chunk(sm + OFF_B + (c16 >> 3) * 16384, row, c16 & 7, v8);
         }
     }
     tc::fence_proxy_async();
@@ -1569,17 +1574,24 @@ seg_correct_kernel(const __grid_constant__ CUtensorMap tmG, const float* __restr
     const uint32_t tbase = *tmem_slot;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t idesc = tc::idesc_f16_f32(128, 128, false, false);
+    const int r = tid & 63, half = tid >> 6;  // this thread's token row: chunk c + half, row r
     uint32_t ph = 0;
     bool ok = true;
     for (int p = blockIdx.z; ok && p < npairs; p += gridDim.z) {
         const int c = m0 + 2 * p;
         const bool two = 2 * p + 1 < NL;
         if (tid == 0) {
-            tc::mbar_expect_tx(bar_tma, (two ? 4 : 2) * 8192);
+            tc::bulk_wait_read_all();  // the previous pair's o tile has left shared memory
+            tc::mbar_expect_tx(bar_tma, (two ? 8 : 4) * 8192);
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                tc::tma_load_3d(sbase + OFF_A + kb * 16384, &tmG, bar_tma, kb * 64, h, b * T + c * C);
-                if (two) tc::tma_load_3d(sbase + OFF_A + kb * 16384 + 8192, &tmG, bar_tma, kb * 64, h, b * T + (c + 1) * C);
+            for (int hb = 0; hb < 2; ++hb) {
+                if (hb == 1 && !two) break;
+                const int row = b * T + (c + hb) * C;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    tc::tma_load_3d(sbase + OFF_A + kb * 16384 + hb * 8192, &tmG, bar_tma, kb * 64, h, row);
+                    tc::tma_load_3d(sbase + OFF_O + kb * 16384 + hb * 8192, &tmO, bar_tma, kb * 64, h, row);
+                }
             }
         }
         ok = tc::mbar_wait(bar_tma, ph, kMaxPolls);
@@ -1598,32 +1610,48 @@ seg_correct_kernel(const __grid_constant__ CUtensorMap tmG, const float* __restr
         if (!__syncthreads_and(ok)) break;
         ph ^= 1u;
         tc::tc_fence_after();
-        const int tok = (tid < 64 ? c * C : (c + 1) * C - 64) + tid;  // this thread's token row
-        TIn* orow = o + ((static_cast<size_t>(b) * T + tok) * H + h) * V;
+        if (half == 0 || two) {
 #pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-            float acc[32];
-            tc::tmem_ld32(tbase + lane_base + q2 * 32, acc);
-            tc::tmem_ld_wait();
-            if (tid < 64 || two) {
+            for (int q2 = 0; q2 < 4; ++q2) {  // 32 value columns at a time
+                float acc[32];
+                tc::tmem_ld32(tbase + lane_base + q2 * 32, acc);
+                tc::tmem_ld_wait();
+                unsigned char* tile = sm + OFF_O + (q2 >> 1) * 16384 + half * 8192;
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    float cur[4];
-                    VecIO<TIn, 4>::load(orow + q2 * 32 + e, cur);
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint4* pp = reinterpret_cast<uint4*>(tile + tc::sw128_off(r, (q2 & 1) * 4 + c8));
+                    uint4 u = *pp;
+                    float cur[8];
+                    VecIO<TIn, 4>::load(reinterpret_cast<const TIn*>(&u), cur);
+                    VecIO<TIn, 4>::load(reinterpret_cast<const TIn*>(&u) + 4, cur + 4);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) cur[i] += acc[e + i];
-                    VecIO<TIn, 4>::store(orow + q2 * 32 + e, cur);
+                    for (int i = 0; i < 8; ++i) cur[i] += acc[c8 * 8 + i];
+                    VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u), cur);
+                    VecIO<TIn, 4>::store(reinterpret_cast<TIn*>(&u) + 4, cur + 4);
+                    *pp = u;
                 }
             }
         }
+        tc::fence_proxy_async();
         tc::tc_fence_before();
-        __syncthreads();  // the A tiles and the accumulator are reused by the next pair
+        __syncthreads();  // the o tile is complete; the A tiles and the accumulator are free again
+        if (tid == 0) {
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                if (hb == 1 && !two) break;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+                    tc::tma_store_3d(&tmO, sbase + OFF_O + kb * 16384 + hb * 8192, kb * 64, h, b * T + (c + hb) * C);
+            }
+            tc::bulk_commit();
+        }
     }
     if (!ok && tid == 0) {  // a wait gave up: record it, let what was issued land, then leave
         atomicExch(&g_timeout_flag, 1u);
         tc::mbar_wait(bar_tma, ph, kMaxPolls >> 4);
         tc::mbar_wait(bar_mma, ph, kMaxPolls >> 4);
     }
+    if (tid == 0) tc::bulk_wait_all();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -1797,12 +1825,13 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        cudaError_t e[6] = {set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC),
+        cudaError_t e[7] = {set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC),
                             set_smem(chunk_prep_kernel<TIn>, prep::SMEM_ALLOC),
                             set_smem(chunk_chain_kernel<TIn, false>, chain::SMEM_ALLOC),
                             set_smem(chunk_chain_kernel<TIn, true>, chain::SMEM_ALLOC),
                             set_smem(chunk_chain_seg_kernel<TIn>, chain::SMEM_ALLOC),
-                            set_smem(seg_correct_kernel<TIn>, segc::SMEM_ALLOC)};
+                            set_smem(seg_correct_kernel<TIn>, segc::SMEM_ALLOC),
+                            set_smem(seg_combine_kernel, COMBINE_SMEM)};
         for (cudaError_t x : e)
             if (x != cudaSuccess && attr_err == cudaSuccess) attr_err = x;
     });
@@ -1869,7 +1898,7 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
         if (e != cudaSuccess || G == 1) return e;
         // the segments' start states (and S_out), then the later segments' output correction
         float* sst = reinterpret_cast<float*>(w + sw.sst);
-        seg_combine_kernel<<<dim3(static_cast<unsigned>(BH), static_cast<unsigned>(a.V / 16)), 256, 0, s>>>(
+        seg_combine_kernel<<<dim3(static_cast<unsigned>(BH), static_cast<unsigned>(a.V / 16)), 256, COMBINE_SMEM, s>>>(
             sg.Z, sg.P, sst, a.S_out, G, a.V);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1877,8 +1906,7 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
         const int pairs = (n_seg + 1) / 2;
         dim3 gr(static_cast<unsigned>(BH), static_cast<unsigned>(G - 1),
                 static_cast<unsigned>(per < pairs ? (per > 0 ? per : 1) : pairs));
-        seg_correct_kernel<TIn><<<gr, 128, segc::SMEM_ALLOC, s>>>(mg, sst, static_cast<TIn*>(a.o), a.T, a.H, a.V, N,
-                                                                 n_seg);
+        seg_correct_kernel<TIn><<<gr, 128, segc::SMEM_ALLOC, s>>>(mg, mo, sst, a.T, a.H, a.V, N, n_seg);
         return cudaGetLastError();
     }
     if (a.alpha) return cudaErrorNotSupported;  // the gate is carried by the two-kernel path only
