@@ -123,8 +123,14 @@ size_t osdn_precond_scan_workspace_bytes(int B, int T, int H, int K, osdn_dtype 
  *   alpha_per_key
  *            1: alpha is [B,T,H,K], one state gate per key channel (OSKDA, Appendix B.2: KDA's
  *            K x V state Diag(alpha_t) S_{t-1}; the state here is its V x K transpose, so column i
- *            is scaled by alpha_{t,i}); such calls run the fp32 CUDA-core kernel.  0: one per head
- *            (OSGDN).  Ignored without alpha; other values OSDN_ERR_ARG.
+ *            is scaled by alpha_{t,i}).  With a workspace of osdn_chunk_fwd_gated_workspace_bytes(
+ *            ..., 2) bytes, bf16/f16 inputs with K = V = 128 run on the tensor cores (the chunk
+ *            form of Listing 3: with Gamma the channels' cumulative gates inside a chunk, the Gram
+ *            and scores of K . Gamma and Q . Gamma against K~ / Gamma as split-bf16 products,
+ *            fp32 UT inverse, fp16 operands in the state pass).  That path needs every channel's
+ *            decay over a chunk (a product of 64 gates) above 1e-30.  Otherwise, or with a smaller
+ *            workspace, the fp32 CUDA-core kernel runs.  0: one per head (OSGDN).  Ignored without
+ *            alpha; other values OSDN_ERR_ARG.
  *   S0       [B,H,V,K] fp32 initial state; NULL means zeros
  *   o        [B,T,H,V] outputs o_t = scale * S_t q_t, dtype `dtype` (written)
  *   S_out    [B,H,V,K] fp32 final state (written; may alias S0)
@@ -165,6 +171,15 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
 size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
                                       osdn_dtype dtype);
 
+/* The same for a gated call: gated = 0 (no gate, as above), 1 (one state gate per head) or 2 (one
+ * per key channel, alpha_per_key = 1).  With gated = 2 and K = V = 128 it is B * H * (T / 64) *
+ * 66048 bytes: besides T', -W and L, each chunk of each head keeps Q . Gamma and K~ . Gamma_C /
+ * Gamma (fp16) and Gamma_C (Gamma: the channels' cumulative gates within the chunk), which lets
+ * osdn_chunk_fwd run that call on the tensor cores (a smaller workspace runs the fp32 CUDA-core
+ * kernel).  0 for invalid arguments. */
+size_t osdn_chunk_fwd_gated_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
+                                            osdn_dtype dtype, int gated);
+
 /*
  * One OSDN layer forward: phase 1 then phase 2, the pages' chunk_osdn (Listing 1: returns o, the
  * final state S and the final preconditioner d) as one call.  Arguments as osdn_precond_scan and
@@ -193,6 +208,10 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
 /* Workspace size in bytes for osdn_layer_fwd's fastest path with these arguments (0 when no
  * workspace is ever used). */
 size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype);
+
+/* The same for a gated call (gated = 0, 1 or 2 as for osdn_chunk_fwd_gated_workspace_bytes). */
+size_t osdn_layer_fwd_gated_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype,
+                                            int gated);
 
 /*
  * The layer forward over packed variable-length sequences (cu_seqlens).  N sequences are
@@ -315,8 +334,9 @@ size_t osdn_layer_bwd_workspace_bytes(int B, int T, int H, int K, int V);
  *   (cudaGetSymbolAddress, which allocates nothing); the first call on a device also loads the
  *   library's device code there, so make that first call before any stream capture.  The
  *   argument checks are osdn_chunk_fwd's and come before the capacity test; only calls that take
- *   the tensor-core path need scratch, so a per-channel gate (alpha_per_key = 1) or fp32 inputs are
- *   never refused for capacity.
+ *   the two-kernel tensor-core path need scratch, so a per-channel gate (alpha_per_key = 1: here the
+ *   CUDA-core kernel, as osdn_chunk_fwd without a workspace) or fp32 inputs are never refused for
+ *   capacity.
  *   All calls share the one array and nothing in it needs to start at zero (each call writes all
  *   the scratch it reads), but calls whose work overlaps on the GPU -- on different streams, or
  *   from different threads -- race on it: serialise them.

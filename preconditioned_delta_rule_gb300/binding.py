@@ -59,6 +59,10 @@ def lib() -> ctypes.CDLL:
     L.osdn_layer_fwd.restype = ctypes.c_int
     L.osdn_layer_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.osdn_layer_fwd_workspace_bytes.restype = sz
+    L.osdn_chunk_fwd_gated_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+    L.osdn_chunk_fwd_gated_workspace_bytes.restype = sz
+    L.osdn_layer_fwd_gated_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+    L.osdn_layer_fwd_gated_workspace_bytes.restype = sz
     ll = ctypes.c_longlong
     L.osdn_layer_fwd_varlen.argtypes = [vp, vp, vp, i, fp, fp, i, fp, i, vp, i, ll, i, fp, fp, vp, vp, fp, fp, i, i, i,
                                         i, f, f, f, f, f, i, vp, sz, vp]
@@ -207,8 +211,9 @@ def osdn_precond_scan_workspace_bytes(B, T, H, K, dtype=torch.bfloat16) -> int:
     return int(lib().osdn_precond_scan_workspace_bytes(B, T, H, K, _code(dtype)))
 
 
-def osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16) -> int:
-    return int(lib().osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, _code(dtype)))
+def osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16, gated=0) -> int:
+    """gated: 0 none, 1 one state gate per head, 2 one per key channel."""
+    return int(lib().osdn_chunk_fwd_gated_workspace_bytes(B, T, H, K, V, chunk, _code(dtype), int(gated)))
 
 
 def _workspace(device, nbytes, role, stream=None):
@@ -245,7 +250,8 @@ def _resolve_workspace(workspace, device, need, role, stream=None):
 def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, alpha=None, o=None, S_out=None, chunk=64,
                    scale=1.0, workspace=None, stream=None):
     """Phase 2 (Eqs. (2), (5), (8)-(11)).  Returns (o [B,T,H,V], S_out [B,H,V,K] fp32).
-    ``alpha`` [B,T,H] fp32: the OSGDN state gate (Appendix B.1, Eqs. (13)-(15)); None for none.
+    ``alpha`` [B,T,H] fp32: the OSGDN state gate (Appendix B.1, Eqs. (13)-(15)), or [B,T,H,K]: one
+    gate per key channel (OSKDA, Appendix B.2); None for none.
 
     ``workspace``: None (default) uses a cached torch buffer of the size the library asks for;
     a uint8 CUDA tensor is used as given; False runs the no-scratch fused kernel."""
@@ -264,7 +270,8 @@ def osdn_chunk_fwd(q, k, k_tilde, v, beta, S0=None, *, alpha=None, o=None, S_out
     if S_out is None:
         S_out = torch.empty((B, H, V, K), device=dev, dtype=torch.float32)
     _check("S_out", S_out, (B, H, V, K), torch.float32, dev)
-    need = osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 else 0
+    gated = 0 if alpha is None else (2 if a_per_key else 1)
+    need = osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, chunk, dt, gated) if T > 0 else 0
     ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "chunk", stream)
     st = lib().osdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(k_tilde), _ptr(v), _code(dt), _ptr(beta),
                               _ptr(alpha), a_per_key, _ptr(S0), _ptr(o), _ptr(S_out), B, T, H, K, V, int(chunk),
@@ -304,8 +311,9 @@ def osdn_check(stream=None, device=None):
     _raise("osdn_check", lib().osdn_check(_stream(dev, stream)))
 
 
-def osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16) -> int:
-    return int(lib().osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, _code(dtype)))
+def osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk=64, dtype=torch.bfloat16, gated=0) -> int:
+    """gated: 0 none, 1 one state gate per head, 2 one per key channel."""
+    return int(lib().osdn_layer_fwd_gated_workspace_bytes(B, T, H, K, V, chunk, _code(dtype), int(gated)))
 
 
 def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, k_tilde=None, o=None,
@@ -338,7 +346,8 @@ def osdn_layer_fwd(q, k, v, beta, r=None, d0=None, S0=None, *, alpha=None, k_til
     if d_out is None:
         d_out = torch.empty((B, H, K), device=dev, dtype=torch.float32)
     _check("d_out", d_out, (B, H, K), torch.float32, dev)
-    need = osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, dt) if T > 0 and T % chunk == 0 else 0
+    gated = 0 if alpha is None else (2 if a_per_key else 1)
+    need = osdn_layer_fwd_workspace_bytes(B, T, H, K, V, chunk, dt, gated) if T > 0 and T % chunk == 0 else 0
     ws_ptr, ws_bytes = _resolve_workspace(workspace, dev, need, "layer", stream)
     st = lib().osdn_layer_fwd(_ptr(q), _ptr(k), _ptr(v), _code(dt), _ptr(beta), _ptr(r), r_per_key, _ptr(alpha),
                               a_per_key, _ptr(d0),

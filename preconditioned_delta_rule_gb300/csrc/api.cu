@@ -167,13 +167,27 @@ osdn_status osdn_chunk_fwd(const void* q, const void* k, const void* k_tilde, co
     return from_cuda(chunk_dispatch(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
-size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
-                                      osdn_dtype dtype) {
+// A stand-in gate pointer for the size queries (never dereferenced): the workspace only depends
+// on whether a gate is given and on its layout.
+static const float* gate_tag(int gated) {
+    static const float tag = 1.f;
+    return gated ? &tag : nullptr;
+}
+
+size_t osdn_chunk_fwd_gated_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype,
+                                            int gated) {
     if (B <= 0 || T <= 0 || H <= 0 || chunk <= 0 || T % chunk != 0) return 0;
-    if (K != 128 || V != 128) return 0;
+    if (K != 128 || V != 128 || gated < 0 || gated > 2) return 0;
     OsdnChunkArgs a{};
     a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.chunk = chunk; a.dtype = dtype;
+    a.alpha = gate_tag(gated);
+    a.alpha_per_key = gated == 2 ? 1 : 0;
     return osdn_chunk_tc_workspace_bytes(a);
+}
+
+size_t osdn_chunk_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk,
+                                      osdn_dtype dtype) {
+    return osdn_chunk_fwd_gated_workspace_bytes(B, T, H, K, V, chunk, dtype, 0);
 }
 
 osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
@@ -214,16 +228,23 @@ osdn_status osdn_layer_fwd(const void* q, const void* k, const void* v, osdn_dty
     return from_cuda(layer_dispatch(sa, ca, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
-size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype) {
-    if (B <= 0 || T <= 0 || H <= 0 || chunk <= 0 || T % chunk != 0) return 0;
+size_t osdn_layer_fwd_gated_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype,
+                                            int gated) {
+    if (B <= 0 || T <= 0 || H <= 0 || chunk <= 0 || T % chunk != 0 || gated < 0 || gated > 2) return 0;
     OsdnScanArgs sa{};
     sa.B = B; sa.T = T; sa.H = H; sa.K = K; sa.k_dtype = dtype; sa.kt_dtype = dtype;
     OsdnChunkArgs ca{};
     ca.B = B; ca.T = T; ca.H = H; ca.K = K; ca.V = V; ca.chunk = chunk; ca.dtype = dtype;
+    ca.alpha = gate_tag(gated);
+    ca.alpha_per_key = gated == 2 ? 1 : 0;
     const size_t fused = osdn_layer_workspace_bytes(sa, ca);
     if (fused) return fused;
     const size_t need_s = osdn_scan_block_workspace_bytes(sa), need_c = osdn_chunk_tc_workspace_bytes(ca);
     return need_c ? align256(need_s) + need_c : need_s;
+}
+
+size_t osdn_layer_fwd_workspace_bytes(int B, int T, int H, int K, int V, int chunk, osdn_dtype dtype) {
+    return osdn_layer_fwd_gated_workspace_bytes(B, T, H, K, V, chunk, dtype, 0);
 }
 
 static OsdnVarlenShape varlen_shape(int N, int max_len, int H, int K, int V, int chunk, osdn_dtype dtype,
@@ -247,7 +268,7 @@ size_t osdn_layer_fwd_varlen_workspace_bytes(int N, int max_len, int H, int K, i
         return 0;
     if (r_mode < 0 || r_mode > 2 || gated < 0 || gated > 2) return 0;
     const OsdnVarlenShape v = varlen_shape(N, max_len, H, K, V, chunk, dtype, r_mode, gated, 0);
-    return align256(osdn_varlen_pad_bytes(v)) + osdn_layer_fwd_workspace_bytes(N, v.Tp, H, K, V, chunk, dtype);
+    return align256(osdn_varlen_pad_bytes(v)) + osdn_layer_fwd_gated_workspace_bytes(N, v.Tp, H, K, V, chunk, dtype, gated);
 }
 
 osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, osdn_dtype dtype, const float* beta,
@@ -286,7 +307,7 @@ osdn_status osdn_layer_fwd_varlen(const void* q, const void* k, const void* v, o
     const int g_mode = alpha ? (alpha_per_key ? 2 : 1) : 0;
     const OsdnVarlenShape vs = varlen_shape(N, max_len, H, K, V, chunk, dtype, r_mode, g_mode, total);
     const size_t pad = align256(osdn_varlen_pad_bytes(vs));
-    const size_t need_layer = osdn_layer_fwd_workspace_bytes(N, vs.Tp, H, K, V, chunk, dtype);
+    const size_t need_layer = osdn_layer_fwd_gated_workspace_bytes(N, vs.Tp, H, K, V, chunk, dtype, g_mode);
     if (workspace_bytes < pad + need_layer) return OSDN_ERR_ARG;
     // the padded batch, each part 256-byte aligned, then the batched layer's own workspace
     unsigned char* w = static_cast<unsigned char*>(workspace);

@@ -469,6 +469,11 @@ constexpr uint32_t WS_T = 0, WS_W = 8192, WS_L = 24576;
 // rho_t = prod_{l > t} alpha_l as 32 fp16 pairs each (tokens 2i, 2i + 1), then gamma_C (fp32)
 constexpr uint32_t WS_GATE = 32768, WS_GAM = 0, WS_RHO = 128, WS_GC = 256;
 constexpr uint32_t WS_CHUNK = 33280;  // a multiple of 128 bytes
+// One state gate per key channel (OSKDA): per chunk of a head T', -W and L as above (with the
+// channel decay inside W and L), then Q . Gamma and K~ . Gamma_C / Gamma as fp16 images in the
+// layout of a loaded tile, then Gamma_C (128 fp32).
+constexpr uint32_t WS_QG = 32768, WS_KTS = 49152, WS_GCV = 65536;
+constexpr uint32_t WS_CHUNK_KDA = 66048;
 
 template <int NW>
 __device__ __forceinline__ void convert_bf16_to_f16(unsigned char* base, int tid) {
@@ -898,6 +903,278 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     if (warp == 0) tc::tmem_dealloc(w.tbase, prep::TMEM_COLS);
 }
 
+
+// =============================================================================================
+// Prep for one state gate per key channel (OSKDA, Appendix B.2; the chunk form of Listing 3).
+// With Gamma_t = prod_{l <= t} alpha_l (per channel, cumulative within the chunk):
+//   A = tril(diag(beta) (K . Gamma) (K~ / Gamma)^T, -1),  T = (I + A)^-1,  T' = T diag(beta),
+//   W = T' (K . Gamma),  L = tril((Q . Gamma) (K~ / Gamma)^T, 0),
+// and for the chain Q . Gamma, K~ . Gamma_C / Gamma and Gamma_C.  K~ / Gamma grows as the decay
+// falls (past fp16's range once a channel decays below ~1e-4 over a chunk), so the scaled tiles
+// are split into bf16 high and low parts (bf16's exponent range, ~16 bits of mantissa together)
+// and each product is formed as hi.hi^T + hi.lo^T + lo.hi^T on the tensor cores; T' enters W the
+// same way.  Every image the chain reads is bounded by the unscaled inputs (the gates are <= 1)
+// and is stored in fp16.  One 128-thread CTA per worker, two per SM, looping over chunks.
+// =============================================================================================
+namespace kdap {
+constexpr uint32_t OFF_AH = 0;       // per key block (16 KB): K rows -> K.Gamma hi | Q rows -> Q.Gamma hi
+                                     //   (after the Gram, the Q slots hold the -W image)
+constexpr uint32_t OFF_AL = 32768;   // per key block: K.Gamma lo | Q.Gamma lo (then T' hi / T' lo)
+constexpr uint32_t OFF_B = 65536;    // K~ -> (K~ / Gamma) hi (16 KB) | lo (16 KB); after the Gram:
+                                     //   A's tiles, T's diagonal tiles, the UT scratch, the L image
+constexpr uint32_t OFF_TD = OFF_B + 10 * kTile * 4;
+constexpr uint32_t OFF_PM = OFF_TD + 4 * kTile * 4;
+constexpr uint32_t OFF_L = OFF_B + 24576;
+constexpr uint32_t OFF_BETA = 98304;
+constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;
+constexpr uint32_t SMEM_ALLOC = OFF_BAR + 32 + 1024;
+constexpr uint32_t TMEM_COLS = 128;
+static_assert(OFF_PM + kUtScratchTiles * kTile * 4 <= OFF_L, "UT scratch below the L image");
+static_assert(2 * SMEM_ALLOC <= 233472, "two workers per SM");
+}  // namespace kdap
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<const uint16_t*>(&h);
+}
+__device__ __forceinline__ float bf16_val(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+__device__ __forceinline__ uint16_t f16_bits(float x) {
+    const __half h = __float2half_rn(x);
+    return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(NTHREADS, 2)
+chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmKT, const float* __restrict__ beta,
+                      const float* __restrict__ alpha, unsigned char* __restrict__ ws, int T, int H, int N, int total) {
+    using namespace kdap;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the chain kernel may set up
+    const uint32_t sbase = tc::smem_u32(sm);
+    const uint32_t bar_tma = sbase + OFF_BAR, bar_mma = sbase + OFF_BAR + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
+    float* AM = reinterpret_cast<float*>(sm + OFF_B);
+    float* TD = reinterpret_cast<float*>(sm + OFF_TD);
+    float* PM = reinterpret_cast<float*>(sm + OFF_PM);
+    float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
+    if (tid == 0) {
+        tc::mbar_init(bar_tma, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::mbar_init_fence();
+        tc::prefetch_tmap(&tmQ);
+        tc::prefetch_tmap(&tmK);
+        tc::prefetch_tmap(&tmKT);
+    }
+    __syncthreads();
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t id_gram = tc::idesc_bf16_f32(128, C, false, false);
+    const uint32_t id_w = tc::idesc_bf16_f32(128, KD, false, true);
+    // this thread's key channel and its place in a loaded 64-wide key-block tile
+    const int ch = tid, kb = ch >> 6, cc = (ch & 63) >> 3, e = ch & 7;
+    uint32_t tph = 0, mph = 0;
+    bool ok = true;
+    for (int q = blockIdx.x; ok && q < total; q += gridDim.x) {
+        const int bh = q / N, n = q - bh * N, b = bh / H, h = bh - b * H;
+        const int row = b * T + n * C;
+        unsigned char* dst = ws + static_cast<size_t>(q) * WS_CHUNK_KDA;
+        if (tid == 0) {
+            tc::bulk_wait_read_all();  // the previous chunk's images have left shared memory
+            tc::mbar_expect_tx(bar_tma, 6 * 8192);
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                tc::tma_load_3d(sbase + OFF_AH + k2 * 16384, &tmK, bar_tma, k2 * 64, h, row);
+                tc::tma_load_3d(sbase + OFF_AH + k2 * 16384 + 8192, &tmQ, bar_tma, k2 * 64, h, row);
+                tc::tma_load_3d(sbase + OFF_B + k2 * 8192, &tmKT, bar_tma, k2 * 64, h, row);
+            }
+        }
+        if (tid < C) sbeta[tid] = beta[(static_cast<size_t>(row) + tid) * H + h];
+        // the channel's cumulative decay over the chunk (fp32, a running product)
+        float gam[C];
+        {
+            const float* ap = alpha + (static_cast<size_t>(row) * H + h) * KD + ch;
+            float g = 1.f;
+#pragma unroll
+            for (int t = 0; t < C; ++t) {
+                g *= ap[static_cast<size_t>(t) * H * KD];
+                gam[t] = g;
+            }
+        }
+        const float gC = gam[C - 1];
+        reinterpret_cast<float*>(dst + WS_GCV)[ch] = gC;
+        ok = tc::mbar_wait(bar_tma, tph, kMaxPolls);
+        if (!__syncthreads_and(ok)) break;
+        tph ^= 1u;
+        // scale the channel's column of K, Q and K~ (64 tokens): bf16 hi / lo parts for the
+        // tensor cores, Q . Gamma and K~ . Gamma_C / Gamma in fp16 for the chain
+        {
+            const uint32_t boff = 2u * e;
+            unsigned char* kq = sm + OFF_AH + kb * 16384;
+            unsigned char* kql = sm + OFF_AL + kb * 16384;
+            unsigned char* kt = sm + OFF_B + kb * 8192;
+            unsigned char* ktl = sm + OFF_B + 16384 + kb * 8192;
+            unsigned char* gq = dst + WS_QG + kb * 8192;
+            unsigned char* gk = dst + WS_KTS + kb * 8192;
+#pragma unroll
+            for (int t = 0; t < C; ++t) {
+                const uint32_t o = tc::sw128_off(t, cc) + boff;
+                const float g = gam[t];
+                const float kx = to_f32(*reinterpret_cast<const TIn*>(kq + o)) * g;
+                const float qx = to_f32(*reinterpret_cast<const TIn*>(kq + 8192 + o)) * g;
+                const float kv = to_f32(*reinterpret_cast<const TIn*>(kt + o));
+                const float zx = kv / fmaxf(g, 1e-30f);
+                const uint16_t kh = bf16_bits(kx), qh = bf16_bits(qx), zh = bf16_bits(zx);
+                *reinterpret_cast<uint16_t*>(kq + o) = kh;
+                *reinterpret_cast<uint16_t*>(kql + o) = bf16_bits(kx - bf16_val(kh));
+                *reinterpret_cast<uint16_t*>(kq + 8192 + o) = qh;
+                *reinterpret_cast<uint16_t*>(kql + 8192 + o) = bf16_bits(qx - bf16_val(qh));
+                *reinterpret_cast<uint16_t*>(kt + o) = zh;
+                *reinterpret_cast<uint16_t*>(ktl + o) = bf16_bits(zx - bf16_val(zh));
+                *reinterpret_cast<uint16_t*>(gq + o) = f16_bits(qx);
+                *reinterpret_cast<uint16_t*>(gk + o) = f16_bits(kv * (gC / fmaxf(g, 1e-30f)));
+            }
+        }
+        tc::fence_proxy_async();
+        __syncthreads();
+        // [K.G; Q.G] (K~/G)^T = hi.hi + hi.lo + lo.hi: lanes 0-63 the Gram, lanes 64-127 the scores
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+                const uint32_t abase = sbase + (part == 2 ? OFF_AL : OFF_AH);
+                const uint32_t bbase = sbase + OFF_B + (part == 1 ? 16384 : 0);
+#pragma unroll
+                for (int st = 0; st < KD / 16; ++st) {
+                    const uint64_t a = tc::sdesc_sw128(abase + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(bbase + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024);
+                    tc::mma_f16(tbase, a, bd, id_gram, (part > 0 || st > 0) ? 1u : 0u);
+                }
+            }
+            tc::mma_commit(bar_mma);
+        }
+        ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
+        if (!__syncthreads_and(ok)) break;
+        mph ^= 1u;
+        tc::tc_fence_after();
+        {
+            const int i = tid & 63;
+            float gr[64];
+            tc::tmem_ld32(tbase + lane_base, *reinterpret_cast<float(*)[32]>(gr));
+            tc::tmem_ld32(tbase + lane_base + 32, *reinterpret_cast<float(*)[32]>(gr + 32));
+            tc::tmem_ld_wait();
+            if (tid < C) {  // Gram rows -> strictly lower A = diag(beta) (K.G) (K~/G)^T
+                const int bi = i >> 4, r = i & 15;
+                const float bt = sbeta[i];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const int bj = j >> 4;
+                    if (bj <= bi) AM[tile_index(bi, bj) * kTile + r * kTileStride + (j & 15)] = (j < i) ? bt * gr[j] : 0.f;
+                }
+            } else {  // score rows -> L = tril(.., 0), fp16 image
+#pragma unroll
+                for (int j = 0; j < 64; ++j) gr[j] = (j <= i) ? gr[j] : 0.f;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + OFF_L, i, c8, gr + 8 * c8);
+            }
+        }
+        tc::tc_fence_before();
+        __syncthreads();
+        ut_inverse_64_aliased(AM, TD, PM, tid, 0);
+        {  // T' = T diag(beta): fp16 image to the workspace, bf16 hi / lo for W
+            const int i = tid >> 1, half = tid & 1, bi = i >> 4, r = i & 15;
+            float tv[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = half * 32 + jj, bj = j >> 4;
+                tv[jj] = ((bj <= bi) ? ut_tile(AM, TD, bi, bj)[r * kTileStride + (j & 15)] : 0.f) * sbeta[j];
+            }
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int c8 = half * 4 + c4;
+                uint32_t w16[4], wh[4], wl[4];
+#pragma unroll
+                for (int p2 = 0; p2 < 4; ++p2) {
+                    const float a0 = tv[c4 * 8 + 2 * p2], a1 = tv[c4 * 8 + 2 * p2 + 1];
+                    w16[p2] = pack_h2(a0, a1);
+                    const uint16_t h0 = bf16_bits(a0), h1 = bf16_bits(a1);
+                    wh[p2] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+                    wl[p2] = static_cast<uint32_t>(bf16_bits(a0 - bf16_val(h0))) |
+                             (static_cast<uint32_t>(bf16_bits(a1 - bf16_val(h1))) << 16);
+                }
+                *reinterpret_cast<uint4*>(dst + WS_T + tc::sw128_off(i, c8)) = make_uint4(w16[0], w16[1], w16[2], w16[3]);
+                *reinterpret_cast<uint4*>(sm + OFF_AL + 8192 + tc::sw128_off(i, c8)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                *reinterpret_cast<uint4*>(sm + OFF_AL + 16384 + 8192 + tc::sw128_off(i, c8)) =
+                    make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            }
+        }
+        tc::fence_proxy_async();
+        tc::tc_fence_before();
+        __syncthreads();
+        // W = T' (K.G) = T'hi (K.G)hi + T'hi (K.G)lo + T'lo (K.G)hi, read from lanes 64-127: the A
+        // operands are [K.G lo (kb); T' hi / lo], whose top rows only fill lanes 0-63
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+                const uint32_t abase = sbase + OFF_AL + (part == 2 ? 16384 : 0);
+                const uint32_t bbase = sbase + (part == 1 ? OFF_AL : OFF_AH);
+#pragma unroll
+                for (int st = 0; st < C / 16; ++st) {
+                    const uint64_t a = tc::sdesc_sw128(abase + st * 32, 16, 1024);
+                    const uint64_t bk = tc::sdesc_sw128(bbase + st * 2048, 16384, 1024);
+                    tc::mma_f16(tbase, a, bk, id_w, (part > 0 || st > 0) ? 1u : 0u);
+                }
+            }
+            tc::mma_commit(bar_mma);
+        }
+        ok = tc::mbar_wait(bar_mma, mph, kMaxPolls);
+        if (!__syncthreads_and(ok)) break;
+        mph ^= 1u;
+        tc::tc_fence_after();
+        if (tid >= C) {  // -W image into the Q slots (Q is no longer needed)
+            const int c = tid - C;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float w[32];
+                tc::tmem_ld32(tbase + lane_base + q4 * 32, w);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = -w[j];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+                    st_row_chunk(sm + OFF_AH + (q4 >> 1) * 16384 + 8192, c, (q4 & 1) * 4 + c4, w + 8 * c4);
+            }
+        }
+        tc::fence_proxy_async();
+        tc::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc::bulk_store(dst + WS_W, sbase + OFF_AH + 8192, 8192);
+            tc::bulk_store(dst + WS_W + 8192, sbase + OFF_AH + 16384 + 8192, 8192);
+            tc::bulk_store(dst + WS_L, sbase + OFF_L, 8192);
+            tc::bulk_commit();
+        }
+    }
+    if (!ok && tid == 0) {  // a wait gave up: record it, let what was issued land, then leave
+        atomicExch(&g_timeout_flag, 1u);
+        tc::mbar_wait(bar_tma, tph, kMaxPolls >> 4);
+        tc::mbar_wait(bar_mma, mph, kMaxPolls >> 4);
+    }
+    if (tid == 0) tc::bulk_wait_all();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+}
+
 namespace chain {
 // Twelve warps with fixed roles (one CTA per (batch, head, 64 rows of S)):
 //   warps 0-3   S^T epilogue (fp32 S^T in tensor memory -> fp16 B operand in shared memory);
@@ -1017,13 +1294,15 @@ struct ChainSeg {
 // and the tokens of K~ by rho (S^T <- gamma_C S^T + (rho . K~)^T X); the S^T epilogue stores the
 // fp16 copy for the S-dependent products from the fp32 state it carries in registers, formed as
 // gamma_C S^T + Y from the update product Y = (rho . K~)^T X that the tensor cores leave on its own.
-template <typename TIn, bool GATED, bool SEG>
+template <typename TIn, bool GATED, bool SEG, bool KDA = false>
 __device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtensorMap& tmKT, const CUtensorMap& tmV,
                                            const CUtensorMap& tmO, const CUtensorMap& tmG, const ChainSeg& sg,
                                            const unsigned char* __restrict__ ws, const float* S0, float* S_out,
                                            int T, int H, int V, int N, float scale) {
     using namespace chain;
+    static_assert(!KDA || GATED, "the channel-gated chain carries its state like the gated one");
     constexpr bool kBf16 = std::is_same<TIn, __nv_bfloat16>::value;
+    constexpr uint32_t kSlot = KDA ? WS_CHUNK_KDA : WS_CHUNK;  // workspace bytes per chunk of a head
     // This CTA's segment of chunks [m0, m0 + NL) and slice (value rows, or key columns of Phi).
     // SEG: blockIdx.y enumerates the first segment's value slices, then for each later segment
     // its value slices and its transition slices (the first segment starts from S0 itself), so
@@ -1101,12 +1380,17 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtenso
                 const uint32_t bar = bars + B_FULL + 8 * s;
                 const uint32_t st = sbase + s * STAGE;
                 const int row = b * T + (m0 + m) * C;
-                const unsigned char* wsc = ws + (static_cast<size_t>(bh) * N + m0 + m) * WS_CHUNK;
+                const unsigned char* wsc = ws + (static_cast<size_t>(bh) * N + m0 + m) * kSlot;
                 tc::mbar_expect_tx(bar, phi ? LOAD_BYTES - (VS / 64) * 8192 : LOAD_BYTES);
+                if (KDA) {  // Q . Gamma and K~ . Gamma_C / Gamma, formed by the prep
+                    tc::bulk_load(st + ST_Q, wsc + WS_QG, 16384, bar);
+                    tc::bulk_load(st + ST_KT, wsc + WS_KTS, 16384, bar);
+                } else {
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-                    tc::tma_load_3d(st + ST_Q + kb * 8192, &tmQ, bar, kb * 64, h, row);
-                    tc::tma_load_3d(st + ST_KT + kb * 8192, &tmKT, bar, kb * 64, h, row);
+                    for (int kb = 0; kb < 2; ++kb) {
+                        tc::tma_load_3d(st + ST_Q + kb * 8192, &tmQ, bar, kb * 64, h, row);
+                        tc::tma_load_3d(st + ST_KT + kb * 8192, &tmKT, bar, kb * 64, h, row);
+                    }
                 }
                 if (!phi) {  // a transition slice has zero values
 #pragma unroll
@@ -1260,11 +1544,11 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtenso
         // the prep), read from the workspace one chunk ahead
         uint32_t gpair = 0, rpair = 0, gnext = 0, rnext = 0;
         auto gates_of = [&](int m) {  // (the gated chain is never segmented: m0 = 0)
-            const uint32_t* wg = reinterpret_cast<const uint32_t*>(ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK + WS_GATE);
+            const uint32_t* wg = reinterpret_cast<const uint32_t*>(ws + (static_cast<size_t>(bh) * N + m) * kSlot + WS_GATE);
             gnext = wg[(WS_GAM >> 2) + lane];
             rnext = wg[(WS_RHO >> 2) + lane];
         };
-        if (GATED) {
+        if (GATED && !KDA) {
             gates_of(0);
             gpair = gnext;
             rpair = rnext;
@@ -1303,7 +1587,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtenso
             } else {
                 uint32_t qh[32];
                 uint32_t gq = 0;  // gated: row r of Q scaled by gamma_r (an fp16 pair of it)
-                if (GATED) {
+                if (GATED && !KDA) {
                     const uint32_t gp = __shfl_sync(0xffffffffu, gpair, r >> 1);
                     const uint32_t g16 = (r & 1) ? (gp >> 16) : (gp & 0xffffu);
                     gq = g16 | (g16 << 16);
@@ -1316,7 +1600,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtenso
                         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            qh[c * 4 + j] = GATED ? mul_f16x2<kBf16>(w[j], gq) : (kBf16 ? bf16x2_to_f16x2(w[j]) : w[j]);
+                            qh[c * 4 + j] = KDA ? w[j] : GATED ? mul_f16x2<kBf16>(w[j], gq) : (kBf16 ? bf16x2_to_f16x2(w[j]) : w[j]);
                     }
                     tc::tmem_st32u(tbase + lane_base + COL_QW + bb * 64 + kb * 32, qh);
                 }
@@ -1325,7 +1609,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtenso
             if (kBf16 && !phi) convert_bf16_to_f16<(VS / 64) * 4>(const_cast<unsigned char*>(stg) + ST_V, w4 * 32 + lane);
             tc::tmem_st_wait();
             warp_publish(bars + B_CONVA + 8 * bb, lane);
-            if (GATED && m + 1 < NL) gates_of(m + 1);
+            if (GATED && !KDA && m + 1 < NL) gates_of(m + 1);
             // K~^T (lane = key); its buffer was last read by the S^T update of chunk m - 1
             if (m >= 1 && !(ok = warp_wait(bars + B_ST, (m - 1) & 1, abort_flag))) break;
             tc::tc_fence_after();
@@ -1338,7 +1622,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtenso
                     const uint32_t a0 = *reinterpret_cast<const uint16_t*>(kt + tc::sw128_off(2 * t2, c));
                     const uint32_t a1 = *reinterpret_cast<const uint16_t*>(kt + tc::sw128_off(2 * t2 + 1, c));
                     const uint32_t pr = a0 | (a1 << 16);
-                    if (GATED) {  // tokens 2 t2, 2 t2 + 1 scaled by their rho
+                    if (KDA) {  // already scaled, fp16
+                        kw[t2] = pr;
+                    } else if (GATED) {  // tokens 2 t2, 2 t2 + 1 scaled by their rho
                         kw[t2] = mul_f16x2<kBf16>(pr, __shfl_sync(0xffffffffu, rpair, t2));
                     } else {
                         kw[t2] = kBf16 ? bf16x2_to_f16x2(pr) : pr;
@@ -1375,8 +1661,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtenso
         // ============================ S^T and X epilogues =====================================
         const int k = tid;  // key coordinate = tensor-memory lane
         // gated: gamma_C of a chunk (the product of its 64 state gates, formed by the prep)
-        auto gamma_c = [&](int m) -> float {
-            return *reinterpret_cast<const float*>(ws + (static_cast<size_t>(bh) * N + m) * WS_CHUNK + WS_GATE + WS_GC);
+        auto gamma_c = [&](int m) -> float {  // channel-gated: this lane's (key channel's) Gamma_C
+            if (KDA) return reinterpret_cast<const float*>(ws + (static_cast<size_t>(bh) * N + m) * kSlot + WS_GCV)[k];
+            return *reinterpret_cast<const float*>(ws + (static_cast<size_t>(bh) * N + m) * kSlot + WS_GATE + WS_GC);
         };
         // gated: this lane's row of S^T (fp32) carried in registers; the update MMA leaves
         // Y = (rho . K~)^T X in tensor memory and S^T <- gamma_C S^T + Y is formed here
@@ -1458,13 +1745,13 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmQ, const CUtenso
     if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
 }
 
-template <typename TIn, bool GATED>
+template <typename TIn, bool GATED, bool KDA = false>
 __global__ void __launch_bounds__(chain::NT, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKT,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                    const unsigned char* __restrict__ ws, const float* S0, float* S_out, int T, int H,
                    int V, int N, float scale) {
-    chain_body<TIn, GATED, false>(tmQ, tmKT, tmV, tmO, tmO, ChainSeg{N, 0, nullptr, nullptr}, ws, S0, S_out, T, H, V,
+    chain_body<TIn, GATED, false, KDA>(tmQ, tmKT, tmV, tmO, tmO, ChainSeg{N, 0, nullptr, nullptr}, ws, S0, S_out, T, H, V,
                                   N, scale);
 }
 // The segmented pass: grid (B H, value slices x (2 G - 1)), see chain_body.
@@ -1825,20 +2112,54 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        cudaError_t e[7] = {set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC),
+        cudaError_t e[9] = {set_smem(chunk_tc_kernel<TIn>, fused::SMEM_ALLOC),
                             set_smem(chunk_prep_kernel<TIn>, prep::SMEM_ALLOC),
                             set_smem(chunk_chain_kernel<TIn, false>, chain::SMEM_ALLOC),
                             set_smem(chunk_chain_kernel<TIn, true>, chain::SMEM_ALLOC),
                             set_smem(chunk_chain_seg_kernel<TIn>, chain::SMEM_ALLOC),
                             set_smem(seg_correct_kernel<TIn>, segc::SMEM_ALLOC),
-                            set_smem(seg_combine_kernel, COMBINE_SMEM)};
+                            set_smem(seg_combine_kernel, COMBINE_SMEM),
+                            set_smem(chunk_prep_kda_kernel<TIn>, kdap::SMEM_ALLOC),
+                            set_smem(chunk_chain_kernel<TIn, true, true>, chain::SMEM_ALLOC)};
         for (cudaError_t x : e)
             if (x != cudaSuccess && attr_err == cudaSuccess) attr_err = x;
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int N = a.T / C;
-    const size_t need = static_cast<size_t>(a.B) * a.H * N * WS_CHUNK;
     dim3 block(NTHREADS);
+    if (a.alpha && a.alpha_per_key) {  // one gate per key channel: its prep, then the channel-gated chain
+        const size_t need_kda = static_cast<size_t>(a.B) * a.H * N * WS_CHUNK_KDA;
+        if (ws == nullptr || ws_bytes < need_kda || chain_only) return cudaErrorNotSupported;
+        unsigned char* w = static_cast<unsigned char*>(ws);
+        const int total = a.B * a.H * N;
+        dim3 gp(static_cast<unsigned>(total < 2 * num_sms() ? total : 2 * num_sms()));
+        chunk_prep_kda_kernel<TIn><<<gp, block, kdap::SMEM_ALLOC, s>>>(mq, mk, mkt, a.beta, a.alpha, w, a.T, a.H, N,
+                                                                      total);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        dim3 gc(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(a.V / VS));
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = gc;
+        cfg.blockDim = dim3(chain::NT);
+        cfg.dynamicSmemBytes = chain::SMEM_ALLOC;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const unsigned char* wsc = w;
+        e = cudaLaunchKernelEx(&cfg, chunk_chain_kernel<TIn, true, true>, mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T,
+                               a.H, a.V, N, a.scale);
+        if (e == cudaErrorNotSupported) {
+            (void)cudaGetLastError();
+            chunk_chain_kernel<TIn, true, true><<<gc, dim3(chain::NT), chain::SMEM_ALLOC, s>>>(
+                mq, mkt, mv, mo, wsc, a.S0, a.S_out, a.T, a.H, a.V, N, a.scale);
+            e = cudaGetLastError();
+        }
+        return e;
+    }
+    const size_t need = static_cast<size_t>(a.B) * a.H * N * WS_CHUNK;
     if (ws != nullptr && ws_bytes >= need) {
         unsigned char* w = static_cast<unsigned char*>(ws);
         const int BH = a.B * a.H;
@@ -1917,9 +2238,9 @@ cudaError_t launch_tc(const OsdnChunkArgs& a, void* ws, size_t ws_bytes, cudaStr
 }
 
 bool tc_covers(const OsdnChunkArgs& a) {
-    // (one state gate per key channel puts the decay inside the Gram's contraction: not built here)
+    // (one state gate per key channel: only with a workspace, through its own prep kernel)
     return a.K == KD && a.V % VS == 0 && a.chunk == C && a.T > 0 && a.T % C == 0 &&
-           (a.dtype == OSDN_BF16 || a.dtype == OSDN_F16) && !(a.alpha && a.alpha_per_key);
+           (a.dtype == OSDN_BF16 || a.dtype == OSDN_F16);
 }
 
 // Workspace of the fused layer: [scan: step sizes, block-start states][chunk counter][chunk
@@ -1940,7 +2261,7 @@ LayerWs layer_ws(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
 }
 
 bool layer_covers(const OsdnScanArgs& sa, const OsdnChunkArgs& ca) {
-    return tc_covers(ca) && ca.V == KD && sa.K == KD && sa.k_dtype == ca.dtype && sa.kt_dtype == ca.dtype && !sa.r_per_key &&
+    return tc_covers(ca) && !(ca.alpha && ca.alpha_per_key) && ca.V == KD && sa.K == KD && sa.k_dtype == ca.dtype && sa.kt_dtype == ca.dtype && !sa.r_per_key &&
            ca.B * ca.H < num_sms() && osdn_scan_block_workspace_bytes(sa) > 0;
 }
 
@@ -2019,7 +2340,7 @@ cudaError_t osdn_launch_layer(const OsdnScanArgs& sa, const OsdnChunkArgs& ca, v
 }
 
 size_t osdn_chunk_tc_plain_workspace_bytes(const OsdnChunkArgs& a) {
-    if (!osdn::tc_covers(a)) return 0;
+    if (!osdn::tc_covers(a) || (a.alpha && a.alpha_per_key)) return 0;
     return static_cast<size_t>(a.B) * a.H * (a.T / osdn::C) * osdn::WS_CHUNK;
 }
 
@@ -2027,6 +2348,7 @@ size_t osdn_chunk_tc_plain_workspace_bytes(const OsdnChunkArgs& a) {
 // query does not see it).
 size_t osdn_chunk_tc_workspace_bytes(const OsdnChunkArgs& a) {
     if (!osdn::tc_covers(a)) return 0;
+    if (a.alpha && a.alpha_per_key) return static_cast<size_t>(a.B) * a.H * (a.T / osdn::C) * osdn::WS_CHUNK_KDA;
     const int G = osdn::seg_count(a.B, a.H, a.T, a.V);
     if (G > 1) return osdn::seg_ws(a, G).total;
     return osdn_chunk_tc_plain_workspace_bytes(a);

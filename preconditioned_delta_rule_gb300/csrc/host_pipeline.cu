@@ -56,7 +56,7 @@ HostLayout host_layout(int B, int T, int H, int K, int V, int chunk, osdn_dtype 
     L.slot[1] = o + s;
     o += 2 * s;
     L.layer = o;
-    o += osdn_layer_fwd_workspace_bytes(B, static_cast<int>(Ts), H, K, V, chunk, dtype);
+    o += osdn_layer_fwd_gated_workspace_bytes(B, static_cast<int>(Ts), H, K, V, chunk, dtype, g_mode);
     L.total = o;
     return L;
 }

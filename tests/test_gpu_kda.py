@@ -110,3 +110,57 @@ def test_channel_gated_decode_against_oracle(dtype, K, V):
         assert_maxabs(o, o_ref, tol, what=f"o step {t}")
     assert_maxabs(Sd, S_ref, tol, what="S")
     assert_rel(dd, d_ref, 1e-5, what="d")
+
+
+# ---- the tensor-core path for one gate per key channel (a workspace of the channel-gated size) ----
+
+def bench_like_gates(shape, seed):
+    """sigmoid(4 + N(0, 1)) per token, head and channel: the bench's channel-gated leg."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.sigmoid(4.0 + torch.randn(*shape, generator=g))
+
+
+@pytest.mark.parametrize("gates", ["bench", "harsh"])
+def test_channel_gated_tensor_core_full_size(gates):
+    """The 340M-shaped layer (B8 H8 T2048) on the tensor-core path against the fp64 oracle: the
+    bench's gates, and gates uniform in [0.6, 1] whose decay over a chunk reaches ~1e-7 (K~ / Gamma
+    far beyond fp16's range, carried by the split-bf16 products)."""
+    w = W.WORKLOADS["layer_340m"]
+    inp = W.make_prefill(w, seed=71)
+    B, T, H, K = inp["k"].shape
+    V = inp["v"].shape[-1]
+    alpha = bench_like_gates((B, T, H, K), 72) if gates == "bench" else channel_gates((B, T, H, K), 72)
+    S0 = torch.randn(B, H, V, K, generator=torch.Generator().manual_seed(73)) * 0.1
+    kt_ref, _ = oracle.precond_scan(inp["k"], inp["beta"], None, None, eta=w.eta)
+    kt = torch.from_numpy(kt_ref).to(inp["k"].dtype)
+    need = binding.osdn_chunk_fwd_workspace_bytes(B, T, H, K, V, 64, inp["k"].dtype, gated=2)
+    assert need == B * H * (T // 64) * 66048
+    dev = to_dev(inp)
+    o, S = osdn_chunk_fwd(dev["q"], dev["k"], kt.cuda(), dev["v"], dev["beta"], S0.cuda(), alpha=alpha.cuda())
+    torch.cuda.synchronize()
+    binding.osdn_check()
+    o_ref, S_ref = oracle.delta_phase2(inp["q"], inp["k"], kt, inp["v"], inp["beta"], S0, alpha=alpha)
+    eo = assert_maxabs(o, o_ref, 2e-2, what="o")
+    es = assert_maxabs(S, S_ref, 2e-2, what="S")
+    print(f"{gates} gates: max|o err| {eo:.3e} max|S err| {es:.3e}")
+
+
+def test_channel_gated_tensor_core_matches_cuda_core_path():
+    """A workspace of the ungated size runs the fp32 CUDA-core kernel; the tensor-core path agrees
+    with it within the 16-bit bar, and a dirty reused workspace gives identical results."""
+    w = W.WORKLOADS["layer_1p3b_apf"]
+    B, H, T = 2, 3, 512
+    inp = W.make_prefill(w, B=B, H=H, T=T, seed=74)
+    alpha = channel_gates((B, T, H, 128), 75, lo=0.8).cuda()
+    dev = to_dev(inp)
+    kt, _ = osdn_precond_scan(dev["k"], dev["beta"], dev["r"], None, eta=w.eta)
+    small = torch.empty(binding.osdn_chunk_fwd_workspace_bytes(B, T, H, 128, 128), dtype=torch.uint8, device="cuda")
+    o1, S1 = osdn_chunk_fwd(dev["q"], dev["k"], kt, dev["v"], dev["beta"], alpha=alpha, workspace=small)
+    big = torch.full((binding.osdn_chunk_fwd_workspace_bytes(B, T, H, 128, 128, gated=2),), 0x7F, dtype=torch.uint8,
+                     device="cuda")
+    o2, S2 = osdn_chunk_fwd(dev["q"], dev["k"], kt, dev["v"], dev["beta"], alpha=alpha, workspace=big)
+    o3, S3 = osdn_chunk_fwd(dev["q"], dev["k"], kt, dev["v"], dev["beta"], alpha=alpha, workspace=big)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o3) and torch.equal(S2, S3)
+    assert_maxabs(o2, o1, 2e-2, what="o tensor-core vs CUDA-core")
+    assert_maxabs(S2, S1, 2e-2, what="S tensor-core vs CUDA-core")

@@ -188,6 +188,21 @@ def test_varlen_validation(L, kw, want):
     assert varlen(L, **kw) == want
 
 
+def test_gated_workspace_size_queries(L):
+    """gated = 2 (one gate per key channel) keeps Q . Gamma, K~ . Gamma_C / Gamma and Gamma_C per
+    chunk besides the images: 66048 bytes per chunk of each head; gated 0 and 1 as the plain query."""
+    f, f0 = L.osdn_chunk_fwd_gated_workspace_bytes, L.osdn_chunk_fwd_workspace_bytes
+    assert f(8, 2048, 8, 128, 128, 64, 1, 0) == f0(8, 2048, 8, 128, 128, 64, 1) == 8 * 8 * 32 * 33280
+    assert f(8, 2048, 8, 128, 128, 64, 1, 1) == 8 * 8 * 32 * 33280
+    assert f(8, 2048, 8, 128, 128, 64, 1, 2) == 8 * 8 * 32 * 66048
+    assert f(8, 2048, 8, 128, 128, 64, 1, 3) == 0 and f(8, 2048, 8, 128, 128, 64, 1, -1) == 0
+    g, g0 = L.osdn_layer_fwd_gated_workspace_bytes, L.osdn_layer_fwd_workspace_bytes
+    assert g(8, 2048, 8, 128, 128, 64, 1, 0) == g0(8, 2048, 8, 128, 128, 64, 1)
+    scan = 4 * 8 * 8 * (2048 + 32 * 256)
+    assert g(8, 2048, 8, 128, 128, 64, 1, 2) == (scan + 255) // 256 * 256 + 8 * 8 * 32 * 66048
+    assert g(8, 2048, 8, 128, 128, 64, 1, 3) == 0
+
+
 def test_varlen_workspace_size_query(L):
     f = L.osdn_layer_fwd_varlen_workspace_bytes
     lay = L.osdn_layer_fwd_workspace_bytes
@@ -200,7 +215,9 @@ def test_varlen_workspace_size_query(L):
     assert f(N, 0, H, 128, 128, 64, 1, 0, 0) > 0   # all empty: one chunk of padding each
     assert f(0, 300, H, 128, 128, 64, 1, 0, 0) == 0
     assert f(N, 300, H, 128, 128, 64, 1, 3, 0) == 0
-    assert f(N, 300, H, 128, 128, 64, 1, 0, 2) == up(pad + up(rows * H * 128 * 4)) + lay(N, Tp, H, 128, 128, 64, 1)
+    # one gate per key channel: the batched layer's workspace is the channel-gated one
+    layg = L.osdn_layer_fwd_gated_workspace_bytes
+    assert f(N, 300, H, 128, 128, 64, 1, 0, 2) == up(pad + up(rows * H * 128 * 4)) + layg(N, Tp, H, 128, 128, 64, 1, 2)
     assert f(N, 300, H, 128, 128, 64, 1, 0, 3) == 0
 
 

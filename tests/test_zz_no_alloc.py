@@ -117,8 +117,9 @@ def test_static_scratch_rejects_requests_over_capacity():
 
 
 def test_static_scratch_channel_gate_needs_no_scratch():
-    """One gate per key channel runs the CUDA-core kernel, which needs no scratch: never refused for
-    capacity, and identical to osdn_chunk_fwd."""
+    """One gate per key channel runs the CUDA-core kernel here, which needs no scratch: never refused
+    for capacity, and identical to osdn_chunk_fwd without a workspace (the same kernel; with the
+    channel-gated workspace osdn_chunk_fwd takes the tensor-core path instead)."""
     B, T, H = 1, 64 * 1009, 1
     gen = torch.Generator().manual_seed(37)
     mk = lambda *s: (torch.randn(*s, generator=gen) * 0.1).to(torch.bfloat16).cuda()
@@ -126,6 +127,6 @@ def test_static_scratch_channel_gate_needs_no_scratch():
     beta = torch.sigmoid(torch.randn(B, T, H, generator=gen)).cuda()
     alpha = torch.sigmoid(4.0 + torch.randn(B, T, H, 128, generator=gen)).cuda()
     g = dict(q=q, k=k, v=v, beta=beta)
-    o_ref, S_ref = osdn_chunk_fwd(q, k, kt, v, beta, None, alpha=alpha)  # [B,T,H,K]: one gate per channel
+    o_ref, S_ref = osdn_chunk_fwd(q, k, kt, v, beta, None, alpha=alpha, workspace=False)  # one gate per channel
     o, S = _run_static(g, kt, None, alpha=alpha, alpha_per_key=1, like=(o_ref, S_ref))
     assert torch.equal(o, o_ref) and torch.equal(S, S_ref)
