@@ -588,7 +588,8 @@ cudaError_t launch_bwd(const OsdnBwdArgs& a, void* ws, cudaStream_t s) {
     // its record of step sizes and block-start states drives the phase-1 reverse sweep
     OsdnScanArgs sa{a.k, a.dtype, a.beta, a.r, a.d0, kt, OSDN_F32, ck1, a.B, a.T, a.H, K, a.eta, a.d_min, a.d_max,
                     a.eps, a.beta_aware, a.r ? a.r_per_key : 0};
-    const size_t scan_ws = (K == 128 && sizeof(TIn) == 2) ? osdn_scan_block_workspace_bytes(sa) : 0;
+    // (the record drives bwd_phase1_blk_kernel, which takes one retention gate per head)
+    const size_t scan_ws = (K == 128 && sizeof(TIn) == 2 && !sa.r_per_key) ? osdn_scan_block_workspace_bytes(sa) : 0;
     float* sws = ck1 + static_cast<size_t>(a.B) * a.H * (nch + 1) * K;
     // d_out of this scan is scratch (ck1 is overwritten below by the phase-1 kernel's checkpoints)
     e = osdn_launch_scan(sa, scan_ws ? sws : nullptr, scan_ws, s);

@@ -21,6 +21,11 @@
 // clip, and the block restarts there with the new classification (after 8 restarts in a block
 // the rest of the block runs token by token).  The result is the sequential algorithm's, up to
 // reassociation.  d is carried across blocks as an unevaluated fp32 pair (hi + lo).
+// With one gate per key coordinate (diag(r_t), Appendix A.5) the free trajectories no longer share
+// one product of gates, so every block is solved by Jacobi sweeps on the clipped recurrence itself:
+// each coordinate runs its own trajectory d_{j+1} = clip(r_{j,i} d_j + g_j s_j) under a guess of
+// the g's, and the products d_j s_j summed over the coordinates give the next guess.  The gates
+// are staged with the keys, in the space the Gram path uses for its fp16 s copies and Gram rows.
 //
 // Mapping: one CTA of 256 threads per (batch, head).  Warpgroup 0 ("chain") runs the serial part
 // above, one key coordinate per thread.  Warpgroup 1 prepares block b+1 (cp.async staging of the
@@ -40,7 +45,7 @@ using namespace scanblk;
 // Set when a bounded wait of the scan kernel gave up (read and cleared by osdn_check).
 __device__ unsigned int g_scan_timeout_flag = 0;
 
-template <typename TIn, typename TOut, bool HAS_R>
+template <typename TIn, typename TOut, int RM>
 __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float* ws_g, float* ws_d) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ uint32_t s_tmem;
@@ -49,7 +54,7 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tbase = s_tmem;
-    scan_block_body<TIn, TOut, HAS_R>(a, ws_g, ws_d, blockIdx.x, smem_raw, tbase, &g_scan_timeout_flag);
+    scan_block_body<TIn, TOut, RM>(a, ws_g, ws_d, blockIdx.x, smem_raw, tbase, &g_scan_timeout_flag);
     if (threadIdx.x < 32) tc::tmem_dealloc(tbase, TMEM_COLS);
 }
 
@@ -59,9 +64,10 @@ __global__ void __launch_bounds__(NT, 1) scan_block_kernel(OsdnScanArgs a, float
 // (head, block, coordinate slice); small CTAs keep many blocks in flight so that loads, the
 // dependent 64-step loop and stores of different blocks overlap.  The key slice (64 rows of
 // 2 EC bytes) moves through shared memory in 16-byte pieces; 16-bit write keys overwrite their key
-// in the tile and leave the same way, fp32 write keys go straight out.
+// in the tile and leave the same way, fp32 write keys go straight out.  RM as in scan_block_body:
+// with one gate per coordinate (RM = 2) each thread reads its coordinate's gates, 32 tokens ahead.
 constexpr int EC = 32;
-template <typename TIn, typename TOut, bool HAS_R>
+template <typename TIn, typename TOut, int RM>
 __global__ void __launch_bounds__(EC) scan_emit_kernel(OsdnScanArgs a, const float* __restrict__ ws_g,
                                                        const float* __restrict__ ws_d) {
     static_assert(sizeof(TIn) == 2, "16-bit keys");
@@ -85,7 +91,7 @@ __global__ void __launch_bounds__(EC) scan_emit_kernel(OsdnScanArgs a, const flo
     for (int jj = i; jj < J; jj += EC) {
         const bool valid = jj < jb;
         sg[jj] = valid ? ws_g[static_cast<size_t>(bh) * T + t0 + jj] : 0.f;
-        sr[jj] = (HAS_R && valid) ? a.r[row0 + static_cast<size_t>(t0 + jj) * H] : 1.f;
+        sr[jj] = (RM == 1 && valid) ? a.r[row0 + static_cast<size_t>(t0 + jj) * H] : 1.f;
     }
     const float* wd = ws_d + (static_cast<size_t>(bh) * nblk + m) * (2 * KD) + c0;
     float d = wd[i] + wd[KD + i];
@@ -94,16 +100,19 @@ __global__ void __launch_bounds__(EC) scan_emit_kernel(OsdnScanArgs a, const flo
     // 32 tokens at a time: keys and increments first, then the serial steps, then the stores
 #pragma unroll
     for (int j0 = 0; j0 < J; j0 += 32) {
-        float kv[32], inc[32], kt[32];
+        float kv[32], inc[32], kt[32], rv[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            kv[j] = j0 + j < jb ? to_f32(tile[(j0 + j) * EC + i]) : 0.f;
+            const bool valid = j0 + j < jb;
+            kv[j] = valid ? to_f32(tile[(j0 + j) * EC + i]) : 0.f;
             inc[j] = replay_inc(sg[j0 + j], kv[j]);
+            if constexpr (RM == 2) rv[j] = valid ? a.r[(row0 + static_cast<size_t>(t0 + j0 + j) * H) * KD + c0 + i] : 1.f;
+            else rv[j] = sr[j0 + j];
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             kt[j] = d * kv[j];
-            d = replay_step(d, sr[j0 + j], inc[j], dmin, dmax);
+            d = replay_step(d, rv[j], inc[j], dmin, dmax);
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -126,11 +135,13 @@ __global__ void __launch_bounds__(EC) scan_emit_kernel(OsdnScanArgs a, const flo
 template <typename TIn, typename TOut>
 cudaError_t launch_b(const OsdnScanArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
     static cudaError_t attr = [] {
-        cudaError_t e1 = cudaFuncSetAttribute(scan_block_kernel<TIn, TOut, true>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-        cudaError_t e2 = cudaFuncSetAttribute(scan_block_kernel<TIn, TOut, false>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-        return e1 != cudaSuccess ? e1 : e2;
+        cudaError_t e[3] = {
+            cudaFuncSetAttribute(scan_block_kernel<TIn, TOut, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC),
+            cudaFuncSetAttribute(scan_block_kernel<TIn, TOut, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC),
+            cudaFuncSetAttribute(scan_block_kernel<TIn, TOut, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC)};
+        for (cudaError_t x : e)
+            if (x != cudaSuccess) return x;
+        return cudaSuccess;
     }();
     if (attr != cudaSuccess) return attr;
     dim3 grid(static_cast<unsigned>(a.B * a.H)), block(NT);
@@ -142,13 +153,16 @@ cudaError_t launch_b(const OsdnScanArgs& a, void* ws, size_t ws_bytes, cudaStrea
         ws_g = static_cast<float*>(ws);
         ws_d = ws_g + static_cast<size_t>(a.B) * a.H * a.T;
     }
-    if (a.r) scan_block_kernel<TIn, TOut, true><<<grid, block, SMEM_ALLOC, s>>>(a, ws_g, ws_d);
-    else scan_block_kernel<TIn, TOut, false><<<grid, block, SMEM_ALLOC, s>>>(a, ws_g, ws_d);
+    const int rm = a.r ? (a.r_per_key ? 2 : 1) : 0;
+    if (rm == 2) scan_block_kernel<TIn, TOut, 2><<<grid, block, SMEM_ALLOC, s>>>(a, ws_g, ws_d);
+    else if (rm == 1) scan_block_kernel<TIn, TOut, 1><<<grid, block, SMEM_ALLOC, s>>>(a, ws_g, ws_d);
+    else scan_block_kernel<TIn, TOut, 0><<<grid, block, SMEM_ALLOC, s>>>(a, ws_g, ws_d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || ws_g == nullptr) return e;
     dim3 ge(static_cast<unsigned>(nblk), static_cast<unsigned>(a.B * a.H), KD / EC), be(EC);
-    if (a.r) scan_emit_kernel<TIn, TOut, true><<<ge, be, 0, s>>>(a, ws_g, ws_d);
-    else scan_emit_kernel<TIn, TOut, false><<<ge, be, 0, s>>>(a, ws_g, ws_d);
+    if (rm == 2) scan_emit_kernel<TIn, TOut, 2><<<ge, be, 0, s>>>(a, ws_g, ws_d);
+    else if (rm == 1) scan_emit_kernel<TIn, TOut, 1><<<ge, be, 0, s>>>(a, ws_g, ws_d);
+    else scan_emit_kernel<TIn, TOut, 0><<<ge, be, 0, s>>>(a, ws_g, ws_d);
     return cudaGetLastError();
 }
 
@@ -175,8 +189,7 @@ cudaError_t osdn_scan_block_read_and_clear_timeout(unsigned int* flag) {
 }
 
 bool osdn_scan_block_covers(const OsdnScanArgs& a) {
-    // (one retention per head: the blocked solve scales the Gram by scalar products of gates)
-    return a.K == osdn::KD && a.T > 0 && (a.k_dtype == OSDN_BF16 || a.k_dtype == OSDN_F16) && !a.r_per_key;
+    return a.K == osdn::KD && a.T > 0 && (a.k_dtype == OSDN_BF16 || a.k_dtype == OSDN_F16);
 }
 
 size_t osdn_scan_block_workspace_bytes(const OsdnScanArgs& a) {

@@ -29,11 +29,12 @@
 // Mapping: one CTA of 256 threads per (batch, head).  Warpgroup 0 ("chain") runs the serial part
 // above, one key coordinate per thread, reading s = k.k straight from the staged keys (the square
 // of a 16-bit key is exact in fp32).  Warpgroup 1 prepares block b+1 (cp.async staging of the keys
-// three blocks ahead, the norms |k_t|^2 and gates, power-of-two-scaled fp16 hi/lo copies of s and
-// the Gram on the tensor cores, copied to shared memory as the chain's Jacobi rows), writes the
-// step sizes and start state of block b to the workspace when there is one, and otherwise emits
-// the write keys of block b by replaying the clipped recurrence with the chain's g values.  The
-// warpgroups hand blocks over through mbarriers.
+// three blocks ahead, the norms |k_t|^2 and gates; when the chain used a Gram in its latest block,
+// power-of-two-scaled fp16 hi/lo copies of s and the Gram on the tensor cores, copied to shared
+// memory as the chain's Jacobi rows; the fp32 s rows), writes the step sizes and start state of
+// block b to the workspace when there is one, and otherwise emits the write keys of block b by
+// replaying the clipped recurrence with the chain's g values.  The warpgroups hand blocks over
+// through mbarriers.
 
 #pragma once
 #include <type_traits>
@@ -91,11 +92,18 @@ constexpr int F_END = F_SMX + 128;
 constexpr uint32_t OFF_BAR = OFF_F + ((F_END * 4 + 127) / 128) * 128;
 constexpr uint32_t SMEM_BASE = OFF_BAR + 128;
 // the all-free Gram of a block (two slots), scaled and masked to l < j, fp32 rows of MROW floats
+// (the third gate slot of the vector-retention mode, which has no Gram)
 constexpr int MROW = J + 4;
 constexpr uint32_t MT_BYTES = J * MROW * 4;
 constexpr uint32_t OFF_MT = ((SMEM_BASE + 127) / 128) * 128;
 constexpr uint32_t SMEM_USED = OFF_MT + 2 * MT_BYTES;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+// Vector retention (one gate per key coordinate, RM = 2): the gates of a block, J x KD fp32 rows,
+// staged with its keys in three slots, in the space of the fp16 s copies and the Gram rows (that
+// mode takes no Gram: every block runs the clipped sweeps).
+constexpr uint32_t RV_BYTES = J * KD * 4;
+__device__ __forceinline__ uint32_t rv_off(int slot) { return slot < 2 ? OFF_SHL + slot * SHL_SLOT : OFF_MT; }
+static_assert(SHL_SLOT >= RV_BYTES && 2 * MT_BYTES >= RV_BYTES && OFF_MT % 16 == 0, "gate slots");
 static_assert(3 * KT_BYTES <= OFF_SHL, "key tiles");
 static_assert(OFF_SHL % 1024 == 0, "swizzle atoms");
 static_assert(SMEM_ALLOC <= 232448, "shared memory");
@@ -198,7 +206,10 @@ __device__ __forceinline__ void rs_level(float (&v)[64], int lane) {
 // (ws_g, ws_d) the step sizes and start state of every block are stored there as soon as the
 // block is solved, each word with one relaxed GPU-scope store and never with the all-ones bit
 // pattern, so a consumer running concurrently may poll for them.
-template <typename TIn, typename TOut, bool HAS_R>
+// RM: 0 no retention, 1 one gate per token and head (Eq. (7)), 2 one gate per key coordinate
+// (diag(r_t), Appendix A.5; no Gram: each block runs the clipped sweeps, whose trajectories take
+// a gate per coordinate as they are, with the coupling bound from |gamma_j b_j| <s_j, sum_l s_l>).
+template <typename TIn, typename TOut, int RM>
 __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws_g, float* ws_d, int bh,
                                                 unsigned char* smem_raw, uint32_t tbase,
                                                 unsigned int* timeout_flag) {
@@ -209,6 +220,8 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
     const int tid = threadIdx.x, warp = tid >> 5;
     const int b = bh / a.H, h = bh % a.H;
     const int T = a.T, H = a.H;
+    constexpr bool HAS_R = RM == 1;  // per-token gates in F_RR
+    constexpr bool VEC = RM == 2;    // per-coordinate gates in the slots at rv_off
     const TIn* kg = static_cast<const TIn*>(a.k);
     TOut* ktg = static_cast<TOut*>(a.k_tilde);
     const size_t row0 = static_cast<size_t>(b) * T * H + h;
@@ -217,7 +230,11 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
     const uint32_t bars = sbase + OFF_BAR;
     const float eta = a.eta, dmin = a.d_min, dmax = a.d_max, eps = a.eps;
     __shared__ int s_abort;
-    __shared__ int s_grams_issued, s_grams_used;  // all-free Grams issued by warpgroup 1 / consumed
+    // The Gram of a block is formed only when the chain used one in its latest finished block
+    // (s_gram_want: every block of a head tends to take the same path).  Per slot: whether this
+    // block's Gram is formed (s_gon), the parity of its barrier phase (s_gpar) and the number of
+    // Grams issued on the slot's barrier so far (s_gcnt).
+    __shared__ int s_gram_want, s_gram_used, s_gon[2], s_gpar[2], s_gcnt[2];
 
     if (tid == 0) {
         for (int q = 0; q < 2; ++q) {
@@ -229,8 +246,8 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
         tc::mbar_init(bars + B_MRDY + 8, 4);
         tc::mbar_init_fence();
         s_abort = 0;
-        s_grams_issued = 0;
-        s_grams_used = 0;
+        s_gram_want = 1;
+        s_gcnt[0] = s_gcnt[1] = 0;
     }
     scan_sync();
     const uint32_t id_hl = tc::idesc_f16_f32(J, 2 * J, false, false);  // M = 64, N = 128
@@ -291,6 +308,16 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     cp_async_4z(F + F_RAWB + (m % 3) * J + u, a.beta + row, valid);
                     if (HAS_R) cp_async_4z(F + F_RAWR + (m % 3) * J + u, a.r + row, valid);
                 }
+                if (VEC) {  // the block's gates, row j = token (zeros past the end: never read)
+                    float* dst = reinterpret_cast<float*>(sm + rv_off(m % 3));
+#pragma unroll
+                    for (int e = 0; e < (J * KD * 4 / 16) / 128; ++e) {
+                        const int piece = e * 128 + u, j = piece >> 5, c = piece & 31;
+                        const bool valid = t0 + j < T;
+                        const size_t row = row0 + static_cast<size_t>(valid ? t0 + j : 0) * H;
+                        cp_async_16z(dst + j * KD + c * 4, a.r + row * KD + c * 4, valid);
+                    }
+                }
             }
             cp_async_commit();
         };
@@ -324,10 +351,58 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 const float bt = F[F_RAWB + (m % 3) * J + j];
                 const float bp = a.beta_aware ? bt : 1.f;
                 F[F_GAM + q * J + j] = valid ? eta * bp / fmaxf(n, eps) : 0.f;
-                F[F_NRM + q * J + j] = n;
-                F[F_SMX + q * J + j] = rowmx;
+                if (!VEC) {
+                    F[F_NRM + q * J + j] = n;
+                    F[F_SMX + q * J + j] = rowmx;
+                }
                 F[F_BP + q * J + j] = bp;
                 F[F_RR + q * J + j] = (HAS_R && valid) ? F[F_RAWR + (m % 3) * J + j] : 1.f;
+            }
+            if constexpr (VEC) {
+                // the fp32 s rows for the chain, then the coupling bound of the block
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float4* dst = reinterpret_cast<float4*>(sf + j * SROW + hf * 64 + c * 8);
+                    dst[0] = make_float4(sv[c * 8], sv[c * 8 + 1], sv[c * 8 + 2], sv[c * 8 + 3]);
+                    dst[1] = make_float4(sv[c * 8 + 4], sv[c * 8 + 5], sv[c * 8 + 6], sv[c * 8 + 7]);
+                }
+                __syncwarp();
+                if ((u & 31) == 0) mbar_arrive(bars + B_PREP + 8 * (m & 1));
+                wg_sync(2);
+                // coordinate u: sum of s over the block's tokens, and whether a gate exceeds 1
+                const float* rv = reinterpret_cast<const float*>(sm + rv_off(m % 3));
+                const int jb = min(J, T - m * J);
+                float cs = 0.f;
+                bool rbad = false;
+#pragma unroll 8
+                for (int l = 0; l < J; ++l) {
+                    cs += sf[l * SROW + u];
+                    if (l < jb) rbad |= !(rv[l * KD + u] <= 1.f);
+                }
+                float* colsum = F + F_NRM;  // (the per-block norms of the Gram path: unused here)
+                colsum[u] = cs;
+                wg_sync(2);
+                // sum_{l<j} M_jl <= <s_j, sum_l s_l> (s >= 0): the sweeps' contraction bound
+                float dot = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) dot = fmaf(sv[c], colsum[hf * 64 + c], dot);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                const int q = m & 1;
+                float tb = fabsf(F[F_GAM + q * J + j] * F[F_BP + q * J + j]) * dot;
+                if (!(tb <= 3.0e38f)) tb = INFINITY;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, o));
+                const bool bad = __any_sync(0xffffffffu, rbad);
+                if ((u & 31) == 0) F[F_NU + 4 * q + (u >> 5)] = bad ? INFINITY : tb;
+                __syncwarp();
+                if ((u & 31) == 0) mbar_arrive(bars + B_MRDY + 8 * q);
+                return;
+            }
+            if (u == 0) {  // form this block's Gram? (a hint from the chain; the decision is uniform)
+                const int q = m & 1;
+                s_gon[q] = *static_cast<volatile int*>(&s_gram_want);
+                s_gpar[q] = s_gcnt[q] & 1;
             }
             wg_sync(2);
             const float bmax = fmaxf(fmaxf(F[F_RED1], F[F_RED1 + 1]), fmaxf(F[F_RED1 + 2], F[F_RED1 + 3]));
@@ -335,32 +410,37 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             if (bmax > 0.f) frexpf(bmax, &ex);
             const float sig = bmax > 0.f ? ldexpf(1.f, 14 - ex) : 1.f;  // max s * sig < 2^14
             if (u == 0) F[F_SIGS + (m & 1)] = sig;
-            unsigned char* sh = sm + OFF_SHL + (m & 1) * SHL_SLOT + hf * SHL_KB;
-            unsigned char* sl = sh + SHL_LO;
+            if (s_gon[m & 1]) {
+                unsigned char* sh = sm + OFF_SHL + (m & 1) * SHL_SLOT + hf * SHL_KB;
+                unsigned char* sl = sh + SHL_LO;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float hi[8], lo[8];
+                for (int c = 0; c < 8; ++c) {
+                    float hi[8], lo[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x = sv[c * 8 + e] * sig;
-                    hi[e] = __half2float(__float2half_rn(x));
-                    lo[e] = x - hi[e];
+                    for (int e = 0; e < 8; ++e) {
+                        const float x = sv[c * 8 + e] * sig;
+                        hi[e] = __half2float(__float2half_rn(x));
+                        lo[e] = x - hi[e];
+                    }
+                    *reinterpret_cast<uint4*>(sh + tc::sw128_off(j, c)) =
+                        make_uint4(pack_h2(hi[0], hi[1]), pack_h2(hi[2], hi[3]), pack_h2(hi[4], hi[5]), pack_h2(hi[6], hi[7]));
+                    *reinterpret_cast<uint4*>(sl + tc::sw128_off(j, c)) =
+                        make_uint4(pack_h2(lo[0], lo[1]), pack_h2(lo[2], lo[3]), pack_h2(lo[4], lo[5]), pack_h2(lo[6], lo[7]));
                 }
-                *reinterpret_cast<uint4*>(sh + tc::sw128_off(j, c)) =
-                    make_uint4(pack_h2(hi[0], hi[1]), pack_h2(hi[2], hi[3]), pack_h2(hi[4], hi[5]), pack_h2(hi[6], hi[7]));
-                *reinterpret_cast<uint4*>(sl + tc::sw128_off(j, c)) =
-                    make_uint4(pack_h2(lo[0], lo[1]), pack_h2(lo[2], lo[3]), pack_h2(lo[4], lo[5]), pack_h2(lo[6], lo[7]));
+                tc::fence_proxy_async();
+                wg_sync(2);
+                // The Gram goes first (its rows are what the chain waits for longest), issued from
+                // warp 6.  (copy_gram waits for every formed Gram before the slot's next one, so no
+                // wait on the barrier can mistake one phase for another.)
+                if (u == 2 * 32) {
+                    const int q = m & 1;
+                    issue_gram(q, COL_G + q * 128, bars + B_GRAM + 8 * q);
+                    s_gcnt[q] = s_gcnt[q] + 1;
+                }
+                __syncwarp();
             }
-            tc::fence_proxy_async();
-            wg_sync(2);
-            // The Gram goes first (its rows are what the chain waits for longest), issued from
-            // warp 6; then the fp32 s tile for the chain, each warp releasing the block once its
-            // rows are stored.
-            if (u == 2 * 32) {
-                issue_gram(m & 1, COL_G + (m & 1) * 128, bars + B_GRAM + 8 * (m & 1));
-                s_grams_issued = m + 1;
-            }
-            __syncwarp();
+            // then the fp32 s tile for the chain, each warp releasing the block once its rows are
+            // stored
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 float4* dst = reinterpret_cast<float4*>(sf + j * SROW + hf * 64 + c * 8);
@@ -371,25 +451,27 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             if ((u & 31) == 0) mbar_arrive(bars + B_PREP + 8 * (m & 1));
         };
 
-        // Gram of block m, tensor memory -> shared memory slot m & 1 (warps 4-5, one row per
-        // thread), scaled back by 1 / sig^2 (exact: powers of two) and masked to l < j, with the
-        // coupling bound of the block's system for the chain's sweep count
+        // Gram of block m (when formed), tensor memory -> shared memory slot m & 1 as the chain's
+        // Jacobi rows (one row per thread of lanes 0-15 of each warp), scaled back by 1 / sig^2
+        // (exact: powers of two) and masked to l < j, with the coupling bound nu of the block's
+        // system for the chain's sweep count.  B_GRAM and B_MRDY of a slot complete one phase per
+        // formed Gram, so both waits take the parity warpgroup 1 recorded for the block.
         auto copy_gram = [&](int m) {
-            const bool okg = tc::mbar_wait(bars + B_GRAM + 8 * (m & 1), (m >> 1) & 1, kMaxPolls);
+            const int q = m & 1;
+            const bool okg = tc::mbar_wait(bars + B_GRAM + 8 * q, static_cast<uint32_t>(s_gpar[q]), kMaxPolls);
             if (!__all_sync(0xffffffffu, okg)) {
                 atomicExch(&s_abort, 1);
                 return;
             }
-            if (u == 0) s_grams_used = m + 1;
             tc::tc_fence_after();
             const int lane = u & 31, j = ((u >> 5) << 4) | (lane & 15);
-            const float isg = 1.f / F[F_SIGS + (m & 1)];
+            const float isg = 1.f / F[F_SIGS + q];
             float g[64];
-            load_gram_row(COL_G + (m & 1) * 128, static_cast<uint32_t>((warp & 3) * 32) << 16, j, isg * isg, g);
+            load_gram_row(COL_G + q * 128, static_cast<uint32_t>((warp & 3) * 32) << 16, j, isg * isg, g);
             tc::tc_fence_before();
-            float t = 0.f;
+            float tb = 0.f;
             if (lane < 16) {
-                float* row = reinterpret_cast<float*>(sm + OFF_MT + (m & 1) * MT_BYTES) + j * MROW;
+                float* row = reinterpret_cast<float*>(sm + OFF_MT + q * MT_BYTES) + j * MROW;
 #pragma unroll
                 for (int l = 0; l < 64; l += 4) *reinterpret_cast<float4*>(row + l) = make_float4(g[l], g[l + 1], g[l + 2], g[l + 3]);
                 // max_j |gamma_j b_j| sum_l M_jl (M >= 0); infinite when it is not finite or a
@@ -397,14 +479,14 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int l = 0; l < 64; ++l) r4[l & 3] += g[l];
-                t = fabsf(F[F_GAM + (m & 1) * J + j] * F[F_BP + (m & 1) * J + j]) * ((r4[0] + r4[1]) + (r4[2] + r4[3]));
-                if (!(t <= 3.0e38f) || (HAS_R && F[F_RR + (m & 1) * J + j] > 1.f)) t = INFINITY;
+                tb = fabsf(F[F_GAM + q * J + j] * F[F_BP + q * J + j]) * ((r4[0] + r4[1]) + (r4[2] + r4[3]));
+                if (!(tb <= 3.0e38f) || (HAS_R && F[F_RR + q * J + j] > 1.f)) tb = INFINITY;
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
-            if (lane == 0) F[F_NU + 4 * (m & 1) + (u >> 5)] = t;
+            for (int o = 16; o > 0; o >>= 1) tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, o));
+            if (lane == 0) F[F_NU + 4 * q + (u >> 5)] = tb;
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars + B_MRDY + 8 * (m & 1));
+            if (lane == 0) mbar_arrive(bars + B_MRDY + 8 * q);
         };
         // step sizes and start state of block m to the workspace (warps 6-7).  A reader in
         // another CTA polls each word until it differs from the all-ones pattern the workspace
@@ -432,14 +514,14 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             cp_async_wait<2>();
             wg_sync(2);
             prepare(0);
-            copy_gram(0);
+            if (!VEC && s_gon[0]) copy_gram(0);
         }
         for (int m = 0; m < nblk; ++m) {
             if (m + 1 < nblk) {
                 cp_async_wait<1>();  // groups 0..m+2 committed; block m+1's has landed
                 wg_sync(2);
                 prepare(m + 1);  // slot (m + 1) & 1: the chain finished block m - 1 with it
-                copy_gram(m + 1);
+                if (!VEC && s_gon[(m + 1) & 1]) copy_gram(m + 1);
             }
             // block m once the chain has fixed its g values
             const bool ok = tc::mbar_wait(bars + B_CHAIN + 8 * (m & 1), (m >> 1) & 1, kMaxPolls);
@@ -456,11 +538,13 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 float d = F[F_DST + q * KD + u] + F[F_DSL + q * KD + u];
                 TOut* out = ktg + (row0 + static_cast<size_t>(t0) * H) * KD + u;
                 const size_t stride = static_cast<size_t>(H) * KD;
+                const float* rv = reinterpret_cast<const float*>(sm + rv_off(m % 3));
 #pragma unroll 4
                 for (int j = 0; j < jb; ++j) {
                     const float kj = ld_key<TIn>(kt, j, u);
                     out[j * stride] = from_f32<TOut>(d * kj);
-                    d = replay_step(d, F[F_RR + q * J + j], replay_inc(F[F_GOUT + q * J + j], kj), dmin, dmax);
+                    const float rj = VEC ? rv[j * KD + u] : F[F_RR + q * J + j];
+                    d = replay_step(d, rj, replay_inc(F[F_GOUT + q * J + j], kj), dmin, dmax);
                 }
             }
             wg_sync(2);
@@ -493,14 +577,34 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             F[F_DSL + q * KD + i] = d_lo;
 
             int p = 0;
-            bool abort_now = false, gram_rows_ready = false, clipped = false;
-            // the all-free Gram rows and the coupling bound nu of this block (copied by warpgroup 1)
+            // vector gates: every block by the clipped sweeps (p = 0)
+            bool abort_now = false, gram_rows_ready = false, clipped = VEC;
+            bool have_rows = false;  // this block's Gram rows
+            if (tid == 0) s_gram_used = 0;
+            // vector gates of the block (tokens past the end keep d: gate 1)
+            auto rvec = [&](int j) -> float {
+                return j < min(J, T - blk * J) ? reinterpret_cast<const float*>(sm + rv_off(blk % 3))[j * KD + i] : 1.f;
+            };
+            // The all-free Gram row jr of this block (lanes 0-15 of each chain warp: an M = 64
+            // product puts row 16 w + l in lane l of quadrant w, the lanes of this warp), read from
+            // tensor memory, scaled back by 1 / sig^2 (exact: powers of two) and masked to l < jr;
+            // and the coupling bound nu = max_j |gamma_j b_j| sum_l M_jl (infinite when it is not
+            // finite or a retention gate exceeds 1) for the sweep count.  With one gate per
+            // coordinate warpgroup 1 forms nu (no Gram).
+            // false: a wait gave up.  Otherwise have_rows says whether the Gram rows (in shared
+            // memory slot q) and the bound nu are there: warpgroup 1 skips a block's Gram when the
+            // chain did not use the last one, and the block then runs the clipped sweeps until no
+            // step size moves, which needs no bound.
             auto gram_ready = [&]() -> bool {
+                if (tid == 0) s_gram_used = 1;
                 if (gram_rows_ready) return true;
-                const bool okr = tc::mbar_wait(bars + B_MRDY + 8 * q, ph, kMaxPolls);
-                if (wg_count(1, okr && !*static_cast<volatile int*>(&s_abort)) != 128) return false;
+                if (VEC || s_gon[q] != 0) {
+                    const uint32_t par = VEC ? ph : static_cast<uint32_t>(s_gpar[q]);
+                    const bool okr = tc::mbar_wait(bars + B_MRDY + 8 * q, par, kMaxPolls);
+                    if (wg_count(1, okr && !*static_cast<volatile int*>(&s_abort)) != 128) return false;
+                    have_rows = true;
+                }
                 gram_rows_ready = true;
-                tc::tc_fence_after();
                 return true;
             };
             // Sweeps needed by the bound nu: each Jacobi sweep shrinks the error by nu (the largest
@@ -525,11 +629,11 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         abort_now = true;
                         break;
                     }
-                    const int K = sweeps_for_nu();
-                    const int nsw = K >= 0 ? min(K + 1, J - p) : J - p;
                     float* red = F + F_DF;  // [4][64] per-warp partial sums (F_DF, F_BPV: free here)
                     const int lane = tid & 31;
                     wg_sync(1);
+                    const int K = have_rows ? sweeps_for_nu() : -1;
+                    const int nsw = K >= 0 ? min(K + 1, J - p) : J - p;
                     if (tid < J) F[F_G + tid] = 0.f;  // tokens before p then leave d unchanged
                     wg_sync(1);
                     for (int it = 0; it < nsw; ++it) {
@@ -552,7 +656,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                                 const int j = j4 + e;
                                 const float sj = s_at(j, i);
                                 v[j] = x * sj;
-                                const float rj = j >= p ? r4[e] : 1.f;
+                                const float rj = VEC ? rvec(j) : (j >= p ? r4[e] : 1.f);
                                 x = fminf(fmaxf(fmaf(rj, x, gg[e] * sj), dmin), dmax);
                             }
                         }
@@ -575,15 +679,29 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         else if (wg_count(1, changed) == 0) break;
                     }
                     if (tid >= p && tid < J) gout[tid] = F[F_G + tid];
-                    // the block end with the final g's, carried as a (hi, lo) pair
-                    for (int j = p; j < J; ++j) {
-                        const float sj = s_at(j, i), g = F[F_G + j], r = HAS_R ? rr[j] : 1.f;
-                        float p1 = r * d_hi, ep = fmaf(r, d_hi, -p1), q1 = g * sj, s1, e1;
-                        two_sum(p1, q1, s1, e1);
-                        const float l1 = fmaf(r, d_lo, ep + e1);
-                        d_hi = s1 + l1;
-                        d_lo = l1 - (d_hi - s1);
-                        pair_clip(d_hi, d_lo, dmin, dmax);
+                    // the block end with the final g's, carried as a (hi, lo) pair: hi takes one
+                    // product and one sum per token, their rounding errors go to lo (off hi's
+                    // dependency chain), the clip acts on hi + lo, and the pair is renormalised once
+                    // (lo gathers at most ~64 ulps of d over the block).  Tokens before p leave it as
+                    // it is (gate 1, step 0).
+                    {
+                        float hi = d_hi, lo = d_lo;
+#pragma unroll 8
+                        for (int j = 0; j < J; ++j) {
+                            const bool act = j >= p;
+                            const float sj = s_at(j, i), g = act ? F[F_G + j] : 0.f;
+                            const float r = act ? (VEC ? rvec(j) : (HAS_R ? rr[j] : 1.f)) : 1.f;
+                            const float p1 = r * hi, ep = fmaf(r, hi, -p1), q1 = g * sj;
+                            float s1, e1;
+                            two_sum(p1, q1, s1, e1);
+                            lo = fmaf(r, lo, ep + e1);
+                            hi = s1;
+                            const float v = hi + lo;
+                            if (v < dmin) { hi = dmin; lo = 0.f; }
+                            if (v > dmax) { hi = dmax; lo = 0.f; }
+                        }
+                        d_hi = hi + lo;
+                        d_lo = lo - (d_hi - hi);
                     }
                     p = J;
                     wg_sync(1);
@@ -715,6 +833,10 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                             abort_now = true;
                             break;
                         }
+                        if (!have_rows) {  // no Gram formed for this block
+                            clipped = true;
+                            continue;
+                        }
                         if (row_thread) {
                             const float* mrow = reinterpret_cast<const float*>(sm + OFF_MT + q * MT_BYTES) + jr * MROW;
 #pragma unroll
@@ -742,8 +864,8 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     }
                     if (nfree == KD) {
                         // from the estimate above (within nu |g|; the rho ratios are <= 1)
-                        const int K = sweeps_for_nu();
                         wg_sync(1);
+                        const int K = sweeps_for_nu();
                         for (int it = 0; K < 0 ? it < J : it < K; ++it) {
                             const float* hc = F + F_H + hb * J;  // h of the previous sweep
                             bool changed = false;
@@ -877,6 +999,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                 atomicExch(&s_abort, 1);
                 break;
             }
+            if (tid == 0) *static_cast<volatile int*>(&s_gram_want) = s_gram_used;
             mbar_arrive(bars + B_CHAIN + 8 * q);
         }
         a.d_out[static_cast<size_t>(bh) * KD + i] = d_hi + d_lo;
@@ -885,9 +1008,10 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
     scan_sync();
     if (tid == 0 && s_abort) {
         atomicExch(timeout_flag, 1u);
-        // drain all-free Grams the chain never consumed before tensor memory is released
-        for (int m = s_grams_used; m < s_grams_issued; ++m)
-            tc::mbar_wait(bars + B_GRAM + 8 * (m & 1), (m >> 1) & 1, kMaxPolls >> 4);
+        // let the last Gram of each slot land before tensor memory is released (each earlier one
+        // was waited for before its barrier was reused)
+        for (int q = 0; q < 2; ++q)
+            if (s_gcnt[q] > 0) tc::mbar_wait(bars + B_GRAM + 8 * q, (s_gcnt[q] - 1) & 1, kMaxPolls >> 4);
     }
     tc::tc_fence_before();
     scan_sync();

@@ -129,3 +129,26 @@ def test_scan_parallel_emission_matches_in_kernel_emission(name, T, eta, kt_dtyp
                                         d_min=w.d_min, d_max=w.d_max, eps=w.eps,
                                         beta_aware=w.beta_aware)
     assert_rel(d1, d_ref, 1e-5, what="d")
+
+
+@pytest.mark.parametrize("eta", [0.3, 1.0])
+def test_scan_blocks_alternating_pinned_and_free(eta):
+    """Head gates of 0.3 and 1 in turns of two blocks: d collapses onto d_min (every coordinate
+    pinned: the block needs no Gram, so none is formed for the next one) and then leaves it (every
+    coordinate free: the Gram the block needs was skipped, and it runs the clipped sweeps until no
+    step size moves).  Both ways, and the emission from the workspace, against the oracle."""
+    w = W.WORKLOADS["layer_1p3b_apf"]
+    B, H, T = 1, 2, 1024
+    inp = W.make_prefill(w, B=B, H=H, T=T, seed=46)
+    t = np.arange(T)
+    r = torch.from_numpy(np.where((t // 128) % 2 == 0, 0.3, 1.0)[None, :, None].repeat(H, 2)).float().contiguous()
+    dev = to_dev(inp)
+    kw = dict(kt_dtype=torch.float32, eta=eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+    kt0, d0 = osdn_precond_scan(dev["k"], dev["beta"], r.cuda(), None, workspace=False, **kw)
+    kt1, d1 = osdn_precond_scan(dev["k"], dev["beta"], r.cuda(), None, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(kt0, kt1) and torch.equal(d0, d1)
+    kt_ref, d_ref = oracle.precond_scan(inp["k"], inp["beta"], r, None, eta=eta, d_min=w.d_min, d_max=w.d_max,
+                                        eps=w.eps)
+    assert_rel(kt0, kt_ref, 1e-5, what="k_tilde")
+    assert_rel(d0, d_ref, 1e-5, what="d")

@@ -2,14 +2,15 @@
 r_{t,h} I: "OSDN: Improving Delta Rule with Provable Online Preconditioning in Linear Attention",
 Appendix A.5, Prop. A.3) against the fp64 oracle: the phase-1 scan, the layer call and the decode
 step.  Bars as for the per-head gate: k~ and d within 1e-5 relative; o and S max-abs 2e-2 (bf16)
-or 1e-4 (fp32).  A vector of equal gates must give exactly what the per-head gate gives on the
-same (token-by-token) kernel."""
+or 1e-4 (fp32).  16-bit keys with K = 128 take the blocked scan (every block by Jacobi sweeps on
+the clipped recurrence, one gate per coordinate); fp32 keys and K = 64 take the token-by-token
+kernel, where a vector of equal gates must give exactly what the per-head gate gives."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from preconditioned_delta_rule_gb300 import osdn_decode_step, osdn_layer_fwd, osdn_precond_scan
+from preconditioned_delta_rule_gb300 import binding, osdn_decode_step, osdn_layer_fwd, osdn_precond_scan
 from preconditioned_delta_rule_gb300 import workloads as W
 from tests._parity import assert_maxabs, assert_rel, np64, to_dev
 
@@ -54,11 +55,83 @@ def test_equal_vector_gates_match_the_head_gate():
     dev = to_dev(inp)
     r_vec = dev["r"][..., None].expand(*dev["r"].shape, 128).contiguous()
     kw = dict(kt_dtype=torch.float32, eta=0.3, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
-    kt1, d1 = osdn_precond_scan(dev["k"], dev["beta"], r_vec, None, **kw)
-    # the per-head gate on the same token-by-token kernel: fp32 keys take it for every gate layout
-    kt2, d2 = osdn_precond_scan(dev["k"].float(), dev["beta"], dev["r"], None, **kw)
+    # fp32 keys: the token-by-token kernel for both gate layouts, the same arithmetic
+    kf = dev["k"].float()
+    kt1, d1 = osdn_precond_scan(kf, dev["beta"], r_vec, None, **kw)
+    kt2, d2 = osdn_precond_scan(kf, dev["beta"], dev["r"], None, **kw)
+    # 16-bit keys: the blocked scan, clipped sweeps for the vector against the Gram solve for the
+    # head gate (the same recurrence, reassociated)
+    kt3, d3 = osdn_precond_scan(dev["k"], dev["beta"], r_vec, None, **kw)
+    kt4, d4 = osdn_precond_scan(dev["k"], dev["beta"], dev["r"], None, **kw)
     torch.cuda.synchronize()
     assert torch.equal(kt1, kt2) and torch.equal(d1, d2)
+    assert_rel(kt3, np64(kt4), 1e-5, what="k_tilde, vector vs head gate")
+    assert_rel(d3, np64(d4), 1e-5, what="d, vector vs head gate")
+    kt_ref, d_ref = oracle.precond_scan(inp["k"], inp["beta"], inp["r"], None, eta=0.3, d_min=w.d_min,
+                                        d_max=w.d_max, eps=w.eps)
+    assert_rel(kt3, kt_ref, 1e-5, what="k_tilde")
+    assert_rel(d3, d_ref, 1e-5, what="d")
+
+
+def test_scan_vector_retention_full_size():
+    """The bench's vector-retention workload (1.3B-shaped, B4 H16 T4096, bf16 keys, gates
+    sigmoid(4 + N(0, 1)) per coordinate) with a start state, on the blocked scan."""
+    w = W.WORKLOADS["layer_1p3b_apf"]
+    inp = W.make_prefill(w)
+    B, T, H, K = inp["k"].shape
+    r = torch.sigmoid(4.0 + torch.randn(B, T, H, K, generator=torch.Generator().manual_seed(4)))
+    d0 = torch.rand(B, H, K, generator=torch.Generator().manual_seed(5)) * 1.5 + 0.5
+    dev = to_dev(inp)
+    kw = dict(eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+    kt, d = osdn_precond_scan(dev["k"], dev["beta"], r.cuda(), d0.cuda(), kt_dtype=torch.float32, **kw)
+    torch.cuda.synchronize()
+    kt_ref, d_ref = oracle.precond_scan(inp["k"], inp["beta"], r, d0, **kw)
+    assert_rel(kt, kt_ref, 1e-5, what="k_tilde")
+    assert_rel(d, d_ref, 1e-5, what="d")
+
+
+@pytest.mark.parametrize("kt_dtype", [torch.bfloat16, torch.float32])
+def test_vector_retention_parallel_emission_matches_in_kernel_emission(kt_dtype):
+    """With a workspace the write keys come from the parallel emission kernel (each thread reads
+    its coordinate's gates); without one the scan writes them: the same replay, bit-identical."""
+    w = W.WORKLOADS["layer_1p3b_apf"]
+    B, H, T = 2, 4, 1000  # ragged last block
+    inp = W.make_prefill(w, B=B, H=H, T=T, seed=44)
+    r = vector_gates((B, T, H, 128), 9, mean=4.0).cuda()
+    dev = to_dev(inp)
+    kw = dict(kt_dtype=kt_dtype, eta=w.eta, d_min=w.d_min, d_max=w.d_max, eps=w.eps)
+    kt0, d0 = osdn_precond_scan(dev["k"], dev["beta"], r, None, workspace=False, **kw)
+    need = binding.osdn_precond_scan_workspace_bytes(B, T, H, 128, dev["k"].dtype)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    kt1, d1 = osdn_precond_scan(dev["k"], dev["beta"], r, None, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(kt0, kt1) and torch.equal(d0, d1)
+    kt_ref, d_ref = oracle.precond_scan(inp["k"], inp["beta"], r.cpu(), None, eta=w.eta, d_min=w.d_min,
+                                        d_max=w.d_max, eps=w.eps)
+    ulp = 2.0 ** -8 if kt_dtype == torch.bfloat16 else 0.0
+    assert_rel(kt0, kt_ref, 1e-5 + ulp, what="k_tilde")
+    assert_rel(d0, d_ref, 1e-5, what="d")
+
+
+def test_vector_gates_above_one_and_clipping():
+    """Gates in [0.95, 1.05] (the sweeps' contraction bound no longer holds: they run until no step
+    size moves) and a narrow box: about 4 % of the coordinates end on each face."""
+    w = W.WORKLOADS["layer_1p3b_apf"]
+    B, H, T = 1, 4, 640
+    inp = W.make_prefill(w, B=B, H=H, T=T, seed=45)
+    g = torch.Generator().manual_seed(10)
+    r = 0.95 + 0.1 * torch.rand(B, T, H, 128, generator=g)
+    box = dict(d_min=0.8, d_max=1.25)
+    dev = to_dev(inp)
+    kt, d = osdn_precond_scan(dev["k"], dev["beta"], r.cuda(), None, kt_dtype=torch.float32, eta=0.3,
+                              eps=w.eps, **box)
+    torch.cuda.synchronize()
+    kt_ref, d_ref = oracle.precond_scan(inp["k"], inp["beta"], r, None, eta=0.3, eps=w.eps, **box)
+    assert_rel(kt, kt_ref, 1e-5, what="k_tilde")
+    assert_rel(d, d_ref, 1e-5, what="d")
+    dd = np64(d)
+    lo, hi = float(np.float32(0.8)), float(np.float32(1.25))  # the box as the fp32 state holds it
+    assert np.any(dd == lo) and np.any(dd == hi) and np.any((dd > lo) & (dd < hi))
 
 
 def test_layer_vector_retention_against_oracle():
