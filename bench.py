@@ -706,7 +706,8 @@ def run_backward(args, dev, stream, hbm_peak):
 
 def run_vector_retention(args, dev, stream, hbm_peak):
     """Phase 1 with one APF gate per key coordinate (diag(r_t), the pages' Appendix A.5) on the
-    1.3B-shaped workload (B=4, H=16, T=4096, bf16 keys): the token-by-token scan kernel, gates
+    1.3B-shaped workload (B=4, H=16, T=4096, bf16 keys): the blocked scan with a gate per key
+    coordinate (every block by clipped sweeps) and the parallel emission kernel, gates
     sigmoid(4 + N(0, 1)) in fp32 resident in HBM, L2 flushed between reps.  The per-head gate's
     blocked scan on the same inputs is timed beside it."""
     from preconditioned_delta_rule_gb300 import binding
@@ -745,7 +746,7 @@ def run_vector_retention(args, dev, stream, hbm_peak):
             "value": th / secs_v / w.H, "unit": "tokens/s", "ms": secs_v * 1e3,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
                          "frac": ach / hbm_peak, "algorithmic_bytes_per_launch": b},
-            "per_head_gate_ms": secs_h * 1e3, "kernel": "scan_warp_kernel (token by token)",
+            "per_head_gate_ms": secs_h * 1e3, "kernel": "scan_block_kernel (clipped sweeps, one gate per coordinate) + scan_emit_kernel",
             "l2": "flushed between reps (256 MiB write outside the timed events)"}
 
 
