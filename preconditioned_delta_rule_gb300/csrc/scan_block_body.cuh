@@ -413,13 +413,17 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             if (s_gon[m & 1]) {
                 unsigned char* sh = sm + OFF_SHL + (m & 1) * SHL_SLOT + hf * SHL_KB;
                 unsigned char* sl = sh + SHL_LO;
+                // hi: x rounded to 11 significant bits in fp32 (add half a unit of bit 13, clear the
+                // 13 low bits; a carry moves into the exponent as it should), which fp16 holds exactly
+                // in its normal range (x < 2^14 here); lo = x - hi is exact, |lo| <= 2^-11 |x|.  Two
+                // packing conversions a pair instead of a round trip through fp16 per value.
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float hi[8], lo[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float x = sv[c * 8 + e] * sig;
-                        hi[e] = __half2float(__float2half_rn(x));
+                        hi[e] = __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
                         lo[e] = x - hi[e];
                     }
                     *reinterpret_cast<uint4*>(sh + tc::sw128_off(j, c)) =
