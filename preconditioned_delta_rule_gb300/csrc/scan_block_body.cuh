@@ -230,8 +230,10 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
     const uint32_t bars = sbase + OFF_BAR;
     const float eta = a.eta, dmin = a.d_min, dmax = a.d_max, eps = a.eps;
     __shared__ int s_abort;
-    // The Gram of a block is formed only when the chain used one in its latest finished block
-    // (s_gram_want: every block of a head tends to take the same path).  Per slot: whether this
+    // With per-head retention gates the Gram of a block is formed only when the chain used one in
+    // its latest finished block (s_gram_want: every block of a head tends to take the same path;
+    // APF gates hold d on d_min, and a block with every coordinate there needs no Gram).  Without
+    // gates whole pinned blocks are rare and every block forms its Gram.  Per slot: whether this
     // block's Gram is formed (s_gon), the parity of its barrier phase (s_gpar) and the number of
     // Grams issued on the slot's barrier so far (s_gcnt).
     __shared__ int s_gram_want, s_gram_used, s_gon[2], s_gpar[2], s_gcnt[2];
@@ -401,7 +403,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             }
             if (u == 0) {  // form this block's Gram? (a hint from the chain; the decision is uniform)
                 const int q = m & 1;
-                s_gon[q] = *static_cast<volatile int*>(&s_gram_want);
+                s_gon[q] = HAS_R ? *static_cast<volatile int*>(&s_gram_want) : 1;
                 s_gpar[q] = s_gcnt[q] & 1;
             }
             wg_sync(2);
@@ -410,7 +412,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             if (bmax > 0.f) frexpf(bmax, &ex);
             const float sig = bmax > 0.f ? ldexpf(1.f, 14 - ex) : 1.f;  // max s * sig < 2^14
             if (u == 0) F[F_SIGS + (m & 1)] = sig;
-            if (s_gon[m & 1]) {
+            if (!HAS_R || s_gon[m & 1]) {
                 unsigned char* sh = sm + OFF_SHL + (m & 1) * SHL_SLOT + hf * SHL_KB;
                 unsigned char* sl = sh + SHL_LO;
                 // hi: x rounded to 11 significant bits in fp32 (add half a unit of bit 13, clear the
@@ -518,14 +520,14 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             cp_async_wait<2>();
             wg_sync(2);
             prepare(0);
-            if (!VEC && s_gon[0]) copy_gram(0);
+            if (!VEC && (!HAS_R || s_gon[0])) copy_gram(0);
         }
         for (int m = 0; m < nblk; ++m) {
             if (m + 1 < nblk) {
                 cp_async_wait<1>();  // groups 0..m+2 committed; block m+1's has landed
                 wg_sync(2);
                 prepare(m + 1);  // slot (m + 1) & 1: the chain finished block m - 1 with it
-                if (!VEC && s_gon[(m + 1) & 1]) copy_gram(m + 1);
+                if (!VEC && (!HAS_R || s_gon[(m + 1) & 1])) copy_gram(m + 1);
             }
             // block m once the chain has fixed its g values
             const bool ok = tc::mbar_wait(bars + B_CHAIN + 8 * (m & 1), (m >> 1) & 1, kMaxPolls);
@@ -596,13 +598,14 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             // finite or a retention gate exceeds 1) for the sweep count.  With one gate per
             // coordinate warpgroup 1 forms nu (no Gram).
             // false: a wait gave up.  Otherwise have_rows says whether the Gram rows (in shared
-            // memory slot q) and the bound nu are there: warpgroup 1 skips a block's Gram when the
-            // chain did not use the last one, and the block then runs the clipped sweeps until no
-            // step size moves, which needs no bound.
+            // memory slot q) and the bound nu are there (warpgroup 1 writes both before the row
+            // barrier): with per-head gates warpgroup 1 skips a block's Gram when the chain did not
+            // use the last one, and the block then runs the clipped sweeps until no step size
+            // moves, which needs no bound.
             auto gram_ready = [&]() -> bool {
                 if (tid == 0) s_gram_used = 1;
                 if (gram_rows_ready) return true;
-                if (VEC || s_gon[q] != 0) {
+                if (VEC || !HAS_R || s_gon[q] != 0) {
                     const uint32_t par = VEC ? ph : static_cast<uint32_t>(s_gpar[q]);
                     const bool okr = tc::mbar_wait(bars + B_MRDY + 8 * q, par, kMaxPolls);
                     if (wg_count(1, okr && !*static_cast<volatile int*>(&s_abort)) != 128) return false;
@@ -633,11 +636,11 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                         abort_now = true;
                         break;
                     }
+                    const int K = have_rows ? sweeps_for_nu() : -1;
+                    const int nsw = K >= 0 ? min(K + 1, J - p) : J - p;
                     float* red = F + F_DF;  // [4][64] per-warp partial sums (F_DF, F_BPV: free here)
                     const int lane = tid & 31;
                     wg_sync(1);
-                    const int K = have_rows ? sweeps_for_nu() : -1;
-                    const int nsw = K >= 0 ? min(K + 1, J - p) : J - p;
                     if (tid < J) F[F_G + tid] = 0.f;  // tokens before p then leave d unchanged
                     wg_sync(1);
                     for (int it = 0; it < nsw; ++it) {
@@ -868,8 +871,8 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     }
                     if (nfree == KD) {
                         // from the estimate above (within nu |g|; the rho ratios are <= 1)
-                        wg_sync(1);
                         const int K = sweeps_for_nu();
+                        wg_sync(1);
                         for (int it = 0; K < 0 ? it < J : it < K; ++it) {
                             const float* hc = F + F_H + hb * J;  // h of the previous sweep
                             bool changed = false;
