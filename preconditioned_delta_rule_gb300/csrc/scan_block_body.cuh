@@ -591,17 +591,14 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
             auto rvec = [&](int j) -> float {
                 return j < min(J, T - blk * J) ? reinterpret_cast<const float*>(sm + rv_off(blk % 3))[j * KD + i] : 1.f;
             };
-            // The all-free Gram row jr of this block (lanes 0-15 of each chain warp: an M = 64
-            // product puts row 16 w + l in lane l of quadrant w, the lanes of this warp), read from
-            // tensor memory, scaled back by 1 / sig^2 (exact: powers of two) and masked to l < jr;
-            // and the coupling bound nu = max_j |gamma_j b_j| sum_l M_jl (infinite when it is not
-            // finite or a retention gate exceeds 1) for the sweep count.  With one gate per
-            // coordinate warpgroup 1 forms nu (no Gram).
-            // false: a wait gave up.  Otherwise have_rows says whether the Gram rows (in shared
-            // memory slot q) and the bound nu are there (warpgroup 1 writes both before the row
-            // barrier): with per-head gates warpgroup 1 skips a block's Gram when the chain did not
-            // use the last one, and the block then runs the clipped sweeps until no step size
-            // moves, which needs no bound.
+            // Waits for the all-free Gram rows of this block (copied by warpgroup 1 to shared
+            // memory slot q) and the coupling bound nu = max_j |gamma_j b_j| sum_l M_jl (infinite
+            // when it is not finite or a retention gate exceeds 1) for the sweep count; with one
+            // gate per coordinate there is no Gram and warpgroup 1 forms nu from the s rows.
+            // false: a wait gave up.  Otherwise have_rows says whether rows and bound are there:
+            // with per-head gates warpgroup 1 skips a block's Gram when the chain did not use the
+            // last one, and the block then runs the clipped sweeps until no step size moves, which
+            // needs no bound.
             auto gram_ready = [&]() -> bool {
                 if (tid == 0) s_gram_used = 1;
                 if (gram_rows_ready) return true;
