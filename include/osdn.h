@@ -83,8 +83,10 @@ typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1, OSDN_F16 = 2 } osdn_dtype;
  *   r        fp32 APF retention; NULL means r = 1 (Eq. (4)).  r_per_key = 0: [B,T,H], one
  *            r_{t,h} broadcast over K (Eq. (7)); r_per_key = 1: [B,T,H,K], the vector retention
  *            diag(r_t) of Appendix A.5 (Prop. A.3), one gate per key coordinate.  Other values of
- *            r_per_key return OSDN_ERR_ARG.  The blocked scan covers one gate per head; vector
- *            retention runs the token-by-token kernel.
+ *            r_per_key return OSDN_ERR_ARG.  With 16-bit keys and K = 128 both layouts run the
+ *            blocked scan (vector gates: every 64-token block by Jacobi sweeps on the clipped
+ *            recurrence, the gates staged with the keys); fp32 keys or K = 64 take the
+ *            token-by-token kernel.
  *   d0       [B,H,K] fp32 initial preconditioner; NULL means d = 1.  Used as given (not clamped).
  *   k_tilde  [B,T,H,K] write keys k~_t = d_t . k_t, dtype kt_dtype (written)
  *   d_out    [B,H,K] fp32 final d_{T} (written; may alias d0)

@@ -178,6 +178,12 @@ __device__ __forceinline__ void pair_advance(float& hi, float& lo, float inc, fl
     hi = h2;
     lo = l2;
 }
+// min(max(a b + c, 0), 1) in one instruction (fma.rn.sat: NaN gives 0).
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+    float r;
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 __device__ __forceinline__ void pair_clip(float& hi, float& lo, float dmin, float dmax) {
     if (hi < dmin || (hi == dmin && lo < 0.f)) { hi = dmin; lo = 0.f; }
     if (hi > dmax || (hi == dmax && lo > 0.f)) { hi = dmax; lo = 0.f; }
@@ -640,9 +646,16 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     wg_sync(1);
                     if (tid < J) F[F_G + tid] = 0.f;  // tokens before p then leave d unchanged
                     wg_sync(1);
+                    // With a finite box the trajectory runs in y = (d - d_min) / (d_max - d_min):
+                    // y' = sat(r y + c), c = (g s + (r - 1) d_min) / (d_max - d_min) formed off the
+                    // chain, one saturating fma per token on it instead of an fma, a max and a min.
+                    // (Not with one gate per head, whose blocks seldom come here: its registers are
+                    // the scarcest.)
+                    const bool unit_box = !HAS_R && dmax > dmin && dmax - dmin < INFINITY;
+                    const float bw = dmax - dmin, ibw = 1.f / bw;
                     for (int it = 0; it < nsw; ++it) {
                         float v[J];
-                        float x = d_hi;
+                        float x = d_hi, y = (d_hi - dmin) * ibw;
 #pragma unroll
                         for (int j4 = 0; j4 < J; j4 += 4) {
                             const float4 g4 = *reinterpret_cast<const float4*>(F + F_G + j4);
@@ -659,9 +672,14 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                             for (int e = 0; e < 4; ++e) {
                                 const int j = j4 + e;
                                 const float sj = s_at(j, i);
-                                v[j] = x * sj;
                                 const float rj = VEC ? rvec(j) : (j >= p ? r4[e] : 1.f);
-                                x = fminf(fmaxf(fmaf(rj, x, gg[e] * sj), dmin), dmax);
+                                if (unit_box) {
+                                    v[j] = fmaf(bw, y, dmin) * sj;
+                                    y = fma_sat(rj, y, fmaf(gg[e], sj, (rj - 1.f) * dmin) * ibw);
+                                } else {
+                                    v[j] = x * sj;
+                                    x = fminf(fmaxf(fmaf(rj, x, gg[e] * sj), dmin), dmax);
+                                }
                             }
                         }
                         // sum over the warp: lane l keeps the sums for tokens 2 l and 2 l + 1
@@ -685,7 +703,7 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                     if (tid >= p && tid < J) gout[tid] = F[F_G + tid];
                     // the block end with the final g's, carried as a (hi, lo) pair: hi takes one
                     // product and one sum per token, their rounding errors go to lo (off hi's
-                    // dependency chain), the clip acts on hi + lo, and the pair is renormalised once
+                    // dependency chain), the clip acts on the pair, and the pair is renormalised once
                     // (lo gathers at most ~64 ulps of d over the block).  Tokens before p leave it as
                     // it is (gate 1, step 0).
                     {
@@ -698,9 +716,11 @@ __device__ __forceinline__ void scan_block_body(const OsdnScanArgs& a, float* ws
                             const float p1 = r * hi, ep = fmaf(r, hi, -p1), q1 = g * sj;
                             float s1, e1;
                             two_sum(p1, q1, s1, e1);
+                            // the clip decides on s1 + r lo (this step's rounding terms ep + e1, under
+                            // an ulp, left out), so that lo's TwoSum stays off hi's chain
+                            const float v = fmaf(r, lo, s1);
                             lo = fmaf(r, lo, ep + e1);
                             hi = s1;
-                            const float v = hi + lo;
                             if (v < dmin) { hi = dmin; lo = 0.f; }
                             if (v > dmax) { hi = dmax; lo = 0.f; }
                         }

@@ -174,3 +174,19 @@ def test_decode_vector_retention(dtype, K, V):
         assert_maxabs(o, o_ref, tol, what=f"o step {t}")
     assert_maxabs(Sd, S_ref, tol, what="S")
     assert_rel(dd, d_ref, 1e-5, what="d")
+
+
+def test_scan_vector_retention_fp16_keys_not_beta_aware():
+    """fp16 keys on the blocked scan's vector-gate mode, with the step not fed by beta."""
+    w = W.WORKLOADS["layer_1p3b_apf"]
+    B, H, T = 2, 3, 448
+    inp = W.make_prefill(w, B=B, H=H, T=T, seed=47)
+    k16 = inp["k"].to(torch.float16)
+    r = vector_gates((B, T, H, 128), 11, mean=4.0)
+    box = dict(d_min=0.1, d_max=4.0)
+    kt, d = osdn_precond_scan(k16.cuda(), inp["beta"].cuda(), r.cuda(), None, kt_dtype=torch.float32,
+                              eta=0.3, eps=w.eps, beta_aware=False, **box)
+    torch.cuda.synchronize()
+    kt_ref, d_ref = oracle.precond_scan(k16, inp["beta"], r, None, eta=0.3, eps=w.eps, beta_aware=False, **box)
+    assert_rel(kt, kt_ref, 1e-5, what="k_tilde")
+    assert_rel(d, d_ref, 1e-5, what="d")
